@@ -1,0 +1,329 @@
+"""Oracle for MagicPIG's LSH-sampled decode attention. TEST INFRASTRUCTURE ONLY.
+
+Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference leg may import,
+call or execute this module; the product package never does, and it shares no code, table or
+helper with the CUDA path. Inputs reach it only from the seeded generators in ``workloads``.
+
+What it is: a plain, slow CPU restatement in float64 (numpy) of one decode step of the method,
+taken step by step in the order of Algorithm 1 ("MagicPIG: LSH Sampling for Efficient LLM
+Generation", method details, "algorithm execution") and of the five-line estimator sketch
+("MagicPIG: don't pick the tallest", section 5, "A hash that knows its odds"):
+
+  1. centre the keys:            kbar_i = k_i - mu, mu the mean key        (data preprocessing)
+  2. SimHash-encode the keys:     bit_{i,j} = [w_j . kbar_i > 0]           (LSH basics; hash choice)
+     and the query (not centred): qbit_j = [w_j . q > 0]
+     L tables of K bits: code_t = sum_b bit_{t*K+b} << b
+  3. collision count:             cnt_i = #{t : code_t(k_i) = code_t(q)}
+  4. sample set:                  S = {i not in T : cnt_i >= 2}            (hash choice; sketch)
+  5. p_i = 1 - arccos(cos(q, kbar_i))/pi,
+     u_i = 1 - (1-p_i^K)^L - L p_i^K (1-p_i^K)^(L-1)                       (u_i formula)
+  6. o = softmax([s_S - log u_S, s_T]) . [V_S, V_T],  s = q.k/sqrt(d)     (Algorithm 1, last step)
+
+Readings of points the pages leave open (each is also listed in the design notes):
+  * p uses the centred key (the sketch's ``cos(q, K_S - mu)``); Algorithm 1 prints the uncentred
+    ||K_S||, but SimHash's 1 - theta/pi holds for the vectors actually hashed, which are centred.
+  * scores use the raw keys for both S and T; the softmax is shift-invariant, so centred scores
+    give the same output (section 5: every score shifts by the same amount).
+  * the query is not centred.
+  * bit = 1 iff the projection is strictly positive.
+  * bit b of table t is hyperplane column t*K + b, least significant bit first.
+  * a zero-length q or kbar has cosine 0, so p = 1/2 (the sketch's note on zero-length vectors).
+  * log u is evaluated stably in the log domain (the sketch's note on stable probability
+    arithmetic): directly when L p^K >= 1/2, else as the binomial tail series from its j = 2 term.
+    If p = 0 (such a key cannot collide in exact arithmetic) log u is clamped to log(DBL_MIN).
+  * if S and T are both empty the output is the zero vector.
+  * GQA: each query head hashes and samples on its own against its KV head's codes.
+
+Parity status (what pins each function; the tests under tests/ hold the pins):
+  simhash_projections / sign_bits / table_codes / encode_*  brute force by definition, collision
+      probability 1 - theta/pi by Monte-Carlo, scale and negation invariants
+  collision_counts / sampled_set                            brute force by definition
+  log_inclusion_probability                                 exact rational binomial tail,
+      Monte-Carlo frequency of >= 2 collisions, closed-form special values
+  snis_attention / decode_head                              K = 0 reduces to full softmax
+      attention; u = 1/2 equals a duplicated key; L = 1 gives exact attention over T;
+      Horvitz-Thompson unbiasedness of the importance weights over hyperplane seeds
+  full_attention                                            textbook special cases (uniform
+      scores give the mean value; one dominant score gives its value)
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+NEAR_TIE_REL = 1e-5           # sign flips are tolerated only where |w.x| < 1e-5 |w| |x|
+LOG_DBL_MIN = math.log(np.finfo(np.float64).tiny)
+
+__all__ = [
+    "NEAR_TIE_REL", "LOG_DBL_MIN", "key_centre", "simhash_projections", "sign_bits", "table_codes",
+    "near_tie_mask", "encode_keys", "encode_query", "collision_counts", "exact_set_mask",
+    "sampled_set", "collision_probability", "log_inclusion_probability",
+    "inclusion_probability", "snis_attention", "full_attention", "decode_head", "decode",
+    "replay_bits", "as64",
+]
+
+
+def as64(x) -> np.ndarray:
+    """Any array-like (numpy, or a CPU torch tensor of any float dtype) as float64 numpy."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------------------------
+# Step 1: centring ("LSH Sampling..." method details, data preprocessing and centering;
+#         "don't pick the tallest" section 5)
+# ----------------------------------------------------------------------------------------------
+def key_centre(keys) -> np.ndarray:
+    """mu = (1/n) sum_i k_i over all n cached keys of one head, in float64. keys: [n, d]."""
+    k = as64(keys)
+    return k.sum(axis=0) / k.shape[0]
+
+
+# ----------------------------------------------------------------------------------------------
+# Step 2: SimHash encoding ("LSH Sampling..." background, LSH basics: Sign(w^T x); method details,
+#         hash-function choice: K x L random vectors, the sign of each projection, K bits per table)
+# ----------------------------------------------------------------------------------------------
+def simhash_projections(x, W) -> np.ndarray:
+    """P = x W: projection of each row of x [m, d] on each hyperplane column of W [d, C]."""
+    return as64(x) @ as64(W)
+
+
+def sign_bits(P) -> np.ndarray:
+    """bit = 1 iff the projection is strictly positive."""
+    return np.asarray(P) > 0.0
+
+
+def table_codes(bits, K: int, L: int) -> np.ndarray:
+    """code_t = sum_b bit[t*K + b] << b for t = 0..L-1. bits: [m, K*L] -> codes [m, L] int64."""
+    bits = np.asarray(bits, dtype=np.int64)
+    if K == 0:
+        return np.zeros((bits.shape[0], L), dtype=np.int64)   # empty codes: all equal
+    bits = bits.reshape(-1, L, K)
+    return (bits << np.arange(K, dtype=np.int64)[None, None, :]).sum(axis=2)
+
+
+def near_tie_mask(P, x, W) -> np.ndarray:
+    """|P_ij| < 1e-5 |w_j| |x_i|: where a sign may legitimately differ from another evaluation."""
+    wn = np.linalg.norm(as64(W), axis=0)
+    xn = np.linalg.norm(as64(x), axis=1)
+    return np.abs(P) < NEAR_TIE_REL * xn[:, None] * wn[None, :]
+
+
+def encode_keys(keys, centre, W, K: int, L: int, chunk: int = 8192):
+    """Centre, project, sign, pack. keys [n, d], centre [d] -> (codes [n, L], bits, near-ties)."""
+    k = as64(keys)
+    mu = as64(centre)
+    n = k.shape[0]
+    C = K * L
+    bits = np.zeros((n, C), dtype=bool)
+    near = np.zeros((n, C), dtype=bool)
+    for s in range(0, n, chunk):
+        kbar = k[s:s + chunk] - mu[None, :]
+        P = simhash_projections(kbar, W)
+        bits[s:s + chunk] = sign_bits(P)
+        near[s:s + chunk] = near_tie_mask(P, kbar, W)
+    return table_codes(bits, K, L), bits, near
+
+
+def encode_query(q, W, K: int, L: int):
+    """The query is hashed as is (not centred). q [m, d] -> (codes [m, L], bits, near-ties)."""
+    qq = np.atleast_2d(as64(q))
+    P = simhash_projections(qq, W)
+    bits = sign_bits(P)
+    return table_codes(bits, K, L), bits, near_tie_mask(P, qq, W)
+
+
+# ----------------------------------------------------------------------------------------------
+# Steps 3-4: collisions and the sample set ("LSH Sampling..." hash-function choice: a key is
+#            sampled only if it shares the query's hash value in at least two tables;
+#            "don't pick the tallest" section 5: S excludes the exact sink and recent tokens)
+# ----------------------------------------------------------------------------------------------
+def collision_counts(key_codes, q_code) -> np.ndarray:
+    """cnt_i = number of tables t with code_t(k_i) == code_t(q). key_codes [n, L], q_code [L]."""
+    return (np.asarray(key_codes) == np.asarray(q_code)[None, :]).sum(axis=1)
+
+
+def exact_set_mask(n: int, n_sink: int, n_local: int) -> np.ndarray:
+    """T = the first n_sink tokens and the last n_local tokens (attended exactly, u = 1)."""
+    T = np.zeros(n, dtype=bool)
+    T[:min(n_sink, n)] = True
+    if n_local > 0:
+        T[max(0, n - n_local):] = True
+    return T
+
+
+def sampled_set(cnt, T_mask) -> np.ndarray:
+    """S = {i not in T : cnt_i >= 2}, ascending."""
+    return np.nonzero((np.asarray(cnt) >= 2) & ~np.asarray(T_mask))[0]
+
+
+# ----------------------------------------------------------------------------------------------
+# Step 5: collision probability and inclusion probability ("LSH Sampling..." background: p = 1 -
+#         theta/pi; hash-function choice: u = 1 - (1-p^K)^L - L p^K (1-p^K)^(L-1);
+#         "don't pick the tallest" section 5: u subtracts the chances of zero and of exactly one
+#         colliding table from 1)
+# ----------------------------------------------------------------------------------------------
+def collision_probability(q, kbar) -> np.ndarray:
+    """p_i = 1 - arccos(cos(q, kbar_i))/pi; cosine 0 when either vector has zero length."""
+    qv = as64(q)
+    kb = np.atleast_2d(as64(kbar))
+    qn = np.linalg.norm(qv)
+    kn = np.linalg.norm(kb, axis=1)
+    dots = kb @ qv
+    cos = np.zeros_like(dots)
+    ok = (kn > 0) & (qn > 0)
+    cos[ok] = dots[ok] / (qn * kn[ok])
+    cos = np.clip(cos, -1.0, 1.0)
+    return 1.0 - np.arccos(cos) / math.pi
+
+
+def _log_u_scalar(p: float, K: int, L: int) -> float:
+    if L < 2:
+        return -math.inf                      # at most one table can collide: u = 0
+    if K == 0:
+        x, logx = 1.0, 0.0                    # p^0 = 1: every key collides in every table
+    else:
+        if p <= 0.0:
+            return LOG_DBL_MIN                # cannot collide in exact arithmetic; clamped
+        logx = K * math.log(p)
+        x = math.exp(logx)
+    lam = L * x
+    if lam >= 0.5:
+        # direct: u = 1 - (1-x)^L - L x (1-x)^(L-1)
+        if x >= 1.0:
+            return 0.0                        # (1-x) = 0 and L >= 2: u = 1
+        l1m = math.log1p(-x)
+        u = 1.0 - math.exp(L * l1m) - L * x * math.exp((L - 1) * l1m)
+        return math.log(u)
+    # series: u = sum_{j>=2} C(L,j) x^j (1-x)^(L-j) = t_2 (1 + sum_{j>=3} t_j / t_2)
+    l1m = math.log1p(-x)
+    log_t2 = math.log(L * (L - 1) / 2.0) + 2.0 * logx + (L - 2) * l1m
+    ratio = x / (1.0 - x)
+    total, term = 1.0, 1.0
+    for j in range(2, L):
+        term *= (L - j) / (j + 1.0) * ratio   # t_{j+1} / t_2
+        total += term
+        if term < 1e-17 * total:
+            break
+    return log_t2 + math.log(total)
+
+
+def log_inclusion_probability(p, K: int, L: int) -> np.ndarray:
+    """log u(p) for an array of p (see _log_u_scalar for the two evaluation branches)."""
+    pa = np.atleast_1d(np.asarray(p, dtype=np.float64))
+    return np.array([_log_u_scalar(float(v), K, L) for v in pa], dtype=np.float64)
+
+
+def inclusion_probability(p, K: int, L: int) -> np.ndarray:
+    return np.exp(log_inclusion_probability(p, K, L))
+
+
+# ----------------------------------------------------------------------------------------------
+# Step 6: the self-normalised importance-sampling estimate over S, joined with exact attention
+#         over T ("LSH Sampling..." method details: estimator approximation; Algorithm 1, last
+#         step; "don't pick the tallest" section 5 sketch, with the exact scores s_exact)
+# ----------------------------------------------------------------------------------------------
+def snis_attention(q, K_S, V_S, logu_S, K_T, V_T, scale: float) -> np.ndarray:
+    """softmax([s_S - log u_S, s_T]) . [V_S, V_T] with s = scale * q.k; zeros if S, T empty."""
+    qv = as64(q)
+    d = qv.shape[0]
+    KS = as64(K_S).reshape(-1, d)
+    KT = as64(K_T).reshape(-1, d)
+    logits = np.concatenate([(KS @ qv) * scale - as64(logu_S).reshape(-1), (KT @ qv) * scale])
+    if logits.size == 0:
+        return np.zeros(d)
+    w = np.exp(logits - logits.max())
+    w /= w.sum()
+    return w @ np.concatenate([as64(V_S).reshape(-1, d), as64(V_T).reshape(-1, d)])
+
+
+def full_attention(q, keys, values, scale: float) -> np.ndarray:
+    """o = softmax(scale q K^T) V, the textbook decode attention ("LSH Sampling..." background)."""
+    s = (as64(keys) @ as64(q)) * scale
+    w = np.exp(s - s.max())
+    return (w / w.sum()) @ as64(values)
+
+
+# ----------------------------------------------------------------------------------------------
+# One query head, and a whole batch
+# ----------------------------------------------------------------------------------------------
+def decode_head(q, keys, values, centre, key_codes, q_code, K: int, L: int, n_sink: int,
+                n_local: int, scale: float | None = None, centred_scores: bool = False) -> dict:
+    """Steps 3-6 for one query head against its KV head's codes."""
+    qv = as64(q)
+    k = as64(keys)
+    v = as64(values)
+    mu = as64(centre)
+    n, d = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    cnt = collision_counts(key_codes, q_code)
+    T = exact_set_mask(n, n_sink, n_local)
+    S = sampled_set(cnt, T)
+    kbar_S = k[S] - mu[None, :]
+    p = collision_probability(qv, kbar_S)
+    logu = log_inclusion_probability(p, K, L) if S.size else np.zeros(0)
+    Tidx = np.nonzero(T)[0]
+    if centred_scores:
+        o = snis_attention(qv, kbar_S, v[S], logu, k[Tidx] - mu[None, :], v[Tidx], scale)
+    else:
+        o = snis_attention(qv, k[S], v[S], logu, k[Tidx], v[Tidx], scale)
+    return {"o": o, "cnt": cnt, "S": S, "p": p, "logu": logu}
+
+
+def replay_bits(oracle_bits, near, other_bits, what: str = "bits"):
+    """Take another evaluation's bits where they differ from the oracle's inside the near-tie band.
+
+    Returns (bits, number of flips taken). A difference outside the band raises AssertionError.
+    """
+    ob = np.asarray(oracle_bits, dtype=bool)
+    gb = np.asarray(other_bits, dtype=bool)
+    diff = ob != gb
+    bad = diff & ~np.asarray(near, dtype=bool)
+    if bad.any():
+        idx = np.argwhere(bad)[:8].tolist()
+        raise AssertionError(f"{what}: {int(bad.sum())} sign mismatches outside the near-tie band"
+                             f" (first {idx})")
+    out = ob.copy()
+    out[diff] = gb[diff]
+    return out, int(diff.sum())
+
+
+def decode(q, keys, values, centre, W, K: int, L: int, n_sink: int, n_local: int,
+           scale: float | None = None, key_bits_override=None, q_bits_override=None) -> dict:
+    """The whole step for a batch. q [B, Hq, d]; keys, values [B, Hkv, n, d]; centre [B, Hkv, d].
+
+    key_bits_override[b][g] / q_bits_override[b][h], when given, replace the oracle's own sign
+    bits (used after replay_bits has checked that they differ only at near-ties).
+    Returns o [B, Hq, d], per-head counts, sets, and the key/query bits used.
+    """
+    qa, ka, va, ca = as64(q), as64(keys), as64(values), as64(centre)
+    B, Hq, d = qa.shape
+    Hkv, n = ka.shape[1], ka.shape[2]
+    G = Hq // Hkv
+    o = np.zeros((B, Hq, d))
+    cnt = np.zeros((B, Hq, n), dtype=np.int64)
+    sets: list[list[np.ndarray]] = [[None] * Hq for _ in range(B)]
+    kbits_all: list[list[np.ndarray]] = [[None] * Hkv for _ in range(B)]
+    qbits_all = np.zeros((B, Hq, K * L), dtype=bool)
+    for b in range(B):
+        for g in range(Hkv):
+            kcodes, kbits, _ = encode_keys(ka[b, g], ca[b, g], W, K, L)
+            if key_bits_override is not None:
+                kbits = np.asarray(key_bits_override[b][g], dtype=bool)
+                kcodes = table_codes(kbits, K, L)
+            kbits_all[b][g] = kbits
+            for h in range(g * G, (g + 1) * G):
+                qcodes, qbits, _ = encode_query(qa[b, h], W, K, L)
+                if q_bits_override is not None:
+                    qbits = np.asarray(q_bits_override[b][h], dtype=bool).reshape(1, -1)
+                    qcodes = table_codes(qbits, K, L)
+                qbits_all[b, h] = qbits[0]
+                r = decode_head(qa[b, h], ka[b, g], va[b, g], ca[b, g], kcodes, qcodes[0], K, L,
+                                n_sink, n_local, scale)
+                o[b, h] = r["o"]
+                cnt[b, h] = r["cnt"]
+                sets[b][h] = r["S"]
+    return {"o": o, "cnt": cnt, "S": sets, "key_bits": kbits_all, "q_bits": qbits_all}

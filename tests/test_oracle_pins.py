@@ -1,0 +1,395 @@
+"""Pins of the fp64 oracle against what the MagicPIG pages and the mathematics fix.
+
+None of these retypes an oracle formula and compares it with itself. Each check comes from
+somewhere else: Monte-Carlo over fresh hyperplanes, exact rational arithmetic, brute-force loops
+on tiny inputs, textbook attention special cases, invariances, and the pages' own numbers.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _pair_at_angle(theta, d=3):
+    x = np.zeros(d)
+    y = np.zeros(d)
+    x[0] = 1.0
+    y[0], y[1] = math.cos(theta), math.sin(theta)
+    return x, y
+
+
+def _brute_attention(q, keys, values, scale):
+    """Softmax attention written as scalar loops (independent of numpy's vector forms)."""
+    s = [scale * sum(qe * ke for qe, ke in zip(q, k)) for k in keys]
+    m = max(s)
+    w = [math.exp(si - m) for si in s]
+    z = sum(w)
+    d = len(values[0])
+    return np.array([sum(w[i] * values[i][e] for i in range(len(keys))) / z for e in range(d)])
+
+
+# ------------------------------------------------------------------------------------------------
+# SimHash: one hyperplane separates two vectors with probability theta/pi
+# ("LSH Sampling..." background, LSH basics; "don't pick the tallest" section 5)
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("deg", [10, 45, 90, 135, 170])
+def test_simhash_bit_agreement_is_one_minus_theta_over_pi(deg):
+    rng = np.random.default_rng(1000 + deg)
+    theta = math.radians(deg)
+    x, y = _pair_at_angle(theta, d=5)
+    N = 100_000
+    W = rng.standard_normal((5, N))
+    bx = O.sign_bits(O.simhash_projections(x[None], W))[0]
+    by = O.sign_bits(O.simhash_projections(y[None], W))[0]
+    freq = float(np.mean(bx == by))
+    p = 1 - theta / math.pi
+    sigma = math.sqrt(p * (1 - p) / N)
+    assert abs(freq - p) < 4.5 * sigma, (freq, p, sigma)
+
+
+# ------------------------------------------------------------------------------------------------
+# u(p): the chance that a key collides in at least 2 of L tables of K bits
+# ("LSH Sampling..." hash-function choice and the u_i formula; "don't pick the tallest" section 5)
+# ------------------------------------------------------------------------------------------------
+def _exact_tail(p: Fraction, K: int, L: int) -> Fraction:
+    x = p ** K
+    return sum(Fraction(math.comb(L, j)) * x ** j * (1 - x) ** (L - j) for j in range(2, L + 1))
+
+
+@pytest.mark.parametrize("K,L", [(2, 3), (3, 5), (8, 75), (9, 120), (10, 150), (11, 300)])
+@pytest.mark.parametrize("p", [Fraction(1, 8), Fraction(1, 4), Fraction(1, 2), Fraction(5, 8),
+                               Fraction(3, 4), Fraction(7, 8), Fraction(15, 16),
+                               Fraction(99, 100)])
+def test_log_u_matches_exact_rational_binomial_tail(K, L, p):
+    exact = _exact_tail(p, K, L)
+    assert exact > 0
+    got = float(O.log_inclusion_probability(float(p), K, L)[0])
+    want = math.log(exact.numerator) - math.log(exact.denominator)
+    assert abs(got - want) < 1e-11 * max(1.0, abs(want)), (got, want)
+
+
+def test_log_u_both_branches_near_the_switch():
+    # L p^K = 1/2 is where the evaluation switches branch; check either side against exact tails
+    K, L = 10, 150
+    p_switch = (0.5 / L) ** (1 / K)
+    for f in (0.97, 0.999, 1.0, 1.001, 1.03):
+        p = Fraction(p_switch * f).limit_denominator(10**9)
+        exact = _exact_tail(p, K, L)
+        got = float(O.log_inclusion_probability(float(p), K, L)[0])
+        want = math.log(exact.numerator) - math.log(exact.denominator)
+        assert abs(got - want) < 1e-11 * abs(want)
+
+
+def test_log_u_special_values():
+    assert O.log_inclusion_probability(1.0, 10, 150)[0] == 0.0          # u(1) = 1
+    assert O.log_inclusion_probability(0.7, 0, 150)[0] == 0.0           # K = 0: p^0 = 1, u = 1
+    assert O.log_inclusion_probability(0.0, 10, 150)[0] == O.LOG_DBL_MIN  # clamped u(0) = 0
+    for p in (0.0, 0.3, 1.0):
+        assert O.log_inclusion_probability(p, 10, 1)[0] == -math.inf    # L = 1: never 2 hits
+    ps = np.linspace(0.01, 1.0, 400)
+    lu = O.log_inclusion_probability(ps, 10, 150)
+    assert np.all(np.diff(lu) >= 0)                                   # monotone in p,
+    assert np.all(np.diff(lu)[lu[1:] < -1e-9] > 0)                    # strictly below u = 1
+
+
+@pytest.mark.parametrize("K,L,target_u,trials", [(2, 3, 0.5, 6000), (3, 5, 0.35, 6000),
+                                                 (8, 75, 0.5, 3000), (10, 150, 0.3, 2000),
+                                                 (10, 150, 0.7, 2000)])
+def test_u_matches_monte_carlo_collision_frequency(K, L, target_u, trials):
+    # pick the angle whose u is target_u, then count >= 2 collisions over fresh hyperplanes
+    lo, hi = 0.0, 1.0
+    for _ in range(60):
+        mid = (lo + hi) / 2
+        if O.inclusion_probability(mid, K, L)[0] < target_u:
+            lo = mid
+        else:
+            hi = mid
+    p = (lo + hi) / 2
+    theta = (1 - p) * math.pi
+    q, k = _pair_at_angle(theta, d=3)
+    rng = np.random.default_rng(7 * K + L)
+    W = rng.standard_normal((3, trials * K * L))
+    kc = O.encode_keys(k[None], np.zeros(3), W, K, trials * L)[0].reshape(trials, L)
+    qc = O.encode_query(q, W, K, trials * L)[0].reshape(trials, L)
+    hits = np.array([O.collision_counts(kc[t][None], qc[t])[0] >= 2 for t in range(trials)])
+    freq = float(hits.mean())
+    u = float(O.inclusion_probability(p, K, L)[0])
+    sigma = math.sqrt(u * (1 - u) / trials)
+    assert abs(freq - u) < 4.5 * sigma, (freq, u, sigma)
+
+
+# ------------------------------------------------------------------------------------------------
+# Codes, counts and the sample set, by brute force on tiny inputs
+# ------------------------------------------------------------------------------------------------
+def _brute_codes(keys, centre, W, K, L):
+    n, d = len(keys), len(centre)
+    out = []
+    for i in range(n):
+        row = []
+        for t in range(L):
+            code = 0
+            for b in range(K):
+                col = t * K + b
+                proj = sum(W[e][col] * (keys[i][e] - centre[e]) for e in range(d))
+                if proj > 0:
+                    code += 2 ** b
+            row.append(code)
+        out.append(row)
+    return out
+
+
+def test_codes_counts_and_set_by_brute_force():
+    rng = np.random.default_rng(3)
+    d, n, K, L = 3, 9, 2, 3
+    keys = rng.standard_normal((n, d)) + np.array([2.0, -1.0, 0.5])
+    W = rng.standard_normal((d, K * L))
+    centre = keys.mean(axis=0)
+    q = rng.standard_normal(d)
+    codes, _, _ = O.encode_keys(keys, centre, W, K, L)
+    assert codes.tolist() == _brute_codes(keys.tolist(), centre.tolist(), W.tolist(), K, L)
+    qcode = O.encode_query(q, W, K, L)[0][0]
+    want_q = _brute_codes([q.tolist()], [0.0] * d, W.tolist(), K, L)[0]
+    assert qcode.tolist() == want_q
+    cnt = O.collision_counts(codes, qcode)
+    brute_cnt = [sum(1 for t in range(L) if codes[i][t] == want_q[t]) for i in range(n)]
+    assert cnt.tolist() == brute_cnt
+    T = O.exact_set_mask(n, 1, 2)
+    assert T.tolist() == [True] + [False] * (n - 3) + [True, True]
+    S = O.sampled_set(cnt, T)
+    assert S.tolist() == [i for i in range(n) if brute_cnt[i] >= 2 and not T[i]]
+
+
+def test_key_along_query_collides_in_every_table():
+    rng = np.random.default_rng(4)
+    d, K, L = 16, 10, 150
+    W = rng.standard_normal((d, K * L))
+    q = rng.standard_normal(d)
+    mu = rng.standard_normal(d) * 3
+    keys = np.stack([mu + s * q for s in (0.01, 1.0, 250.0)])
+    codes, _, _ = O.encode_keys(keys, mu, W, K, L)
+    qcode = O.encode_query(q, W, K, L)[0][0]
+    assert O.collision_counts(codes, qcode).tolist() == [L, L, L]
+
+
+def test_negated_centred_key_flips_every_bit():
+    rng = np.random.default_rng(5)
+    d, K, L = 32, 8, 75
+    W = rng.standard_normal((d, K * L))
+    mu = rng.standard_normal(d)
+    k = rng.standard_normal((20, d)) + mu
+    _, bits, _ = O.encode_keys(k, mu, W, K, L)
+    _, bits_neg, _ = O.encode_keys(2 * mu - k, mu, W, K, L)
+    assert np.array_equal(bits, ~bits_neg)
+
+
+def test_zero_length_vectors():
+    rng = np.random.default_rng(6)
+    d, K, L = 8, 4, 6
+    W = rng.standard_normal((d, K * L))
+    _, qbits, _ = O.encode_query(np.zeros(d), W, K, L)
+    assert not qbits.any()                               # strict > 0
+    p = O.collision_probability(np.zeros(d), rng.standard_normal((3, d)))
+    assert np.all(p == 0.5)
+    p = O.collision_probability(rng.standard_normal(d), np.zeros((2, d)))
+    assert np.all(p == 0.5)
+
+
+# ------------------------------------------------------------------------------------------------
+# The estimator
+# ------------------------------------------------------------------------------------------------
+def test_full_attention_textbook_cases():
+    rng = np.random.default_rng(8)
+    keys = np.zeros((5, 4))
+    vals = rng.standard_normal((5, 3))
+    q = rng.standard_normal(4)
+    assert np.allclose(O.full_attention(q, keys, vals, 1.0), vals.mean(axis=0), atol=1e-15)
+    keys2 = rng.standard_normal((5, 4)) * 0.01
+    keys2[2] = q * 1000
+    assert np.allclose(O.full_attention(q, keys2, vals, 1.0), vals[2], atol=1e-12)
+    keys3 = rng.standard_normal((7, 4))
+    vals3 = rng.standard_normal((7, 4))
+    assert np.allclose(O.full_attention(q, keys3, vals3, 0.5),
+                       _brute_attention(q.tolist(), keys3.tolist(), vals3.tolist(), 0.5),
+                       atol=1e-13)
+
+
+def test_K0_reduces_to_full_softmax_attention():
+    # K = 0: empty codes always agree, every key collides in all L >= 2 tables, u = 1
+    rng = np.random.default_rng(9)
+    d, n = 16, 50
+    keys = rng.standard_normal((n, d)) + 1.5
+    vals = rng.standard_normal((n, d))
+    q = rng.standard_normal(d)
+    W = np.zeros((d, 0))
+    mu = O.key_centre(keys)
+    kc, _, _ = O.encode_keys(keys, mu, W, 0, 4)
+    qc = O.encode_query(q, W, 0, 4)[0][0]
+    r = O.decode_head(q, keys, vals, mu, kc, qc, 0, 4, n_sink=2, n_local=5)
+    assert r["S"].tolist() == list(range(2, n - 5))
+    assert np.all(r["logu"] == 0.0)
+    want = _brute_attention(q.tolist(), keys.tolist(), vals.tolist(), 1 / math.sqrt(d))
+    assert np.allclose(r["o"], want, rtol=0, atol=1e-13)
+
+
+def test_half_inclusion_probability_equals_a_duplicated_key():
+    # weight exp(s - log u) with u = 1/2 counts the key twice: same as attention over a multiset
+    rng = np.random.default_rng(10)
+    d = 8
+    KS = rng.standard_normal((3, d))
+    VS = rng.standard_normal((3, d))
+    KT = rng.standard_normal((2, d))
+    VT = rng.standard_normal((2, d))
+    q = rng.standard_normal(d)
+    got = O.snis_attention(q, KS, VS, np.array([math.log(0.5), 0.0, math.log(0.25)]), KT, VT,
+                           0.7)
+    mk = [KS[0], KS[0], KS[1], KS[2], KS[2], KS[2], KS[2], KT[0], KT[1]]
+    mv = [VS[0], VS[0], VS[1], VS[2], VS[2], VS[2], VS[2], VT[0], VT[1]]
+    want = _brute_attention(q.tolist(), [k.tolist() for k in mk], [v.tolist() for v in mv], 0.7)
+    assert np.allclose(got, want, atol=1e-13)
+
+
+def test_single_table_leaves_only_the_exact_set():
+    # L = 1: no key can collide in two tables, S is empty, o = exact attention over T
+    rng = np.random.default_rng(11)
+    d, n = 16, 40
+    keys = rng.standard_normal((n, d))
+    vals = rng.standard_normal((n, d))
+    q = rng.standard_normal(d)
+    W = rng.standard_normal((d, 3))
+    mu = O.key_centre(keys)
+    kc, _, _ = O.encode_keys(keys, mu, W, 3, 1)
+    qc = O.encode_query(q, W, 3, 1)[0][0]
+    r = O.decode_head(q, keys, vals, mu, kc, qc, 3, 1, n_sink=3, n_local=4)
+    assert r["S"].size == 0
+    T = list(range(3)) + list(range(n - 4, n))
+    want = _brute_attention(q.tolist(), keys[T].tolist(), vals[T].tolist(), 1 / math.sqrt(d))
+    assert np.allclose(r["o"], want, atol=1e-13)
+
+
+def test_empty_sample_and_exact_sets_give_zero():
+    d = 4
+    o = O.snis_attention(np.ones(d), np.zeros((0, d)), np.zeros((0, d)), np.zeros(0),
+                         np.zeros((0, d)), np.zeros((0, d)), 1.0)
+    assert np.array_equal(o, np.zeros(d))
+
+
+def test_centring_leaves_the_output_unchanged():
+    # every score shifts by q.mu, which the softmax ignores ("don't pick the tallest" section 5)
+    rng = np.random.default_rng(12)
+    d, n, K, L = 32, 300, 4, 12
+    mu = rng.standard_normal(d) * 4
+    keys = rng.standard_normal((n, d)) + mu
+    vals = rng.standard_normal((n, d))
+    q = -mu / np.linalg.norm(mu) + 0.3 * rng.standard_normal(d)
+    W = rng.standard_normal((d, K * L))
+    c = O.key_centre(keys)
+    kc, _, _ = O.encode_keys(keys, c, W, K, L)
+    qc = O.encode_query(q, W, K, L)[0][0]
+    a = O.decode_head(q, keys, vals, c, kc, qc, K, L, 2, 8)
+    b = O.decode_head(q, keys, vals, c, kc, qc, K, L, 2, 8, centred_scores=True)
+    assert a["S"].size > 10
+    assert np.allclose(a["o"], b["o"], rtol=0, atol=1e-12)
+
+
+def test_importance_weights_are_unbiased_over_hyperplane_draws():
+    # Horvitz-Thompson: E[sum_{i in S} f_i / u_i] = sum_i f_i exactly when u_i = P[i in S].
+    # This fails for a wrong u, a wrong sign of log u, or a wrong ">= 2 tables" rule.
+    rng = np.random.default_rng(13)
+    d, n, K, L, M = 6, 40, 2, 6, 20000
+    keys = rng.standard_normal((n, d))
+    vals = rng.standard_normal((n, d))
+    q = rng.standard_normal(d)
+    mu = O.key_centre(keys)
+    scale = 1 / math.sqrt(d)
+    s = keys @ q * scale
+    logu = O.log_inclusion_probability(O.collision_probability(q, keys - mu), K, L)
+    W = rng.standard_normal((d, M * K * L))
+    kc = O.encode_keys(keys, mu, W, K, M * L)[0].reshape(n, M, L)
+    qc = O.encode_query(q, W, K, M * L)[0][0].reshape(M, L)
+    T = O.exact_set_mask(n, 0, 0)
+    num = np.zeros((M, d))
+    den = np.zeros(M)
+    for m in range(M):
+        S = O.sampled_set(O.collision_counts(kc[:, m, :], qc[m]), T)
+        wS = np.exp(s[S] - logu[S])
+        num[m] = wS @ vals[S]
+        den[m] = wS.sum()
+    want_num = np.exp(s) @ vals
+    want_den = np.exp(s).sum()
+    se_den = den.std(ddof=1) / math.sqrt(M)
+    assert abs(den.mean() - want_den) < 4.5 * se_den, (den.mean(), want_den, se_den)
+    se_num = num.std(axis=0, ddof=1) / math.sqrt(M)
+    assert np.all(np.abs(num.mean(axis=0) - want_num) < 4.5 * se_num + 1e-12)
+
+
+def test_expected_sample_size_is_the_sum_of_inclusion_probabilities():
+    rng = np.random.default_rng(14)
+    d, n, K, L, M = 128, 1024, 8, 75, 60
+    mu = rng.standard_normal(d)
+    mu *= 8 / np.linalg.norm(mu)
+    keys = rng.standard_normal((n, d)) + mu
+    q = -4 * mu / 8 + 0.5 * rng.standard_normal(d)
+    c = O.key_centre(keys)
+    T = O.exact_set_mask(n, 4, 64)
+    u = O.inclusion_probability(O.collision_probability(q, keys - c), K, L)
+    want = u[~T].sum()
+    sizes = []
+    for m in range(M):
+        W = rng.standard_normal((d, K * L))
+        kc, _, _ = O.encode_keys(keys, c, W, K, L)
+        qc = O.encode_query(q, W, K, L)[0][0]
+        sizes.append(O.sampled_set(O.collision_counts(kc, qc), T).size)
+    sizes = np.array(sizes, dtype=float)
+    se = sizes.std(ddof=1) / math.sqrt(M)
+    assert abs(sizes.mean() - want) < 4.5 * se + 0.5, (sizes.mean(), want, se)
+
+
+def test_without_centring_almost_no_key_is_sampled():
+    # "don't pick the tallest" section 5 / "LSH Sampling..." ablation: raw keys sit in one cone
+    # away from the query, so they rarely share its buckets; centring brings them back
+    import torch
+    from workloads import WORKLOADS, make_hyperplanes, make_layer
+    wl = WORKLOADS["tiny_f32_n4096"]
+    x = make_layer(wl, 0)
+    W = make_hyperplanes(wl)
+    keys = x["keys"][0, 0]
+    q = x["q"][0, 0]
+    T = O.exact_set_mask(wl.n, wl.n_sink, wl.n_local)
+    qc = O.encode_query(q, W, wl.K, wl.L)[0][0]
+    frac = {}
+    for name, c in (("centred", O.key_centre(keys)), ("raw", np.zeros(wl.d))):
+        kc, _, _ = O.encode_keys(keys, c, W, wl.K, wl.L)
+        frac[name] = O.sampled_set(O.collision_counts(kc, qc), T).size / (~T).sum()
+    assert frac["raw"] < 0.005 and frac["centred"] > 0.01, frac
+    assert frac["raw"] < 0.25 * frac["centred"], frac
+    del torch
+
+
+# ------------------------------------------------------------------------------------------------
+# The pages' own arithmetic, re-derived from the workload shapes
+# ------------------------------------------------------------------------------------------------
+def test_page_arithmetic_matches_the_96k_workload():
+    from workloads import WORKLOADS
+    g = json.load(open(os.path.join(HERE, "golden", "page_arithmetic.json")))
+    wl = WORKLOADS["llama8b_n96k_32layers"]
+    per_token = wl.layers * wl.Hkv * wl.d * 2 * 2
+    assert per_token == g["kv_bytes_per_token"]["value"]
+    assert per_token * wl.n == g["kv_bytes_96k_context"]["value"]
+    assert 4 * wl.L == g["table_entry_bytes_per_key"]["value"]
+    tables = 4 * wl.L * wl.n * wl.layers * wl.Hkv
+    assert abs(tables / 2**30 - g["table_bytes_96k_gib"]["value"]) < 0.05
+    entries = wl.L * wl.n // 2**wl.K
+    assert entries == g["entries_scanned_per_query"]["value"]
+    assert 4 * entries == g["index_bytes_scanned_per_query"]["value"]
+    key_bytes = wl.n * wl.d * 2
+    assert key_bytes == g["key_bytes_one_head_one_layer"]["value"]
+    assert abs(100 * 4 * entries / key_bytes - g["scan_fraction_percent"]["value"]) < 0.005
+    projector = wl.d * wl.C * 2                    # bf16 projector
+    assert abs(projector / 1000 - g["projector_kb"]["value"]) < 0.05 * g["projector_kb"]["value"]
