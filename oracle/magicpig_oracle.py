@@ -33,6 +33,8 @@ Readings of points the pages leave open (each is also listed in the design notes
     If p = 0 (such a key cannot collide in exact arithmetic) log u is clamped to log(DBL_MIN).
   * if S and T are both empty the output is the zero vector.
   * GQA: each query head hashes and samples on its own against its KV head's codes.
+  * near ties: another evaluation may disagree on a sign bit only where
+    |w_j.(k_i - mu)| < 1e-5 |w_j| |k_i| (raw key norm) or |w_j.q| < 1e-5 |w_j| |q|.
 
 Parity status (what pins each function; the tests under tests/ hold the pins):
   simhash_projections / sign_bits / table_codes / encode_*  brute force by definition, collision
@@ -105,7 +107,11 @@ def table_codes(bits, K: int, L: int) -> np.ndarray:
 
 
 def near_tie_mask(P, x, W) -> np.ndarray:
-    """|P_ij| < 1e-5 |w_j| |x_i|: where a sign may legitimately differ from another evaluation."""
+    """|P_ij| < 1e-5 |w_j| |x_i|: where a sign may legitimately differ from another evaluation.
+
+    x is the vector as it was given (the raw key or the query), not the centred key: an
+    evaluation that projects the raw key and subtracts w_j.mu makes rounding errors that scale
+    with |w_j| |k_i|, and a key lying exactly on the centre still gets a non-empty band."""
     wn = np.linalg.norm(as64(W), axis=0)
     xn = np.linalg.norm(as64(x), axis=1)
     return np.abs(P) < NEAR_TIE_REL * xn[:, None] * wn[None, :]
@@ -123,7 +129,7 @@ def encode_keys(keys, centre, W, K: int, L: int, chunk: int = 8192):
         kbar = k[s:s + chunk] - mu[None, :]
         P = simhash_projections(kbar, W)
         bits[s:s + chunk] = sign_bits(P)
-        near[s:s + chunk] = near_tie_mask(P, kbar, W)
+        near[s:s + chunk] = near_tie_mask(P, k[s:s + chunk], W)
     return table_codes(bits, K, L), bits, near
 
 
