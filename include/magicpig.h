@@ -1,0 +1,191 @@
+/*
+ * magicpig.h -- C ABI of libmagicpig, LSH-sampled decode attention on one GB300 (sm_103a).
+ *
+ * The method is MagicPIG's ("MagicPIG: LSH Sampling for Efficient LLM Generation", method
+ * details; "MagicPIG: don't pick the tallest", section 5): keys are centred and SimHash-encoded
+ * into L tables of K bits; a decode query keeps the keys whose code equals its own in at least
+ * two tables, weights each kept key by its closed-form inclusion probability u, and merges that
+ * self-normalised importance-sampled attention with exact attention over the sink and local
+ * tokens. Everything stays in device memory; every step runs in this library's CUDA kernels.
+ *
+ * Conventions for every entry point below:
+ *   - Pointers to tensors are DEVICE pointers owned by the caller. Nothing here allocates device
+ *     memory; scratch comes from a caller-provided workspace whose size a *_workspace_bytes
+ *     function returns. Workspace pointers must be 256-byte aligned.
+ *   - Tensors are contiguous, row-major:
+ *       keys, values  [B][Hkv][n][d]       (MP_BF16 or MP_F32)
+ *       q             [B][Hq][d]           (MP_BF16 or MP_F32)
+ *       out           [B][Hq][d]           float32
+ *       centre        [B][Hkv][d]          float32  (mu, the mean key of each head)
+ *       W             [d][K*L]             (MP_BF16 or MP_F32); column j = t*K + b is bit b
+ *                                          (least significant first) of table t. One W serves
+ *                                          every head and layer.
+ *   - GQA: query head h reads KV head h / (Hq / Hkv); Hq must be a multiple of Hkv.
+ *   - d must be 128. 0 <= K <= 32 and 1 <= L; K == 0 is the degenerate case where every key
+ *     collides in every table (u = 1 when L >= 2).
+ *   - Packed codes ("codes") are bit-sliced in blocks of 1024 keys: for head (b, g) and block
+ *     blk = i / 1024, plane j (= t*K + b) is a row of 32 uint32 words, and bit (i % 32) of word
+ *     (i % 1024) / 32 holds the sign bit of key i for hyperplane j. Layout:
+ *       codes[((b*Hkv + g)*nblk + blk)*(K*L) + j][w],   nblk = ceil(n / 1024).
+ *     Bits of padding positions (i >= n in the last block) are unspecified.
+ *   - Calls are asynchronous on `stream`: argument checks run on the host and return an error
+ *     before anything is launched; device-side problems (a bounded wait that gave up) set a
+ *     device status word that mp_device_status() reads.
+ *   - No global mutable state besides that status word; calls on different streams may run
+ *     concurrently if their buffers do not overlap.
+ */
+#ifndef MAGICPIG_H
+#define MAGICPIG_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MP_API __attribute__((visibility("default")))
+#else
+#define MP_API
+#endif
+
+#define MP_ABI_VERSION 1
+#define MP_KEYS_PER_BLOCK 1024
+
+typedef enum {
+    MP_OK = 0,
+    MP_ERR_INVALID_ARG = 1,   /* bad shape, null pointer, misalignment, inconsistent sizes */
+    MP_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement (e.g. d != 128) */
+    MP_ERR_CUDA = 3,          /* a CUDA runtime call failed; cudaGetLastError() has the cause */
+    MP_ERR_TIMEOUT = 4,       /* a device-side bounded wait gave up (see mp_device_status) */
+    MP_ERR_WORKSPACE = 5      /* the workspace passed is smaller than *_workspace_bytes */
+} mp_status;
+
+typedef enum { MP_F32 = 0, MP_BF16 = 1 } mp_dtype;
+
+/* Decode parameters. K, L: LSH bits per table and tables ("LSH Sampling...", method details,
+ * hash-function choice). n_sink, n_local: the exact set T = {0..n_sink-1} u {n-n_local..n-1},
+ * attended with u = 1 and never sampled (Algorithm 1's static cache; "don't pick the tallest",
+ * section 5). scale: score scale, 0 means 1/sqrt(d). flags: must be 0. */
+typedef struct {
+    int K;
+    int L;
+    int n_sink;
+    int n_local;
+    float scale;
+    unsigned flags;
+} mp_params;
+
+/* Human-readable name of a status code (static storage). */
+MP_API const char* mp_status_string(mp_status s);
+
+/* MP_ABI_VERSION of the loaded library. */
+MP_API int mp_abi_version(void);
+
+/* Bytes of packed codes for B*Hkv heads of n keys: B*Hkv*ceil(n/1024)*K*L*128. */
+MP_API size_t mp_codes_bytes(int B, int Hkv, int n, int K, int L);
+
+/* Workspace bytes mp_key_mean needs (fixed-order partial sums). */
+MP_API size_t mp_key_mean_workspace_bytes(int B, int Hkv, int n, int d);
+
+/* Centre of the cached keys: centre[b][g][:] = (1/n) sum_i keys[b][g][i][:], float32
+ * accumulation in a fixed order (run-to-run identical).
+ * ("LSH Sampling...", method details, data preprocessing and centering: keys are centred before
+ * the tables are built; "don't pick the tallest", section 5.)
+ * Errors: MP_ERR_INVALID_ARG for n < 1, null pointers; MP_ERR_WORKSPACE if ws_bytes is short. */
+MP_API mp_status mp_key_mean(const void* keys, mp_dtype key_dtype, int B, int Hkv, int n, int d,
+                             float* centre, void* workspace, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/* Build the hash tables of one layer: centre each key, project it on the K*L hyperplanes of W,
+ * keep the sign (bit = 1 iff w_j.(k_i - mu) > 0), pack into the bit-sliced codes above.
+ * ("LSH Sampling...", background, LSH basics: Sign(w^T x); method details, hash-function choice
+ * and system co-design item 2: the random projection runs on the GPU.)
+ * bf16 keys with a bf16 W run on the tcgen05 tensor cores (exact products, fp32 accumulation);
+ * other dtype pairs use an fp32 CUDA-core kernel.
+ * codes: mp_codes_bytes(B, Hkv, n, K, L) bytes, 16-byte aligned; may be NULL when K == 0.
+ * Errors: MP_ERR_INVALID_ARG (shapes, null, misalignment), MP_ERR_UNSUPPORTED (d != 128). */
+MP_API mp_status mp_build_tables(const void* keys, mp_dtype key_dtype, const float* centre,
+                                 const void* W, mp_dtype w_dtype, int B, int Hkv, int n, int d,
+                                 int K, int L, uint32_t* codes, cudaStream_t stream);
+
+/* Workspace bytes mp_decode_attention (and its two halves below) need for these shapes;
+ * 0 if the shapes or parameters are invalid. */
+MP_API size_t mp_decode_workspace_bytes(int B, int Hq, int Hkv, int n, int d,
+                                        const mp_params* prm);
+
+/* One decode step of LSH-sampled attention for B*Hq query rows (Algorithm 1 of "LSH
+ * Sampling...", method details, algorithm execution):
+ *   q_code = Encode(q, W)                              (q is not centred)
+ *   cnt_i  = #{t : code_t(k_i) == code_t(q)}           from the packed codes
+ *   S      = {i not in T : cnt_i >= 2}
+ *   p_i    = 1 - arccos(q.(k_i - mu) / (|q| |k_i - mu|)) / pi
+ *   u_i    = 1 - (1 - p_i^K)^L - L p_i^K (1 - p_i^K)^(L-1)      (evaluated stably in log space)
+ *   out    = softmax([s_S - log u_S, s_T]) . [V_S, V_T],   s = scale * q.k_i  (raw keys)
+ * The softmax over S and T is computed in pieces of 1024 keys and merged by log-sum-exp (the
+ * "recursive attention" merge of the system co-design section). If S and T are both empty the
+ * output row is zero. Zero-length q or k - mu gives cosine 0 (p = 1/2).
+ * Errors: MP_ERR_INVALID_ARG (shapes, null, Hq % Hkv, n_sink/n_local < 0, flags != 0),
+ *         MP_ERR_UNSUPPORTED (d != 128, Hq/Hkv not in {1, 2, 4, 8}, or K*L*(Hq/Hkv) so
+ *         large that a CTA's query masks no longer fit in shared memory),
+ *         MP_ERR_WORKSPACE (ws_bytes < mp_decode_workspace_bytes). */
+MP_API mp_status mp_decode_attention(const void* q, mp_dtype q_dtype, const uint32_t* codes,
+                                     const float* centre, const void* W, mp_dtype w_dtype,
+                                     const void* keys, const void* values, mp_dtype kv_dtype,
+                                     int B, int Hq, int Hkv, int n, int d, const mp_params* prm,
+                                     float* out, void* workspace, size_t ws_bytes,
+                                     cudaStream_t stream);
+
+/* The two halves of mp_decode_attention, for callers that schedule or time them apart. Both
+ * take the same workspace; mp_sampled_attention reads what mp_encode_query wrote there for the
+ * same q, centre and shapes, so the two must run in that order on the same stream.
+ *
+ * mp_encode_query: q_code = Encode(q, W), plus |q| and q.mu (Algorithm 1's first step).
+ * mp_sampled_attention: collision counts, S, gather of K_S and V_S, importance weights, and the
+ * merged softmax with the exact set T (Algorithm 1's remaining steps).
+ * Errors as mp_decode_attention. */
+MP_API mp_status mp_encode_query(const void* q, mp_dtype q_dtype, const float* centre,
+                                 const void* W, mp_dtype w_dtype, int B, int Hq, int Hkv, int n,
+                                 int d, const mp_params* prm, void* workspace, size_t ws_bytes,
+                                 cudaStream_t stream);
+MP_API mp_status mp_sampled_attention(const void* q, mp_dtype q_dtype, const uint32_t* codes,
+                                      const float* centre, const void* keys, const void* values,
+                                      mp_dtype kv_dtype, int B, int Hq, int Hkv, int n, int d,
+                                      const mp_params* prm, float* out, void* workspace,
+                                      size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes mp_debug_select needs. */
+MP_API size_t mp_debug_workspace_bytes(int B, int Hq, int Hkv, int n, int d,
+                                       const mp_params* prm);
+
+/* mp_decode_attention plus what it decided, for checking against a reference:
+ *   q_bits    [B][Hq][ceil(K*L/32)] uint32: bit j%32 of word j/32 is the query's sign bit j
+ *   sel_idx   [B][Hq][n] int32: ascending indices of S (the sampled set, T excluded), the first
+ *             sel_count[b][h] entries are valid
+ *   sel_count [B][Hq] int32
+ *   cnt       [B][Hq][n] uint8 collision counts (saturating at 255), or NULL to skip
+ * The selection comes from the same kernel mp_decode_attention runs; cnt from a separate
+ * counting kernel. Errors as mp_decode_attention. */
+MP_API mp_status mp_debug_select(const void* q, mp_dtype q_dtype, const uint32_t* codes,
+                                 const float* centre, const void* W, mp_dtype w_dtype,
+                                 const void* keys, const void* values, mp_dtype kv_dtype, int B,
+                                 int Hq, int Hkv, int n, int d, const mp_params* prm, float* out,
+                                 uint32_t* q_bits, int32_t* sel_idx, int32_t* sel_count,
+                                 uint8_t* cnt, void* workspace, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+/* Unpack codes into one integer per (key, table): table_codes[b][g][i][t] = code_t(k_i) =
+ * sum_b bit_{i, t*K+b} << b. Requires K <= 32. */
+MP_API mp_status mp_codes_unpack(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
+                                 uint32_t* table_codes, cudaStream_t stream);
+
+/* Synchronise the current device, return its status word (MP_OK or MP_ERR_TIMEOUT) through
+ * *status and reset it to MP_OK. Returns MP_ERR_CUDA if the device cannot be reached. */
+MP_API mp_status mp_device_status(int* status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MAGICPIG_H */

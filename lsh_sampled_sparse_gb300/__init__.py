@@ -1,0 +1,27 @@
+"""LSH-sampled decode attention (MagicPIG) on one GB300: Python binding of libmagicpig.
+
+Every step of the path runs in the library's CUDA kernels; this module only checks tensor
+arguments, allocates outputs and workspaces with PyTorch, and calls the C ABI declared in
+include/magicpig.h. There is no CPU fallback: without the built library every call raises.
+"""
+from .binding import (  # noqa: F401
+    MP_BF16,
+    MP_F32,
+    MagicPIGError,
+    Params,
+    abi_version,
+    build_tables,
+    codes_bytes,
+    codes_unpack,
+    debug_select,
+    debug_workspace_bytes,
+    decode_attention,
+    decode_workspace_bytes,
+    device_status,
+    encode_query,
+    key_mean,
+    key_mean_workspace_bytes,
+    lib,
+    library_path,
+    sampled_attention,
+)

@@ -1,0 +1,278 @@
+"""ctypes binding of libmagicpig: argument checks and marshalling only.
+
+Names follow the C ABI in include/magicpig.h without the ``mp_`` prefix. Tensors are PyTorch CUDA
+tensors; outputs and workspaces are allocated here with PyTorch when the caller passes none.
+Packed codes and bit vectors are held in int32 tensors (the same bits as the ABI's uint32).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+MP_F32, MP_BF16 = 0, 1
+_c_int, _c_size, _vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+
+
+class MagicPIGError(RuntimeError):
+    """A libmagicpig call returned a status other than MP_OK, or the library is missing."""
+
+
+class Params(ctypes.Structure):
+    """mp_params: K bits per table, L tables, exact sink/local sizes, score scale (0: 1/sqrt(d))."""
+
+    _fields_ = [("K", ctypes.c_int), ("L", ctypes.c_int), ("n_sink", ctypes.c_int),
+                ("n_local", ctypes.c_int), ("scale", ctypes.c_float), ("flags", ctypes.c_uint)]
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmagicpig.so")
+
+
+def _declare(L):
+    P = ctypes.POINTER(Params)
+    sig = {
+        "mp_status_string": (ctypes.c_char_p, [_c_int]),
+        "mp_abi_version": (_c_int, []),
+        "mp_codes_bytes": (_c_size, [_c_int] * 5),
+        "mp_key_mean_workspace_bytes": (_c_size, [_c_int] * 4),
+        "mp_key_mean": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_size,
+                                 _vp]),
+        "mp_build_tables": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 6 + [_vp, _vp]),
+        "mp_decode_workspace_bytes": (_c_size, [_c_int] * 5 + [P]),
+        "mp_debug_workspace_bytes": (_c_size, [_c_int] * 5 + [P]),
+        "mp_decode_attention": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int]
+                                + [_c_int] * 5 + [P, _vp, _vp, _c_size, _vp]),
+        "mp_encode_query": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 5
+                            + [P, _vp, _c_size, _vp]),
+        "mp_sampled_attention": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int]
+                                 + [_c_int] * 5 + [P, _vp, _vp, _c_size, _vp]),
+        "mp_debug_select": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int]
+                            + [_c_int] * 5 + [P, _vp, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
+        "mp_codes_unpack": (_c_int, [_vp] + [_c_int] * 5 + [_vp, _vp]),
+        "mp_device_status": (_c_int, [ctypes.POINTER(_c_int)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+
+
+def lib():
+    """The loaded libmagicpig (raises MagicPIGError if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise MagicPIGError(
+                f"{path} is missing; build it with `python -m lsh_sampled_sparse_gb300.build`."
+                " There is no CPU fallback.")
+        handle = ctypes.CDLL(path)
+        _declare(handle)
+        _LIB = handle
+    return _LIB
+
+
+def abi_version() -> int:
+    return int(lib().mp_abi_version())
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise MagicPIGError(f"{what} failed: {lib().mp_status_string(status).decode()}")
+
+
+def _ptr(t):
+    return None if t is None else _vp(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return _vp(stream.cuda_stream)
+
+
+def _dtype(t: torch.Tensor, name: str) -> int:
+    if t.dtype == torch.bfloat16:
+        return MP_BF16
+    if t.dtype == torch.float32:
+        return MP_F32
+    raise TypeError(f"{name}: dtype {t.dtype} is not float32 or bfloat16")
+
+
+def _cuda(t, name: str, ndim: int | None = None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    return t
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _workspace(ws, nbytes: int, device):
+    if ws is None:
+        return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    _cuda(ws, "workspace")
+    if _nbytes(ws) < nbytes:
+        raise ValueError(f"workspace has {_nbytes(ws)} bytes, needs {nbytes}")
+    return ws
+
+
+def codes_bytes(B: int, Hkv: int, n: int, K: int, L: int) -> int:
+    return int(lib().mp_codes_bytes(B, Hkv, n, K, L))
+
+
+def key_mean_workspace_bytes(B: int, Hkv: int, n: int, d: int) -> int:
+    return int(lib().mp_key_mean_workspace_bytes(B, Hkv, n, d))
+
+
+def decode_workspace_bytes(B, Hq, Hkv, n, d, K, L, n_sink, n_local, scale=0.0) -> int:
+    p = Params(K, L, n_sink, n_local, scale, 0)
+    return int(lib().mp_decode_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
+
+
+def debug_workspace_bytes(B, Hq, Hkv, n, d, K, L, n_sink, n_local, scale=0.0) -> int:
+    p = Params(K, L, n_sink, n_local, scale, 0)
+    return int(lib().mp_debug_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
+
+
+def key_mean(keys, centre=None, workspace=None, stream=None):
+    """mu[b, g] = mean of keys[b, g, :, :] over the n cached keys (float32 [B, Hkv, d])."""
+    _cuda(keys, "keys", 4)
+    B, Hkv, n, d = keys.shape
+    if centre is None:
+        centre = torch.empty(B, Hkv, d, dtype=torch.float32, device=keys.device)
+    _cuda(centre, "centre", 3)
+    ws = _workspace(workspace, key_mean_workspace_bytes(B, Hkv, n, d), keys.device)
+    _check(lib().mp_key_mean(_ptr(keys), _dtype(keys, "keys"), B, Hkv, n, d, _ptr(centre),
+                             _ptr(ws), _nbytes(ws), _stream(stream)), "mp_key_mean")
+    return centre
+
+
+def build_tables(keys, centre, W, K: int, L: int, codes=None, stream=None):
+    """Packed bit-sliced SimHash codes of every key (int32 tensor of codes_bytes/4 words)."""
+    _cuda(keys, "keys", 4)
+    B, Hkv, n, d = keys.shape
+    nbytes = codes_bytes(B, Hkv, n, K, L)
+    if codes is None:
+        codes = torch.empty(max(nbytes // 4, 4), dtype=torch.int32, device=keys.device)
+    _cuda(codes, "codes")
+    if _nbytes(codes) < nbytes:
+        raise ValueError("codes buffer too small")
+    _cuda(centre, "centre", 3)
+    _cuda(W, "W", 2)
+    _check(lib().mp_build_tables(_ptr(keys), _dtype(keys, "keys"), _ptr(centre), _ptr(W),
+                                 _dtype(W, "W"), B, Hkv, n, d, K, L, _ptr(codes),
+                                 _stream(stream)), "mp_build_tables")
+    return codes
+
+
+def decode_attention(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int,
+                     n_local: int, scale: float = 0.0, out=None, workspace=None, stream=None):
+    """One LSH-sampled decode step; returns out [B, Hq, d] float32."""
+    _cuda(q, "q", 3)
+    _cuda(keys, "keys", 4)
+    _cuda(values, "values", 4)
+    _cuda(centre, "centre", 3)
+    B, Hq, d = q.shape
+    Hkv, n = keys.shape[1], keys.shape[2]
+    if values.shape != keys.shape or values.dtype != keys.dtype:
+        raise ValueError("values must match keys in shape and dtype")
+    if out is None:
+        out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
+    _cuda(out, "out", 3)
+    p = Params(K, L, n_sink, n_local, scale, 0)
+    need = int(lib().mp_decode_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
+    if need == 0:
+        raise MagicPIGError("mp_decode_workspace_bytes rejected the shapes/parameters")
+    ws = _workspace(workspace, need, q.device)
+    _check(lib().mp_decode_attention(
+        _ptr(q), _dtype(q, "q"), _ptr(codes), _ptr(centre), _ptr(W), _dtype(W, "W"), _ptr(keys),
+        _ptr(values), _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out),
+        _ptr(ws), _nbytes(ws), _stream(stream)), "mp_decode_attention")
+    return out
+
+
+def encode_query(q, centre, W, keys_shape, K: int, L: int, n_sink: int, n_local: int,
+                 workspace, scale: float = 0.0, stream=None):
+    """First half of decode_attention: query codes and norms into `workspace`."""
+    _cuda(q, "q", 3)
+    _cuda(centre, "centre", 3)
+    _cuda(workspace, "workspace")
+    B, Hq, d = q.shape
+    Hkv, n = keys_shape[1], keys_shape[2]
+    p = Params(K, L, n_sink, n_local, scale, 0)
+    _check(lib().mp_encode_query(_ptr(q), _dtype(q, "q"), _ptr(centre), _ptr(W), _dtype(W, "W"),
+                                 B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(workspace),
+                                 _nbytes(workspace), _stream(stream)), "mp_encode_query")
+
+
+def sampled_attention(q, codes, centre, keys, values, K: int, L: int, n_sink: int, n_local: int,
+                      out, workspace, scale: float = 0.0, stream=None):
+    """Second half of decode_attention (after encode_query filled `workspace`)."""
+    _cuda(q, "q", 3)
+    _cuda(keys, "keys", 4)
+    _cuda(values, "values", 4)
+    _cuda(out, "out", 3)
+    _cuda(workspace, "workspace")
+    B, Hq, d = q.shape
+    Hkv, n = keys.shape[1], keys.shape[2]
+    p = Params(K, L, n_sink, n_local, scale, 0)
+    _check(lib().mp_sampled_attention(
+        _ptr(q), _dtype(q, "q"), _ptr(codes), _ptr(centre), _ptr(keys), _ptr(values),
+        _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)), "mp_sampled_attention")
+    return out
+
+
+def debug_select(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int, n_local: int,
+                 scale: float = 0.0, counts: bool = True, stream=None) -> dict:
+    """Decode plus its decisions: out, q_bits, per-row ascending sample sets, collision counts."""
+    _cuda(q, "q", 3)
+    _cuda(keys, "keys", 4)
+    B, Hq, d = q.shape
+    Hkv, n = keys.shape[1], keys.shape[2]
+    dev = q.device
+    C = K * L
+    qwords = (C + 31) // 32
+    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+    q_bits = torch.zeros(B, Hq, max(qwords, 1), dtype=torch.int32, device=dev)
+    sel_idx = torch.full((B, Hq, n), -1, dtype=torch.int32, device=dev)
+    sel_count = torch.zeros(B, Hq, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(B, Hq, n, dtype=torch.uint8, device=dev) if counts else None
+    p = Params(K, L, n_sink, n_local, scale, 0)
+    need = int(lib().mp_debug_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
+    if need == 0:
+        raise MagicPIGError("mp_debug_workspace_bytes rejected the shapes/parameters")
+    ws = _workspace(None, need, dev)
+    _check(lib().mp_debug_select(
+        _ptr(q), _dtype(q, "q"), _ptr(codes), _ptr(centre), _ptr(W), _dtype(W, "W"), _ptr(keys),
+        _ptr(values), _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out),
+        _ptr(q_bits) if qwords else None, _ptr(sel_idx), _ptr(sel_count), _ptr(cnt), _ptr(ws),
+        _nbytes(ws), _stream(stream)), "mp_debug_select")
+    return {"out": out, "q_bits": q_bits[..., :qwords], "sel_idx": sel_idx,
+            "sel_count": sel_count, "cnt": cnt}
+
+
+def codes_unpack(codes, B: int, Hkv: int, n: int, K: int, L: int, stream=None):
+    """code_t(k_i) per key and table: int32 [B, Hkv, n, L]."""
+    out = torch.empty(B, Hkv, n, L, dtype=torch.int32, device=codes.device)
+    _check(lib().mp_codes_unpack(_ptr(codes), B, Hkv, n, K, L, _ptr(out), _stream(stream)),
+           "mp_codes_unpack")
+    return out
+
+
+def device_status() -> int:
+    """Synchronise the device; return and clear its status word (0 = MP_OK, 4 = timeout)."""
+    v = _c_int(0)
+    _check(lib().mp_device_status(ctypes.byref(v)), "mp_device_status")
+    return int(v.value)

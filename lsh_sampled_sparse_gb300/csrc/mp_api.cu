@@ -1,0 +1,336 @@
+// Host side of the C ABI declared in include/magicpig.h: argument checks (before any launch),
+// workspace layout, kernel selection, and the device status word.
+#include <math.h>
+
+#include <mutex>
+
+#include "mp_internal.cuh"
+
+namespace mp {
+
+// One status word per device; kernels with bounded waits raise MP_ERR_TIMEOUT here.
+__device__ int g_device_status;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+int* g_status_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+bool g_prepared[kMaxDevices] = {};
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// First use on a device: resolve the status word's address, read the SM count, load every
+// kernel and raise shared-memory limits, so that later calls (possibly inside a stream
+// capture) only launch.
+bool ensure_prepared() {
+    const int dev = current_device();
+    if (dev < 0) return false;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_prepared[dev]) return true;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return false;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    if (prepare_misc() != cudaSuccess || prepare_decode() != cudaSuccess) return false;
+    prepare_encode_tc();   // failure only disables the tensor-core encoder
+    cudaGetLastError();
+    g_status_ptr[dev] = static_cast<int*>(p);
+    g_sm_count[dev] = sms;
+    g_prepared[dev] = true;
+    return true;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool valid_dtype(mp_dtype t) { return t == MP_F32 || t == MP_BF16; }
+
+bool fill_shape(int B, int Hq, int Hkv, int n, int d, const mp_params* prm, DecodeShape* s) {
+    if (!prm) return false;
+    if (B < 1 || Hq < 1 || Hkv < 1 || n < 1 || d < 1) return false;
+    if (Hq % Hkv) return false;
+    if (prm->K < 0 || prm->K > 32 || prm->L < 1 || prm->n_sink < 0 || prm->n_local < 0 ||
+        prm->flags != 0u || !(prm->scale >= 0.0f))
+        return false;
+    if (static_cast<long long>(prm->K) * prm->L > (1 << 20)) return false;
+    s->B = B;
+    s->Hq = Hq;
+    s->Hkv = Hkv;
+    s->n = n;
+    s->d = d;
+    s->K = prm->K;
+    s->L = prm->L;
+    s->C = prm->K * prm->L;
+    s->qwords = (s->C + 31) / 32;
+    s->nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
+    s->n_sink = prm->n_sink;
+    s->n_local = prm->n_local;
+    s->scale = prm->scale > 0.0f ? prm->scale : 1.0f / sqrtf(static_cast<float>(d));
+    return true;
+}
+
+mp_status to_status(cudaError_t e) { return e == cudaSuccess ? MP_OK : MP_ERR_CUDA; }
+}  // namespace
+
+int* device_status_ptr() {
+    const int dev = current_device();
+    return dev < 0 ? nullptr : g_status_ptr[dev];
+}
+int device_sm_count() {
+    const int dev = current_device();
+    return dev < 0 || g_sm_count[dev] <= 0 ? 148 : g_sm_count[dev];
+}
+
+size_t decode_scratch_bytes(const DecodeShape& s, bool debug) {
+    const size_t rows = static_cast<size_t>(s.B) * s.Hq;
+    size_t b = 0;
+    b += align256(rows * s.qwords * 4);                  // qbits
+    b += align256(rows * 16);                            // qstat
+    b += align256(rows * s.nblk * 4) * 2;                // pm, pl
+    b += align256(rows * s.nblk * kD * 4);               // po
+    b += align256(static_cast<size_t>(s.B) * s.Hkv * 4); // counters
+    if (debug) b += align256(rows * s.nblk * 32 * 4);    // selmask
+    return b;
+}
+
+DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug) {
+    const size_t rows = static_cast<size_t>(s.B) * s.Hq;
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    DecodeScratch d;
+    d.qbits = reinterpret_cast<uint32_t*>(p);
+    p += align256(rows * s.qwords * 4);
+    d.qstat = reinterpret_cast<float4*>(p);
+    p += align256(rows * 16);
+    d.pm = reinterpret_cast<float*>(p);
+    p += align256(rows * s.nblk * 4);
+    d.pl = reinterpret_cast<float*>(p);
+    p += align256(rows * s.nblk * 4);
+    d.po = reinterpret_cast<float*>(p);
+    p += align256(rows * s.nblk * kD * 4);
+    d.counters = reinterpret_cast<unsigned*>(p);
+    p += align256(static_cast<size_t>(s.B) * s.Hkv * 4);
+    d.selmask = debug ? reinterpret_cast<uint32_t*>(p) : nullptr;
+    return d;
+}
+
+}  // namespace mp
+
+using namespace mp;
+
+static mp_status check_decode(const void* q, mp_dtype q_dtype, const uint32_t* codes,
+                              const float* centre, const void* W, mp_dtype w_dtype,
+                              const void* keys, const void* values, mp_dtype kv_dtype, int B,
+                              int Hq, int Hkv, int n, int d, const mp_params* prm, float* out,
+                              void* workspace, size_t ws_bytes, bool debug, DecodeShape* s) {
+    if (!fill_shape(B, Hq, Hkv, n, d, prm, s)) return MP_ERR_INVALID_ARG;
+    if (!valid_dtype(q_dtype) || !valid_dtype(w_dtype) || !valid_dtype(kv_dtype))
+        return MP_ERR_INVALID_ARG;
+    if (!q || !centre || !keys || !values || !out || !workspace) return MP_ERR_INVALID_ARG;
+    if (s->C > 0 && (!codes || !W)) return MP_ERR_INVALID_ARG;
+    if (!aligned(keys, 16) || !aligned(values, 16) || !aligned(out, 4) ||
+        !aligned(centre, 16) || !aligned(q, q_dtype == MP_BF16 ? 2 : 4) ||
+        !aligned(workspace, 256) || (codes && !aligned(codes, 16)))
+        return MP_ERR_INVALID_ARG;
+    if (d != kD) return MP_ERR_UNSUPPORTED;
+    if (!decode_supported(*s, kv_dtype == MP_BF16)) return MP_ERR_UNSUPPORTED;
+    if (ws_bytes < decode_scratch_bytes(*s, debug)) return MP_ERR_WORKSPACE;
+    return MP_OK;
+}
+
+extern "C" {
+
+const char* mp_status_string(mp_status s) {
+    switch (s) {
+        case MP_OK: return "MP_OK";
+        case MP_ERR_INVALID_ARG: return "MP_ERR_INVALID_ARG";
+        case MP_ERR_UNSUPPORTED: return "MP_ERR_UNSUPPORTED";
+        case MP_ERR_CUDA: return "MP_ERR_CUDA";
+        case MP_ERR_TIMEOUT: return "MP_ERR_TIMEOUT";
+        case MP_ERR_WORKSPACE: return "MP_ERR_WORKSPACE";
+        default: return "MP_UNKNOWN_STATUS";
+    }
+}
+
+int mp_abi_version(void) { return MP_ABI_VERSION; }
+
+size_t mp_codes_bytes(int B, int Hkv, int n, int K, int L) {
+    if (B < 1 || Hkv < 1 || n < 1 || K < 0 || L < 1) return 0;
+    const size_t nblk = (static_cast<size_t>(n) + kKeysPerBlock - 1) / kKeysPerBlock;
+    return static_cast<size_t>(B) * Hkv * nblk * static_cast<size_t>(K) * L * kWordsPerBlock * 4;
+}
+
+size_t mp_key_mean_workspace_bytes(int B, int Hkv, int n, int d) {
+    if (B < 1 || Hkv < 1 || n < 1 || d != kD) return 0;
+    return align256(static_cast<size_t>(B) * Hkv * key_mean_splits(n) * kD * 4);
+}
+
+mp_status mp_key_mean(const void* keys, mp_dtype key_dtype, int B, int Hkv, int n, int d,
+                      float* centre, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (!keys || !centre || !workspace || !valid_dtype(key_dtype)) return MP_ERR_INVALID_ARG;
+    if (B < 1 || Hkv < 1 || n < 1 || d < 1) return MP_ERR_INVALID_ARG;
+    if (d != kD) return MP_ERR_UNSUPPORTED;
+    if (!aligned(keys, 16) || !aligned(centre, 4) || !aligned(workspace, 256))
+        return MP_ERR_INVALID_ARG;
+    if (ws_bytes < mp_key_mean_workspace_bytes(B, Hkv, n, d)) return MP_ERR_WORKSPACE;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    return to_status(launch_key_mean(keys, key_dtype == MP_BF16, B * Hkv, n, centre,
+                                     static_cast<float*>(workspace), key_mean_splits(n), stream));
+}
+
+mp_status mp_build_tables(const void* keys, mp_dtype key_dtype, const float* centre,
+                          const void* W, mp_dtype w_dtype, int B, int Hkv, int n, int d, int K,
+                          int L, uint32_t* codes, cudaStream_t stream) {
+    if (B < 1 || Hkv < 1 || n < 1 || d < 1 || K < 0 || K > 32 || L < 1)
+        return MP_ERR_INVALID_ARG;
+    if (!valid_dtype(key_dtype) || !valid_dtype(w_dtype)) return MP_ERR_INVALID_ARG;
+    if (d != kD) return MP_ERR_UNSUPPORTED;
+    if (static_cast<long long>(K) * L > (1 << 20)) return MP_ERR_INVALID_ARG;
+    if (K == 0) return MP_OK;   // no hyperplanes: nothing to encode
+    if (!keys || !centre || !W || !codes) return MP_ERR_INVALID_ARG;
+    if (!aligned(keys, 16) || !aligned(codes, 16) || !aligned(centre, 4) ||
+        !aligned(W, w_dtype == MP_BF16 ? 2 : 4))
+        return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    if (key_dtype == MP_BF16 && w_dtype == MP_BF16) {
+        const cudaError_t e =
+            launch_encode_tc(keys, centre, W, B, Hkv, n, K, L, codes, device_status_ptr(), stream);
+        if (e != cudaErrorNotSupported) return to_status(e);
+        cudaGetLastError();
+    }
+    return to_status(launch_encode_simt(keys, key_dtype == MP_BF16, centre, W, w_dtype == MP_BF16,
+                                        B, Hkv, n, K, L, codes, stream));
+}
+
+size_t mp_decode_workspace_bytes(int B, int Hq, int Hkv, int n, int d, const mp_params* prm) {
+    DecodeShape s;
+    if (!fill_shape(B, Hq, Hkv, n, d, prm, &s)) return 0;
+    return decode_scratch_bytes(s, false);
+}
+
+size_t mp_debug_workspace_bytes(int B, int Hq, int Hkv, int n, int d, const mp_params* prm) {
+    DecodeShape s;
+    if (!fill_shape(B, Hq, Hkv, n, d, prm, &s)) return 0;
+    return decode_scratch_bytes(s, true);
+}
+
+mp_status mp_decode_attention(const void* q, mp_dtype q_dtype, const uint32_t* codes,
+                              const float* centre, const void* W, mp_dtype w_dtype,
+                              const void* keys, const void* values, mp_dtype kv_dtype, int B,
+                              int Hq, int Hkv, int n, int d, const mp_params* prm, float* out,
+                              void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    DecodeShape s;
+    const mp_status st = check_decode(q, q_dtype, codes, centre, W, w_dtype, keys, values,
+                                      kv_dtype, B, Hq, Hkv, n, d, prm, out, workspace, ws_bytes,
+                                      false, &s);
+    if (st != MP_OK) return st;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
+    cudaError_t e = launch_qencode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
+                                   stream);
+    if (e != cudaSuccess) return MP_ERR_CUDA;
+    return to_status(launch_collide(q, q_dtype == MP_BF16, codes, centre, keys, values,
+                                    kv_dtype == MP_BF16, s, out, ws, stream));
+}
+
+mp_status mp_encode_query(const void* q, mp_dtype q_dtype, const float* centre, const void* W,
+                          mp_dtype w_dtype, int B, int Hq, int Hkv, int n, int d,
+                          const mp_params* prm, void* workspace, size_t ws_bytes,
+                          cudaStream_t stream) {
+    DecodeShape s;
+    if (!fill_shape(B, Hq, Hkv, n, d, prm, &s)) return MP_ERR_INVALID_ARG;
+    if (!valid_dtype(q_dtype) || !valid_dtype(w_dtype)) return MP_ERR_INVALID_ARG;
+    if (!q || !centre || !workspace || (s.C > 0 && !W)) return MP_ERR_INVALID_ARG;
+    if (!aligned(q, q_dtype == MP_BF16 ? 2 : 4) || !aligned(centre, 16) ||
+        !aligned(workspace, 256))
+        return MP_ERR_INVALID_ARG;
+    if (d != kD) return MP_ERR_UNSUPPORTED;
+    if (ws_bytes < decode_scratch_bytes(s, false)) return MP_ERR_WORKSPACE;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
+    return to_status(launch_qencode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
+                                    stream));
+}
+
+mp_status mp_sampled_attention(const void* q, mp_dtype q_dtype, const uint32_t* codes,
+                               const float* centre, const void* keys, const void* values,
+                               mp_dtype kv_dtype, int B, int Hq, int Hkv, int n, int d,
+                               const mp_params* prm, float* out, void* workspace,
+                               size_t ws_bytes, cudaStream_t stream) {
+    DecodeShape s;
+    // W is only read by the query encoding; q stands in for it in the shared checks
+    const mp_status st = check_decode(q, q_dtype, codes, centre, q, MP_F32, keys, values,
+                                      kv_dtype, B, Hq, Hkv, n, d, prm, out, workspace, ws_bytes,
+                                      false, &s);
+    if (st != MP_OK) return st;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
+    return to_status(launch_collide(q, q_dtype == MP_BF16, codes, centre, keys, values,
+                                    kv_dtype == MP_BF16, s, out, ws, stream));
+}
+
+mp_status mp_debug_select(const void* q, mp_dtype q_dtype, const uint32_t* codes,
+                          const float* centre, const void* W, mp_dtype w_dtype, const void* keys,
+                          const void* values, mp_dtype kv_dtype, int B, int Hq, int Hkv, int n,
+                          int d, const mp_params* prm, float* out, uint32_t* q_bits,
+                          int32_t* sel_idx, int32_t* sel_count, uint8_t* cnt, void* workspace,
+                          size_t ws_bytes, cudaStream_t stream) {
+    DecodeShape s;
+    const mp_status st = check_decode(q, q_dtype, codes, centre, W, w_dtype, keys, values,
+                                      kv_dtype, B, Hq, Hkv, n, d, prm, out, workspace, ws_bytes,
+                                      true, &s);
+    if (st != MP_OK) return st;
+    if (!sel_idx || !sel_count || (s.qwords > 0 && !q_bits)) return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    DecodeScratch ws = carve_decode_scratch(workspace, s, true);
+    if (s.qwords > 0) ws.qbits = q_bits;
+    cudaError_t e = launch_qencode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
+                                   stream);
+    if (e != cudaSuccess) return MP_ERR_CUDA;
+    e = launch_collide(q, q_dtype == MP_BF16, codes, centre, keys, values, kv_dtype == MP_BF16, s,
+                       out, ws, stream);
+    if (e != cudaSuccess) return MP_ERR_CUDA;
+    e = launch_compact_selection(ws.selmask, s.B * s.Hq, s.n, s.nblk, sel_idx, sel_count, stream);
+    if (e != cudaSuccess) return MP_ERR_CUDA;
+    if (cnt) {
+        if (s.C == 0) {
+            // no hyperplanes: every table agrees for every key
+            const size_t total = static_cast<size_t>(s.B) * s.Hq * s.n;
+            e = cudaMemsetAsync(cnt, s.L > 255 ? 255 : s.L, total, stream);
+        } else {
+            e = launch_collision_counts(codes, ws.qbits, s, cnt, stream);
+        }
+        if (e != cudaSuccess) return MP_ERR_CUDA;
+    }
+    return MP_OK;
+}
+
+mp_status mp_codes_unpack(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
+                          uint32_t* table_codes, cudaStream_t stream) {
+    if (B < 1 || Hkv < 1 || n < 1 || K < 0 || K > 32 || L < 1 || !table_codes)
+        return MP_ERR_INVALID_ARG;
+    if (K > 0 && !codes) return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    if (K == 0)
+        return to_status(cudaMemsetAsync(table_codes, 0,
+                                         static_cast<size_t>(B) * Hkv * n * L * 4, stream));
+    return to_status(launch_codes_unpack(codes, B * Hkv, n, K, L, table_codes, stream));
+}
+
+mp_status mp_device_status(int* status) {
+    if (!status) return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MP_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return MP_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return MP_ERR_CUDA;
+    *status = v;
+    return MP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,452 @@
+// Key encoding on the tcgen05 tensor cores: codes = [W^T (k - mu) > 0], bit-sliced.
+//
+// The SimHash projection of every cached key on K*L hyperplanes ("MagicPIG: LSH Sampling for
+// Efficient LLM Generation", background, LSH basics: Sign(w^T x); method details, hash-function
+// choice; system co-design item 2: the random projection is a dense GEMM kept on the GPU) is
+// the one dense contraction of the path: [keys x 128] x [128 x K*L].
+//
+// With bf16 keys and a bf16 W every product is exact in fp32, so the MMA computes w_j . k_i
+// with fp32 accumulation; the centre enters as the per-(head, plane) constant c_j = w_j . mu
+// and the sign test is [w_j . k_i > c_j], i.e. [w_j . (k_i - mu) > 0].
+//
+// Structure (one CTA per SM, persistent over a contiguous range of 1024-key blocks, and one
+// 256-hyperplane chunk of W held in shared memory for the CTA's whole life):
+//   warp 0   TMA producer: 128-key x 128-dim bf16 tiles, 128-byte swizzle, 3-stage ring
+//   warp 1   TMEM allocator and single-thread MMA issuer: M=128, N<=256, K=16 x 8 per tile,
+//            double-buffered fp32 accumulators (2 x 256 TMEM columns)
+//   warps 2-9 epilogue: tcgen05.ld the accumulator, compare with c_j, warp ballot -> one
+//            32-key word per hyperplane, stage a block's words in shared memory, then write
+//            each plane row (128 bytes) of the block with coalesced stores.
+// Every mbarrier wait is bounded; on expiry the CTA records MP_ERR_TIMEOUT in the device status
+// word, stops issuing work, and still releases its TMEM before returning.
+#include <cuda.h>
+
+#include "mp_internal.cuh"
+
+namespace mp {
+namespace {
+
+constexpr int kTileM = 128;            // keys per MMA tile (TMEM lanes)
+constexpr int kChunkN = 256;           // hyperplanes per CTA (MMA N, TMEM columns per buffer)
+constexpr int kStages = 3;             // A-tile ring depth
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr uint32_t kStageBytes = kTileM * kD * 2;      // 32 KB: two 64-column swizzled halves
+constexpr uint32_t kHalfBytes = kTileM * 128;          // 16 KB: 128 rows x 128 bytes
+constexpr uint32_t kBBytes = kChunkN * kD * 2;         // 64 KB
+constexpr uint32_t kBHalfBytes = kChunkN * 128;        // 32 KB
+constexpr int kStgPitch = kWordsPerBlock * 8 + 1;      // 257: staging row pitch (words)
+
+constexpr uint32_t kOffA = 0;
+constexpr uint32_t kOffB = kOffA + kStages * kStageBytes;
+constexpr uint32_t kOffStg = kOffB + kBBytes;
+constexpr uint32_t kOffCvec = kOffStg + kWordsPerBlock * kStgPitch * 4;
+constexpr uint32_t kOffBars = kOffCvec + kChunkN * 4;
+constexpr uint32_t kOffMisc = kOffBars + 128;
+constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+static_assert(kStgPitch == 257, "staging pitch");
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s: far beyond any real wait
+
+struct EncodeArgs {
+    const float* centre;            // [BH][128]
+    const __nv_bfloat16* W;         // [128][C]
+    uint32_t* codes;
+    int* status;
+    int C, nchunk, nblk, n, units, parts;
+};
+
+// ---- PTX wrappers -----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait: false on timeout (status raised, abort flag set) or when another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicExch(status, (int)MP_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address >> 4
+    d |= static_cast<uint64_t>(1) << 16;                    // leading offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride offset: 8 rows x 128 B
+    d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+        "[%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void epi_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    encode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const EncodeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem + kOffA;
+    uint8_t* sB = smem + kOffB;
+    uint32_t* stg = reinterpret_cast<uint32_t*>(smem + kOffStg);
+    float* cvec = reinterpret_cast<float*>(smem + kOffCvec);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int chunk = blockIdx.x % a.nchunk;
+    const int part = blockIdx.x / a.nchunk;
+    const int j0 = chunk * kChunkN;
+    const int Nc = min(kChunkN, a.C - j0);          // real hyperplanes in this chunk
+    const int Nmma = (Nc + 15) & ~15;               // MMA N (multiple of 16)
+    const int u_begin = static_cast<int>((static_cast<long long>(a.units) * part) / a.parts);
+    const int u_end = static_cast<int>((static_cast<long long>(a.units) * (part + 1)) / a.parts);
+
+    const uint32_t bar_full = smem_u32(bars);            // [kStages]
+    const uint32_t bar_empty = bar_full + 8 * kStages;   // [kStages]
+    const uint32_t bar_tfull = bar_empty + 8 * kStages;  // [2]
+    const uint32_t bar_tempty = bar_tfull + 16;          // [2]
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar_tfull + 8 * s, 1);
+            mbar_init(bar_tempty + 8 * s, kEpiWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // W chunk -> shared memory as the B operand: row r = hyperplane j0 + r, K-major, swizzled.
+    for (int idx = tid; idx < kChunkN * kD; idx += kThreads) {
+        const int r = idx % kChunkN, e = idx / kChunkN;
+        __nv_bfloat16 w = __float2bfloat16(0.0f);
+        if (r < Nc) w = a.W[static_cast<size_t>(e) * a.C + j0 + r];
+        const uint32_t off = (e >> 6) * kBHalfBytes + r * 128 + ((((e & 63) >> 3) ^ (r & 7)) << 4) +
+                             ((e & 7) << 1);
+        *reinterpret_cast<__nv_bfloat16*>(sB + off) = w;
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(2 * kChunkN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int u = u_begin; u < u_end && ok; ++u) {
+                const int bg = u / a.nblk, blk = u % a.nblk;
+                const int rows = min(kKeysPerBlock, a.n - blk * kKeysPerBlock);
+                const int ntile = (rows + kTileM - 1) / kTileM;
+                for (int t = 0; t < ntile; ++t, ++it) {
+                    const int s = it % kStages;
+                    const uint32_t ph = (it / kStages) & 1;
+                    if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+                    const uint32_t dst = smem_u32(sA + s * kStageBytes);
+                    const int row0 = blk * kKeysPerBlock + t * kTileM;
+                    tma_load_3d(dst, &kmap, bar_full + 8 * s, 0, row0, bg);
+                    tma_load_3d(dst + kHalfBytes, &kmap, bar_full + 8 * s, 64, row0, bg);
+                }
+            }
+            if (!ok) {
+                // drain: let loads already issued land before the CTA can exit (bounded)
+                for (int k = 1; k <= kStages && it - k >= 0; ++k) {
+                    const int i2 = it - k;
+                    volatile int never = 0;
+                    mbar_wait(bar_full + 8 * (i2 % kStages), (i2 / kStages) & 1, &never, a.status);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = make_idesc(kTileM, Nmma);
+            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+            int it = 0;
+            bool ok = true;
+            for (int u = u_begin; u < u_end && ok; ++u) {
+                const int blk = u % a.nblk;
+                const int rows = min(kKeysPerBlock, a.n - blk * kKeysPerBlock);
+                const int ntile = (rows + kTileM - 1) / kTileM;
+                for (int t = 0; t < ntile; ++t, ++it) {
+                    const int s = it % kStages;
+                    const int ab = it & 1;
+                    if (!mbar_wait(bar_full + 8 * s, (it / kStages) & 1, abort_flag, a.status) ||
+                        !mbar_wait(bar_tempty + 8 * ab, ((it >> 1) & 1) ^ 1, abort_flag,
+                                   a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + ab * kChunkN;
+#pragma unroll
+                    for (int k = 0; k < kD / 16; ++k) {
+                        const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
+                        const uint32_t kboff = (k >> 2) * kBHalfBytes + (k & 3) * 32;
+                        tc_mma(d_tmem, sw128_desc(a_base + s * kStageBytes + koff),
+                               sw128_desc(b_base + kboff), idesc, k > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar_empty + 8 * s);
+                    tc_commit(bar_tfull + 8 * ab);
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue ----------------
+        const int ew = warp - 2;                 // 0..7
+        const int quad = warp & 3;               // TMEM lane quadrant this warp may read
+        const int half = ew >> 2;                // which 128 columns
+        const int et = tid - 64;                 // 0..255
+        bool aborted = false;
+        int it = 0;
+        int cur_bg = -1;
+        for (int u = u_begin; u < u_end; ++u) {
+            const int bg = u / a.nblk, blk = u % a.nblk;
+            const int rows = min(kKeysPerBlock, a.n - blk * kKeysPerBlock);
+            const int ntile = (rows + kTileM - 1) / kTileM;
+            if (bg != cur_bg) {
+                // c_j = w_j . mu for this head, from the bf16 W chunk already in shared memory
+                epi_sync();
+                if (et < Nc) {
+                    const float* mu = a.centre + static_cast<size_t>(bg) * kD;
+                    float c = 0.0f;
+                    for (int e = 0; e < kD; ++e) {
+                        const uint32_t off = (e >> 6) * kBHalfBytes + et * 128 +
+                                             ((((e & 63) >> 3) ^ (et & 7)) << 4) + ((e & 7) << 1);
+                        c = fmaf(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sB + off)),
+                                 __ldg(mu + e), c);
+                    }
+                    cvec[et] = c;
+                }
+                epi_sync();
+                cur_bg = bg;
+            }
+            for (int t = 0; t < ntile; ++t, ++it) {
+                const int ab = it & 1;
+                if (!aborted) {
+                    const bool got = mbar_wait(bar_tfull + 8 * ab, (it >> 1) & 1, abort_flag,
+                                               a.status);
+                    aborted = !__all_sync(0xffffffffu, got);   // keep the warp uniform
+                }
+                if (!aborted) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int cg = 0; cg < 4; ++cg) {
+                        const int col0 = half * 128 + cg * 32;
+                        if (col0 >= Nc) break;
+                        uint32_t v[32];
+                        tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                      ab * kChunkN + col0,
+                                  v);
+                        tmem_ld_wait();
+                        uint32_t mine = 0;
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const float4 cc = *reinterpret_cast<const float4*>(cvec + col0 + 4 * c4);
+                            const float cs[4] = {cc.x, cc.y, cc.z, cc.w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int c = 4 * c4 + q;
+                                const uint32_t bal =
+                                    __ballot_sync(0xffffffffu, __uint_as_float(v[c]) > cs[q]);
+                                if (lane == c) mine = bal;
+                            }
+                        }
+                        if (col0 + lane < Nc) stg[(t * 4 + quad) * kStgPitch + col0 + lane] = mine;
+                    }
+                    tc_fence_before();
+                }
+                __syncwarp();
+                if (lane == 0 && !aborted) mbar_arrive(bar_tempty + 8 * ab);
+            }
+            epi_sync();
+            if (!aborted) {
+                uint32_t* dst = a.codes + (static_cast<size_t>(bg) * a.nblk + blk) *
+                                              static_cast<size_t>(a.C) * kWordsPerBlock +
+                                static_cast<size_t>(j0) * kWordsPerBlock;
+                for (int r = ew; r < Nc; r += kEpiWarps)
+                    dst[r * kWordsPerBlock + lane] = stg[lane * kStgPitch + r];
+            }
+            epi_sync();
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(2 * kChunkN)
+                     : "memory");
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+cudaError_t prepare_encode_tc() {
+    cudaError_t e = cudaFuncSetAttribute(encode_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return encode_tiled_fn() ? cudaSuccess : cudaErrorNotSupported;
+}
+
+cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* W, int B,
+                             int Hkv, int n, int K, int L, uint32_t* codes, int* status,
+                             cudaStream_t st) {
+    const int C = K * L;
+    if (C == 0 || n == 0) return cudaSuccess;
+    EncodeTiledFn enc = encode_tiled_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap map;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(n),
+                                static_cast<cuuint64_t>(B) * Hkv};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                                   static_cast<cuuint64_t>(n) * kD * 2};
+    const cuuint32_t box[3] = {64, kTileM, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(keys), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    EncodeArgs a;
+    a.centre = centre;
+    a.W = reinterpret_cast<const __nv_bfloat16*>(W);
+    a.codes = codes;
+    a.status = status;
+    a.C = C;
+    a.nchunk = (C + kChunkN - 1) / kChunkN;
+    a.nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
+    a.n = n;
+    a.units = B * Hkv * a.nblk;
+    int parts = device_sm_count() / a.nchunk;
+    if (parts < 1) parts = 1;
+    if (parts > a.units) parts = a.units;
+    a.parts = parts;
+    encode_tc_kernel<<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
+    return cudaGetLastError();
+}
+
+}  // namespace mp

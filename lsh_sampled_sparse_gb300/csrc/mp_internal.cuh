@@ -1,0 +1,89 @@
+// Internal declarations shared by the translation units of libmagicpig.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "magicpig.h"
+
+namespace mp {
+
+constexpr int kKeysPerBlock = MP_KEYS_PER_BLOCK;   // keys per bit-sliced code block
+constexpr int kWordsPerBlock = kKeysPerBlock / 32;  // uint32 words per plane row
+constexpr int kD = 128;                             // the only head dimension supported
+
+// Device status word values (mp_status codes); kernels only ever raise MP_ERR_TIMEOUT.
+int* device_status_ptr();          // address of this device's status word (nullptr on error)
+int device_sm_count();
+
+// Scratch carved out of the decode workspace (all pointers 256-byte aligned).
+struct DecodeScratch {
+    uint32_t* qbits;     // [B*Hq][qwords] query sign bits
+    float4* qstat;       // [B*Hq] {|q|, q.mu, 0, 0}
+    float* pm;           // [B*Hq][nblk] running max of each block's partial softmax
+    float* pl;           // [B*Hq][nblk] its sum of weights
+    float* po;           // [B*Hq][nblk][128] its weighted value sum
+    unsigned* counters;  // [B*Hkv] blocks finished, for the last block's merge
+    uint32_t* selmask;   // [B*Hq][nblk][32] selection bits (debug only, else nullptr)
+};
+
+struct DecodeShape {
+    int B, Hq, Hkv, n, d, K, L, C, qwords, nblk, n_sink, n_local;
+    float scale;
+};
+
+size_t decode_scratch_bytes(const DecodeShape& s, bool debug);
+DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug);
+
+// ---- launchers (each returns the launch error, cudaSuccess otherwise) -------------------------
+cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int n, float* centre,
+                            float* partial, int nsplit, cudaStream_t st);
+int key_mean_splits(int n);
+
+cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* W, int B,
+                             int Hkv, int n, int K, int L, uint32_t* codes, int* status,
+                             cudaStream_t st);
+cudaError_t launch_encode_simt(const void* keys, bool keys_bf16, const float* centre,
+                               const void* W, bool w_bf16, int B, int Hkv, int n, int K, int L,
+                               uint32_t* codes, cudaStream_t st);
+
+// query sign bits, |q| and q.mu into the scratch; also resets the merge counters
+cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, const void* W,
+                           bool w_bf16, const DecodeShape& s, const DecodeScratch& ws,
+                           cudaStream_t st);
+// fused collide/select/gather/attend/merge; cudaErrorNotSupported if it cannot fit a CTA
+cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
+                           const float* centre, const void* keys, const void* values,
+                           bool kv_bf16, const DecodeShape& s, float* out,
+                           const DecodeScratch& ws, cudaStream_t st);
+bool decode_supported(const DecodeShape& s, bool kv_bf16);
+
+cudaError_t launch_compact_selection(const uint32_t* selmask, int rows, int n, int nblk,
+                                     int32_t* sel_idx, int32_t* sel_count, cudaStream_t st);
+cudaError_t launch_collision_counts(const uint32_t* codes, const uint32_t* qbits,
+                                    const DecodeShape& s, uint8_t* cnt, cudaStream_t st);
+cudaError_t launch_codes_unpack(const uint32_t* codes, int BH, int n, int K, int L,
+                                uint32_t* out, cudaStream_t st);
+
+// Force-load every kernel of the library (so that nothing loads lazily inside a stream capture)
+// and raise the dynamic shared-memory limits once per device.
+cudaError_t prepare_encode_tc();
+cudaError_t prepare_decode();
+cudaError_t prepare_misc();
+
+// ---- small device helpers ---------------------------------------------------------------------
+__device__ __forceinline__ float to_float(float x) { return x; }
+__device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ float load_elem(const void* p, bool bf16, size_t i) {
+    return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i])
+                : reinterpret_cast<const float*>(p)[i];
+}
+
+// bits of a 32-key word whose offset within the word is below x (x may be out of [0, 32])
+__device__ __forceinline__ uint32_t bits_below(int x) {
+    return x <= 0 ? 0u : (x >= 32 ? 0xffffffffu : ((1u << x) - 1u));
+}
+
+}  // namespace mp

@@ -1,0 +1,251 @@
+// Key centre, the fp32 CUDA-core encoder, and the inspection kernels (selection lists,
+// collision counts, unpacked codes).
+#include "mp_internal.cuh"
+
+namespace mp {
+namespace {
+
+// ------------------------------------------------------------------------------------------------
+// Centre: mu = (1/n) sum_i k_i per head ("LSH Sampling...", method details, data preprocessing
+// and centering). Fixed partition into row ranges, fixed reduction order: run-to-run identical.
+// ------------------------------------------------------------------------------------------------
+constexpr int kMeanRows = 512;     // rows per partial sum
+constexpr int kMeanThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kMeanThreads)
+    key_mean_partial_kernel(const T* keys, int n, int nsplit, float* partial) {
+    // thread -> (column group of 16 bytes, row phase); rows stride by the number of row phases
+    constexpr int kPer = 16 / sizeof(T);                 // elements per 16-byte load
+    constexpr int kGroups = kD / kPer;                   // column groups per row
+    constexpr int kPhases = kMeanThreads / kGroups;      // rows read in parallel
+    __shared__ float red[kPhases][kD + 4];
+    const int bh = blockIdx.y, split = blockIdx.x;
+    const int cg = threadIdx.x % kGroups, ph = threadIdx.x / kGroups;
+    const int r0 = split * kMeanRows, r1 = min(n, r0 + kMeanRows);
+    const T* base = keys + static_cast<size_t>(bh) * n * kD + cg * kPer;
+    float acc[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = 0.0f;
+#pragma unroll 4
+    for (int r = r0 + ph; r < r1; r += kPhases) {
+        const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(base + static_cast<size_t>(r) * kD));
+        const T* v = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) acc[i] += to_float(v[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) red[ph][cg * kPer + i] = acc[i];
+    __syncthreads();
+    if (threadIdx.x < kD) {
+        float s = 0.0f;
+        for (int p = 0; p < kPhases; ++p) s += red[p][threadIdx.x];
+        partial[(static_cast<size_t>(bh) * nsplit + split) * kD + threadIdx.x] = s;
+    }
+}
+
+__global__ void key_mean_final_kernel(const float* partial, int nsplit, int n, float* centre) {
+    const int bh = blockIdx.x, e = threadIdx.x;
+    float s = 0.0f;
+    for (int k = 0; k < nsplit; ++k) s += partial[(static_cast<size_t>(bh) * nsplit + k) * kD + e];
+    centre[static_cast<size_t>(bh) * kD + e] = s / static_cast<float>(n);
+}
+
+// ------------------------------------------------------------------------------------------------
+// fp32 CUDA-core encoder for dtype pairs the tensor-core path does not take (fp32 keys or W):
+// bit_{i,j} = [sum_e W[e][j] (k_i[e] - mu[e]) > 0] in fp32, one key per thread, a warp's 32 keys
+// form one word per hyperplane through a ballot.
+// ------------------------------------------------------------------------------------------------
+constexpr int kSimtKeys = 64;      // keys per CTA (2 words)
+constexpr int kSimtPlanes = 16;    // hyperplanes per pass
+
+__global__ void __launch_bounds__(kSimtKeys)
+    encode_simt_kernel(const void* keys, int keys_bf16, const float* centre, const void* W,
+                       int w_bf16, int n, int C, int nblk, uint32_t* codes) {
+    __shared__ float kbar[kSimtKeys][kD + 1];
+    __shared__ float Wsm[kD][kSimtPlanes];
+    const int bh = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    const int warp = tid >> 5;
+    const int i0 = tile * kSimtKeys;
+    for (int idx = tid; idx < kSimtKeys * kD; idx += kSimtKeys) {
+        const int r = idx / kD, e = idx % kD, i = i0 + r;
+        float v = 0.0f;
+        if (i < n)
+            v = load_elem(keys, keys_bf16, (static_cast<size_t>(bh) * n + i) * kD + e) -
+                centre[static_cast<size_t>(bh) * kD + e];
+        kbar[r][e] = v;
+    }
+    const int blk = i0 / kKeysPerBlock;
+    const int word = (i0 % kKeysPerBlock) / 32 + warp;
+    uint32_t* dst = codes + (static_cast<size_t>(bh) * nblk + blk) * static_cast<size_t>(C) *
+                                kWordsPerBlock + word;
+    for (int j0 = 0; j0 < C; j0 += kSimtPlanes) {
+        __syncthreads();
+        for (int idx = tid; idx < kD * kSimtPlanes; idx += kSimtKeys) {
+            const int e = idx / kSimtPlanes, c = idx % kSimtPlanes, j = j0 + c;
+            Wsm[e][c] = j < C ? load_elem(W, w_bf16, static_cast<size_t>(e) * C + j) : 0.0f;
+        }
+        __syncthreads();
+        float P[kSimtPlanes];
+#pragma unroll
+        for (int c = 0; c < kSimtPlanes; ++c) P[c] = 0.0f;
+        for (int e = 0; e < kD; ++e) {
+            const float x = kbar[tid][e];
+#pragma unroll
+            for (int c = 0; c < kSimtPlanes; ++c) P[c] = fmaf(Wsm[e][c], x, P[c]);
+        }
+        uint32_t mine = 0;
+#pragma unroll
+        for (int c = 0; c < kSimtPlanes; ++c) {
+            const uint32_t bal = __ballot_sync(0xffffffffu, P[c] > 0.0f);
+            if (lane == c) mine = bal;
+        }
+        if (lane < kSimtPlanes && j0 + lane < C)
+            dst[static_cast<size_t>(j0 + lane) * kWordsPerBlock] = mine;
+    }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Inspection kernels
+// ------------------------------------------------------------------------------------------------
+// Per query row: ascending indices of the selected keys from the per-block selection words.
+__global__ void compact_selection_kernel(const uint32_t* selmask, int n, int nblk, int32_t* sel_idx,
+                                         int32_t* sel_count) {
+    const int row = blockIdx.x, lane = threadIdx.x;
+    const uint32_t* m = selmask + static_cast<size_t>(row) * nblk * 32;
+    int32_t* out = sel_idx + static_cast<size_t>(row) * n;
+    int pos = 0;
+    for (int blk = 0; blk < nblk; ++blk) {
+        const uint32_t w = m[blk * 32 + lane];
+        const int c = __popc(w);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int p = pos + incl - c;
+        uint32_t bits = w;
+        while (bits) {
+            const int bit = __ffs(bits) - 1;
+            bits &= bits - 1;
+            out[p++] = blk * kKeysPerBlock + lane * 32 + bit;
+        }
+        pos += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) sel_count[row] = pos;
+}
+
+// Exact collision counts, one thread per (key, query row), straight from the definition.
+__global__ void collision_counts_kernel(const uint32_t* codes, const uint32_t* qbits, int n,
+                                        int nblk, int Hq, int G, int K, int L, int qwords,
+                                        uint8_t* cnt) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int row = blockIdx.y;
+    if (i >= n) return;
+    const int b = row / Hq, h = row % Hq, bh = b * (Hq / G) + h / G;
+    const int C = K * L;
+    const uint32_t* cb = codes + (static_cast<size_t>(bh) * nblk + i / kKeysPerBlock) *
+                                     static_cast<size_t>(C) * kWordsPerBlock +
+                         (i % kKeysPerBlock) / 32;
+    const uint32_t* qb = qbits + static_cast<size_t>(row) * qwords;
+    int c = 0;
+    for (int t = 0; t < L; ++t) {
+        bool eq = true;
+        for (int bb = 0; bb < K; ++bb) {
+            const int j = t * K + bb;
+            const uint32_t kbit = (cb[static_cast<size_t>(j) * kWordsPerBlock] >> (i & 31)) & 1u;
+            const uint32_t qbit = (qb[j >> 5] >> (j & 31)) & 1u;
+            eq = eq && (kbit == qbit);
+        }
+        c += eq ? 1 : 0;
+    }
+    cnt[static_cast<size_t>(row) * n + i] = static_cast<uint8_t>(c > 255 ? 255 : c);
+}
+
+__global__ void codes_unpack_kernel(const uint32_t* codes, int n, int nblk, int K, int L,
+                                    uint32_t* out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    const int bh = blockIdx.y;
+    if (i >= n) return;
+    const int C = K * L;
+    const uint32_t* cb = codes + (static_cast<size_t>(bh) * nblk + i / kKeysPerBlock) *
+                                     static_cast<size_t>(C) * kWordsPerBlock +
+                         (i % kKeysPerBlock) / 32;
+    for (int t = 0; t < L; ++t) {
+        uint32_t code = 0;
+        for (int bb = 0; bb < K; ++bb) {
+            const int j = t * K + bb;
+            code |= ((cb[static_cast<size_t>(j) * kWordsPerBlock] >> (i & 31)) & 1u) << bb;
+        }
+        out[(static_cast<size_t>(bh) * n + i) * L + t] = code;
+    }
+}
+
+}  // namespace
+
+int key_mean_splits(int n) { return (n + kMeanRows - 1) / kMeanRows; }
+
+cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int n, float* centre,
+                            float* partial, int nsplit, cudaStream_t st) {
+    const dim3 grid(nsplit, BH);
+    if (bf16)
+        key_mean_partial_kernel<__nv_bfloat16><<<grid, kMeanThreads, 0, st>>>(
+            reinterpret_cast<const __nv_bfloat16*>(keys), n, nsplit, partial);
+    else
+        key_mean_partial_kernel<float><<<grid, kMeanThreads, 0, st>>>(
+            reinterpret_cast<const float*>(keys), n, nsplit, partial);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    key_mean_final_kernel<<<BH, kD, 0, st>>>(partial, nsplit, n, centre);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_encode_simt(const void* keys, bool keys_bf16, const float* centre,
+                               const void* W, bool w_bf16, int B, int Hkv, int n, int K, int L,
+                               uint32_t* codes, cudaStream_t st) {
+    const int C = K * L;
+    if (C == 0 || n == 0) return cudaSuccess;
+    const int nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
+    const dim3 grid((n + kSimtKeys - 1) / kSimtKeys, B * Hkv);
+    encode_simt_kernel<<<grid, kSimtKeys, 0, st>>>(keys, keys_bf16, centre, W, w_bf16, n, C,
+                                                    nblk, codes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compact_selection(const uint32_t* selmask, int rows, int n, int nblk,
+                                     int32_t* sel_idx, int32_t* sel_count, cudaStream_t st) {
+    compact_selection_kernel<<<rows, 32, 0, st>>>(selmask, n, nblk, sel_idx, sel_count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_collision_counts(const uint32_t* codes, const uint32_t* qbits,
+                                    const DecodeShape& s, uint8_t* cnt, cudaStream_t st) {
+    const dim3 grid((s.n + 255) / 256, s.B * s.Hq);
+    collision_counts_kernel<<<grid, 256, 0, st>>>(codes, qbits, s.n, s.nblk, s.Hq, s.Hq / s.Hkv,
+                                                  s.K, s.L, s.qwords, cnt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_codes_unpack(const uint32_t* codes, int BH, int n, int K, int L,
+                                uint32_t* out, cudaStream_t st) {
+    const int nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
+    const dim3 grid((n + 255) / 256, BH);
+    codes_unpack_kernel<<<grid, 256, 0, st>>>(codes, n, nblk, K, L, out);
+    return cudaGetLastError();
+}
+
+cudaError_t prepare_misc() {
+    cudaFuncAttributes fa;
+    cudaError_t e;
+    if ((e = cudaFuncGetAttributes(&fa, key_mean_partial_kernel<float>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, key_mean_partial_kernel<__nv_bfloat16>)) != cudaSuccess)
+        return e;
+    if ((e = cudaFuncGetAttributes(&fa, key_mean_final_kernel)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, encode_simt_kernel)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, compact_selection_kernel)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, collision_counts_kernel)) != cudaSuccess) return e;
+    return cudaFuncGetAttributes(&fa, codes_unpack_kernel);
+}
+
+}  // namespace mp

@@ -1,0 +1,141 @@
+"""The C ABI on the host, with no GPU work: the library loads, exports what the header declares,
+and rejects bad arguments before anything could be launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "magicpig.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from lsh_sampled_sparse_gb300.build import build
+    build()
+    import lsh_sampled_sparse_gb300 as mp
+    return mp.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^MP_API\s+[\w\s\*]+?\b(mp_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("mp_key_mean", "mp_build_tables", "mp_decode_attention", "mp_encode_query",
+                 "mp_sampled_attention", "mp_debug_select", "mp_codes_unpack",
+                 "mp_device_status", "mp_codes_bytes"):
+        assert must in names
+    assert len(names) == len(set(names))
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(L):
+    import lsh_sampled_sparse_gb300 as mp
+    assert mp.abi_version() == 1
+    names = [L.mp_status_string(i).decode() for i in range(6)]
+    assert names == ["MP_OK", "MP_ERR_INVALID_ARG", "MP_ERR_UNSUPPORTED", "MP_ERR_CUDA",
+                     "MP_ERR_TIMEOUT", "MP_ERR_WORKSPACE"]
+
+
+def test_codes_bytes(L):
+    import lsh_sampled_sparse_gb300 as mp
+    # 1024-key blocks of K*L rows of 128 bytes: 187.5 bytes per key at (10, 150)
+    assert mp.codes_bytes(1, 8, 98304, 10, 150) == 8 * 96 * 1500 * 128
+    assert mp.codes_bytes(1, 1, 98304, 10, 150) / 98304 == 187.5
+    assert mp.codes_bytes(1, 1, 1, 10, 150) == 1500 * 128          # padded to a block
+    assert mp.codes_bytes(2, 3, 1025, 8, 75) == 2 * 3 * 2 * 600 * 128
+    assert mp.codes_bytes(1, 1, 100, 0, 4) == 0
+    assert mp.codes_bytes(0, 1, 100, 10, 150) == 0
+
+
+def test_workspace_sizes(L):
+    import lsh_sampled_sparse_gb300 as mp
+    assert mp.decode_workspace_bytes(1, 32, 8, 98304, 128, 10, 150, 4, 64) > 0
+    assert mp.debug_workspace_bytes(1, 32, 8, 98304, 128, 10, 150, 4, 64) > \
+        mp.decode_workspace_bytes(1, 32, 8, 98304, 128, 10, 150, 4, 64)
+    assert mp.decode_workspace_bytes(1, 32, 7, 1000, 128, 10, 150, 4, 64) == 0   # Hq % Hkv
+    assert mp.decode_workspace_bytes(1, 4, 1, 1000, 128, 33, 2, 4, 64) == 0      # K > 32
+    assert mp.decode_workspace_bytes(1, 4, 1, 1000, 128, 10, 0, 4, 64) == 0      # L < 1
+    assert mp.decode_workspace_bytes(1, 4, 1, 1000, 128, 10, 5, -1, 64) == 0     # n_sink < 0
+    assert mp.key_mean_workspace_bytes(1, 8, 98304, 128) > 0
+    assert mp.key_mean_workspace_bytes(1, 8, 98304, 64) == 0
+
+
+def _decode(L, ws_bytes=1 << 20, d=128, Hq=4, Hkv=1, n=1000, K=10, Lt=150, flags=0,
+            null_q=False, ptr=0x10000):
+    import lsh_sampled_sparse_gb300 as mp
+    p = mp.Params(K, Lt, 4, 64, 0.0, flags)
+    P = ctypes.c_void_p
+    q = None if null_q else P(ptr)
+    return L.mp_decode_attention(q, 1, P(ptr), P(ptr), P(ptr), 1, P(ptr), P(ptr), 1, 1, Hq, Hkv,
+                                 n, d, ctypes.byref(p), P(ptr), P(ptr), ws_bytes, None)
+
+
+def test_decode_rejects_bad_arguments_before_launch(L):
+    INVALID, UNSUPPORTED, WORKSPACE = 1, 2, 5
+    assert _decode(L, null_q=True) == INVALID
+    assert _decode(L, Hq=6, Hkv=4) == INVALID
+    assert _decode(L, flags=1) == INVALID
+    assert _decode(L, K=-1) == INVALID
+    assert _decode(L, ptr=0x10004) == INVALID                   # misaligned pointers
+    assert _decode(L, d=64) == UNSUPPORTED
+    assert _decode(L, Hq=3, Hkv=1) == UNSUPPORTED               # GQA group of 3
+    assert _decode(L, Hq=16, Hkv=1) == UNSUPPORTED              # GQA group of 16
+    assert _decode(L, ws_bytes=16) == WORKSPACE
+
+
+def test_split_halves_reject_bad_arguments_before_launch(L):
+    import lsh_sampled_sparse_gb300 as mp
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    p = mp.Params(10, 150, 4, 64, 0.0, 0)
+    assert L.mp_encode_query(None, 1, ok, ok, 1, 1, 4, 1, 1000, 128, ctypes.byref(p), ok,
+                             1 << 20, None) == 1
+    assert L.mp_encode_query(ok, 1, ok, ok, 1, 1, 4, 1, 1000, 64, ctypes.byref(p), ok,
+                             1 << 20, None) == 2
+    assert L.mp_encode_query(ok, 1, ok, ok, 1, 1, 4, 1, 1000, 128, ctypes.byref(p), ok,
+                             16, None) == 5
+    assert L.mp_sampled_attention(ok, 1, None, ok, ok, ok, 1, 1, 4, 1, 1000, 128,
+                                  ctypes.byref(p), ok, ok, 1 << 20, None) == 1
+    assert L.mp_sampled_attention(ok, 1, ok, ok, ok, ok, 1, 1, 4, 1, 1000, 128,
+                                  ctypes.byref(p), ok, ok, 16, None) == 5
+
+
+def test_build_and_mean_reject_bad_arguments(L):
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    assert L.mp_build_tables(None, 1, ok, ok, 1, 1, 1, 100, 128, 10, 150, ok, None) == 1
+    assert L.mp_build_tables(ok, 1, ok, ok, 1, 1, 1, 100, 64, 10, 150, ok, None) == 2
+    assert L.mp_build_tables(ok, 1, ok, ok, 1, 1, 1, 100, 128, 33, 150, ok, None) == 1
+    assert L.mp_build_tables(ok, 7, ok, ok, 1, 1, 1, 100, 128, 10, 150, ok, None) == 1
+    assert L.mp_build_tables(P(0x10002), 1, ok, ok, 1, 1, 1, 100, 128, 10, 150, ok, None) == 1
+    # K == 0: nothing to encode, nothing touched
+    assert L.mp_build_tables(None, 1, None, None, 1, 1, 1, 100, 128, 0, 150, None, None) == 0
+    assert L.mp_key_mean(ok, 1, 1, 1, 0, 128, ok, ok, 1 << 20, None) == 1
+    assert L.mp_key_mean(ok, 1, 1, 1, 100, 64, ok, ok, 1 << 20, None) == 2
+    assert L.mp_key_mean(ok, 1, 1, 8, 98304, 128, ok, ok, 16, None) == 5
+
+
+def test_binding_refuses_cpu_tensors(L):
+    import torch
+
+    import lsh_sampled_sparse_gb300 as mp
+    with pytest.raises(TypeError):
+        mp.key_mean(torch.zeros(1, 1, 16, 128))
+
+
+def test_package_has_no_cpu_fallback_and_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "lsh_sampled_sparse_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
