@@ -1,0 +1,535 @@
+#!/usr/bin/env python3
+"""Benchmark of LSH-sampled decode attention (MagicPIG) on GB300.
+
+One step = the whole path over one batch of synthetic input: for every layer, centre the keys
+(mp_key_mean), build the packed SimHash codes (mp_build_tables, tcgen05), encode the queries
+(mp_encode_query) and run the fused collide/select/gather/attend kernel (mp_sampled_attention).
+Default workload: Llama-3.1-8B-shaped decode at 96K context (B=1, 32 query / 8 KV heads, d=128,
+n=98,304, 32 layers, (K, L) = (10, 150), 4 sink + 64 local tokens exact), bf16 K/V.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). --impl reference times the fp64 CPU oracle on a bounded sample of
+the same workload. Under torchrun every rank runs its own copy of the workload (weak scaling, no
+collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, make_hyperplanes, make_layer  # noqa: E402
+
+METRIC = "decode-attention queries/s and HBM GB/s (% of peak) at 96K ctx, 1×GB300"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ("key_mean", "build_tables", "encode_query", "sampled_attention")
+# kernels each stage launches (one library call each)
+STAGE_LAUNCHES = {"key_mean": 2, "build_tables": 1, "encode_query": 1, "sampled_attention": 1}
+STAGE_SOURCES = {"key_mean": "mp_misc.cu", "build_tables": "mp_encode_tc.cu",
+                 "encode_query": "mp_decode.cu", "sampled_attention": "mp_decode.cu"}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="llama8b_n96k_32layers", choices=sorted(WORKLOADS))
+    ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no collective on the data path)
+# ------------------------------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend)
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(world: int, value: float, device) -> float:
+    """Max of a per-rank float over all ranks (the slowest rank sets the job's time)."""
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank_step: int, steps: int, max_ms: float) -> float:
+    """Units all ranks processed / the slowest rank's time (weak scaling)."""
+    return world * units_per_rank_step * steps / (max_ms / 1e3)
+
+
+# ------------------------------------------------------------------------------------------------
+# measured peaks, clocks, profiler-derived traffic
+# ------------------------------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def source_sha(name: str) -> str:
+    path = os.path.join(ROOT, "lsh_sampled_sparse_gb300", "csrc", name)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(stage: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        tab = json.load(f)
+    e = tab.get(stage, {}).get(workload)
+    if not e or e.get("source_sha") != source_sha(STAGE_SOURCES[stage]):
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+class Layer:
+    __slots__ = ("keys", "values", "q", "centre", "codes", "out")
+
+
+def setup_inputs(mp, wl, layers: int, device):
+    W = make_hyperplanes(wl, device=device)
+    codes_words = mp.codes_bytes(wl.B, wl.Hkv, wl.n, wl.K, wl.L) // 4
+    state = []
+    for layer in range(layers):
+        x = make_layer(wl, layer, device=device)
+        s = Layer()
+        s.keys, s.values, s.q = x["keys"], x["values"], x["q"]
+        s.centre = torch.empty(wl.B, wl.Hkv, wl.d, dtype=torch.float32, device=device)
+        s.codes = torch.empty(max(codes_words, 4), dtype=torch.int32, device=device)
+        s.out = torch.empty(wl.B, wl.Hq, wl.d, dtype=torch.float32, device=device)
+        state.append(s)
+    ws_mean = torch.empty(max(mp.key_mean_workspace_bytes(wl.B, wl.Hkv, wl.n, wl.d), 256),
+                          dtype=torch.uint8, device=device)
+    ws_dec = torch.empty(mp.decode_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.n, wl.d, wl.K, wl.L,
+                                                   wl.n_sink, wl.n_local),
+                         dtype=torch.uint8, device=device)
+    return W, state, ws_mean, ws_dec
+
+
+def run_step(mp, wl, W, state, ws_mean, ws_dec, stream, marks=None):
+    """One pass of the whole path over every layer. marks[layer]: 5 events around the 4 stages."""
+    for li, s in enumerate(state):
+        ev = marks[li] if marks is not None else None
+        if ev:
+            ev[0].record(stream)
+        mp.key_mean(s.keys, s.centre, ws_mean, stream)
+        if ev:
+            ev[1].record(stream)
+        mp.build_tables(s.keys, s.centre, W, wl.K, wl.L, s.codes, stream)
+        if ev:
+            ev[2].record(stream)
+        mp.encode_query(s.q, s.centre, W, s.keys.shape, wl.K, wl.L, wl.n_sink, wl.n_local,
+                        ws_dec, stream=stream)
+        if ev:
+            ev[3].record(stream)
+        mp.sampled_attention(s.q, s.codes, s.centre, s.keys, s.values, wl.K, wl.L, wl.n_sink,
+                             wl.n_local, s.out, ws_dec, stream=stream)
+        if ev:
+            ev[4].record(stream)
+
+
+def sample_set_sizes(mp, wl, W, state):
+    """|union over the GQA group of S_h| and sum of |S_h| per (layer, b, g), from the library's
+    own selection (mp_debug_select), untimed; used only to count algorithmic bytes."""
+    union, total = [], []
+    for s in state:
+        d = mp.debug_select(s.q, s.codes, s.centre, W, s.keys, s.values, wl.K, wl.L, wl.n_sink,
+                            wl.n_local, counts=False)
+        idx = d["sel_idx"]
+        cnt = d["sel_count"].cpu()
+        for b in range(wl.B):
+            for g in range(wl.Hkv):
+                sets = [idx[b, h, :int(cnt[b, h])] for h in range(g * wl.G, (g + 1) * wl.G)]
+                total.append(sum(int(x.numel()) for x in sets))
+                union.append(int(torch.unique(torch.cat(sets)).numel()))
+    return union, total
+
+
+def algorithmic(wl, union_sizes):
+    """Per-launch algorithmic bytes / flops of each stage (per-layer averages)."""
+    es = 2 if wl.kv_dtype == torch.bfloat16 else 4
+    qs = 2 if wl.q_dtype == torch.bfloat16 else 4
+    units = wl.B * wl.Hkv
+    n_exact = min(wl.n, wl.n_sink + wl.n_local)
+    codes = wl.n * wl.C / 8                                  # packed bits per (b, g)
+    mean_union = sum(union_sizes) / max(1, len(union_sizes))
+    return {
+        "key_mean": {"bytes": units * (wl.n * wl.d * es + wl.d * 4)},
+        "build_tables": {"flops": units * 2.0 * wl.n * wl.d * wl.C,
+                         "bytes": units * (wl.n * wl.d * es + codes)},
+        "encode_query": {"bytes": wl.B * wl.Hq * wl.d * qs + wl.d * wl.C * 2},
+        "sampled_attention": {"bytes": units * (codes + (mean_union + n_exact) * 2 * wl.d * es)
+                              + wl.B * wl.Hq * wl.d * (qs + 4)},
+        "mean_union_rows": mean_union,
+    }
+
+
+ORACLE_SAMPLE_KEYS = 16384   # keys per oracle sample; every oracle step is linear in n
+
+
+def oracle_unit_seconds(O, kb, vb, qb, Wc, wl, n_s):
+    """Seconds the fp64 oracle (as it stands) takes for A0-A5 of one (b, g) unit whose context is
+    the first n_s keys, all G query heads of the group."""
+    import numpy as np
+    k = kb[:n_s]
+    v = vb[:n_s]
+    t0 = time.perf_counter()
+    mu = O.key_centre(k).astype(np.float32)                                 # A0
+    kcodes, _, _ = O.encode_keys(k, mu, Wc, wl.K, wl.L)                     # A1
+    for h in range(qb.shape[0]):
+        qc = O.encode_query(qb[h], Wc, wl.K, wl.L)[0][0]                    # A2
+        O.decode_head(qb[h], k, v, mu, kcodes, qc, wl.K, wl.L, wl.n_sink,
+                      wl.n_local)                                           # A3-A5
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_sample(wl, state, W, budget_s: float):
+    """Oracle throughput on whole-unit samples of the workload, scaled to the full context."""
+    import oracle as O
+    keys, values, q = state[0].keys, state[0].values, state[0].q
+    Wc = W.detach().cpu()
+    n_s = min(wl.n, ORACLE_SAMPLE_KEYS)
+    t_total, units = 0.0, 0
+    for u in range(wl.B * wl.Hkv):
+        b, g = divmod(u, wl.Hkv)
+        t_total += oracle_unit_seconds(O, keys[b, g, :n_s].cpu(), values[b, g, :n_s].cpu(),
+                                       q[b, g * wl.G:(g + 1) * wl.G].cpu(), Wc, wl, n_s)
+        units += 1
+        if t_total >= budget_s:
+            break
+    t_full = t_total * wl.n / n_s             # the same units at the full context length
+    cores = len(os.sched_getaffinity(0))
+    return {"value": units * wl.G / t_full, "unit": "queries/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{units} (layer 0, sequence, KV head) unit(s) of {wl.name}, each A0 centre,"
+                      f" A1 encode on {wl.C} hyperplanes, A2-A5 for its {wl.G} query heads, run"
+                      f" on the first {n_s} of the {wl.n} keys ({t_total:.1f} s) and scaled"
+                      f" x{wl.n / n_s:g} to the full context (every oracle step is linear in n);"
+                      f" fp64 numpy"}
+
+
+def run_e2e(mp, wl, W, state, ws_mean, ws_dec, steps: int):
+    """The same step through the public API with host buffers: every step copies every layer's
+    K, V, q (and W) from pinned host memory on a copy stream, overlapped with the previous
+    layers' compute, and reads every layer's output back to pinned host memory."""
+    hs = []
+    for s in state:
+        hk = torch.empty(s.keys.shape, dtype=s.keys.dtype, pin_memory=True)
+        hv = torch.empty(s.values.shape, dtype=s.values.dtype, pin_memory=True)
+        hq = torch.empty(s.q.shape, dtype=s.q.dtype, pin_memory=True)
+        hk.copy_(s.keys)
+        hv.copy_(s.values)
+        hq.copy_(s.q)
+        ho = torch.empty(s.out.shape, dtype=s.out.dtype, pin_memory=True)
+        hs.append((hk, hv, hq, ho))
+    hW = torch.empty(W.shape, dtype=W.dtype, pin_memory=True)
+    hW.copy_(W)
+    h2d = sum(a.numel() * a.element_size() for t in hs for a in t[:3]) + \
+        hW.numel() * hW.element_size()
+    d2h = sum(t[3].numel() * t[3].element_size() for t in hs)
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in state]
+
+    def one():
+        copy.wait_stream(comp)
+        with torch.cuda.stream(copy):
+            W.copy_(hW, non_blocking=True)
+            for li, (s, (hk, hv, hq, _)) in enumerate(zip(state, hs)):
+                s.keys.copy_(hk, non_blocking=True)
+                s.values.copy_(hv, non_blocking=True)
+                s.q.copy_(hq, non_blocking=True)
+                ready[li].record(copy)
+        for li, (s, (_, _, _, ho)) in enumerate(zip(state, hs)):
+            comp.wait_event(ready[li])
+            run_step(mp, wl, W, [s], ws_mean, ws_dec, comp)
+            ho.copy_(s.out, non_blocking=True)
+        comp.synchronize()
+
+    one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = (time.perf_counter() - t0) / steps
+    hs.clear()
+    return dt, h2d, d2h
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    from lsh_sampled_sparse_gb300.build import build
+    if rank == 0:
+        build()
+    dist_barrier(world)
+    import lsh_sampled_sparse_gb300 as mp
+    mp.lib()
+
+    wl = WORKLOADS[args.workload]
+    layers = args.layers or wl.layers
+    W, state, ws_mean, ws_dec = setup_inputs(mp, wl, layers, device)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        run_step(mp, wl, W, state, ws_mean, ws_dec, stream)
+    torch.cuda.synchronize()
+
+    marks = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(layers)]
+             for _ in range(args.steps)]
+    begin = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    begin.record(stream)
+    for k in range(args.steps):
+        run_step(mp, wl, W, state, ws_mean, ws_dec, stream, marks[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    clk = clocks.stop()
+    total_ms = dist_max(world, begin.elapsed_time(end), device)
+    ms_per_step = total_ms / args.steps
+    assert mp.device_status() == 0, "a device-side wait gave up during the timed region"
+
+    stage_ms = {k: 0.0 for k in STAGES}
+    for step_marks in marks:
+        for ev in step_marks:
+            for i, k in enumerate(STAGES):
+                stage_ms[k] += ev[i].elapsed_time(ev[i + 1])
+    queries_per_step = wl.B * wl.Hq * layers
+    value = job_throughput(world, queries_per_step, args.steps, total_ms)
+    per_stage = {k: v / args.steps for k, v in stage_ms.items()}        # ms per step
+    per_launch = {k: per_stage[k] / layers for k in STAGES}             # ms per call
+
+    union, total = sample_set_sizes(mp, wl, W, state)
+    alg = algorithmic(wl, union)
+    peaks, peak_src = load_peaks()
+    rooflines = {}
+    for k in STAGES:
+        t = per_launch[k] / 1e3
+        if k == "build_tables":
+            ach = alg[k]["flops"] / t / 1e12
+            rooflines[k] = {"bound": "tensor", "achieved": ach,
+                            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                            "frac": ach / peaks["bf16_tflops_sustained"],
+                            "hbm_gbs": alg[k]["bytes"] / t / 1e9}
+        else:
+            ach = alg[k]["bytes"] / t / 1e9
+            rooflines[k] = {"bound": "hbm" if k != "encode_query" else "latency",
+                            "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": ach / peaks["hbm_gbs"]}
+        rooflines[k]["ms_per_launch"] = per_launch[k]
+        rooflines[k]["share"] = per_stage[k] / max(1e-9, sum(per_stage.values()))
+        rooflines[k]["traffic"] = profiled_traffic(k, wl.name)
+    dominant = max(STAGES, key=lambda k: per_stage[k])
+    roof = dict(rooflines[dominant])
+    roof["kernel"] = dominant
+    roof["peak_source"] = "of measured (MEASURED_PEAKS.json)" if peak_src == "measured" \
+        else "of fallback"
+
+    decode_ms = per_stage["encode_query"] + per_stage["sampled_attention"]
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "queries/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "n": wl.n, "d": wl.d,
+            "layers": layers, "K": wl.K, "L": wl.L, "n_sink": wl.n_sink,
+            "n_local": wl.n_local, "kv_dtype": str(wl.kv_dtype).replace("torch.", ""),
+            "step": "A0 centre + A1 encode (tcgen05) + A2 query encode + A3-A5 "
+                    "collide/gather/attend/merge, every layer",
+            "l2": f"inputs larger than L2: {2 * layers * wl.B * wl.Hkv * wl.n * wl.d * 2 / 1e9:.1f}"
+                  " GB of K/V per step (L2 129 MB)",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": roof,
+        "rooflines": rooflines,
+        "decode_only": {
+            "queries_per_s": queries_per_step / (decode_ms / 1e3),
+            "attention_ms_per_token": decode_ms,
+            "sampled_attention_gbs": rooflines["sampled_attention"]["achieved"],
+        },
+        "sample_sets": {
+            "mean_union_rows_per_kv_head": alg["mean_union_rows"],
+            "mean_rows_per_query_head": sum(total) / max(1, len(total)) / wl.G,
+            "fraction_of_n": sum(total) / max(1, len(total)) / wl.G / wl.n,
+        },
+        "gpu_launches": sum(STAGE_LAUNCHES.values()) * layers * args.steps,
+        "clocks": clk,
+    }
+
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(wl, state, W, args.cpu_seconds)
+    if not args.no_e2e:
+        dt, h2d, d2h = run_e2e(mp, wl, W, state, ws_mean, ws_dec, args.e2e_steps)
+        dt = dist_max(world, dt, device)
+        line["e2e"] = {"value": world * queries_per_step / dt, "unit": "queries/s",
+                       "ms_per_step": dt * 1e3, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h,
+                       "note": "public API with host buffers: pinned H2D of every layer's K, V, q"
+                               " and W each step (copy stream overlapped with compute), D2H of"
+                               " every output"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle, as it stands, on a bounded sample of the workload
+# ------------------------------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle as O
+    wl = WORKLOADS[args.workload]
+    # per step: one (b, g) unit of layer 0 on the first ORACLE_SAMPLE_KEYS keys, inputs drawn on
+    # the CPU from the same recipe; the time is scaled linearly to the full context
+    n_s = min(wl.n, ORACLE_SAMPLE_KEYS)
+    unit_wl = wl.replace(B=1, Hq=wl.G, Hkv=1, layers=1)
+    x = make_layer(unit_wl, 0)
+    W = make_hyperplanes(wl)
+    kb, vb, qb = x["keys"][0, 0], x["values"][0, 0], x["q"][0]
+    for _ in range(args.warmup):
+        oracle_unit_seconds(O, kb, vb, qb, W, wl, n_s)
+    ts = [oracle_unit_seconds(O, kb, vb, qb, W, wl, n_s) for _ in range(args.steps)]
+    dt = sum(ts) / len(ts) * wl.n / n_s
+    value = wl.G / dt
+    cores = len(os.sched_getaffinity(0))
+    sample = (f"per step one (sequence, KV head) unit of layer 0 of {wl.name}: A0 centre, A1 "
+              f"encode on {wl.C} hyperplanes, A2-A5 for {wl.G} query heads, run on the first "
+              f"{n_s} of the {wl.n} keys and scaled x{wl.n / n_s:g} to the full context (every "
+              f"oracle step is linear in n); fp64 numpy oracle")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "n": wl.n,
+                   "d": wl.d, "layers": wl.layers, "K": wl.K, "L": wl.L},
+        "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
