@@ -181,6 +181,31 @@ MP_API mp_status mp_debug_select(const void* q, mp_dtype q_dtype, const uint32_t
 MP_API mp_status mp_codes_unpack(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
                                  uint32_t* table_codes, cudaStream_t stream);
 
+/* Size of the fixed scratch array mp_decode_attention_noalloc uses (8 MiB). */
+#define MP_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* mp_decode_attention for callers that cannot allocate device memory. The paper has no
+ * counterpart; this entry point exists for callers such as plugins of a runtime that owns all
+ * device memory through its own pool, or latency-critical loops where an allocation (which may
+ * synchronise the device) is not allowed, or code that holds no allocator at all. It takes the
+ * same inputs and output as mp_decode_attention, without a workspace: its scratch is a fixed
+ * array of MP_NOALLOC_SCRATCH_BYTES inside the library, resident on every GPU that loads the
+ * library until the process exits. It never allocates or frees memory.
+ *   - The first call on a device (with that device current) resolves the array's address and
+ *     loads the decode kernels; make that first call before any stream capture.
+ *   - Shapes that need more scratch than the array holds (mp_decode_workspace_bytes() above
+ *     MP_NOALLOC_SCRATCH_BYTES) are rejected with MP_ERR_WORKSPACE before anything is launched.
+ *   - Every call on a device shares the one array. The merge counters are reset at the start of
+ *     each call and the rest is written before it is read, so sequential calls are independent;
+ *     calls whose kernels overlap on the GPU (other streams, unordered threads) race on it.
+ * Other errors as mp_decode_attention. */
+MP_API mp_status mp_decode_attention_noalloc(const void* q, mp_dtype q_dtype,
+                                             const uint32_t* codes, const float* centre,
+                                             const void* W, mp_dtype w_dtype, const void* keys,
+                                             const void* values, mp_dtype kv_dtype, int B, int Hq,
+                                             int Hkv, int n, int d, const mp_params* prm,
+                                             float* out, cudaStream_t stream);
+
 /* Synchronise the current device, return its status word (MP_OK or MP_ERR_TIMEOUT) through
  * *status and reset it to MP_OK. Returns MP_ERR_CUDA if the device cannot be reached. */
 MP_API mp_status mp_device_status(int* status);

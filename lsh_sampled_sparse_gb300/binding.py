@@ -53,6 +53,8 @@ def _declare(L):
                                  + [_c_int] * 5 + [P, _vp, _vp, _c_size, _vp]),
         "mp_debug_select": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp, _c_int]
                             + [_c_int] * 5 + [P, _vp, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
+        "mp_decode_attention_noalloc": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp,
+                                                 _c_int] + [_c_int] * 5 + [P, _vp, _vp]),
         "mp_codes_unpack": (_c_int, [_vp] + [_c_int] * 5 + [_vp, _vp]),
         "mp_device_status": (_c_int, [ctypes.POINTER(_c_int)]),
     }
