@@ -43,7 +43,7 @@ STAGE_SOURCES = {"key_mean": "mp_misc.cu", "build_tables": "mp_encode_tc.cu",
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama8b_n96k_32layers", choices=sorted(WORKLOADS))
@@ -106,7 +106,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling every 200 ms while the timed region runs."""
+    """nvidia-smi sampling every 50 ms; started under load just before the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -123,7 +123,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -378,9 +378,13 @@ def run_ours(args):
     begin = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
+    clocks.start()
+    t_roll = time.perf_counter()          # keep the GPU busy while the sampler starts up
+    while time.perf_counter() - t_roll < 0.4:
+        run_step(mp, wl, W, state, ws_mean, ws_dec, stream)
+        torch.cuda.synchronize()
     dist_barrier(world)
     torch.cuda.synchronize()
-    clocks.start()
     begin.record(stream)
     for k in range(args.steps):
         run_step(mp, wl, W, state, ws_mean, ws_dec, stream, marks[k])

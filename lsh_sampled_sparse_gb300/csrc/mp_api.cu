@@ -67,6 +67,7 @@ bool fill_shape(int B, int Hq, int Hkv, int n, int d, const mp_params* prm, Deco
     s->L = prm->L;
     s->C = prm->K * prm->L;
     s->qwords = (s->C + 31) / 32;
+    s->cpad = (s->C + 3) & ~3;
     s->nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
     s->n_sink = prm->n_sink;
     s->n_local = prm->n_local;
@@ -90,11 +91,15 @@ size_t decode_scratch_bytes(const DecodeShape& s, bool debug) {
     const size_t rows = static_cast<size_t>(s.B) * s.Hq;
     size_t b = 0;
     b += align256(rows * s.qwords * 4);                  // qbits
+    b += align256(rows * s.cpad * 4);                    // qmask
     b += align256(rows * 16);                            // qstat
-    b += align256(rows * s.nblk * 4) * 2;                // pm, pl
-    b += align256(rows * s.nblk * kD * 4);               // po
-    b += align256(static_cast<size_t>(s.B) * s.Hkv * 4); // counters
-    if (debug) b += align256(rows * s.nblk * 32 * 4);    // selmask
+    const size_t nsb = (s.nblk + kAttendBlockGroup - 1) / kAttendBlockGroup;
+    b += align256(rows * nsb * 4) * 2;                   // pm, pl
+    b += align256(rows * nsb * kD * 4);                  // po
+    b += align256(rows * 4);                             // counters
+    b += align256(rows * s.nblk * 32 * 4);               // selection words
+    b += align256((kLogUTableIntervals + 1) * 4);        // log u table
+    (void)debug;                                         // the debug path needs nothing more
     return b;
 }
 
@@ -104,17 +109,23 @@ DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug) {
     DecodeScratch d;
     d.qbits = reinterpret_cast<uint32_t*>(p);
     p += align256(rows * s.qwords * 4);
+    d.qmask = reinterpret_cast<uint32_t*>(p);
+    p += align256(rows * s.cpad * 4);
     d.qstat = reinterpret_cast<float4*>(p);
     p += align256(rows * 16);
+    const size_t nsb = (s.nblk + kAttendBlockGroup - 1) / kAttendBlockGroup;
     d.pm = reinterpret_cast<float*>(p);
-    p += align256(rows * s.nblk * 4);
+    p += align256(rows * nsb * 4);
     d.pl = reinterpret_cast<float*>(p);
-    p += align256(rows * s.nblk * 4);
+    p += align256(rows * nsb * 4);
     d.po = reinterpret_cast<float*>(p);
-    p += align256(rows * s.nblk * kD * 4);
+    p += align256(rows * nsb * kD * 4);
     d.counters = reinterpret_cast<unsigned*>(p);
-    p += align256(static_cast<size_t>(s.B) * s.Hkv * 4);
-    d.selmask = debug ? reinterpret_cast<uint32_t*>(p) : nullptr;
+    p += align256(rows * 4);
+    d.selmask = reinterpret_cast<uint32_t*>(p);
+    p += align256(rows * s.nblk * 32 * 4);
+    d.logu_tab = reinterpret_cast<float*>(p);
+    (void)debug;
     return d;
 }
 

@@ -16,56 +16,163 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr float kLogFltMin = -87.336544750553102f;   // log(FLT_MIN)
 constexpr float kPi = 3.14159265358979323846f;
-constexpr int kTFlag = 1 << 15;                     // list entry belongs to the exact set T
 constexpr int kCombinePitch = 132;                  // floats per (warp, head) partial: o, m, l
+constexpr int kAttendBlocks = kAttendBlockGroup;
+constexpr int kRingDepth = 4;                       // tables in flight per warp in the async scan
+constexpr int kRingMinK = 8, kRingMaxK = 11;        // K range the async scan handles
+constexpr int kLuIntervals = kLogUTableIntervals;   // log u table: cosine grid on [-1, 1]
+
+// log u(p) = log P[Binomial(L, p^K) >= 2] in fp32 with the accurate library functions, used to
+// fill the per-call table of log u over the cosine; same two-branch definition as below.
+__device__ float log_inclusion_ref(float p, int K, int L) {
+    if (L < 2) return -INFINITY;
+    if (K == 0) return 0.0f;
+    if (!(p > 0.0f)) return kLogFltMin;
+    const float lx = static_cast<float>(K) * logf(p);
+    const float x = expf(lx);
+    const float Lf = static_cast<float>(L);
+    if (x >= 1.0f) return 0.0f;
+    const float l1 = log1pf(-x);
+    if (Lf * x >= 0.5f) {
+        const float u = 1.0f - expf(Lf * l1) - Lf * x * expf((Lf - 1.0f) * l1);
+        return logf(fmaxf(u, 1.17549435e-38f));
+    }
+    const float r = x / (1.0f - x);
+    float term = 1.0f, tot = 1.0f;
+    for (int j = 2; j < L; ++j) {
+        term *= static_cast<float>(L - j) / static_cast<float>(j + 1) * r;
+        tot += term;
+        if (term < 1e-9f * tot) break;
+    }
+    return logf(0.5f * Lf * (Lf - 1.0f)) + 2.0f * lx + (Lf - 2.0f) * l1 + logf(tot);
+}
+
+// 1 / (j + 1) for the binomial-tail series below
+__constant__ float c_inv_next[66] = {
+    1.0f / 1, 1.0f / 2, 1.0f / 3, 1.0f / 4, 1.0f / 5, 1.0f / 6, 1.0f / 7, 1.0f / 8, 1.0f / 9,
+    1.0f / 10, 1.0f / 11, 1.0f / 12, 1.0f / 13, 1.0f / 14, 1.0f / 15, 1.0f / 16, 1.0f / 17,
+    1.0f / 18, 1.0f / 19, 1.0f / 20, 1.0f / 21, 1.0f / 22, 1.0f / 23, 1.0f / 24, 1.0f / 25,
+    1.0f / 26, 1.0f / 27, 1.0f / 28, 1.0f / 29, 1.0f / 30, 1.0f / 31, 1.0f / 32, 1.0f / 33,
+    1.0f / 34, 1.0f / 35, 1.0f / 36, 1.0f / 37, 1.0f / 38, 1.0f / 39, 1.0f / 40, 1.0f / 41,
+    1.0f / 42, 1.0f / 43, 1.0f / 44, 1.0f / 45, 1.0f / 46, 1.0f / 47, 1.0f / 48, 1.0f / 49,
+    1.0f / 50, 1.0f / 51, 1.0f / 52, 1.0f / 53, 1.0f / 54, 1.0f / 55, 1.0f / 56, 1.0f / 57,
+    1.0f / 58, 1.0f / 59, 1.0f / 60, 1.0f / 61, 1.0f / 62, 1.0f / 63, 1.0f / 64, 1.0f / 65,
+    1.0f / 66};
+
+// log u(p) = log P[Binomial(L, p^K) >= 2] in fp32, two branches: directly when L p^K >= 1/2,
+// else as log t_2 + log(1 + sum_{j>=3} t_j / t_2) with t_j the binomial terms; p <= 0 clamps to
+// log(FLT_MIN). log C(L, 2) comes in as log_c2, the series ratios (L - j) / (j + 1) use a
+// reciprocal table (at most 64 terms: below L p^K = 1/2 they shrink at least threefold per step),
+// log p and exp use the fast hardware approximations (errors far below the 1e-3 output
+// tolerance); log1p(-x) stays exact because (L - 2) multiplies it.
+__device__ __forceinline__ float log_inclusion_fast(float p, int K, int L, float log_c2) {
+    if (L < 2) return -INFINITY;
+    if (K == 0) return 0.0f;                       // p^0 = 1 and L >= 2: u = 1
+    if (!(p > 0.0f)) return kLogFltMin;
+    const float lx = static_cast<float>(K) * __logf(p);
+    const float x = __expf(lx);
+    const float Lf = static_cast<float>(L);
+    if (x >= 1.0f) return 0.0f;
+    const float l1 = log1pf(-x);
+    if (Lf * x >= 0.5f) {
+        const float u = 1.0f - __expf(Lf * l1) - Lf * x * __expf((Lf - 1.0f) * l1);
+        return __logf(fmaxf(u, 1.17549435e-38f));
+    }
+    const float r = __fdividef(x, 1.0f - x);
+    float term = 1.0f, tot = 1.0f;
+    const int jmax = min(L, 65);
+    for (int j = 2; j < jmax; ++j) {
+        term *= (Lf - static_cast<float>(j)) * c_inv_next[j] * r;
+        tot += term;
+        if (term < 1e-9f * tot) break;
+    }
+    return log_c2 + 2.0f * lx + (Lf - 2.0f) * l1 + __logf(tot);
+}
 
 // ------------------------------------------------------------------------------------------------
-// Query encoding: qbit_j = [w_j . q > 0] (the query is not centred), |q| and q.mu for the cosine
+// Query encoding: qbit_j = [w_j . q > 0] (the query is not centred), |q| and q.mu for the cosine.
+// One warp per query row, one lane per hyperplane of a 32-plane word. Besides the packed bits it
+// writes the per-plane XOR masks the scan uses (0 where the query bit is 1, ~0 where it is 0),
+// laid out [sequence x KV head][plane][head of the group] so a scan CTA copies its group's masks
+// in one contiguous piece.
 // ------------------------------------------------------------------------------------------------
-constexpr int kQPlanes = 64;    // hyperplanes per CTA
-constexpr int kQRows = 32;      // query rows per CTA
+constexpr int kQRows = 8;       // query rows per CTA (one per warp)
 
 struct QArgs {
     const void* q;
     const void* W;
     const float* centre;
     uint32_t* qbits;
+    uint32_t* qmask;
     float4* qstat;
     unsigned* counters;
-    int q_bf16, w_bf16, BHq, Hq, G, C, qwords, n_counters;
+    float* logu_tab;
+    int q_bf16, w_bf16, BHq, Hq, G, C, cpad, qwords, n_counters, K, L, qrow_ctas;
 };
 
 __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
-    __shared__ float Ws[kD][kQPlanes];
     __shared__ float Qs[kQRows][kD];
+    __shared__ float Ws[kD][32];                 // this word's 32 hyperplane columns
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int j0 = blockIdx.x * kQPlanes, r0 = blockIdx.y * kQRows;
-    const int nq = min(kQRows, a.BHq - r0);
-    for (int idx = tid; idx < kD * kQPlanes; idx += kThreads) {
-        const int e = idx / kQPlanes, c = idx % kQPlanes, j = j0 + c;
-        Ws[e][c] = j < a.C ? load_elem(a.W, a.w_bf16, static_cast<size_t>(e) * a.C + j) : 0.0f;
+    if (blockIdx.y == a.qrow_ctas) {
+        // the extra row of CTAs fills the log u table on the cosine grid c_i = -1 + 2 i / N
+        for (int i = blockIdx.x * kThreads + tid; i <= kLuIntervals; i += gridDim.x * kThreads) {
+            const float c = fminf(1.0f, -1.0f + 2.0f * static_cast<float>(i) / kLuIntervals);
+            a.logu_tab[i] = log_inclusion_ref(1.0f - acosf(c) / kPi, a.K, a.L);
+        }
+        return;
     }
-    for (int idx = tid; idx < nq * kD; idx += kThreads)
-        Qs[idx / kD][idx % kD] = load_elem(a.q, a.q_bf16, static_cast<size_t>(r0) * kD + idx);
+    const int wd = blockIdx.x, r0 = blockIdx.y * kQRows;
+    const int nq = min(kQRows, a.BHq - r0);
+    {
+        // all loads first, then the stores: the loop bodies must not wait for each other
+        constexpr int kQPer = kQRows * kD / kThreads, kWPer = kD * 32 / kThreads;
+        float qv[kQPer], wv[kWPer];
+#pragma unroll
+        for (int k = 0; k < kQPer; ++k) {
+            const int idx = tid + k * kThreads;
+            qv[k] = idx < nq * kD ? load_elem(a.q, a.q_bf16, static_cast<size_t>(r0) * kD + idx)
+                                  : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < kWPer; ++k) {
+            const int idx = tid + k * kThreads, e = idx >> 5, j = wd * 32 + (idx & 31);
+            wv[k] = j < a.C ? load_elem(a.W, a.w_bf16, static_cast<size_t>(e) * a.C + j) : 0.0f;
+        }
+#pragma unroll
+        for (int k = 0; k < kQPer; ++k) {
+            const int idx = tid + k * kThreads;
+            Qs[idx / kD][idx % kD] = qv[k];
+        }
+#pragma unroll
+        for (int k = 0; k < kWPer; ++k) {
+            const int idx = tid + k * kThreads;
+            Ws[idx >> 5][idx & 31] = wv[k];
+        }
+    }
     __syncthreads();
-    for (int pr = warp; pr < nq * 2; pr += kWarps) {
-        const int qi = pr >> 1, wd = pr & 1, c = wd * 32 + lane, j = j0 + c;
+    const int row = r0 + warp;
+    const int Hkv = a.Hq / a.G;
+    if (warp < nq && a.C > 0) {
+        const int j = wd * 32 + lane;
         float s = 0.0f;
 #pragma unroll 16
-        for (int e = 0; e < kD; ++e) s = fmaf(Ws[e][c], Qs[qi][e], s);
-        const uint32_t word = __ballot_sync(0xffffffffu, j < a.C && s > 0.0f);
-        const int wi = (j0 >> 5) + wd;
-        if (lane == 0 && wi < a.qwords)
-            a.qbits[static_cast<size_t>(r0 + qi) * a.qwords + wi] = word;
+        for (int e = 0; e < kD; ++e) s = fmaf(Ws[e][lane], Qs[warp][e], s);
+        const bool bit = j < a.C && s > 0.0f;
+        const uint32_t word = __ballot_sync(0xffffffffu, bit);
+        if (lane == 0) a.qbits[static_cast<size_t>(row) * a.qwords + wd] = word;
+        const int b = row / a.Hq, h = row % a.Hq;
+        const size_t bg = static_cast<size_t>(b) * Hkv + h / a.G;
+        if (j < a.cpad)
+            a.qmask[(bg * a.cpad + j) * a.G + (h % a.G)] = bit ? 0u : 0xffffffffu;
     }
     if (blockIdx.x == 0) {
-        const int Hkv = a.Hq / a.G;
-        for (int qi = warp; qi < nq; qi += kWarps) {
-            const int row = r0 + qi, b = row / a.Hq, h = row % a.Hq, g = h / a.G;
+        if (warp < nq) {
+            const int b = row / a.Hq, h = row % a.Hq, g = h / a.G;
             const float* mu = a.centre + (static_cast<size_t>(b) * Hkv + g) * kD;
             float nn = 0.0f, qm = 0.0f;
             for (int e = lane; e < kD; e += 32) {
-                const float x = Qs[qi][e];
+                const float x = Qs[warp][e];
                 nn = fmaf(x, x, nn);
                 qm = fmaf(x, mu[e], qm);
             }
@@ -82,44 +189,11 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// log u(p) = log P[Binomial(L, p^K) >= 2], stable in fp32: directly when L p^K >= 1/2, else as
-// t_2 (1 + sum_{j>=3} t_j / t_2) with t_j the binomial terms. p <= 0 clamps to log(FLT_MIN).
-// ------------------------------------------------------------------------------------------------
-__device__ float log_inclusion(float p, int K, int L) {
-    if (L < 2) return -INFINITY;
-    float x, lx;
-    if (K == 0) {
-        x = 1.0f;
-        lx = 0.0f;
-    } else {
-        if (!(p > 0.0f)) return kLogFltMin;
-        lx = static_cast<float>(K) * logf(p);
-        x = expf(lx);
-    }
-    const float Lf = static_cast<float>(L);
-    if (Lf * x >= 0.5f) {
-        if (x >= 1.0f) return 0.0f;
-        const float l1 = log1pf(-x);
-        const float u = 1.0f - expf(Lf * l1) - Lf * x * expf((Lf - 1.0f) * l1);
-        return logf(fmaxf(u, 1.17549435e-38f));
-    }
-    const float l1 = log1pf(-x);
-    const float r = x / (1.0f - x);
-    float term = 1.0f, tot = 1.0f;
-    for (int j = 2; j < L; ++j) {
-        term *= static_cast<float>(L - j) / static_cast<float>(j + 1) * r;
-        tot += term;
-        if (term < 1e-9f * tot) break;
-    }
-    return logf(0.5f * Lf * (Lf - 1.0f)) + 2.0f * lx + (Lf - 2.0f) * l1 + logf(tot);
-}
-
-// ------------------------------------------------------------------------------------------------
 // Fused collide -> select -> gather -> attend, one CTA per (1024-key block, sequence x KV head)
 // ------------------------------------------------------------------------------------------------
 struct CArgs {
     const uint32_t* codes;
-    const uint32_t* qbits;
+    const uint32_t* qmask;
     const float4* qstat;
     const void* q;
     const float* centre;
@@ -131,7 +205,7 @@ struct CArgs {
     unsigned* counters;
     float* out;
     uint32_t* selmask;
-    int q_bf16, n, nblk, Hq, Hkv, K, L, C, qwords, n_sink, n_local;
+    int q_bf16, n, nblk, Hq, Hkv, K, L, C, cpad, n_sink, n_local;
     float scale;
 };
 
@@ -142,18 +216,18 @@ __host__ __device__ constexpr int stage_rows() {
 
 __host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 
-template <int G, typename KV>
-__host__ __device__ size_t region_bytes(int C) {
-    const size_t a = static_cast<size_t>(C) * G * 4;
-    const size_t b = static_cast<size_t>(kWarps) * G * kCombinePitch * 4;
-    return align16(a > b ? a : b);
+template <typename KV>
+constexpr size_t attend_smem_bytes() {
+    return 2 * align16(stage_rows<KV>() * kD * sizeof(KV)) + kAttendBlocks * kKeysPerBlock * 4 +
+           2 * kD * 4 + kWarps * kCombinePitch * 4 + 32;
 }
 
-template <int G, typename KV>
-size_t collide_smem_bytes(int C) {
-    return region_bytes<G, KV>(C) + 2 * align16(stage_rows<KV>() * kD * sizeof(KV)) +
-           align16(G * kD * 4) + kD * 4 + align16(G * 32 * 4) + kKeysPerBlock * 4 +
-           kKeysPerBlock * 2 + 16;
+template <int G>
+size_t collide_smem_bytes(int cpad, int K) {
+    const size_t ring = (K >= kRingMinK && K <= kRingMaxK)
+                            ? static_cast<size_t>(kWarps) * kRingDepth * K * kWordsPerBlock * 4
+                            : 0;
+    return static_cast<size_t>(cpad) * G * 4 + static_cast<size_t>(kWarps) * 2 * G * 32 * 4 + ring;
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -166,13 +240,22 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
 
-__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
-__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(p);
-    const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-    const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
-    return make_float4(a.x, a.y, b.x, b.y);
+// 8 consecutive elements of a K or V row as floats
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
 }
 
 template <int G>
@@ -196,99 +279,204 @@ __device__ __forceinline__ void load_qneg(const uint32_t* p, uint32_t (&v)[G]) {
     }
 }
 
-template <int G, typename KV>
-__global__ void __launch_bounds__(kThreads) collide_attend_kernel(const CArgs a) {
+// Phase 1 for a compile-time K: tables [t0, t1) of one 32-key word (this lane). The K plane
+// words of table t+1 are loaded while table t is reduced, so two tables' loads are in flight.
+template <int G, int K>
+__device__ __forceinline__ void scan_tables_k(const uint32_t* cb, const uint32_t* qneg, int t0,
+                                              int t1, uint32_t (&ge1)[G], uint32_t (&ge2)[G]) {
+    uint32_t cur[K], nxt[K];
+    if (t0 < t1) {
+#pragma unroll
+        for (int b = 0; b < K; ++b) cur[b] = __ldcs(cb + static_cast<size_t>(t0 * K + b) * kWordsPerBlock);
+    }
+    for (int t = t0; t < t1; ++t) {
+        if (t + 1 < t1) {
+#pragma unroll
+            for (int b = 0; b < K; ++b)
+                nxt[b] = __ldcs(cb + static_cast<size_t>((t + 1) * K + b) * kWordsPerBlock);
+        }
+        uint32_t acc[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h] = 0xffffffffu;
+#pragma unroll
+        for (int b = 0; b < K; ++b) {
+            uint32_t qn[G];
+            load_qneg<G>(qneg + (t * K + b) * G, qn);
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h] &= cur[b] ^ qn[h];
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            ge2[h] |= ge1[h] & acc[h];
+            ge1[h] |= acc[h];
+        }
+#pragma unroll
+        for (int b = 0; b < K; ++b) cur[b] = nxt[b];
+    }
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait_pending() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Phase 1 for a compile-time K with the plane rows streamed through a per-warp shared-memory
+// ring: table t + kRingDepth - 1 is copied (cp.async, 16 B per lane) while table t is reduced,
+// so each warp keeps kRingDepth tables (kRingDepth * K * 128 bytes) in flight without holding
+// them in registers. cb points at the block's first plane row (no lane offset).
+template <int G, int K>
+__device__ __forceinline__ void scan_tables_async(const uint32_t* cb, uint32_t* ring,
+                                                  const uint32_t* qneg, int t0, int t1, int lane,
+                                                  uint32_t (&ge1)[G], uint32_t (&ge2)[G]) {
+    constexpr int kSlot = K * kWordsPerBlock;      // words per table
+    constexpr int kPieces = K * 8;                 // 16-byte pieces per table
+    auto issue = [&](int t, int slot) {
+        const uint32_t* src = cb + static_cast<size_t>(t) * kSlot;
+        uint32_t* dst = ring + slot * kSlot;
+#pragma unroll
+        for (int pc = lane; pc < kPieces; pc += 32) cp_async16(dst + 4 * pc, src + 4 * pc);
+    };
+#pragma unroll
+    for (int d = 0; d < kRingDepth - 1; ++d) {
+        if (t0 + d < t1) issue(t0 + d, d);
+        cp_async_commit();
+    }
+    int slot = 0;
+    for (int t = t0; t < t1; ++t) {
+        const int nt = t + kRingDepth - 1;
+        if (nt < t1) issue(nt, (slot + kRingDepth - 1) % kRingDepth);
+        cp_async_commit();
+        cp_async_wait_pending<kRingDepth - 1>();   // this lane's pieces of table t have landed
+        __syncwarp();                              // ... and every other lane's
+        const uint32_t* planes = ring + slot * kSlot + lane;
+        uint32_t acc[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) acc[h] = 0xffffffffu;
+#pragma unroll
+        for (int b = 0; b < K; ++b) {
+            const uint32_t x = planes[b * kWordsPerBlock];
+            uint32_t qn[G];
+            load_qneg<G>(qneg + (t * K + b) * G, qn);
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h] &= x ^ qn[h];
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            ge2[h] |= ge1[h] & acc[h];
+            ge1[h] |= acc[h];
+        }
+        __syncwarp();                              // the slot is refilled next iteration
+        slot = (slot + 1) % kRingDepth;
+    }
+    cp_async_wait_pending<0>();
+}
+
+// Phase 1 for any K: the planes of [t0, t1) as one stream, 16 loads in flight.
+template <int G>
+__device__ __forceinline__ void scan_tables_any(const uint32_t* cb, const uint32_t* qneg, int K,
+                                                int t0, int t1, uint32_t (&ge1)[G],
+                                                uint32_t (&ge2)[G]) {
+    uint32_t acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = 0xffffffffu;
+    const int jend = t1 * K;
+    int bb = 0;
+    for (int j = t0 * K; j < jend; j += 16) {
+        uint32_t x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            x[i] = (j + i < jend) ? __ldcs(cb + static_cast<size_t>(j + i) * kWordsPerBlock) : 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (j + i < jend) {
+                uint32_t qn[G];
+                load_qneg<G>(qneg + (j + i) * G, qn);
+#pragma unroll
+                for (int h = 0; h < G; ++h) acc[h] &= x[i] ^ qn[h];
+                if (++bb == K) {
+                    bb = 0;
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        ge2[h] |= ge1[h] & acc[h];
+                        ge1[h] |= acc[h];
+                        acc[h] = 0xffffffffu;
+                    }
+                }
+            }
+        }
+    }
+}
+
+struct AArgs {
+    const uint32_t* selmask;
+    const float4* qstat;
+    const void* q;
+    const float* centre;
+    const void* keys;
+    const void* values;
+    float* pm;
+    float* pl;
+    float* po;
+    unsigned* counters;
+    float* out;
+    const float* logu_tab;
+    int q_bf16, n, nblk, nsb, Hq, Hkv, G, K, L, n_sink, n_local;
+    float scale, log_c2;
+};
+
+// Collide + select: per (1024-key block, sequence x KV head) the selection words
+// S_h = [>= 2 of L tables match] & valid & not T, for every query head h of the group.
+template <int G>
+__global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
-    constexpr int CH = stage_rows<KV>();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int blk = blockIdx.x, bg = blockIdx.y;
     const int b = bg / a.Hkv, g = bg % a.Hkv;
     const int row0 = b * a.Hq + g * G;          // first query row of this KV head's group
+    uint32_t* qneg = reinterpret_cast<uint32_t*>(smem);                    // [cpad][G]
+    uint32_t* gebuf = qneg + static_cast<size_t>(a.cpad) * G;              // [8][2][G][32]
+    uint32_t* ring = gebuf + kWarps * 2 * G * 32 +                         // [8][depth][K][32]
+                     static_cast<size_t>(warp) * kRingDepth * a.K * kWordsPerBlock;
 
-    size_t off = 0;
-    uint32_t* region = reinterpret_cast<uint32_t*>(smem + off);
-    off += region_bytes<G, KV>(a.C);
-    KV* stK = reinterpret_cast<KV*>(smem + off);
-    off += align16(CH * kD * sizeof(KV));
-    KV* stV = reinterpret_cast<KV*>(smem + off);
-    off += align16(CH * kD * sizeof(KV));
-    float* qf = reinterpret_cast<float*>(smem + off);
-    off += align16(G * kD * 4);
-    float* muf = reinterpret_cast<float*>(smem + off);
-    off += kD * 4;
-    uint32_t* sel = reinterpret_cast<uint32_t*>(smem + off);
-    off += align16(G * 32 * 4);
-    int* lidx = reinterpret_cast<int*>(smem + off);
-    off += kKeysPerBlock * 4;
-    uint16_t* lhm = reinterpret_cast<uint16_t*>(smem + off);
-    off += kKeysPerBlock * 2;
-    int* misc = reinterpret_cast<int*>(smem + off);
-    uint32_t* qneg = region;                                  // phase 1: [C][G] match masks
-    uint32_t* gebuf = reinterpret_cast<uint32_t*>(stK);       // phase 1 -> 2: warp counters
-    float* cbuf = reinterpret_cast<float*>(region);           // end: [warp][G][132] partials
-
-    // ---- prologue: query bits as XOR masks (0 where the query bit is 1), q and mu as floats
-    for (int j = tid; j < a.C; j += kThreads) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const uint32_t w = a.qbits[static_cast<size_t>(row0 + h) * a.qwords + (j >> 5)];
-            qneg[j * G + h] = ((w >> (j & 31)) & 1u) ? 0u : 0xffffffffu;
-        }
+    // ---- prologue: the group's query masks (one contiguous piece), q and mu as floats
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(a.qmask +
+                                                          static_cast<size_t>(bg) * a.cpad * G);
+        const int n16 = a.cpad * G / 4;
+        for (int i = tid; i < n16; i += kThreads) cp_async16(qneg + 4 * i, src + i);
     }
-    for (int idx = tid; idx < G * kD; idx += kThreads)
-        qf[idx] = load_elem(a.q, a.q_bf16, static_cast<size_t>(row0) * kD + idx);
-    if (tid < kD) muf[tid] = a.centre[static_cast<size_t>(bg) * kD + tid];
+    cp_async_wait_all();
     __syncthreads();
 
     // ---- phase 1: per 32-key word (lane), per table, match = AND_b (plane ^ qmask); keep
     //      bit-sliced saturating counters ge1 = (>= 1 match), ge2 = (>= 2 matches)
     uint32_t ge1[G], ge2[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        ge1[h] = 0u;
+        ge2[h] = 0u;
+    }
     {
         const int t0 = (a.L * warp) / kWarps, t1 = (a.L * (warp + 1)) / kWarps;
-        if (a.K == 0) {
+        const uint32_t* cb0 = a.codes +
+                              (static_cast<size_t>(bg) * a.nblk + blk) * a.C * kWordsPerBlock;
+        const uint32_t* cb = cb0 + lane;
+        switch (a.K) {
+            case 0:
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                ge1[h] = (t1 - t0 >= 1) ? 0xffffffffu : 0u;
-                ge2[h] = (t1 - t0 >= 2) ? 0xffffffffu : 0u;
-            }
-        } else {
-            uint32_t acc[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                acc[h] = 0xffffffffu;
-                ge1[h] = 0u;
-                ge2[h] = 0u;
-            }
-            const uint32_t* cb = a.codes +
-                                 (static_cast<size_t>(bg) * a.nblk + blk) * a.C * kWordsPerBlock +
-                                 lane;
-            const int jend = t1 * a.K;
-            int bb = 0;
-            for (int j = t0 * a.K; j < jend; j += 16) {
-                uint32_t x[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    x[i] = (j + i < jend) ? __ldcs(cb + static_cast<size_t>(j + i) * kWordsPerBlock)
-                                          : 0u;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    if (j + i < jend) {
-                        uint32_t qn[G];
-                        load_qneg<G>(qneg + (j + i) * G, qn);
-#pragma unroll
-                        for (int h = 0; h < G; ++h) acc[h] &= x[i] ^ qn[h];
-                        if (++bb == a.K) {
-                            bb = 0;
-#pragma unroll
-                            for (int h = 0; h < G; ++h) {
-                                ge2[h] |= ge1[h] & acc[h];
-                                ge1[h] |= acc[h];
-                                acc[h] = 0xffffffffu;
-                            }
-                        }
-                    }
+                for (int h = 0; h < G; ++h) {
+                    ge1[h] = (t1 - t0 >= 1) ? 0xffffffffu : 0u;
+                    ge2[h] = (t1 - t0 >= 2) ? 0xffffffffu : 0u;
                 }
-            }
+                break;
+            case 8: scan_tables_async<G, 8>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
+            case 9: scan_tables_async<G, 9>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
+            case 10: scan_tables_async<G, 10>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
+            case 11: scan_tables_async<G, 11>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
+            default: scan_tables_any<G>(cb, qneg, a.K, t0, t1, ge1, ge2); break;
         }
     }
 #pragma unroll
@@ -312,24 +500,53 @@ __global__ void __launch_bounds__(kThreads) collide_attend_kernel(const CArgs a)
         const uint32_t tm =
             (bits_below(a.n_sink - key0) | ~bits_below(a.n - a.n_local - key0)) & valid;
         const uint32_t s = g2 & valid & ~tm;
-        sel[h * 32 + w] = s;
-        if (a.selmask) a.selmask[(static_cast<size_t>(row0 + h) * a.nblk + blk) * 32 + w] = s;
+        a.selmask[(static_cast<size_t>(row0 + h) * a.nblk + blk) * 32 + w] = s;
     }
     __syncthreads();
+}
 
-    // ---- compaction: ascending list of the block's keys in S_h (any h) or in T
-    if (warp == 0) {
-        const int key0 = blk * kKeysPerBlock + lane * 32;
+// Gather + weight + attend for one query head over kAttendBlocks consecutive 1024-key blocks:
+// the ascending list of keys in S_h or in T, their K/V rows, the importance weights and one
+// partial softmax; the last CTA of each query row merges the row's partials by log-sum-exp.
+template <typename KV>
+__global__ void __launch_bounds__(kThreads, 4) attend_kernel(const AArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    constexpr int CH = stage_rows<KV>();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int sb = blockIdx.x, row = blockIdx.y;
+    const int b = row / a.Hq, h = row % a.Hq;
+    const int bg = b * a.Hkv + h / a.G;
+    const int blk0 = sb * kAttendBlocks;
+    const int nb = min(kAttendBlocks, a.nblk - blk0);
+
+    size_t off = 0;
+    KV* stK = reinterpret_cast<KV*>(smem + off);
+    off += align16(CH * kD * sizeof(KV));
+    KV* stV = reinterpret_cast<KV*>(smem + off);
+    off += align16(CH * kD * sizeof(KV));
+    int* lidx = reinterpret_cast<int*>(smem + off);        // bit 31: the key is in T
+    off += kAttendBlocks * kKeysPerBlock * 4;
+    float* qf = reinterpret_cast<float*>(smem + off);
+    off += kD * 4;
+    float* muf = reinterpret_cast<float*>(smem + off);
+    off += kD * 4;
+    float* cbuf = reinterpret_cast<float*>(smem + off);     // [warp][132]: o, m, l
+    off += kWarps * kCombinePitch * 4;
+    int* misc = reinterpret_cast<int*>(smem + off);         // [0..3] block counts, [4] last
+
+    // ---- prologue: q row, mu, and per block the count of keys in S_h or T
+    if (tid < kD) {
+        qf[tid] = load_elem(a.q, a.q_bf16, static_cast<size_t>(row) * kD + tid);
+        muf[tid] = a.centre[static_cast<size_t>(bg) * kD + tid];
+    }
+    uint32_t U = 0u, tm = 0u;
+    int key0 = 0, excl = 0;
+    if (warp < nb) {
+        const int blk = blk0 + warp;
+        key0 = blk * kKeysPerBlock + lane * 32;
         const uint32_t valid = bits_below(a.n - key0);
-        const uint32_t tm =
-            (bits_below(a.n_sink - key0) | ~bits_below(a.n - a.n_local - key0)) & valid;
-        uint32_t s[G];
-        uint32_t U = tm;
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            s[h] = sel[h * 32 + lane];
-            U |= s[h];
-        }
+        tm = (bits_below(a.n_sink - key0) | ~bits_below(a.n - a.n_local - key0)) & valid;
+        U = a.selmask[(static_cast<size_t>(row) * a.nblk + blk) * 32 + lane] | tm;
         const int c = __popc(U);
         int incl = c;
 #pragma unroll
@@ -337,42 +554,39 @@ __global__ void __launch_bounds__(kThreads) collide_attend_kernel(const CArgs a)
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += y;
         }
-        int pos = incl - c;
+        excl = incl - c;
+        if (lane == 31) misc[warp] = incl;
+    }
+    __syncthreads();
+    int nsel = 0, base = 0;
+    for (int w = 0; w < nb; ++w) {
+        if (w < warp) base += misc[w];
+        nsel += misc[w];
+    }
+    if (warp < nb) {
+        int pos = base + excl;
         uint32_t bits = U;
         while (bits) {
             const int bit = __ffs(bits) - 1;
             bits &= bits - 1;
-            int hm;
-            if ((tm >> bit) & 1u) {
-                hm = kTFlag | ((1 << G) - 1);
-            } else {
-                hm = 0;
-#pragma unroll
-                for (int h = 0; h < G; ++h) hm |= static_cast<int>((s[h] >> bit) & 1u) << h;
-            }
-            lidx[pos] = key0 + bit;
-            lhm[pos] = static_cast<uint16_t>(hm);
-            ++pos;
+            lidx[pos++] = (key0 + bit) | static_cast<int>(((tm >> bit) & 1u) << 31);
         }
-        if (lane == 31) misc[0] = incl;
     }
     __syncthreads();
-    const int nsel = misc[0];
 
-    // ---- phase 2: gather the listed K/V rows, weight, online softmax per head
-    float m[G], l[G];
-    float4 o[G];
-    float qn[G], qmu[G];
+    // ---- gather the listed rows; each half-warp takes one row (16 lanes x 8 elements)
+    const int half = lane >> 4, hl = lane & 15;
+    const float4 st = a.qstat[row];
+    const float qn = st.x, qmu = st.y;
+    float q8[8], mu8[8];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.0f;
-        o[h] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        const float4 st = a.qstat[row0 + h];
-        qn[h] = st.x;
-        qmu[h] = st.y;
+    for (int i = 0; i < 8; ++i) {
+        q8[i] = qf[8 * hl + i];
+        mu8[i] = muf[8 * hl + i];
     }
-    const float4 mu4 = reinterpret_cast<const float4*>(muf)[lane];
+    float m = -INFINITY, l = 0.0f, o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = 0.0f;
     const KV* Kb = reinterpret_cast<const KV*>(a.keys) + static_cast<size_t>(bg) * a.n * kD;
     const KV* Vb = reinterpret_cast<const KV*>(a.values) + static_cast<size_t>(bg) * a.n * kD;
     constexpr int P = kD * static_cast<int>(sizeof(KV)) / 16;   // 16-byte pieces per row
@@ -380,138 +594,165 @@ __global__ void __launch_bounds__(kThreads) collide_attend_kernel(const CArgs a)
         const int nrow = min(CH, nsel - c0);
         for (int pc = tid; pc < nrow * 2 * P; pc += kThreads) {
             const int r = pc / (2 * P), rem = pc % (2 * P), arr = rem / P, piece = rem % P;
-            const KV* src = (arr ? Vb : Kb) + static_cast<size_t>(lidx[c0 + r]) * kD;
+            const KV* src = (arr ? Vb : Kb) + static_cast<size_t>(lidx[c0 + r] & 0x7fffffff) * kD;
             KV* dst = (arr ? stV : stK) + r * kD;
             cp_async16(reinterpret_cast<uint8_t*>(dst) + piece * 16,
                        reinterpret_cast<const uint8_t*>(src) + piece * 16);
         }
         cp_async_wait_all();
         __syncthreads();
-        for (int r = warp; r < nrow; r += kWarps) {
-            const float4 kf = load4(stK + r * kD + 4 * lane);
-            const float4 vf = load4(stV + r * kD + 4 * lane);
-            const float dx = kf.x - mu4.x, dy = kf.y - mu4.y, dz = kf.z - mu4.z, dw = kf.w - mu4.w;
-            float kb2 = dx * dx + dy * dy + dz * dz + dw * dw;
-            float dot[G];
+        for (int r0 = 2 * warp; r0 < nrow; r0 += 2 * kWarps) {
+            const int r = r0 + half;
+            const bool live = r < nrow;            // an odd last row leaves one half idle
+            const int rr = live ? r : r0;
+            float kf[8], vf[8];
+            load8(stK + rr * kD + 8 * hl, kf);
+            load8(stV + rr * kD + 8 * hl, vf);
+            float kb2 = 0.0f, dot = 0.0f;
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float4 q4 = reinterpret_cast<const float4*>(qf)[h * 32 + lane];
-                dot[h] = q4.x * kf.x + q4.y * kf.y + q4.z * kf.z + q4.w * kf.w;
+            for (int i = 0; i < 8; ++i) {
+                const float dk = kf[i] - mu8[i];
+                kb2 = fmaf(dk, dk, kb2);
+                dot = fmaf(q8[i], kf[i], dot);
             }
 #pragma unroll
-            for (int sh = 16; sh; sh >>= 1) {
+            for (int sh = 8; sh; sh >>= 1) {
                 kb2 += __shfl_xor_sync(0xffffffffu, kb2, sh);
-#pragma unroll
-                for (int h = 0; h < G; ++h) dot[h] += __shfl_xor_sync(0xffffffffu, dot[h], sh);
+                dot += __shfl_xor_sync(0xffffffffu, dot, sh);
             }
-            const int hm = lhm[c0 + r];
-            const float kbn = sqrtf(kb2);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                if (!((hm >> h) & 1)) continue;
+            if (live) {
+                const bool in_t = lidx[c0 + r] < 0;
                 float lw = 0.0f;
-                if (!(hm & kTFlag)) {
-                    const float den = qn[h] * kbn;
-                    float cs = den > 0.0f ? (dot[h] - qmu[h]) / den : 0.0f;
+                if (!in_t && a.K > 0) {
+                    const float den = qn * sqrtf(kb2);
+                    float cs = den > 0.0f ? __fdividef(dot - qmu, den) : 0.0f;
                     cs = fminf(1.0f, fmaxf(-1.0f, cs));
-                    lw = log_inclusion(1.0f - acosf(cs) / kPi, a.K, a.L);
+                    if (cs > -0.9f && cs < 0.999f) {
+                        // linear interpolation in the per-call table of log u over the cosine
+                        const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
+                        const int i = min(static_cast<int>(tt), kLuIntervals - 1);
+                        const float f0 = __ldg(a.logu_tab + i), f1 = __ldg(a.logu_tab + i + 1);
+                        lw = fmaf(tt - static_cast<float>(i), f1 - f0, f0);
+                    } else {
+                        lw = log_inclusion_fast(1.0f - acosf(cs) * (1.0f / kPi), a.K, a.L,
+                                                a.log_c2);
+                    }
                 }
-                const float logit = dot[h] * a.scale - lw;
-                const float mn = fmaxf(m[h], logit);
-                const float corr = expf(m[h] - mn);
-                const float pw = expf(logit - mn);
-                l[h] = l[h] * corr + pw;
-                o[h].x = o[h].x * corr + pw * vf.x;
-                o[h].y = o[h].y * corr + pw * vf.y;
-                o[h].z = o[h].z * corr + pw * vf.z;
-                o[h].w = o[h].w * corr + pw * vf.w;
-                m[h] = mn;
+                const float logit = dot * a.scale - lw;
+                const float mn = fmaxf(m, logit);
+                const float corr = __expf(m - mn);
+                const float pw = __expf(logit - mn);
+                l = l * corr + pw;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = fmaf(o[i], corr, pw * vf[i]);
+                m = mn;
             }
         }
         __syncthreads();
     }
 
-    // ---- merge the warps' partials into this block's partial (fixed order)
+    // ---- merge the two half-warps, then the warps (fixed order)
+    {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, 16);
+        const float lo = __shfl_xor_sync(0xffffffffu, l, 16);
+        const float mn = fmaxf(m, mo);
+        const float sa = mn == -INFINITY ? 0.0f : __expf(m - mn);
+        const float sb2 = mn == -INFINITY ? 0.0f : __expf(mo - mn);
+        l = l * sa + lo * sb2;
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-        float* dst = cbuf + (warp * G + h) * kCombinePitch;
-        reinterpret_cast<float4*>(dst)[lane] = o[h];
+        for (int i = 0; i < 8; ++i) {
+            const float oo = __shfl_xor_sync(0xffffffffu, o[i], 16);
+            o[i] = o[i] * sa + oo * sb2;
+        }
+        m = mn;
+        float* dst = cbuf + warp * kCombinePitch;
+        if (half == 0) {
+            reinterpret_cast<float4*>(dst)[2 * hl] = make_float4(o[0], o[1], o[2], o[3]);
+            reinterpret_cast<float4*>(dst)[2 * hl + 1] = make_float4(o[4], o[5], o[6], o[7]);
+        }
         if (lane == 0) {
-            dst[128] = m[h];
-            dst[129] = l[h];
+            dst[128] = m;
+            dst[129] = l;
         }
     }
     __syncthreads();
-    for (int x = tid; x < G * kD; x += kThreads) {
-        const int h = x / kD, e = x % kD;
+    const size_t prow = static_cast<size_t>(row) * a.nsb + sb;
+    if (tid < kD) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cbuf[(w * G + h) * kCombinePitch + 128]);
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cbuf[w * kCombinePitch + 128]);
         float Ls = 0.0f, Os = 0.0f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
-                const float* r = cbuf + (w * G + h) * kCombinePitch;
-                const float s = expf(r[128] - M);
+                const float* r = cbuf + w * kCombinePitch;
+                const float s = __expf(r[128] - M);
                 Ls += s * r[129];
-                Os += s * r[e];
+                Os += s * r[tid];
             }
         }
-        const size_t prow = static_cast<size_t>(row0 + h) * a.nblk + blk;
-        a.po[prow * kD + e] = Os;
-        if (e == 0) {
+        a.po[prow * kD + tid] = Os;
+        if (tid == 0) {
             a.pm[prow] = M;
             a.pl[prow] = Ls;
         }
     }
 
-    // ---- the last block of this (sequence, KV head) merges all blocks' partials
+    // ---- the last CTA of this query row merges the row's partials
     __threadfence();
     __syncthreads();
-    if (tid == 0) misc[1] = (atomicAdd(a.counters + bg, 1u) == static_cast<unsigned>(a.nblk - 1));
+    if (tid == 0) misc[4] = (atomicAdd(a.counters + row, 1u) == static_cast<unsigned>(a.nsb - 1));
     __syncthreads();
-    if (!misc[1]) return;
+    if (!misc[4]) return;
     __threadfence();
-    for (int x = tid; x < G * kD; x += kThreads) {
-        const int h = x / kD, e = x % kD;
-        const size_t base = static_cast<size_t>(row0 + h) * a.nblk;
+    if (tid < kD) {
+        const size_t rb = static_cast<size_t>(row) * a.nsb;
         float M = -INFINITY;
-        for (int j = 0; j < a.nblk; ++j) M = fmaxf(M, __ldcg(a.pm + base + j));
-        float res = 0.0f;
+        for (int j = 0; j < a.nsb; ++j) M = fmaxf(M, __ldcg(a.pm + rb + j));
+        float Ls = 0.0f, Os = 0.0f;
         if (M != -INFINITY) {
-            float Ls = 0.0f, Os = 0.0f;
-            for (int j = 0; j < a.nblk; ++j) {
-                const float s = expf(__ldcg(a.pm + base + j) - M);
-                Ls += s * __ldcg(a.pl + base + j);
-                Os += s * __ldcg(a.po + (base + j) * kD + e);
+#pragma unroll 4
+            for (int j = 0; j < a.nsb; ++j) {
+                const float s = expf(__ldcg(a.pm + rb + j) - M);
+                Ls += s * __ldcg(a.pl + rb + j);
+                Os += s * __ldcg(a.po + (rb + j) * kD + tid);
             }
-            res = Os / Ls;
         }
-        a.out[static_cast<size_t>(row0 + h) * kD + e] = res;
+        a.out[static_cast<size_t>(row) * kD + tid] = Ls > 0.0f ? Os / Ls : 0.0f;
+        if (tid == 0) a.counters[row] = 0u;
     }
-    if (tid == 0) a.counters[bg] = 0u;
 }
 
-typedef void (*CollideFn)(const CArgs);
+typedef void (*KernelFn)(const CArgs);
 
-CollideFn pick(int G, bool kv_bf16) {
+KernelFn pick_collide(int G) {
     switch (G) {
-        case 1: return kv_bf16 ? collide_attend_kernel<1, __nv_bfloat16> : collide_attend_kernel<1, float>;
-        case 2: return kv_bf16 ? collide_attend_kernel<2, __nv_bfloat16> : collide_attend_kernel<2, float>;
-        case 4: return kv_bf16 ? collide_attend_kernel<4, __nv_bfloat16> : collide_attend_kernel<4, float>;
-        case 8: return kv_bf16 ? collide_attend_kernel<8, __nv_bfloat16> : collide_attend_kernel<8, float>;
+        case 1: return collide_kernel<1>;
+        case 2: return collide_kernel<2>;
+        case 4: return collide_kernel<4>;
+        case 8: return collide_kernel<8>;
         default: return nullptr;
     }
 }
 
-size_t smem_for(int G, bool kv_bf16, int C) {
+typedef void (*AttendFn)(const AArgs);
+
+AttendFn pick_attend(bool kv_bf16) {
+    return kv_bf16 ? attend_kernel<__nv_bfloat16> : attend_kernel<float>;
+}
+
+size_t collide_smem_for(int G, int cpad, int K) {
     switch (G) {
-        case 1: return kv_bf16 ? collide_smem_bytes<1, __nv_bfloat16>(C) : collide_smem_bytes<1, float>(C);
-        case 2: return kv_bf16 ? collide_smem_bytes<2, __nv_bfloat16>(C) : collide_smem_bytes<2, float>(C);
-        case 4: return kv_bf16 ? collide_smem_bytes<4, __nv_bfloat16>(C) : collide_smem_bytes<4, float>(C);
-        case 8: return kv_bf16 ? collide_smem_bytes<8, __nv_bfloat16>(C) : collide_smem_bytes<8, float>(C);
+        case 1: return collide_smem_bytes<1>(cpad, K);
+        case 2: return collide_smem_bytes<2>(cpad, K);
+        case 4: return collide_smem_bytes<4>(cpad, K);
+        case 8: return collide_smem_bytes<8>(cpad, K);
         default: return 0;
     }
+}
+
+size_t attend_smem_for(bool kv_bf16) {
+    return kv_bf16 ? attend_smem_bytes<__nv_bfloat16>() : attend_smem_bytes<float>();
 }
 
 constexpr size_t kMaxSmem = 232448;   // 227 KB opt-in per CTA
@@ -520,19 +761,24 @@ constexpr size_t kMaxSmem = 232448;   // 227 KB opt-in per CTA
 
 bool decode_supported(const DecodeShape& s, bool kv_bf16) {
     const int G = s.Hq / s.Hkv;
-    if (!pick(G, kv_bf16)) return false;
-    return smem_for(G, kv_bf16, s.C) <= kMaxSmem;
+    if (!pick_collide(G)) return false;
+    return collide_smem_for(G, s.cpad, s.K) <= kMaxSmem && attend_smem_for(kv_bf16) <= kMaxSmem;
 }
 
 cudaError_t prepare_decode() {
     const int Gs[4] = {1, 2, 4, 8};
-    for (int i = 0; i < 4; ++i)
-        for (int bf = 0; bf < 2; ++bf) {
-            cudaError_t e = cudaFuncSetAttribute(pick(Gs[i], bf != 0),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(kMaxSmem));
-            if (e != cudaSuccess) return e;
-        }
+    for (int i = 0; i < 4; ++i) {
+        cudaError_t e = cudaFuncSetAttribute(pick_collide(Gs[i]),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kMaxSmem));
+        if (e != cudaSuccess) return e;
+    }
+    for (int bf = 0; bf < 2; ++bf) {
+        cudaError_t e = cudaFuncSetAttribute(pick_attend(bf != 0),
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kMaxSmem));
+        if (e != cudaSuccess) return e;
+    }
     cudaFuncAttributes fa;
     return cudaFuncGetAttributes(&fa, qencode_kernel);
 }
@@ -545,6 +791,7 @@ cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, cons
     qa.W = W;
     qa.centre = centre;
     qa.qbits = ws.qbits;
+    qa.qmask = ws.qmask;
     qa.qstat = ws.qstat;
     qa.counters = ws.counters;
     qa.q_bf16 = q_bf16;
@@ -553,10 +800,14 @@ cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, cons
     qa.Hq = s.Hq;
     qa.G = s.Hq / s.Hkv;
     qa.C = s.C;
+    qa.cpad = s.cpad;
     qa.qwords = s.qwords;
-    qa.n_counters = s.B * s.Hkv;
-    const int gx = (s.C + kQPlanes - 1) / kQPlanes;
-    const dim3 qgrid(gx > 0 ? gx : 1, (qa.BHq + kQRows - 1) / kQRows);
+    qa.n_counters = s.B * s.Hq;
+    qa.logu_tab = ws.logu_tab;
+    qa.K = s.K;
+    qa.L = s.L;
+    qa.qrow_ctas = (qa.BHq + kQRows - 1) / kQRows;
+    const dim3 qgrid(s.qwords > 0 ? s.qwords : 1, qa.qrow_ctas + 1);
     qencode_kernel<<<qgrid, kThreads, 0, st>>>(qa);
     return cudaGetLastError();
 }
@@ -568,7 +819,7 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     const int G = s.Hq / s.Hkv;
     CArgs ca;
     ca.codes = codes;
-    ca.qbits = ws.qbits;
+    ca.qmask = ws.qmask;
     ca.qstat = ws.qstat;
     ca.q = q;
     ca.centre = centre;
@@ -588,14 +839,44 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     ca.K = s.K;
     ca.L = s.L;
     ca.C = s.C;
-    ca.qwords = s.qwords;
+    ca.cpad = s.cpad;
     ca.n_sink = s.n_sink;
     ca.n_local = s.n_local;
     ca.scale = s.scale;
-    CollideFn fn = pick(G, kv_bf16);
-    const size_t smem = smem_for(G, kv_bf16, s.C);
-    if (!fn || smem > kMaxSmem) return cudaErrorNotSupported;
-    fn<<<dim3(s.nblk, s.B * s.Hkv), kThreads, smem, st>>>(ca);
+    KernelFn scan = pick_collide(G);
+    AttendFn attend = pick_attend(kv_bf16);
+    const size_t smem_scan = collide_smem_for(G, s.cpad, s.K), smem_att = attend_smem_for(kv_bf16);
+    if (!scan || smem_scan > kMaxSmem || smem_att > kMaxSmem) return cudaErrorNotSupported;
+    scan<<<dim3(s.nblk, s.B * s.Hkv), kThreads, smem_scan, st>>>(ca);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    AArgs aa;
+    aa.selmask = ws.selmask;
+    aa.qstat = ws.qstat;
+    aa.q = q;
+    aa.centre = centre;
+    aa.keys = keys;
+    aa.values = values;
+    aa.pm = ws.pm;
+    aa.pl = ws.pl;
+    aa.po = ws.po;
+    aa.counters = ws.counters;
+    aa.out = out;
+    aa.logu_tab = ws.logu_tab;
+    aa.q_bf16 = q_bf16;
+    aa.n = s.n;
+    aa.nblk = s.nblk;
+    aa.nsb = (s.nblk + kAttendBlocks - 1) / kAttendBlocks;
+    aa.Hq = s.Hq;
+    aa.Hkv = s.Hkv;
+    aa.G = G;
+    aa.K = s.K;
+    aa.L = s.L;
+    aa.n_sink = s.n_sink;
+    aa.n_local = s.n_local;
+    aa.scale = s.scale;
+    aa.log_c2 = s.L >= 2 ? logf(0.5f * static_cast<float>(s.L) * static_cast<float>(s.L - 1)) : 0.0f;
+    attend<<<dim3(aa.nsb, s.B * s.Hq), kThreads, smem_att, st>>>(aa);
     return cudaGetLastError();
 }
 

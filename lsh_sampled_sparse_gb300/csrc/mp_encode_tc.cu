@@ -14,9 +14,11 @@
 //   warp 0   TMA producer: 128-key x 128-dim bf16 tiles, 128-byte swizzle, 3-stage ring
 //   warp 1   TMEM allocator and single-thread MMA issuer: M=128, N<=256, K=16 x 8 per tile,
 //            double-buffered fp32 accumulators (2 x 256 TMEM columns)
-//   warps 2-9 epilogue: tcgen05.ld the accumulator, compare with c_j, warp ballot -> one
-//            32-key word per hyperplane, stage a block's words in shared memory, then write
-//            each plane row (128 bytes) of the block with coalesced stores.
+//   warps 2-17 epilogue: tcgen05.ld the accumulator; per key (lane) shift the sign bit of
+//            c_j - acc into a 32-bit word for 32 hyperplanes (funnel shift, no predicates),
+//            transpose the 32x32 bit block across the warp with 5 shuffle stages so that each
+//            lane holds one hyperplane's 32-key word, stage a block's words in shared memory,
+//            then write each plane row (128 bytes) of the block with coalesced stores.
 // Every mbarrier wait is bounded; on expiry the CTA records MP_ERR_TIMEOUT in the device status
 // word, stops issuing work, and still releases its TMEM before returning.
 #include <cuda.h>
@@ -29,7 +31,9 @@ namespace {
 constexpr int kTileM = 128;            // keys per MMA tile (TMEM lanes)
 constexpr int kChunkN = 256;           // hyperplanes per CTA (MMA N, TMEM columns per buffer)
 constexpr int kStages = 3;             // A-tile ring depth
-constexpr int kEpiWarps = 8;
+// 16 epilogue warps + 2 = 18 warps: some SM sub-partition holds 5 of them, and its 16K
+// registers cap the kernel at 96 registers per thread (ptxas picks that from the launch bound).
+constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kStageBytes = kTileM * kD * 2;      // 32 KB: two 64-column swizzled halves
 constexpr uint32_t kHalfBytes = kTileM * 128;          // 16 KB: 128 rows x 128 bytes
@@ -168,6 +172,33 @@ __device__ __forceinline__ void tmem_ld_wait() {
 __device__ __forceinline__ void epi_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
 }
+// Bit c of the result = [acc_c > c_c] for c in 0..31: the sign bit of c_c - acc_c, shifted in
+// by funnel shifts in four independent 8-column chains.
+__device__ __forceinline__ uint32_t pack_signs(const uint32_t (&v)[32], const float* cv) {
+    uint32_t x[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int c = 7; c >= 0; --c) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float d = cv[8 * k + c] - __uint_as_float(v[8 * k + c]);
+            x[k] = __funnelshift_l(__float_as_uint(d), x[k], 1);
+        }
+    }
+    return x[0] | (x[1] << 8) | (x[2] << 16) | (x[3] << 24);
+}
+// 32x32 bit-matrix transpose across a warp: on entry bit b of lane r is element (r, b); on exit
+// bit r of lane b is that element. Each stage swaps the off-diagonal s x s blocks.
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+    const uint32_t low[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        const int s = 16 >> i;
+        const uint32_t m = low[i];   // bit positions b with (b & s) == 0
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
+        x = (lane & s) ? ((x & ~m) | ((y & ~m) >> s)) : ((x & m) | ((y & m) << s));
+    }
+    return x;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     encode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const EncodeArgs a) {
@@ -298,10 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue ----------------
-        const int ew = warp - 2;                 // 0..7
+        const int ew = warp - 2;                 // 0..15
         const int quad = warp & 3;               // TMEM lane quadrant this warp may read
-        const int half = ew >> 2;                // which 128 columns
-        const int et = tid - 64;                 // 0..255
+        const int colq = ew >> 2;                // which 64 columns
+        const int et = tid - 64;                 // 0..511
         bool aborted = false;
         int it = 0;
         int cur_bg = -1;
@@ -335,29 +366,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!aborted) {
                     tc_fence_after();
-#pragma unroll 1
-                    for (int cg = 0; cg < 4; ++cg) {
-                        const int col0 = half * 128 + cg * 32;
-                        if (col0 >= Nc) break;
-                        uint32_t v[32];
-                        tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                      ab * kChunkN + col0,
-                                  v);
-                        tmem_ld_wait();
-                        uint32_t mine = 0;
-#pragma unroll
-                        for (int c4 = 0; c4 < 8; ++c4) {
-                            const float4 cc = *reinterpret_cast<const float4*>(cvec + col0 + 4 * c4);
-                            const float cs[4] = {cc.x, cc.y, cc.z, cc.w};
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const int c = 4 * c4 + q;
-                                const uint32_t bal =
-                                    __ballot_sync(0xffffffffu, __uint_as_float(v[c]) > cs[q]);
-                                if (lane == c) mine = bal;
-                            }
-                        }
-                        if (col0 + lane < Nc) stg[(t * 4 + quad) * kStgPitch + col0 + lane] = mine;
+                    // both 32-column groups of this warp's 64 columns: one TMEM wait, then
+                    // two independent pack + transpose chains
+                    const int colA = colq * 64, colB = colq * 64 + 32;
+                    const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                          ab * kChunkN;
+                    uint32_t va[32], vb[32];
+                    if (colA < Nc) tmem_ld32(trow + colA, va);
+                    if (colB < Nc) tmem_ld32(trow + colB, vb);
+                    tmem_ld_wait();
+                    if (colA < Nc) {
+                        const uint32_t x = warp_transpose32(pack_signs(va, cvec + colA), lane);
+                        if (colA + lane < Nc) stg[(t * 4 + quad) * kStgPitch + colA + lane] = x;
+                    }
+                    if (colB < Nc) {
+                        const uint32_t x = warp_transpose32(pack_signs(vb, cvec + colB), lane);
+                        if (colB + lane < Nc) stg[(t * 4 + quad) * kStgPitch + colB + lane] = x;
                     }
                     tc_fence_before();
                 }

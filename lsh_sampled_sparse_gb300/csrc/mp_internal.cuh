@@ -12,6 +12,8 @@ namespace mp {
 constexpr int kKeysPerBlock = MP_KEYS_PER_BLOCK;   // keys per bit-sliced code block
 constexpr int kWordsPerBlock = kKeysPerBlock / 32;  // uint32 words per plane row
 constexpr int kD = 128;                             // the only head dimension supported
+constexpr int kAttendBlockGroup = 4;                // 1024-key blocks per attend CTA
+constexpr int kLogUTableIntervals = 4096;           // log u table over the cosine in [-1, 1]
 
 // Device status word values (mp_status codes); kernels only ever raise MP_ERR_TIMEOUT.
 int* device_status_ptr();          // address of this device's status word (nullptr on error)
@@ -20,16 +22,19 @@ int device_sm_count();
 // Scratch carved out of the decode workspace (all pointers 256-byte aligned).
 struct DecodeScratch {
     uint32_t* qbits;     // [B*Hq][qwords] query sign bits
+    uint32_t* qmask;     // [B*Hkv][cpad][G] per-plane XOR masks (0 where the query bit is 1)
     float4* qstat;       // [B*Hq] {|q|, q.mu, 0, 0}
-    float* pm;           // [B*Hq][nblk] running max of each block's partial softmax
-    float* pl;           // [B*Hq][nblk] its sum of weights
-    float* po;           // [B*Hq][nblk][128] its weighted value sum
-    unsigned* counters;  // [B*Hkv] blocks finished, for the last block's merge
-    uint32_t* selmask;   // [B*Hq][nblk][32] selection bits (debug only, else nullptr)
+    float* pm;           // [B*Hq][nsb] max logit of each attend CTA's partial softmax
+    float* pl;           // [B*Hq][nsb] its sum of weights
+    float* po;           // [B*Hq][nsb][128] its weighted value sum
+    unsigned* counters;  // [B*Hq] attend CTAs finished, for the last one's merge
+    uint32_t* selmask;   // [B*Hq][nblk][32] selection words, written by the scan kernel
+    float* logu_tab;     // [kLogUTableIntervals + 1] log u at cosines -1 + 2 i / intervals
 };
 
 struct DecodeShape {
     int B, Hq, Hkv, n, d, K, L, C, qwords, nblk, n_sink, n_local;
+    int cpad;            // C rounded up to a multiple of 4 (16-byte rows of query masks)
     float scale;
 };
 

@@ -75,6 +75,7 @@ extern "C" mp_status mp_decode_attention_noalloc(
     s.L = prm->L;
     s.C = prm->K * prm->L;
     s.qwords = (s.C + 31) / 32;
+    s.cpad = (s.C + 3) & ~3;
     s.nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
     s.n_sink = prm->n_sink;
     s.n_local = prm->n_local;

@@ -59,7 +59,7 @@ def test_codes_bytes(L):
 def test_workspace_sizes(L):
     import lsh_sampled_sparse_gb300 as mp
     assert mp.decode_workspace_bytes(1, 32, 8, 98304, 128, 10, 150, 4, 64) > 0
-    assert mp.debug_workspace_bytes(1, 32, 8, 98304, 128, 10, 150, 4, 64) > \
+    assert mp.debug_workspace_bytes(1, 32, 8, 98304, 128, 10, 150, 4, 64) >= \
         mp.decode_workspace_bytes(1, 32, 8, 98304, 128, 10, 150, 4, 64)
     assert mp.decode_workspace_bytes(1, 32, 7, 1000, 128, 10, 150, 4, 64) == 0   # Hq % Hkv
     assert mp.decode_workspace_bytes(1, 4, 1, 1000, 128, 33, 2, 4, 64) == 0      # K > 32
