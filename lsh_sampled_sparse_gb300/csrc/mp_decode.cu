@@ -18,6 +18,8 @@ constexpr float kLogFltMin = -87.336544750553102f;   // log(FLT_MIN)
 constexpr float kPi = 3.14159265358979323846f;
 constexpr int kCombinePitch = 132;                  // floats per (warp, head) partial: o, m, l
 constexpr int kAttendBlocks = kAttendBlockGroup;
+constexpr int kAWarps = kAttendBlockGroup;          // attend CTA: one warp per block of its group
+constexpr int kAThreads = 32 * kAWarps;
 constexpr int kRingDepth = 4;                       // tables in flight per warp in the async scan
 constexpr int kRingMinK = 8, kRingMaxK = 11;        // K range the async scan handles
 constexpr int kLuIntervals = kLogUTableIntervals;   // log u table: cosine grid on [-1, 1]
@@ -214,12 +216,9 @@ __host__ __device__ constexpr int stage_rows() {
     return sizeof(KV) == 2 ? 64 : 32;   // 32 KB of K+V rows either way
 }
 
-__host__ __device__ constexpr size_t align16(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
-
 template <typename KV>
 constexpr size_t attend_smem_bytes() {
-    return 2 * align16(stage_rows<KV>() * kD * sizeof(KV)) + kAttendBlocks * kKeysPerBlock * 4 +
-           2 * kD * 4 + kWarps * kCombinePitch * 4 + 32;
+    return kAttendBlocks * kKeysPerBlock * 4 + kAWarps * kCombinePitch * 4 + 32;
 }
 
 template <int G>
@@ -238,24 +237,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-}
-
-// 8 consecutive elements of a K or V row as floats
-__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 4);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-        v[2 * i] = f.x;
-        v[2 * i + 1] = f.y;
-    }
 }
 
 template <int G>
@@ -505,13 +486,63 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     __syncthreads();
 }
 
+// A K or V row fragment: the 8 elements [8 hl, 8 hl + 8) a lane of a half-warp holds
+template <typename KV>
+struct RowFrag;
+template <>
+struct RowFrag<__nv_bfloat16> {
+    uint4 k, v;
+    __device__ __forceinline__ void load(const __nv_bfloat16* kp, const __nv_bfloat16* vp) {
+        k = __ldg(reinterpret_cast<const uint4*>(kp));
+        v = __ldg(reinterpret_cast<const uint4*>(vp));
+    }
+    __device__ __forceinline__ void unpack(float (&kf)[8], float (&vf)[8]) const {
+        const uint32_t kw[4] = {k.x, k.y, k.z, k.w}, vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw[i]));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[i]));
+            kf[2 * i] = a.x;
+            kf[2 * i + 1] = a.y;
+            vf[2 * i] = b.x;
+            vf[2 * i + 1] = b.y;
+        }
+    }
+};
+template <>
+struct RowFrag<float> {
+    float4 k0, k1, v0, v1;
+    __device__ __forceinline__ void load(const float* kp, const float* vp) {
+        k0 = __ldg(reinterpret_cast<const float4*>(kp));
+        k1 = __ldg(reinterpret_cast<const float4*>(kp) + 1);
+        v0 = __ldg(reinterpret_cast<const float4*>(vp));
+        v1 = __ldg(reinterpret_cast<const float4*>(vp) + 1);
+    }
+    __device__ __forceinline__ void unpack(float (&kf)[8], float (&vf)[8]) const {
+        kf[0] = k0.x; kf[1] = k0.y; kf[2] = k0.z; kf[3] = k0.w;
+        kf[4] = k1.x; kf[5] = k1.y; kf[6] = k1.z; kf[7] = k1.w;
+        vf[0] = v0.x; vf[1] = v0.y; vf[2] = v0.z; vf[3] = v0.w;
+        vf[4] = v1.x; vf[5] = v1.y; vf[6] = v1.z; vf[7] = v1.w;
+    }
+};
+
+__device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned* p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
 // Gather + weight + attend for one query head over kAttendBlocks consecutive 1024-key blocks:
 // the ascending list of keys in S_h or in T, their K/V rows, the importance weights and one
 // partial softmax; the last CTA of each query row merges the row's partials by log-sum-exp.
+// Each half-warp reads its rows straight from global memory (16 lanes x 16 bytes of a bf16 row),
+// with the next row's loads in flight while the current row is reduced.
 template <typename KV>
-__global__ void __launch_bounds__(kThreads, 4) attend_kernel(const AArgs a) {
+__global__ void __launch_bounds__(kAThreads, 8) attend_kernel(const AArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
-    constexpr int CH = stage_rows<KV>();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sb = blockIdx.x, row = blockIdx.y;
     const int b = row / a.Hq, h = row % a.Hq;
@@ -519,26 +550,11 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const AArgs a) {
     const int blk0 = sb * kAttendBlocks;
     const int nb = min(kAttendBlocks, a.nblk - blk0);
 
-    size_t off = 0;
-    KV* stK = reinterpret_cast<KV*>(smem + off);
-    off += align16(CH * kD * sizeof(KV));
-    KV* stV = reinterpret_cast<KV*>(smem + off);
-    off += align16(CH * kD * sizeof(KV));
-    int* lidx = reinterpret_cast<int*>(smem + off);        // bit 31: the key is in T
-    off += kAttendBlocks * kKeysPerBlock * 4;
-    float* qf = reinterpret_cast<float*>(smem + off);
-    off += kD * 4;
-    float* muf = reinterpret_cast<float*>(smem + off);
-    off += kD * 4;
-    float* cbuf = reinterpret_cast<float*>(smem + off);     // [warp][132]: o, m, l
-    off += kWarps * kCombinePitch * 4;
-    int* misc = reinterpret_cast<int*>(smem + off);         // [0..3] block counts, [4] last
+    int* lidx = reinterpret_cast<int*>(smem);               // bit 31: the key is in T
+    float* cbuf = reinterpret_cast<float*>(smem + kAttendBlocks * kKeysPerBlock * 4);
+    int* misc = reinterpret_cast<int*>(cbuf + kAWarps * kCombinePitch);  // [0..3] counts, [4]
 
-    // ---- prologue: q row, mu, and per block the count of keys in S_h or T
-    if (tid < kD) {
-        qf[tid] = load_elem(a.q, a.q_bf16, static_cast<size_t>(row) * kD + tid);
-        muf[tid] = a.centre[static_cast<size_t>(bg) * kD + tid];
-    }
+    // ---- per block the keys in S_h or T, listed in ascending order
     uint32_t U = 0u, tm = 0u;
     int key0 = 0, excl = 0;
     if (warp < nb) {
@@ -557,6 +573,15 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const AArgs a) {
         excl = incl - c;
         if (lane == 31) misc[warp] = incl;
     }
+    const int half = lane >> 4, hl = lane & 15;
+    const float4 st = a.qstat[row];
+    const float qn = st.x, qmu = st.y;
+    float q8[8], mu8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        q8[i] = load_elem(a.q, a.q_bf16, static_cast<size_t>(row) * kD + 8 * hl + i);
+        mu8[i] = a.centre[static_cast<size_t>(bg) * kD + 8 * hl + i];
+    }
     __syncthreads();
     int nsel = 0, base = 0;
     for (int w = 0; w < nb; ++w) {
@@ -574,81 +599,70 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const AArgs a) {
     }
     __syncthreads();
 
-    // ---- gather the listed rows; each half-warp takes one row (16 lanes x 8 elements)
-    const int half = lane >> 4, hl = lane & 15;
-    const float4 st = a.qstat[row];
-    const float qn = st.x, qmu = st.y;
-    float q8[8], mu8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        q8[i] = qf[8 * hl + i];
-        mu8[i] = muf[8 * hl + i];
-    }
+    // ---- rows: half-warp hw takes list entries hw, hw + 16, ... (the warp stays converged)
     float m = -INFINITY, l = 0.0f, o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = 0.0f;
-    const KV* Kb = reinterpret_cast<const KV*>(a.keys) + static_cast<size_t>(bg) * a.n * kD;
-    const KV* Vb = reinterpret_cast<const KV*>(a.values) + static_cast<size_t>(bg) * a.n * kD;
-    constexpr int P = kD * static_cast<int>(sizeof(KV)) / 16;   // 16-byte pieces per row
-    for (int c0 = 0; c0 < nsel; c0 += CH) {
-        const int nrow = min(CH, nsel - c0);
-        for (int pc = tid; pc < nrow * 2 * P; pc += kThreads) {
-            const int r = pc / (2 * P), rem = pc % (2 * P), arr = rem / P, piece = rem % P;
-            const KV* src = (arr ? Vb : Kb) + static_cast<size_t>(lidx[c0 + r] & 0x7fffffff) * kD;
-            KV* dst = (arr ? stV : stK) + r * kD;
-            cp_async16(reinterpret_cast<uint8_t*>(dst) + piece * 16,
-                       reinterpret_cast<const uint8_t*>(src) + piece * 16);
+    const KV* Kb = reinterpret_cast<const KV*>(a.keys) + static_cast<size_t>(bg) * a.n * kD + 8 * hl;
+    const KV* Vb = reinterpret_cast<const KV*>(a.values) + static_cast<size_t>(bg) * a.n * kD + 8 * hl;
+    constexpr int kStride = 2 * kAWarps;
+    RowFrag<KV> cur, nxt;
+    int r = 2 * warp + half;
+    int ent = r < nsel ? lidx[r] : 0;
+    if (r < nsel) {
+        const size_t key = static_cast<size_t>(ent & 0x7fffffff) * kD;
+        cur.load(Kb + key, Vb + key);
+    }
+    for (int r0 = 2 * warp; r0 < nsel; r0 += kStride) {
+        const bool live = r < nsel;
+        const int rn = r + kStride;
+        const int ent_n = rn < nsel ? lidx[rn] : 0;
+        if (rn < nsel) {
+            const size_t key = static_cast<size_t>(ent_n & 0x7fffffff) * kD;
+            nxt.load(Kb + key, Vb + key);
         }
-        cp_async_wait_all();
-        __syncthreads();
-        for (int r0 = 2 * warp; r0 < nrow; r0 += 2 * kWarps) {
-            const int r = r0 + half;
-            const bool live = r < nrow;            // an odd last row leaves one half idle
-            const int rr = live ? r : r0;
-            float kf[8], vf[8];
-            load8(stK + rr * kD + 8 * hl, kf);
-            load8(stV + rr * kD + 8 * hl, vf);
-            float kb2 = 0.0f, dot = 0.0f;
+        float kf[8], vf[8];
+        cur.unpack(kf, vf);
+        float kb2 = 0.0f, dot = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float dk = kf[i] - mu8[i];
-                kb2 = fmaf(dk, dk, kb2);
-                dot = fmaf(q8[i], kf[i], dot);
-            }
+        for (int i = 0; i < 8; ++i) {
+            const float dk = kf[i] - mu8[i];
+            kb2 = fmaf(dk, dk, kb2);
+            dot = fmaf(q8[i], kf[i], dot);
+        }
 #pragma unroll
-            for (int sh = 8; sh; sh >>= 1) {
-                kb2 += __shfl_xor_sync(0xffffffffu, kb2, sh);
-                dot += __shfl_xor_sync(0xffffffffu, dot, sh);
-            }
-            if (live) {
-                const bool in_t = lidx[c0 + r] < 0;
-                float lw = 0.0f;
-                if (!in_t && a.K > 0) {
-                    const float den = qn * sqrtf(kb2);
-                    float cs = den > 0.0f ? __fdividef(dot - qmu, den) : 0.0f;
-                    cs = fminf(1.0f, fmaxf(-1.0f, cs));
-                    if (cs > -0.9f && cs < 0.999f) {
-                        // linear interpolation in the per-call table of log u over the cosine
-                        const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
-                        const int i = min(static_cast<int>(tt), kLuIntervals - 1);
-                        const float f0 = __ldg(a.logu_tab + i), f1 = __ldg(a.logu_tab + i + 1);
-                        lw = fmaf(tt - static_cast<float>(i), f1 - f0, f0);
-                    } else {
-                        lw = log_inclusion_fast(1.0f - acosf(cs) * (1.0f / kPi), a.K, a.L,
-                                                a.log_c2);
-                    }
+        for (int sh = 8; sh; sh >>= 1) {
+            kb2 += __shfl_xor_sync(0xffffffffu, kb2, sh);
+            dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+        }
+        if (live) {
+            float lw = 0.0f;
+            if (ent >= 0 && a.K > 0) {
+                const float den = qn * sqrtf(kb2);
+                float cs = den > 0.0f ? __fdividef(dot - qmu, den) : 0.0f;
+                cs = fminf(1.0f, fmaxf(-1.0f, cs));
+                if (cs > -0.9f && cs < 0.999f) {
+                    // linear interpolation in the per-call table of log u over the cosine
+                    const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
+                    const int i = min(static_cast<int>(tt), kLuIntervals - 1);
+                    const float f0 = __ldg(a.logu_tab + i), f1 = __ldg(a.logu_tab + i + 1);
+                    lw = fmaf(tt - static_cast<float>(i), f1 - f0, f0);
+                } else {
+                    lw = log_inclusion_fast(1.0f - acosf(cs) * (1.0f / kPi), a.K, a.L, a.log_c2);
                 }
-                const float logit = dot * a.scale - lw;
-                const float mn = fmaxf(m, logit);
-                const float corr = __expf(m - mn);
-                const float pw = __expf(logit - mn);
-                l = l * corr + pw;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) o[i] = fmaf(o[i], corr, pw * vf[i]);
-                m = mn;
             }
+            const float logit = dot * a.scale - lw;
+            const float mn = fmaxf(m, logit);
+            const float corr = __expf(m - mn);
+            const float pw = __expf(logit - mn);
+            l = l * corr + pw;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = fmaf(o[i], corr, pw * vf[i]);
+            m = mn;
         }
-        __syncthreads();
+        cur = nxt;
+        ent = ent_n;
+        r = rn;
     }
 
     // ---- merge the two half-warps, then the warps (fixed order)
@@ -680,15 +694,15 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const AArgs a) {
     if (tid < kD) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cbuf[w * kCombinePitch + 128]);
+        for (int w = 0; w < kAWarps; ++w) M = fmaxf(M, cbuf[w * kCombinePitch + 128]);
         float Ls = 0.0f, Os = 0.0f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float* r = cbuf + w * kCombinePitch;
-                const float s = __expf(r[128] - M);
-                Ls += s * r[129];
-                Os += s * r[tid];
+            for (int w = 0; w < kAWarps; ++w) {
+                const float* rr = cbuf + w * kCombinePitch;
+                const float s = __expf(rr[128] - M);
+                Ls += s * rr[129];
+                Os += s * rr[tid];
             }
         }
         a.po[prow * kD + tid] = Os;
@@ -698,13 +712,13 @@ __global__ void __launch_bounds__(kThreads, 4) attend_kernel(const AArgs a) {
         }
     }
 
-    // ---- the last CTA of this query row merges the row's partials
-    __threadfence();
+    // ---- the last CTA of this query row merges the row's partials: the barrier orders every
+    //      thread's partial writes before thread 0's release-acquire increment
     __syncthreads();
-    if (tid == 0) misc[4] = (atomicAdd(a.counters + row, 1u) == static_cast<unsigned>(a.nsb - 1));
+    if (tid == 0)
+        misc[4] = (atomic_add_acq_rel_gpu(a.counters + row, 1u) == static_cast<unsigned>(a.nsb - 1));
     __syncthreads();
     if (!misc[4]) return;
-    __threadfence();
     if (tid < kD) {
         const size_t rb = static_cast<size_t>(row) * a.nsb;
         float M = -INFINITY;
@@ -876,7 +890,7 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     aa.n_local = s.n_local;
     aa.scale = s.scale;
     aa.log_c2 = s.L >= 2 ? logf(0.5f * static_cast<float>(s.L) * static_cast<float>(s.L - 1)) : 0.0f;
-    attend<<<dim3(aa.nsb, s.B * s.Hq), kThreads, smem_att, st>>>(aa);
+    attend<<<dim3(aa.nsb, s.B * s.Hq), kAThreads, smem_att, st>>>(aa);
     return cudaGetLastError();
 }
 

@@ -7,18 +7,24 @@
 //
 // With bf16 keys and a bf16 W every product is exact in fp32, so the MMA computes w_j . k_i
 // with fp32 accumulation; the centre enters as the per-(head, plane) constant c_j = w_j . mu
-// and the sign test is [w_j . k_i > c_j], i.e. [w_j . (k_i - mu) > 0].
+// and the sign test is [w_j . k_i > c_j], i.e. [w_j . (k_i - mu) > 0]. The constant is folded
+// into the contraction as one more K=16 step: its A slice is [1, 1, 1, 0, ...] in every row and
+// its B slice holds c_j split exactly into three bf16 terms (c = hi + mid + lo to 2^-24 of c), so
+// that step sets the accumulator to c_j and the eight K=16 steps over the key dimensions add
+// k_i . (-w_j). The result is c_j - w_j . k_i and its sign bit is the code bit.
 //
 // Structure (one CTA per SM, persistent over a contiguous range of 1024-key blocks, and one
 // 256-hyperplane chunk of W held in shared memory for the CTA's whole life):
 //   warp 0   TMA producer: 128-key x 128-dim bf16 tiles, 128-byte swizzle, 3-stage ring
-//   warp 1   TMEM allocator and single-thread MMA issuer: M=128, N<=256, K=16 x 8 per tile,
-//            double-buffered fp32 accumulators (2 x 256 TMEM columns)
-//   warps 2-17 epilogue: tcgen05.ld the accumulator; per key (lane) shift the sign bit of
-//            c_j - acc into a 32-bit word for 32 hyperplanes (funnel shift, no predicates),
-//            transpose the 32x32 bit block across the warp with 5 shuffle stages so that each
-//            lane holds one hyperplane's 32-key word, stage a block's words in shared memory,
-//            then write each plane row (128 bytes) of the block with coalesced stores.
+//   warp 1   TMEM allocator and single-thread MMA issuer: M=128, N<=256, K=16 x (1 + 8) per
+//            tile, double-buffered fp32 accumulators (2 x 256 TMEM columns)
+//   warps 2-17 epilogue: tcgen05.ld the accumulator; per key (lane) shift its sign bits into
+//            a 32-bit word for 32 hyperplanes (funnel shift, no predicates), transpose the
+//            32x32 bit block across the warp with 5 shuffle stages so that each lane holds one
+//            hyperplane's 32-key word, stage a block's words in shared memory, then write each
+//            plane row (128 bytes) of the block with coalesced stores. When the head changes
+//            they also write the new c_j slice (three head slots, so that a slot is rewritten
+//            only after the MMAs of the head that used it have completed).
 // Every mbarrier wait is bounded; on expiry the CTA records MP_ERR_TIMEOUT in the device status
 // word, stops issuing work, and still releases its TMEM before returning.
 #include <cuda.h>
@@ -43,13 +49,20 @@ constexpr int kStgPitch = kWordsPerBlock * 8 + 1;      // 257: staging row pitch
 
 constexpr uint32_t kOffA = 0;
 constexpr uint32_t kOffB = kOffA + kStages * kStageBytes;
-constexpr uint32_t kOffStg = kOffB + kBBytes;
-constexpr uint32_t kOffCvec = kOffStg + kWordsPerBlock * kStgPitch * 4;
-constexpr uint32_t kOffBars = kOffCvec + kChunkN * 4;
+// Centre region: 256 rows x 128 bytes, 128-byte swizzle, four K=16 slices per row: slices 0-2
+// hold the c_j terms of three heads (B operand, rows = hyperplanes), slice 3 of rows 0-127 the
+// constant [1, 1, 1, 0, ...] (A operand, rows = keys).
+constexpr uint32_t kOffC = kOffB + kBBytes;
+constexpr uint32_t kCBytes = kChunkN * 128;            // 32 KB
+constexpr int kCSlots = 3;
+constexpr int kOnesSlice = 3;
+constexpr uint32_t kOffStg = kOffC + kCBytes;
+constexpr uint32_t kOffBars = kOffStg + kWordsPerBlock * kStgPitch * 4;
 constexpr uint32_t kOffMisc = kOffBars + 128;
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
 static_assert(kStgPitch == 257, "staging pitch");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffC % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s: far beyond any real wait
 
@@ -172,30 +185,33 @@ __device__ __forceinline__ void tmem_ld_wait() {
 __device__ __forceinline__ void epi_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
 }
-// Bit c of the result = [acc_c > c_c] for c in 0..31: the sign bit of c_c - acc_c, shifted in
-// by funnel shifts in four independent 8-column chains.
-__device__ __forceinline__ uint32_t pack_signs(const uint32_t (&v)[32], const float* cv) {
+// Bit c of the result = the sign bit of accumulator column c (c_c - w_c . k, so the bit is
+// [w_c . k > c_c]) for c in 0..31, shifted in by funnel shifts in four independent chains.
+__device__ __forceinline__ uint32_t pack_signs(const uint32_t (&v)[32]) {
     uint32_t x[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int c = 7; c >= 0; --c) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float d = cv[8 * k + c] - __uint_as_float(v[8 * k + c]);
-            x[k] = __funnelshift_l(__float_as_uint(d), x[k], 1);
-        }
+        for (int k = 0; k < 4; ++k) x[k] = __funnelshift_l(v[8 * k + c], x[k], 1);
     }
     return x[0] | (x[1] << 8) | (x[2] << 16) | (x[3] << 24);
 }
 // 32x32 bit-matrix transpose across a warp: on entry bit b of lane r is element (r, b); on exit
 // bit r of lane b is that element. Each stage swaps the off-diagonal s x s blocks.
+// Lanes without bit s of their index keep the positions b with (b & s) == 0 and take the
+// partner's such bits moved up by s; lanes with bit s keep the others and take the partner's
+// moved down by s. A rotation does both moves (the bits it wraps around are masked off), so a
+// stage is one shuffle, one funnel shift and one three-input logic op.
 __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
     const uint32_t low[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
 #pragma unroll
     for (int i = 0; i < 5; ++i) {
         const int s = 16 >> i;
-        const uint32_t m = low[i];   // bit positions b with (b & s) == 0
+        const bool up = (lane & s) != 0;
+        const uint32_t keep = up ? ~low[i] : low[i];
         const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
-        x = (lane & s) ? ((x & ~m) | ((y & ~m) >> s)) : ((x & m) | ((y & m) << s));
+        const uint32_t r = __funnelshift_l(y, y, up ? 32 - s : s);   // rotate left
+        x = (x & keep) | (r & ~keep);
     }
     return x;
 }
@@ -208,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sA = smem + kOffA;
     uint8_t* sB = smem + kOffB;
     uint32_t* stg = reinterpret_cast<uint32_t*>(smem + kOffStg);
-    float* cvec = reinterpret_cast<float*>(smem + kOffCvec);
+    uint8_t* sC = smem + kOffC;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -239,14 +255,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    // W chunk -> shared memory as the B operand: row r = hyperplane j0 + r, K-major, swizzled.
-    for (int idx = tid; idx < kChunkN * kD; idx += kThreads) {
-        const int r = idx % kChunkN, e = idx / kChunkN;
-        __nv_bfloat16 w = __float2bfloat16(0.0f);
-        if (r < Nc) w = a.W[static_cast<size_t>(e) * a.C + j0 + r];
-        const uint32_t off = (e >> 6) * kBHalfBytes + r * 128 + ((((e & 63) >> 3) ^ (r & 7)) << 4) +
-                             ((e & 7) << 1);
-        *reinterpret_cast<__nv_bfloat16*>(sB + off) = w;
+    // -W chunk -> shared memory as the B operand: row r = hyperplane j0 + r, K-major, swizzled
+    // (negating a bf16 is exact). Batches of 16 loads per thread are in flight at once.
+    {
+        constexpr int kElems = kChunkN * kD, kBatch = 16;
+        for (int base = 0; base < kElems; base += kThreads * kBatch) {
+            __nv_bfloat16 w[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int idx = base + k * kThreads + tid;
+                const int r = idx % kChunkN, e = idx / kChunkN;
+                w[k] = __float2bfloat16(0.0f);
+                if (idx < kElems && r < Nc) w[k] = __hneg(a.W[static_cast<size_t>(e) * a.C + j0 + r]);
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int idx = base + k * kThreads + tid;
+                const int r = idx % kChunkN, e = idx / kChunkN;
+                const uint32_t off = (e >> 6) * kBHalfBytes + r * 128 +
+                                     ((((e & 63) >> 3) ^ (r & 7)) << 4) + ((e & 7) << 1);
+                if (idx < kElems) *reinterpret_cast<__nv_bfloat16*>(sB + off) = w[k];
+            }
+        }
+    }
+    // centre region: zero, then [1, 1, 1, 0, 0, 0, 0, 0] in the first 16 bytes of slice 3, rows
+    // 0-127 (the rest of the slice stays 0)
+    for (int i = tid; i < static_cast<int>(kCBytes / 16); i += kThreads)
+        reinterpret_cast<uint4*>(sC)[i] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+    if (tid < kTileM) {
+        const uint32_t one2 = 0x3F803F80u;   // two bf16 1.0
+        *reinterpret_cast<uint4*>(sC + tid * 128 + (((2 * kOnesSlice) ^ (tid & 7)) << 4)) =
+            make_uint4(one2, 0x00003F80u, 0u, 0u);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -297,30 +337,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idesc = make_idesc(kTileM, Nmma);
-            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+            const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB), c_base = smem_u32(sC);
             int it = 0;
             bool ok = true;
             for (int u = u_begin; u < u_end && ok; ++u) {
                 const int blk = u % a.nblk;
+                const uint32_t c_slice = static_cast<uint32_t>((u / a.nblk) % kCSlots) * 32;
                 const int rows = min(kKeysPerBlock, a.n - blk * kKeysPerBlock);
                 const int ntile = (rows + kTileM - 1) / kTileM;
                 for (int t = 0; t < ntile; ++t, ++it) {
                     const int s = it % kStages;
                     const int ab = it & 1;
                     if (!mbar_wait(bar_full + 8 * s, (it / kStages) & 1, abort_flag, a.status) ||
-                        !mbar_wait(bar_tempty + 8 * ab, ((it >> 1) & 1) ^ 1, abort_flag,
-                                   a.status)) {
+                        !mbar_wait(bar_tempty + 8 * ab, (it >> 1) & 1, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + ab * kChunkN;
+                    // D = 1 . c (three bf16 terms), then D += k . (-w) over the 128 dimensions
+                    tc_mma(d_tmem, sw128_desc(c_base + kOnesSlice * 32), sw128_desc(c_base + c_slice),
+                           idesc, 0u);
 #pragma unroll
                     for (int k = 0; k < kD / 16; ++k) {
                         const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
                         const uint32_t kboff = (k >> 2) * kBHalfBytes + (k & 3) * 32;
                         tc_mma(d_tmem, sw128_desc(a_base + s * kStageBytes + koff),
-                               sw128_desc(b_base + kboff), idesc, k > 0 ? 1u : 0u);
+                               sw128_desc(b_base + kboff), idesc, 1u);
                     }
                     tc_commit(bar_empty + 8 * s);
                     tc_commit(bar_tfull + 8 * ab);
@@ -331,32 +374,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- epilogue ----------------
         const int ew = warp - 2;                 // 0..15
         const int quad = warp & 3;               // TMEM lane quadrant this warp may read
-        const int colq = ew >> 2;                // which 64 columns
+        const int colA = (ew >> 2) * 64;         // this warp's two 32-column groups start here
         const int et = tid - 64;                 // 0..511
+        const uint32_t tquad = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
         bool aborted = false;
-        int it = 0;
-        int cur_bg = -1;
-        for (int u = u_begin; u < u_end; ++u) {
-            const int bg = u / a.nblk, blk = u % a.nblk;
-            const int rows = min(kKeysPerBlock, a.n - blk * kKeysPerBlock);
-            const int ntile = (rows + kTileM - 1) / kTileM;
-            if (bg != cur_bg) {
-                // c_j = w_j . mu for this head, from the bf16 W chunk already in shared memory
-                epi_sync();
+        // c_j = w_j . mu of head h, as three bf16 terms, into centre slot h % 3 (thread et
+        // writes hyperplane row et). The MMAs that read the slot last (head h - 3) are complete:
+        // this runs for the tile two ahead of the one being drained, and heads never decrease.
+        int c_head = -1;
+        auto ensure_c = [&](int h) {
+            if (h == c_head) return;
+            c_head = h;
+            if (et < kChunkN) {
+                float c = 0.0f;
                 if (et < Nc) {
-                    const float* mu = a.centre + static_cast<size_t>(bg) * kD;
-                    float c = 0.0f;
+                    const float* mu = a.centre + static_cast<size_t>(h) * kD;
                     for (int e = 0; e < kD; ++e) {
                         const uint32_t off = (e >> 6) * kBHalfBytes + et * 128 +
                                              ((((e & 63) >> 3) ^ (et & 7)) << 4) + ((e & 7) << 1);
-                        c = fmaf(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sB + off)),
+                        c = fmaf(-__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sB + off)),
                                  __ldg(mu + e), c);
                     }
-                    cvec[et] = c;
                 }
-                epi_sync();
-                cur_bg = bg;
+                c += 0.0f;                       // never -0: the sign bit must mean c - w.k < 0
+                const __nv_bfloat16 hi = __float2bfloat16_rn(c);
+                const float r1 = c - __bfloat162float(hi);
+                const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+                const uint32_t w01 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
+                                     (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
+                const uint32_t w2 = __bfloat16_as_ushort(lo);
+                const int slot = h % kCSlots;
+                *reinterpret_cast<uint4*>(sC + et * 128 + (((2 * slot) ^ (et & 7)) << 4)) =
+                    make_uint4(w01, w2, 0u, 0u);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
+        };
+        auto tiles_of = [&](int u) {
+            const int rows = min(kKeysPerBlock, a.n - (u % a.nblk) * kKeysPerBlock);
+            return (rows + kTileM - 1) / kTileM;
+        };
+        // the next tile whose centre slot has to be ready: two ahead of the one drained
+        int fu = u_begin, ft = 0;
+        auto fill_next = [&](int ab) {
+            if (fu >= u_end) return;
+            ensure_c(fu / a.nblk);
+            if (++ft == tiles_of(fu)) {
+                ft = 0;
+                ++fu;
+            }
+        };
+        for (int ab = 0; ab < 2; ++ab) {
+            fill_next(ab);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty + 8 * ab);
+        }
+        int it = 0;
+        for (int u = u_begin; u < u_end; ++u) {
+            const int bg = u / a.nblk, blk = u % a.nblk;
+            const int ntile = tiles_of(u);
             for (int t = 0; t < ntile; ++t, ++it) {
                 const int ab = it & 1;
                 if (!aborted) {
@@ -366,25 +443,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!aborted) {
                     tc_fence_after();
-                    // both 32-column groups of this warp's 64 columns: one TMEM wait, then
-                    // two independent pack + transpose chains
-                    const int colA = colq * 64, colB = colq * 64 + 32;
-                    const uint32_t trow = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                          ab * kChunkN;
-                    uint32_t va[32], vb[32];
-                    if (colA < Nc) tmem_ld32(trow + colA, va);
-                    if (colB < Nc) tmem_ld32(trow + colB, vb);
-                    tmem_ld_wait();
-                    if (colA < Nc) {
-                        const uint32_t x = warp_transpose32(pack_signs(va, cvec + colA), lane);
-                        if (colA + lane < Nc) stg[(t * 4 + quad) * kStgPitch + colA + lane] = x;
+                    // this warp's two 32-column groups: load and pack each (one TMEM wait per
+                    // group keeps 32 accumulator registers live), then the two transposes
+                    const uint32_t trow = tquad + ab * kChunkN;
+                    uint32_t x[2] = {0u, 0u};
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        if (colA + 32 * g < Nc) {
+                            uint32_t v[32];
+                            tmem_ld32(trow + colA + 32 * g, v);
+                            tmem_ld_wait();
+                            x[g] = pack_signs(v);
+                        }
                     }
-                    if (colB < Nc) {
-                        const uint32_t x = warp_transpose32(pack_signs(vb, cvec + colB), lane);
-                        if (colB + lane < Nc) stg[(t * 4 + quad) * kStgPitch + colB + lane] = x;
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        const int col = colA + 32 * g;
+                        if (col < Nc) {
+                            const uint32_t y = warp_transpose32(x[g], lane);
+                            if (col + lane < Nc) stg[(t * 4 + quad) * kStgPitch + col + lane] = y;
+                        }
                     }
-                    tc_fence_before();
                 }
+                fill_next(ab);                   // the tile two ahead is released by this arrival
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0 && !aborted) mbar_arrive(bar_tempty + 8 * ab);
             }
