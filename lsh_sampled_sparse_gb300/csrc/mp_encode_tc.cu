@@ -410,66 +410,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
         };
-        auto tiles_of = [&](int u) {
-            const int rows = min(kKeysPerBlock, a.n - (u % a.nblk) * kKeysPerBlock);
+        auto tiles_in_block = [&](int blk) {
+            const int rows = min(kKeysPerBlock, a.n - blk * kKeysPerBlock);
             return (rows + kTileM - 1) / kTileM;
         };
-        // the next tile whose centre slot has to be ready: two ahead of the one drained
-        int fu = u_begin, ft = 0;
-        auto fill_next = [&](int ab) {
+        // The next tile whose centre slot has to be ready (two ahead of the one being drained),
+        // tracked incrementally: unit fu = (fbg, fblk), tile ft of fnt.
+        int fu = u_begin, ft = 0, fbg = u_begin / a.nblk, fblk = u_begin % a.nblk;
+        int fnt = tiles_in_block(fblk);
+        auto fill_next = [&]() {
             if (fu >= u_end) return;
-            ensure_c(fu / a.nblk);
-            if (++ft == tiles_of(fu)) {
+            ensure_c(fbg);
+            if (++ft == fnt) {
                 ft = 0;
                 ++fu;
+                if (++fblk == a.nblk) {
+                    fblk = 0;
+                    ++fbg;
+                }
+                fnt = tiles_in_block(fblk);
             }
         };
-        for (int ab = 0; ab < 2; ++ab) {
-            fill_next(ab);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty + 8 * ab);
-        }
-        int it = 0;
-        for (int u = u_begin; u < u_end; ++u) {
-            const int bg = u / a.nblk, blk = u % a.nblk;
-            const int ntile = tiles_of(u);
-            for (int t = 0; t < ntile; ++t, ++it) {
-                const int ab = it & 1;
-                if (!aborted) {
-                    const bool got = mbar_wait(bar_tfull + 8 * ab, (it >> 1) & 1, abort_flag,
-                                               a.status);
-                    aborted = !__all_sync(0xffffffffu, got);   // keep the warp uniform
-                }
-                if (!aborted) {
-                    tc_fence_after();
-                    // this warp's two 32-column groups: load and pack each (one TMEM wait per
-                    // group keeps 32 accumulator registers live), then the two transposes
-                    const uint32_t trow = tquad + ab * kChunkN;
-                    uint32_t x[2] = {0u, 0u};
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        if (colA + 32 * g < Nc) {
-                            uint32_t v[32];
-                            tmem_ld32(trow + colA + 32 * g, v);
-                            tmem_ld_wait();
-                            x[g] = pack_signs(v);
-                        }
-                    }
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        const int col = colA + 32 * g;
-                        if (col < Nc) {
-                            const uint32_t y = warp_transpose32(x[g], lane);
-                            if (col + lane < Nc) stg[(t * 4 + quad) * kStgPitch + col + lane] = y;
-                        }
-                    }
-                }
-                fill_next(ab);                   // the tile two ahead is released by this arrival
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0 && !aborted) mbar_arrive(bar_tempty + 8 * ab);
-            }
+        // one unit's staged words -> its Nc plane rows in global memory (coalesced rows)
+        auto store_unit = [&](int bg, int blk) {
             epi_sync();
             if (!aborted) {
                 uint32_t* dst = a.codes + (static_cast<size_t>(bg) * a.nblk + blk) *
@@ -479,7 +442,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst[r * kWordsPerBlock + lane] = stg[lane * kStgPitch + r];
             }
             epi_sync();
+        };
+        for (int ab = 0; ab < 2; ++ab) {
+            fill_next();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty + 8 * ab);
         }
+        int it = 0;
+        int prev_bg = -1, prev_blk = 0;          // the unit whose words are still staged
+        int bg = u_begin / a.nblk, blk = u_begin % a.nblk;
+        for (int u = u_begin; u < u_end; ++u) {
+            const int ntile = tiles_in_block(blk);
+            for (int t = 0; t < ntile; ++t, ++it) {
+                const int ab = it & 1;
+                if (!aborted) {
+                    const bool got = mbar_wait(bar_tfull + 8 * ab, (it >> 1) & 1, abort_flag,
+                                               a.status);
+                    aborted = !__all_sync(0xffffffffu, got);   // keep the warp uniform
+                }
+                // sign bits of this warp's two 32-column groups into registers (one TMEM wait
+                // per group keeps 32 accumulator registers live) ...
+                uint32_t x[2] = {0u, 0u};
+                if (!aborted) {
+                    tc_fence_after();
+                    const uint32_t trow = tquad + ab * kChunkN;
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        if (colA + 32 * g < Nc) {
+                            uint32_t v[32];
+                            tmem_ld32(trow + colA + 32 * g, v);
+                            tmem_ld_wait();
+                            x[g] = pack_signs(v);
+                        }
+                    }
+                }
+                // ... which frees the accumulator buffer for the tile two ahead at once
+                fill_next();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0 && !aborted) mbar_arrive(bar_tempty + 8 * ab);
+                // the previous unit's rows go out only now, after this unit's first buffer
+                // was released, so that the MMA keeps running meanwhile
+                if (t == 0 && prev_bg >= 0) store_unit(prev_bg, prev_blk);
+                if (!aborted) {
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        const int col = colA + 32 * g;
+                        if (col < Nc) {
+                            const uint32_t y = warp_transpose32(x[g], lane);
+                            if (col + lane < Nc) stg[(t * 4 + quad) * kStgPitch + col + lane] = y;
+                        }
+                    }
+                }
+            }
+            prev_bg = bg;
+            prev_blk = blk;
+            if (++blk == a.nblk) {
+                blk = 0;
+                ++bg;
+            }
+        }
+        if (prev_bg >= 0) store_unit(prev_bg, prev_blk);
     }
     tc_fence_before();
     __syncthreads();
