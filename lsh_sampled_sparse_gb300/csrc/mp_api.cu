@@ -93,9 +93,9 @@ size_t decode_scratch_bytes(const DecodeShape& s, bool debug) {
     b += align256(rows * s.qwords * 4);                  // qbits
     b += align256(rows * s.cpad * 4);                    // qmask
     b += align256(rows * 16);                            // qstat
-    const size_t nsb = (s.nblk + kAttendBlockGroup - 1) / kAttendBlockGroup;
-    b += align256(rows * nsb * 4) * 2;                   // pm, pl
-    b += align256(rows * nsb * kD * 4);                  // po
+    const size_t nsp = attend_partials(s.nblk);
+    b += align256(rows * nsp * 4) * 2;                   // pm, pl
+    b += align256(rows * nsp * kD * 4);                  // po
     b += align256(rows * 4);                             // counters
     b += align256(rows * s.nblk * 32 * 4);               // selection words
     b += align256((kLogUTableIntervals + 1) * 4);        // log u table
@@ -113,13 +113,13 @@ DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug) {
     p += align256(rows * s.cpad * 4);
     d.qstat = reinterpret_cast<float4*>(p);
     p += align256(rows * 16);
-    const size_t nsb = (s.nblk + kAttendBlockGroup - 1) / kAttendBlockGroup;
+    const size_t nsp = attend_partials(s.nblk);
     d.pm = reinterpret_cast<float*>(p);
-    p += align256(rows * nsb * 4);
+    p += align256(rows * nsp * 4);
     d.pl = reinterpret_cast<float*>(p);
-    p += align256(rows * nsb * 4);
+    p += align256(rows * nsp * 4);
     d.po = reinterpret_cast<float*>(p);
-    p += align256(rows * nsb * kD * 4);
+    p += align256(rows * nsp * kD * 4);
     d.counters = reinterpret_cast<unsigned*>(p);
     p += align256(rows * 4);
     d.selmask = reinterpret_cast<uint32_t*>(p);

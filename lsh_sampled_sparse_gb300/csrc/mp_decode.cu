@@ -535,44 +535,27 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned* p, unsigned
     return old;
 }
 
-// Gather + weight + attend for one query head over kAttendBlocks consecutive 1024-key blocks:
-// the ascending list of keys in S_h or in T, their K/V rows, the importance weights and one
-// partial softmax; the last CTA of each query row merges the row's partials by log-sum-exp.
+// Gather + weight + attend for one query head. CTA sb < nsb takes the sampled keys S_h of
+// kAttendBlocks consecutive 1024-key blocks (ascending, from the selection words); CTA nsb takes
+// the exact set T = [0, n_sink) u [n - n_local, n) with log u = 0, so that the 68 sink/local rows
+// do not pile onto the CTA of the last blocks. Each CTA folds its rows into one partial softmax;
+// the last CTA of each query row merges the row's nsb + 1 partials by log-sum-exp.
 // Each half-warp reads its rows straight from global memory (16 lanes x 16 bytes of a bf16 row),
-// with the next row's loads in flight while the current row is reduced.
+// with the rows two and one ahead in flight while the current row is reduced.
 template <typename KV>
-__global__ void __launch_bounds__(kAThreads, 8) attend_kernel(const AArgs a) {
+__global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int sb = blockIdx.x, row = blockIdx.y;
     const int b = row / a.Hq, h = row % a.Hq;
     const int bg = b * a.Hkv + h / a.G;
-    const int blk0 = sb * kAttendBlocks;
-    const int nb = min(kAttendBlocks, a.nblk - blk0);
+    const bool exact = sb == a.nsb;              // this CTA takes T
+    const int nsp = a.nsb + 1;                   // partials per query row
 
-    int* lidx = reinterpret_cast<int*>(smem);               // bit 31: the key is in T
+    int* lidx = reinterpret_cast<int*>(smem);
     float* cbuf = reinterpret_cast<float*>(smem + kAttendBlocks * kKeysPerBlock * 4);
     int* misc = reinterpret_cast<int*>(cbuf + kAWarps * kCombinePitch);  // [0..3] counts, [4]
 
-    // ---- per block the keys in S_h or T, listed in ascending order
-    uint32_t U = 0u, tm = 0u;
-    int key0 = 0, excl = 0;
-    if (warp < nb) {
-        const int blk = blk0 + warp;
-        key0 = blk * kKeysPerBlock + lane * 32;
-        const uint32_t valid = bits_below(a.n - key0);
-        tm = (bits_below(a.n_sink - key0) | ~bits_below(a.n - a.n_local - key0)) & valid;
-        U = a.selmask[(static_cast<size_t>(row) * a.nblk + blk) * 32 + lane] | tm;
-        const int c = __popc(U);
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        excl = incl - c;
-        if (lane == 31) misc[warp] = incl;
-    }
     const int half = lane >> 4, hl = lane & 15;
     const float4 st = a.qstat[row];
     const float qn = st.x, qmu = st.y;
@@ -582,47 +565,77 @@ __global__ void __launch_bounds__(kAThreads, 8) attend_kernel(const AArgs a) {
         q8[i] = load_elem(a.q, a.q_bf16, static_cast<size_t>(row) * kD + 8 * hl + i);
         mu8[i] = a.centre[static_cast<size_t>(bg) * kD + 8 * hl + i];
     }
-    __syncthreads();
-    int nsel = 0, base = 0;
-    for (int w = 0; w < nb; ++w) {
-        if (w < warp) base += misc[w];
-        nsel += misc[w];
-    }
-    if (warp < nb) {
-        int pos = base + excl;
-        uint32_t bits = U;
-        while (bits) {
-            const int bit = __ffs(bits) - 1;
-            bits &= bits - 1;
-            lidx[pos++] = (key0 + bit) | static_cast<int>(((tm >> bit) & 1u) << 31);
-        }
-    }
-    __syncthreads();
 
-    // ---- rows: half-warp hw takes list entries hw, hw + 16, ... (the warp stays converged)
+    // ---- the rows of this CTA: T by arithmetic, or the selected keys of its blocks by a list
+    const int t_a = min(a.n_sink, a.n), t_b = max(a.n - a.n_local, t_a);
+    int nsel;
+    if (exact) {
+        nsel = t_a + (a.n - t_b);
+    } else {
+        const int blk0 = sb * kAttendBlocks;
+        const int nb = min(kAttendBlocks, a.nblk - blk0);
+        uint32_t U = 0u;
+        int key0 = 0, excl = 0;
+        if (warp < nb) {
+            const int blk = blk0 + warp;
+            key0 = blk * kKeysPerBlock + lane * 32;
+            U = a.selmask[(static_cast<size_t>(row) * a.nblk + blk) * 32 + lane];
+            const int c = __popc(U);
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            excl = incl - c;
+            if (lane == 31) misc[warp] = incl;
+        }
+        __syncthreads();
+        int base = 0;
+        nsel = 0;
+        for (int w = 0; w < nb; ++w) {
+            if (w < warp) base += misc[w];
+            nsel += misc[w];
+        }
+        if (warp < nb) {
+            int pos = base + excl;
+            uint32_t bits = U;
+            while (bits) {
+                const int bit = __ffs(bits) - 1;
+                bits &= bits - 1;
+                lidx[pos++] = key0 + bit;
+            }
+        }
+        __syncthreads();
+    }
+    auto key_of = [&](int r) { return exact ? (r < t_a ? r : t_b + (r - t_a)) : lidx[r]; };
+
+    // ---- rows: half-warp hw takes entries hw, hw + 8, ... (the warp stays converged)
     float m = -INFINITY, l = 0.0f, o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = 0.0f;
     const KV* Kb = reinterpret_cast<const KV*>(a.keys) + static_cast<size_t>(bg) * a.n * kD + 8 * hl;
     const KV* Vb = reinterpret_cast<const KV*>(a.values) + static_cast<size_t>(bg) * a.n * kD + 8 * hl;
     constexpr int kStride = 2 * kAWarps;
-    RowFrag<KV> cur, nxt;
+    const bool weighted = !exact && a.K > 0;
+    RowFrag<KV> f0, f1, f2;
     int r = 2 * warp + half;
-    int ent = r < nsel ? lidx[r] : 0;
     if (r < nsel) {
-        const size_t key = static_cast<size_t>(ent & 0x7fffffff) * kD;
-        cur.load(Kb + key, Vb + key);
+        const size_t key = static_cast<size_t>(key_of(r)) * kD;
+        f0.load(Kb + key, Vb + key);
+    }
+    if (r + kStride < nsel) {
+        const size_t key = static_cast<size_t>(key_of(r + kStride)) * kD;
+        f1.load(Kb + key, Vb + key);
     }
     for (int r0 = 2 * warp; r0 < nsel; r0 += kStride) {
         const bool live = r < nsel;
-        const int rn = r + kStride;
-        const int ent_n = rn < nsel ? lidx[rn] : 0;
-        if (rn < nsel) {
-            const size_t key = static_cast<size_t>(ent_n & 0x7fffffff) * kD;
-            nxt.load(Kb + key, Vb + key);
+        if (r + 2 * kStride < nsel) {
+            const size_t key = static_cast<size_t>(key_of(r + 2 * kStride)) * kD;
+            f2.load(Kb + key, Vb + key);
         }
         float kf[8], vf[8];
-        cur.unpack(kf, vf);
+        f0.unpack(kf, vf);
         float kb2 = 0.0f, dot = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -637,7 +650,7 @@ __global__ void __launch_bounds__(kAThreads, 8) attend_kernel(const AArgs a) {
         }
         if (live) {
             float lw = 0.0f;
-            if (ent >= 0 && a.K > 0) {
+            if (weighted) {
                 const float den = qn * sqrtf(kb2);
                 float cs = den > 0.0f ? __fdividef(dot - qmu, den) : 0.0f;
                 cs = fminf(1.0f, fmaxf(-1.0f, cs));
@@ -645,8 +658,8 @@ __global__ void __launch_bounds__(kAThreads, 8) attend_kernel(const AArgs a) {
                     // linear interpolation in the per-call table of log u over the cosine
                     const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
                     const int i = min(static_cast<int>(tt), kLuIntervals - 1);
-                    const float f0 = __ldg(a.logu_tab + i), f1 = __ldg(a.logu_tab + i + 1);
-                    lw = fmaf(tt - static_cast<float>(i), f1 - f0, f0);
+                    const float g0 = __ldg(a.logu_tab + i), g1 = __ldg(a.logu_tab + i + 1);
+                    lw = fmaf(tt - static_cast<float>(i), g1 - g0, g0);
                 } else {
                     lw = log_inclusion_fast(1.0f - acosf(cs) * (1.0f / kPi), a.K, a.L, a.log_c2);
                 }
@@ -660,9 +673,9 @@ __global__ void __launch_bounds__(kAThreads, 8) attend_kernel(const AArgs a) {
             for (int i = 0; i < 8; ++i) o[i] = fmaf(o[i], corr, pw * vf[i]);
             m = mn;
         }
-        cur = nxt;
-        ent = ent_n;
-        r = rn;
+        f0 = f1;
+        f1 = f2;
+        r += kStride;
     }
 
     // ---- merge the two half-warps, then the warps (fixed order)
@@ -690,7 +703,7 @@ __global__ void __launch_bounds__(kAThreads, 8) attend_kernel(const AArgs a) {
         }
     }
     __syncthreads();
-    const size_t prow = static_cast<size_t>(row) * a.nsb + sb;
+    const size_t prow = static_cast<size_t>(row) * nsp + sb;
     if (tid < kD) {
         float M = -INFINITY;
 #pragma unroll
@@ -716,17 +729,17 @@ __global__ void __launch_bounds__(kAThreads, 8) attend_kernel(const AArgs a) {
     //      thread's partial writes before thread 0's release-acquire increment
     __syncthreads();
     if (tid == 0)
-        misc[4] = (atomic_add_acq_rel_gpu(a.counters + row, 1u) == static_cast<unsigned>(a.nsb - 1));
+        misc[4] = (atomic_add_acq_rel_gpu(a.counters + row, 1u) == static_cast<unsigned>(nsp - 1));
     __syncthreads();
     if (!misc[4]) return;
     if (tid < kD) {
-        const size_t rb = static_cast<size_t>(row) * a.nsb;
+        const size_t rb = static_cast<size_t>(row) * nsp;
         float M = -INFINITY;
-        for (int j = 0; j < a.nsb; ++j) M = fmaxf(M, __ldcg(a.pm + rb + j));
+        for (int j = 0; j < nsp; ++j) M = fmaxf(M, __ldcg(a.pm + rb + j));
         float Ls = 0.0f, Os = 0.0f;
         if (M != -INFINITY) {
 #pragma unroll 4
-            for (int j = 0; j < a.nsb; ++j) {
+            for (int j = 0; j < nsp; ++j) {
                 const float s = expf(__ldcg(a.pm + rb + j) - M);
                 Ls += s * __ldcg(a.pl + rb + j);
                 Os += s * __ldcg(a.po + (rb + j) * kD + tid);
@@ -890,7 +903,7 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     aa.n_local = s.n_local;
     aa.scale = s.scale;
     aa.log_c2 = s.L >= 2 ? logf(0.5f * static_cast<float>(s.L) * static_cast<float>(s.L - 1)) : 0.0f;
-    attend<<<dim3(aa.nsb, s.B * s.Hq), kAThreads, smem_att, st>>>(aa);
+    attend<<<dim3(aa.nsb + 1, s.B * s.Hq), kAThreads, smem_att, st>>>(aa);
     return cudaGetLastError();
 }
 

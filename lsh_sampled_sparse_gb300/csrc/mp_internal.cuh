@@ -15,6 +15,10 @@ constexpr int kD = 128;                             // the only head dimension s
 constexpr int kAttendBlockGroup = 4;                // 1024-key blocks per attend CTA
 constexpr int kLogUTableIntervals = 4096;           // log u table over the cosine in [-1, 1]
 
+// Partial softmax states per query row: one per group of kAttendBlockGroup blocks (sampled
+// keys) plus one for the exact sink/local set.
+inline int attend_partials(int nblk) { return (nblk + kAttendBlockGroup - 1) / kAttendBlockGroup + 1; }
+
 // Device status word values (mp_status codes); kernels only ever raise MP_ERR_TIMEOUT.
 int* device_status_ptr();          // address of this device's status word (nullptr on error)
 int device_sm_count();
@@ -24,9 +28,9 @@ struct DecodeScratch {
     uint32_t* qbits;     // [B*Hq][qwords] query sign bits
     uint32_t* qmask;     // [B*Hkv][cpad][G] per-plane XOR masks (0 where the query bit is 1)
     float4* qstat;       // [B*Hq] {|q|, q.mu, 0, 0}
-    float* pm;           // [B*Hq][nsb] max logit of each attend CTA's partial softmax
-    float* pl;           // [B*Hq][nsb] its sum of weights
-    float* po;           // [B*Hq][nsb][128] its weighted value sum
+    float* pm;           // [B*Hq][nsp] max logit of each attend CTA's partial softmax
+    float* pl;           // [B*Hq][nsp] its sum of weights
+    float* po;           // [B*Hq][nsp][128] its weighted value sum
     unsigned* counters;  // [B*Hq] attend CTAs finished, for the last one's merge
     uint32_t* selmask;   // [B*Hq][nblk][32] selection words, written by the scan kernel
     float* logu_tab;     // [kLogUTableIntervals + 1] log u at cosines -1 + 2 i / intervals
