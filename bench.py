@@ -35,7 +35,7 @@ METRIC = "decode-attention queries/s and HBM GB/s (% of peak) at 96K ctx, 1×GB3
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ("key_mean", "build_tables", "encode_query", "sampled_attention")
 # kernels each stage launches (one library call each)
-STAGE_LAUNCHES = {"key_mean": 2, "build_tables": 1, "encode_query": 1, "sampled_attention": 1}
+STAGE_LAUNCHES = {"key_mean": 2, "build_tables": 1, "encode_query": 1, "sampled_attention": 2}
 STAGE_SOURCES = {"key_mean": "mp_misc.cu", "build_tables": "mp_encode_tc.cu",
                  "encode_query": "mp_decode.cu", "sampled_attention": "mp_decode.cu"}
 
@@ -52,6 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the timed steps eagerly instead of as one captured CUDA graph")
     return ap.parse_args(argv)
 
 
@@ -373,8 +375,17 @@ def run_ours(args):
         run_step(mp, wl, W, state, ws_mean, ws_dec, stream)
     torch.cuda.synchronize()
 
-    marks = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(layers)]
-             for _ in range(args.steps)]
+    use_graph = not args.no_graph
+    if use_graph:
+        try:       # events that stay timestamps inside a captured graph (event record nodes)
+            torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            use_graph = False
+
+    def stage_event():
+        return torch.cuda.Event(enable_timing=True, external=use_graph) if use_graph \
+            else torch.cuda.Event(enable_timing=True)
+    marks = [[[stage_event() for _ in range(5)] for _ in range(layers)] for _ in range(args.steps)]
     begin = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
@@ -383,11 +394,28 @@ def run_ours(args):
     while time.perf_counter() - t_roll < 0.4:
         run_step(mp, wl, W, state, ws_mean, ws_dec, stream)
         torch.cuda.synchronize()
+    # The timed region: K steps with CUDA events between the stages of every layer, captured once
+    # as a CUDA graph (kernel launches replayed without per-launch host work) and replayed once.
+    graph = None
+    if use_graph:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                cap = torch.cuda.current_stream()
+                for k in range(args.steps):
+                    run_step(mp, wl, W, state, ws_mean, ws_dec, cap, marks[k])
+        except Exception as e:          # capture unsupported here: fall back to eager launches
+            print(f"[bench] graph capture failed ({e}); timing eager launches", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize()
     dist_barrier(world)
     torch.cuda.synchronize()
     begin.record(stream)
-    for k in range(args.steps):
-        run_step(mp, wl, W, state, ws_mean, ws_dec, stream, marks[k])
+    if graph is not None:
+        graph.replay()
+    else:
+        for k in range(args.steps):
+            run_step(mp, wl, W, state, ws_mean, ws_dec, stream, marks[k])
     end.record(stream)
     torch.cuda.synchronize()
     dist_barrier(world)
@@ -455,6 +483,8 @@ def run_ours(args):
             "l2": f"inputs larger than L2: {2 * layers * wl.B * wl.Hkv * wl.n * wl.d * 2 / 1e9:.1f}"
                   " GB of K/V per step (L2 129 MB)",
             "parallelism": f"replicas x{world}",
+            "launch": "one CUDA graph of the K timed steps" if graph is not None
+                      else "eager stream launches",
         },
         "roofline": roof,
         "rooflines": rooflines,

@@ -24,6 +24,16 @@ constexpr int kRingDepth = 4;                       // tables in flight per warp
 constexpr int kRingMinK = 8, kRingMaxK = 11;        // K range the async scan handles
 constexpr int kLuIntervals = kLogUTableIntervals;   // log u table: cosine grid on [-1, 1]
 
+// Programmatic dependent launch: the next kernel in the stream may be scheduled once every CTA
+// of this one has started; a kernel launched that way waits for its predecessor's completion
+// (and memory) before it touches anything the predecessor writes.
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_predecessor() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // log u(p) = log P[Binomial(L, p^K) >= 2] in fp32 with the accurate library functions, used to
 // fill the per-call table of log u over the cosine; same two-branch definition as below.
 __device__ float log_inclusion_ref(float p, int K, int L) {
@@ -116,6 +126,7 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
     __shared__ float Qs[kQRows][kD];
     __shared__ float Ws[kD][32];                 // this word's 32 hyperplane columns
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    allow_dependents();                          // the scan may start streaming codes meanwhile
     if (blockIdx.y == a.qrow_ctas) {
         // the extra row of CTAs fills the log u table on the cosine grid c_i = -1 + 2 i / N
         for (int i = blockIdx.x * kThreads + tid; i <= kLuIntervals; i += gridDim.x * kThreads) {
@@ -422,6 +433,20 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     uint32_t* ring = gebuf + kWarps * 2 * G * 32 +                         // [8][depth][K][32]
                      static_cast<size_t>(warp) * kRingDepth * a.K * kWordsPerBlock;
 
+    // ---- before the query masks exist: let the attend kernel be scheduled (it waits for this
+    //      kernel's completion itself), and pull this warp's first tables of codes (an input of
+    //      the call) into L2
+    allow_dependents();
+    {
+        const int t0 = (a.L * warp) / kWarps;
+        const uint32_t* first = a.codes + (static_cast<size_t>(bg) * a.nblk + blk) * a.C * kWordsPerBlock +
+                                static_cast<size_t>(t0) * a.K * kWordsPerBlock;
+        const int rows = min(kRingDepth * a.K, ((a.L * (warp + 1)) / kWarps - t0) * a.K);
+        for (int r = lane; r < rows; r += 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(first + static_cast<size_t>(r) * kWordsPerBlock));
+    }
+    wait_for_predecessor();
+
     // ---- prologue: the group's query masks (one contiguous piece), q and mu as floats
     {
         const uint4* src = reinterpret_cast<const uint4*>(a.qmask +
@@ -557,14 +582,15 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     int* misc = reinterpret_cast<int*>(cbuf + kAWarps * kCombinePitch);  // [0..3] counts, [4]
 
     const int half = lane >> 4, hl = lane & 15;
-    const float4 st = a.qstat[row];
-    const float qn = st.x, qmu = st.y;
-    float q8[8], mu8[8];
+    float q8[8], mu8[8];                         // inputs of the call: readable right away
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         q8[i] = load_elem(a.q, a.q_bf16, static_cast<size_t>(row) * kD + 8 * hl + i);
         mu8[i] = a.centre[static_cast<size_t>(bg) * kD + 8 * hl + i];
     }
+    wait_for_predecessor();                      // selection words, query norms, log u table
+    const float4 st = a.qstat[row];
+    const float qn = st.x, qmu = st.y;
 
     // ---- the rows of this CTA: T by arithmetic, or the selected keys of its blocks by a list
     const int t_a = min(a.n_sink, a.n), t_b = max(a.n - a.n_local, t_a);
@@ -732,22 +758,55 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
         misc[4] = (atomic_add_acq_rel_gpu(a.counters + row, 1u) == static_cast<unsigned>(nsp - 1));
     __syncthreads();
     if (!misc[4]) return;
-    if (tid < kD) {
-        const size_t rb = static_cast<size_t>(row) * nsp;
-        float M = -INFINITY;
-        for (int j = 0; j < nsp; ++j) M = fmaxf(M, __ldcg(a.pm + rb + j));
-        float Ls = 0.0f, Os = 0.0f;
-        if (M != -INFINITY) {
-#pragma unroll 4
-            for (int j = 0; j < nsp; ++j) {
-                const float s = expf(__ldcg(a.pm + rb + j) - M);
-                Ls += s * __ldcg(a.pl + rb + j);
-                Os += s * __ldcg(a.po + (rb + j) * kD + tid);
-            }
+
+    // ---- merge: the partial outputs are staged in shared memory (the row list's space) with
+    //      cp.async, issued before the maximum is known; m of every partial is loaded meanwhile
+    //      and sc[j] = exp(m_j - M) kept in cbuf. Rounds of kMergeCap partials.
+    constexpr int kMergeCap = kAttendBlocks * kKeysPerBlock * 4 / (kD * 4);
+    float* stage = reinterpret_cast<float*>(smem);
+    float* red = cbuf;                            // [0, 8): reductions
+    float* sc = cbuf + 8;                         // scales, kMergeCap at a time
+    const size_t rb = static_cast<size_t>(row) * nsp;
+    auto stage_round = [&](int j0) {
+        const int cnt = min(kMergeCap, nsp - j0);
+        const float* src = a.po + (rb + j0) * kD;
+        for (int i = tid; i < cnt * (kD / 4); i += kAThreads) cp_async16(stage + 4 * i, src + 4 * i);
+        cp_async_commit();
+    };
+    stage_round(0);
+    float mx = -INFINITY;
+    for (int j = tid; j < nsp; j += kAThreads) mx = fmaxf(mx, __ldcg(a.pm + rb + j));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAWarps; ++w) M = fmaxf(M, red[w]);
+    float ls = 0.0f, Os = 0.0f;
+    for (int j0 = 0; j0 < nsp; j0 += kMergeCap) {
+        const int cnt = min(kMergeCap, nsp - j0);
+        if (tid < cnt) {
+            const float sj = M == -INFINITY ? 0.0f : expf(__ldcg(a.pm + rb + j0 + tid) - M);
+            sc[tid] = sj;
+            ls = fmaf(sj, __ldcg(a.pl + rb + j0 + tid), ls);
         }
-        a.out[static_cast<size_t>(row) * kD + tid] = Ls > 0.0f ? Os / Ls : 0.0f;
-        if (tid == 0) a.counters[row] = 0u;
+        cp_async_wait_pending<0>();
+        __syncthreads();                         // staged rows and scales visible to all
+#pragma unroll 8
+        for (int j = 0; j < cnt; ++j) Os = fmaf(sc[j], stage[j * kD + tid], Os);
+        __syncthreads();                         // stage and scales are refilled next round
+        if (j0 + kMergeCap < nsp) stage_round(j0 + kMergeCap);
     }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    if (lane == 0) red[4 + warp] = ls;
+    __syncthreads();
+    float Ls = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kAWarps; ++w) Ls += red[4 + w];
+    a.out[static_cast<size_t>(row) * kD + tid] = Ls > 0.0f ? Os / Ls : 0.0f;
+    if (tid == 0) a.counters[row] = 0u;
 }
 
 typedef void (*KernelFn)(const CArgs);
@@ -783,6 +842,23 @@ size_t attend_smem_for(bool kv_bf16) {
 }
 
 constexpr size_t kMaxSmem = 232448;   // 227 KB opt-in per CTA
+
+// launch `kern` so that it may be scheduled while the previous kernel in the stream finishes
+template <typename Arg>
+cudaError_t launch_dependent(void (*kern)(Arg), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, const Arg& arg) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, arg);
+}
 
 }  // namespace
 
@@ -874,8 +950,8 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     AttendFn attend = pick_attend(kv_bf16);
     const size_t smem_scan = collide_smem_for(G, s.cpad, s.K), smem_att = attend_smem_for(kv_bf16);
     if (!scan || smem_scan > kMaxSmem || smem_att > kMaxSmem) return cudaErrorNotSupported;
-    scan<<<dim3(s.nblk, s.B * s.Hkv), kThreads, smem_scan, st>>>(ca);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(scan, dim3(s.nblk, s.B * s.Hkv), dim3(kThreads), smem_scan,
+                                     st, ca);
     if (e != cudaSuccess) return e;
     AArgs aa;
     aa.selmask = ws.selmask;
@@ -903,8 +979,8 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     aa.n_local = s.n_local;
     aa.scale = s.scale;
     aa.log_c2 = s.L >= 2 ? logf(0.5f * static_cast<float>(s.L) * static_cast<float>(s.L - 1)) : 0.0f;
-    attend<<<dim3(aa.nsb + 1, s.B * s.Hq), kAThreads, smem_att, st>>>(aa);
-    return cudaGetLastError();
+    return launch_dependent(attend, dim3(aa.nsb + 1, s.B * s.Hq), dim3(kAThreads), smem_att, st,
+                            aa);
 }
 
 }  // namespace mp
