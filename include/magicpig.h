@@ -87,14 +87,17 @@ MP_API int mp_abi_version(void);
 /* Bytes of packed codes for B*Hkv heads of n keys: B*Hkv*ceil(n/1024)*K*L*128. */
 MP_API size_t mp_codes_bytes(int B, int Hkv, int n, int K, int L);
 
-/* Workspace bytes mp_key_mean needs (fixed-order partial sums). */
+/* Workspace bytes mp_key_mean needs: fixed-order partial sums plus one counter per head (the
+ * call clears the counters itself; the workspace needs no initial contents). */
 MP_API size_t mp_key_mean_workspace_bytes(int B, int Hkv, int n, int d);
 
 /* Centre of the cached keys: centre[b][g][:] = (1/n) sum_i keys[b][g][i][:], float32
  * accumulation in a fixed order (run-to-run identical).
  * ("LSH Sampling...", method details, data preprocessing and centering: keys are centred before
  * the tables are built; "don't pick the tallest", section 5.)
- * Errors: MP_ERR_INVALID_ARG for n < 1, null pointers; MP_ERR_WORKSPACE if ws_bytes is short. */
+ * One kernel: each CTA sums a range of 1024 rows, the last CTA of a head adds the ranges in
+ * order. Errors: MP_ERR_INVALID_ARG for n < 1, null pointers; MP_ERR_WORKSPACE if ws_bytes is
+ * short. */
 MP_API mp_status mp_key_mean(const void* keys, mp_dtype key_dtype, int B, int Hkv, int n, int d,
                              float* centre, void* workspace, size_t ws_bytes,
                              cudaStream_t stream);

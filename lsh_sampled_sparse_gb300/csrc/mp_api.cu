@@ -177,7 +177,9 @@ size_t mp_codes_bytes(int B, int Hkv, int n, int K, int L) {
 
 size_t mp_key_mean_workspace_bytes(int B, int Hkv, int n, int d) {
     if (B < 1 || Hkv < 1 || n < 1 || d != kD) return 0;
-    return align256(static_cast<size_t>(B) * Hkv * key_mean_splits(n) * kD * 4);
+    // partial column sums per row range, then one counter per head
+    return align256(static_cast<size_t>(B) * Hkv * key_mean_splits(n) * kD * 4 +
+                    static_cast<size_t>(B) * Hkv * 4);
 }
 
 mp_status mp_key_mean(const void* keys, mp_dtype key_dtype, int B, int Hkv, int n, int d,

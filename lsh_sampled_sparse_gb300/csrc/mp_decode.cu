@@ -18,8 +18,10 @@ constexpr float kLogFltMin = -87.336544750553102f;   // log(FLT_MIN)
 constexpr float kPi = 3.14159265358979323846f;
 constexpr int kCombinePitch = 132;                  // floats per (warp, head) partial: o, m, l
 constexpr int kAttendBlocks = kAttendBlockGroup;
-constexpr int kAWarps = kAttendBlockGroup;          // attend CTA: one warp per block of its group
+constexpr int kAWarps = 4;                          // attend CTA: 4 warps, 8 half-warps on rows
+static_assert(kAttendBlocks <= kAWarps, "one warp lists each block of an attend CTA");
 constexpr int kAThreads = 32 * kAWarps;
+static_assert(kAThreads == kD, "the attend merge gives one thread to each of the 128 output dims");
 constexpr int kRingDepth = 4;                       // tables in flight per warp in the async scan
 constexpr int kRingMinK = 8, kRingMaxK = 11;        // K range the async scan handles
 constexpr int kLuIntervals = kLogUTableIntervals;   // log u table: cosine grid on [-1, 1]
@@ -227,9 +229,24 @@ __host__ __device__ constexpr int stage_rows() {
     return sizeof(KV) == 2 ? 64 : 32;   // 32 KB of K+V rows either way
 }
 
-template <typename KV>
-constexpr size_t attend_smem_bytes() {
-    return kAttendBlocks * kKeysPerBlock * 4 + kAWarps * kCombinePitch * 4 + 32;
+// Attend CTA shared memory: [work][cbuf][misc]. The work region holds the CTA's row list, and in
+// the merging CTA up to `merge_cap` staged partial outputs (all of them unless that exceeds
+// 48 KB; the merge then runs in rounds).
+struct AttendSmem {
+    size_t work, total;
+    int merge_cap;
+};
+inline AttendSmem attend_smem(int nsp) {
+    constexpr size_t kList = static_cast<size_t>(kAttendBlocks) * kKeysPerBlock * 4;
+    constexpr size_t kRow = static_cast<size_t>(kD) * 4;
+    size_t work = static_cast<size_t>(nsp) * kRow;
+    if (work > 48 * 1024) work = 48 * 1024;
+    if (work < kList) work = kList;
+    AttendSmem m;
+    m.work = work;
+    m.merge_cap = static_cast<int>(work / kRow);
+    m.total = work + static_cast<size_t>(kAWarps) * kCombinePitch * 4 + 32;
+    return m;
 }
 
 template <int G>
@@ -417,6 +434,8 @@ struct AArgs {
     const float* logu_tab;
     int q_bf16, n, nblk, nsb, Hq, Hkv, G, K, L, n_sink, n_local;
     float scale, log_c2;
+    int merge_cap;                               // partials staged per merge round
+    int work_bytes;                              // bytes of the list / merge stage region
 };
 
 // Collide + select: per (1024-key block, sequence x KV head) the selection words
@@ -578,7 +597,7 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     const int nsp = a.nsb + 1;                   // partials per query row
 
     int* lidx = reinterpret_cast<int*>(smem);
-    float* cbuf = reinterpret_cast<float*>(smem + kAttendBlocks * kKeysPerBlock * 4);
+    float* cbuf = reinterpret_cast<float*>(smem + a.work_bytes);
     int* misc = reinterpret_cast<int*>(cbuf + kAWarps * kCombinePitch);  // [0..3] counts, [4]
 
     const int half = lane >> 4, hl = lane & 15;
@@ -762,7 +781,7 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     // ---- merge: the partial outputs are staged in shared memory (the row list's space) with
     //      cp.async, issued before the maximum is known; m of every partial is loaded meanwhile
     //      and sc[j] = exp(m_j - M) kept in cbuf. Rounds of kMergeCap partials.
-    constexpr int kMergeCap = kAttendBlocks * kKeysPerBlock * 4 / (kD * 4);
+    const int kMergeCap = a.merge_cap;
     float* stage = reinterpret_cast<float*>(smem);
     float* red = cbuf;                            // [0, 8): reductions
     float* sc = cbuf + 8;                         // scales, kMergeCap at a time
@@ -837,9 +856,7 @@ size_t collide_smem_for(int G, int cpad, int K) {
     }
 }
 
-size_t attend_smem_for(bool kv_bf16) {
-    return kv_bf16 ? attend_smem_bytes<__nv_bfloat16>() : attend_smem_bytes<float>();
-}
+size_t attend_smem_for(int nblk) { return attend_smem(attend_partials(nblk)).total; }
 
 constexpr size_t kMaxSmem = 232448;   // 227 KB opt-in per CTA
 
@@ -865,7 +882,8 @@ cudaError_t launch_dependent(void (*kern)(Arg), dim3 grid, dim3 block, size_t sm
 bool decode_supported(const DecodeShape& s, bool kv_bf16) {
     const int G = s.Hq / s.Hkv;
     if (!pick_collide(G)) return false;
-    return collide_smem_for(G, s.cpad, s.K) <= kMaxSmem && attend_smem_for(kv_bf16) <= kMaxSmem;
+    (void)kv_bf16;
+    return collide_smem_for(G, s.cpad, s.K) <= kMaxSmem && attend_smem_for(s.nblk) <= kMaxSmem;
 }
 
 cudaError_t prepare_decode() {
@@ -948,7 +966,7 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     ca.scale = s.scale;
     KernelFn scan = pick_collide(G);
     AttendFn attend = pick_attend(kv_bf16);
-    const size_t smem_scan = collide_smem_for(G, s.cpad, s.K), smem_att = attend_smem_for(kv_bf16);
+    const size_t smem_scan = collide_smem_for(G, s.cpad, s.K), smem_att = attend_smem_for(s.nblk);
     if (!scan || smem_scan > kMaxSmem || smem_att > kMaxSmem) return cudaErrorNotSupported;
     cudaError_t e = launch_dependent(scan, dim3(s.nblk, s.B * s.Hkv), dim3(kThreads), smem_scan,
                                      st, ca);
@@ -979,6 +997,11 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     aa.n_local = s.n_local;
     aa.scale = s.scale;
     aa.log_c2 = s.L >= 2 ? logf(0.5f * static_cast<float>(s.L) * static_cast<float>(s.L - 1)) : 0.0f;
+    {
+        const AttendSmem m = attend_smem(attend_partials(s.nblk));
+        aa.merge_cap = m.merge_cap;
+        aa.work_bytes = static_cast<int>(m.work);
+    }
     return launch_dependent(attend, dim3(aa.nsb + 1, s.B * s.Hq), dim3(kAThreads), smem_att, st,
                             aa);
 }

@@ -9,25 +9,29 @@ namespace {
 // Centre: mu = (1/n) sum_i k_i per head ("LSH Sampling...", method details, data preprocessing
 // and centering). Fixed partition into row ranges, fixed reduction order: run-to-run identical.
 // ------------------------------------------------------------------------------------------------
-constexpr int kMeanRows = 512;     // rows per partial sum
+constexpr int kMeanRows = 1024;    // rows per partial sum
 constexpr int kMeanThreads = 256;
 
+// One CTA per (row range, head): the range's column sums into `partial`; the last CTA of a head
+// to finish (release-acquire counter) adds the head's partials in range order and writes mu.
 template <typename T>
 __global__ void __launch_bounds__(kMeanThreads)
-    key_mean_partial_kernel(const T* keys, int n, int nsplit, float* partial) {
+    key_mean_kernel(const T* keys, int n, int nsplit, float* partial, unsigned* counters,
+                    float* centre) {
     // thread -> (column group of 16 bytes, row phase); rows stride by the number of row phases
     constexpr int kPer = 16 / sizeof(T);                 // elements per 16-byte load
     constexpr int kGroups = kD / kPer;                   // column groups per row
     constexpr int kPhases = kMeanThreads / kGroups;      // rows read in parallel
     __shared__ float red[kPhases][kD + 4];
-    const int bh = blockIdx.y, split = blockIdx.x;
-    const int cg = threadIdx.x % kGroups, ph = threadIdx.x / kGroups;
+    __shared__ int last;
+    const int bh = blockIdx.y, split = blockIdx.x, tid = threadIdx.x;
+    const int cg = tid % kGroups, ph = tid / kGroups;
     const int r0 = split * kMeanRows, r1 = min(n, r0 + kMeanRows);
     const T* base = keys + static_cast<size_t>(bh) * n * kD + cg * kPer;
     float acc[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) acc[i] = 0.0f;
-#pragma unroll 4
+#pragma unroll 8
     for (int r = r0 + ph; r < r1; r += kPhases) {
         const uint4 raw = __ldcs(reinterpret_cast<const uint4*>(base + static_cast<size_t>(r) * kD));
         const T* v = reinterpret_cast<const T*>(&raw);
@@ -37,18 +41,33 @@ __global__ void __launch_bounds__(kMeanThreads)
 #pragma unroll
     for (int i = 0; i < kPer; ++i) red[ph][cg * kPer + i] = acc[i];
     __syncthreads();
-    if (threadIdx.x < kD) {
+    if (tid < kD) {
         float s = 0.0f;
-        for (int p = 0; p < kPhases; ++p) s += red[p][threadIdx.x];
-        partial[(static_cast<size_t>(bh) * nsplit + split) * kD + threadIdx.x] = s;
+        for (int p = 0; p < kPhases; ++p) s += red[p][tid];
+        partial[(static_cast<size_t>(bh) * nsplit + split) * kD + tid] = s;
     }
-}
-
-__global__ void key_mean_final_kernel(const float* partial, int nsplit, int n, float* centre) {
-    const int bh = blockIdx.x, e = threadIdx.x;
+    __syncthreads();
+    if (tid == 0) {
+        unsigned old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(old)
+                     : "l"(counters + bh)
+                     : "memory");
+        last = old == static_cast<unsigned>(nsplit - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    // the head's partials, in range order: two halves of the ranges, one column per thread
+    const int col = tid % kD, half = tid / kD;
+    const float* ph0 = partial + static_cast<size_t>(bh) * nsplit * kD + col;
     float s = 0.0f;
-    for (int k = 0; k < nsplit; ++k) s += partial[(static_cast<size_t>(bh) * nsplit + k) * kD + e];
-    centre[static_cast<size_t>(bh) * kD + e] = s / static_cast<float>(n);
+#pragma unroll 8
+    for (int k = half; k < nsplit; k += 2) s += __ldcg(ph0 + static_cast<size_t>(k) * kD);
+    red[half][col] = s;
+    __syncthreads();
+    if (tid < kD) centre[static_cast<size_t>(bh) * kD + tid] = (red[0][tid] + red[1][tid]) /
+                                                               static_cast<float>(n);
+    if (tid == 0) counters[bh] = 0u;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -188,16 +207,17 @@ int key_mean_splits(int n) { return (n + kMeanRows - 1) / kMeanRows; }
 
 cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int n, float* centre,
                             float* partial, int nsplit, cudaStream_t st) {
+    // the per-head counters follow the partial sums in the workspace; they start at zero
+    unsigned* counters = reinterpret_cast<unsigned*>(partial + static_cast<size_t>(BH) * nsplit * kD);
+    cudaError_t e = cudaMemsetAsync(counters, 0, static_cast<size_t>(BH) * sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
     const dim3 grid(nsplit, BH);
     if (bf16)
-        key_mean_partial_kernel<__nv_bfloat16><<<grid, kMeanThreads, 0, st>>>(
-            reinterpret_cast<const __nv_bfloat16*>(keys), n, nsplit, partial);
+        key_mean_kernel<__nv_bfloat16><<<grid, kMeanThreads, 0, st>>>(
+            reinterpret_cast<const __nv_bfloat16*>(keys), n, nsplit, partial, counters, centre);
     else
-        key_mean_partial_kernel<float><<<grid, kMeanThreads, 0, st>>>(
-            reinterpret_cast<const float*>(keys), n, nsplit, partial);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    key_mean_final_kernel<<<BH, kD, 0, st>>>(partial, nsplit, n, centre);
+        key_mean_kernel<float><<<grid, kMeanThreads, 0, st>>>(
+            reinterpret_cast<const float*>(keys), n, nsplit, partial, counters, centre);
     return cudaGetLastError();
 }
 
@@ -238,10 +258,8 @@ cudaError_t launch_codes_unpack(const uint32_t* codes, int BH, int n, int K, int
 cudaError_t prepare_misc() {
     cudaFuncAttributes fa;
     cudaError_t e;
-    if ((e = cudaFuncGetAttributes(&fa, key_mean_partial_kernel<float>)) != cudaSuccess) return e;
-    if ((e = cudaFuncGetAttributes(&fa, key_mean_partial_kernel<__nv_bfloat16>)) != cudaSuccess)
-        return e;
-    if ((e = cudaFuncGetAttributes(&fa, key_mean_final_kernel)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, key_mean_kernel<float>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, key_mean_kernel<__nv_bfloat16>)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, encode_simt_kernel)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, compact_selection_kernel)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, collision_counts_kernel)) != cudaSuccess) return e;
