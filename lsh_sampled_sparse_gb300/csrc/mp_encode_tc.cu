@@ -41,9 +41,6 @@ constexpr int kStages = 3;             // A-tile ring depth
 // registers cap the kernel at 96 registers per thread (ptxas picks that from the launch bound).
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-// each epilogue warp drains one TMEM lane quadrant x kEpiGroups groups of 32 columns
-constexpr int kEpiGroups = kChunkN / 32 / (kEpiWarps / 4);
-static_assert(kEpiGroups * 32 * (kEpiWarps / 4) == kChunkN, "epilogue warps cover the chunk");
 constexpr uint32_t kStageBytes = kTileM * kD * 2;      // 32 KB: two 64-column swizzled halves
 constexpr uint32_t kHalfBytes = kTileM * 128;          // 16 KB: 128 rows x 128 bytes
 constexpr uint32_t kBBytes = kChunkN * kD * 2;         // 64 KB
@@ -377,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- epilogue ----------------
         const int ew = warp - 2;                 // 0..15
         const int quad = warp & 3;               // TMEM lane quadrant this warp may read
-        const int colA = (ew >> 2) * 32 * kEpiGroups;   // this warp's column groups start here
+        const int colA = (ew >> 2) * 64;         // this warp's two 32-column groups start here
         const int et = tid - 64;                 // 0..511
         const uint32_t tquad = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
         bool aborted = false;
@@ -464,16 +461,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                a.status);
                     aborted = !__all_sync(0xffffffffu, got);   // keep the warp uniform
                 }
-                // sign bits of this warp's 32-column groups into registers (one TMEM wait per
-                // group keeps 32 accumulator registers live) ...
-                uint32_t x[kEpiGroups];
-#pragma unroll
-                for (int g = 0; g < kEpiGroups; ++g) x[g] = 0u;
+                // sign bits of this warp's two 32-column groups into registers (one TMEM wait
+                // per group keeps 32 accumulator registers live) ...
+                uint32_t x[2] = {0u, 0u};
                 if (!aborted) {
                     tc_fence_after();
                     const uint32_t trow = tquad + ab * kChunkN;
 #pragma unroll
-                    for (int g = 0; g < kEpiGroups; ++g) {
+                    for (int g = 0; g < 2; ++g) {
                         if (colA + 32 * g < Nc) {
                             uint32_t v[32];
                             tmem_ld32(trow + colA + 32 * g, v);
@@ -492,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t == 0 && prev_bg >= 0) store_unit(prev_bg, prev_blk);
                 if (!aborted) {
 #pragma unroll
-                    for (int g = 0; g < kEpiGroups; ++g) {
+                    for (int g = 0; g < 2; ++g) {
                         const int col = colA + 32 * g;
                         if (col < Nc) {
                             const uint32_t y = warp_transpose32(x[g], lane);
