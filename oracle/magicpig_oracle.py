@@ -40,6 +40,9 @@ Parity status (what pins each function; the tests under tests/ hold the pins):
   simhash_projections / sign_bits / table_codes / encode_*  brute force by definition, collision
       probability 1 - theta/pi by Monte-Carlo, scale and negation invariants
   collision_counts / sampled_set                            brute force by definition
+  bucket_tables / bucket_collision_counts                   equal to the direct code comparison;
+      bucket sizes sum to n; scanned entries average L n / 2^K for uniform codes (14,400 at
+      n = 98,304, (10, 150), the pages' figure)
   log_inclusion_probability                                 exact rational binomial tail,
       Monte-Carlo frequency of >= 2 collisions, closed-form special values
   snis_attention / decode_head                              K = 0 reduces to full softmax
@@ -62,7 +65,7 @@ __all__ = [
     "near_tie_mask", "encode_keys", "encode_query", "collision_counts", "exact_set_mask",
     "sampled_set", "collision_probability", "log_inclusion_probability",
     "inclusion_probability", "snis_attention", "full_attention", "decode_head", "decode",
-    "replay_bits", "as64",
+    "replay_bits", "as64", "bucket_tables", "bucket_collision_counts",
 ]
 
 
@@ -149,6 +152,33 @@ def encode_query(q, W, K: int, L: int):
 def collision_counts(key_codes, q_code) -> np.ndarray:
     """cnt_i = number of tables t with code_t(k_i) == code_t(q). key_codes [n, L], q_code [L]."""
     return (np.asarray(key_codes) == np.asarray(q_code)[None, :]).sum(axis=1)
+
+
+def bucket_tables(key_codes, K: int, L: int):
+    """The L hash tables as buckets: for table t, bucket c holds every key i with code_t(k_i) = c.
+
+    ("LSH Sampling...", system co-design item 3: the query's codes are looked up in L prebuilt
+    tables; "don't pick the tallest", section 6: every table stores a pointer to every key.)
+    Returns (offsets [L, 2^K + 1], members [L, n]): members[t, offsets[t, c]:offsets[t, c + 1]]
+    are the keys of bucket c of table t, ascending."""
+    codes = np.asarray(key_codes, dtype=np.int64)
+    n = codes.shape[0]
+    nb = 1 << K
+    offsets = np.zeros((L, nb + 1), dtype=np.int64)
+    members = np.zeros((L, n), dtype=np.int64)
+    for t in range(L):
+        counts = np.bincount(codes[:, t], minlength=nb)
+        offsets[t, 1:] = np.cumsum(counts)
+        members[t] = np.argsort(codes[:, t], kind="stable")   # by bucket, keys ascending within
+    return offsets, members
+
+
+def bucket_collision_counts(offsets, members, q_code, n: int) -> np.ndarray:
+    """cnt_i from the tables: every table adds one to each key in the query's bucket."""
+    cnt = np.zeros(n, dtype=np.int64)
+    for t, c in enumerate(np.asarray(q_code, dtype=np.int64)):
+        cnt[members[t, offsets[t, c]:offsets[t, c + 1]]] += 1
+    return cnt
 
 
 def exact_set_mask(n: int, n_sink: int, n_local: int) -> np.ndarray:

@@ -166,6 +166,41 @@ def test_codes_counts_and_set_by_brute_force():
     assert S.tolist() == [i for i in range(n) if brute_cnt[i] >= 2 and not T[i]]
 
 
+def test_bucket_tables_by_brute_force():
+    """Buckets hold exactly the keys of their code, ascending; the query's buckets count each
+    key once per table it shares ("LSH Sampling..." system co-design item 3; "don't pick the
+    tallest" section 6). The counts are checked against scalar loops over the codes."""
+    rng = np.random.default_rng(21)
+    n, K, L = 37, 3, 5
+    codes = rng.integers(0, 1 << K, size=(n, L))
+    offsets, members = O.bucket_tables(codes, K, L)
+    for t in range(L):
+        assert offsets[t, 0] == 0 and offsets[t, -1] == n
+        for c in range(1 << K):
+            got = members[t, offsets[t, c]:offsets[t, c + 1]].tolist()
+            assert got == [i for i in range(n) if codes[i][t] == c]
+    for _ in range(5):
+        qc = rng.integers(0, 1 << K, size=L)
+        brute = [sum(1 for t in range(L) if codes[i][t] == qc[t]) for i in range(n)]
+        assert O.bucket_collision_counts(offsets, members, qc, n).tolist() == brute
+
+
+def test_scanned_entries_average_the_pages_figure():
+    """With evenly filled buckets a query scans L n / 2^K entries: 14,400 at n = 98,304 and
+    (10, 150) ("don't pick the tallest", section 6). Uniform random codes stand in for evenly
+    filled buckets; the mean over random queries must sit within a few standard errors."""
+    g = json.load(open(os.path.join(HERE, "golden", "page_arithmetic.json")))
+    n, K, L = 98304, 10, 150
+    rng = np.random.default_rng(22)
+    codes = rng.integers(0, 1 << K, size=(n, L))
+    offsets, _ = O.bucket_tables(codes, K, L)
+    sizes = np.diff(offsets, axis=1)                       # [L, 2^K]
+    scanned = [int(sizes[np.arange(L), rng.integers(0, 1 << K, size=L)].sum()) for _ in range(64)]
+    se = math.sqrt(L * n * 2.0 ** -K) / math.sqrt(len(scanned))   # binomial bucket sizes
+    assert abs(np.mean(scanned) - g["entries_scanned_per_query"]["value"]) < 5 * se
+    assert 4 * L * n // (1 << K) == g["index_bytes_scanned_per_query"]["value"]
+
+
 def test_key_along_query_collides_in_every_table():
     rng = np.random.default_rng(4)
     d, K, L = 16, 10, 150
