@@ -159,6 +159,37 @@ MP_API mp_status mp_sampled_attention(const void* q, mp_dtype q_dtype, const uin
                                       const mp_params* prm, float* out, void* workspace,
                                       size_t ws_bytes, cudaStream_t stream);
 
+/* ---- Bucketed hash tables ---------------------------------------------------------------------
+ * The retrieval structure of the pages: per table, the keys of each K-bit code ("LSH Sampling...",
+ * system co-design item 3: the query's codes are looked up in L prebuilt hash tables; "don't pick
+ * the tallest", section 6: every table stores a pointer to every key, and a query scans about
+ * L n / 2^K entries). Layout per (sequence, KV head), 32-bit words: offsets[L][2^K + 1], then
+ * members[L][n]; members[t][offsets[t][c] .. offsets[t][c+1]) are the keys with code c in table
+ * t. The order inside a bucket is not fixed (a bucket is a set).
+ * mp_buckets_bytes: bytes for B*Hkv such tables (L (2^K + 1 + n) words each); 0 if K > 12 or the
+ * shapes are invalid. */
+MP_API size_t mp_buckets_bytes(int B, int Hkv, int n, int K, int L);
+
+/* Build the bucketed tables from the packed codes of mp_build_tables (same B, Hkv, n, K, L).
+ * buckets: caller-owned device memory of mp_buckets_bytes bytes, 4-byte aligned; codes may be
+ * NULL when K == 0. Errors: MP_ERR_INVALID_ARG (shapes, null, misalignment), MP_ERR_UNSUPPORTED
+ * (K > 12). */
+MP_API mp_status mp_build_buckets(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
+                                  uint32_t* buckets, cudaStream_t stream);
+
+/* mp_sampled_attention with the bucketed tables instead of a scan of the packed codes: each
+ * query row reads its bucket in every table and keeps the keys hit by >= 2 tables (the same S as
+ * the scan, bit for bit), then the same gather, importance weights and merged softmax. Needs the
+ * query encoding of mp_encode_query in the workspace first, like mp_sampled_attention.
+ * buckets: 16-byte aligned. Errors as mp_sampled_attention; MP_ERR_UNSUPPORTED also for K > 12. */
+MP_API mp_status mp_sampled_attention_buckets(const void* q, mp_dtype q_dtype,
+                                              const uint32_t* buckets, const float* centre,
+                                              const void* keys, const void* values,
+                                              mp_dtype kv_dtype, int B, int Hq, int Hkv, int n,
+                                              int d, const mp_params* prm, float* out,
+                                              void* workspace, size_t ws_bytes,
+                                              cudaStream_t stream);
+
 /* Workspace bytes mp_debug_select needs. */
 MP_API size_t mp_debug_workspace_bytes(int B, int Hq, int Hkv, int n, int d,
                                        const mp_params* prm);

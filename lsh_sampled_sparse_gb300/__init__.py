@@ -10,7 +10,9 @@ from .binding import (  # noqa: F401
     MagicPIGError,
     Params,
     abi_version,
+    build_buckets,
     build_tables,
+    buckets_bytes,
     codes_bytes,
     codes_unpack,
     debug_select,
@@ -24,4 +26,5 @@ from .binding import (  # noqa: F401
     lib,
     library_path,
     sampled_attention,
+    sampled_attention_buckets,
 )

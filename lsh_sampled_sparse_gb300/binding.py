@@ -56,6 +56,10 @@ def _declare(L):
         "mp_decode_attention_noalloc": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _c_int, _vp, _vp,
                                                  _c_int] + [_c_int] * 5 + [P, _vp, _vp]),
         "mp_codes_unpack": (_c_int, [_vp] + [_c_int] * 5 + [_vp, _vp]),
+        "mp_buckets_bytes": (_c_size, [_c_int] * 5),
+        "mp_build_buckets": (_c_int, [_vp] + [_c_int] * 5 + [_vp, _vp]),
+        "mp_sampled_attention_buckets": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int]
+                                         + [_c_int] * 5 + [P, _vp, _vp, _c_size, _vp]),
         "mp_device_status": (_c_int, [ctypes.POINTER(_c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -233,6 +237,45 @@ def sampled_attention(q, codes, centre, keys, values, K: int, L: int, n_sink: in
         _ptr(q), _dtype(q, "q"), _ptr(codes), _ptr(centre), _ptr(keys), _ptr(values),
         _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out), _ptr(workspace),
         _nbytes(workspace), _stream(stream)), "mp_sampled_attention")
+    return out
+
+
+def buckets_bytes(B: int, Hkv: int, n: int, K: int, L: int) -> int:
+    return int(lib().mp_buckets_bytes(B, Hkv, n, K, L))
+
+
+def build_buckets(codes, B: int, Hkv: int, n: int, K: int, L: int, buckets=None, stream=None):
+    """Bucketed hash tables from the packed codes (int32 tensor of buckets_bytes/4 words)."""
+    nbytes = buckets_bytes(B, Hkv, n, K, L)
+    if nbytes == 0:
+        raise ValueError("unsupported bucket table shape (K must be <= 12)")
+    if buckets is None:
+        buckets = torch.empty(nbytes // 4, dtype=torch.int32, device=codes.device)
+    _cuda(codes, "codes")
+    _cuda(buckets, "buckets")
+    if _nbytes(buckets) < nbytes:
+        raise ValueError("buckets buffer too small")
+    _check(lib().mp_build_buckets(_ptr(codes), B, Hkv, n, K, L, _ptr(buckets), _stream(stream)),
+           "mp_build_buckets")
+    return buckets
+
+
+def sampled_attention_buckets(q, buckets, centre, keys, values, K: int, L: int, n_sink: int,
+                              n_local: int, out, workspace, scale: float = 0.0, stream=None):
+    """sampled_attention with the bucketed tables in place of the code scan."""
+    _cuda(q, "q", 3)
+    _cuda(keys, "keys", 4)
+    _cuda(values, "values", 4)
+    _cuda(out, "out", 3)
+    _cuda(workspace, "workspace")
+    _cuda(buckets, "buckets")
+    B, Hq, d = q.shape
+    Hkv, n = keys.shape[1], keys.shape[2]
+    p = Params(K, L, n_sink, n_local, scale, 0)
+    _check(lib().mp_sampled_attention_buckets(
+        _ptr(q), _dtype(q, "q"), _ptr(buckets), _ptr(centre), _ptr(keys), _ptr(values),
+        _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out), _ptr(workspace),
+        _nbytes(workspace), _stream(stream)), "mp_sampled_attention_buckets")
     return out
 
 

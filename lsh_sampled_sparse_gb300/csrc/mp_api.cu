@@ -37,7 +37,9 @@ bool ensure_prepared() {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return false;
-    if (prepare_misc() != cudaSuccess || prepare_decode() != cudaSuccess) return false;
+    if (prepare_misc() != cudaSuccess || prepare_decode() != cudaSuccess ||
+        prepare_buckets() != cudaSuccess)
+        return false;
     prepare_encode_tc();   // failure only disables the tensor-core encoder
     cudaGetLastError();
     g_status_ptr[dev] = static_cast<int*>(p);
@@ -98,6 +100,7 @@ size_t decode_scratch_bytes(const DecodeShape& s, bool debug) {
     b += align256(rows * nsp * kD * 4);                  // po
     b += align256(rows * 4);                             // counters
     b += align256(rows * s.nblk * 32 * 4);               // selection words
+    b += align256(rows * s.nblk * 32 * 4);               // >= 1 bitmap of the bucketed lookup
     b += align256((kLogUTableIntervals + 1) * 4);        // log u table
     (void)debug;                                         // the debug path needs nothing more
     return b;
@@ -123,6 +126,8 @@ DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug) {
     d.counters = reinterpret_cast<unsigned*>(p);
     p += align256(rows * 4);
     d.selmask = reinterpret_cast<uint32_t*>(p);
+    p += align256(rows * s.nblk * 32 * 4);
+    d.sel_ge1 = reinterpret_cast<uint32_t*>(p);
     p += align256(rows * s.nblk * 32 * 4);
     d.logu_tab = reinterpret_cast<float*>(p);
     (void)debug;
@@ -284,6 +289,41 @@ mp_status mp_sampled_attention(const void* q, mp_dtype q_dtype, const uint32_t* 
     const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
     return to_status(launch_collide(q, q_dtype == MP_BF16, codes, centre, keys, values,
                                     kv_dtype == MP_BF16, s, out, ws, stream));
+}
+
+size_t mp_buckets_bytes(int B, int Hkv, int n, int K, int L) {
+    return bucket_table_bytes(B, Hkv, n, K, L);
+}
+
+mp_status mp_build_buckets(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
+                           uint32_t* buckets, cudaStream_t stream) {
+    if (B < 1 || Hkv < 1 || n < 1 || K < 0 || K > 32 || L < 1) return MP_ERR_INVALID_ARG;
+    if (K > kMaxBucketBits) return MP_ERR_UNSUPPORTED;
+    if (!buckets || (K > 0 && !codes)) return MP_ERR_INVALID_ARG;
+    if ((codes && !aligned(codes, 16)) || !aligned(buckets, 4)) return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    return to_status(launch_bucket_build(codes, B, Hkv, n, K, L, buckets, stream));
+}
+
+mp_status mp_sampled_attention_buckets(const void* q, mp_dtype q_dtype, const uint32_t* buckets,
+                                       const float* centre, const void* keys,
+                                       const void* values, mp_dtype kv_dtype, int B, int Hq,
+                                       int Hkv, int n, int d, const mp_params* prm, float* out,
+                                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (!buckets) return MP_ERR_INVALID_ARG;
+    DecodeShape s;
+    // the buckets stand in for the codes, q for W, in the shared checks
+    const mp_status st = check_decode(q, q_dtype, buckets, centre, q, MP_F32, keys, values,
+                                      kv_dtype, B, Hq, Hkv, n, d, prm, out, workspace, ws_bytes,
+                                      false, &s);
+    if (st != MP_OK) return st;
+    if (s.K > kMaxBucketBits) return MP_ERR_UNSUPPORTED;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
+    cudaError_t e = launch_bucket_lookup(buckets, ws.qbits, s, ws.sel_ge1, ws.selmask, stream);
+    if (e != cudaSuccess) return MP_ERR_CUDA;
+    return to_status(launch_attend(q, q_dtype == MP_BF16, centre, keys, values,
+                                   kv_dtype == MP_BF16, s, out, ws, stream));
 }
 
 mp_status mp_debug_select(const void* q, mp_dtype q_dtype, const uint32_t* codes,

@@ -624,7 +624,14 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
         if (warp < nb) {
             const int blk = blk0 + warp;
             key0 = blk * kKeysPerBlock + lane * 32;
-            U = a.selmask[(static_cast<size_t>(row) * a.nblk + blk) * 32 + lane];
+            {
+                // the scan already masked its words; selection words from elsewhere (the
+                // bucketed lookup's >= 2 bitmap) need valid & not T here
+                const uint32_t valid = bits_below(a.n - key0);
+                const uint32_t tmask =
+                    (bits_below(a.n_sink - key0) | ~bits_below(a.n - a.n_local - key0)) & valid;
+                U = a.selmask[(static_cast<size_t>(row) * a.nblk + blk) * 32 + lane] & valid & ~tmask;
+            }
             const int c = __popc(U);
             int incl = c;
 #pragma unroll
@@ -965,12 +972,22 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     ca.n_local = s.n_local;
     ca.scale = s.scale;
     KernelFn scan = pick_collide(G);
-    AttendFn attend = pick_attend(kv_bf16);
-    const size_t smem_scan = collide_smem_for(G, s.cpad, s.K), smem_att = attend_smem_for(s.nblk);
-    if (!scan || smem_scan > kMaxSmem || smem_att > kMaxSmem) return cudaErrorNotSupported;
+    const size_t smem_scan = collide_smem_for(G, s.cpad, s.K);
+    if (!scan || smem_scan > kMaxSmem || attend_smem_for(s.nblk) > kMaxSmem)
+        return cudaErrorNotSupported;
     cudaError_t e = launch_dependent(scan, dim3(s.nblk, s.B * s.Hkv), dim3(kThreads), smem_scan,
                                      st, ca);
     if (e != cudaSuccess) return e;
+    return launch_attend(q, q_bf16, centre, keys, values, kv_bf16, s, out, ws, st);
+}
+
+cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const void* keys,
+                          const void* values, bool kv_bf16, const DecodeShape& s, float* out,
+                          const DecodeScratch& ws, cudaStream_t st) {
+    const int G = s.Hq / s.Hkv;
+    AttendFn attend = pick_attend(kv_bf16);
+    const size_t smem_att = attend_smem_for(s.nblk);
+    if (smem_att > kMaxSmem) return cudaErrorNotSupported;
     AArgs aa;
     aa.selmask = ws.selmask;
     aa.qstat = ws.qstat;

@@ -14,6 +14,7 @@ constexpr int kWordsPerBlock = kKeysPerBlock / 32;  // uint32 words per plane ro
 constexpr int kD = 128;                             // the only head dimension supported
 constexpr int kAttendBlockGroup = 4;                // 1024-key blocks per attend CTA
 constexpr int kLogUTableIntervals = 4096;           // log u table over the cosine in [-1, 1]
+constexpr int kMaxBucketBits = 12;                  // bucketed tables: at most 2^12 buckets a table
 
 // Partial softmax states per query row: one per group of kAttendBlockGroup blocks (sampled
 // keys) plus one for the exact sink/local set.
@@ -33,6 +34,7 @@ struct DecodeScratch {
     float* po;           // [B*Hq][nsp][128] its weighted value sum
     unsigned* counters;  // [B*Hq] attend CTAs finished, for the last one's merge
     uint32_t* selmask;   // [B*Hq][nblk][32] selection words, written by the scan kernel
+    uint32_t* sel_ge1;   // [B*Hq][nblk][32] keys hit by >= 1 table (bucketed lookup only)
     float* logu_tab;     // [kLogUTableIntervals + 1] log u at cosines -1 + 2 i / intervals
 };
 
@@ -67,6 +69,20 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
                            bool kv_bf16, const DecodeShape& s, float* out,
                            const DecodeScratch& ws, cudaStream_t st);
 bool decode_supported(const DecodeShape& s, bool kv_bf16);
+// the attend kernel alone, on selection words already in ws.selmask (masked with valid & not T)
+cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const void* keys,
+                          const void* values, bool kv_bf16, const DecodeShape& s, float* out,
+                          const DecodeScratch& ws, cudaStream_t st);
+
+// ---- bucketed hash tables (mp_buckets.cu) ------------------------------------------------------
+size_t bucket_table_bytes(int B, int Hkv, int n, int K, int L);   // 0 if unsupported
+cudaError_t launch_bucket_build(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
+                                uint32_t* buckets, cudaStream_t st);
+// ge1 / ge2 bitmaps of the query rows' bucket hits, in the selection-word layout
+cudaError_t launch_bucket_lookup(const uint32_t* buckets, const uint32_t* qbits,
+                                 const DecodeShape& s, uint32_t* ge1, uint32_t* ge2,
+                                 cudaStream_t st);
+cudaError_t prepare_buckets();
 
 cudaError_t launch_compact_selection(const uint32_t* selmask, int rows, int n, int nblk,
                                      int32_t* sel_idx, int32_t* sel_count, cudaStream_t st);
