@@ -52,6 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-buckets", action="store_true",
+                    help="skip the bucketed-table retrieval measurement")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of as one captured CUDA graph")
     return ap.parse_args(argv)
@@ -226,6 +228,87 @@ def run_step(mp, wl, W, state, ws_mean, ws_dec, stream, marks=None):
                              wl.n_local, s.out, ws_dec, stream=stream)
         if ev:
             ev[4].record(stream)
+
+
+def run_buckets(mp, wl, W, state, ws_dec, steps: int, use_graph: bool, peaks):
+    """The bucketed-table retrieval (mp_build_buckets + mp_sampled_attention_buckets) on the same
+    layers: build time per layer, then K decode steps (query encode + bucket lookup + gather /
+    weight / merge over every layer), CUDA events around each layer's sampled attention."""
+    nbytes = mp.buckets_bytes(wl.B, wl.Hkv, wl.n, wl.K, wl.L)
+    if nbytes == 0:
+        return None
+    dev = state[0].keys.device
+    tables = [torch.empty(nbytes // 4, dtype=torch.int32, device=dev) for _ in state]
+    build = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in state]
+    stream = torch.cuda.current_stream()
+    for rnd in range(2):                              # the second round is the one timed
+        for s, t, ev in zip(state, tables, build):
+            ev[0].record(stream)
+            mp.build_buckets(s.codes, wl.B, wl.Hkv, wl.n, wl.K, wl.L, buckets=t, stream=stream)
+            ev[1].record(stream)
+    torch.cuda.synchronize()
+    build_us = statistics.median(e0.elapsed_time(e1) * 1e3 for e0, e1 in build)
+
+    def step(marks, strm):
+        for li, (s, t) in enumerate(zip(state, tables)):
+            mp.encode_query(s.q, s.centre, W, s.keys.shape, wl.K, wl.L, wl.n_sink, wl.n_local,
+                            ws_dec, stream=strm)
+            if marks is not None:
+                marks[li][0].record(strm)
+            mp.sampled_attention_buckets(s.q, t, s.centre, s.keys, s.values, wl.K, wl.L,
+                                         wl.n_sink, wl.n_local, s.out, ws_dec, stream=strm)
+            if marks is not None:
+                marks[li][1].record(strm)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True, external=use_graph) if use_graph \
+            else torch.cuda.Event(enable_timing=True)
+    marks = [[[ev(), ev()] for _ in state] for _ in range(steps)]
+    for _ in range(3):
+        step(None, stream)
+    torch.cuda.synchronize()
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream()
+            for k in range(steps):
+                step(marks[k], cap)
+    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    begin.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for k in range(steps):
+            step(marks[k], stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    assert mp.device_status() == 0
+    ms_step = begin.elapsed_time(end) / steps
+    sa_us = sum(m[0].elapsed_time(m[1]) for sm in marks for m in sm) * 1e3 / (steps * len(state))
+
+    # bytes the lookup reads: every query row's bucket in each table (from the library's own
+    # query bits and the bucket offsets), plus the offsets it reads
+    nb = 1 << wl.K
+    scanned = []
+    for s, t in zip(state, tables):
+        d = mp.debug_select(s.q, s.codes, s.centre, W, s.keys, s.values, wl.K, wl.L, wl.n_sink,
+                            wl.n_local, counts=False)
+        bits = d["q_bits"].reshape(wl.B, wl.Hq, -1).to(torch.int64) & 0xffffffff
+        pos = torch.arange(wl.K * wl.L, device=dev)
+        qb = (bits[..., pos // 32] >> (pos % 32)) & 1                  # [B, Hq, C]
+        code = (qb.reshape(wl.B, wl.Hq, wl.L, wl.K) << torch.arange(wl.K, device=dev)).sum(-1)
+        off = t[:wl.B * wl.Hkv * wl.L * (nb + 1 + wl.n)].reshape(wl.B * wl.Hkv, -1)
+        off = off[:, :wl.L * (nb + 1)].reshape(wl.B, wl.Hkv, wl.L, nb + 1).to(torch.int64)
+        off = off.repeat_interleave(wl.G, dim=1)                         # per query head
+        lo = torch.gather(off, 3, code.unsqueeze(-1)).squeeze(-1)
+        hi = torch.gather(off, 3, (code + 1).unsqueeze(-1)).squeeze(-1)
+        scanned.append(float((hi - lo).sum(-1).double().mean()))
+    return {"build_us_per_layer": build_us, "tables_bytes_per_layer": nbytes,
+            "decode_ms_per_step": ms_step, "sampled_attention_us_per_layer": sa_us,
+            "scanned_entries_per_query": statistics.mean(scanned)}
 
 
 def sample_set_sizes(mp, wl, W, state):
@@ -502,6 +585,33 @@ def run_ours(args):
         "clocks": clk,
     }
 
+    if not args.no_buckets:
+        bk = run_buckets(mp, wl, W, state, ws_dec, args.steps, use_graph, peaks)
+        if bk is not None:
+            es = 2 if wl.kv_dtype == torch.bfloat16 else 4
+            qs = 2 if wl.q_dtype == torch.bfloat16 else 4
+            units = wl.B * wl.Hkv
+            n_exact = min(wl.n, wl.n_sink + wl.n_local)
+            rows_bytes = units * (alg["mean_union_rows"] + n_exact) * 2 * wl.d * es
+            look_bytes = wl.B * wl.Hq * (bk["scanned_entries_per_query"] + 2 * wl.L) * 4
+            sa_bytes = look_bytes + rows_bytes + wl.B * wl.Hq * wl.d * (qs + 4)
+            sa_gbs = sa_bytes / (bk["sampled_attention_us_per_layer"] * 1e-6) / 1e9
+            build_bytes = 2 * units * wl.n * wl.C / 8 + bk["tables_bytes_per_layer"]
+            line["buckets"] = {
+                "what": "mp_build_buckets + mp_sampled_attention_buckets (the pages' bucketed "
+                        "retrieval) on the same layers; bit-identical outputs to the code scan",
+                "decode_queries_per_s": world * queries_per_step /
+                                        ((bk["decode_ms_per_step"]) / 1e3),
+                "decode_ms_per_token": bk["decode_ms_per_step"],
+                "sampled_attention_us_per_layer": bk["sampled_attention_us_per_layer"],
+                "sampled_attention_gbs": sa_gbs,
+                "sampled_attention_frac": sa_gbs / peaks["hbm_gbs"],
+                "sampled_attention_bytes_per_layer": sa_bytes,
+                "scanned_entries_per_query": bk["scanned_entries_per_query"],
+                "build_us_per_layer": bk["build_us_per_layer"],
+                "build_gbs": build_bytes / (bk["build_us_per_layer"] * 1e-6) / 1e9,
+                "tables_bytes_per_layer": bk["tables_bytes_per_layer"],
+            }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(wl, state, W, args.cpu_seconds)
     if not args.no_e2e:
