@@ -300,7 +300,7 @@ def run_buckets(mp, wl, W, state, ws_dec, steps: int, use_graph: bool, peaks):
         pos = torch.arange(wl.K * wl.L, device=dev)
         qb = (bits[..., pos // 32] >> (pos % 32)) & 1                  # [B, Hq, C]
         code = (qb.reshape(wl.B, wl.Hq, wl.L, wl.K) << torch.arange(wl.K, device=dev)).sum(-1)
-        off = t[:wl.B * wl.Hkv * wl.L * (nb + 1 + wl.n)].reshape(wl.B * wl.Hkv, -1)
+        off = t[:wl.B * wl.Hkv * wl.L * (nb + 1 + wl.n + 8 * nb)].reshape(wl.B * wl.Hkv, -1)
         off = off[:, :wl.L * (nb + 1)].reshape(wl.B, wl.Hkv, wl.L, nb + 1).to(torch.int64)
         off = off.repeat_interleave(wl.G, dim=1)                         # per query head
         lo = torch.gather(off, 3, code.unsqueeze(-1)).squeeze(-1)

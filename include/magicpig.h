@@ -164,10 +164,10 @@ MP_API mp_status mp_sampled_attention(const void* q, mp_dtype q_dtype, const uin
  * system co-design item 3: the query's codes are looked up in L prebuilt hash tables; "don't pick
  * the tallest", section 6: every table stores a pointer to every key, and a query scans about
  * L n / 2^K entries). Layout per (sequence, KV head), 32-bit words: offsets[L][2^K + 1], then
- * members[L][n]; members[t][offsets[t][c] .. offsets[t][c+1]) are the keys with code c in table
- * t. The order inside a bucket is not fixed (a bucket is a set).
- * mp_buckets_bytes: bytes for B*Hkv such tables (L (2^K + 1 + n) words each); 0 if K > 12 or the
- * shapes are invalid. */
+ * members[L][n], then the build's scratch [L][8][2^K]; members[t][offsets[t][c] .. offsets[t][c+1])
+ * are the keys with code c in table t. The order inside a bucket is not fixed (a bucket is a set).
+ * mp_buckets_bytes: bytes for B*Hkv such tables (L (2^K + 1 + n + 8 * 2^K) words each); 0 if
+ * K > 12 or the shapes are invalid. */
 MP_API size_t mp_buckets_bytes(int B, int Hkv, int n, int K, int L);
 
 /* Build the bucketed tables from the packed codes of mp_build_tables (same B, Hkv, n, K, L).

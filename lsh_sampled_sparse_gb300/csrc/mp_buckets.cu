@@ -3,13 +3,17 @@
 // tables) and of "MagicPIG: don't pick the tallest" (section 6: every table stores a pointer to
 // every key; a query scans about L n / 2^K entries).
 //
-// Layout per (sequence, KV head), in 32-bit words: offsets [L][2^K + 1], then members [L][n];
+// Layout per (sequence, KV head), in 32-bit words: offsets [L][2^K + 1], then members [L][n],
+// then the build's scratch [L][kBucketRanges][2^K];
 // members[t][offsets[t][c] .. offsets[t][c + 1]) are the keys whose table-t code is c. The order
 // of keys inside a bucket is not fixed (buckets are sets); everything that reads them only counts.
 //
-// Build: one CTA per (table, sequence x KV head) reads that table's K plane rows of every
-// 1024-key block twice: the first pass counts codes in a shared-memory histogram, an exclusive
-// scan turns the counts into offsets, the second pass places each key at its bucket's cursor.
+// Build, three kernels over (table, sequence x KV head) split into kBucketRanges key ranges:
+// each range counts its codes (shared-memory histogram), one CTA per table turns the counts into
+// offsets and per-range write bases (an exclusive scan over codes, ranges in order within a
+// code), and each range places its keys at its bases. The ranges of one table run side by side,
+// so the table's members array (n words) stays in L2 while it fills. The counts and bases live
+// in kBucketRanges * 2^K scratch words per table after the members.
 // Lookup: one CTA per (query row, chunk of tables) reads the query's bucket in each table and
 // sets the key's bit in two saturating bitmaps, ge1 (>= 1 table) and ge2 (>= 2 tables), stored in
 // the selection-word layout of the dense scan ([row][block][32 words]).
@@ -21,79 +25,116 @@ namespace {
 constexpr int kBuildThreads = 256;
 constexpr int kLookupThreads = 256;
 constexpr int kLookupTables = 8;      // tables per lookup CTA
+constexpr int kStageBlocks = 4;       // 1024-key blocks whose plane rows a build CTA stages at once
+constexpr int kStageRow = kWordsPerBlock + 1;   // staged plane row stride (words): lanes reading
+                                                // word w of planes 0..K-1 hit distinct banks
 
-__device__ __forceinline__ size_t bucket_words(int n, int K, int L) {
-    return static_cast<size_t>(L) * ((1u << K) + 1 + static_cast<size_t>(n));
+// words per (sequence, KV head): offsets, members, then the build's per-range counts / bases
+__host__ __device__ __forceinline__ size_t bucket_words(int n, int K, int L) {
+    const size_t nb = static_cast<size_t>(1) << K;
+    return static_cast<size_t>(L) * ((nb + 1) + static_cast<size_t>(n) + kBucketRanges * nb);
 }
 
-// code of key `i` of the staged block (plane p of the table is the 32-word row planes[p])
-__device__ __forceinline__ uint32_t key_code(const uint32_t* planes, int K, int i) {
-    const int w = i >> 5, b = i & 31;
-    uint32_t c = 0u;
-    for (int p = 0; p < K; ++p) c |= ((planes[p * kWordsPerBlock + w] >> b) & 1u) << p;
-    return c;
+// Walk the keys of key range `range` of table t: stage kStageBlocks blocks' plane rows at a
+// time (row stride kStageRow); then each warp takes 32-key words: lane p < K holds plane p's word, and one 32x32 bit
+// transpose leaves in lane j the K-bit code of the word's key j. f(key, code) is called by the
+// lane of every key (keys past n are skipped).
+template <typename F>
+__device__ __forceinline__ void for_range_keys(const uint32_t* codes, int bh, int t, int range,
+                                              int n, int K, int L, int nblk, uint32_t* stage,
+                                              F&& f) {
+    const int C = K * L, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b0 = (nblk * range) / kBucketRanges, b1 = (nblk * (range + 1)) / kBucketRanges;
+    const int rowsz = K * kWordsPerBlock, srow = K * kStageRow;
+    for (int blk = b0; blk < b1; blk += kStageBlocks) {
+        const int nbk = min(kStageBlocks, b1 - blk);
+        __syncthreads();                          // the previous stage is consumed
+        for (int i = tid; i < nbk * rowsz; i += kBuildThreads) {
+            const int kb = i / rowsz, w = i % rowsz;
+            stage[kb * srow + (w / kWordsPerBlock) * kStageRow + w % kWordsPerBlock] =
+                __ldcs(codes + (static_cast<size_t>(bh) * nblk + blk + kb) * C * kWordsPerBlock +
+                       static_cast<size_t>(t) * rowsz + w);
+        }
+        __syncthreads();
+        for (int wi = warp; wi < nbk * kWordsPerBlock; wi += kBuildThreads / 32) {
+            const int kb = wi / kWordsPerBlock, w = wi % kWordsPerBlock;
+            const uint32_t x = lane < K ? stage[kb * srow + lane * kStageRow + w] : 0u;
+            const uint32_t code = warp_transpose32(x, lane);
+            const int key = (blk + kb) * kKeysPerBlock + w * 32 + lane;
+            if (key < n) f(key, code);
+        }
+    }
 }
 
+// 1. per key range: its count of every code -> scratch[t][range][c]
 __global__ void __launch_bounds__(kBuildThreads)
-    bucket_build_kernel(const uint32_t* codes, int n, int K, int L, int nblk, uint32_t* buckets) {
+    bucket_count_kernel(const uint32_t* codes, int n, int K, int L, int nblk, uint32_t* buckets) {
     extern __shared__ __align__(16) uint32_t sm[];
-    const int nb = 1 << K;
-    uint32_t* hist = sm;                          // [2^K] counts, then cursors
-    uint32_t* planes = sm + nb;                   // [K][32] one block's plane rows of this table
+    const int nb = 1 << K, range = blockIdx.x, t = blockIdx.y, bh = blockIdx.z;
+    uint32_t* hist = sm;
+    uint32_t* stage = sm + nb;
+    for (int c = threadIdx.x; c < nb; c += kBuildThreads) hist[c] = 0u;
+    for_range_keys(codes, bh, t, range, n, K, L, nblk, stage,
+                   [&](int, uint32_t c) { atomicAdd(&hist[c], 1u); });
+    __syncthreads();
+    uint32_t* scratch = buckets + static_cast<size_t>(bh) * bucket_words(n, K, L) +
+                        static_cast<size_t>(L) * ((nb + 1) + static_cast<size_t>(n)) +
+                        (static_cast<size_t>(t) * kBucketRanges + range) * nb;
+    for (int c = threadIdx.x; c < nb; c += kBuildThreads) scratch[c] = hist[c];
+}
+
+// 2. per table: offsets = exclusive scan over codes of the total counts; each range's count is
+//    replaced by its write base: offsets[c] + the counts of the lower ranges for code c
+__global__ void __launch_bounds__(kBuildThreads)
+    bucket_scan_kernel(int n, int K, int L, uint32_t* buckets) {
     __shared__ uint32_t wsum[kBuildThreads / 32];
-    const int t = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x, lane = tid & 31,
-              warp = tid >> 5;
-    const int C = K * L;
+    const int nb = 1 << K, t = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     uint32_t* base = buckets + static_cast<size_t>(bh) * bucket_words(n, K, L);
     uint32_t* offsets = base + static_cast<size_t>(t) * (nb + 1);
-    uint32_t* members = base + static_cast<size_t>(L) * (nb + 1) + static_cast<size_t>(t) * n;
-    for (int c = tid; c < nb; c += kBuildThreads) hist[c] = 0u;
-
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int blk = 0; blk < nblk; ++blk) {
-            __syncthreads();                      // previous block's planes fully consumed
-            const uint32_t* rows = codes + (static_cast<size_t>(bh) * nblk + blk) * C * kWordsPerBlock +
-                                   static_cast<size_t>(t) * K * kWordsPerBlock;
-            for (int i = tid; i < K * kWordsPerBlock; i += kBuildThreads) planes[i] = __ldcs(rows + i);
-            __syncthreads();
-            for (int i = tid; i < kKeysPerBlock; i += kBuildThreads) {
-                const int key = blk * kKeysPerBlock + i;
-                if (key >= n) break;
-                const uint32_t c = key_code(planes, K, i);
-                if (pass == 0) {
-                    atomicAdd(&hist[c], 1u);
-                } else {
-                    const uint32_t pos = atomicAdd(&hist[c], 1u);
-                    members[pos] = static_cast<uint32_t>(key);
-                }
-            }
-        }
-        if (pass == 1) break;
-        // exclusive scan of the counts: thread tid owns a contiguous run of buckets
-        __syncthreads();
-        const int per = (nb + kBuildThreads - 1) / kBuildThreads;
-        const int c0 = min(nb, tid * per), c1 = min(nb, c0 + per);
-        uint32_t run = 0u;
-        for (int c = c0; c < c1; ++c) run += hist[c];
-        uint32_t incl = run;
+    uint32_t* scratch = base + static_cast<size_t>(L) * ((nb + 1) + static_cast<size_t>(n)) +
+                        static_cast<size_t>(t) * kBucketRanges * nb;
+    const int per = (nb + kBuildThreads - 1) / kBuildThreads;
+    const int c0 = min(nb, tid * per), c1 = min(nb, c0 + per);
+    uint32_t run = 0u;
+    for (int c = c0; c < c1; ++c)
+        for (int r = 0; r < kBucketRanges; ++r) run += scratch[r * nb + c];
+    uint32_t incl = run;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) wsum[warp] = incl;
-        __syncthreads();
-        uint32_t before = 0u;
-        for (int w = 0; w < warp; ++w) before += wsum[w];
-        uint32_t acc = before + incl - run;
-        for (int c = c0; c < c1; ++c) {
-            const uint32_t cnt = hist[c];
-            offsets[c] = acc;
-            hist[c] = acc;                        // cursor for the second pass
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    uint32_t acc = incl - run;
+    for (int w = 0; w < warp; ++w) acc += wsum[w];
+    for (int c = c0; c < c1; ++c) {
+        offsets[c] = acc;
+        for (int r = 0; r < kBucketRanges; ++r) {
+            const uint32_t cnt = scratch[r * nb + c];
+            scratch[r * nb + c] = acc;
             acc += cnt;
         }
-        if (tid == kBuildThreads - 1) offsets[nb] = acc;
     }
+    if (tid == kBuildThreads - 1) offsets[nb] = acc;
+}
+
+// 3. per key range: every key to its bucket, from the range's base (cursors in shared memory)
+__global__ void __launch_bounds__(kBuildThreads)
+    bucket_scatter_kernel(const uint32_t* codes, int n, int K, int L, int nblk, uint32_t* buckets) {
+    extern __shared__ __align__(16) uint32_t sm[];
+    const int nb = 1 << K, range = blockIdx.x, t = blockIdx.y, bh = blockIdx.z;
+    uint32_t* cursor = sm;
+    uint32_t* stage = sm + nb;
+    uint32_t* base = buckets + static_cast<size_t>(bh) * bucket_words(n, K, L);
+    const uint32_t* scratch = base + static_cast<size_t>(L) * ((nb + 1) + static_cast<size_t>(n)) +
+                              (static_cast<size_t>(t) * kBucketRanges + range) * nb;
+    uint32_t* members = base + static_cast<size_t>(L) * (nb + 1) + static_cast<size_t>(t) * n;
+    for (int c = threadIdx.x; c < nb; c += kBuildThreads) cursor[c] = scratch[c];
+    for_range_keys(codes, bh, t, range, n, K, L, nblk, stage, [&](int key, uint32_t c) {
+        members[atomicAdd(&cursor[c], 1u)] = static_cast<uint32_t>(key);
+    });
 }
 
 // the K-bit code of table t in a row of query bits
@@ -135,16 +176,22 @@ __global__ void __launch_bounds__(kLookupThreads)
 
 size_t bucket_table_bytes(int B, int Hkv, int n, int K, int L) {
     if (B < 1 || Hkv < 1 || n < 1 || K < 0 || K > kMaxBucketBits || L < 1) return 0;
-    return static_cast<size_t>(B) * Hkv * static_cast<size_t>(L) *
-           ((static_cast<size_t>(1) << K) + 1 + static_cast<size_t>(n)) * 4;
+    return static_cast<size_t>(B) * Hkv * bucket_words(n, K, L) * 4;
 }
 
 cudaError_t launch_bucket_build(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
                                 uint32_t* buckets, cudaStream_t st) {
     const int nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
-    const size_t smem = (static_cast<size_t>(1) << K) * 4 + static_cast<size_t>(K) * kWordsPerBlock * 4;
-    bucket_build_kernel<<<dim3(L, B * Hkv), kBuildThreads, smem, st>>>(codes, n, K, L, nblk,
-                                                                       buckets);
+    const size_t smem = (static_cast<size_t>(1) << K) * 4 +
+                        static_cast<size_t>(kStageBlocks) * K * kStageRow * 4;
+    const dim3 ranges(kBucketRanges, L, B * Hkv);   // the ranges of one table run side by side
+    bucket_count_kernel<<<ranges, kBuildThreads, smem, st>>>(codes, n, K, L, nblk, buckets);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bucket_scan_kernel<<<dim3(L, B * Hkv), kBuildThreads, 0, st>>>(n, K, L, buckets);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bucket_scatter_kernel<<<ranges, kBuildThreads, smem, st>>>(codes, n, K, L, nblk, buckets);
     return cudaGetLastError();
 }
 
@@ -164,8 +211,10 @@ cudaError_t launch_bucket_lookup(const uint32_t* buckets, const uint32_t* qbits,
 
 cudaError_t prepare_buckets() {
     cudaFuncAttributes fa;
-    cudaError_t e = cudaFuncGetAttributes(&fa, bucket_build_kernel);
+    cudaError_t e = cudaFuncGetAttributes(&fa, bucket_count_kernel);
     if (e != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, bucket_scan_kernel)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, bucket_scatter_kernel)) != cudaSuccess) return e;
     return cudaFuncGetAttributes(&fa, bucket_lookup_kernel);
 }
 

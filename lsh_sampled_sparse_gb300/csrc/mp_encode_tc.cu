@@ -198,24 +198,6 @@ __device__ __forceinline__ uint32_t pack_signs(const uint32_t (&v)[32]) {
 }
 // 32x32 bit-matrix transpose across a warp: on entry bit b of lane r is element (r, b); on exit
 // bit r of lane b is that element. Each stage swaps the off-diagonal s x s blocks.
-// Lanes without bit s of their index keep the positions b with (b & s) == 0 and take the
-// partner's such bits moved up by s; lanes with bit s keep the others and take the partner's
-// moved down by s. A rotation does both moves (the bits it wraps around are masked off), so a
-// stage is one shuffle, one funnel shift and one three-input logic op.
-__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
-    const uint32_t low[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
-#pragma unroll
-    for (int i = 0; i < 5; ++i) {
-        const int s = 16 >> i;
-        const bool up = (lane & s) != 0;
-        const uint32_t keep = up ? ~low[i] : low[i];
-        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
-        const uint32_t r = __funnelshift_l(y, y, up ? 32 - s : s);   // rotate left
-        x = (x & keep) | (r & ~keep);
-    }
-    return x;
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     encode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const EncodeArgs a) {
     extern __shared__ uint8_t smem_raw[];

@@ -15,6 +15,7 @@ constexpr int kD = 128;                             // the only head dimension s
 constexpr int kAttendBlockGroup = 4;                // 1024-key blocks per attend CTA
 constexpr int kLogUTableIntervals = 4096;           // log u table over the cosine in [-1, 1]
 constexpr int kMaxBucketBits = 12;                  // bucketed tables: at most 2^12 buckets a table
+constexpr int kBucketRanges = 8;                    // key ranges a table's bucket build is split into
 
 // Partial softmax states per query row: one per group of kAttendBlockGroup blocks (sampled
 // keys) plus one for the exact sink/local set.
@@ -104,6 +105,26 @@ __device__ __forceinline__ float to_float(__nv_bfloat16 x) { return __bfloat162f
 __device__ __forceinline__ float load_elem(const void* p, bool bf16, size_t i) {
     return bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i])
                 : reinterpret_cast<const float*>(p)[i];
+}
+
+// 32x32 bit-matrix transpose across a warp: on entry bit b of lane r is element (r, b); on exit
+// bit r of lane b is that element. Each stage swaps the off-diagonal s x s blocks.
+// Lanes without bit s of their index keep the positions b with (b & s) == 0 and take the
+// partner's such bits moved up by s; lanes with bit s keep the others and take the partner's
+// moved down by s. A rotation does both moves (the bits it wraps around are masked off), so a
+// stage is one shuffle, one funnel shift and one three-input logic op.
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+    const uint32_t low[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        const int s = 16 >> i;
+        const bool up = (lane & s) != 0;
+        const uint32_t keep = up ? ~low[i] : low[i];
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
+        const uint32_t r = __funnelshift_l(y, y, up ? 32 - s : s);   // rotate left
+        x = (x & keep) | (r & ~keep);
+    }
+    return x;
 }
 
 // bits of a 32-key word whose offset within the word is below x (x may be out of [0, 32])

@@ -39,10 +39,10 @@ def _setup(mp, wl, layer=0):
 
 def _unpack_buckets(buckets, B, Hkv, n, K, L):
     nb = 1 << K
-    per = L * (nb + 1 + n)
+    per = L * (nb + 1 + n + 8 * nb)               # offsets, members, build scratch
     flat = buckets.cpu().numpy().astype(np.int64)[:B * Hkv * per].reshape(B * Hkv, per)
     offsets = flat[:, :L * (nb + 1)].reshape(B * Hkv, L, nb + 1)
-    members = flat[:, L * (nb + 1):].reshape(B * Hkv, L, n)
+    members = flat[:, L * (nb + 1):L * (nb + 1 + n)].reshape(B * Hkv, L, n)
     return offsets, members
 
 
