@@ -8,15 +8,20 @@
 // members[t][offsets[t][c] .. offsets[t][c + 1]) are the keys whose table-t code is c. The order
 // of keys inside a bucket is not fixed (buckets are sets); everything that reads them only counts.
 //
-// Build, three kernels over (table, sequence x KV head) split into kBucketRanges key ranges:
-// each range counts its codes (shared-memory histogram), one CTA per table turns the counts into
-// offsets and per-range write bases (an exclusive scan over codes, ranges in order within a
-// code), and each range places its keys at its bases. The ranges of one table run side by side,
-// so the table's members array (n words) stays in L2 while it fills. The counts and bases live
-// in kBucketRanges * 2^K scratch words per table after the members.
+// Build, one kernel: a cluster of kBucketRanges CTAs per (table, sequence x KV head), each CTA
+// one key range. A CTA stages its range's plane rows, counts its codes in a shared-memory
+// histogram (the count's old value is the key's rank among the range's keys of that code), reads
+// the other ranges' histograms through distributed shared memory to get the table's offsets and
+// its own write base per code, sorts its keys by code in shared memory and writes them out in
+// runs, so a bucket's part from one range is one contiguous store. Ranges too large for shared
+// memory (very long contexts) take three kernels instead: per-range counts to the scratch words,
+// one CTA per table scanning them into offsets and write bases, and a scatter with one shared
+// atomic per key; the scratch [kBucketRanges][2^K] per table after the members serves them.
 // Lookup: one CTA per (query row, chunk of tables) reads the query's bucket in each table and
 // sets the key's bit in two saturating bitmaps, ge1 (>= 1 table) and ge2 (>= 2 tables), stored in
 // the selection-word layout of the dense scan ([row][block][32 words]).
+#include <cooperative_groups.h>
+
 #include "mp_internal.cuh"
 
 namespace mp {
@@ -26,6 +31,9 @@ constexpr int kBuildThreads = 256;
 constexpr int kLookupThreads = 256;
 constexpr int kLookupTables = 8;      // tables per lookup CTA
 constexpr int kStageBlocks = 4;       // 1024-key blocks whose plane rows a build CTA stages at once
+constexpr size_t kClusterBuildSmem = 200 * 1024;   // dynamic shared memory of a cluster-build CTA
+constexpr int kClusterThreads = 512;  // threads of a cluster-build CTA
+constexpr int kWordsAtOnce = 4;       // 32-key words a cluster-build warp decodes together
 constexpr int kStageRow = kWordsPerBlock + 1;   // staged plane row stride (words): lanes reading
                                                 // word w of planes 0..K-1 hit distinct banks
 
@@ -137,6 +145,182 @@ __global__ void __launch_bounds__(kBuildThreads)
     });
 }
 
+// warp_transpose32 of U independent words, interleaved so that their shuffles overlap
+template <int U>
+__device__ __forceinline__ void warp_transpose32_x(uint32_t (&x)[U], int lane) {
+    const uint32_t low[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+        const int s = 16 >> i;
+        const bool up = (lane & s) != 0;
+        const uint32_t keep = up ? ~low[i] : low[i];
+        uint32_t y[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) y[u] = __shfl_xor_sync(0xffffffffu, x[u], s);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t r = __funnelshift_l(y[u], y[u], up ? 32 - s : s);
+            x[u] = (x[u] & keep) | (r & ~keep);
+        }
+    }
+}
+
+// Codes of the staged 32-key words w0 .. w0 + U - 1 (lane j gets key j's code of each word;
+// words at or past nw give 0). Plane rows are kStageRow words apart, blocks srow words apart.
+template <int U>
+__device__ __forceinline__ void staged_codes(const uint32_t* stage, int w0, int nw, int K,
+                                             int srow, int lane, uint32_t (&x)[U]) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int wi = w0 + u;
+        x[u] = (lane < K && wi < nw)
+                   ? stage[(wi / kWordsPerBlock) * srow + lane * kStageRow + wi % kWordsPerBlock]
+                   : 0u;
+    }
+    warp_transpose32_x<U>(x, lane);
+}
+
+// In-place exclusive prefix sum of v[0, nb) by the whole CTA of T threads; wsum holds T / 32
+// words. Ends with a barrier.
+template <int T>
+__device__ void block_exclusive_scan(uint32_t* v, int nb, uint32_t* wsum) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (nb + T - 1) / T;
+    const int c0 = min(nb, tid * per), c1 = min(nb, c0 + per);
+    uint32_t run = 0u;
+    for (int c = c0; c < c1; ++c) run += v[c];
+    uint32_t incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    uint32_t acc = incl - run;
+    for (int w = 0; w < warp; ++w) acc += wsum[w];
+    for (int c = c0; c < c1; ++c) {
+        const uint32_t x = v[c];
+        v[c] = acc;
+        acc += x;
+    }
+    __syncthreads();
+}
+
+// Shared memory of the cluster build for ranges of at most `rb` blocks, in bytes: three code
+// arrays, then per key the (code, rank) word and the sorted (code, key) word; the staged plane
+// rows share the sorted words' space (they are dead once every key has its code and rank).
+__host__ __device__ __forceinline__ size_t cluster_build_smem(int rb, int K) {
+    const size_t nb = static_cast<size_t>(1) << K;
+    const size_t keys = static_cast<size_t>(rb) * kKeysPerBlock;
+    const size_t stage = static_cast<size_t>(rb) * K * kStageRow;
+    return (3 * nb + keys + (stage > keys ? stage : keys)) * 4;
+}
+
+// One CTA per key range, kBucketRanges CTAs (a cluster) per table. Each warp takes kWordsAtOnce
+// 32-key words at a time so that their shuffles and shared atomics overlap.
+__global__ void __cluster_dims__(kBucketRanges, 1, 1) __launch_bounds__(kClusterThreads)
+    bucket_build_cluster_kernel(const uint32_t* codes, int n, int K, int L, int nblk,
+                                uint32_t* buckets) {
+    namespace cg = cooperative_groups;
+    constexpr int T = kClusterThreads, U = kWordsAtOnce;
+    cg::cluster_group cluster = cg::this_cluster();
+    extern __shared__ __align__(16) uint32_t sm[];
+    __shared__ uint32_t wsum[T / 32];
+    const int nb = 1 << K, r = static_cast<int>(cluster.block_rank()), t = blockIdx.y,
+              bh = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rb = (nblk + kBucketRanges - 1) / kBucketRanges;
+    const int b0 = (nblk * r) / kBucketRanges, b1 = (nblk * (r + 1)) / kBucketRanges;
+    const int nbk = b1 - b0, nw = nbk * kWordsPerBlock, k0 = b0 * kKeysPerBlock;
+    const int m = max(0, min(n, b1 * kKeysPerBlock) - k0);        // keys of this range
+    const int C = K * L, srow = K * kStageRow;
+    uint32_t* hist = sm;                   // [nb] this range's count of each code
+    uint32_t* total = sm + nb;             // [nb] the table's count, then its offsets
+    uint32_t* delta = sm + 2 * nb;         // [nb] lower ranges' count, then output - sorted pos
+    uint32_t* crank = sm + 3 * nb;         // [rb * 1024] (code << 16) | rank, by key
+    uint32_t* ent = crank + static_cast<size_t>(rb) * kKeysPerBlock;   // sorted (code << 16) | key
+    uint32_t* stage = ent;                 // [rb][K][kStageRow] the range's plane rows (pass 1)
+
+    for (int c = tid; c < nb; c += T) hist[c] = 0u;
+    {   // plane rows as 16-byte loads: row j = kb * K + p is staged at j * kStageRow
+        const int per = K * (kWordsPerBlock / 4);
+        const uint32_t* src = codes + (static_cast<size_t>(bh) * nblk + b0) * C * kWordsPerBlock +
+                              static_cast<size_t>(t) * K * kWordsPerBlock;
+        for (int j = tid; j < nbk * per; j += T) {
+            const int kb = j / per, q = j - kb * per;        // q: plane * 8 + 16-byte chunk
+            const uint4 v = __ldcs(reinterpret_cast<const uint4*>(
+                src + static_cast<size_t>(kb) * C * kWordsPerBlock) + q);
+            uint32_t* d = stage + (kb * K + (q >> 3)) * kStageRow + (q & 7) * 4;
+            d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+        }
+    }
+    __syncthreads();
+    // pass 1: count; the count before the key's own is its rank within (range, code)
+    for (int w0 = warp * U; w0 < nw; w0 += (T / 32) * U) {
+        uint32_t c[U], rk[U];
+        staged_codes<U>(stage, w0, nw, K, srow, lane, c);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            rk[u] = (w0 + u) * 32 + lane < m ? atomicAdd(&hist[c[u]], 1u) : 0u;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = (w0 + u) * 32 + lane;
+            if (i < m) crank[i] = (c[u] << 16) | rk[u];
+        }
+    }
+    cluster.sync();                        // every range's histogram is complete
+    for (int c = tid; c < nb; c += T) {
+        uint32_t v[kBucketRanges];
+#pragma unroll
+        for (int q = 0; q < kBucketRanges; ++q) v[q] = cluster.map_shared_rank(hist, q)[c];
+        uint32_t tot = 0u, pre = 0u;
+#pragma unroll
+        for (int q = 0; q < kBucketRanges; ++q) {
+            pre += q < r ? v[q] : 0u;
+            tot += v[q];
+        }
+        total[c] = tot;
+        delta[c] = pre;
+    }
+    cluster.sync();                        // no peer reads this CTA's histogram any more
+    block_exclusive_scan<T>(total, nb, wsum);                 // the table's offsets
+    uint32_t* base = buckets + static_cast<size_t>(bh) * bucket_words(n, K, L);
+    if (r == 0) {
+        uint32_t* offsets = base + static_cast<size_t>(t) * (nb + 1);
+        for (int c = tid; c < nb; c += T) offsets[c] = total[c];
+        if (tid == 0) offsets[nb] = static_cast<uint32_t>(n);
+    }
+    for (int c = tid; c < nb; c += T) delta[c] += total[c];   // this range's base
+    block_exclusive_scan<T>(hist, nb, wsum);                  // sorted start of each code
+    for (int c = tid; c < nb; c += T) delta[c] -= hist[c];
+    // pass 2: sort the range's keys by code in shared memory (the stage is dead)
+    for (int i0 = tid; i0 < m; i0 += T * U) {         // loads first, U keys a thread at once
+        uint32_t e[U], dst[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) e[u] = i0 + u * T < m ? crank[i0 + u * T] : 0u;
+#pragma unroll
+        for (int u = 0; u < U; ++u) dst[u] = hist[e[u] >> 16] + (e[u] & 0xffffu);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i0 + u * T < m) ent[dst[u]] = (e[u] & 0xffff0000u) | static_cast<uint32_t>(i0 + u * T);
+    }
+    __syncthreads();
+    // pass 3: sorted position p of code c goes to members[p + delta[c]]
+    uint32_t* members = base + static_cast<size_t>(L) * (nb + 1) + static_cast<size_t>(t) * n;
+    for (int p0 = tid; p0 < m; p0 += T * U) {
+        uint32_t e[U], dl[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) e[u] = p0 + u * T < m ? ent[p0 + u * T] : 0u;
+#pragma unroll
+        for (int u = 0; u < U; ++u) dl[u] = delta[e[u] >> 16];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (p0 + u * T < m)
+                members[p0 + u * T + dl[u]] = static_cast<uint32_t>(k0) + (e[u] & 0xffffu);
+    }
+}
+
 // the K-bit code of table t in a row of query bits
 __device__ __forceinline__ uint32_t query_code(const uint32_t* qb, int K, int t) {
     if (K == 0) return 0u;
@@ -182,9 +366,16 @@ size_t bucket_table_bytes(int B, int Hkv, int n, int K, int L) {
 cudaError_t launch_bucket_build(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
                                 uint32_t* buckets, cudaStream_t st) {
     const int nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
+    const dim3 ranges(kBucketRanges, L, B * Hkv);   // the ranges of one table run side by side
+    const int rb = (nblk + kBucketRanges - 1) / kBucketRanges;
+    const size_t csmem = cluster_build_smem(rb, K);
+    if (csmem <= kClusterBuildSmem && rb * kKeysPerBlock <= 65536) {
+        bucket_build_cluster_kernel<<<ranges, kClusterThreads, csmem, st>>>(codes, n, K, L, nblk,
+                                                                            buckets);
+        return cudaGetLastError();
+    }
     const size_t smem = (static_cast<size_t>(1) << K) * 4 +
                         static_cast<size_t>(kStageBlocks) * K * kStageRow * 4;
-    const dim3 ranges(kBucketRanges, L, B * Hkv);   // the ranges of one table run side by side
     bucket_count_kernel<<<ranges, kBuildThreads, smem, st>>>(codes, n, K, L, nblk, buckets);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -215,6 +406,10 @@ cudaError_t prepare_buckets() {
     if (e != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, bucket_scan_kernel)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, bucket_scatter_kernel)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(bucket_build_cluster_kernel,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kClusterBuildSmem))) != cudaSuccess)
+        return e;
     return cudaFuncGetAttributes(&fa, bucket_lookup_kernel);
 }
 

@@ -103,6 +103,15 @@ def test_buckets_degenerate_K0_and_single_table(mp):
         assert np.array_equal(out_scan, out_buck)
 
 
+def test_buckets_long_context_three_kernel_build(mp):
+    # ranges of 26+ blocks do not fit one CTA's shared memory: the counted three-kernel build
+    wl = small_workload(B=1, Hq=2, Hkv=1, n=210_000, K=10, L=3, kv_dtype=BF)
+    x, W, centre, codes = _setup(mp, wl)
+    buckets = _check_build(mp, wl, codes)
+    out_scan, out_buck = _decode_both(mp, wl, x, W, centre, codes, buckets)
+    assert np.array_equal(out_scan, out_buck)
+
+
 def test_buckets_reject_too_many_bits(mp):
     assert mp.buckets_bytes(1, 1, 1000, 13, 10) == 0
     with pytest.raises(ValueError):
