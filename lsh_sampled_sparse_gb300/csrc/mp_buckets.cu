@@ -17,8 +17,8 @@
 // memory (very long contexts) take three kernels instead: per-range counts to the scratch words,
 // one CTA per table scanning them into offsets and write bases, and a scatter with one shared
 // atomic per key; the scratch [kBucketRanges][2^K] per table after the members serves them.
-// Lookup: one CTA per (query row, chunk of tables) reads the query's bucket in each table and
-// sets the key's bit in two saturating bitmaps, ge1 (>= 1 table) and ge2 (>= 2 tables), stored in
+// Lookup: one warp per (query row, table) reads the query's bucket and sets each key's bit in
+// two saturating bitmaps, ge1 (>= 1 table) and ge2 (>= 2 tables), stored in
 // the selection-word layout of the dense scan ([row][block][32 words]).
 #include <cooperative_groups.h>
 
@@ -28,8 +28,8 @@ namespace mp {
 namespace {
 
 constexpr int kBuildThreads = 256;
-constexpr int kLookupThreads = 256;
-constexpr int kLookupTables = 8;      // tables per lookup CTA
+constexpr int kLookupWarps = 8;       // tables per lookup CTA, one warp each
+constexpr int kLookupUnroll = 4;      // bucket entries a lookup lane loads before its atomics
 constexpr int kStageBlocks = 4;       // 1024-key blocks whose plane rows a build CTA stages at once
 constexpr size_t kClusterBuildSmem = 200 * 1024;   // dynamic shared memory of a cluster-build CTA
 constexpr int kClusterThreads = 512;  // threads of a cluster-build CTA
@@ -330,28 +330,44 @@ __device__ __forceinline__ uint32_t query_code(const uint32_t* qb, int K, int t)
     return static_cast<uint32_t>((v >> s) & ((1ull << K) - 1ull));
 }
 
-__global__ void __launch_bounds__(kLookupThreads)
+// Programmatic dependent launch: let the next kernel in the stream (the attend kernel, which
+// waits for this grid's completion before it reads the bitmaps) launch and run its prologue.
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// One warp per (query row, table): the query's bucket in that table, kLookupUnroll entries a lane
+// loaded before their atomics are issued, so that a warp waits about three memory round trips.
+__global__ void __launch_bounds__(kLookupWarps * 32)
     bucket_lookup_kernel(const uint32_t* buckets, const uint32_t* qbits, int qwords, int Hq,
                          int Hkv, int n, int K, int L, int nblk, uint32_t* ge1, uint32_t* ge2) {
-    const int row = blockIdx.y, tid = threadIdx.x;
+    allow_dependents();
+    constexpr int U = kLookupUnroll;
+    const int row = blockIdx.y, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kLookupWarps + (threadIdx.x >> 5);
+    if (t >= L) return;
     const int G = Hq / Hkv, b = row / Hq, h = row % Hq;
     const int bh = b * Hkv + h / G;
     const int nb = 1 << K;
     const uint32_t* base = buckets + static_cast<size_t>(bh) * bucket_words(n, K, L);
-    const uint32_t* qb = qbits + static_cast<size_t>(row) * qwords;
+    const uint32_t c = query_code(qbits + static_cast<size_t>(row) * qwords, K, t);
+    const uint32_t* off = base + static_cast<size_t>(t) * (nb + 1);
+    const uint32_t lo = __ldg(off + c), hi = __ldg(off + c + 1);
+    const uint32_t* mem = base + static_cast<size_t>(L) * (nb + 1) + static_cast<size_t>(t) * n;
     uint32_t* g1 = ge1 + static_cast<size_t>(row) * nblk * kWordsPerBlock;
     uint32_t* g2 = ge2 + static_cast<size_t>(row) * nblk * kWordsPerBlock;
-    const int t0 = blockIdx.x * kLookupTables, t1 = min(L, t0 + kLookupTables);
-    for (int t = t0; t < t1; ++t) {
-        const uint32_t c = query_code(qb, K, t);
-        const uint32_t* off = base + static_cast<size_t>(t) * (nb + 1);
-        const uint32_t lo = __ldg(off + c), hi = __ldg(off + c + 1);
-        const uint32_t* mem = base + static_cast<size_t>(L) * (nb + 1) + static_cast<size_t>(t) * n;
-        for (uint32_t i = lo + tid; i < hi; i += kLookupThreads) {
-            const uint32_t key = __ldg(mem + i);
-            const uint32_t bit = 1u << (key & 31u);
-            // saturating count: the second table to hit the key sees its first bit set
-            if (atomicOr(g1 + (key >> 5), bit) & bit) atomicOr(g2 + (key >> 5), bit);
+    for (uint32_t i0 = lo + lane; i0 < hi; i0 += 32u * U) {
+        uint32_t key[U], old[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) key[u] = i0 + 32u * u < hi ? __ldg(mem + i0 + 32u * u) : ~0u;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            old[u] = key[u] != ~0u ? atomicOr(g1 + (key[u] >> 5), 1u << (key[u] & 31u)) : 0u;
+        // saturating count: the second table to hit the key sees its first bit set
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const uint32_t bit = 1u << (key[u] & 31u);
+            if (key[u] != ~0u && (old[u] & bit)) atomicOr(g2 + (key[u] >> 5), bit);
         }
     }
 }
@@ -389,14 +405,24 @@ cudaError_t launch_bucket_build(const uint32_t* codes, int B, int Hkv, int n, in
 cudaError_t launch_bucket_lookup(const uint32_t* buckets, const uint32_t* qbits,
                                  const DecodeShape& s, uint32_t* ge1, uint32_t* ge2,
                                  cudaStream_t st) {
-    const size_t words = static_cast<size_t>(s.B) * s.Hq * s.nblk * kWordsPerBlock;
-    cudaError_t e = cudaMemsetAsync(ge1, 0, words * 4, st);
+    const size_t bytes = static_cast<size_t>(s.B) * s.Hq * s.nblk * kWordsPerBlock * 4;
+    // one memset when the two bitmaps are neighbours (the decode workspace carves them so)
+    uint32_t* lo_map = ge1 < ge2 ? ge1 : ge2;
+    uint32_t* hi_map = ge1 < ge2 ? ge2 : ge1;
+    const size_t gap = static_cast<size_t>(reinterpret_cast<uint8_t*>(hi_map) -
+                                           reinterpret_cast<uint8_t*>(lo_map));
+    cudaError_t e;
+    if (gap >= bytes && gap <= bytes + 256) {
+        e = cudaMemsetAsync(lo_map, 0, gap + bytes, st);
+    } else {
+        e = cudaMemsetAsync(ge1, 0, bytes, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(ge2, 0, bytes, st);
+    }
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(ge2, 0, words * 4, st);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((s.L + kLookupTables - 1) / kLookupTables, s.B * s.Hq);
-    bucket_lookup_kernel<<<grid, kLookupThreads, 0, st>>>(buckets, qbits, s.qwords, s.Hq, s.Hkv,
-                                                          s.n, s.K, s.L, s.nblk, ge1, ge2);
+    const dim3 grid((s.L + kLookupWarps - 1) / kLookupWarps, s.B * s.Hq);
+    bucket_lookup_kernel<<<grid, kLookupWarps * 32, 0, st>>>(buckets, qbits, s.qwords, s.Hq,
+                                                             s.Hkv, s.n, s.K, s.L, s.nblk, ge1,
+                                                             ge2);
     return cudaGetLastError();
 }
 
