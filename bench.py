@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="llama8b_n96k_32layers", choices=sorted(WORKLOADS))
     ap.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
+    ap.add_argument("--lsh", default="", metavar="K,L",
+                    help="override the workload's (K, L), e.g. 9,120 or 11,300")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -57,6 +59,15 @@ def parse_args(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of as one captured CUDA graph")
     return ap.parse_args(argv)
+
+
+def workload_from_args(args):
+    """The named workload, with (K, L) replaced when --lsh asks for another pair."""
+    wl = WORKLOADS[args.workload]
+    if args.lsh:
+        K, L = (int(x) for x in args.lsh.split(","))
+        wl = wl.replace(K=K, L=L)
+    return wl
 
 
 # ------------------------------------------------------------------------------------------------
@@ -495,7 +506,7 @@ def run_ours(args):
     import lsh_sampled_sparse_gb300 as mp
     mp.lib()
 
-    wl = WORKLOADS[args.workload]
+    wl = workload_from_args(args)
     layers = args.layers or wl.layers
     W, state, ws_mean, ws_dec = setup_inputs(mp, wl, layers, device)
     stream = torch.cuda.current_stream()
@@ -695,7 +706,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle as O
-    wl = WORKLOADS[args.workload]
+    wl = workload_from_args(args)
     # per step: one (b, g) unit of layer 0 on the first ORACLE_SAMPLE_KEYS keys, inputs drawn on
     # the CPU from the same recipe; the time is scaled linearly to the full context
     n_s = min(wl.n, ORACLE_SAMPLE_KEYS)
