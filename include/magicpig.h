@@ -13,7 +13,10 @@
  *     memory; scratch comes from a caller-provided workspace whose size a *_workspace_bytes
  *     function returns. Workspace pointers must be 256-byte aligned.
  *   - Tensors are contiguous, row-major:
- *       keys, values  [B][Hkv][n][d]       (MP_BF16 or MP_F32)
+ *       keys, values  [B][Hkv][n_cap][d]   (MP_BF16 or MP_F32); n_cap = n unless a call takes
+ *                                          a capacity (mp_params.n_capacity, or an n_capacity
+ *                                          argument): a cache allocated for n_cap tokens per
+ *                                          head of which the first n are in use
  *       q             [B][Hq][d]           (MP_BF16 or MP_F32)
  *       out           [B][Hq][d]           float32
  *       centre        [B][Hkv][d]          float32  (mu, the mean key of each head)
@@ -26,8 +29,8 @@
  *   - Packed codes ("codes") are bit-sliced in blocks of 1024 keys: for head (b, g) and block
  *     blk = i / 1024, plane j (= t*K + b) is a row of 32 uint32 words, and bit (i % 32) of word
  *     (i % 1024) / 32 holds the sign bit of key i for hyperplane j. Layout:
- *       codes[((b*Hkv + g)*nblk + blk)*(K*L) + j][w],   nblk = ceil(n / 1024).
- *     Bits of padding positions (i >= n in the last block) are unspecified.
+ *       codes[((b*Hkv + g)*nblk + blk)*(K*L) + j][w],   nblk = ceil(n_cap / 1024).
+ *     Bits of positions i >= n (padding, or capacity not yet in use) are unspecified.
  *   - Calls are asynchronous on `stream`: argument checks run on the host and return an error
  *     before anything is launched; device-side problems (a bounded wait that gave up) set a
  *     device status word that mp_device_status() reads.
@@ -51,7 +54,7 @@ extern "C" {
 #define MP_API
 #endif
 
-#define MP_ABI_VERSION 1
+#define MP_ABI_VERSION 2
 #define MP_KEYS_PER_BLOCK 1024
 
 typedef enum {
@@ -68,7 +71,12 @@ typedef enum { MP_F32 = 0, MP_BF16 = 1 } mp_dtype;
 /* Decode parameters. K, L: LSH bits per table and tables ("LSH Sampling...", method details,
  * hash-function choice). n_sink, n_local: the exact set T = {0..n_sink-1} u {n-n_local..n-1},
  * attended with u = 1 and never sampled (Algorithm 1's static cache; "don't pick the tallest",
- * section 5). scale: score scale, 0 means 1/sqrt(d). flags: must be 0. */
+ * section 5). scale: score scale, 0 means 1/sqrt(d). flags: must be 0.
+ * n_capacity: tokens per head the keys, values and codes are laid out for (0 means n; else
+ * n_capacity >= n). A decode cache that grows by appending (mp_encode_keys) keeps one
+ * n_capacity for its lifetime and passes the current length as n.
+ * n_indexed: keys [0, n_indexed) of each head are in the bucketed tables (0 means n; else
+ * n_indexed <= n); only mp_sampled_attention_buckets reads it. */
 typedef struct {
     int K;
     int L;
@@ -76,6 +84,8 @@ typedef struct {
     int n_local;
     float scale;
     unsigned flags;
+    int n_capacity;
+    int n_indexed;
 } mp_params;
 
 /* Human-readable name of a status code (static storage). */
@@ -102,6 +112,12 @@ MP_API mp_status mp_key_mean(const void* keys, mp_dtype key_dtype, int B, int Hk
                              float* centre, void* workspace, size_t ws_bytes,
                              cudaStream_t stream);
 
+/* mp_key_mean over the first n keys of a cache laid out for n_capacity tokens per head
+ * (n <= n_capacity); the workspace is mp_key_mean_workspace_bytes(B, Hkv, n, d). */
+MP_API mp_status mp_key_mean_cap(const void* keys, mp_dtype key_dtype, int B, int Hkv,
+                                 int n_capacity, int n, int d, float* centre, void* workspace,
+                                 size_t ws_bytes, cudaStream_t stream);
+
 /* Build the hash tables of one layer: centre each key, project it on the K*L hyperplanes of W,
  * keep the sign (bit = 1 iff w_j.(k_i - mu) > 0), pack into the bit-sliced codes above.
  * ("LSH Sampling...", background, LSH basics: Sign(w^T x); method details, hash-function choice
@@ -113,6 +129,27 @@ MP_API mp_status mp_key_mean(const void* keys, mp_dtype key_dtype, int B, int Hk
 MP_API mp_status mp_build_tables(const void* keys, mp_dtype key_dtype, const float* centre,
                                  const void* W, mp_dtype w_dtype, int B, int Hkv, int n, int d,
                                  int K, int L, uint32_t* codes, cudaStream_t stream);
+
+/* Encode keys [n_begin, n_end) of every head of a cache laid out for n_capacity tokens per head
+ * into codes laid out for n_capacity (mp_codes_bytes(B, Hkv, n_capacity, K, L) bytes), with a
+ * given centre. This is the incremental append of decode tokens: after a build over the prompt
+ * (mp_key_mean_cap + mp_encode_keys(0, n)), each new token's key is written to the cache at
+ * position n and encoded with mp_encode_keys(n, n + 1); the next decode passes n + 1. The local
+ * window of T slides with n, so the key that leaves it joins the sampled keys with the code it
+ * got when it was appended. The centre stays the one of the build: the pages compute it once,
+ * before the tables are built ("LSH Sampling...", method details, data preprocessing and
+ * centering) and say nothing of updates; codes and the weights p_i both use the centre the
+ * caller passes, so any fixed centre gives a consistent sampler, and refreshing it means a
+ * rebuild (mp_key_mean_cap, then mp_encode_keys over [0, n)).
+ * Bits of keys outside [n_begin, n_end) that share a 32-key word with the range are kept. Short
+ * ranges (up to 64 keys) run on CUDA cores; longer ones re-encode whole 1024-key blocks (bf16
+ * keys and W: tensor cores), which rewrites the blocks' other keys with their own codes again.
+ * Errors: MP_ERR_INVALID_ARG (shapes, n_begin < 0, n_end > n_capacity, n_begin > n_end, null,
+ * misalignment), MP_ERR_UNSUPPORTED (d != 128). An empty range does nothing. */
+MP_API mp_status mp_encode_keys(const void* keys, mp_dtype key_dtype, const float* centre,
+                                const void* W, mp_dtype w_dtype, int B, int Hkv, int n_capacity,
+                                int n_begin, int n_end, int d, int K, int L, uint32_t* codes,
+                                cudaStream_t stream);
 
 /* Workspace bytes mp_decode_attention (and its two halves below) need for these shapes;
  * 0 if the shapes or parameters are invalid. */
@@ -177,13 +214,25 @@ MP_API size_t mp_buckets_bytes(int B, int Hkv, int n, int K, int L);
 MP_API mp_status mp_build_buckets(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
                                   uint32_t* buckets, cudaStream_t stream);
 
+/* mp_build_buckets over keys [0, n) of codes laid out for n_capacity tokens per head (the
+ * appendable cache of mp_encode_keys); buckets is mp_buckets_bytes(B, Hkv, n, K, L) bytes. A
+ * decode then passes n_indexed = n in mp_params while its own n grows. */
+MP_API mp_status mp_build_buckets_cap(const uint32_t* codes, int B, int Hkv, int n_capacity,
+                                      int n, int K, int L, uint32_t* buckets,
+                                      cudaStream_t stream);
+
 /* mp_sampled_attention with the bucketed tables instead of a scan of the packed codes: each
  * query row reads its bucket in every table and keeps the keys hit by >= 2 tables (the same S as
  * the scan, bit for bit), then the same gather, importance weights and merged softmax. Needs the
  * query encoding of mp_encode_query in the workspace first, like mp_sampled_attention.
+ * The tables cover keys [0, prm->n_indexed); keys appended since (up to n) are found by the code
+ * scan over the 1024-key blocks from n_indexed / 1024 on, which replaces the lookup's result in
+ * those blocks. So codes must be passed too (NULL only when n_indexed == n and n is a multiple
+ * of 1024, or K == 0) and the tables must have been built for n_indexed keys.
  * buckets: 16-byte aligned. Errors as mp_sampled_attention; MP_ERR_UNSUPPORTED also for K > 12. */
 MP_API mp_status mp_sampled_attention_buckets(const void* q, mp_dtype q_dtype,
-                                              const uint32_t* buckets, const float* centre,
+                                              const uint32_t* buckets, const uint32_t* codes,
+                                              const float* centre,
                                               const void* keys, const void* values,
                                               mp_dtype kv_dtype, int B, int Hq, int Hkv, int n,
                                               int d, const mp_params* prm, float* out,

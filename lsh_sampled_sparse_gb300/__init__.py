@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     decode_attention,
     decode_workspace_bytes,
     device_status,
+    encode_keys,
     encode_query,
     key_mean,
     key_mean_workspace_bytes,

@@ -20,10 +20,26 @@ class MagicPIGError(RuntimeError):
 
 
 class Params(ctypes.Structure):
-    """mp_params: K bits per table, L tables, exact sink/local sizes, score scale (0: 1/sqrt(d))."""
+    """mp_params: K bits per table, L tables, exact sink/local sizes, score scale (0: 1/sqrt(d)),
+    flags (0), the cache capacity per head (0: n) and the keys in the bucketed tables (0: n)."""
 
     _fields_ = [("K", ctypes.c_int), ("L", ctypes.c_int), ("n_sink", ctypes.c_int),
-                ("n_local", ctypes.c_int), ("scale", ctypes.c_float), ("flags", ctypes.c_uint)]
+                ("n_local", ctypes.c_int), ("scale", ctypes.c_float), ("flags", ctypes.c_uint),
+                ("n_capacity", ctypes.c_int), ("n_indexed", ctypes.c_int)]
+
+
+def _params(K, L, n_sink, n_local, scale=0.0, n_capacity=0, n_indexed=0) -> Params:
+    return Params(K, L, n_sink, n_local, scale, 0, n_capacity, n_indexed)
+
+
+def _lengths(keys_shape, n):
+    """(n, n_capacity) of a cache tensor [B, Hkv, n_capacity, d] of which n keys are in use."""
+    cap = int(keys_shape[2])
+    if n is None:
+        return cap, cap
+    if not 1 <= n <= cap:
+        raise ValueError(f"n = {n} outside [1, {cap}] (the cache's capacity)")
+    return int(n), cap
 
 
 _LIB = None
@@ -42,6 +58,8 @@ def _declare(L):
         "mp_key_mean_workspace_bytes": (_c_size, [_c_int] * 4),
         "mp_key_mean": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _c_size,
                                  _vp]),
+        "mp_key_mean_cap": (_c_int, [_vp, _c_int] + [_c_int] * 5 + [_vp, _vp, _c_size, _vp]),
+        "mp_encode_keys": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 8 + [_vp, _vp]),
         "mp_build_tables": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 6 + [_vp, _vp]),
         "mp_decode_workspace_bytes": (_c_size, [_c_int] * 5 + [P]),
         "mp_debug_workspace_bytes": (_c_size, [_c_int] * 5 + [P]),
@@ -58,7 +76,8 @@ def _declare(L):
         "mp_codes_unpack": (_c_int, [_vp] + [_c_int] * 5 + [_vp, _vp]),
         "mp_buckets_bytes": (_c_size, [_c_int] * 5),
         "mp_build_buckets": (_c_int, [_vp] + [_c_int] * 5 + [_vp, _vp]),
-        "mp_sampled_attention_buckets": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int]
+        "mp_build_buckets_cap": (_c_int, [_vp] + [_c_int] * 6 + [_vp, _vp]),
+        "mp_sampled_attention_buckets": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int]
                                          + [_c_int] * 5 + [P, _vp, _vp, _c_size, _vp]),
         "mp_device_status": (_c_int, [ctypes.POINTER(_c_int)]),
     }
@@ -142,25 +161,28 @@ def key_mean_workspace_bytes(B: int, Hkv: int, n: int, d: int) -> int:
 
 
 def decode_workspace_bytes(B, Hq, Hkv, n, d, K, L, n_sink, n_local, scale=0.0) -> int:
-    p = Params(K, L, n_sink, n_local, scale, 0)
+    p = _params(K, L, n_sink, n_local, scale)
     return int(lib().mp_decode_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
 
 
 def debug_workspace_bytes(B, Hq, Hkv, n, d, K, L, n_sink, n_local, scale=0.0) -> int:
-    p = Params(K, L, n_sink, n_local, scale, 0)
+    p = _params(K, L, n_sink, n_local, scale)
     return int(lib().mp_debug_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
 
 
-def key_mean(keys, centre=None, workspace=None, stream=None):
-    """mu[b, g] = mean of keys[b, g, :, :] over the n cached keys (float32 [B, Hkv, d])."""
+def key_mean(keys, centre=None, workspace=None, stream=None, n=None):
+    """mu[b, g] = mean of the first n keys of keys[b, g] (float32 [B, Hkv, d]); n defaults to
+    keys.shape[2], a larger keys.shape[2] is the cache's capacity."""
     _cuda(keys, "keys", 4)
-    B, Hkv, n, d = keys.shape
+    B, Hkv, cap, d = keys.shape
+    n, cap = _lengths(keys.shape, n)
     if centre is None:
         centre = torch.empty(B, Hkv, d, dtype=torch.float32, device=keys.device)
     _cuda(centre, "centre", 3)
     ws = _workspace(workspace, key_mean_workspace_bytes(B, Hkv, n, d), keys.device)
-    _check(lib().mp_key_mean(_ptr(keys), _dtype(keys, "keys"), B, Hkv, n, d, _ptr(centre),
-                             _ptr(ws), _nbytes(ws), _stream(stream)), "mp_key_mean")
+    _check(lib().mp_key_mean_cap(_ptr(keys), _dtype(keys, "keys"), B, Hkv, cap, n, d,
+                                 _ptr(centre), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "mp_key_mean_cap")
     return centre
 
 
@@ -182,21 +204,41 @@ def build_tables(keys, centre, W, K: int, L: int, codes=None, stream=None):
     return codes
 
 
+def encode_keys(keys, centre, W, K: int, L: int, n_begin: int, n_end: int, codes,
+                stream=None):
+    """(Re)encode keys [n_begin, n_end) of the cache keys [B, Hkv, n_capacity, d] into codes laid
+    out for n_capacity (the incremental append of decode tokens)."""
+    _cuda(keys, "keys", 4)
+    B, Hkv, cap, d = keys.shape
+    _cuda(codes, "codes")
+    if _nbytes(codes) < codes_bytes(B, Hkv, cap, K, L):
+        raise ValueError("codes buffer too small for the cache's capacity")
+    _cuda(centre, "centre", 3)
+    _cuda(W, "W", 2)
+    _check(lib().mp_encode_keys(_ptr(keys), _dtype(keys, "keys"), _ptr(centre), _ptr(W),
+                                _dtype(W, "W"), B, Hkv, cap, n_begin, n_end, d, K, L,
+                                _ptr(codes), _stream(stream)), "mp_encode_keys")
+    return codes
+
+
 def decode_attention(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int,
-                     n_local: int, scale: float = 0.0, out=None, workspace=None, stream=None):
-    """One LSH-sampled decode step; returns out [B, Hq, d] float32."""
+                     n_local: int, scale: float = 0.0, out=None, workspace=None, stream=None,
+                     n=None):
+    """One LSH-sampled decode step over the first n keys (default: all of keys.shape[2]);
+    returns out [B, Hq, d] float32."""
     _cuda(q, "q", 3)
     _cuda(keys, "keys", 4)
     _cuda(values, "values", 4)
     _cuda(centre, "centre", 3)
     B, Hq, d = q.shape
-    Hkv, n = keys.shape[1], keys.shape[2]
+    Hkv = keys.shape[1]
+    n, cap = _lengths(keys.shape, n)
     if values.shape != keys.shape or values.dtype != keys.dtype:
         raise ValueError("values must match keys in shape and dtype")
     if out is None:
         out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
     _cuda(out, "out", 3)
-    p = Params(K, L, n_sink, n_local, scale, 0)
+    p = _params(K, L, n_sink, n_local, scale, cap)
     need = int(lib().mp_decode_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
     if need == 0:
         raise MagicPIGError("mp_decode_workspace_bytes rejected the shapes/parameters")
@@ -209,21 +251,22 @@ def decode_attention(q, codes, centre, W, keys, values, K: int, L: int, n_sink: 
 
 
 def encode_query(q, centre, W, keys_shape, K: int, L: int, n_sink: int, n_local: int,
-                 workspace, scale: float = 0.0, stream=None):
+                 workspace, scale: float = 0.0, stream=None, n=None):
     """First half of decode_attention: query codes and norms into `workspace`."""
     _cuda(q, "q", 3)
     _cuda(centre, "centre", 3)
     _cuda(workspace, "workspace")
     B, Hq, d = q.shape
-    Hkv, n = keys_shape[1], keys_shape[2]
-    p = Params(K, L, n_sink, n_local, scale, 0)
+    Hkv = keys_shape[1]
+    n, cap = _lengths(keys_shape, n)
+    p = _params(K, L, n_sink, n_local, scale, cap)
     _check(lib().mp_encode_query(_ptr(q), _dtype(q, "q"), _ptr(centre), _ptr(W), _dtype(W, "W"),
                                  B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(workspace),
                                  _nbytes(workspace), _stream(stream)), "mp_encode_query")
 
 
 def sampled_attention(q, codes, centre, keys, values, K: int, L: int, n_sink: int, n_local: int,
-                      out, workspace, scale: float = 0.0, stream=None):
+                      out, workspace, scale: float = 0.0, stream=None, n=None):
     """Second half of decode_attention (after encode_query filled `workspace`)."""
     _cuda(q, "q", 3)
     _cuda(keys, "keys", 4)
@@ -231,8 +274,9 @@ def sampled_attention(q, codes, centre, keys, values, K: int, L: int, n_sink: in
     _cuda(out, "out", 3)
     _cuda(workspace, "workspace")
     B, Hq, d = q.shape
-    Hkv, n = keys.shape[1], keys.shape[2]
-    p = Params(K, L, n_sink, n_local, scale, 0)
+    Hkv = keys.shape[1]
+    n, cap = _lengths(keys.shape, n)
+    p = _params(K, L, n_sink, n_local, scale, cap)
     _check(lib().mp_sampled_attention(
         _ptr(q), _dtype(q, "q"), _ptr(codes), _ptr(centre), _ptr(keys), _ptr(values),
         _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out), _ptr(workspace),
@@ -244,8 +288,10 @@ def buckets_bytes(B: int, Hkv: int, n: int, K: int, L: int) -> int:
     return int(lib().mp_buckets_bytes(B, Hkv, n, K, L))
 
 
-def build_buckets(codes, B: int, Hkv: int, n: int, K: int, L: int, buckets=None, stream=None):
-    """Bucketed hash tables from the packed codes (int32 tensor of buckets_bytes/4 words)."""
+def build_buckets(codes, B: int, Hkv: int, n: int, K: int, L: int, buckets=None, stream=None,
+                  n_capacity=None):
+    """Bucketed hash tables of keys [0, n) from the packed codes (laid out for n_capacity keys
+    per head, default n); an int32 tensor of buckets_bytes/4 words."""
     nbytes = buckets_bytes(B, Hkv, n, K, L)
     if nbytes == 0:
         raise ValueError("unsupported bucket table shape (K must be <= 12)")
@@ -255,14 +301,18 @@ def build_buckets(codes, B: int, Hkv: int, n: int, K: int, L: int, buckets=None,
     _cuda(buckets, "buckets")
     if _nbytes(buckets) < nbytes:
         raise ValueError("buckets buffer too small")
-    _check(lib().mp_build_buckets(_ptr(codes), B, Hkv, n, K, L, _ptr(buckets), _stream(stream)),
-           "mp_build_buckets")
+    cap = n if n_capacity is None else int(n_capacity)
+    _check(lib().mp_build_buckets_cap(_ptr(codes), B, Hkv, cap, n, K, L, _ptr(buckets),
+                                      _stream(stream)), "mp_build_buckets_cap")
     return buckets
 
 
 def sampled_attention_buckets(q, buckets, centre, keys, values, K: int, L: int, n_sink: int,
-                              n_local: int, out, workspace, scale: float = 0.0, stream=None):
-    """sampled_attention with the bucketed tables in place of the code scan."""
+                              n_local: int, out, workspace, scale: float = 0.0, stream=None,
+                              codes=None, n=None, n_indexed=None):
+    """sampled_attention with the bucketed tables in place of the code scan. The tables hold
+    keys [0, n_indexed) (default n); keys appended since are found by scanning their codes, so
+    `codes` is needed when n_indexed < n."""
     _cuda(q, "q", 3)
     _cuda(keys, "keys", 4)
     _cuda(values, "values", 4)
@@ -270,22 +320,24 @@ def sampled_attention_buckets(q, buckets, centre, keys, values, K: int, L: int, 
     _cuda(workspace, "workspace")
     _cuda(buckets, "buckets")
     B, Hq, d = q.shape
-    Hkv, n = keys.shape[1], keys.shape[2]
-    p = Params(K, L, n_sink, n_local, scale, 0)
+    Hkv = keys.shape[1]
+    n, cap = _lengths(keys.shape, n)
+    p = _params(K, L, n_sink, n_local, scale, cap, 0 if n_indexed is None else int(n_indexed))
     _check(lib().mp_sampled_attention_buckets(
-        _ptr(q), _dtype(q, "q"), _ptr(buckets), _ptr(centre), _ptr(keys), _ptr(values),
-        _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out), _ptr(workspace),
-        _nbytes(workspace), _stream(stream)), "mp_sampled_attention_buckets")
+        _ptr(q), _dtype(q, "q"), _ptr(buckets), _ptr(codes), _ptr(centre), _ptr(keys),
+        _ptr(values), _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out),
+        _ptr(workspace), _nbytes(workspace), _stream(stream)), "mp_sampled_attention_buckets")
     return out
 
 
 def debug_select(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int, n_local: int,
-                 scale: float = 0.0, counts: bool = True, stream=None) -> dict:
+                 scale: float = 0.0, counts: bool = True, stream=None, n=None) -> dict:
     """Decode plus its decisions: out, q_bits, per-row ascending sample sets, collision counts."""
     _cuda(q, "q", 3)
     _cuda(keys, "keys", 4)
     B, Hq, d = q.shape
-    Hkv, n = keys.shape[1], keys.shape[2]
+    Hkv = keys.shape[1]
+    n, cap = _lengths(keys.shape, n)
     dev = q.device
     C = K * L
     qwords = (C + 31) // 32
@@ -294,7 +346,7 @@ def debug_select(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int,
     sel_idx = torch.full((B, Hq, n), -1, dtype=torch.int32, device=dev)
     sel_count = torch.zeros(B, Hq, dtype=torch.int32, device=dev)
     cnt = torch.zeros(B, Hq, n, dtype=torch.uint8, device=dev) if counts else None
-    p = Params(K, L, n_sink, n_local, scale, 0)
+    p = _params(K, L, n_sink, n_local, scale, cap)
     need = int(lib().mp_debug_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
     if need == 0:
         raise MagicPIGError("mp_debug_workspace_bytes rejected the shapes/parameters")

@@ -60,6 +60,8 @@ bool fill_shape(int B, int Hq, int Hkv, int n, int d, const mp_params* prm, Deco
         prm->flags != 0u || !(prm->scale >= 0.0f))
         return false;
     if (static_cast<long long>(prm->K) * prm->L > (1 << 20)) return false;
+    if (prm->n_capacity < 0 || (prm->n_capacity > 0 && prm->n_capacity < n)) return false;
+    if (prm->n_indexed < 0 || prm->n_indexed > n) return false;
     s->B = B;
     s->Hq = Hq;
     s->Hkv = Hkv;
@@ -71,6 +73,9 @@ bool fill_shape(int B, int Hq, int Hkv, int n, int d, const mp_params* prm, Deco
     s->qwords = (s->C + 31) / 32;
     s->cpad = (s->C + 3) & ~3;
     s->nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
+    s->ncap = prm->n_capacity > 0 ? prm->n_capacity : n;
+    s->cblk = (s->ncap + kKeysPerBlock - 1) / kKeysPerBlock;
+    s->n_indexed = prm->n_indexed > 0 ? prm->n_indexed : n;
     s->n_sink = prm->n_sink;
     s->n_local = prm->n_local;
     s->scale = prm->scale > 0.0f ? prm->scale : 1.0f / sqrtf(static_cast<float>(d));
@@ -189,39 +194,61 @@ size_t mp_key_mean_workspace_bytes(int B, int Hkv, int n, int d) {
 
 mp_status mp_key_mean(const void* keys, mp_dtype key_dtype, int B, int Hkv, int n, int d,
                       float* centre, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    return mp_key_mean_cap(keys, key_dtype, B, Hkv, n, n, d, centre, workspace, ws_bytes, stream);
+}
+
+mp_status mp_key_mean_cap(const void* keys, mp_dtype key_dtype, int B, int Hkv, int n_capacity,
+                          int n, int d, float* centre, void* workspace, size_t ws_bytes,
+                          cudaStream_t stream) {
     if (!keys || !centre || !workspace || !valid_dtype(key_dtype)) return MP_ERR_INVALID_ARG;
-    if (B < 1 || Hkv < 1 || n < 1 || d < 1) return MP_ERR_INVALID_ARG;
+    if (B < 1 || Hkv < 1 || n < 1 || d < 1 || n_capacity < n) return MP_ERR_INVALID_ARG;
     if (d != kD) return MP_ERR_UNSUPPORTED;
     if (!aligned(keys, 16) || !aligned(centre, 4) || !aligned(workspace, 256))
         return MP_ERR_INVALID_ARG;
     if (ws_bytes < mp_key_mean_workspace_bytes(B, Hkv, n, d)) return MP_ERR_WORKSPACE;
     if (!ensure_prepared()) return MP_ERR_CUDA;
-    return to_status(launch_key_mean(keys, key_dtype == MP_BF16, B * Hkv, n, centre,
+    return to_status(launch_key_mean(keys, key_dtype == MP_BF16, B * Hkv, n_capacity, n, centre,
                                      static_cast<float*>(workspace), key_mean_splits(n), stream));
 }
 
 mp_status mp_build_tables(const void* keys, mp_dtype key_dtype, const float* centre,
                           const void* W, mp_dtype w_dtype, int B, int Hkv, int n, int d, int K,
                           int L, uint32_t* codes, cudaStream_t stream) {
-    if (B < 1 || Hkv < 1 || n < 1 || d < 1 || K < 0 || K > 32 || L < 1)
+    if (n < 1) return MP_ERR_INVALID_ARG;
+    return mp_encode_keys(keys, key_dtype, centre, W, w_dtype, B, Hkv, n, 0, n, d, K, L, codes,
+                          stream);
+}
+
+mp_status mp_encode_keys(const void* keys, mp_dtype key_dtype, const float* centre,
+                         const void* W, mp_dtype w_dtype, int B, int Hkv, int n_capacity,
+                         int n_begin, int n_end, int d, int K, int L, uint32_t* codes,
+                         cudaStream_t stream) {
+    if (B < 1 || Hkv < 1 || n_capacity < 1 || d < 1 || K < 0 || K > 32 || L < 1)
         return MP_ERR_INVALID_ARG;
+    if (n_begin < 0 || n_end > n_capacity || n_begin > n_end) return MP_ERR_INVALID_ARG;
     if (!valid_dtype(key_dtype) || !valid_dtype(w_dtype)) return MP_ERR_INVALID_ARG;
     if (d != kD) return MP_ERR_UNSUPPORTED;
     if (static_cast<long long>(K) * L > (1 << 20)) return MP_ERR_INVALID_ARG;
-    if (K == 0) return MP_OK;   // no hyperplanes: nothing to encode
+    if (K == 0 || n_begin == n_end) return MP_OK;   // nothing to encode
     if (!keys || !centre || !W || !codes) return MP_ERR_INVALID_ARG;
     if (!aligned(keys, 16) || !aligned(codes, 16) || !aligned(centre, 4) ||
         !aligned(W, w_dtype == MP_BF16 ? 2 : 4))
         return MP_ERR_INVALID_ARG;
     if (!ensure_prepared()) return MP_ERR_CUDA;
-    if (key_dtype == MP_BF16 && w_dtype == MP_BF16) {
-        const cudaError_t e =
-            launch_encode_tc(keys, centre, W, B, Hkv, n, K, L, codes, device_status_ptr(), stream);
+    const bool kbf = key_dtype == MP_BF16, wbf = w_dtype == MP_BF16;
+    if (n_end - n_begin <= kAppendMaxKeys)
+        return to_status(launch_encode_append(keys, kbf, centre, W, wbf, B, Hkv, n_capacity,
+                                              n_begin, n_end, K, L, codes, stream));
+    const int blk0 = n_begin / kKeysPerBlock;
+    const int blk1 = (n_end + kKeysPerBlock - 1) / kKeysPerBlock;
+    if (kbf && wbf) {
+        const cudaError_t e = launch_encode_tc(keys, centre, W, B, Hkv, n_capacity, blk0, blk1,
+                                               K, L, codes, device_status_ptr(), stream);
         if (e != cudaErrorNotSupported) return to_status(e);
         cudaGetLastError();
     }
-    return to_status(launch_encode_simt(keys, key_dtype == MP_BF16, centre, W, w_dtype == MP_BF16,
-                                        B, Hkv, n, K, L, codes, stream));
+    return to_status(launch_encode_simt(keys, kbf, centre, W, wbf, B, Hkv, n_capacity, blk0,
+                                        blk1, K, L, codes, stream));
 }
 
 size_t mp_decode_workspace_bytes(int B, int Hq, int Hkv, int n, int d, const mp_params* prm) {
@@ -297,19 +324,27 @@ size_t mp_buckets_bytes(int B, int Hkv, int n, int K, int L) {
 
 mp_status mp_build_buckets(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
                            uint32_t* buckets, cudaStream_t stream) {
-    if (B < 1 || Hkv < 1 || n < 1 || K < 0 || K > 32 || L < 1) return MP_ERR_INVALID_ARG;
+    return mp_build_buckets_cap(codes, B, Hkv, n, n, K, L, buckets, stream);
+}
+
+mp_status mp_build_buckets_cap(const uint32_t* codes, int B, int Hkv, int n_capacity, int n,
+                               int K, int L, uint32_t* buckets, cudaStream_t stream) {
+    if (B < 1 || Hkv < 1 || n < 1 || n_capacity < n || K < 0 || K > 32 || L < 1)
+        return MP_ERR_INVALID_ARG;
     if (K > kMaxBucketBits) return MP_ERR_UNSUPPORTED;
     if (!buckets || (K > 0 && !codes)) return MP_ERR_INVALID_ARG;
     if ((codes && !aligned(codes, 16)) || !aligned(buckets, 4)) return MP_ERR_INVALID_ARG;
     if (!ensure_prepared()) return MP_ERR_CUDA;
-    return to_status(launch_bucket_build(codes, B, Hkv, n, K, L, buckets, stream));
+    const int cblk = (n_capacity + kKeysPerBlock - 1) / kKeysPerBlock;
+    return to_status(launch_bucket_build(codes, B, Hkv, cblk, n, K, L, buckets, stream));
 }
 
 mp_status mp_sampled_attention_buckets(const void* q, mp_dtype q_dtype, const uint32_t* buckets,
-                                       const float* centre, const void* keys,
-                                       const void* values, mp_dtype kv_dtype, int B, int Hq,
-                                       int Hkv, int n, int d, const mp_params* prm, float* out,
-                                       void* workspace, size_t ws_bytes, cudaStream_t stream) {
+                                       const uint32_t* codes, const float* centre,
+                                       const void* keys, const void* values, mp_dtype kv_dtype,
+                                       int B, int Hq, int Hkv, int n, int d,
+                                       const mp_params* prm, float* out, void* workspace,
+                                       size_t ws_bytes, cudaStream_t stream) {
     if (!buckets) return MP_ERR_INVALID_ARG;
     DecodeShape s;
     // the buckets stand in for the codes, q for W, in the shared checks
@@ -318,10 +353,17 @@ mp_status mp_sampled_attention_buckets(const void* q, mp_dtype q_dtype, const ui
                                       false, &s);
     if (st != MP_OK) return st;
     if (s.K > kMaxBucketBits) return MP_ERR_UNSUPPORTED;
+    // keys appended since the tables were built come from a scan of their code blocks
+    const bool tail = s.n_indexed < s.n && s.C > 0;
+    if (tail && (!codes || !aligned(codes, 16))) return MP_ERR_INVALID_ARG;
     if (!ensure_prepared()) return MP_ERR_CUDA;
     const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
     cudaError_t e = launch_bucket_lookup(buckets, ws.qbits, s, ws.sel_ge1, ws.selmask, stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
+    if (tail)
+        return to_status(launch_collide(q, q_dtype == MP_BF16, codes, centre, keys, values,
+                                        kv_dtype == MP_BF16, s, out, ws, stream,
+                                        s.n_indexed / kKeysPerBlock));
     return to_status(launch_attend(q, q_dtype == MP_BF16, centre, keys, values,
                                    kv_dtype == MP_BF16, s, out, ws, stream));
 }

@@ -49,7 +49,8 @@ __host__ __device__ __forceinline__ size_t bucket_words(int n, int K, int L) {
 // lane of every key (keys past n are skipped).
 template <typename F>
 __device__ __forceinline__ void for_range_keys(const uint32_t* codes, int bh, int t, int range,
-                                              int n, int K, int L, int nblk, uint32_t* stage,
+                                              int n, int K, int L, int nblk, int cblk,
+                                              uint32_t* stage,
                                               F&& f) {
     const int C = K * L, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b0 = (nblk * range) / kBucketRanges, b1 = (nblk * (range + 1)) / kBucketRanges;
@@ -60,7 +61,7 @@ __device__ __forceinline__ void for_range_keys(const uint32_t* codes, int bh, in
         for (int i = tid; i < nbk * rowsz; i += kBuildThreads) {
             const int kb = i / rowsz, w = i % rowsz;
             stage[kb * srow + (w / kWordsPerBlock) * kStageRow + w % kWordsPerBlock] =
-                __ldcs(codes + (static_cast<size_t>(bh) * nblk + blk + kb) * C * kWordsPerBlock +
+                __ldcs(codes + (static_cast<size_t>(bh) * cblk + blk + kb) * C * kWordsPerBlock +
                        static_cast<size_t>(t) * rowsz + w);
         }
         __syncthreads();
@@ -76,13 +77,14 @@ __device__ __forceinline__ void for_range_keys(const uint32_t* codes, int bh, in
 
 // 1. per key range: its count of every code -> scratch[t][range][c]
 __global__ void __launch_bounds__(kBuildThreads)
-    bucket_count_kernel(const uint32_t* codes, int n, int K, int L, int nblk, uint32_t* buckets) {
+    bucket_count_kernel(const uint32_t* codes, int n, int K, int L, int nblk, int cblk,
+                        uint32_t* buckets) {
     extern __shared__ __align__(16) uint32_t sm[];
     const int nb = 1 << K, range = blockIdx.x, t = blockIdx.y, bh = blockIdx.z;
     uint32_t* hist = sm;
     uint32_t* stage = sm + nb;
     for (int c = threadIdx.x; c < nb; c += kBuildThreads) hist[c] = 0u;
-    for_range_keys(codes, bh, t, range, n, K, L, nblk, stage,
+    for_range_keys(codes, bh, t, range, n, K, L, nblk, cblk, stage,
                    [&](int, uint32_t c) { atomicAdd(&hist[c], 1u); });
     __syncthreads();
     uint32_t* scratch = buckets + static_cast<size_t>(bh) * bucket_words(n, K, L) +
@@ -130,7 +132,8 @@ __global__ void __launch_bounds__(kBuildThreads)
 
 // 3. per key range: every key to its bucket, from the range's base (cursors in shared memory)
 __global__ void __launch_bounds__(kBuildThreads)
-    bucket_scatter_kernel(const uint32_t* codes, int n, int K, int L, int nblk, uint32_t* buckets) {
+    bucket_scatter_kernel(const uint32_t* codes, int n, int K, int L, int nblk, int cblk,
+                          uint32_t* buckets) {
     extern __shared__ __align__(16) uint32_t sm[];
     const int nb = 1 << K, range = blockIdx.x, t = blockIdx.y, bh = blockIdx.z;
     uint32_t* cursor = sm;
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(kBuildThreads)
                               (static_cast<size_t>(t) * kBucketRanges + range) * nb;
     uint32_t* members = base + static_cast<size_t>(L) * (nb + 1) + static_cast<size_t>(t) * n;
     for (int c = threadIdx.x; c < nb; c += kBuildThreads) cursor[c] = scratch[c];
-    for_range_keys(codes, bh, t, range, n, K, L, nblk, stage, [&](int key, uint32_t c) {
+    for_range_keys(codes, bh, t, range, n, K, L, nblk, cblk, stage, [&](int key, uint32_t c) {
         members[atomicAdd(&cursor[c], 1u)] = static_cast<uint32_t>(key);
     });
 }
@@ -220,7 +223,7 @@ __host__ __device__ __forceinline__ size_t cluster_build_smem(int rb, int K) {
 // One CTA per key range, kBucketRanges CTAs (a cluster) per table. Each warp takes kWordsAtOnce
 // 32-key words at a time so that their shuffles and shared atomics overlap.
 __global__ void __cluster_dims__(kBucketRanges, 1, 1) __launch_bounds__(kClusterThreads)
-    bucket_build_cluster_kernel(const uint32_t* codes, int n, int K, int L, int nblk,
+    bucket_build_cluster_kernel(const uint32_t* codes, int n, int K, int L, int nblk, int cblk,
                                 uint32_t* buckets) {
     namespace cg = cooperative_groups;
     constexpr int T = kClusterThreads, U = kWordsAtOnce;
@@ -245,7 +248,7 @@ __global__ void __cluster_dims__(kBucketRanges, 1, 1) __launch_bounds__(kCluster
     for (int c = tid; c < nb; c += T) hist[c] = 0u;
     {   // plane rows as 16-byte loads: row j = kb * K + p is staged at j * kStageRow
         const int per = K * (kWordsPerBlock / 4);
-        const uint32_t* src = codes + (static_cast<size_t>(bh) * nblk + b0) * C * kWordsPerBlock +
+        const uint32_t* src = codes + (static_cast<size_t>(bh) * cblk + b0) * C * kWordsPerBlock +
                               static_cast<size_t>(t) * K * kWordsPerBlock;
         for (int j = tid; j < nbk * per; j += T) {
             const int kb = j / per, q = j - kb * per;        // q: plane * 8 + 16-byte chunk
@@ -379,26 +382,27 @@ size_t bucket_table_bytes(int B, int Hkv, int n, int K, int L) {
     return static_cast<size_t>(B) * Hkv * bucket_words(n, K, L) * 4;
 }
 
-cudaError_t launch_bucket_build(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
-                                uint32_t* buckets, cudaStream_t st) {
+cudaError_t launch_bucket_build(const uint32_t* codes, int B, int Hkv, int cblk, int n, int K,
+                                int L, uint32_t* buckets, cudaStream_t st) {
     const int nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
     const dim3 ranges(kBucketRanges, L, B * Hkv);   // the ranges of one table run side by side
     const int rb = (nblk + kBucketRanges - 1) / kBucketRanges;
     const size_t csmem = cluster_build_smem(rb, K);
     if (csmem <= kClusterBuildSmem && rb * kKeysPerBlock <= 65536) {
         bucket_build_cluster_kernel<<<ranges, kClusterThreads, csmem, st>>>(codes, n, K, L, nblk,
-                                                                            buckets);
+                                                                            cblk, buckets);
         return cudaGetLastError();
     }
     const size_t smem = (static_cast<size_t>(1) << K) * 4 +
                         static_cast<size_t>(kStageBlocks) * K * kStageRow * 4;
-    bucket_count_kernel<<<ranges, kBuildThreads, smem, st>>>(codes, n, K, L, nblk, buckets);
+    bucket_count_kernel<<<ranges, kBuildThreads, smem, st>>>(codes, n, K, L, nblk, cblk, buckets);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     bucket_scan_kernel<<<dim3(L, B * Hkv), kBuildThreads, 0, st>>>(n, K, L, buckets);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bucket_scatter_kernel<<<ranges, kBuildThreads, smem, st>>>(codes, n, K, L, nblk, buckets);
+    bucket_scatter_kernel<<<ranges, kBuildThreads, smem, st>>>(codes, n, K, L, nblk, cblk,
+                                                               buckets);
     return cudaGetLastError();
 }
 
@@ -421,8 +425,8 @@ cudaError_t launch_bucket_lookup(const uint32_t* buckets, const uint32_t* qbits,
     if (e != cudaSuccess) return e;
     const dim3 grid((s.L + kLookupWarps - 1) / kLookupWarps, s.B * s.Hq);
     bucket_lookup_kernel<<<grid, kLookupWarps * 32, 0, st>>>(buckets, qbits, s.qwords, s.Hq,
-                                                             s.Hkv, s.n, s.K, s.L, s.nblk, ge1,
-                                                             ge2);
+                                                             s.Hkv, s.n_indexed, s.K, s.L, s.nblk,
+                                                             ge1, ge2);
     return cudaGetLastError();
 }
 

@@ -221,6 +221,8 @@ struct CArgs {
     float* out;
     uint32_t* selmask;
     int q_bf16, n, nblk, Hq, Hkv, K, L, C, cpad, n_sink, n_local;
+    int cblk;                                    // code blocks per head in memory
+    int blk0;                                    // first block scanned (grid x + blk0)
     float scale;
 };
 
@@ -433,6 +435,7 @@ struct AArgs {
     float* out;
     const float* logu_tab;
     int q_bf16, n, nblk, nsb, Hq, Hkv, G, K, L, n_sink, n_local;
+    int ncap;                                    // K/V rows per head in memory
     float scale, log_c2;
     int merge_cap;                               // partials staged per merge round
     int work_bytes;                              // bytes of the list / merge stage region
@@ -444,7 +447,7 @@ template <int G>
 __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int blk = blockIdx.x, bg = blockIdx.y;
+    const int blk = blockIdx.x + a.blk0, bg = blockIdx.y;
     const int b = bg / a.Hkv, g = bg % a.Hkv;
     const int row0 = b * a.Hq + g * G;          // first query row of this KV head's group
     uint32_t* qneg = reinterpret_cast<uint32_t*>(smem);                    // [cpad][G]
@@ -458,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     allow_dependents();
     {
         const int t0 = (a.L * warp) / kWarps;
-        const uint32_t* first = a.codes + (static_cast<size_t>(bg) * a.nblk + blk) * a.C * kWordsPerBlock +
+        const uint32_t* first = a.codes + (static_cast<size_t>(bg) * a.cblk + blk) * a.C * kWordsPerBlock +
                                 static_cast<size_t>(t0) * a.K * kWordsPerBlock;
         const int rows = min(kRingDepth * a.K, ((a.L * (warp + 1)) / kWarps - t0) * a.K);
         for (int r = lane; r < rows; r += 32)
@@ -487,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     {
         const int t0 = (a.L * warp) / kWarps, t1 = (a.L * (warp + 1)) / kWarps;
         const uint32_t* cb0 = a.codes +
-                              (static_cast<size_t>(bg) * a.nblk + blk) * a.C * kWordsPerBlock;
+                              (static_cast<size_t>(bg) * a.cblk + blk) * a.C * kWordsPerBlock;
         const uint32_t* cb = cb0 + lane;
         switch (a.K) {
             case 0:
@@ -666,8 +669,8 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     float m = -INFINITY, l = 0.0f, o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = 0.0f;
-    const KV* Kb = reinterpret_cast<const KV*>(a.keys) + static_cast<size_t>(bg) * a.n * kD + 8 * hl;
-    const KV* Vb = reinterpret_cast<const KV*>(a.values) + static_cast<size_t>(bg) * a.n * kD + 8 * hl;
+    const KV* Kb = reinterpret_cast<const KV*>(a.keys) + static_cast<size_t>(bg) * a.ncap * kD + 8 * hl;
+    const KV* Vb = reinterpret_cast<const KV*>(a.values) + static_cast<size_t>(bg) * a.ncap * kD + 8 * hl;
     constexpr int kStride = 2 * kAWarps;
     const bool weighted = !exact && a.K > 0;
     RowFrag<KV> f0, f1, f2;
@@ -943,7 +946,7 @@ cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, cons
 cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
                            const float* centre, const void* keys, const void* values,
                            bool kv_bf16, const DecodeShape& s, float* out,
-                           const DecodeScratch& ws, cudaStream_t st) {
+                           const DecodeScratch& ws, cudaStream_t st, int blk0) {
     const int G = s.Hq / s.Hkv;
     CArgs ca;
     ca.codes = codes;
@@ -970,14 +973,19 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     ca.cpad = s.cpad;
     ca.n_sink = s.n_sink;
     ca.n_local = s.n_local;
+    ca.cblk = s.cblk;
+    ca.blk0 = blk0;
     ca.scale = s.scale;
     KernelFn scan = pick_collide(G);
     const size_t smem_scan = collide_smem_for(G, s.cpad, s.K);
     if (!scan || smem_scan > kMaxSmem || attend_smem_for(s.nblk) > kMaxSmem)
         return cudaErrorNotSupported;
-    cudaError_t e = launch_dependent(scan, dim3(s.nblk, s.B * s.Hkv), dim3(kThreads), smem_scan,
-                                     st, ca);
-    if (e != cudaSuccess) return e;
+    if (blk0 < 0 || blk0 > s.nblk) return cudaErrorInvalidValue;
+    if (blk0 < s.nblk) {
+        const cudaError_t e = launch_dependent(scan, dim3(s.nblk - blk0, s.B * s.Hkv),
+                                               dim3(kThreads), smem_scan, st, ca);
+        if (e != cudaSuccess) return e;
+    }
     return launch_attend(q, q_bf16, centre, keys, values, kv_bf16, s, out, ws, st);
 }
 
@@ -1012,6 +1020,7 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
     aa.L = s.L;
     aa.n_sink = s.n_sink;
     aa.n_local = s.n_local;
+    aa.ncap = s.ncap;
     aa.scale = s.scale;
     aa.log_c2 = s.L >= 2 ? logf(0.5f * static_cast<float>(s.L) * static_cast<float>(s.L - 1)) : 0.0f;
     {

@@ -72,6 +72,8 @@ struct EncodeArgs {
     uint32_t* codes;
     int* status;
     int C, nchunk, nblk, n, units, parts;
+    int blk0;                       // first block encoded; a unit's block is blk0 + u % nblk
+    int cblk;                       // code blocks per head in memory (the codes' head stride)
 };
 
 // ---- PTX wrappers -----------------------------------------------------------------------------
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int u = u_begin; u < u_end && ok; ++u) {
                 const int bg = u / a.nblk, blk = u % a.nblk;
-                const int rows = min(kKeysPerBlock, a.n - blk * kKeysPerBlock);
+                const int rows = min(kKeysPerBlock, a.n - (a.blk0 + blk) * kKeysPerBlock);
                 const int ntile = (rows + kTileM - 1) / kTileM;
                 for (int t = 0; t < ntile; ++t, ++it) {
                     const int s = it % kStages;
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
                     const uint32_t dst = smem_u32(sA + s * kStageBytes);
-                    const int row0 = blk * kKeysPerBlock + t * kTileM;
+                    const int row0 = (a.blk0 + blk) * kKeysPerBlock + t * kTileM;
                     tma_load_3d(dst, &kmap, bar_full + 8 * s, 0, row0, bg);
                     tma_load_3d(dst + kHalfBytes, &kmap, bar_full + 8 * s, 64, row0, bg);
                 }
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = u_begin; u < u_end && ok; ++u) {
                 const int blk = u % a.nblk;
                 const uint32_t c_slice = static_cast<uint32_t>((u / a.nblk) % kCSlots) * 32;
-                const int rows = min(kKeysPerBlock, a.n - blk * kKeysPerBlock);
+                const int rows = min(kKeysPerBlock, a.n - (a.blk0 + blk) * kKeysPerBlock);
                 const int ntile = (rows + kTileM - 1) / kTileM;
                 for (int t = 0; t < ntile; ++t, ++it) {
                     const int s = it % kStages;
@@ -393,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         auto tiles_in_block = [&](int blk) {
-            const int rows = min(kKeysPerBlock, a.n - blk * kKeysPerBlock);
+            const int rows = min(kKeysPerBlock, a.n - (a.blk0 + blk) * kKeysPerBlock);
             return (rows + kTileM - 1) / kTileM;
         };
         // The next tile whose centre slot has to be ready (two ahead of the one being drained),
@@ -417,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto store_unit = [&](int bg, int blk) {
             epi_sync();
             if (!aborted) {
-                uint32_t* dst = a.codes + (static_cast<size_t>(bg) * a.nblk + blk) *
+                uint32_t* dst = a.codes + (static_cast<size_t>(bg) * a.cblk + a.blk0 + blk) *
                                               static_cast<size_t>(a.C) * kWordsPerBlock +
                                 static_cast<size_t>(j0) * kWordsPerBlock;
                 for (int r = ew; r < Nc; r += kEpiWarps)
@@ -526,17 +528,17 @@ cudaError_t prepare_encode_tc() {
 }
 
 cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* W, int B,
-                             int Hkv, int n, int K, int L, uint32_t* codes, int* status,
-                             cudaStream_t st) {
+                             int Hkv, int ncap, int blk0, int blk1, int K, int L,
+                             uint32_t* codes, int* status, cudaStream_t st) {
     const int C = K * L;
-    if (C == 0 || n == 0) return cudaSuccess;
+    if (C == 0 || blk1 <= blk0) return cudaSuccess;
     EncodeTiledFn enc = encode_tiled_fn();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap map;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(n),
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(ncap),
                                 static_cast<cuuint64_t>(B) * Hkv};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
-                                   static_cast<cuuint64_t>(n) * kD * 2};
+                                   static_cast<cuuint64_t>(ncap) * kD * 2};
     const cuuint32_t box[3] = {64, kTileM, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(keys), dims,
@@ -550,8 +552,10 @@ cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* 
     a.status = status;
     a.C = C;
     a.nchunk = (C + kChunkN - 1) / kChunkN;
-    a.nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
-    a.n = n;
+    a.nblk = blk1 - blk0;
+    a.n = ncap;
+    a.blk0 = blk0;
+    a.cblk = (ncap + kKeysPerBlock - 1) / kKeysPerBlock;
     a.units = B * Hkv * a.nblk;
     int parts = device_sm_count() / a.nchunk;
     if (parts < 1) parts = 1;

@@ -16,6 +16,7 @@ constexpr int kAttendBlockGroup = 4;                // 1024-key blocks per atten
 constexpr int kLogUTableIntervals = 4096;           // log u table over the cosine in [-1, 1]
 constexpr int kMaxBucketBits = 12;                  // bucketed tables: at most 2^12 buckets a table
 constexpr int kBucketRanges = 8;                    // key ranges a table's bucket build is split into
+constexpr int kAppendMaxKeys = 64;                  // mp_encode_keys ranges up to this run on CUDA cores
 
 // Partial softmax states per query row: one per group of kAttendBlockGroup blocks (sampled
 // keys) plus one for the exact sink/local set.
@@ -42,6 +43,9 @@ struct DecodeScratch {
 struct DecodeShape {
     int B, Hq, Hkv, n, d, K, L, C, qwords, nblk, n_sink, n_local;
     int cpad;            // C rounded up to a multiple of 4 (16-byte rows of query masks)
+    int ncap;            // K/V rows per (sequence, KV head) in memory (>= n)
+    int cblk;            // code blocks per (sequence, KV head) in memory: ceil(ncap / 1024)
+    int n_indexed;       // keys in the bucketed tables (<= n)
     float scale;
 };
 
@@ -49,26 +53,33 @@ size_t decode_scratch_bytes(const DecodeShape& s, bool debug);
 DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug);
 
 // ---- launchers (each returns the launch error, cudaSuccess otherwise) -------------------------
-cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int n, float* centre,
+cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int ncap, int n, float* centre,
                             float* partial, int nsplit, cudaStream_t st);
 int key_mean_splits(int n);
 
+// Encode whole 1024-key blocks [blk0, blk1) of every head of a cache laid out for ncap keys
+// per head (keys >= ncap read as zero).
 cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* W, int B,
-                             int Hkv, int n, int K, int L, uint32_t* codes, int* status,
-                             cudaStream_t st);
+                             int Hkv, int ncap, int blk0, int blk1, int K, int L,
+                             uint32_t* codes, int* status, cudaStream_t st);
 cudaError_t launch_encode_simt(const void* keys, bool keys_bf16, const float* centre,
-                               const void* W, bool w_bf16, int B, int Hkv, int n, int K, int L,
-                               uint32_t* codes, cudaStream_t st);
+                               const void* W, bool w_bf16, int B, int Hkv, int ncap, int blk0,
+                               int blk1, int K, int L, uint32_t* codes, cudaStream_t st);
+// Encode keys [n0, n1) (a short range) into their words, keeping the other keys' bits.
+cudaError_t launch_encode_append(const void* keys, bool keys_bf16, const float* centre,
+                                 const void* W, bool w_bf16, int B, int Hkv, int ncap, int n0,
+                                 int n1, int K, int L, uint32_t* codes, cudaStream_t st);
 
 // query sign bits, |q| and q.mu into the scratch; also resets the merge counters
 cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, const void* W,
                            bool w_bf16, const DecodeShape& s, const DecodeScratch& ws,
                            cudaStream_t st);
-// fused collide/select/gather/attend/merge; cudaErrorNotSupported if it cannot fit a CTA
+// the code scan over blocks [blk0, nblk) (selection words of those blocks), then the attend
+// kernel over every block; cudaErrorNotSupported if it cannot fit a CTA
 cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
                            const float* centre, const void* keys, const void* values,
                            bool kv_bf16, const DecodeShape& s, float* out,
-                           const DecodeScratch& ws, cudaStream_t st);
+                           const DecodeScratch& ws, cudaStream_t st, int blk0 = 0);
 bool decode_supported(const DecodeShape& s, bool kv_bf16);
 // the attend kernel alone, on selection words already in ws.selmask (masked with valid & not T)
 cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const void* keys,
@@ -77,9 +88,11 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
 
 // ---- bucketed hash tables (mp_buckets.cu) ------------------------------------------------------
 size_t bucket_table_bytes(int B, int Hkv, int n, int K, int L);   // 0 if unsupported
-cudaError_t launch_bucket_build(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
-                                uint32_t* buckets, cudaStream_t st);
-// ge1 / ge2 bitmaps of the query rows' bucket hits, in the selection-word layout
+// tables of keys [0, n) of codes laid out for cblk blocks per head
+cudaError_t launch_bucket_build(const uint32_t* codes, int B, int Hkv, int cblk, int n, int K,
+                                int L, uint32_t* buckets, cudaStream_t st);
+// ge1 / ge2 bitmaps of the query rows' bucket hits (tables of s.n_indexed keys), in the
+// selection-word layout
 cudaError_t launch_bucket_lookup(const uint32_t* buckets, const uint32_t* qbits,
                                  const DecodeShape& s, uint32_t* ge1, uint32_t* ge2,
                                  cudaStream_t st);

@@ -16,8 +16,8 @@ constexpr int kMeanThreads = 256;
 // to finish (release-acquire counter) adds the head's partials in range order and writes mu.
 template <typename T>
 __global__ void __launch_bounds__(kMeanThreads)
-    key_mean_kernel(const T* keys, int n, int nsplit, float* partial, unsigned* counters,
-                    float* centre) {
+    key_mean_kernel(const T* keys, int ncap, int n, int nsplit, float* partial,
+                    unsigned* counters, float* centre) {
     // thread -> (column group of 16 bytes, row phase); rows stride by the number of row phases
     constexpr int kPer = 16 / sizeof(T);                 // elements per 16-byte load
     constexpr int kGroups = kD / kPer;                   // column groups per row
@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(kMeanThreads)
     const int bh = blockIdx.y, split = blockIdx.x, tid = threadIdx.x;
     const int cg = tid % kGroups, ph = tid / kGroups;
     const int r0 = split * kMeanRows, r1 = min(n, r0 + kMeanRows);
-    const T* base = keys + static_cast<size_t>(bh) * n * kD + cg * kPer;
+    const T* base = keys + static_cast<size_t>(bh) * ncap * kD + cg * kPer;
     float acc[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) acc[i] = 0.0f;
@@ -73,30 +73,31 @@ __global__ void __launch_bounds__(kMeanThreads)
 // ------------------------------------------------------------------------------------------------
 // fp32 CUDA-core encoder for dtype pairs the tensor-core path does not take (fp32 keys or W):
 // bit_{i,j} = [sum_e W[e][j] (k_i[e] - mu[e]) > 0] in fp32, one key per thread, a warp's 32 keys
-// form one word per hyperplane through a ballot.
+// form one word per hyperplane through a ballot. Whole 1024-key blocks from blk0 on (keys at or
+// past ncap read as zero).
 // ------------------------------------------------------------------------------------------------
 constexpr int kSimtKeys = 64;      // keys per CTA (2 words)
 constexpr int kSimtPlanes = 16;    // hyperplanes per pass
 
 __global__ void __launch_bounds__(kSimtKeys)
     encode_simt_kernel(const void* keys, int keys_bf16, const float* centre, const void* W,
-                       int w_bf16, int n, int C, int nblk, uint32_t* codes) {
+                       int w_bf16, int ncap, int C, int cblk, int blk0, uint32_t* codes) {
     __shared__ float kbar[kSimtKeys][kD + 1];
     __shared__ float Wsm[kD][kSimtPlanes];
     const int bh = blockIdx.y, tile = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     const int warp = tid >> 5;
-    const int i0 = tile * kSimtKeys;
+    const int i0 = blk0 * kKeysPerBlock + tile * kSimtKeys;
     for (int idx = tid; idx < kSimtKeys * kD; idx += kSimtKeys) {
         const int r = idx / kD, e = idx % kD, i = i0 + r;
         float v = 0.0f;
-        if (i < n)
-            v = load_elem(keys, keys_bf16, (static_cast<size_t>(bh) * n + i) * kD + e) -
+        if (i < ncap)
+            v = load_elem(keys, keys_bf16, (static_cast<size_t>(bh) * ncap + i) * kD + e) -
                 centre[static_cast<size_t>(bh) * kD + e];
         kbar[r][e] = v;
     }
     const int blk = i0 / kKeysPerBlock;
     const int word = (i0 % kKeysPerBlock) / 32 + warp;
-    uint32_t* dst = codes + (static_cast<size_t>(bh) * nblk + blk) * static_cast<size_t>(C) *
+    uint32_t* dst = codes + (static_cast<size_t>(bh) * cblk + blk) * static_cast<size_t>(C) *
                                 kWordsPerBlock + word;
     for (int j0 = 0; j0 < C; j0 += kSimtPlanes) {
         __syncthreads();
@@ -122,6 +123,51 @@ __global__ void __launch_bounds__(kSimtKeys)
         if (lane < kSimtPlanes && j0 + lane < C)
             dst[static_cast<size_t>(j0 + lane) * kWordsPerBlock] = mine;
     }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Append: keys [n0, n1) of a short range (<= kAppendMaxKeys) into the words they share with other
+// keys. One CTA per (chunk of 32 hyperplanes, head); warp w takes the range's w-th 32-key word,
+// lane j hyperplane j0 + j, and rewrites that word's bits of the range only (each (plane, word)
+// has one owner, so a plain read-modify-write). Same fp32 arithmetic as encode_simt_kernel: the
+// sum over e in order of W[e][j] (k[e] - mu[e]).
+// ------------------------------------------------------------------------------------------------
+constexpr int kAppendWarps = (kAppendMaxKeys + 31) / 32 + 1;   // words a range can touch
+
+__global__ void __launch_bounds__(kAppendWarps * 32)
+    encode_append_kernel(const void* keys, int keys_bf16, const float* centre, const void* W,
+                         int w_bf16, int ncap, int n0, int n1, int C, int cblk, uint32_t* codes) {
+    __shared__ float kbar[kAppendMaxKeys][kD];
+    const int bh = blockIdx.y, j0 = blockIdx.x * 32, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int m = n1 - n0;
+    for (int idx = tid; idx < m * kD; idx += kAppendWarps * 32) {
+        const int r = idx / kD, e = idx % kD;
+        kbar[r][e] = load_elem(keys, keys_bf16, (static_cast<size_t>(bh) * ncap + n0 + r) * kD + e) -
+                     centre[static_cast<size_t>(bh) * kD + e];
+    }
+    __syncthreads();
+    const int w = n0 / 32 + warp;                       // absolute 32-key word
+    const int k0 = max(n0, w * 32), k1 = min(n1, w * 32 + 32);
+    const int j = j0 + lane;
+    if (k0 >= k1 || j >= C) return;
+    float P[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r) P[r] = 0.0f;
+    for (int e = 0; e < kD; ++e) {
+        const float wv = load_elem(W, w_bf16, static_cast<size_t>(e) * C + j);
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            if (k0 + r < k1) P[r] = fmaf(wv, kbar[k0 + r - n0][e], P[r]);
+    }
+    uint32_t bits = 0u;
+#pragma unroll
+    for (int r = 0; r < 32; ++r)
+        if (k0 + r < k1 && P[r] > 0.0f) bits |= 1u << ((k0 + r) & 31);
+    const uint32_t range = bits_below(k1 - w * 32) & ~bits_below(k0 - w * 32);
+    uint32_t* dst = codes + ((static_cast<size_t>(bh) * cblk + w / kWordsPerBlock) * C + j) *
+                                kWordsPerBlock + w % kWordsPerBlock;
+    *dst = (*dst & ~range) | bits;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -205,7 +251,7 @@ __global__ void codes_unpack_kernel(const uint32_t* codes, int n, int nblk, int 
 
 int key_mean_splits(int n) { return (n + kMeanRows - 1) / kMeanRows; }
 
-cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int n, float* centre,
+cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int ncap, int n, float* centre,
                             float* partial, int nsplit, cudaStream_t st) {
     // the per-head counters follow the partial sums in the workspace; they start at zero
     unsigned* counters = reinterpret_cast<unsigned*>(partial + static_cast<size_t>(BH) * nsplit * kD);
@@ -214,22 +260,36 @@ cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int n, float* c
     const dim3 grid(nsplit, BH);
     if (bf16)
         key_mean_kernel<__nv_bfloat16><<<grid, kMeanThreads, 0, st>>>(
-            reinterpret_cast<const __nv_bfloat16*>(keys), n, nsplit, partial, counters, centre);
+            reinterpret_cast<const __nv_bfloat16*>(keys), ncap, n, nsplit, partial, counters,
+            centre);
     else
         key_mean_kernel<float><<<grid, kMeanThreads, 0, st>>>(
-            reinterpret_cast<const float*>(keys), n, nsplit, partial, counters, centre);
+            reinterpret_cast<const float*>(keys), ncap, n, nsplit, partial, counters, centre);
     return cudaGetLastError();
 }
 
 cudaError_t launch_encode_simt(const void* keys, bool keys_bf16, const float* centre,
-                               const void* W, bool w_bf16, int B, int Hkv, int n, int K, int L,
-                               uint32_t* codes, cudaStream_t st) {
+                               const void* W, bool w_bf16, int B, int Hkv, int ncap, int blk0,
+                               int blk1, int K, int L, uint32_t* codes, cudaStream_t st) {
     const int C = K * L;
-    if (C == 0 || n == 0) return cudaSuccess;
-    const int nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
-    const dim3 grid((n + kSimtKeys - 1) / kSimtKeys, B * Hkv);
-    encode_simt_kernel<<<grid, kSimtKeys, 0, st>>>(keys, keys_bf16, centre, W, w_bf16, n, C,
-                                                    nblk, codes);
+    if (C == 0 || blk1 <= blk0) return cudaSuccess;
+    const int cblk = (ncap + kKeysPerBlock - 1) / kKeysPerBlock;
+    const dim3 grid((blk1 - blk0) * (kKeysPerBlock / kSimtKeys), B * Hkv);
+    encode_simt_kernel<<<grid, kSimtKeys, 0, st>>>(keys, keys_bf16, centre, W, w_bf16, ncap, C,
+                                                    cblk, blk0, codes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_encode_append(const void* keys, bool keys_bf16, const float* centre,
+                                 const void* W, bool w_bf16, int B, int Hkv, int ncap, int n0,
+                                 int n1, int K, int L, uint32_t* codes, cudaStream_t st) {
+    const int C = K * L;
+    if (C == 0 || n1 <= n0) return cudaSuccess;
+    if (n1 - n0 > kAppendMaxKeys) return cudaErrorInvalidValue;
+    const int cblk = (ncap + kKeysPerBlock - 1) / kKeysPerBlock;
+    const dim3 grid((C + 31) / 32, B * Hkv);
+    encode_append_kernel<<<grid, kAppendWarps * 32, 0, st>>>(keys, keys_bf16, centre, W, w_bf16,
+                                                             ncap, n0, n1, C, cblk, codes);
     return cudaGetLastError();
 }
 
@@ -242,7 +302,7 @@ cudaError_t launch_compact_selection(const uint32_t* selmask, int rows, int n, i
 cudaError_t launch_collision_counts(const uint32_t* codes, const uint32_t* qbits,
                                     const DecodeShape& s, uint8_t* cnt, cudaStream_t st) {
     const dim3 grid((s.n + 255) / 256, s.B * s.Hq);
-    collision_counts_kernel<<<grid, 256, 0, st>>>(codes, qbits, s.n, s.nblk, s.Hq, s.Hq / s.Hkv,
+    collision_counts_kernel<<<grid, 256, 0, st>>>(codes, qbits, s.n, s.cblk, s.Hq, s.Hq / s.Hkv,
                                                   s.K, s.L, s.qwords, cnt);
     return cudaGetLastError();
 }
@@ -261,6 +321,7 @@ cudaError_t prepare_misc() {
     if ((e = cudaFuncGetAttributes(&fa, key_mean_kernel<float>)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, key_mean_kernel<__nv_bfloat16>)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, encode_simt_kernel)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, encode_append_kernel)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, compact_selection_kernel)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, collision_counts_kernel)) != cudaSuccess) return e;
     return cudaFuncGetAttributes(&fa, codes_unpack_kernel);

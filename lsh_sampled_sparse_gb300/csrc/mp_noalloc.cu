@@ -77,6 +77,9 @@ extern "C" mp_status mp_decode_attention_noalloc(
     s.qwords = (s.C + 31) / 32;
     s.cpad = (s.C + 3) & ~3;
     s.nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
+    s.ncap = prm->n_capacity > 0 ? prm->n_capacity : n;
+    s.cblk = (s.ncap + kKeysPerBlock - 1) / kKeysPerBlock;
+    s.n_indexed = prm->n_indexed > 0 ? prm->n_indexed : n;
     s.n_sink = prm->n_sink;
     s.n_local = prm->n_local;
     s.scale = prm->scale > 0.0f ? prm->scale : 1.0f / sqrtf(static_cast<float>(d));

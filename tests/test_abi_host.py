@@ -39,7 +39,9 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_status_strings_and_version(L):
     import lsh_sampled_sparse_gb300 as mp
-    assert mp.abi_version() == 1
+    header_version = int(re.search(r"#define MP_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
+    assert mp.abi_version() == header_version
+    assert ctypes.sizeof(mp.Params) == 32          # mp_params: 8 four-byte fields
     names = [L.mp_status_string(i).decode() for i in range(6)]
     assert names == ["MP_OK", "MP_ERR_INVALID_ARG", "MP_ERR_UNSUPPORTED", "MP_ERR_CUDA",
                      "MP_ERR_TIMEOUT", "MP_ERR_WORKSPACE"]
@@ -122,6 +124,37 @@ def test_build_and_mean_reject_bad_arguments(L):
     assert L.mp_key_mean(ok, 1, 1, 1, 0, 128, ok, ok, 1 << 20, None) == 1
     assert L.mp_key_mean(ok, 1, 1, 1, 100, 64, ok, ok, 1 << 20, None) == 2
     assert L.mp_key_mean(ok, 1, 1, 8, 98304, 128, ok, ok, 16, None) == 5
+
+
+def test_capacity_and_append_reject_bad_arguments(L):
+    import lsh_sampled_sparse_gb300 as mp
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    INVALID = 1
+
+    def ws(n, n_capacity=0, n_indexed=0):
+        p = mp.Params(10, 150, 4, 64, 0.0, 0, n_capacity, n_indexed)
+        return L.mp_decode_workspace_bytes(1, 4, 1, n, 128, ctypes.byref(p))
+    assert ws(1000) > 0 and ws(1000, 4096) == ws(1000) and ws(1000, 0, 500) == ws(1000)
+    assert ws(1000, 999) == 0                     # capacity below the length
+    assert ws(1000, -1) == 0
+    assert ws(1000, 0, 1001) == 0                 # more keys indexed than cached
+    # mp_encode_keys(keys, dt, centre, W, wdt, B, Hkv, n_capacity, n_begin, n_end, d, K, L, codes)
+    def enc(cap, n0, n1, d=128, K=10, keys=ok):
+        return L.mp_encode_keys(keys, 1, ok, ok, 1, 1, 1, cap, n0, n1, d, K, 150, ok, None)
+    assert enc(4096, 100, 4097) == INVALID        # past the capacity
+    assert enc(4096, -1, 10) == INVALID
+    assert enc(4096, 20, 10) == INVALID           # reversed range
+    assert enc(4096, 0, 10, d=64) == 2
+    assert enc(4096, 0, 10, keys=None) == INVALID
+    assert enc(4096, 10, 10, keys=None) == 0      # empty range: nothing touched
+    assert enc(4096, 0, 10, K=0, keys=None) == 0  # no hyperplanes
+    assert L.mp_key_mean_cap(ok, 1, 1, 1, 99, 100, 128, ok, ok, 1 << 20, None) == INVALID
+    assert L.mp_build_buckets_cap(ok, 1, 1, 99, 100, 10, 150, ok, None) == INVALID
+    # the bucketed decode needs the codes for keys appended after the tables were built
+    p = mp.Params(10, 150, 4, 64, 0.0, 0, 0, 500)
+    assert L.mp_sampled_attention_buckets(ok, 1, ok, None, ok, ok, ok, 1, 1, 4, 1, 1000, 128,
+                                          ctypes.byref(p), ok, ok, 1 << 24, None) == INVALID
 
 
 def test_binding_refuses_cpu_tensors(L):
