@@ -276,6 +276,37 @@ def run_decode_only(mp, wl, W, state, ws_dec, steps: int, use_graph: bool) -> fl
     return begin.elapsed_time(end) / steps
 
 
+def run_append(mp, wl, W, state, steps: int, use_graph: bool) -> float:
+    """us per layer to append one decode token's key (mp_encode_keys over one key, here the
+    last cached key re-encoded in place), K steps over every layer in one CUDA graph."""
+    stream = torch.cuda.current_stream()
+
+    def step(strm):
+        for s in state:
+            mp.encode_keys(s.keys, s.centre, W, wl.K, wl.L, wl.n - 1, wl.n, s.codes, stream=strm)
+    for _ in range(3):
+        step(stream)
+    torch.cuda.synchronize()
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream()
+            for _ in range(steps):
+                step(cap)
+    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    begin.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(steps):
+            step(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return begin.elapsed_time(end) * 1e3 / (steps * len(state))
+
+
 def run_buckets(mp, wl, W, state, ws_dec, steps: int, use_graph: bool, peaks):
     """The bucketed-table retrieval (mp_build_buckets + mp_sampled_attention_buckets) on the same
     layers: build time per layer, then K decode steps (query encode + bucket lookup + gather /
@@ -612,6 +643,7 @@ def run_ours(args):
         else "of fallback"
 
     decode_ms = run_decode_only(mp, wl, W, state, ws_dec, args.steps, graph is not None)
+    append_us = run_append(mp, wl, W, state, args.steps, graph is not None)
     line = {
         "metric": METRIC,
         "value": value,
@@ -646,6 +678,9 @@ def run_ours(args):
             "queries_per_s": world * queries_per_step / (decode_ms / 1e3),
             "attention_ms_per_token": decode_ms,
             "sampled_attention_gbs": rooflines["sampled_attention"]["achieved"],
+            "append_us_per_layer": append_us,
+            "append_note": "mp_encode_keys of one new key per layer (all heads), the incremental "
+                           "append a decode step adds before its attention",
         },
         "sample_sets": {
             "mean_union_rows_per_kv_head": alg["mean_union_rows"],

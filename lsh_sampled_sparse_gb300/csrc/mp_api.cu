@@ -38,7 +38,7 @@ bool ensure_prepared() {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return false;
     if (prepare_misc() != cudaSuccess || prepare_decode() != cudaSuccess ||
-        prepare_buckets() != cudaSuccess)
+        prepare_buckets() != cudaSuccess || prepare_append() != cudaSuccess)
         return false;
     prepare_encode_tc();   // failure only disables the tensor-core encoder
     cudaGetLastError();

@@ -110,6 +110,7 @@ cudaError_t launch_codes_unpack(const uint32_t* codes, int BH, int n, int K, int
 cudaError_t prepare_encode_tc();
 cudaError_t prepare_decode();
 cudaError_t prepare_misc();
+cudaError_t prepare_append();
 
 // ---- small device helpers ---------------------------------------------------------------------
 __device__ __forceinline__ float to_float(float x) { return x; }

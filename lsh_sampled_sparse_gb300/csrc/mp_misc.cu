@@ -126,51 +126,6 @@ __global__ void __launch_bounds__(kSimtKeys)
 }
 
 // ------------------------------------------------------------------------------------------------
-// Append: keys [n0, n1) of a short range (<= kAppendMaxKeys) into the words they share with other
-// keys. One CTA per (chunk of 32 hyperplanes, head); warp w takes the range's w-th 32-key word,
-// lane j hyperplane j0 + j, and rewrites that word's bits of the range only (each (plane, word)
-// has one owner, so a plain read-modify-write). Same fp32 arithmetic as encode_simt_kernel: the
-// sum over e in order of W[e][j] (k[e] - mu[e]).
-// ------------------------------------------------------------------------------------------------
-constexpr int kAppendWarps = (kAppendMaxKeys + 31) / 32 + 1;   // words a range can touch
-
-__global__ void __launch_bounds__(kAppendWarps * 32)
-    encode_append_kernel(const void* keys, int keys_bf16, const float* centre, const void* W,
-                         int w_bf16, int ncap, int n0, int n1, int C, int cblk, uint32_t* codes) {
-    __shared__ float kbar[kAppendMaxKeys][kD];
-    const int bh = blockIdx.y, j0 = blockIdx.x * 32, tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5;
-    const int m = n1 - n0;
-    for (int idx = tid; idx < m * kD; idx += kAppendWarps * 32) {
-        const int r = idx / kD, e = idx % kD;
-        kbar[r][e] = load_elem(keys, keys_bf16, (static_cast<size_t>(bh) * ncap + n0 + r) * kD + e) -
-                     centre[static_cast<size_t>(bh) * kD + e];
-    }
-    __syncthreads();
-    const int w = n0 / 32 + warp;                       // absolute 32-key word
-    const int k0 = max(n0, w * 32), k1 = min(n1, w * 32 + 32);
-    const int j = j0 + lane;
-    if (k0 >= k1 || j >= C) return;
-    float P[32];
-#pragma unroll
-    for (int r = 0; r < 32; ++r) P[r] = 0.0f;
-    for (int e = 0; e < kD; ++e) {
-        const float wv = load_elem(W, w_bf16, static_cast<size_t>(e) * C + j);
-#pragma unroll
-        for (int r = 0; r < 32; ++r)
-            if (k0 + r < k1) P[r] = fmaf(wv, kbar[k0 + r - n0][e], P[r]);
-    }
-    uint32_t bits = 0u;
-#pragma unroll
-    for (int r = 0; r < 32; ++r)
-        if (k0 + r < k1 && P[r] > 0.0f) bits |= 1u << ((k0 + r) & 31);
-    const uint32_t range = bits_below(k1 - w * 32) & ~bits_below(k0 - w * 32);
-    uint32_t* dst = codes + ((static_cast<size_t>(bh) * cblk + w / kWordsPerBlock) * C + j) *
-                                kWordsPerBlock + w % kWordsPerBlock;
-    *dst = (*dst & ~range) | bits;
-}
-
-// ------------------------------------------------------------------------------------------------
 // Inspection kernels
 // ------------------------------------------------------------------------------------------------
 // Per query row: ascending indices of the selected keys from the per-block selection words.
@@ -280,19 +235,6 @@ cudaError_t launch_encode_simt(const void* keys, bool keys_bf16, const float* ce
     return cudaGetLastError();
 }
 
-cudaError_t launch_encode_append(const void* keys, bool keys_bf16, const float* centre,
-                                 const void* W, bool w_bf16, int B, int Hkv, int ncap, int n0,
-                                 int n1, int K, int L, uint32_t* codes, cudaStream_t st) {
-    const int C = K * L;
-    if (C == 0 || n1 <= n0) return cudaSuccess;
-    if (n1 - n0 > kAppendMaxKeys) return cudaErrorInvalidValue;
-    const int cblk = (ncap + kKeysPerBlock - 1) / kKeysPerBlock;
-    const dim3 grid((C + 31) / 32, B * Hkv);
-    encode_append_kernel<<<grid, kAppendWarps * 32, 0, st>>>(keys, keys_bf16, centre, W, w_bf16,
-                                                             ncap, n0, n1, C, cblk, codes);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_compact_selection(const uint32_t* selmask, int rows, int n, int nblk,
                                      int32_t* sel_idx, int32_t* sel_count, cudaStream_t st) {
     compact_selection_kernel<<<rows, 32, 0, st>>>(selmask, n, nblk, sel_idx, sel_count);
@@ -321,7 +263,6 @@ cudaError_t prepare_misc() {
     if ((e = cudaFuncGetAttributes(&fa, key_mean_kernel<float>)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, key_mean_kernel<__nv_bfloat16>)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, encode_simt_kernel)) != cudaSuccess) return e;
-    if ((e = cudaFuncGetAttributes(&fa, encode_append_kernel)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, compact_selection_kernel)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, collision_counts_kernel)) != cudaSuccess) return e;
     return cudaFuncGetAttributes(&fa, codes_unpack_kernel);
