@@ -50,6 +50,10 @@ Parity status (what pins each function; the tests under tests/ hold the pins):
       Horvitz-Thompson unbiasedness of the importance weights over hyperplane seeds
   full_attention                                            textbook special cases (uniform
       scores give the mean value; one dominant score gives its value)
+  mips_* / encode_keys_mips / collision_probability_mips   augmented keys have length r; the
+      formula equals the plain cosine of the augmented vectors; Monte-Carlo bit agreement over
+      fresh (d+1)-row hyperplanes; p follows the inner product where the plain cosine does not;
+      brute-force codes; Horvitz-Thompson unbiasedness with the variant's u
 """
 from __future__ import annotations
 
@@ -65,7 +69,8 @@ __all__ = [
     "near_tie_mask", "encode_keys", "encode_query", "collision_counts", "exact_set_mask",
     "sampled_set", "collision_probability", "log_inclusion_probability",
     "inclusion_probability", "snis_attention", "full_attention", "decode_head", "decode",
-    "replay_bits", "as64", "bucket_tables", "bucket_collision_counts",
+    "replay_bits", "as64", "bucket_tables", "bucket_collision_counts", "mips_radius",
+    "mips_augment_keys", "mips_augment_query", "encode_keys_mips", "collision_probability_mips",
 ]
 
 
@@ -215,6 +220,62 @@ def collision_probability(q, kbar) -> np.ndarray:
     return 1.0 - np.arccos(cos) / math.pi
 
 
+# ----------------------------------------------------------------------------------------------
+# MIPS -> cosine variant ("LSH Sampling...", method details, variance reduction with LSH: with
+# r = max_i |k_i|, q is extended by a 0 and k_i by sqrt(r^2 - |k_i|^2), so that every extended
+# key has length r and the cosine of the extended pair is q.k_i / (|q| r), an increasing function
+# of the inner product). The keys extended here are the centred ones: the centring of the data
+# preprocessing step comes before the tables are built. W then has d + 1 rows; the query's extra
+# coordinate is 0, so its bits use only the first d rows.
+# ----------------------------------------------------------------------------------------------
+def mips_radius(keys, centre) -> float:
+    """r = max_i |k_i - mu| over the keys given (0 for no keys)."""
+    kbar = as64(keys) - as64(centre)[None, :]
+    return float(np.max(np.linalg.norm(kbar, axis=1))) if kbar.shape[0] else 0.0
+
+
+def mips_augment_keys(keys, centre, r: float) -> np.ndarray:
+    """khat_i = [k_i - mu, sqrt(max(0, r^2 - |k_i - mu|^2))], [n, d + 1]: length r for every key
+    no longer than r (a key appended later and longer than r gets 0 and keeps its length)."""
+    kbar = as64(keys) - as64(centre)[None, :]
+    extra = np.sqrt(np.maximum(0.0, r * r - np.sum(kbar * kbar, axis=1)))
+    return np.concatenate([kbar, extra[:, None]], axis=1)
+
+
+def mips_augment_query(q) -> np.ndarray:
+    """qhat = [q, 0], [m, d + 1]."""
+    qv = np.atleast_2d(as64(q))
+    return np.concatenate([qv, np.zeros((qv.shape[0], 1))], axis=1)
+
+
+def encode_keys_mips(keys, centre, W_aug, r: float, K: int, L: int):
+    """Codes of the extended centred keys on the d + 1 rows of W_aug: (codes [n, L], bits, near).
+
+    Near ties: |P_ij| < 1e-5 |w_j| (|k_i| + r) with w_j the full column, since an evaluation that
+    projects the raw key, subtracts w_j.mu and adds the extra term makes rounding errors of that
+    size."""
+    k = as64(keys)
+    Wa = as64(W_aug)
+    khat = mips_augment_keys(k, centre, r)
+    P = simhash_projections(khat, Wa)
+    bits = sign_bits(P)
+    wn = np.linalg.norm(Wa, axis=0)
+    scale = np.linalg.norm(k, axis=1) + r
+    near = np.abs(P) < NEAR_TIE_REL * scale[:, None] * wn[None, :]
+    return table_codes(bits, K, L), bits, near
+
+
+def collision_probability_mips(q, kbar, r: float) -> np.ndarray:
+    """p_i = 1 - arccos(q.kbar_i / (|q| r))/pi, the cosine clipped to [-1, 1] (a key longer
+    than r would exceed it); cosine 0 when q or r is 0."""
+    qv = as64(q)
+    kb = np.atleast_2d(as64(kbar))
+    qn = float(np.linalg.norm(qv))
+    dots = kb @ qv
+    cos = np.zeros_like(dots) if qn == 0.0 or r == 0.0 else np.clip(dots / (qn * r), -1.0, 1.0)
+    return 1.0 - np.arccos(cos) / math.pi
+
+
 def _log_u_scalar(p: float, K: int, L: int) -> float:
     if L < 2:
         return -math.inf                      # at most one table can collide: u = 0
@@ -286,8 +347,10 @@ def full_attention(q, keys, values, scale: float) -> np.ndarray:
 # One query head, and a whole batch
 # ----------------------------------------------------------------------------------------------
 def decode_head(q, keys, values, centre, key_codes, q_code, K: int, L: int, n_sink: int,
-                n_local: int, scale: float | None = None, centred_scores: bool = False) -> dict:
-    """Steps 3-6 for one query head against its KV head's codes."""
+                n_local: int, scale: float | None = None, centred_scores: bool = False,
+                radius: float | None = None) -> dict:
+    """Steps 3-6 for one query head against its KV head's codes. With `radius` (the MIPS variant)
+    p uses q.kbar_i / (|q| r) in place of the cosine."""
     qv = as64(q)
     k = as64(keys)
     v = as64(values)
@@ -299,7 +362,8 @@ def decode_head(q, keys, values, centre, key_codes, q_code, K: int, L: int, n_si
     T = exact_set_mask(n, n_sink, n_local)
     S = sampled_set(cnt, T)
     kbar_S = k[S] - mu[None, :]
-    p = collision_probability(qv, kbar_S)
+    p = collision_probability(qv, kbar_S) if radius is None else \
+        collision_probability_mips(qv, kbar_S, radius)
     logu = log_inclusion_probability(p, K, L) if S.size else np.zeros(0)
     Tidx = np.nonzero(T)[0]
     if centred_scores:
@@ -328,8 +392,12 @@ def replay_bits(oracle_bits, near, other_bits, what: str = "bits"):
 
 
 def decode(q, keys, values, centre, W, K: int, L: int, n_sink: int, n_local: int,
-           scale: float | None = None, key_bits_override=None, q_bits_override=None) -> dict:
+           scale: float | None = None, key_bits_override=None, q_bits_override=None,
+           radius=None) -> dict:
     """The whole step for a batch. q [B, Hq, d]; keys, values [B, Hkv, n, d]; centre [B, Hkv, d].
+
+    radius [B, Hkv], when given, selects the MIPS variant: W has d + 1 rows, the keys are hashed
+    extended (encode_keys_mips) and p uses the radius; the query uses the first d rows.
 
     key_bits_override[b][g] / q_bits_override[b][h], when given, replace the oracle's own sign
     bits (used after replay_bits has checked that they differ only at near-ties).
@@ -346,19 +414,24 @@ def decode(q, keys, values, centre, W, K: int, L: int, n_sink: int, n_local: int
     qbits_all = np.zeros((B, Hq, K * L), dtype=bool)
     for b in range(B):
         for g in range(Hkv):
-            kcodes, kbits, _ = encode_keys(ka[b, g], ca[b, g], W, K, L)
+            if radius is None:
+                kcodes, kbits, _ = encode_keys(ka[b, g], ca[b, g], W, K, L)
+            else:
+                kcodes, kbits, _ = encode_keys_mips(ka[b, g], ca[b, g], W, float(radius[b][g]),
+                                                    K, L)
             if key_bits_override is not None:
                 kbits = np.asarray(key_bits_override[b][g], dtype=bool)
                 kcodes = table_codes(kbits, K, L)
             kbits_all[b][g] = kbits
             for h in range(g * G, (g + 1) * G):
-                qcodes, qbits, _ = encode_query(qa[b, h], W, K, L)
+                qcodes, qbits, _ = encode_query(qa[b, h], as64(W)[:d], K, L)
                 if q_bits_override is not None:
                     qbits = np.asarray(q_bits_override[b][h], dtype=bool).reshape(1, -1)
                     qcodes = table_codes(qbits, K, L)
                 qbits_all[b, h] = qbits[0]
                 r = decode_head(qa[b, h], ka[b, g], va[b, g], ca[b, g], kcodes, qcodes[0], K, L,
-                                n_sink, n_local, scale)
+                                n_sink, n_local, scale,
+                                radius=None if radius is None else float(radius[b][g]))
                 o[b, h] = r["o"]
                 cnt[b, h] = r["cnt"]
                 sets[b][h] = r["S"]

@@ -428,3 +428,107 @@ def test_page_arithmetic_matches_the_96k_workload():
     assert abs(100 * 4 * entries / key_bytes - g["scan_fraction_percent"]["value"]) < 0.005
     projector = wl.d * wl.C * 2                    # bf16 projector
     assert abs(projector / 1000 - g["projector_kb"]["value"]) < 0.05 * g["projector_kb"]["value"]
+
+
+# ------------------------------------------------------------------------------------------------
+# MIPS -> cosine variant ("LSH Sampling..." method details, variance reduction with LSH: keys
+# extended by sqrt(r^2 - |k|^2), the query by 0, r the longest key; here the centred keys)
+# ------------------------------------------------------------------------------------------------
+def _mips_case(seed, n=12, d=5):
+    rng = np.random.default_rng(seed)
+    keys = rng.standard_normal((n, d)) * rng.uniform(0.3, 2.0, size=(n, 1))
+    q = rng.standard_normal(d)
+    return keys, q, O.key_centre(keys)
+
+
+def test_mips_radius_and_extended_lengths():
+    keys, q, mu = _mips_case(21)
+    want_r = max(math.sqrt(sum((k[e] - mu[e]) ** 2 for e in range(len(mu)))) for k in keys)
+    r = O.mips_radius(keys, mu)
+    assert abs(r - want_r) < 1e-12
+    khat = O.mips_augment_keys(keys, mu, r)
+    assert np.allclose(np.linalg.norm(khat, axis=1), r, rtol=0, atol=1e-12)
+    assert np.allclose(khat[:, :-1], keys - mu, rtol=0, atol=0)
+    assert np.all(khat[:, -1] >= 0)
+    assert O.mips_augment_query(q).tolist() == [list(q) + [0.0]]
+
+
+def test_mips_probability_is_the_plain_cosine_of_the_extended_pair():
+    keys, q, mu = _mips_case(22)
+    r = O.mips_radius(keys, mu)
+    plain = O.collision_probability(O.mips_augment_query(q)[0], O.mips_augment_keys(keys, mu, r))
+    assert np.allclose(O.collision_probability_mips(q, keys - mu, r), plain, rtol=0, atol=1e-12)
+
+
+def test_mips_bit_agreement_monte_carlo():
+    # each extended key agrees with the query on one hyperplane of d + 1 rows with probability
+    # p_mips; the query's bits come from the first d rows only
+    keys, q, mu = _mips_case(23, n=4)
+    r = O.mips_radius(keys, mu)
+    rng = np.random.default_rng(24)
+    N = 100_000
+    W = rng.standard_normal((keys.shape[1] + 1, N))
+    _, kbits, _ = O.encode_keys_mips(keys, mu, W, r, 1, N)
+    _, qbits, _ = O.encode_query(q, W[:-1], 1, N)
+    p = O.collision_probability_mips(q, keys - mu, r)
+    for i in range(keys.shape[0]):
+        freq = float(np.mean(kbits[i] == qbits[0]))
+        sigma = math.sqrt(p[i] * (1 - p[i]) / N)
+        assert abs(freq - p[i]) < 4.5 * sigma, (i, freq, p[i], sigma)
+
+
+def test_mips_probability_follows_the_inner_product():
+    # a short key along q has the larger cosine, a long key at an angle the larger inner
+    # product: the plain probability ranks the short key first, the MIPS variant the long one
+    q = np.array([1.0, 0.0, 0.0])
+    mu = np.zeros(3)
+    keys = np.array([[0.5, 0.05, 0.0], [3.0, 2.0, 0.0], [0.0, 0.0, 1.0]])
+    r = O.mips_radius(keys, mu)
+    plain = O.collision_probability(q, keys)
+    mips = O.collision_probability_mips(q, keys, r)
+    assert plain[0] > plain[1] and mips[1] > mips[0]
+    order = np.argsort(keys @ q)
+    assert np.all(np.diff(mips[order]) > 0)
+
+
+def test_mips_codes_by_brute_force():
+    keys, q, mu = _mips_case(25, n=6, d=3)
+    K, L = 2, 3
+    rng = np.random.default_rng(26)
+    W = rng.standard_normal((4, K * L))
+    r = O.mips_radius(keys, mu)
+    codes, _, _ = O.encode_keys_mips(keys, mu, W, r, K, L)
+    for i, k in enumerate(keys):
+        kb = [k[e] - mu[e] for e in range(3)]
+        a = math.sqrt(max(0.0, r * r - sum(x * x for x in kb)))
+        for t in range(L):
+            c = 0
+            for b in range(K):
+                j = t * K + b
+                P = sum(W[e][j] * kb[e] for e in range(3)) + W[3][j] * a
+                c |= (1 if P > 0 else 0) << b
+            assert codes[i, t] == c
+
+
+def test_mips_importance_weights_are_unbiased_over_hyperplane_draws():
+    # Horvitz-Thompson with the variant's inclusion probability: fails if p ignored the radius
+    # or the query took the extra row
+    rng = np.random.default_rng(27)
+    d, n, K, L, M = 6, 40, 2, 6, 20000
+    keys = rng.standard_normal((n, d)) * rng.uniform(0.5, 1.5, size=(n, 1))
+    vals = rng.standard_normal((n, d))
+    q = rng.standard_normal(d)
+    mu = O.key_centre(keys)
+    r = O.mips_radius(keys, mu)
+    s = keys @ q / math.sqrt(d)
+    logu = O.log_inclusion_probability(O.collision_probability_mips(q, keys - mu, r), K, L)
+    W = rng.standard_normal((d + 1, M * K * L))
+    kc = O.encode_keys_mips(keys, mu, W, r, K, M * L)[0].reshape(n, M, L)
+    qc = O.encode_query(q, W[:d], K, M * L)[0][0].reshape(M, L)
+    T = O.exact_set_mask(n, 0, 0)
+    den = np.zeros(M)
+    for m in range(M):
+        S = O.sampled_set(O.collision_counts(kc[:, m, :], qc[m]), T)
+        den[m] = np.exp(s[S] - logu[S]).sum()
+    se = den.std(ddof=1) / math.sqrt(M)
+    assert abs(den.mean() - np.exp(s).sum()) < 4.5 * se, (den.mean(), np.exp(s).sum(), se)
