@@ -54,7 +54,7 @@ extern "C" {
 #define MP_API
 #endif
 
-#define MP_ABI_VERSION 2
+#define MP_ABI_VERSION 3
 #define MP_KEYS_PER_BLOCK 1024
 
 typedef enum {
@@ -71,12 +71,14 @@ typedef enum { MP_F32 = 0, MP_BF16 = 1 } mp_dtype;
 /* Decode parameters. K, L: LSH bits per table and tables ("LSH Sampling...", method details,
  * hash-function choice). n_sink, n_local: the exact set T = {0..n_sink-1} u {n-n_local..n-1},
  * attended with u = 1 and never sampled (Algorithm 1's static cache; "don't pick the tallest",
- * section 5). scale: score scale, 0 means 1/sqrt(d). flags: must be 0.
+ * section 5). scale: score scale, 0 means 1/sqrt(d). flags: 0, or MP_FLAG_MIPS.
  * n_capacity: tokens per head the keys, values and codes are laid out for (0 means n; else
  * n_capacity >= n). A decode cache that grows by appending (mp_encode_keys) keeps one
  * n_capacity for its lifetime and passes the current length as n.
  * n_indexed: keys [0, n_indexed) of each head are in the bucketed tables (0 means n; else
- * n_indexed <= n); only mp_sampled_attention_buckets reads it. */
+ * n_indexed <= n); only mp_sampled_attention_buckets reads it.
+ * radius: with MP_FLAG_MIPS, [B][Hkv] float32 device array from mp_key_radius (the longest
+ * centred key of each head); NULL otherwise. */
 typedef struct {
     int K;
     int L;
@@ -86,7 +88,16 @@ typedef struct {
     unsigned flags;
     int n_capacity;
     int n_indexed;
+    const float* radius;
 } mp_params;
+
+/* MIPS -> cosine variant ("LSH Sampling...", method details, variance reduction with LSH): the
+ * query is extended by a 0 and each centred key k - mu by sqrt(r^2 - |k - mu|^2), r the longest
+ * centred key, so the collision probability grows with the inner product: p_i = 1 -
+ * arccos(q.(k_i - mu) / (|q| r)) / pi replaces the cosine of q and k_i - mu. W then has d + 1
+ * rows ([d + 1][K*L]; the query uses the first d), the codes come from mp_encode_keys_mips, and
+ * every decode call of the variant sets this flag and mp_params.radius. */
+#define MP_FLAG_MIPS 1u
 
 /* Human-readable name of a status code (static storage). */
 MP_API const char* mp_status_string(mp_status s);
@@ -213,6 +224,23 @@ MP_API size_t mp_buckets_bytes(int B, int Hkv, int n, int K, int L);
  * (K > 12). */
 MP_API mp_status mp_build_buckets(const uint32_t* codes, int B, int Hkv, int n, int K, int L,
                                   uint32_t* buckets, cudaStream_t stream);
+
+/* MIPS variant: radius[b][g] = max over keys [0, n) of |k_i - mu| (float32, [B][Hkv], written
+ * by this call; fp32 arithmetic). The keys are laid out for n_capacity tokens per head.
+ * Errors: MP_ERR_INVALID_ARG (shapes, null, misalignment), MP_ERR_UNSUPPORTED (d != 128). */
+MP_API mp_status mp_key_radius(const void* keys, mp_dtype key_dtype, const float* centre,
+                               int B, int Hkv, int n_capacity, int n, int d, float* radius,
+                               cudaStream_t stream);
+
+/* MIPS variant of mp_encode_keys: codes of keys [n_begin, n_end) from the extended centred keys,
+ * bit = [sum_e W[e][j] (k[e] - mu[e]) + W[d][j] sqrt(max(0, r^2 - |k - mu|^2)) > 0] in fp32 on
+ * CUDA cores. W_aug: [d + 1][K*L]; radius from mp_key_radius (a key longer than r, appended
+ * after r was taken, gets 0 in the extra coordinate). Other keys' bits in the words the range
+ * touches are kept. Errors as mp_encode_keys; MP_ERR_INVALID_ARG also for a NULL radius. */
+MP_API mp_status mp_encode_keys_mips(const void* keys, mp_dtype key_dtype, const float* centre,
+                                     const void* W_aug, mp_dtype w_dtype, const float* radius,
+                                     int B, int Hkv, int n_capacity, int n_begin, int n_end,
+                                     int d, int K, int L, uint32_t* codes, cudaStream_t stream);
 
 /* mp_build_buckets over keys [0, n) of codes laid out for n_capacity tokens per head (the
  * appendable cache of mp_encode_keys); buckets is mp_buckets_bytes(B, Hkv, n, K, L) bytes. A

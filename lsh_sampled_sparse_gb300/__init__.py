@@ -7,6 +7,7 @@ include/magicpig.h. There is no CPU fallback: without the built library every ca
 from .binding import (  # noqa: F401
     MP_BF16,
     MP_F32,
+    MP_FLAG_MIPS,
     MagicPIGError,
     Params,
     abi_version,
@@ -21,8 +22,10 @@ from .binding import (  # noqa: F401
     decode_workspace_bytes,
     device_status,
     encode_keys,
+    encode_keys_mips,
     encode_query,
     key_mean,
+    key_radius,
     key_mean_workspace_bytes,
     lib,
     library_path,

@@ -19,17 +19,27 @@ class MagicPIGError(RuntimeError):
     """A libmagicpig call returned a status other than MP_OK, or the library is missing."""
 
 
+MP_FLAG_MIPS = 1
+
+
 class Params(ctypes.Structure):
     """mp_params: K bits per table, L tables, exact sink/local sizes, score scale (0: 1/sqrt(d)),
-    flags (0), the cache capacity per head (0: n) and the keys in the bucketed tables (0: n)."""
+    flags (0 or MP_FLAG_MIPS), the cache capacity per head (0: n), the keys in the bucketed
+    tables (0: n), and the MIPS variant's radii (a device pointer, or None)."""
 
     _fields_ = [("K", ctypes.c_int), ("L", ctypes.c_int), ("n_sink", ctypes.c_int),
                 ("n_local", ctypes.c_int), ("scale", ctypes.c_float), ("flags", ctypes.c_uint),
-                ("n_capacity", ctypes.c_int), ("n_indexed", ctypes.c_int)]
+                ("n_capacity", ctypes.c_int), ("n_indexed", ctypes.c_int),
+                ("radius", ctypes.c_void_p)]
 
 
-def _params(K, L, n_sink, n_local, scale=0.0, n_capacity=0, n_indexed=0) -> Params:
-    return Params(K, L, n_sink, n_local, scale, 0, n_capacity, n_indexed)
+def _params(K, L, n_sink, n_local, scale=0.0, n_capacity=0, n_indexed=0, radius=None) -> Params:
+    if radius is not None:
+        _cuda(radius, "radius")
+        if radius.dtype != torch.float32:
+            raise TypeError("radius must be float32")
+    return Params(K, L, n_sink, n_local, scale, MP_FLAG_MIPS if radius is not None else 0,
+                  n_capacity, n_indexed, None if radius is None else radius.data_ptr())
 
 
 def _lengths(keys_shape, n):
@@ -60,6 +70,9 @@ def _declare(L):
                                  _vp]),
         "mp_key_mean_cap": (_c_int, [_vp, _c_int] + [_c_int] * 5 + [_vp, _vp, _c_size, _vp]),
         "mp_encode_keys": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 8 + [_vp, _vp]),
+        "mp_key_radius": (_c_int, [_vp, _c_int, _vp] + [_c_int] * 5 + [_vp, _vp]),
+        "mp_encode_keys_mips": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _vp] + [_c_int] * 8
+                                + [_vp, _vp]),
         "mp_build_tables": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 6 + [_vp, _vp]),
         "mp_decode_workspace_bytes": (_c_size, [_c_int] * 5 + [P]),
         "mp_debug_workspace_bytes": (_c_size, [_c_int] * 5 + [P]),
@@ -221,9 +234,47 @@ def encode_keys(keys, centre, W, K: int, L: int, n_begin: int, n_end: int, codes
     return codes
 
 
+def key_radius(keys, centre, n=None, radius=None, stream=None):
+    """MIPS variant: radius[b, g] = max over the first n keys of |k - mu| (float32 [B, Hkv])."""
+    _cuda(keys, "keys", 4)
+    _cuda(centre, "centre", 3)
+    B, Hkv, cap, d = keys.shape
+    n, cap = _lengths(keys.shape, n)
+    if radius is None:
+        radius = torch.empty(B, Hkv, dtype=torch.float32, device=keys.device)
+    _cuda(radius, "radius")
+    _check(lib().mp_key_radius(_ptr(keys), _dtype(keys, "keys"), _ptr(centre), B, Hkv, cap, n, d,
+                               _ptr(radius), _stream(stream)), "mp_key_radius")
+    return radius
+
+
+def encode_keys_mips(keys, centre, W_aug, radius, K: int, L: int, n_begin: int, n_end: int,
+                     codes=None, stream=None):
+    """MIPS variant: codes of keys [n_begin, n_end) from the keys extended by
+    sqrt(r^2 - |k - mu|^2), W_aug [d + 1, K*L]; codes laid out for keys.shape[2] keys per head."""
+    _cuda(keys, "keys", 4)
+    B, Hkv, cap, d = keys.shape
+    nbytes = codes_bytes(B, Hkv, cap, K, L)
+    if codes is None:
+        codes = torch.empty(max(nbytes // 4, 4), dtype=torch.int32, device=keys.device)
+    _cuda(codes, "codes")
+    if _nbytes(codes) < nbytes:
+        raise ValueError("codes buffer too small for the cache's capacity")
+    _cuda(centre, "centre", 3)
+    _cuda(W_aug, "W_aug", 2)
+    _cuda(radius, "radius")
+    if W_aug.shape[0] != d + 1:
+        raise ValueError("W_aug must have d + 1 rows")
+    _check(lib().mp_encode_keys_mips(_ptr(keys), _dtype(keys, "keys"), _ptr(centre), _ptr(W_aug),
+                                     _dtype(W_aug, "W_aug"), _ptr(radius), B, Hkv, cap, n_begin,
+                                     n_end, d, K, L, _ptr(codes), _stream(stream)),
+           "mp_encode_keys_mips")
+    return codes
+
+
 def decode_attention(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int,
                      n_local: int, scale: float = 0.0, out=None, workspace=None, stream=None,
-                     n=None):
+                     n=None, radius=None):
     """One LSH-sampled decode step over the first n keys (default: all of keys.shape[2]);
     returns out [B, Hq, d] float32."""
     _cuda(q, "q", 3)
@@ -238,7 +289,7 @@ def decode_attention(q, codes, centre, W, keys, values, K: int, L: int, n_sink: 
     if out is None:
         out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
     _cuda(out, "out", 3)
-    p = _params(K, L, n_sink, n_local, scale, cap)
+    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius)
     need = int(lib().mp_decode_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
     if need == 0:
         raise MagicPIGError("mp_decode_workspace_bytes rejected the shapes/parameters")
@@ -251,7 +302,7 @@ def decode_attention(q, codes, centre, W, keys, values, K: int, L: int, n_sink: 
 
 
 def encode_query(q, centre, W, keys_shape, K: int, L: int, n_sink: int, n_local: int,
-                 workspace, scale: float = 0.0, stream=None, n=None):
+                 workspace, scale: float = 0.0, stream=None, n=None, radius=None):
     """First half of decode_attention: query codes and norms into `workspace`."""
     _cuda(q, "q", 3)
     _cuda(centre, "centre", 3)
@@ -259,14 +310,14 @@ def encode_query(q, centre, W, keys_shape, K: int, L: int, n_sink: int, n_local:
     B, Hq, d = q.shape
     Hkv = keys_shape[1]
     n, cap = _lengths(keys_shape, n)
-    p = _params(K, L, n_sink, n_local, scale, cap)
+    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius)
     _check(lib().mp_encode_query(_ptr(q), _dtype(q, "q"), _ptr(centre), _ptr(W), _dtype(W, "W"),
                                  B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(workspace),
                                  _nbytes(workspace), _stream(stream)), "mp_encode_query")
 
 
 def sampled_attention(q, codes, centre, keys, values, K: int, L: int, n_sink: int, n_local: int,
-                      out, workspace, scale: float = 0.0, stream=None, n=None):
+                      out, workspace, scale: float = 0.0, stream=None, n=None, radius=None):
     """Second half of decode_attention (after encode_query filled `workspace`)."""
     _cuda(q, "q", 3)
     _cuda(keys, "keys", 4)
@@ -276,7 +327,7 @@ def sampled_attention(q, codes, centre, keys, values, K: int, L: int, n_sink: in
     B, Hq, d = q.shape
     Hkv = keys.shape[1]
     n, cap = _lengths(keys.shape, n)
-    p = _params(K, L, n_sink, n_local, scale, cap)
+    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius)
     _check(lib().mp_sampled_attention(
         _ptr(q), _dtype(q, "q"), _ptr(codes), _ptr(centre), _ptr(keys), _ptr(values),
         _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out), _ptr(workspace),
@@ -309,7 +360,7 @@ def build_buckets(codes, B: int, Hkv: int, n: int, K: int, L: int, buckets=None,
 
 def sampled_attention_buckets(q, buckets, centre, keys, values, K: int, L: int, n_sink: int,
                               n_local: int, out, workspace, scale: float = 0.0, stream=None,
-                              codes=None, n=None, n_indexed=None):
+                              codes=None, n=None, n_indexed=None, radius=None):
     """sampled_attention with the bucketed tables in place of the code scan. The tables hold
     keys [0, n_indexed) (default n); keys appended since are found by scanning their codes, so
     `codes` is needed when n_indexed < n."""
@@ -322,7 +373,8 @@ def sampled_attention_buckets(q, buckets, centre, keys, values, K: int, L: int, 
     B, Hq, d = q.shape
     Hkv = keys.shape[1]
     n, cap = _lengths(keys.shape, n)
-    p = _params(K, L, n_sink, n_local, scale, cap, 0 if n_indexed is None else int(n_indexed))
+    p = _params(K, L, n_sink, n_local, scale, cap, 0 if n_indexed is None else int(n_indexed),
+                radius=radius)
     _check(lib().mp_sampled_attention_buckets(
         _ptr(q), _dtype(q, "q"), _ptr(buckets), _ptr(codes), _ptr(centre), _ptr(keys),
         _ptr(values), _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out),
@@ -331,7 +383,8 @@ def sampled_attention_buckets(q, buckets, centre, keys, values, K: int, L: int, 
 
 
 def debug_select(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int, n_local: int,
-                 scale: float = 0.0, counts: bool = True, stream=None, n=None) -> dict:
+                 scale: float = 0.0, counts: bool = True, stream=None, n=None,
+                 radius=None) -> dict:
     """Decode plus its decisions: out, q_bits, per-row ascending sample sets, collision counts."""
     _cuda(q, "q", 3)
     _cuda(keys, "keys", 4)
@@ -346,7 +399,7 @@ def debug_select(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int,
     sel_idx = torch.full((B, Hq, n), -1, dtype=torch.int32, device=dev)
     sel_count = torch.zeros(B, Hq, dtype=torch.int32, device=dev)
     cnt = torch.zeros(B, Hq, n, dtype=torch.uint8, device=dev) if counts else None
-    p = _params(K, L, n_sink, n_local, scale, cap)
+    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius)
     need = int(lib().mp_debug_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
     if need == 0:
         raise MagicPIGError("mp_debug_workspace_bytes rejected the shapes/parameters")

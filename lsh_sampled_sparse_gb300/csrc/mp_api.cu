@@ -38,7 +38,8 @@ bool ensure_prepared() {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return false;
     if (prepare_misc() != cudaSuccess || prepare_decode() != cudaSuccess ||
-        prepare_buckets() != cudaSuccess || prepare_append() != cudaSuccess)
+        prepare_buckets() != cudaSuccess || prepare_append() != cudaSuccess ||
+        prepare_mips() != cudaSuccess)
         return false;
     prepare_encode_tc();   // failure only disables the tensor-core encoder
     cudaGetLastError();
@@ -57,8 +58,11 @@ bool fill_shape(int B, int Hq, int Hkv, int n, int d, const mp_params* prm, Deco
     if (B < 1 || Hq < 1 || Hkv < 1 || n < 1 || d < 1) return false;
     if (Hq % Hkv) return false;
     if (prm->K < 0 || prm->K > 32 || prm->L < 1 || prm->n_sink < 0 || prm->n_local < 0 ||
-        prm->flags != 0u || !(prm->scale >= 0.0f))
+        (prm->flags & ~MP_FLAG_MIPS) != 0u || !(prm->scale >= 0.0f))
         return false;
+    // the MIPS variant needs the radii; without the flag there must be none
+    if (((prm->flags & MP_FLAG_MIPS) != 0u) != (prm->radius != nullptr)) return false;
+    if (prm->radius && (reinterpret_cast<uintptr_t>(prm->radius) & 3u)) return false;
     if (static_cast<long long>(prm->K) * prm->L > (1 << 20)) return false;
     if (prm->n_capacity < 0 || (prm->n_capacity > 0 && prm->n_capacity < n)) return false;
     if (prm->n_indexed < 0 || prm->n_indexed > n) return false;
@@ -76,6 +80,7 @@ bool fill_shape(int B, int Hq, int Hkv, int n, int d, const mp_params* prm, Deco
     s->ncap = prm->n_capacity > 0 ? prm->n_capacity : n;
     s->cblk = (s->ncap + kKeysPerBlock - 1) / kKeysPerBlock;
     s->n_indexed = prm->n_indexed > 0 ? prm->n_indexed : n;
+    s->radius = prm->radius;
     s->n_sink = prm->n_sink;
     s->n_local = prm->n_local;
     s->scale = prm->scale > 0.0f ? prm->scale : 1.0f / sqrtf(static_cast<float>(d));
@@ -249,6 +254,40 @@ mp_status mp_encode_keys(const void* keys, mp_dtype key_dtype, const float* cent
     }
     return to_status(launch_encode_simt(keys, kbf, centre, W, wbf, B, Hkv, n_capacity, blk0,
                                         blk1, K, L, codes, stream));
+}
+
+mp_status mp_key_radius(const void* keys, mp_dtype key_dtype, const float* centre, int B,
+                        int Hkv, int n_capacity, int n, int d, float* radius,
+                        cudaStream_t stream) {
+    if (!keys || !centre || !radius || !valid_dtype(key_dtype)) return MP_ERR_INVALID_ARG;
+    if (B < 1 || Hkv < 1 || n < 1 || d < 1 || n_capacity < n) return MP_ERR_INVALID_ARG;
+    if (d != kD) return MP_ERR_UNSUPPORTED;
+    if (!aligned(keys, 16) || !aligned(centre, 4) || !aligned(radius, 4))
+        return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    return to_status(launch_key_radius(keys, key_dtype == MP_BF16, centre, B * Hkv, n_capacity,
+                                       n, radius, stream));
+}
+
+mp_status mp_encode_keys_mips(const void* keys, mp_dtype key_dtype, const float* centre,
+                              const void* W_aug, mp_dtype w_dtype, const float* radius, int B,
+                              int Hkv, int n_capacity, int n_begin, int n_end, int d, int K,
+                              int L, uint32_t* codes, cudaStream_t stream) {
+    if (B < 1 || Hkv < 1 || n_capacity < 1 || d < 1 || K < 0 || K > 32 || L < 1)
+        return MP_ERR_INVALID_ARG;
+    if (n_begin < 0 || n_end > n_capacity || n_begin > n_end) return MP_ERR_INVALID_ARG;
+    if (!valid_dtype(key_dtype) || !valid_dtype(w_dtype)) return MP_ERR_INVALID_ARG;
+    if (d != kD) return MP_ERR_UNSUPPORTED;
+    if (static_cast<long long>(K) * L > (1 << 20)) return MP_ERR_INVALID_ARG;
+    if (K == 0 || n_begin == n_end) return MP_OK;
+    if (!keys || !centre || !W_aug || !radius || !codes) return MP_ERR_INVALID_ARG;
+    if (!aligned(keys, 16) || !aligned(codes, 16) || !aligned(centre, 4) ||
+        !aligned(radius, 4) || !aligned(W_aug, w_dtype == MP_BF16 ? 2 : 4))
+        return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    return to_status(launch_encode_mips(keys, key_dtype == MP_BF16, centre, W_aug,
+                                        w_dtype == MP_BF16, radius, B, Hkv, n_capacity, n_begin,
+                                        n_end, K, L, codes, stream));
 }
 
 size_t mp_decode_workspace_bytes(int B, int Hq, int Hkv, int n, int d, const mp_params* prm) {

@@ -436,6 +436,7 @@ struct AArgs {
     const float* logu_tab;
     int q_bf16, n, nblk, nsb, Hq, Hkv, G, K, L, n_sink, n_local;
     int ncap;                                    // K/V rows per head in memory
+    const float* radius;                         // MIPS variant: longest centred key per head
     float scale, log_c2;
     int merge_cap;                               // partials staged per merge round
     int work_bytes;                              // bytes of the list / merge stage region
@@ -613,6 +614,7 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     wait_for_predecessor();                      // selection words, query norms, log u table
     const float4 st = a.qstat[row];
     const float qn = st.x, qmu = st.y;
+    const float rad = a.radius ? a.radius[bg] : 0.0f;   // MIPS: cos = q.(k - mu) / (|q| r)
 
     // ---- the rows of this CTA: T by arithmetic, or the selected keys of its blocks by a list
     const int t_a = min(a.n_sink, a.n), t_b = max(a.n - a.n_local, t_a);
@@ -706,7 +708,7 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
         if (live) {
             float lw = 0.0f;
             if (weighted) {
-                const float den = qn * sqrtf(kb2);
+                const float den = qn * (a.radius ? rad : sqrtf(kb2));
                 float cs = den > 0.0f ? __fdividef(dot - qmu, den) : 0.0f;
                 cs = fminf(1.0f, fmaxf(-1.0f, cs));
                 if (cs > -0.9f && cs < 0.999f) {
@@ -1021,6 +1023,7 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
     aa.n_sink = s.n_sink;
     aa.n_local = s.n_local;
     aa.ncap = s.ncap;
+    aa.radius = s.radius;
     aa.scale = s.scale;
     aa.log_c2 = s.L >= 2 ? logf(0.5f * static_cast<float>(s.L) * static_cast<float>(s.L - 1)) : 0.0f;
     {

@@ -47,6 +47,7 @@ struct DecodeShape {
     int cblk;            // code blocks per (sequence, KV head) in memory: ceil(ncap / 1024)
     int n_indexed;       // keys in the bucketed tables (<= n)
     float scale;
+    const float* radius; // MIPS variant: [B*Hkv] longest centred key; nullptr otherwise
 };
 
 size_t decode_scratch_bytes(const DecodeShape& s, bool debug);
@@ -111,6 +112,17 @@ cudaError_t prepare_encode_tc();
 cudaError_t prepare_decode();
 cudaError_t prepare_misc();
 cudaError_t prepare_append();
+cudaError_t prepare_mips();
+
+// ---- MIPS -> cosine variant (mp_mips.cu) -------------------------------------------------------
+// radius[bh] = max over keys [0, n) of |k - mu|
+cudaError_t launch_key_radius(const void* keys, bool keys_bf16, const float* centre, int BH,
+                              int ncap, int n, float* radius, cudaStream_t st);
+// codes of keys [n0, n1) from the keys extended by sqrt(r^2 - |k - mu|^2), W with d + 1 rows
+cudaError_t launch_encode_mips(const void* keys, bool keys_bf16, const float* centre,
+                               const void* W, bool w_bf16, const float* radius, int B, int Hkv,
+                               int ncap, int n0, int n1, int K, int L, uint32_t* codes,
+                               cudaStream_t st);
 
 // ---- small device helpers ---------------------------------------------------------------------
 __device__ __forceinline__ float to_float(float x) { return x; }

@@ -80,6 +80,7 @@ extern "C" mp_status mp_decode_attention_noalloc(
     s.ncap = prm->n_capacity > 0 ? prm->n_capacity : n;
     s.cblk = (s.ncap + kKeysPerBlock - 1) / kKeysPerBlock;
     s.n_indexed = prm->n_indexed > 0 ? prm->n_indexed : n;
+    s.radius = prm->radius;
     s.n_sink = prm->n_sink;
     s.n_local = prm->n_local;
     s.scale = prm->scale > 0.0f ? prm->scale : 1.0f / sqrtf(static_cast<float>(d));

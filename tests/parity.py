@@ -56,10 +56,11 @@ class UnitReport:
 
 
 def check_unit(b: int, g: int, *, q, keys, values, centre, W, K, L, n_sink, n_local, gpu: dict,
-               unpacked=None, scale=None, check_counts=True) -> UnitReport:
+               unpacked=None, scale=None, check_counts=True, radius=None) -> UnitReport:
     """Compare one (b, g) unit. q/keys/values/centre/W are the inputs both sides were given
     (torch tensors on any device, or arrays); gpu holds debug_select's outputs moved to the CPU
-    and, when K > 0, the unpacked key codes [B, Hkv, n, L]."""
+    and, when K > 0, the unpacked key codes [B, Hkv, n, L]. radius (the unit's longest centred
+    key, as the GPU used it) selects the MIPS variant: W then has d + 1 rows."""
     rep = UnitReport()
     kb = O.as64(keys[b, g])
     vb = O.as64(values[b, g])
@@ -68,7 +69,11 @@ def check_unit(b: int, g: int, *, q, keys, values, centre, W, K, L, n_sink, n_lo
     Hkv = keys.shape[1]
     G = Hq // Hkv
     C = K * L
-    _, obits, onear = O.encode_keys(kb, mu, W, K, L)
+    Wd = O.as64(W)[:kb.shape[1]]                 # the query's rows (all of W but the MIPS row)
+    if radius is None:
+        _, obits, onear = O.encode_keys(kb, mu, W, K, L)
+    else:
+        _, obits, onear = O.encode_keys_mips(kb, mu, W, float(radius), K, L)
     if C:
         gbits = unpacked_to_bits(unpacked[b, g], K)
         kbits, rep.key_flips = O.replay_bits(obits, onear, gbits, what=f"key bits ({b},{g})")
@@ -77,12 +82,13 @@ def check_unit(b: int, g: int, *, q, keys, values, centre, W, K, L, n_sink, n_lo
     kcodes = O.table_codes(kbits, K, L)
     for h in range(g * G, (g + 1) * G):
         qv = O.as64(q[b, h])
-        _, qb, qnear = O.encode_query(qv, W, K, L)
+        _, qb, qnear = O.encode_query(qv, Wd, K, L)
         gq = words_to_bits(gpu["q_bits"][b, h], C)
         qbits, f = O.replay_bits(qb[0], qnear[0], gq, what=f"query bits ({b},{h})")
         rep.q_flips += f
         qcode = O.table_codes(qbits[None, :], K, L)[0]
-        r = O.decode_head(qv, kb, vb, mu, kcodes, qcode, K, L, n_sink, n_local, scale)
+        r = O.decode_head(qv, kb, vb, mu, kcodes, qcode, K, L, n_sink, n_local, scale,
+                          radius=None if radius is None else float(radius))
         if check_counts and gpu.get("cnt") is not None:
             want_cnt = np.minimum(r["cnt"], 255)
             got_cnt = np.asarray(gpu["cnt"][b, h], dtype=np.int64)

@@ -41,7 +41,7 @@ def test_status_strings_and_version(L):
     import lsh_sampled_sparse_gb300 as mp
     header_version = int(re.search(r"#define MP_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
     assert mp.abi_version() == header_version
-    assert ctypes.sizeof(mp.Params) == 32          # mp_params: 8 four-byte fields
+    assert ctypes.sizeof(mp.Params) == 40          # mp_params: 8 four-byte fields, a pointer
     names = [L.mp_status_string(i).decode() for i in range(6)]
     assert names == ["MP_OK", "MP_ERR_INVALID_ARG", "MP_ERR_UNSUPPORTED", "MP_ERR_CUDA",
                      "MP_ERR_TIMEOUT", "MP_ERR_WORKSPACE"]
@@ -155,6 +155,32 @@ def test_capacity_and_append_reject_bad_arguments(L):
     p = mp.Params(10, 150, 4, 64, 0.0, 0, 0, 500)
     assert L.mp_sampled_attention_buckets(ok, 1, ok, None, ok, ok, ok, 1, 1, 4, 1, 1000, 128,
                                           ctypes.byref(p), ok, ok, 1 << 24, None) == INVALID
+
+
+def test_mips_variant_rejects_bad_arguments(L):
+    import lsh_sampled_sparse_gb300 as mp
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+
+    def ws(flags, radius):
+        p = mp.Params(10, 150, 4, 64, 0.0, flags, 0, 0, radius)
+        return L.mp_decode_workspace_bytes(1, 4, 1, 1000, 128, ctypes.byref(p))
+    assert ws(0, None) > 0 and ws(mp.MP_FLAG_MIPS, 0x10000) == ws(0, None)
+    assert ws(mp.MP_FLAG_MIPS, None) == 0        # the variant needs its radii
+    assert ws(0, 0x10000) == 0                   # radii without the flag
+    assert ws(2, None) == 0                      # unknown flag
+    assert ws(mp.MP_FLAG_MIPS, 0x10002) == 0     # misaligned radii
+    # mp_key_radius(keys, dt, centre, B, Hkv, n_capacity, n, d, radius)
+    assert L.mp_key_radius(ok, 1, ok, 1, 1, 100, 100, 128, None, None) == 1
+    assert L.mp_key_radius(ok, 1, ok, 1, 1, 99, 100, 128, ok, None) == 1
+    assert L.mp_key_radius(ok, 1, ok, 1, 1, 100, 100, 64, ok, None) == 2
+    # mp_encode_keys_mips(keys, dt, centre, W, wdt, radius, B, Hkv, cap, n0, n1, d, K, L, codes)
+    assert L.mp_encode_keys_mips(ok, 1, ok, ok, 1, None, 1, 1, 100, 0, 100, 128, 10, 150, ok,
+                                 None) == 1
+    assert L.mp_encode_keys_mips(ok, 1, ok, ok, 1, ok, 1, 1, 100, 0, 101, 128, 10, 150, ok,
+                                 None) == 1
+    assert L.mp_encode_keys_mips(None, 1, None, None, 1, None, 1, 1, 100, 5, 5, 128, 10, 150,
+                                 None, None) == 0
 
 
 def test_binding_refuses_cpu_tensors(L):
