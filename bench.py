@@ -56,6 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-buckets", action="store_true",
                     help="skip the bucketed-table retrieval measurement")
+    ap.add_argument("--no-mips", action="store_true",
+                    help="skip the MIPS -> cosine variant measurement")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of as one captured CUDA graph")
     return ap.parse_args(argv)
@@ -305,6 +307,71 @@ def run_append(mp, wl, W, state, steps: int, use_graph: bool) -> float:
     end.record(stream)
     torch.cuda.synchronize()
     return begin.elapsed_time(end) * 1e3 / (steps * len(state))
+
+
+def run_mips(mp, wl, state, ws_dec, steps: int, use_graph: bool) -> dict:
+    """The MIPS -> cosine variant on the same layers: radius + CUDA-core encoding per layer
+    (timed on the first layer), then K decode steps over every layer in one CUDA graph."""
+    dev = state[0].keys.device
+    W_aug = make_hyperplanes(wl.replace(d=wl.d + 1), device=dev)
+    stream = torch.cuda.current_stream()
+    codes, radii = [], []
+    for s in state:
+        codes.append(torch.empty_like(s.codes))
+        radii.append(torch.empty(wl.B, wl.Hkv, dtype=torch.float32, device=dev))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for li, s in enumerate(state):
+        if li == 0:
+            ev[0].record(stream)
+        mp.key_radius(s.keys, s.centre, radius=radii[li], stream=stream)
+        if li == 0:
+            ev[1].record(stream)
+        mp.encode_keys_mips(s.keys, s.centre, W_aug, radii[li], wl.K, wl.L, 0, wl.n, codes[li],
+                            stream=stream)
+        if li == 0:
+            ev[2].record(stream)
+    torch.cuda.synchronize()
+    radius_us = ev[0].elapsed_time(ev[1]) * 1e3
+    encode_us = ev[1].elapsed_time(ev[2]) * 1e3
+
+    def step(strm):
+        for s, c, r in zip(state, codes, radii):
+            mp.encode_query(s.q, s.centre, W_aug, s.keys.shape, wl.K, wl.L, wl.n_sink,
+                            wl.n_local, ws_dec, stream=strm, radius=r)
+            mp.sampled_attention(s.q, c, s.centre, s.keys, s.values, wl.K, wl.L, wl.n_sink,
+                                 wl.n_local, s.out, ws_dec, stream=strm, radius=r)
+    for _ in range(3):
+        step(stream)
+    torch.cuda.synchronize()
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream()
+            for _ in range(steps):
+                step(cap)
+    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    begin.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(steps):
+            step(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    assert mp.device_status() == 0
+    ms = begin.elapsed_time(end) / steps
+    s0 = state[0]
+    d = mp.debug_select(s0.q, codes[0], s0.centre, W_aug, s0.keys, s0.values, wl.K, wl.L,
+                        wl.n_sink, wl.n_local, counts=False, radius=radii[0])
+    rows = float(d["sel_count"].double().mean())
+    return {"what": "MIPS -> cosine variant (keys extended by sqrt(r^2 - |k - mu|^2)) on the same "
+                    "layers: radius and CUDA-core encoding per layer, decode over every layer",
+            "radius_us_per_layer": radius_us, "encode_us_per_layer": encode_us,
+            "decode_ms_per_token": ms,
+            "decode_queries_per_s": wl.B * wl.Hq * len(state) / (ms / 1e3),
+            "mean_rows_per_query_head": rows}
 
 
 def run_buckets(mp, wl, W, state, ws_dec, steps: int, use_graph: bool, peaks):
@@ -686,6 +753,11 @@ def run_ours(args):
             "mean_union_rows_per_kv_head": alg["mean_union_rows"],
             "mean_rows_per_query_head": sum(total) / max(1, len(total)) / wl.G,
             "fraction_of_n": sum(total) / max(1, len(total)) / wl.G / wl.n,
+            "per_kv_head_group_rows_min_max": [min(total) if total else 0,
+                                               max(total) if total else 0],
+            "per_kv_head_group_rows_cv": float(statistics.pstdev(total) /
+                                               max(1e-9, statistics.mean(total)))
+                                         if total else 0.0,
         },
         "gpu_launches": sum(STAGE_LAUNCHES.values()) * layers * args.steps,
         "clocks": clk,
@@ -718,6 +790,8 @@ def run_ours(args):
                 "build_gbs": build_bytes / (bk["build_us_per_layer"] * 1e-6) / 1e9,
                 "tables_bytes_per_layer": bk["tables_bytes_per_layer"],
             }
+    if not args.no_mips:
+        line["mips"] = run_mips(mp, wl, state, ws_dec, args.steps, graph is not None)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(wl, state, W, args.cpu_seconds)
     if not args.no_e2e:

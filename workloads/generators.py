@@ -19,6 +19,12 @@ Recipe per (sequence, KV head), with u a uniform random unit vector:
   v_i       ~ N(0, I)
   q_h      *= exp(N(0, s^2))                       only where a workload asks for log-normal
                                                    query norms
+  k_i      += sqrt(a) xi_i v,  xi_i ~ N(0, 1)      only where a workload asks for a spread key
+                                                   cone (i >= 1): covariance I + a v v^T with
+                                                   a = A exp(N(0, s_a^2)) per (sequence, KV
+                                                   head) and v = unit(qbar + 0.5 e), e a random
+                                                   unit vector: a direction near the group's
+                                                   queries, so the sample sizes differ by head
 Hyperplanes W ~ N(0, 1) of shape [d, K*L], one matrix for every head and layer of a run (the
 shared random projector of the system design section). Workloads stored in bf16 round W to bf16:
 at (K, L) = (10, 150) that is the 128 x 1500 x 2 B = 384,000 B (about 400 KB) projector size the
@@ -60,6 +66,8 @@ class Workload:
     q_noise: float = 0.5
     sink_sigmas: float = 12.0
     q_lognormal_sigma: float = 0.0
+    key_spread: float = 0.0           # A of the spread key cone (0: isotropic keys)
+    key_spread_sigma: float = 0.0     # s_a, the log-normal spread of a between heads
 
     @property
     def G(self) -> int:
@@ -90,6 +98,12 @@ WORKLOADS: dict[str, Workload] = {
     "llama8b_b32_n32k": Workload(
         "llama8b_b32_n32k", 3, B=32, Hq=32, Hkv=8, n=32768, d=128, K=10, L=150, n_sink=4,
         n_local=64, q_lognormal_sigma=0.3),
+    # as llama8b_b32_n32k, and each head's keys spread along a direction near its queries
+    # (covariance I + a v v^T, a = 16 exp(N(0, 0.3^2))): an added variant whose sample sizes
+    # differ between heads
+    "llama8b_b32_n32k_spread": Workload(
+        "llama8b_b32_n32k_spread", 5, B=32, Hq=32, Hkv=8, n=32768, d=128, K=10, L=150, n_sink=4,
+        n_local=64, q_lognormal_sigma=0.3, key_spread=16.0, key_spread_sigma=0.3),
     # Llama-3.1-70B-shaped (GQA group 8), 128K context, batch 2, 80 layers
     "llama70b_b2_n128k_80layers": Workload(
         "llama70b_b2_n128k_80layers", 4, B=2, Hq=64, Hkv=8, n=131072, d=128, K=10, L=150,
@@ -141,6 +155,15 @@ def make_layer(wl: Workload, layer: int = 0, device="cpu") -> dict:
     if n > 0:
         keys[:, :, 0, :] = mu + wl.sink_sigmas * qbar
     values = torch.randn(B, Hkv, n, d, generator=g, device=device, dtype=f32)
+    if wl.key_spread > 0 and n > 1:
+        a = wl.key_spread * torch.exp(
+            wl.key_spread_sigma * torch.randn(B, Hkv, 1, 1, generator=g, device=device, dtype=f32))
+        e = torch.randn(B, Hkv, d, generator=g, device=device, dtype=f32)
+        e = e / e.norm(dim=-1, keepdim=True)
+        v = qbar + 0.5 * e
+        v = v / v.norm(dim=-1, keepdim=True)
+        xi = torch.randn(B, Hkv, n - 1, 1, generator=g, device=device, dtype=f32)
+        keys[:, :, 1:, :] += a.sqrt() * xi * v[:, :, None, :]
     return {
         "keys": keys.to(wl.kv_dtype).contiguous(),
         "values": values.to(wl.kv_dtype).contiguous(),
