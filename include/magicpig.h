@@ -233,14 +233,20 @@ MP_API mp_status mp_key_radius(const void* keys, mp_dtype key_dtype, const float
                                cudaStream_t stream);
 
 /* MIPS variant of mp_encode_keys: codes of keys [n_begin, n_end) from the extended centred keys,
- * bit = [sum_e W[e][j] (k[e] - mu[e]) + W[d][j] sqrt(max(0, r^2 - |k - mu|^2)) > 0] in fp32 on
- * CUDA cores. W_aug: [d + 1][K*L]; radius from mp_key_radius (a key longer than r, appended
- * after r was taken, gets 0 in the extra coordinate). Other keys' bits in the words the range
- * touches are kept. Errors as mp_encode_keys; MP_ERR_INVALID_ARG also for a NULL radius. */
+ * bit = [sum_e W[e][j] (k[e] - mu[e]) + W[d][j] sqrt(max(0, r^2 - |k - mu|^2)) > 0].
+ * W_aug: [d + 1][K*L]; radius from mp_key_radius (a key longer than r, appended after r was
+ * taken, gets 0 in the extra coordinate).
+ * norms_scratch: NULL, or caller-owned device memory of B*Hkv*n_capacity floats. With it, bf16
+ * keys and W and more than 64 keys, whole 1024-key blocks are re-encoded on the tensor cores
+ * (the centred part by MMA, the extra coordinate added in fp32 before the sign; the norms of
+ * the blocks' keys are written to the scratch first). Otherwise fp32 CUDA cores encode the range
+ * itself, keeping the other keys' bits of the words it touches.
+ * Errors as mp_encode_keys; MP_ERR_INVALID_ARG also for a NULL radius. */
 MP_API mp_status mp_encode_keys_mips(const void* keys, mp_dtype key_dtype, const float* centre,
                                      const void* W_aug, mp_dtype w_dtype, const float* radius,
                                      int B, int Hkv, int n_capacity, int n_begin, int n_end,
-                                     int d, int K, int L, uint32_t* codes, cudaStream_t stream);
+                                     int d, int K, int L, uint32_t* codes, float* norms_scratch,
+                                     cudaStream_t stream);
 
 /* mp_build_buckets over keys [0, n) of codes laid out for n_capacity tokens per head (the
  * appendable cache of mp_encode_keys); buckets is mp_buckets_bytes(B, Hkv, n, K, L) bytes. A

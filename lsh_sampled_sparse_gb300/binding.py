@@ -72,7 +72,7 @@ def _declare(L):
         "mp_encode_keys": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 8 + [_vp, _vp]),
         "mp_key_radius": (_c_int, [_vp, _c_int, _vp] + [_c_int] * 5 + [_vp, _vp]),
         "mp_encode_keys_mips": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _vp] + [_c_int] * 8
-                                + [_vp, _vp]),
+                                + [_vp, _vp, _vp]),
         "mp_build_tables": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 6 + [_vp, _vp]),
         "mp_decode_workspace_bytes": (_c_size, [_c_int] * 5 + [P]),
         "mp_debug_workspace_bytes": (_c_size, [_c_int] * 5 + [P]),
@@ -249,9 +249,11 @@ def key_radius(keys, centre, n=None, radius=None, stream=None):
 
 
 def encode_keys_mips(keys, centre, W_aug, radius, K: int, L: int, n_begin: int, n_end: int,
-                     codes=None, stream=None):
+                     codes=None, stream=None, tensor_cores: bool = True, norms_scratch=None):
     """MIPS variant: codes of keys [n_begin, n_end) from the keys extended by
-    sqrt(r^2 - |k - mu|^2), W_aug [d + 1, K*L]; codes laid out for keys.shape[2] keys per head."""
+    sqrt(r^2 - |k - mu|^2), W_aug [d + 1, K*L]; codes laid out for keys.shape[2] keys per head.
+    tensor_cores: let long bf16 ranges run on the tensor-core encoder (a scratch of one float
+    per cached key is allocated unless norms_scratch is given)."""
     _cuda(keys, "keys", 4)
     B, Hkv, cap, d = keys.shape
     nbytes = codes_bytes(B, Hkv, cap, K, L)
@@ -265,10 +267,18 @@ def encode_keys_mips(keys, centre, W_aug, radius, K: int, L: int, n_begin: int, 
     _cuda(radius, "radius")
     if W_aug.shape[0] != d + 1:
         raise ValueError("W_aug must have d + 1 rows")
+    scratch = None
+    if tensor_cores:
+        scratch = norms_scratch
+        if scratch is None:
+            scratch = torch.empty(B * Hkv * cap, dtype=torch.float32, device=keys.device)
+        _cuda(scratch, "norms_scratch")
+        if _nbytes(scratch) < B * Hkv * cap * 4:
+            raise ValueError("norms_scratch needs one float per cached key")
     _check(lib().mp_encode_keys_mips(_ptr(keys), _dtype(keys, "keys"), _ptr(centre), _ptr(W_aug),
                                      _dtype(W_aug, "W_aug"), _ptr(radius), B, Hkv, cap, n_begin,
-                                     n_end, d, K, L, _ptr(codes), _stream(stream)),
-           "mp_encode_keys_mips")
+                                     n_end, d, K, L, _ptr(codes), _ptr(scratch),
+                                     _stream(stream)), "mp_encode_keys_mips")
     return codes
 
 

@@ -2,6 +2,8 @@
 // workspace layout, kernel selection, and the device status word.
 #include <math.h>
 
+#include <algorithm>
+
 #include <mutex>
 
 #include "mp_internal.cuh"
@@ -272,7 +274,8 @@ mp_status mp_key_radius(const void* keys, mp_dtype key_dtype, const float* centr
 mp_status mp_encode_keys_mips(const void* keys, mp_dtype key_dtype, const float* centre,
                               const void* W_aug, mp_dtype w_dtype, const float* radius, int B,
                               int Hkv, int n_capacity, int n_begin, int n_end, int d, int K,
-                              int L, uint32_t* codes, cudaStream_t stream) {
+                              int L, uint32_t* codes, float* norms_scratch,
+                              cudaStream_t stream) {
     if (B < 1 || Hkv < 1 || n_capacity < 1 || d < 1 || K < 0 || K > 32 || L < 1)
         return MP_ERR_INVALID_ARG;
     if (n_begin < 0 || n_end > n_capacity || n_begin > n_end) return MP_ERR_INVALID_ARG;
@@ -282,9 +285,24 @@ mp_status mp_encode_keys_mips(const void* keys, mp_dtype key_dtype, const float*
     if (K == 0 || n_begin == n_end) return MP_OK;
     if (!keys || !centre || !W_aug || !radius || !codes) return MP_ERR_INVALID_ARG;
     if (!aligned(keys, 16) || !aligned(codes, 16) || !aligned(centre, 4) ||
-        !aligned(radius, 4) || !aligned(W_aug, w_dtype == MP_BF16 ? 2 : 4))
+        !aligned(radius, 4) || !aligned(W_aug, w_dtype == MP_BF16 ? 2 : 4) ||
+        !aligned(norms_scratch, 4))
         return MP_ERR_INVALID_ARG;
     if (!ensure_prepared()) return MP_ERR_CUDA;
+    if (norms_scratch && key_dtype == MP_BF16 && w_dtype == MP_BF16 &&
+        n_end - n_begin > kAppendMaxKeys) {
+        // whole blocks on the tensor cores: the norms of every key of those blocks first
+        const int blk0 = n_begin / kKeysPerBlock;
+        const int blk1 = (n_end + kKeysPerBlock - 1) / kKeysPerBlock;
+        cudaError_t e = launch_key_radius(keys, true, centre, B * Hkv, n_capacity, n_end, nullptr,
+                                          stream, norms_scratch, blk0 * kKeysPerBlock,
+                                          std::min(blk1 * kKeysPerBlock, n_capacity));
+        if (e != cudaSuccess) return MP_ERR_CUDA;
+        e = launch_encode_tc(keys, centre, W_aug, B, Hkv, n_capacity, blk0, blk1, K, L, codes,
+                             device_status_ptr(), stream, norms_scratch, radius);
+        if (e != cudaErrorNotSupported) return to_status(e);
+        cudaGetLastError();
+    }
     return to_status(launch_encode_mips(keys, key_dtype == MP_BF16, centre, W_aug,
                                         w_dtype == MP_BF16, radius, B, Hkv, n_capacity, n_begin,
                                         n_end, K, L, codes, stream));

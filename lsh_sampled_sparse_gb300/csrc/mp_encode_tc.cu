@@ -59,7 +59,8 @@ constexpr int kOnesSlice = 3;
 constexpr uint32_t kOffStg = kOffC + kCBytes;
 constexpr uint32_t kOffBars = kOffStg + kWordsPerBlock * kStgPitch * 4;
 constexpr uint32_t kOffMisc = kOffBars + 128;
-constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+constexpr uint32_t kOffWd = kOffMisc + 16;             // MIPS: W[d][j0 + r] as floats
+constexpr uint32_t kSmemBytes = kOffWd + kChunkN * 4 + 1024;  // + alignment slack
 static_assert(kStgPitch == 257, "staging pitch");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffC % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
@@ -74,6 +75,9 @@ struct EncodeArgs {
     int C, nchunk, nblk, n, units, parts;
     int blk0;                       // first block encoded; a unit's block is blk0 + u % nblk
     int cblk;                       // code blocks per head in memory (the codes' head stride)
+    // MIPS variant only: |k_i - mu| per key [BH][n] and r per head [BH]
+    const float* norms;
+    const float* radius;
 };
 
 // ---- PTX wrappers -----------------------------------------------------------------------------
@@ -198,8 +202,10 @@ __device__ __forceinline__ uint32_t pack_signs(const uint32_t (&v)[32]) {
     }
     return x[0] | (x[1] << 8) | (x[2] << 16) | (x[3] << 24);
 }
-// 32x32 bit-matrix transpose across a warp: on entry bit b of lane r is element (r, b); on exit
-// bit r of lane b is that element. Each stage swaps the off-diagonal s x s blocks.
+// kMips: the MIPS -> cosine variant, whose keys carry an extra coordinate a_i = sqrt(max(0,
+// r^2 - |k_i - mu|^2)) on a (d + 1)-th row of W: the epilogue subtracts W[d][j] a_i from each
+// accumulator before taking its sign (one fp32 FMA per element).
+template <bool kMips>
 __global__ void __launch_bounds__(kThreads, 1)
     encode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const EncodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -362,6 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int et = tid - 64;                 // 0..511
         const uint32_t tquad = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
         bool aborted = false;
+        float* sWd = reinterpret_cast<float*>(smem + kOffWd);
+        if constexpr (kMips) {
+            if (et < kChunkN)
+                sWd[et] = et < Nc ? __bfloat162float(a.W[static_cast<size_t>(kD) * a.C + j0 + et])
+                                  : 0.0f;
+            epi_sync();
+        }
         // c_j = w_j . mu of head h, as three bf16 terms, into centre slot h % 3 (thread et
         // writes hyperplane row et). The MMAs that read the slot last (head h - 3) are complete:
         // this runs for the tile two ahead of the one being drained, and heads never decrease.
@@ -448,6 +461,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // sign bits of this warp's two 32-column groups into registers (one TMEM wait
                 // per group keeps 32 accumulator registers live) ...
                 uint32_t x[2] = {0u, 0u};
+                float aext = 0.0f;           // MIPS: this lane's key's extra coordinate
+                if constexpr (kMips) {
+                    const int key = (a.blk0 + blk) * kKeysPerBlock + t * kTileM + quad * 32 + lane;
+                    const float r = __ldg(a.radius + bg);
+                    const float nk = key < a.n ? __ldg(a.norms + static_cast<size_t>(bg) * a.n + key)
+                                               : r;
+                    aext = sqrtf(fmaxf(0.0f, fmaf(r, r, -nk * nk)));
+                }
                 if (!aborted) {
                     tc_fence_after();
                     const uint32_t trow = tquad + ab * kChunkN;
@@ -457,6 +478,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint32_t v[32];
                             tmem_ld32(trow + colA + 32 * g, v);
                             tmem_ld_wait();
+                            if constexpr (kMips) {
+                                const float4* wd4 = reinterpret_cast<const float4*>(sWd + colA + 32 * g);
+#pragma unroll
+                                for (int c4 = 0; c4 < 8; ++c4) {
+                                    const float4 w = wd4[c4];
+                                    v[4 * c4 + 0] = __float_as_uint(fmaf(-w.x, aext, __uint_as_float(v[4 * c4 + 0])));
+                                    v[4 * c4 + 1] = __float_as_uint(fmaf(-w.y, aext, __uint_as_float(v[4 * c4 + 1])));
+                                    v[4 * c4 + 2] = __float_as_uint(fmaf(-w.z, aext, __uint_as_float(v[4 * c4 + 2])));
+                                    v[4 * c4 + 3] = __float_as_uint(fmaf(-w.w, aext, __uint_as_float(v[4 * c4 + 3])));
+                                }
+                            }
                             x[g] = pack_signs(v);
                         }
                     }
@@ -521,15 +553,19 @@ EncodeTiledFn encode_tiled_fn() {
 }  // namespace
 
 cudaError_t prepare_encode_tc() {
-    cudaError_t e = cudaFuncSetAttribute(encode_tc_kernel,
+    cudaError_t e = cudaFuncSetAttribute(encode_tc_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(encode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
     if (e != cudaSuccess) return e;
     return encode_tiled_fn() ? cudaSuccess : cudaErrorNotSupported;
 }
 
 cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* W, int B,
                              int Hkv, int ncap, int blk0, int blk1, int K, int L,
-                             uint32_t* codes, int* status, cudaStream_t st) {
+                             uint32_t* codes, int* status, cudaStream_t st, const float* norms,
+                             const float* radius) {
     const int C = K * L;
     if (C == 0 || blk1 <= blk0) return cudaSuccess;
     EncodeTiledFn enc = encode_tiled_fn();
@@ -556,12 +592,17 @@ cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* 
     a.n = ncap;
     a.blk0 = blk0;
     a.cblk = (ncap + kKeysPerBlock - 1) / kKeysPerBlock;
+    a.norms = norms;
+    a.radius = radius;
     a.units = B * Hkv * a.nblk;
     int parts = device_sm_count() / a.nchunk;
     if (parts < 1) parts = 1;
     if (parts > a.units) parts = a.units;
     a.parts = parts;
-    encode_tc_kernel<<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
+    if (norms)
+        encode_tc_kernel<true><<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
+    else
+        encode_tc_kernel<false><<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
     return cudaGetLastError();
 }
 

@@ -60,9 +60,12 @@ int key_mean_splits(int n);
 
 // Encode whole 1024-key blocks [blk0, blk1) of every head of a cache laid out for ncap keys
 // per head (keys >= ncap read as zero).
+// With norms (|k_i - mu| per key, [B*Hkv][ncap]) and radius ([B*Hkv]): the MIPS variant, W with
+// d + 1 rows.
 cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* W, int B,
                              int Hkv, int ncap, int blk0, int blk1, int K, int L,
-                             uint32_t* codes, int* status, cudaStream_t st);
+                             uint32_t* codes, int* status, cudaStream_t st,
+                             const float* norms = nullptr, const float* radius = nullptr);
 cudaError_t launch_encode_simt(const void* keys, bool keys_bf16, const float* centre,
                                const void* W, bool w_bf16, int B, int Hkv, int ncap, int blk0,
                                int blk1, int K, int L, uint32_t* codes, cudaStream_t st);
@@ -115,9 +118,11 @@ cudaError_t prepare_append();
 cudaError_t prepare_mips();
 
 // ---- MIPS -> cosine variant (mp_mips.cu) -------------------------------------------------------
-// radius[bh] = max over keys [0, n) of |k - mu|
+// radius[bh] = max over keys [0, n) of |k - mu| (radius may be null), and with norms
+// ([BH][ncap]) |k_i - mu| of keys [k0, k1) as well (k0 = 0, k1 = n when only the radius is asked)
 cudaError_t launch_key_radius(const void* keys, bool keys_bf16, const float* centre, int BH,
-                              int ncap, int n, float* radius, cudaStream_t st);
+                              int ncap, int n, float* radius, cudaStream_t st,
+                              float* norms = nullptr, int k0 = 0, int k1 = -1);
 // codes of keys [n0, n1) from the keys extended by sqrt(r^2 - |k - mu|^2), W with d + 1 rows
 cudaError_t launch_encode_mips(const void* keys, bool keys_bf16, const float* centre,
                                const void* W, bool w_bf16, const float* radius, int B, int Hkv,

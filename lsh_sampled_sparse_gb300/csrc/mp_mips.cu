@@ -16,30 +16,47 @@ constexpr int kRadiusThreads = 256;
 constexpr int kMipsKeys = 64;          // keys per encoding CTA (two 32-key words)
 constexpr int kMipsPlanes = 16;        // hyperplanes per pass
 
-// radius[bh] = max_i |k_i - mu| over keys [0, n): a warp per key row, lane 4 consecutive
-// elements; the maximum of non-negative floats through their ordered bit patterns.
+constexpr int kRadiusRowsAtOnce = 4;   // key rows a warp has in flight
+
+// |k_i - mu| of keys [k0, k1): a warp per key row (kRadiusRowsAtOnce rows in flight), lane 4
+// consecutive elements. With radius: its maximum into radius[bh] (the maximum of non-negative
+// floats through their ordered bit patterns); with norms: each row's into norms[bh][i].
 __global__ void __launch_bounds__(kRadiusThreads)
-    key_radius_kernel(const void* keys, int keys_bf16, const float* centre, int ncap, int n,
-                      float* radius) {
+    key_radius_kernel(const void* keys, int keys_bf16, const float* centre, int ncap, int k0,
+                      int k1, float* radius, float* norms) {
+    constexpr int U = kRadiusRowsAtOnce;
     const int bh = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int r0 = blockIdx.x * kRadiusRows, r1 = min(n, r0 + kRadiusRows);
+    const int r0 = k0 + blockIdx.x * kRadiusRows, r1 = min(k1, r0 + kRadiusRows);
     float mu[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) mu[i] = centre[static_cast<size_t>(bh) * kD + 4 * lane + i];
     float best = 0.0f;
-    for (int r = r0 + warp; r < r1; r += kRadiusThreads / 32) {
-        const size_t base = (static_cast<size_t>(bh) * ncap + r) * kD + 4 * lane;
-        float s = 0.0f;
+    for (int rb = r0 + warp * U; rb < r1; rb += (kRadiusThreads / 32) * U) {
+        float s[U];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float x = load_elem(keys, keys_bf16, base + i) - mu[i];
-            s = fmaf(x, x, s);
+        for (int u = 0; u < U; ++u) {
+            const int r = min(rb + u, r1 - 1);            // past r1: a repeat of the last row
+            const size_t base = (static_cast<size_t>(bh) * ncap + r) * kD + 4 * lane;
+            s[u] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x = load_elem(keys, keys_bf16, base + i) - mu[i];
+                s[u] = fmaf(x, x, s[u]);
+            }
         }
 #pragma unroll
-        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        best = fmaxf(best, sqrtf(s));
+        for (int o = 16; o; o >>= 1)
+#pragma unroll
+            for (int u = 0; u < U; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], o);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float nr = sqrtf(s[u]);
+            best = fmaxf(best, nr);
+            if (norms && lane == u && rb + u < r1) norms[static_cast<size_t>(bh) * ncap + rb + u] = nr;
+        }
     }
-    if (lane == 0) atomicMax(reinterpret_cast<unsigned*>(radius + bh), __float_as_uint(best));
+    if (radius && lane == 0)
+        atomicMax(reinterpret_cast<unsigned*>(radius + bh), __float_as_uint(best));
 }
 
 // Codes of keys [n0, n1) from the extended centred keys: one key per thread, a warp's 32 keys
@@ -104,11 +121,18 @@ __global__ void __launch_bounds__(kMipsKeys)
 }  // namespace
 
 cudaError_t launch_key_radius(const void* keys, bool keys_bf16, const float* centre, int BH,
-                              int ncap, int n, float* radius, cudaStream_t st) {
-    cudaError_t e = cudaMemsetAsync(radius, 0, static_cast<size_t>(BH) * sizeof(float), st);
-    if (e != cudaSuccess) return e;
-    const dim3 grid((n + kRadiusRows - 1) / kRadiusRows, BH);
-    key_radius_kernel<<<grid, kRadiusThreads, 0, st>>>(keys, keys_bf16, centre, ncap, n, radius);
+                              int ncap, int n, float* radius, cudaStream_t st, float* norms,
+                              int k0, int k1) {
+    if (k1 < 0) k1 = n;
+    if (radius) {
+        const cudaError_t e = cudaMemsetAsync(radius, 0, static_cast<size_t>(BH) * sizeof(float),
+                                              st);
+        if (e != cudaSuccess) return e;
+    }
+    if (k1 <= k0) return cudaSuccess;
+    const dim3 grid((k1 - k0 + kRadiusRows - 1) / kRadiusRows, BH);
+    key_radius_kernel<<<grid, kRadiusThreads, 0, st>>>(keys, keys_bf16, centre, ncap, k0, k1,
+                                                       radius, norms);
     return cudaGetLastError();
 }
 

@@ -176,11 +176,13 @@ def test_mips_variant_rejects_bad_arguments(L):
     assert L.mp_key_radius(ok, 1, ok, 1, 1, 100, 100, 64, ok, None) == 2
     # mp_encode_keys_mips(keys, dt, centre, W, wdt, radius, B, Hkv, cap, n0, n1, d, K, L, codes)
     assert L.mp_encode_keys_mips(ok, 1, ok, ok, 1, None, 1, 1, 100, 0, 100, 128, 10, 150, ok,
-                                 None) == 1
+                                 None, None) == 1
     assert L.mp_encode_keys_mips(ok, 1, ok, ok, 1, ok, 1, 1, 100, 0, 101, 128, 10, 150, ok,
-                                 None) == 1
+                                 None, None) == 1
+    assert L.mp_encode_keys_mips(ok, 1, ok, ok, 1, ok, 1, 1, 100, 0, 100, 128, 10, 150, ok,
+                                 P(0x10002), None) == 1          # misaligned scratch
     assert L.mp_encode_keys_mips(None, 1, None, None, 1, None, 1, 1, 100, 5, 5, 128, 10, 150,
-                                 None, None) == 0
+                                 None, None, None) == 0
 
 
 def test_binding_refuses_cpu_tensors(L):

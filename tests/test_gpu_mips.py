@@ -33,11 +33,13 @@ def _w_aug(wl):
     return make_hyperplanes(wl.replace(d=wl.d + 1)).contiguous()
 
 
-@pytest.mark.parametrize("shape", [
-    dict(B=1, Hq=4, Hkv=2, n=3000, K=10, L=150, kv_dtype=BF),
-    dict(B=2, Hq=2, Hkv=1, n=1500, K=8, L=75, kv_dtype=F32, q_dtype=F32, w_dtype=F32),
+@pytest.mark.parametrize("shape,tensor_cores", [
+    (dict(B=1, Hq=4, Hkv=2, n=3000, K=10, L=150, kv_dtype=BF), True),
+    (dict(B=1, Hq=4, Hkv=2, n=3000, K=10, L=150, kv_dtype=BF), False),
+    (dict(B=2, Hq=2, Hkv=1, n=1500, K=8, L=75, kv_dtype=F32, q_dtype=F32, w_dtype=F32), True),
 ])
-def test_mips_decode_matches_the_oracle(mp, shape):
+def test_mips_decode_matches_the_oracle(mp, shape, tensor_cores):
+    # bf16 with tensor_cores: the tcgen05 encoder adds the extra coordinate in its epilogue
     wl = small_workload(**shape)
     x = make_layer(wl)
     xc = {k: v.cuda() for k, v in x.items()}
@@ -45,7 +47,8 @@ def test_mips_decode_matches_the_oracle(mp, shape):
     Wc = W.cuda()
     centre = mp.key_mean(xc["keys"])
     radius = mp.key_radius(xc["keys"], centre)
-    codes = mp.encode_keys_mips(xc["keys"], centre, Wc, radius, wl.K, wl.L, 0, wl.n)
+    codes = mp.encode_keys_mips(xc["keys"], centre, Wc, radius, wl.K, wl.L, 0, wl.n,
+                                tensor_cores=tensor_cores)
     dbg = mp.debug_select(xc["q"], codes, centre, Wc, xc["keys"], xc["values"], wl.K, wl.L,
                           wl.n_sink, wl.n_local, radius=radius)
     prod = mp.decode_attention(xc["q"], codes, centre, Wc, xc["keys"], xc["values"], wl.K, wl.L,
@@ -76,10 +79,13 @@ def test_mips_ranges_equal_a_full_encode_and_buckets_equal_the_scan(mp):
     W = _w_aug(wl).cuda()
     centre = mp.key_mean(xc["keys"])
     radius = mp.key_radius(xc["keys"], centre)
-    full = mp.encode_keys_mips(xc["keys"], centre, W, radius, wl.K, wl.L, 0, wl.n)
+    # the CUDA-core encoder over ranges gives the codes of one pass over all keys, bit for bit
+    full = mp.encode_keys_mips(xc["keys"], centre, W, radius, wl.K, wl.L, 0, wl.n,
+                               tensor_cores=False)
     parts = torch.zeros_like(full)
     for a, b in [(0, 1000), (1000, 1001), (1001, 1030), (1030, 2047), (2047, 2600)]:
-        mp.encode_keys_mips(xc["keys"], centre, W, radius, wl.K, wl.L, a, b, parts)
+        mp.encode_keys_mips(xc["keys"], centre, W, radius, wl.K, wl.L, a, b, parts,
+                            tensor_cores=False)
     u_full = mp.codes_unpack(full, wl.B, wl.Hkv, wl.n, wl.K, wl.L)
     u_parts = mp.codes_unpack(parts, wl.B, wl.Hkv, wl.n, wl.K, wl.L)
     assert torch.equal(u_full, u_parts)
