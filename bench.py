@@ -757,6 +757,10 @@ def run_ours(args):
                     "decode steps)",
             "queries_per_s": world * queries_per_step / (decode_ms / 1e3),
             "attention_ms_per_token": decode_ms,
+            "hbm_gbs": (alg["sampled_attention"]["bytes"] + alg["encode_query"]["bytes"]) * layers
+                       / (decode_ms / 1e3) / 1e9,
+            "hbm_frac": (alg["sampled_attention"]["bytes"] + alg["encode_query"]["bytes"]) * layers
+                        / (decode_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
             "sampled_attention_gbs": rooflines["sampled_attention"]["achieved"],
             "append_us_per_layer": append_us,
             "append_note": "mp_encode_keys of one new key per layer (all heads), the incremental "
