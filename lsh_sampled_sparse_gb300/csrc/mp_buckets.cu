@@ -8,8 +8,9 @@
 // members[t][offsets[t][c] .. offsets[t][c + 1]) are the keys whose table-t code is c. The order
 // of keys inside a bucket is not fixed (buckets are sets); everything that reads them only counts.
 //
-// Build, one kernel: a cluster of kBucketRanges CTAs per (table, sequence x KV head), each CTA
-// one key range. A CTA stages its range's plane rows, counts its codes in a shared-memory
+// Build, one kernel: a cluster of R CTAs per (table, sequence x KV head), each CTA one key range
+// (R = 1, 2, 4 or 8, so that a range holds about 12 blocks: short contexts take fewer, longer
+// ranges and pay the per-range histogram work fewer times). A CTA stages its range's plane rows, counts its codes in a shared-memory
 // histogram (the count's old value is the key's rank among the range's keys of that code), reads
 // the other ranges' histograms through distributed shared memory to get the table's offsets and
 // its own write base per code, sorts its keys by code in shared memory and writes them out in
@@ -33,6 +34,8 @@ constexpr int kLookupUnroll = 4;      // bucket entries a lookup lane loads befo
 constexpr int kStageBlocks = 4;       // 1024-key blocks whose plane rows a build CTA stages at once
 constexpr size_t kClusterBuildSmem = 200 * 1024;   // dynamic shared memory of a cluster-build CTA
 constexpr int kClusterThreads = 512;  // threads of a cluster-build CTA
+constexpr int kMaxClusterRanges = 8;  // CTAs (key ranges) of a cluster-build table, at most
+constexpr int kClusterRangeBlocks = 12;   // blocks a cluster-build range aims at
 constexpr int kWordsAtOnce = 4;       // 32-key words a cluster-build warp decodes together
 constexpr int kStageRow = kWordsPerBlock + 1;   // staged plane row stride (words): lanes reading
                                                 // word w of planes 0..K-1 hit distinct banks
@@ -220,9 +223,11 @@ __host__ __device__ __forceinline__ size_t cluster_build_smem(int rb, int K) {
     return (3 * nb + keys + (stage > keys ? stage : keys)) * 4;
 }
 
-// One CTA per key range, kBucketRanges CTAs (a cluster) per table. Each warp takes kWordsAtOnce
-// 32-key words at a time so that their shuffles and shared atomics overlap.
-__global__ void __cluster_dims__(kBucketRanges, 1, 1) __launch_bounds__(kClusterThreads)
+// One CTA per key range, a cluster of R CTAs per table (grid x = R; the cluster size is set at
+// launch). Each warp takes kWordsAtOnce 32-key words at a time so that their shuffles and shared
+// atomics overlap.
+template <int R>
+__global__ void __launch_bounds__(kClusterThreads)
     bucket_build_cluster_kernel(const uint32_t* codes, int n, int K, int L, int nblk, int cblk,
                                 uint32_t* buckets) {
     namespace cg = cooperative_groups;
@@ -233,8 +238,8 @@ __global__ void __cluster_dims__(kBucketRanges, 1, 1) __launch_bounds__(kCluster
     const int nb = 1 << K, r = static_cast<int>(cluster.block_rank()), t = blockIdx.y,
               bh = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int rb = (nblk + kBucketRanges - 1) / kBucketRanges;
-    const int b0 = (nblk * r) / kBucketRanges, b1 = (nblk * (r + 1)) / kBucketRanges;
+    const int rb = (nblk + R - 1) / R;
+    const int b0 = (nblk * r) / R, b1 = (nblk * (r + 1)) / R;
     const int nbk = b1 - b0, nw = nbk * kWordsPerBlock, k0 = b0 * kKeysPerBlock;
     const int m = max(0, min(n, b1 * kKeysPerBlock) - k0);        // keys of this range
     const int C = K * L, srow = K * kStageRow;
@@ -274,12 +279,12 @@ __global__ void __cluster_dims__(kBucketRanges, 1, 1) __launch_bounds__(kCluster
     }
     cluster.sync();                        // every range's histogram is complete
     for (int c = tid; c < nb; c += T) {
-        uint32_t v[kBucketRanges];
+        uint32_t v[R];
 #pragma unroll
-        for (int q = 0; q < kBucketRanges; ++q) v[q] = cluster.map_shared_rank(hist, q)[c];
+        for (int q = 0; q < R; ++q) v[q] = cluster.map_shared_rank(hist, q)[c];
         uint32_t tot = 0u, pre = 0u;
 #pragma unroll
-        for (int q = 0; q < kBucketRanges; ++q) {
+        for (int q = 0; q < R; ++q) {
             pre += q < r ? v[q] : 0u;
             tot += v[q];
         }
@@ -382,17 +387,44 @@ size_t bucket_table_bytes(int B, int Hkv, int n, int K, int L) {
     return static_cast<size_t>(B) * Hkv * bucket_words(n, K, L) * 4;
 }
 
+// Ranges per table for the cluster build: about kClusterRangeBlocks blocks each, 1 to 8.
+int cluster_ranges(int nblk) {
+    int R = 1;
+    while (R < kMaxClusterRanges && nblk > R * kClusterRangeBlocks) R *= 2;
+    return R;
+}
+
 cudaError_t launch_bucket_build(const uint32_t* codes, int B, int Hkv, int cblk, int n, int K,
                                 int L, uint32_t* buckets, cudaStream_t st) {
     const int nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
-    const dim3 ranges(kBucketRanges, L, B * Hkv);   // the ranges of one table run side by side
-    const int rb = (nblk + kBucketRanges - 1) / kBucketRanges;
+    const int R = cluster_ranges(nblk);
+    const int rb = (nblk + R - 1) / R;
     const size_t csmem = cluster_build_smem(rb, K);
     if (csmem <= kClusterBuildSmem && rb * kKeysPerBlock <= 65536) {
-        bucket_build_cluster_kernel<<<ranges, kClusterThreads, csmem, st>>>(codes, n, K, L, nblk,
-                                                                            cblk, buckets);
-        return cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(R, L, B * Hkv);        // the ranges of one table run side by side
+        cfg.blockDim = dim3(kClusterThreads);
+        cfg.dynamicSmemBytes = csmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = R;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        switch (R) {
+            case 1: return cudaLaunchKernelEx(&cfg, bucket_build_cluster_kernel<1>, codes, n, K,
+                                              L, nblk, cblk, buckets);
+            case 2: return cudaLaunchKernelEx(&cfg, bucket_build_cluster_kernel<2>, codes, n, K,
+                                              L, nblk, cblk, buckets);
+            case 4: return cudaLaunchKernelEx(&cfg, bucket_build_cluster_kernel<4>, codes, n, K,
+                                              L, nblk, cblk, buckets);
+            default: return cudaLaunchKernelEx(&cfg, bucket_build_cluster_kernel<8>, codes, n, K,
+                                               L, nblk, cblk, buckets);
+        }
     }
+    const dim3 ranges(kBucketRanges, L, B * Hkv);
     const size_t smem = (static_cast<size_t>(1) << K) * 4 +
                         static_cast<size_t>(kStageBlocks) * K * kStageRow * 4;
     bucket_count_kernel<<<ranges, kBuildThreads, smem, st>>>(codes, n, K, L, nblk, cblk, buckets);
@@ -436,10 +468,11 @@ cudaError_t prepare_buckets() {
     if (e != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, bucket_scan_kernel)) != cudaSuccess) return e;
     if ((e = cudaFuncGetAttributes(&fa, bucket_scatter_kernel)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(bucket_build_cluster_kernel,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(kClusterBuildSmem))) != cudaSuccess)
-        return e;
+    for (auto fn : {bucket_build_cluster_kernel<1>, bucket_build_cluster_kernel<2>,
+                    bucket_build_cluster_kernel<4>, bucket_build_cluster_kernel<8>})
+        if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kClusterBuildSmem))) != cudaSuccess)
+            return e;
     return cudaFuncGetAttributes(&fa, bucket_lookup_kernel);
 }
 
