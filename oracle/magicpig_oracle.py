@@ -54,6 +54,9 @@ Parity status (what pins each function; the tests under tests/ hold the pins):
       formula equals the plain cosine of the augmented vectors; Monte-Carlo bit agreement over
       fresh (d+1)-row hyperplanes; p follows the inner product where the plain cosine does not;
       brute-force codes; Horvitz-Thompson unbiasedness with the variant's u
+  cp_hash / encode_*_cp / cp_collision_probability          p(0) = 1/(2d), p(1) = 1, p(-1) = 0
+      in closed form; Monte-Carlo collision frequency over fresh Gaussian rotations; brute-force
+      codes; Horvitz-Thompson unbiasedness with the cross-polytope u
 """
 from __future__ import annotations
 
@@ -71,6 +74,8 @@ __all__ = [
     "inclusion_probability", "snis_attention", "full_attention", "decode_head", "decode",
     "replay_bits", "as64", "bucket_tables", "bucket_collision_counts", "mips_radius",
     "mips_augment_keys", "mips_augment_query", "encode_keys_mips", "collision_probability_mips",
+    "cp_hash", "encode_keys_cp", "encode_query_cp", "cp_collision_probability", "CP_RHO_MAX",
+    "replay_codes",
 ]
 
 
@@ -276,6 +281,112 @@ def collision_probability_mips(q, kbar, r: float) -> np.ndarray:
     return 1.0 - np.arccos(cos) / math.pi
 
 
+# ----------------------------------------------------------------------------------------------
+# Cross-polytope hashing (the hash the pages name as future work to shrink the tables: "LSH
+# Sampling...", conclusion). A table hashes x to the signed index of the largest |coordinate| of
+# G x, G a d x d matrix of i.i.d. N(0, 1) entries, one per table: 2d possible codes, one byte for
+# d = 128. Keys are centred first and the query is not, as for SimHash; one hash per table (K = 1).
+# For a Gaussian G the coordinate pairs ((G x)_i, (G y)_i) of unit x, y are i.i.d. standard
+# bivariate normal with correlation rho = cos(x, y), so
+#   p(rho) = 2d * int_{a>0} int_{b>0} phi_rho(a, b) F_rho(a, b)^(d-1) da db,
+#   F_rho(a, b) = P[|X| < a, |Y| < b] = int_{-a}^{a} phi(t) [Phi((b - rho t)/s) -
+#                 Phi((-b - rho t)/s)] dt,   s = sqrt(1 - rho^2),
+# (the first coordinate is the largest for both with the same sign; 2d such events). Evaluated
+# by Gauss-Legendre quadrature on [0, 8] (the tails beyond 8 standard deviations are below
+# 1e-15); above rho = CP_RHO_MAX the density is too narrow for the quadrature, and p is taken
+# linearly between p(CP_RHO_MAX) and p(1) = 1 (a reading: the pages give nothing, and such
+# cosines do not occur in the workloads).
+# ----------------------------------------------------------------------------------------------
+CP_RHO_MAX = 0.99
+
+
+def cp_hash(x, G, raw=None):
+    """Signed argmax of |G x| for each row of x [m, d], G [d, d]: code 2 i + (1 if (G x)_i < 0).
+
+    Returns (codes [m], runner-up codes [m], near [m]): near marks rows whose two largest |G x|
+    differ by less than 1e-5 |g|max |raw| (raw: the vector as it was given, default x), where
+    another evaluation may legitimately pick the runner-up."""
+    xv = as64(np.atleast_2d(x))
+    Gv = as64(G)
+    y = xv @ Gv.T
+    ay = np.abs(y)
+    order = np.argsort(-ay, axis=1, kind="stable")
+    rows = np.arange(y.shape[0])
+    i1, i2 = order[:, 0], order[:, 1]
+    code = 2 * i1 + (y[rows, i1] < 0).astype(np.int64)
+    alt = 2 * i2 + (y[rows, i2] < 0).astype(np.int64)
+    rn = np.linalg.norm(as64(np.atleast_2d(raw if raw is not None else x)), axis=1)
+    gmax = float(np.max(np.linalg.norm(Gv, axis=1)))
+    near = (ay[rows, i1] - ay[rows, i2]) < NEAR_TIE_REL * gmax * rn
+    return code, alt, near
+
+
+def encode_keys_cp(keys, centre, G):
+    """Codes [n, L] of the centred keys, G [L, d, d]; also runner-up codes and near-tie marks."""
+    k = as64(keys)
+    kbar = k - as64(centre)[None, :]
+    parts = [cp_hash(kbar, G[t], raw=k) for t in range(G.shape[0])]
+    return tuple(np.stack([pt[j] for pt in parts], axis=1) for j in range(3))
+
+
+def encode_query_cp(q, G):
+    """Codes [m, L] of the query rows (not centred); also runner-up codes and near-tie marks."""
+    parts = [cp_hash(q, G[t]) for t in range(G.shape[0])]
+    return tuple(np.stack([pt[j] for pt in parts], axis=1) for j in range(3))
+
+
+def replay_codes(oracle_codes, alt, near, other_codes, what: str = "codes"):
+    """Take another evaluation's codes where they differ from the oracle's at a near tie of the
+    two largest coordinates and equal the runner-up; any other difference raises."""
+    oc = np.asarray(oracle_codes)
+    gc = np.asarray(other_codes)
+    diff = oc != gc
+    bad = diff & ~(np.asarray(near, dtype=bool) & (gc == np.asarray(alt)))
+    if bad.any():
+        idx = np.argwhere(bad)[:8].tolist()
+        raise AssertionError(f"{what}: {int(bad.sum())} code mismatches outside the near-tie band"
+                             f" (first {idx})")
+    out = oc.copy()
+    out[diff] = gc[diff]
+    return out, int(diff.sum())
+
+
+def _cp_quadrature(rho: float, d: int, nodes: int) -> float:
+    x, w = np.polynomial.legendre.leggauss(nodes)
+    top = 8.0
+    a = (x + 1.0) * top / 2.0
+    wa = w * top / 2.0
+    s = math.sqrt(1.0 - rho * rho)
+    t = x[None, :] * a[:, None]                       # inner nodes on [-a, a], per a
+    wt = w[None, :] * a[:, None]
+    phi_t = np.exp(-t * t / 2.0) / math.sqrt(2.0 * math.pi)
+    from scipy.special import ndtr
+    b = a[None, None, :]
+    inner = ndtr((b - rho * t[:, :, None]) / s) - ndtr((-b - rho * t[:, :, None]) / s)
+    F = np.einsum("at,atb->ab", wt * phi_t, inner)    # F_rho(a_i, b_j)
+    A, Bm = np.meshgrid(a, a, indexing="ij")
+    dens = np.exp(-(A * A - 2.0 * rho * A * Bm + Bm * Bm) / (2.0 * s * s)) / (2.0 * math.pi * s)
+    return float(2 * d * np.sum(wa[:, None] * wa[None, :] * dens *
+                                np.power(np.clip(F, 0.0, 1.0), d - 1)))
+
+
+def cp_collision_probability(rho, d: int = 128) -> np.ndarray:
+    """p(rho) for each cosine in rho (see the section comment); -1 -> 0, 1 -> 1."""
+    r = np.clip(np.atleast_1d(as64(rho)), -1.0, 1.0)
+    out = np.zeros_like(r)
+    for i, v in enumerate(r):
+        if v >= 1.0:
+            out[i] = 1.0
+        elif v <= -1.0:
+            out[i] = 0.0
+        elif v > CP_RHO_MAX:
+            p0 = _cp_quadrature(CP_RHO_MAX, d, 192)
+            out[i] = p0 + (1.0 - p0) * (v - CP_RHO_MAX) / (1.0 - CP_RHO_MAX)
+        else:
+            out[i] = _cp_quadrature(float(v), d, 96 if abs(v) <= 0.95 else 192)
+    return out
+
+
 def _log_u_scalar(p: float, K: int, L: int) -> float:
     if L < 2:
         return -math.inf                      # at most one table can collide: u = 0
@@ -348,9 +459,10 @@ def full_attention(q, keys, values, scale: float) -> np.ndarray:
 # ----------------------------------------------------------------------------------------------
 def decode_head(q, keys, values, centre, key_codes, q_code, K: int, L: int, n_sink: int,
                 n_local: int, scale: float | None = None, centred_scores: bool = False,
-                radius: float | None = None) -> dict:
+                radius: float | None = None, cross_polytope: bool = False) -> dict:
     """Steps 3-6 for one query head against its KV head's codes. With `radius` (the MIPS variant)
-    p uses q.kbar_i / (|q| r) in place of the cosine."""
+    p uses q.kbar_i / (|q| r) in place of the cosine; with cross_polytope, p is the
+    cross-polytope collision probability of that cosine (codes are then cross-polytope codes)."""
     qv = as64(q)
     k = as64(keys)
     v = as64(values)
@@ -362,8 +474,17 @@ def decode_head(q, keys, values, centre, key_codes, q_code, K: int, L: int, n_si
     T = exact_set_mask(n, n_sink, n_local)
     S = sampled_set(cnt, T)
     kbar_S = k[S] - mu[None, :]
-    p = collision_probability(qv, kbar_S) if radius is None else \
-        collision_probability_mips(qv, kbar_S, radius)
+    if cross_polytope:
+        kn = np.linalg.norm(kbar_S, axis=1)
+        qn = float(np.linalg.norm(qv))
+        ok = (kn > 0) & (qn > 0)
+        cos = np.zeros(kbar_S.shape[0])
+        cos[ok] = (kbar_S[ok] @ qv) / (qn * kn[ok])
+        p = cp_collision_probability(np.clip(cos, -1.0, 1.0), d)
+    elif radius is None:
+        p = collision_probability(qv, kbar_S)
+    else:
+        p = collision_probability_mips(qv, kbar_S, radius)
     logu = log_inclusion_probability(p, K, L) if S.size else np.zeros(0)
     Tidx = np.nonzero(T)[0]
     if centred_scores:

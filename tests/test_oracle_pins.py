@@ -532,3 +532,87 @@ def test_mips_importance_weights_are_unbiased_over_hyperplane_draws():
         den[m] = np.exp(s[S] - logu[S]).sum()
     se = den.std(ddof=1) / math.sqrt(M)
     assert abs(den.mean() - np.exp(s).sum()) < 4.5 * se, (den.mean(), np.exp(s).sum(), se)
+
+
+# ------------------------------------------------------------------------------------------------
+# Cross-polytope hashing (named by "LSH Sampling..." conclusion as the hash to shrink the tables):
+# code = signed argmax of |G x|, G Gaussian d x d
+# ------------------------------------------------------------------------------------------------
+def test_cp_probability_closed_forms():
+    for d in (8, 128):
+        p = O.cp_collision_probability([0.0, 1.0, -1.0], d)
+        assert abs(p[0] - 1.0 / (2 * d)) < 1e-10 / d      # independent: same index and sign
+        assert p[1] == 1.0 and p[2] == 0.0
+    # d = 1: the code is the sign alone, so p is SimHash's 1 - arccos(rho)/pi
+    rho = np.array([-0.8, -0.3, 0.0, 0.4, 0.9])
+    assert np.allclose(O.cp_collision_probability(rho, 1), 1 - np.arccos(rho) / math.pi,
+                       rtol=0, atol=1e-9)
+    grid = np.linspace(-0.95, 0.99, 40)
+    assert np.all(np.diff(O.cp_collision_probability(grid, 16)) > 0)
+
+
+@pytest.mark.parametrize("rho", [-0.4, 0.0, 0.3, 0.7, 0.95])
+def test_cp_collision_frequency_monte_carlo(rho):
+    d, N = 16, 40_000
+    rng = np.random.default_rng(int(1000 * rho) + 5000)
+    x, y = _pair_at_angle(math.acos(rho), d=d)
+    G = rng.standard_normal((N, d, d))
+    yx, yy = G @ x, G @ y
+    ix, iy = np.argmax(np.abs(yx), axis=1), np.argmax(np.abs(yy), axis=1)
+    r = np.arange(N)
+    same = (ix == iy) & (np.sign(yx[r, ix]) == np.sign(yy[r, iy]))
+    p = float(O.cp_collision_probability([rho], d)[0])
+    sigma = math.sqrt(p * (1 - p) / N)
+    assert abs(float(np.mean(same)) - p) < 4.5 * sigma + 1e-12, (rho, float(np.mean(same)), p)
+
+
+def test_cp_codes_by_brute_force():
+    rng = np.random.default_rng(31)
+    d, L, n = 4, 3, 7
+    G = rng.standard_normal((L, d, d))
+    keys = rng.standard_normal((n, d))
+    mu = O.key_centre(keys)
+    codes, _, _ = O.encode_keys_cp(keys, mu, G)
+    for i in range(n):
+        kb = [keys[i][e] - mu[e] for e in range(d)]
+        for t in range(L):
+            y = [sum(G[t][j][e] * kb[e] for e in range(d)) for j in range(d)]
+            j = max(range(d), key=lambda jj: abs(y[jj]))
+            assert codes[i, t] == 2 * j + (1 if y[j] < 0 else 0)
+    qc, _, _ = O.encode_query_cp(keys[:2], G)             # the query is hashed as given
+    assert np.array_equal(qc[0], O.encode_keys_cp(keys[:1], np.zeros(d), G)[0][0])
+
+
+def test_cp_code_replay_accepts_only_runner_up_near_ties():
+    oc = np.array([[4, 7]])
+    alt = np.array([[5, 2]])
+    near = np.array([[True, False]])
+    out, flips = O.replay_codes(oc, alt, near, np.array([[5, 7]]))
+    assert flips == 1 and out.tolist() == [[5, 7]]
+    with pytest.raises(AssertionError):
+        O.replay_codes(oc, alt, near, np.array([[6, 7]]))     # not the runner-up
+    with pytest.raises(AssertionError):
+        O.replay_codes(oc, alt, near, np.array([[4, 2]]))     # not a near tie
+
+
+def test_cp_importance_weights_are_unbiased_over_rotation_draws():
+    # Horvitz-Thompson with the cross-polytope inclusion probability (one hash per table)
+    rng = np.random.default_rng(33)
+    d, n, L, M = 6, 30, 5, 8000
+    keys = rng.standard_normal((n, d))
+    q = rng.standard_normal(d)
+    mu = O.key_centre(keys)
+    kbar = keys - mu
+    cos = (kbar @ q) / (np.linalg.norm(kbar, axis=1) * np.linalg.norm(q))
+    logu = O.log_inclusion_probability(O.cp_collision_probability(cos, d), 1, L)
+    s = keys @ q / math.sqrt(d)
+    T = O.exact_set_mask(n, 0, 0)
+    den = np.zeros(M)
+    for m in range(M):
+        G = rng.standard_normal((L, d, d))
+        kc = O.encode_keys_cp(keys, mu, G)[0]
+        qc = O.encode_query_cp(q, G)[0][0]
+        S = O.sampled_set(O.collision_counts(kc, qc), T)
+        den[m] = np.exp(s[S] - logu[S]).sum()
+    se = den.std(ddof=1) / math.sqrt(M)
+    assert abs(den.mean() - np.exp(s).sum()) < 4.5 * se, (den.mean(), np.exp(s).sum(), se)
