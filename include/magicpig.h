@@ -54,7 +54,7 @@ extern "C" {
 #define MP_API
 #endif
 
-#define MP_ABI_VERSION 3
+#define MP_ABI_VERSION 4
 #define MP_KEYS_PER_BLOCK 1024
 
 typedef enum {
@@ -71,14 +71,17 @@ typedef enum { MP_F32 = 0, MP_BF16 = 1 } mp_dtype;
 /* Decode parameters. K, L: LSH bits per table and tables ("LSH Sampling...", method details,
  * hash-function choice). n_sink, n_local: the exact set T = {0..n_sink-1} u {n-n_local..n-1},
  * attended with u = 1 and never sampled (Algorithm 1's static cache; "don't pick the tallest",
- * section 5). scale: score scale, 0 means 1/sqrt(d). flags: 0, or MP_FLAG_MIPS.
+ * section 5). scale: score scale, 0 means 1/sqrt(d). flags: 0, MP_FLAG_MIPS or
+ * MP_FLAG_CROSS_POLYTOPE.
  * n_capacity: tokens per head the keys, values and codes are laid out for (0 means n; else
  * n_capacity >= n). A decode cache that grows by appending (mp_encode_keys) keeps one
  * n_capacity for its lifetime and passes the current length as n.
  * n_indexed: keys [0, n_indexed) of each head are in the bucketed tables (0 means n; else
  * n_indexed <= n); only mp_sampled_attention_buckets reads it.
  * radius: with MP_FLAG_MIPS, [B][Hkv] float32 device array from mp_key_radius (the longest
- * centred key of each head); NULL otherwise. */
+ * centred key of each head); NULL otherwise.
+ * logu_table: with MP_FLAG_CROSS_POLYTOPE, the MP_LOGU_TABLE_ENTRIES floats of mp_cp_logu_table
+ * for this K and L; NULL otherwise. */
 typedef struct {
     int K;
     int L;
@@ -89,6 +92,7 @@ typedef struct {
     int n_capacity;
     int n_indexed;
     const float* radius;
+    const float* logu_table;
 } mp_params;
 
 /* MIPS -> cosine variant ("LSH Sampling...", method details, variance reduction with LSH): the
@@ -98,6 +102,18 @@ typedef struct {
  * rows ([d + 1][K*L]; the query uses the first d), the codes come from mp_encode_keys_mips, and
  * every decode call of the variant sets this flag and mp_params.radius. */
 #define MP_FLAG_MIPS 1u
+
+/* Cross-polytope variant (the hash "LSH Sampling..." names in its conclusion as the way to shrink
+ * the tables): table t hashes x to the signed index of the largest |coordinate| of G_t x, G_t a
+ * d x d matrix of i.i.d. N(0, 1) entries, code = 2 i + (1 if negative), one byte (d = 128); keys
+ * are centred, the query is not; one hash per table (K must be 1). W is then G: [L][d][d], row j
+ * of G_t at (t * d + j) * d. Codes are bytes [B][Hkv][ceil(n_cap/1024)][L][1024] (mp_cp_codes_bytes,
+ * written by mp_encode_keys_cp). p_i is the collision probability of two vectors at the cosine
+ * of q and k_i - mu for Gaussian G, p(rho) = 2d int int_{a,b>0} phi_rho(a,b) P[|X|<a, |Y|<b]^(d-1),
+ * which has no closed form: the decode reads log u from mp_params.logu_table, built once by
+ * mp_cp_logu_table (Gauss-Legendre quadrature; above rho = 0.99 p runs linearly to p(1) = 1). */
+#define MP_FLAG_CROSS_POLYTOPE 2u
+#define MP_LOGU_TABLE_ENTRIES 4097
 
 /* Human-readable name of a status code (static storage). */
 MP_API const char* mp_status_string(mp_status s);
@@ -247,6 +263,27 @@ MP_API mp_status mp_encode_keys_mips(const void* keys, mp_dtype key_dtype, const
                                      int B, int Hkv, int n_capacity, int n_begin, int n_end,
                                      int d, int K, int L, uint32_t* codes, float* norms_scratch,
                                      cudaStream_t stream);
+
+/* Cross-polytope variant: bytes of codes for B*Hkv heads of n keys and L tables,
+ * B*Hkv*ceil(n/1024)*L*1024; 0 for invalid shapes. */
+MP_API size_t mp_cp_codes_bytes(int B, int Hkv, int n, int L);
+
+/* Cross-polytope variant: log u at the MP_LOGU_TABLE_ENTRIES cosines -1 + 2 i / 4096, i.e.
+ * log P[Binomial(L, p^K) >= 2] with p the cross-polytope collision probability (d = 128),
+ * into the caller's float32 device array `table`, for mp_params.logu_table. One kernel of a few
+ * milliseconds; build it once per (K, L). Errors: MP_ERR_INVALID_ARG (K, L < 1, null,
+ * misalignment), MP_ERR_UNSUPPORTED (d != 128). */
+MP_API mp_status mp_cp_logu_table(int K, int L, int d, float* table, cudaStream_t stream);
+
+/* Cross-polytope variant: codes of keys [n_begin, n_end) of a cache laid out for n_capacity
+ * tokens per head, G [L][d][d] (MP_F32 or MP_BF16), fp32 on CUDA cores, ties to the smaller
+ * index; other keys' bytes are untouched, so this serves both the build and appends.
+ * codes: mp_cp_codes_bytes(B, Hkv, n_capacity, L) bytes, 16-byte aligned.
+ * Errors: MP_ERR_INVALID_ARG (shapes, range, null, misalignment), MP_ERR_UNSUPPORTED (d != 128). */
+MP_API mp_status mp_encode_keys_cp(const void* keys, mp_dtype key_dtype, const float* centre,
+                                   const void* G, mp_dtype g_dtype, int B, int Hkv,
+                                   int n_capacity, int n_begin, int n_end, int d, int L,
+                                   uint8_t* codes, cudaStream_t stream);
 
 /* mp_build_buckets over keys [0, n) of codes laid out for n_capacity tokens per head (the
  * appendable cache of mp_encode_keys); buckets is mp_buckets_bytes(B, Hkv, n, K, L) bytes. A

@@ -7,7 +7,9 @@ include/magicpig.h. There is no CPU fallback: without the built library every ca
 from .binding import (  # noqa: F401
     MP_BF16,
     MP_F32,
+    MP_FLAG_CROSS_POLYTOPE,
     MP_FLAG_MIPS,
+    MP_LOGU_TABLE_ENTRIES,
     MagicPIGError,
     Params,
     abi_version,
@@ -16,12 +18,15 @@ from .binding import (  # noqa: F401
     buckets_bytes,
     codes_bytes,
     codes_unpack,
+    cp_codes_bytes,
+    cp_logu_table,
     debug_select,
     debug_workspace_bytes,
     decode_attention,
     decode_workspace_bytes,
     device_status,
     encode_keys,
+    encode_keys_cp,
     encode_keys_mips,
     encode_query,
     key_mean,

@@ -20,26 +20,35 @@ class MagicPIGError(RuntimeError):
 
 
 MP_FLAG_MIPS = 1
+MP_FLAG_CROSS_POLYTOPE = 2
+MP_LOGU_TABLE_ENTRIES = 4097
 
 
 class Params(ctypes.Structure):
     """mp_params: K bits per table, L tables, exact sink/local sizes, score scale (0: 1/sqrt(d)),
-    flags (0 or MP_FLAG_MIPS), the cache capacity per head (0: n), the keys in the bucketed
-    tables (0: n), and the MIPS variant's radii (a device pointer, or None)."""
+    flags (0, MP_FLAG_MIPS or MP_FLAG_CROSS_POLYTOPE), the cache capacity per head (0: n), the
+    keys in the bucketed tables (0: n), the MIPS variant's radii and the cross-polytope variant's
+    log u table (device pointers, or None)."""
 
     _fields_ = [("K", ctypes.c_int), ("L", ctypes.c_int), ("n_sink", ctypes.c_int),
                 ("n_local", ctypes.c_int), ("scale", ctypes.c_float), ("flags", ctypes.c_uint),
                 ("n_capacity", ctypes.c_int), ("n_indexed", ctypes.c_int),
-                ("radius", ctypes.c_void_p)]
+                ("radius", ctypes.c_void_p), ("logu_table", ctypes.c_void_p)]
 
 
-def _params(K, L, n_sink, n_local, scale=0.0, n_capacity=0, n_indexed=0, radius=None) -> Params:
-    if radius is not None:
-        _cuda(radius, "radius")
-        if radius.dtype != torch.float32:
-            raise TypeError("radius must be float32")
-    return Params(K, L, n_sink, n_local, scale, MP_FLAG_MIPS if radius is not None else 0,
-                  n_capacity, n_indexed, None if radius is None else radius.data_ptr())
+def _params(K, L, n_sink, n_local, scale=0.0, n_capacity=0, n_indexed=0, radius=None,
+            logu_table=None) -> Params:
+    flags = 0
+    for t, name, flag in ((radius, "radius", MP_FLAG_MIPS),
+                          (logu_table, "logu_table", MP_FLAG_CROSS_POLYTOPE)):
+        if t is not None:
+            _cuda(t, name)
+            if t.dtype != torch.float32:
+                raise TypeError(f"{name} must be float32")
+            flags |= flag
+    return Params(K, L, n_sink, n_local, scale, flags, n_capacity, n_indexed,
+                  None if radius is None else radius.data_ptr(),
+                  None if logu_table is None else logu_table.data_ptr())
 
 
 def _lengths(keys_shape, n):
@@ -71,6 +80,9 @@ def _declare(L):
         "mp_key_mean_cap": (_c_int, [_vp, _c_int] + [_c_int] * 5 + [_vp, _vp, _c_size, _vp]),
         "mp_encode_keys": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 8 + [_vp, _vp]),
         "mp_key_radius": (_c_int, [_vp, _c_int, _vp] + [_c_int] * 5 + [_vp, _vp]),
+        "mp_cp_codes_bytes": (_c_size, [_c_int] * 4),
+        "mp_cp_logu_table": (_c_int, [_c_int] * 3 + [_vp, _vp]),
+        "mp_encode_keys_cp": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 7 + [_vp, _vp]),
         "mp_encode_keys_mips": (_c_int, [_vp, _c_int, _vp, _vp, _c_int, _vp] + [_c_int] * 8
                                 + [_vp, _vp, _vp]),
         "mp_build_tables": (_c_int, [_vp, _c_int, _vp, _vp, _c_int] + [_c_int] * 6 + [_vp, _vp]),
@@ -282,9 +294,43 @@ def encode_keys_mips(keys, centre, W_aug, radius, K: int, L: int, n_begin: int, 
     return codes
 
 
+def cp_codes_bytes(B: int, Hkv: int, n: int, L: int) -> int:
+    return int(lib().mp_cp_codes_bytes(B, Hkv, n, L))
+
+
+def cp_logu_table(K: int, L: int, table=None, d: int = 128, stream=None):
+    """Cross-polytope variant: log u at MP_LOGU_TABLE_ENTRIES cosines on [-1, 1] (float32)."""
+    if table is None:
+        table = torch.empty(MP_LOGU_TABLE_ENTRIES, dtype=torch.float32, device="cuda")
+    _cuda(table, "table")
+    if table.numel() < MP_LOGU_TABLE_ENTRIES or table.dtype != torch.float32:
+        raise ValueError("the table needs MP_LOGU_TABLE_ENTRIES float32 entries")
+    _check(lib().mp_cp_logu_table(K, L, d, _ptr(table), _stream(stream)), "mp_cp_logu_table")
+    return table
+
+
+def encode_keys_cp(keys, centre, G, L: int, n_begin: int, n_end: int, codes=None, stream=None):
+    """Cross-polytope variant: byte codes of keys [n_begin, n_end) (G [L, d, d]); codes laid out
+    for keys.shape[2] keys per head."""
+    _cuda(keys, "keys", 4)
+    B, Hkv, cap, d = keys.shape
+    nbytes = cp_codes_bytes(B, Hkv, cap, L)
+    if codes is None:
+        codes = torch.empty(nbytes, dtype=torch.uint8, device=keys.device)
+    _cuda(codes, "codes")
+    if _nbytes(codes) < nbytes:
+        raise ValueError("codes buffer too small for the cache's capacity")
+    _cuda(centre, "centre", 3)
+    _cuda(G, "G", 3)
+    _check(lib().mp_encode_keys_cp(_ptr(keys), _dtype(keys, "keys"), _ptr(centre), _ptr(G),
+                                   _dtype(G, "G"), B, Hkv, cap, n_begin, n_end, d, L,
+                                   _ptr(codes), _stream(stream)), "mp_encode_keys_cp")
+    return codes
+
+
 def decode_attention(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int,
                      n_local: int, scale: float = 0.0, out=None, workspace=None, stream=None,
-                     n=None, radius=None):
+                     n=None, radius=None, logu_table=None):
     """One LSH-sampled decode step over the first n keys (default: all of keys.shape[2]);
     returns out [B, Hq, d] float32."""
     _cuda(q, "q", 3)
@@ -299,7 +345,7 @@ def decode_attention(q, codes, centre, W, keys, values, K: int, L: int, n_sink: 
     if out is None:
         out = torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
     _cuda(out, "out", 3)
-    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius)
+    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius, logu_table=logu_table)
     need = int(lib().mp_decode_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
     if need == 0:
         raise MagicPIGError("mp_decode_workspace_bytes rejected the shapes/parameters")
@@ -312,7 +358,8 @@ def decode_attention(q, codes, centre, W, keys, values, K: int, L: int, n_sink: 
 
 
 def encode_query(q, centre, W, keys_shape, K: int, L: int, n_sink: int, n_local: int,
-                 workspace, scale: float = 0.0, stream=None, n=None, radius=None):
+                 workspace, scale: float = 0.0, stream=None, n=None, radius=None,
+                 logu_table=None):
     """First half of decode_attention: query codes and norms into `workspace`."""
     _cuda(q, "q", 3)
     _cuda(centre, "centre", 3)
@@ -320,14 +367,15 @@ def encode_query(q, centre, W, keys_shape, K: int, L: int, n_sink: int, n_local:
     B, Hq, d = q.shape
     Hkv = keys_shape[1]
     n, cap = _lengths(keys_shape, n)
-    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius)
+    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius, logu_table=logu_table)
     _check(lib().mp_encode_query(_ptr(q), _dtype(q, "q"), _ptr(centre), _ptr(W), _dtype(W, "W"),
                                  B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(workspace),
                                  _nbytes(workspace), _stream(stream)), "mp_encode_query")
 
 
 def sampled_attention(q, codes, centre, keys, values, K: int, L: int, n_sink: int, n_local: int,
-                      out, workspace, scale: float = 0.0, stream=None, n=None, radius=None):
+                      out, workspace, scale: float = 0.0, stream=None, n=None, radius=None,
+                      logu_table=None):
     """Second half of decode_attention (after encode_query filled `workspace`)."""
     _cuda(q, "q", 3)
     _cuda(keys, "keys", 4)
@@ -337,7 +385,7 @@ def sampled_attention(q, codes, centre, keys, values, K: int, L: int, n_sink: in
     B, Hq, d = q.shape
     Hkv = keys.shape[1]
     n, cap = _lengths(keys.shape, n)
-    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius)
+    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius, logu_table=logu_table)
     _check(lib().mp_sampled_attention(
         _ptr(q), _dtype(q, "q"), _ptr(codes), _ptr(centre), _ptr(keys), _ptr(values),
         _dtype(keys, "keys"), B, Hq, Hkv, n, d, ctypes.byref(p), _ptr(out), _ptr(workspace),
@@ -394,7 +442,7 @@ def sampled_attention_buckets(q, buckets, centre, keys, values, K: int, L: int, 
 
 def debug_select(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int, n_local: int,
                  scale: float = 0.0, counts: bool = True, stream=None, n=None,
-                 radius=None) -> dict:
+                 radius=None, logu_table=None) -> dict:
     """Decode plus its decisions: out, q_bits, per-row ascending sample sets, collision counts."""
     _cuda(q, "q", 3)
     _cuda(keys, "keys", 4)
@@ -403,13 +451,13 @@ def debug_select(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int,
     n, cap = _lengths(keys.shape, n)
     dev = q.device
     C = K * L
-    qwords = (C + 31) // 32
+    qwords = (C + 31) // 32 if logu_table is None else (L + 3) // 4   # bits, or code bytes
     out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
     q_bits = torch.zeros(B, Hq, max(qwords, 1), dtype=torch.int32, device=dev)
     sel_idx = torch.full((B, Hq, n), -1, dtype=torch.int32, device=dev)
     sel_count = torch.zeros(B, Hq, dtype=torch.int32, device=dev)
     cnt = torch.zeros(B, Hq, n, dtype=torch.uint8, device=dev) if counts else None
-    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius)
+    p = _params(K, L, n_sink, n_local, scale, cap, radius=radius, logu_table=logu_table)
     need = int(lib().mp_debug_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
     if need == 0:
         raise MagicPIGError("mp_debug_workspace_bytes rejected the shapes/parameters")

@@ -41,7 +41,7 @@ bool ensure_prepared() {
         return false;
     if (prepare_misc() != cudaSuccess || prepare_decode() != cudaSuccess ||
         prepare_buckets() != cudaSuccess || prepare_append() != cudaSuccess ||
-        prepare_mips() != cudaSuccess)
+        prepare_mips() != cudaSuccess || prepare_cross_polytope() != cudaSuccess)
         return false;
     prepare_encode_tc();   // failure only disables the tensor-core encoder
     cudaGetLastError();
@@ -60,8 +60,14 @@ bool fill_shape(int B, int Hq, int Hkv, int n, int d, const mp_params* prm, Deco
     if (B < 1 || Hq < 1 || Hkv < 1 || n < 1 || d < 1) return false;
     if (Hq % Hkv) return false;
     if (prm->K < 0 || prm->K > 32 || prm->L < 1 || prm->n_sink < 0 || prm->n_local < 0 ||
-        (prm->flags & ~MP_FLAG_MIPS) != 0u || !(prm->scale >= 0.0f))
+        (prm->flags & ~(MP_FLAG_MIPS | MP_FLAG_CROSS_POLYTOPE)) != 0u || !(prm->scale >= 0.0f))
         return false;
+    // cross-polytope: one hash per table, the caller's log u table, not with the MIPS variant
+    const bool cp = (prm->flags & MP_FLAG_CROSS_POLYTOPE) != 0u;
+    if (cp && (prm->K != 1 || (prm->flags & MP_FLAG_MIPS) != 0u || !prm->logu_table ||
+               (reinterpret_cast<uintptr_t>(prm->logu_table) & 3u)))
+        return false;
+    if (!cp && prm->logu_table) return false;
     // the MIPS variant needs the radii; without the flag there must be none
     if (((prm->flags & MP_FLAG_MIPS) != 0u) != (prm->radius != nullptr)) return false;
     if (prm->radius && (reinterpret_cast<uintptr_t>(prm->radius) & 3u)) return false;
@@ -76,13 +82,15 @@ bool fill_shape(int B, int Hq, int Hkv, int n, int d, const mp_params* prm, Deco
     s->K = prm->K;
     s->L = prm->L;
     s->C = prm->K * prm->L;
-    s->qwords = (s->C + 31) / 32;
+    s->qwords = cp ? (prm->L + 3) / 4 : (s->C + 31) / 32;   // bits, or code bytes
     s->cpad = (s->C + 3) & ~3;
     s->nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
     s->ncap = prm->n_capacity > 0 ? prm->n_capacity : n;
     s->cblk = (s->ncap + kKeysPerBlock - 1) / kKeysPerBlock;
     s->n_indexed = prm->n_indexed > 0 ? prm->n_indexed : n;
     s->radius = prm->radius;
+    s->cp = cp;
+    s->logu_ext = prm->logu_table;
     s->n_sink = prm->n_sink;
     s->n_local = prm->n_local;
     s->scale = prm->scale > 0.0f ? prm->scale : 1.0f / sqrtf(static_cast<float>(d));
@@ -144,6 +152,25 @@ DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug) {
     d.logu_tab = reinterpret_cast<float*>(p);
     (void)debug;
     return d;
+}
+
+// The query encoding and the scan + attend of the decode, for the SimHash codes or the
+// cross-polytope ones.
+cudaError_t query_encode(const void* q, bool q_bf16, const float* centre, const void* W,
+                         bool w_bf16, const DecodeShape& s, const DecodeScratch& ws,
+                         cudaStream_t st) {
+    return s.cp ? launch_qencode_cp(q, q_bf16, centre, W, w_bf16, s, ws, st)
+                : launch_qencode(q, q_bf16, centre, W, w_bf16, s, ws, st);
+}
+
+cudaError_t scan_and_attend(const void* q, bool q_bf16, const uint32_t* codes,
+                            const float* centre, const void* keys, const void* values,
+                            bool kv_bf16, const DecodeShape& s, float* out,
+                            const DecodeScratch& ws, cudaStream_t st, int blk0 = 0) {
+    return s.cp ? launch_collide_cp(q, q_bf16, reinterpret_cast<const uint8_t*>(codes), centre,
+                                    keys, values, kv_bf16, s, out, ws, st, blk0)
+                : launch_collide(q, q_bf16, codes, centre, keys, values, kv_bf16, s, out, ws, st,
+                                 blk0);
 }
 
 }  // namespace mp
@@ -308,6 +335,33 @@ mp_status mp_encode_keys_mips(const void* keys, mp_dtype key_dtype, const float*
                                         n_end, K, L, codes, stream));
 }
 
+size_t mp_cp_codes_bytes(int B, int Hkv, int n, int L) { return cp_codes_bytes(B, Hkv, n, L); }
+
+mp_status mp_cp_logu_table(int K, int L, int d, float* table, cudaStream_t stream) {
+    if (K < 1 || L < 1 || !table || !aligned(table, 4)) return MP_ERR_INVALID_ARG;
+    if (d != kD) return MP_ERR_UNSUPPORTED;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    return to_status(launch_cp_logu_table(K, L, table, stream));
+}
+
+mp_status mp_encode_keys_cp(const void* keys, mp_dtype key_dtype, const float* centre,
+                            const void* G, mp_dtype g_dtype, int B, int Hkv, int n_capacity,
+                            int n_begin, int n_end, int d, int L, uint8_t* codes,
+                            cudaStream_t stream) {
+    if (B < 1 || Hkv < 1 || n_capacity < 1 || d < 1 || L < 1) return MP_ERR_INVALID_ARG;
+    if (n_begin < 0 || n_end > n_capacity || n_begin > n_end) return MP_ERR_INVALID_ARG;
+    if (!valid_dtype(key_dtype) || !valid_dtype(g_dtype)) return MP_ERR_INVALID_ARG;
+    if (d != kD) return MP_ERR_UNSUPPORTED;
+    if (n_begin == n_end) return MP_OK;
+    if (!keys || !centre || !G || !codes) return MP_ERR_INVALID_ARG;
+    if (!aligned(keys, 16) || !aligned(codes, 16) || !aligned(centre, 4) ||
+        !aligned(G, g_dtype == MP_BF16 ? 2 : 4))
+        return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    return to_status(launch_encode_cp(keys, key_dtype == MP_BF16, centre, G, g_dtype == MP_BF16,
+                                      B, Hkv, n_capacity, n_begin, n_end, L, codes, stream));
+}
+
 size_t mp_decode_workspace_bytes(int B, int Hq, int Hkv, int n, int d, const mp_params* prm) {
     DecodeShape s;
     if (!fill_shape(B, Hq, Hkv, n, d, prm, &s)) return 0;
@@ -332,10 +386,10 @@ mp_status mp_decode_attention(const void* q, mp_dtype q_dtype, const uint32_t* c
     if (st != MP_OK) return st;
     if (!ensure_prepared()) return MP_ERR_CUDA;
     const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
-    cudaError_t e = launch_qencode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
+    cudaError_t e = query_encode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
                                    stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
-    return to_status(launch_collide(q, q_dtype == MP_BF16, codes, centre, keys, values,
+    return to_status(scan_and_attend(q, q_dtype == MP_BF16, codes, centre, keys, values,
                                     kv_dtype == MP_BF16, s, out, ws, stream));
 }
 
@@ -354,7 +408,7 @@ mp_status mp_encode_query(const void* q, mp_dtype q_dtype, const float* centre, 
     if (ws_bytes < decode_scratch_bytes(s, false)) return MP_ERR_WORKSPACE;
     if (!ensure_prepared()) return MP_ERR_CUDA;
     const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
-    return to_status(launch_qencode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
+    return to_status(query_encode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
                                     stream));
 }
 
@@ -371,7 +425,7 @@ mp_status mp_sampled_attention(const void* q, mp_dtype q_dtype, const uint32_t* 
     if (st != MP_OK) return st;
     if (!ensure_prepared()) return MP_ERR_CUDA;
     const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
-    return to_status(launch_collide(q, q_dtype == MP_BF16, codes, centre, keys, values,
+    return to_status(scan_and_attend(q, q_dtype == MP_BF16, codes, centre, keys, values,
                                     kv_dtype == MP_BF16, s, out, ws, stream));
 }
 
@@ -409,7 +463,7 @@ mp_status mp_sampled_attention_buckets(const void* q, mp_dtype q_dtype, const ui
                                       kv_dtype, B, Hq, Hkv, n, d, prm, out, workspace, ws_bytes,
                                       false, &s);
     if (st != MP_OK) return st;
-    if (s.K > kMaxBucketBits) return MP_ERR_UNSUPPORTED;
+    if (s.K > kMaxBucketBits || s.cp) return MP_ERR_UNSUPPORTED;
     // keys appended since the tables were built come from a scan of their code blocks
     const bool tail = s.n_indexed < s.n && s.C > 0;
     if (tail && (!codes || !aligned(codes, 16))) return MP_ERR_INVALID_ARG;
@@ -418,7 +472,7 @@ mp_status mp_sampled_attention_buckets(const void* q, mp_dtype q_dtype, const ui
     cudaError_t e = launch_bucket_lookup(buckets, ws.qbits, s, ws.sel_ge1, ws.selmask, stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
     if (tail)
-        return to_status(launch_collide(q, q_dtype == MP_BF16, codes, centre, keys, values,
+        return to_status(scan_and_attend(q, q_dtype == MP_BF16, codes, centre, keys, values,
                                         kv_dtype == MP_BF16, s, out, ws, stream,
                                         s.n_indexed / kKeysPerBlock));
     return to_status(launch_attend(q, q_dtype == MP_BF16, centre, keys, values,
@@ -437,13 +491,14 @@ mp_status mp_debug_select(const void* q, mp_dtype q_dtype, const uint32_t* codes
                                       true, &s);
     if (st != MP_OK) return st;
     if (!sel_idx || !sel_count || (s.qwords > 0 && !q_bits)) return MP_ERR_INVALID_ARG;
+    if (s.cp && cnt) return MP_ERR_UNSUPPORTED;   // counts are for the SimHash codes only
     if (!ensure_prepared()) return MP_ERR_CUDA;
     DecodeScratch ws = carve_decode_scratch(workspace, s, true);
     if (s.qwords > 0) ws.qbits = q_bits;
-    cudaError_t e = launch_qencode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
+    cudaError_t e = query_encode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
                                    stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
-    e = launch_collide(q, q_dtype == MP_BF16, codes, centre, keys, values, kv_dtype == MP_BF16, s,
+    e = scan_and_attend(q, q_dtype == MP_BF16, codes, centre, keys, values, kv_dtype == MP_BF16, s,
                        out, ws, stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
     e = launch_compact_selection(ws.selmask, s.B * s.Hq, s.n, s.nblk, sel_idx, sel_count, stream);

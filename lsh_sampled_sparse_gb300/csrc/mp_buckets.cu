@@ -338,12 +338,6 @@ __device__ __forceinline__ uint32_t query_code(const uint32_t* qb, int K, int t)
     return static_cast<uint32_t>((v >> s) & ((1ull << K) - 1ull));
 }
 
-// Programmatic dependent launch: let the next kernel in the stream (the attend kernel, which
-// waits for this grid's completion before it reads the bitmaps) launch and run its prologue.
-__device__ __forceinline__ void allow_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
 // One warp per (query row, table): the query's bucket in that table, kLookupUnroll entries a lane
 // loaded before their atomics are issued, so that a warp waits about three memory round trips.
 __global__ void __launch_bounds__(kLookupWarps * 32)

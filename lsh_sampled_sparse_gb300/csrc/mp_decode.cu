@@ -26,41 +26,6 @@ constexpr int kRingDepth = 4;                       // tables in flight per warp
 constexpr int kRingMinK = 8, kRingMaxK = 11;        // K range the async scan handles
 constexpr int kLuIntervals = kLogUTableIntervals;   // log u table: cosine grid on [-1, 1]
 
-// Programmatic dependent launch: the next kernel in the stream may be scheduled once every CTA
-// of this one has started; a kernel launched that way waits for its predecessor's completion
-// (and memory) before it touches anything the predecessor writes.
-__device__ __forceinline__ void allow_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void wait_for_predecessor() {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// log u(p) = log P[Binomial(L, p^K) >= 2] in fp32 with the accurate library functions, used to
-// fill the per-call table of log u over the cosine; same two-branch definition as below.
-__device__ float log_inclusion_ref(float p, int K, int L) {
-    if (L < 2) return -INFINITY;
-    if (K == 0) return 0.0f;
-    if (!(p > 0.0f)) return kLogFltMin;
-    const float lx = static_cast<float>(K) * logf(p);
-    const float x = expf(lx);
-    const float Lf = static_cast<float>(L);
-    if (x >= 1.0f) return 0.0f;
-    const float l1 = log1pf(-x);
-    if (Lf * x >= 0.5f) {
-        const float u = 1.0f - expf(Lf * l1) - Lf * x * expf((Lf - 1.0f) * l1);
-        return logf(fmaxf(u, 1.17549435e-38f));
-    }
-    const float r = x / (1.0f - x);
-    float term = 1.0f, tot = 1.0f;
-    for (int j = 2; j < L; ++j) {
-        term *= static_cast<float>(L - j) / static_cast<float>(j + 1) * r;
-        tot += term;
-        if (term < 1e-9f * tot) break;
-    }
-    return logf(0.5f * Lf * (Lf - 1.0f)) + 2.0f * lx + (Lf - 2.0f) * l1 + logf(tot);
-}
-
 // 1 / (j + 1) for the binomial-tail series below
 __constant__ float c_inv_next[66] = {
     1.0f / 1, 1.0f / 2, 1.0f / 3, 1.0f / 4, 1.0f / 5, 1.0f / 6, 1.0f / 7, 1.0f / 8, 1.0f / 9,
@@ -437,6 +402,7 @@ struct AArgs {
     int q_bf16, n, nblk, nsb, Hq, Hkv, G, K, L, n_sink, n_local;
     int ncap;                                    // K/V rows per head in memory
     const float* radius;                         // MIPS variant: longest centred key per head
+    int table_only;                              // log u from the table at every cosine
     float scale, log_c2;
     int merge_cap;                               // partials staged per merge round
     int work_bytes;                              // bytes of the list / merge stage region
@@ -711,7 +677,7 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
                 const float den = qn * (a.radius ? rad : sqrtf(kb2));
                 float cs = den > 0.0f ? __fdividef(dot - qmu, den) : 0.0f;
                 cs = fminf(1.0f, fmaxf(-1.0f, cs));
-                if (cs > -0.9f && cs < 0.999f) {
+                if (a.table_only || (cs > -0.9f && cs < 0.999f)) {
                     // linear interpolation in the per-call table of log u over the cosine
                     const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
                     const int i = min(static_cast<int>(tt), kLuIntervals - 1);
@@ -873,22 +839,6 @@ size_t attend_smem_for(int nblk) { return attend_smem(attend_partials(nblk)).tot
 constexpr size_t kMaxSmem = 232448;   // 227 KB opt-in per CTA
 
 // launch `kern` so that it may be scheduled while the previous kernel in the stream finishes
-template <typename Arg>
-cudaError_t launch_dependent(void (*kern)(Arg), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t st, const Arg& arg) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, arg);
-}
-
 }  // namespace
 
 bool decode_supported(const DecodeShape& s, bool kv_bf16) {
@@ -1010,7 +960,8 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
     aa.po = ws.po;
     aa.counters = ws.counters;
     aa.out = out;
-    aa.logu_tab = ws.logu_tab;
+    aa.logu_tab = s.logu_ext ? s.logu_ext : ws.logu_tab;
+    aa.table_only = s.logu_ext != nullptr;     // no closed form for p: the table everywhere
     aa.q_bf16 = q_bf16;
     aa.n = s.n;
     aa.nblk = s.nblk;

@@ -48,6 +48,8 @@ struct DecodeShape {
     int n_indexed;       // keys in the bucketed tables (<= n)
     float scale;
     const float* radius; // MIPS variant: [B*Hkv] longest centred key; nullptr otherwise
+    bool cp;             // cross-polytope variant: byte codes, qwords = ceil(L / 4) words of codes
+    const float* logu_ext;   // cross-polytope: the caller's log u table (nullptr otherwise)
 };
 
 size_t decode_scratch_bytes(const DecodeShape& s, bool debug);
@@ -116,6 +118,25 @@ cudaError_t prepare_decode();
 cudaError_t prepare_misc();
 cudaError_t prepare_append();
 cudaError_t prepare_mips();
+cudaError_t prepare_cross_polytope();
+
+// ---- cross-polytope variant (mp_cross_polytope.cu) ----------------------------------------------
+size_t cp_codes_bytes(int B, int Hkv, int n, int L);
+// log u over kLogUTableIntervals + 1 cosines on [-1, 1] for the cross-polytope p (one hash a table)
+cudaError_t launch_cp_logu_table(int K, int L, float* table, cudaStream_t st);
+// codes of keys [n0, n1): bytes [B*Hkv][ceil(ncap/1024)][L][1024]; G [L][d][d]
+cudaError_t launch_encode_cp(const void* keys, bool keys_bf16, const float* centre, const void* G,
+                             bool g_bf16, int B, int Hkv, int ncap, int n0, int n1, int L,
+                             uint8_t* codes, cudaStream_t st);
+// query codes (bytes in ws.qbits), |q|, q.mu, and the merge counters
+cudaError_t launch_qencode_cp(const void* q, bool q_bf16, const float* centre, const void* G,
+                              bool g_bf16, const DecodeShape& s, const DecodeScratch& ws,
+                              cudaStream_t st);
+// the byte-code scan over blocks [blk0, nblk), then the attend kernel over every block
+cudaError_t launch_collide_cp(const void* q, bool q_bf16, const uint8_t* codes,
+                              const float* centre, const void* keys, const void* values,
+                              bool kv_bf16, const DecodeShape& s, float* out,
+                              const DecodeScratch& ws, cudaStream_t st, int blk0 = 0);
 
 // ---- MIPS -> cosine variant (mp_mips.cu) -------------------------------------------------------
 // radius[bh] = max over keys [0, n) of |k - mu| (radius may be null), and with norms
@@ -128,6 +149,23 @@ cudaError_t launch_encode_mips(const void* keys, bool keys_bf16, const float* ce
                                const void* W, bool w_bf16, const float* radius, int B, int Hkv,
                                int ncap, int n0, int n1, int K, int L, uint32_t* codes,
                                cudaStream_t st);
+
+// Launch `kern` as a programmatic dependent of the previous kernel in the stream.
+template <typename Arg>
+cudaError_t launch_dependent(void (*kern)(Arg), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, const Arg& arg) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, arg);
+}
 
 // ---- small device helpers ---------------------------------------------------------------------
 __device__ __forceinline__ float to_float(float x) { return x; }
@@ -156,6 +194,41 @@ __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
         x = (x & keep) | (r & ~keep);
     }
     return x;
+}
+
+// Programmatic dependent launch: the next kernel in the stream may be scheduled once every CTA
+// of this one has started; a kernel launched that way waits for its predecessor's completion
+// (and memory) before it touches anything the predecessor writes.
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void wait_for_predecessor() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// log u(p) = log P[Binomial(L, p^K) >= 2] in fp32 with the accurate library functions, used to
+// fill the per-call table of log u over the cosine; same two-branch definition as below.
+__device__ inline float log_inclusion_ref(float p, int K, int L) {
+    if (L < 2) return -INFINITY;
+    if (K == 0) return 0.0f;
+    if (!(p > 0.0f)) return -87.336544750553102f;   // log(FLT_MIN)
+    const float lx = static_cast<float>(K) * logf(p);
+    const float x = expf(lx);
+    const float Lf = static_cast<float>(L);
+    if (x >= 1.0f) return 0.0f;
+    const float l1 = log1pf(-x);
+    if (Lf * x >= 0.5f) {
+        const float u = 1.0f - expf(Lf * l1) - Lf * x * expf((Lf - 1.0f) * l1);
+        return logf(fmaxf(u, 1.17549435e-38f));
+    }
+    const float r = x / (1.0f - x);
+    float term = 1.0f, tot = 1.0f;
+    for (int j = 2; j < L; ++j) {
+        term *= static_cast<float>(L - j) / static_cast<float>(j + 1) * r;
+        tot += term;
+        if (term < 1e-9f * tot) break;
+    }
+    return logf(0.5f * Lf * (Lf - 1.0f)) + 2.0f * lx + (Lf - 2.0f) * l1 + logf(tot);
 }
 
 // bits of a 32-key word whose offset within the word is below x (x may be out of [0, 32])

@@ -65,6 +65,7 @@ extern "C" mp_status mp_decode_attention_noalloc(
                        (w_dtype == MP_F32 || w_dtype == MP_BF16) &&
                        (kv_dtype == MP_F32 || kv_dtype == MP_BF16);
     if (!dt_ok) return MP_ERR_INVALID_ARG;
+    if (prm->flags & MP_FLAG_CROSS_POLYTOPE) return MP_ERR_UNSUPPORTED;
     DecodeShape s;
     s.B = B;
     s.Hq = Hq;
@@ -81,6 +82,8 @@ extern "C" mp_status mp_decode_attention_noalloc(
     s.cblk = (s.ncap + kKeysPerBlock - 1) / kKeysPerBlock;
     s.n_indexed = prm->n_indexed > 0 ? prm->n_indexed : n;
     s.radius = prm->radius;
+    s.cp = false;
+    s.logu_ext = nullptr;
     s.n_sink = prm->n_sink;
     s.n_local = prm->n_local;
     s.scale = prm->scale > 0.0f ? prm->scale : 1.0f / sqrtf(static_cast<float>(d));

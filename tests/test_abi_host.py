@@ -41,7 +41,7 @@ def test_status_strings_and_version(L):
     import lsh_sampled_sparse_gb300 as mp
     header_version = int(re.search(r"#define MP_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
     assert mp.abi_version() == header_version
-    assert ctypes.sizeof(mp.Params) == 40          # mp_params: 8 four-byte fields, a pointer
+    assert ctypes.sizeof(mp.Params) == 48          # mp_params: 8 four-byte fields, 2 pointers
     names = [L.mp_status_string(i).decode() for i in range(6)]
     assert names == ["MP_OK", "MP_ERR_INVALID_ARG", "MP_ERR_UNSUPPORTED", "MP_ERR_CUDA",
                      "MP_ERR_TIMEOUT", "MP_ERR_WORKSPACE"]
@@ -183,6 +183,33 @@ def test_mips_variant_rejects_bad_arguments(L):
                                  P(0x10002), None) == 1          # misaligned scratch
     assert L.mp_encode_keys_mips(None, 1, None, None, 1, None, 1, 1, 100, 5, 5, 128, 10, 150,
                                  None, None, None) == 0
+
+
+def test_cross_polytope_variant_rejects_bad_arguments(L):
+    import lsh_sampled_sparse_gb300 as mp
+    P = ctypes.c_void_p
+    ok = P(0x10000)
+    CP, MIPS = mp.MP_FLAG_CROSS_POLYTOPE, mp.MP_FLAG_MIPS
+
+    def ws(K, flags, radius=None, table=None):
+        p = mp.Params(K, 20, 4, 64, 0.0, flags, 0, 0, radius, table)
+        return L.mp_decode_workspace_bytes(1, 4, 1, 1000, 128, ctypes.byref(p))
+    assert ws(1, CP, table=0x10000) > 0
+    assert ws(1, CP) == 0                         # the variant needs its log u table
+    assert ws(2, CP, table=0x10000) == 0          # one hash per table
+    assert ws(1, CP | MIPS, 0x10000, 0x10000) == 0
+    assert ws(1, 0, table=0x10000) == 0           # a table without the flag
+    assert ws(1, CP, table=0x10002) == 0          # misaligned table
+    assert L.mp_cp_logu_table(0, 20, 128, ok, None) == 1
+    assert L.mp_cp_logu_table(1, 20, 64, ok, None) == 2
+    assert L.mp_cp_logu_table(1, 20, 128, None, None) == 1
+    assert L.mp_cp_codes_bytes(1, 8, 98304, 20) == 8 * 96 * 20 * 1024
+    assert L.mp_cp_codes_bytes(1, 8, 0, 20) == 0
+    # mp_encode_keys_cp(keys, dt, centre, G, gdt, B, Hkv, cap, n0, n1, d, L, codes)
+    assert L.mp_encode_keys_cp(ok, 1, ok, ok, 1, 1, 1, 100, 0, 101, 128, 20, ok, None) == 1
+    assert L.mp_encode_keys_cp(ok, 1, ok, ok, 1, 1, 1, 100, 0, 50, 64, 20, ok, None) == 2
+    assert L.mp_encode_keys_cp(None, 1, None, None, 1, 1, 1, 100, 7, 7, 128, 20, None,
+                               None) == 0
 
 
 def test_binding_refuses_cpu_tensors(L):
