@@ -58,6 +58,8 @@ def parse_args(argv=None):
                     help="skip the bucketed-table retrieval measurement")
     ap.add_argument("--no-mips", action="store_true",
                     help="skip the MIPS -> cosine variant measurement")
+    ap.add_argument("--no-cross-polytope", action="store_true",
+                    help="skip the cross-polytope variant measurement")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of as one captured CUDA graph")
     return ap.parse_args(argv)
@@ -385,6 +387,77 @@ def run_mips(mp, wl, state, ws_dec, steps: int, use_graph: bool) -> dict:
             "decode_ms_per_token": ms,
             "decode_queries_per_s": wl.B * wl.Hq * len(state) / (ms / 1e3),
             "mean_rows_per_query_head": rows}
+
+
+CP_TABLES = 16     # cross-polytope tables (one hash each): a sample size near the (10, 150) one
+
+
+def run_cross_polytope(mp, wl, state, steps: int, use_graph: bool) -> dict:
+    """The cross-polytope variant on the same layers: its log u table (once), the CUDA-core
+    encoding (timed on the first layer), then K decode steps over every layer in one graph."""
+    dev = state[0].keys.device
+    L = CP_TABLES
+    g = torch.Generator(device=dev)
+    g.manual_seed(20241016 + 777)
+    G = torch.randn(L, wl.d, wl.d, generator=g, device=dev).to(wl.w_dtype).contiguous()
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev[0].record(stream)
+    table = mp.cp_logu_table(1, L, stream=stream)
+    ev[1].record(stream)
+    codes = []
+    for li, s in enumerate(state):
+        c = torch.empty(mp.cp_codes_bytes(wl.B, wl.Hkv, wl.n, L), dtype=torch.uint8, device=dev)
+        if li == 0:
+            ev[2].record(stream)
+        mp.encode_keys_cp(s.keys, s.centre, G, L, 0, wl.n, c, stream=stream)
+        if li == 0:
+            ev[3].record(stream)
+        codes.append(c)
+    torch.cuda.synchronize()
+    ws = torch.empty(mp.decode_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.n, wl.d, 1, L,
+                                               wl.n_sink, wl.n_local, logu_table=table),
+                     dtype=torch.uint8, device=dev)
+
+    def step(strm):
+        for s, c in zip(state, codes):
+            mp.encode_query(s.q, s.centre, G, s.keys.shape, 1, L, wl.n_sink, wl.n_local, ws,
+                            stream=strm, logu_table=table)
+            mp.sampled_attention(s.q, c, s.centre, s.keys, s.values, 1, L, wl.n_sink,
+                                 wl.n_local, s.out, ws, stream=strm, logu_table=table)
+    for _ in range(3):
+        step(stream)
+    torch.cuda.synchronize()
+    graph = None
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            cap = torch.cuda.current_stream()
+            for _ in range(steps):
+                step(cap)
+    begin, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    begin.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(steps):
+            step(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    assert mp.device_status() == 0
+    ms = begin.elapsed_time(end) / steps
+    s0 = state[0]
+    d = mp.debug_select(s0.q, codes[0], s0.centre, G, s0.keys, s0.values, 1, L, wl.n_sink,
+                        wl.n_local, counts=False, logu_table=table)
+    return {"what": f"cross-polytope variant (one hash per table, L = {L}) on the same layers: "
+                    "log u table once, CUDA-core encoding per layer, decode over every layer",
+            "L": L, "table_ms": ev[0].elapsed_time(ev[1]),
+            "encode_us_per_layer": ev[2].elapsed_time(ev[3]) * 1e3,
+            "codes_bytes_per_layer": len(state) and codes[0].numel(),
+            "decode_ms_per_token": ms,
+            "decode_queries_per_s": wl.B * wl.Hq * len(state) / (ms / 1e3),
+            "mean_rows_per_query_head": float(d["sel_count"].double().mean())}
 
 
 def run_buckets(mp, wl, W, state, ws_dec, steps: int, use_graph: bool, peaks):
@@ -809,6 +882,8 @@ def run_ours(args):
             }
     if not args.no_mips:
         line["mips"] = run_mips(mp, wl, state, ws_dec, args.steps, graph is not None)
+    if not args.no_cross_polytope:
+        line["cross_polytope"] = run_cross_polytope(mp, wl, state, args.steps, graph is not None)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(wl, state, W, args.cpu_seconds)
     if not args.no_e2e:

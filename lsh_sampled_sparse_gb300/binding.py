@@ -185,8 +185,11 @@ def key_mean_workspace_bytes(B: int, Hkv: int, n: int, d: int) -> int:
     return int(lib().mp_key_mean_workspace_bytes(B, Hkv, n, d))
 
 
-def decode_workspace_bytes(B, Hq, Hkv, n, d, K, L, n_sink, n_local, scale=0.0) -> int:
-    p = _params(K, L, n_sink, n_local, scale)
+def decode_workspace_bytes(B, Hq, Hkv, n, d, K, L, n_sink, n_local, scale=0.0, radius=None,
+                           logu_table=None) -> int:
+    """Workspace bytes of a decode with these shapes (and variant: pass the variant's radius or
+    log u table as the decode will)."""
+    p = _params(K, L, n_sink, n_local, scale, radius=radius, logu_table=logu_table)
     return int(lib().mp_decode_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
 
 

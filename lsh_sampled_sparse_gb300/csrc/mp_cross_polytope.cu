@@ -28,6 +28,7 @@ constexpr int kCpOut = 16;           // projections a thread accumulates at once
 constexpr int kCpThreads = 256;      // collide CTA
 constexpr int kCpWarps = kCpThreads / 32;
 constexpr int kCpQThreads = 128;     // query CTA: one thread per projection
+constexpr int kCpQRows = 4;          // query rows per query CTA (<= the CTA's warps)
 constexpr int kCpTableThreads = 256;
 constexpr int kGlMax = 192;          // Gauss-Legendre nodes, at most
 constexpr double kCpRhoMax = 0.99;
@@ -105,55 +106,76 @@ struct CpQArgs {
     uint8_t* qcodes;          // [rows][qbytes]
     float4* qstat;            // [rows] {|q|, q.mu}
     unsigned* counters;       // [rows], reset here
-    int q_bf16, g_bf16, Hq, G_heads, L, qbytes;
+    int q_bf16, g_bf16, Hq, G_heads, L, qbytes, rows;
 };
 
-// One CTA per (table, query row): thread j computes (G_t q)_j, the CTA keeps the first index of
-// the largest |y|. The CTAs of table 0 also write |q| and q.mu and reset the row's merge counter.
+// One CTA per (table, group of kCpQRows query rows): G_t is staged in shared memory (rows padded
+// to 129 floats) with coalesced loads; thread j computes (G_t q)_j for each row of the group, and
+// per row the CTA keeps the first index of the largest |y|. The CTAs of table 0 also write |q|
+// and q.mu and reset the merge counters of their rows.
 __global__ void __launch_bounds__(kCpQThreads) qencode_cp_kernel(const CpQArgs a) {
-    __shared__ float qs[kD];
-    __shared__ float wbest[kCpQThreads / 32];
-    __shared__ int wcode[kCpQThreads / 32];
+    extern __shared__ __align__(16) float qsm[];
+    float* Gs = qsm;                              // [kD][kD + 1]
+    float* qs = qsm + kD * (kD + 1);              // [kCpQRows][kD]
+    __shared__ float wbest[kCpQRows][kCpQThreads / 32];
+    __shared__ int wcode[kCpQRows][kCpQThreads / 32];
     allow_dependents();                           // the scan may start meanwhile
-    const int t = blockIdx.x, row = blockIdx.y, j = threadIdx.x, lane = j & 31, warp = j >> 5;
-    qs[j] = load_elem(a.q, a.q_bf16, static_cast<size_t>(row) * kD + j);
+    const int t = blockIdx.x, r0 = blockIdx.y * kCpQRows, j = threadIdx.x;
+    const int lane = j & 31, warp = j >> 5;
+    const int nr = min(kCpQRows, a.rows - r0);
+    for (int idx = j; idx < kD * kD; idx += kCpQThreads)
+        Gs[(idx / kD) * (kD + 1) + idx % kD] =
+            load_elem(a.G, a.g_bf16, static_cast<size_t>(t) * kD * kD + idx);
+    for (int idx = j; idx < kCpQRows * kD; idx += kCpQThreads)
+        qs[idx] = idx < nr * kD ? load_elem(a.q, a.q_bf16, static_cast<size_t>(r0) * kD + idx)
+                                : 0.0f;
     __syncthreads();
-    float y = 0.0f;
-    for (int e = 0; e < kD; ++e)
-        y = fmaf(load_elem(a.G, a.g_bf16, (static_cast<size_t>(t) * kD + j) * kD + e), qs[e], y);
-    float best = fabsf(y);
-    int code = 2 * j + (y < 0.0f ? 1 : 0);
+    float y[kCpQRows];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {                // larger |y| wins, the smaller index on a tie
-        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oc = __shfl_xor_sync(0xffffffffu, code, o);
-        if (ob > best || (ob == best && oc < code)) {
-            best = ob;
-            code = oc;
+    for (int r = 0; r < kCpQRows; ++r) y[r] = 0.0f;
+    for (int e = 0; e < kD; ++e) {
+        const float g = Gs[j * (kD + 1) + e];
+#pragma unroll
+        for (int r = 0; r < kCpQRows; ++r) y[r] = fmaf(g, qs[r * kD + e], y[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < kCpQRows; ++r) {
+        float best = fabsf(y[r]);
+        int code = 2 * j + (y[r] < 0.0f ? 1 : 0);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {            // larger |y| wins, the smaller index on a tie
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oc = __shfl_xor_sync(0xffffffffu, code, o);
+            if (ob > best || (ob == best && oc < code)) {
+                best = ob;
+                code = oc;
+            }
+        }
+        if (lane == 0) {
+            wbest[r][warp] = best;
+            wcode[r][warp] = code;
         }
     }
-    if (lane == 0) {
-        wbest[warp] = best;
-        wcode[warp] = code;
-    }
     __syncthreads();
-    if (j == 0) {
-        float b = wbest[0];
-        int c = wcode[0];
+    if (j < nr) {
+        float b = wbest[j][0];
+        int c = wcode[j][0];
         for (int w = 1; w < kCpQThreads / 32; ++w)
-            if (wbest[w] > b || (wbest[w] == b && wcode[w] < c)) {
-                b = wbest[w];
-                c = wcode[w];
+            if (wbest[j][w] > b || (wbest[j][w] == b && wcode[j][w] < c)) {
+                b = wbest[j][w];
+                c = wcode[j][w];
             }
-        a.qcodes[static_cast<size_t>(row) * a.qbytes + t] = static_cast<uint8_t>(c);
+        a.qcodes[static_cast<size_t>(r0 + j) * a.qbytes + t] = static_cast<uint8_t>(c);
     }
-    if (t == 0 && warp == 0) {
+    if (t == 0 && warp < nr) {                    // warp r: |q| and q.mu of row r0 + r
+        const int row = r0 + warp;
         const int b = row / a.Hq, h = row % a.Hq, Hkv = a.Hq / a.G_heads;
         const float* mu = a.centre + (static_cast<size_t>(b) * Hkv + h / a.G_heads) * kD;
         float nn = 0.0f, qm = 0.0f;
         for (int e = lane; e < kD; e += 32) {
-            nn = fmaf(qs[e], qs[e], nn);
-            qm = fmaf(qs[e], mu[e], qm);
+            const float x = qs[warp * kD + e];
+            nn = fmaf(x, x, nn);
+            qm = fmaf(x, mu[e], qm);
         }
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
@@ -392,7 +414,10 @@ cudaError_t launch_qencode_cp(const void* q, bool q_bf16, const float* centre, c
     a.G_heads = s.Hq / s.Hkv;
     a.L = s.L;
     a.qbytes = s.qwords * 4;
-    qencode_cp_kernel<<<dim3(s.L, s.B * s.Hq), kCpQThreads, 0, st>>>(a);
+    a.rows = s.B * s.Hq;
+    const size_t smem = (static_cast<size_t>(kD) * (kD + 1) + static_cast<size_t>(kCpQRows) * kD) *
+                        sizeof(float);
+    qencode_cp_kernel<<<dim3(s.L, (a.rows + kCpQRows - 1) / kCpQRows), kCpQThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -432,7 +457,11 @@ cudaError_t prepare_cross_polytope() {
                                                           sizeof(float)));
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, qencode_cp_kernel)) != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(qencode_cp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>((static_cast<size_t>(kD) * (kD + 1) +
+                                                    static_cast<size_t>(kCpQRows) * kD) *
+                                                   sizeof(float)))) != cudaSuccess)
+        return e;
     if ((e = cudaFuncGetAttributes(&fa, cp_logu_table_kernel)) != cudaSuccess) return e;
     for (int G : {1, 2, 4, 8}) {
         size_t sm = 0;
