@@ -451,7 +451,8 @@ def run_cross_polytope(mp, wl, state, steps: int, use_graph: bool) -> dict:
     d = mp.debug_select(s0.q, codes[0], s0.centre, G, s0.keys, s0.values, 1, L, wl.n_sink,
                         wl.n_local, counts=False, logu_table=table)
     return {"what": f"cross-polytope variant (one hash per table, L = {L}) on the same layers: "
-                    "log u table once, CUDA-core encoding per layer, decode over every layer",
+                    "log u table once, tcgen05 encoding (argmax epilogue) per layer, decode over "
+                    "every layer",
             "L": L, "table_ms": ev[0].elapsed_time(ev[1]),
             "encode_us_per_layer": ev[2].elapsed_time(ev[3]) * 1e3,
             "codes_bytes_per_layer": len(state) and codes[0].numel(),

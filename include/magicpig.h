@@ -276,8 +276,10 @@ MP_API size_t mp_cp_codes_bytes(int B, int Hkv, int n, int L);
 MP_API mp_status mp_cp_logu_table(int K, int L, int d, float* table, cudaStream_t stream);
 
 /* Cross-polytope variant: codes of keys [n_begin, n_end) of a cache laid out for n_capacity
- * tokens per head, G [L][d][d] (MP_F32 or MP_BF16), fp32 on CUDA cores, ties to the smaller
- * index; other keys' bytes are untouched, so this serves both the build and appends.
+ * tokens per head, G [L][d][d] (MP_F32 or MP_BF16), ties to the smaller index. With bf16 keys and
+ * G and more than 64 keys, whole 1024-key blocks are re-encoded on the tensor cores (the
+ * encoder's projections, an argmax instead of the signs); otherwise fp32 CUDA cores encode the
+ * range itself and leave other keys' bytes untouched (appends).
  * codes: mp_cp_codes_bytes(B, Hkv, n_capacity, L) bytes, 16-byte aligned.
  * Errors: MP_ERR_INVALID_ARG (shapes, range, null, misalignment), MP_ERR_UNSUPPORTED (d != 128). */
 MP_API mp_status mp_encode_keys_cp(const void* keys, mp_dtype key_dtype, const float* centre,

@@ -358,6 +358,16 @@ mp_status mp_encode_keys_cp(const void* keys, mp_dtype key_dtype, const float* c
         !aligned(G, g_dtype == MP_BF16 ? 2 : 4))
         return MP_ERR_INVALID_ARG;
     if (!ensure_prepared()) return MP_ERR_CUDA;
+    if (key_dtype == MP_BF16 && g_dtype == MP_BF16 && n_end - n_begin > kAppendMaxKeys) {
+        // whole 1024-key blocks on the tensor cores (a table is d hyperplanes of the encoder)
+        const int blk0 = n_begin / kKeysPerBlock;
+        const int blk1 = (n_end + kKeysPerBlock - 1) / kKeysPerBlock;
+        const cudaError_t e = launch_encode_tc(keys, centre, G, B, Hkv, n_capacity, blk0, blk1, kD,
+                                               L, reinterpret_cast<uint32_t*>(codes),
+                                               device_status_ptr(), stream, nullptr, nullptr, true);
+        if (e != cudaErrorNotSupported) return to_status(e);
+        cudaGetLastError();
+    }
     return to_status(launch_encode_cp(keys, key_dtype == MP_BF16, centre, G, g_dtype == MP_BF16,
                                       B, Hkv, n_capacity, n_begin, n_end, L, codes, stream));
 }

@@ -66,6 +66,10 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffC % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
 
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s: far beyond any real wait
+constexpr int kSign = 0, kMips = 1, kArgmax = 2;         // epilogue modes of the encoder
+constexpr uint32_t kXchOff = 2 * kKeysPerBlock;          // argmax: exchange area after the codes
+static_assert(kXchOff + 2 * 2 * 2 * kTileM * 8 <= kWordsPerBlock * kStgPitch * 4,
+              "the argmax staging fits the word staging area");
 
 struct EncodeArgs {
     const float* centre;            // [BH][128]
@@ -202,10 +206,14 @@ __device__ __forceinline__ uint32_t pack_signs(const uint32_t (&v)[32]) {
     }
     return x[0] | (x[1] << 8) | (x[2] << 16) | (x[3] << 24);
 }
-// kMips: the MIPS -> cosine variant, whose keys carry an extra coordinate a_i = sqrt(max(0,
-// r^2 - |k_i - mu|^2)) on a (d + 1)-th row of W: the epilogue subtracts W[d][j] a_i from each
-// accumulator before taking its sign (one fp32 FMA per element).
-template <bool kMips>
+// kMode: kSign, the SimHash codes; kMips, the MIPS -> cosine variant, whose keys carry an extra
+// coordinate a_i = sqrt(max(0, r^2 - |k_i - mu|^2)) on a (d + 1)-th row of W: the epilogue
+// subtracts W[d][j] a_i from each accumulator before taking its sign (one fp32 FMA per element);
+// kArgmax, the cross-polytope codes: W is G [L][d][d] (hyperplane j = row j % d of G_{j / d}), a
+// chunk holds two tables, and the epilogue keeps, per key and table, the first index of the
+// largest |accumulator| (two warps cover a table's 128 columns and meet in shared memory), then
+// writes one code byte per (table, key).
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     encode_tc_kernel(const __grid_constant__ CUtensorMap kmap, const EncodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -256,7 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int idx = base + k * kThreads + tid;
                 const int r = idx % kChunkN, e = idx / kChunkN;
                 w[k] = __float2bfloat16(0.0f);
-                if (idx < kElems && r < Nc) w[k] = __hneg(a.W[static_cast<size_t>(e) * a.C + j0 + r]);
+                if (idx < kElems && r < Nc)
+                    w[k] = __hneg(kMode == kArgmax ? a.W[static_cast<size_t>(j0 + r) * kD + e]
+                                                   : a.W[static_cast<size_t>(e) * a.C + j0 + r]);
             }
 #pragma unroll
             for (int k = 0; k < kBatch; ++k) {
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tquad = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
         bool aborted = false;
         float* sWd = reinterpret_cast<float*>(smem + kOffWd);
-        if constexpr (kMips) {
+        if constexpr (kMode == kMips) {
             if (et < kChunkN)
                 sWd[et] = et < Nc ? __bfloat162float(a.W[static_cast<size_t>(kD) * a.C + j0 + et])
                                   : 0.0f;
@@ -428,15 +438,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fnt = tiles_in_block(fblk);
             }
         };
-        // one unit's staged words -> its Nc plane rows in global memory (coalesced rows)
+        // one unit's staged words -> its Nc plane rows in global memory (coalesced rows); for
+        // the argmax codes, its Nc / d table rows of 1024 code bytes
+        uint8_t* stg_bytes = reinterpret_cast<uint8_t*>(stg);
         auto store_unit = [&](int bg, int blk) {
             epi_sync();
             if (!aborted) {
-                uint32_t* dst = a.codes + (static_cast<size_t>(bg) * a.cblk + a.blk0 + blk) *
-                                              static_cast<size_t>(a.C) * kWordsPerBlock +
-                                static_cast<size_t>(j0) * kWordsPerBlock;
-                for (int r = ew; r < Nc; r += kEpiWarps)
-                    dst[r * kWordsPerBlock + lane] = stg[lane * kStgPitch + r];
+                if constexpr (kMode == kArgmax) {
+                    const int ntab = Nc / kD, L = a.C / kD;
+                    uint8_t* dst = reinterpret_cast<uint8_t*>(a.codes) +
+                                   ((static_cast<size_t>(bg) * a.cblk + a.blk0 + blk) * L + j0 / kD) *
+                                       kKeysPerBlock;
+                    if (et < ntab * (kKeysPerBlock / 4))
+                        reinterpret_cast<uint32_t*>(dst)[et] =
+                            reinterpret_cast<const uint32_t*>(stg_bytes)[et];
+                } else {
+                    uint32_t* dst = a.codes + (static_cast<size_t>(bg) * a.cblk + a.blk0 + blk) *
+                                                  static_cast<size_t>(a.C) * kWordsPerBlock +
+                                    static_cast<size_t>(j0) * kWordsPerBlock;
+                    for (int r = ew; r < Nc; r += kEpiWarps)
+                        dst[r * kWordsPerBlock + lane] = stg[lane * kStgPitch + r];
+                }
             }
             epi_sync();
         };
@@ -461,8 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // sign bits of this warp's two 32-column groups into registers (one TMEM wait
                 // per group keeps 32 accumulator registers live) ...
                 uint32_t x[2] = {0u, 0u};
+                float best64 = -1.0f;        // argmax: this lane's key over this warp's 64 columns
+                int code64 = 0;
                 float aext = 0.0f;           // MIPS: this lane's key's extra coordinate
-                if constexpr (kMips) {
+                if constexpr (kMode == kMips) {
                     const int key = (a.blk0 + blk) * kKeysPerBlock + t * kTileM + quad * 32 + lane;
                     const float r = __ldg(a.radius + bg);
                     const float nk = key < a.n ? __ldg(a.norms + static_cast<size_t>(bg) * a.n + key)
@@ -478,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint32_t v[32];
                             tmem_ld32(trow + colA + 32 * g, v);
                             tmem_ld_wait();
-                            if constexpr (kMips) {
+                            if constexpr (kMode == kMips) {
                                 const float4* wd4 = reinterpret_cast<const float4*>(sWd + colA + 32 * g);
 #pragma unroll
                                 for (int c4 = 0; c4 < 8; ++c4) {
@@ -489,7 +513,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     v[4 * c4 + 3] = __float_as_uint(fmaf(-w.w, aext, __uint_as_float(v[4 * c4 + 3])));
                                 }
                             }
-                            x[g] = pack_signs(v);
+                            if constexpr (kMode == kArgmax) {
+                                // y = -accumulator; first index of the largest |y| of the group
+                                float bst = -1.0f;
+                                int cd = 0;
+#pragma unroll
+                                for (int c = 0; c < 32; ++c) {
+                                    const float ac = __uint_as_float(v[c]);
+                                    if (fabsf(ac) > bst) {
+                                        bst = fabsf(ac);
+                                        cd = 2 * ((colA & (kD - 1)) + 32 * g + c) + (ac > 0.0f ? 1 : 0);
+                                    }
+                                }
+                                if (g == 0 || bst > best64) {
+                                    best64 = bst;
+                                    code64 = cd;
+                                }
+                            } else {
+                                x[g] = pack_signs(v);
+                            }
                         }
                     }
                 }
@@ -501,7 +543,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the previous unit's rows go out only now, after this unit's first buffer
                 // was released, so that the MMA keeps running meanwhile
                 if (t == 0 && prev_bg >= 0) store_unit(prev_bg, prev_blk);
-                if (!aborted) {
+                if constexpr (kMode == kArgmax) {
+                    // the two halves of a table meet: (|y|, code) per (table, half, key row) in
+                    // the exchange area (two parities, so a tile's reads never race the next
+                    // tile's writes), then the lower half picks and stages the code byte
+                    const int tab = colA / kD, half = (colA / 64) & 1, row = quad * 32 + lane;
+                    float2* xch = reinterpret_cast<float2*>(stg_bytes + kXchOff) +
+                                  (it & 1) * (2 * 2 * kTileM);
+                    if (!aborted && colA < Nc)
+                        xch[(tab * 2 + half) * kTileM + row] =
+                            make_float2(best64, __int_as_float(code64));
+                    epi_sync();
+                    if (!aborted && colA < Nc && half == 0) {
+                        const float2 o = xch[(tab * 2 + 1) * kTileM + row];
+                        const int code = o.x > best64 ? __float_as_int(o.y) : code64;
+                        stg_bytes[tab * kKeysPerBlock + t * kTileM + row] = static_cast<uint8_t>(code);
+                    }
+                } else if (!aborted) {
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {
                         const int col = colA + 32 * g;
@@ -553,19 +611,18 @@ EncodeTiledFn encode_tiled_fn() {
 }  // namespace
 
 cudaError_t prepare_encode_tc() {
-    cudaError_t e = cudaFuncSetAttribute(encode_tc_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(encode_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e != cudaSuccess) return e;
+    for (auto fn : {encode_tc_kernel<kSign>, encode_tc_kernel<kMips>, encode_tc_kernel<kArgmax>}) {
+        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   kSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
     return encode_tiled_fn() ? cudaSuccess : cudaErrorNotSupported;
 }
 
 cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* W, int B,
                              int Hkv, int ncap, int blk0, int blk1, int K, int L,
                              uint32_t* codes, int* status, cudaStream_t st, const float* norms,
-                             const float* radius) {
+                             const float* radius, bool argmax) {
     const int C = K * L;
     if (C == 0 || blk1 <= blk0) return cudaSuccess;
     EncodeTiledFn enc = encode_tiled_fn();
@@ -599,10 +656,12 @@ cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* 
     if (parts < 1) parts = 1;
     if (parts > a.units) parts = a.units;
     a.parts = parts;
-    if (norms)
-        encode_tc_kernel<true><<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
+    if (argmax)
+        encode_tc_kernel<kArgmax><<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
+    else if (norms)
+        encode_tc_kernel<kMips><<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
     else
-        encode_tc_kernel<false><<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
+        encode_tc_kernel<kSign><<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
     return cudaGetLastError();
 }
 

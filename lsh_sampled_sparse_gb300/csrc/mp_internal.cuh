@@ -63,11 +63,13 @@ int key_mean_splits(int n);
 // Encode whole 1024-key blocks [blk0, blk1) of every head of a cache laid out for ncap keys
 // per head (keys >= ncap read as zero).
 // With norms (|k_i - mu| per key, [B*Hkv][ncap]) and radius ([B*Hkv]): the MIPS variant, W with
-// d + 1 rows.
+// d + 1 rows. With argmax: the cross-polytope codes (bytes), W = G [L][d][d], K = d (a table is
+// d hyperplanes).
 cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* W, int B,
                              int Hkv, int ncap, int blk0, int blk1, int K, int L,
                              uint32_t* codes, int* status, cudaStream_t st,
-                             const float* norms = nullptr, const float* radius = nullptr);
+                             const float* norms = nullptr, const float* radius = nullptr,
+                             bool argmax = false);
 cudaError_t launch_encode_simt(const void* keys, bool keys_bf16, const float* centre,
                                const void* W, bool w_bf16, int B, int Hkv, int ncap, int blk0,
                                int blk1, int K, int L, uint32_t* codes, cudaStream_t st);

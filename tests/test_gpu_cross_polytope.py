@@ -60,11 +60,14 @@ def test_cp_logu_table_matches_the_oracle(mp):
             assert abs(g - w) <= 2e-4 * max(1.0, abs(w)), (i, g, w)
 
 
-def test_cp_decode_matches_the_oracle(mp):
-    wl = small_workload(B=1, Hq=4, Hkv=2, n=2000, K=1, L=L_CP)
+@pytest.mark.parametrize("dt", [BF, F32])
+def test_cp_decode_matches_the_oracle(mp, dt):
+    # bf16: the tensor-core encoder's argmax epilogue; fp32: the CUDA-core encoder
+    wl = small_workload(B=1, Hq=4, Hkv=2, n=2000, K=1, L=L_CP, kv_dtype=dt, q_dtype=dt,
+                        w_dtype=dt)
     x = make_layer(wl)
     xc = {k: v.cuda() for k, v in x.items()}
-    G = _rotations(L_CP, wl.d, 77, BF)
+    G = _rotations(L_CP, wl.d, 77, dt)
     Gc = G.cuda()
     table = mp.cp_logu_table(1, L_CP)
     centre = mp.key_mean(xc["keys"])
