@@ -139,3 +139,46 @@ def test_cp_ranges_and_spare_capacity(mp):
     torch.cuda.synchronize()
     assert torch.equal(got, want)
     assert mp.device_status() == 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(B=1, Hq=8, Hkv=1, n=1500, L=15),      # odd L: the last encoder chunk holds one table
+    dict(B=2, Hq=2, Hkv=2, n=1100, L=3),       # no GQA, few tables, a ragged block
+])
+def test_cp_odd_tables_and_group_sizes(mp, shape):
+    L = shape.pop("L")
+    wl = small_workload(K=1, L=L, **shape)
+    x = make_layer(wl)
+    xc = {k: v.cuda() for k, v in x.items()}
+    G = _rotations(L, wl.d, 79, BF)
+    Gc = G.cuda()
+    table = mp.cp_logu_table(1, L)
+    centre = mp.key_mean(xc["keys"])
+    codes = mp.encode_keys_cp(xc["keys"], centre, Gc, L, 0, wl.n)        # tensor cores
+    simt = torch.zeros_like(codes)
+    for a in range(0, wl.n, 64):                                          # CUDA cores
+        mp.encode_keys_cp(xc["keys"], centre, Gc, L, a, min(wl.n, a + 64), simt)
+    dbg = mp.debug_select(xc["q"], codes, centre, Gc, xc["keys"], xc["values"], 1, L,
+                          wl.n_sink, wl.n_local, counts=False, logu_table=table)
+    torch.cuda.synchronize()
+    assert mp.device_status() == 0
+    gk = _unpack(codes, wl.B, wl.Hkv, wl.n, L)
+    gs = _unpack(simt, wl.B, wl.Hkv, wl.n, L)
+    cen = centre.cpu().double().numpy()
+    Gd = G.double().numpy()
+    qbytes = dbg["q_bits"].cpu().numpy().view(np.uint8).reshape(wl.B, wl.Hq, -1)[:, :, :L]
+    for b in range(wl.B):
+        for g in range(wl.Hkv):
+            keys = O.as64(x["keys"][b, g])
+            oc, alt, near = O.encode_keys_cp(keys, cen[b, g], Gd)
+            kc, _ = O.replay_codes(oc, alt, near, gk[b, g], what="tensor-core codes")
+            O.replay_codes(oc, alt, near, gs[b, g], what="CUDA-core codes")
+            for h in range(g * wl.G, (g + 1) * wl.G):
+                qv = O.as64(x["q"][b, h])
+                qo, qa, qn = O.encode_query_cp(qv, Gd)
+                qc, _ = O.replay_codes(qo, qa, qn, qbytes[b, h][None, :].astype(np.int64))
+                r = O.decode_head(qv, keys, O.as64(x["values"][b, g]), cen[b, g], kc, qc[0], 1, L,
+                                  wl.n_sink, wl.n_local, cross_polytope=True)
+                cnt = int(dbg["sel_count"][b, h])
+                assert np.array_equal(dbg["sel_idx"][b, h, :cnt].cpu().numpy(), r["S"])
+                assert row_rel_err(dbg["out"][b, h].cpu().numpy(), r["o"]) <= OUT_REL_TOL
