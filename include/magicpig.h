@@ -111,7 +111,9 @@ typedef struct {
  * written by mp_encode_keys_cp). p_i is the collision probability of two vectors at the cosine
  * of q and k_i - mu for Gaussian G, p(rho) = 2d int int_{a,b>0} phi_rho(a,b) P[|X|<a, |Y|<b]^(d-1),
  * which has no closed form: the decode reads log u from mp_params.logu_table, built once by
- * mp_cp_logu_table (Gauss-Legendre quadrature; above rho = 0.99 p runs linearly to p(1) = 1). */
+ * mp_cp_logu_table (Gauss-Legendre quadrature; above rho = 0.99 p runs linearly to p(1) = 1).
+ * Not with the MIPS variant, the bucketed tables or mp_decode_attention_noalloc
+ * (MP_ERR_UNSUPPORTED there), and mp_debug_select gives no collision counts for it. */
 #define MP_FLAG_CROSS_POLYTOPE 2u
 #define MP_LOGU_TABLE_ENTRIES 4097
 

@@ -15,8 +15,6 @@
 // (mp_cp_logu_table); the decode then runs the same attend kernel on that table.
 #include <math.h>
 
-#include <vector>
-
 #include "mp_internal.cuh"
 
 namespace mp {

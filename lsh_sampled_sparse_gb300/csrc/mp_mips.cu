@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kMipsKeys)
                        int cblk, uint32_t* codes) {
     __shared__ float kbar[kMipsKeys][kD + 1];
     __shared__ float Wsm[kD + 1][kMipsPlanes];
-    const int bh = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int bh = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
     const int i0 = (n0 / kMipsKeys + blockIdx.x) * kMipsKeys;
     for (int idx = tid; idx < kMipsKeys * kD; idx += kMipsKeys) {
         const int r = idx / kD, e = idx % kD, i = i0 + r;
@@ -115,7 +115,6 @@ __global__ void __launch_bounds__(kMipsKeys)
             *p = keep == 0xffffffffu ? mine : ((*p & ~keep) | (mine & keep));
         }
     }
-    (void)warp;
 }
 
 }  // namespace
