@@ -21,6 +21,7 @@ constexpr int kAttendBlocks = kAttendBlockGroup;
 constexpr int kAWarps = 4;                          // attend CTA: 4 warps, 8 half-warps on rows
 static_assert(kAttendBlocks <= kAWarps, "one warp lists each block of an attend CTA");
 constexpr int kAThreads = 32 * kAWarps;
+constexpr int kRing = 4;                            // rows in flight per lane (cp.async ring)
 static_assert(kAThreads == kD, "the attend merge gives one thread to each of the 128 output dims");
 constexpr int kRingDepth = 4;                       // tables in flight per warp in the async scan
 constexpr int kRingMinK = 8, kRingMaxK = 11;        // K range the async scan handles
@@ -203,7 +204,13 @@ struct AttendSmem {
     size_t work, total;
     int merge_cap;
 };
-inline AttendSmem attend_smem(int nsp) {
+// Bytes of the per-lane row ring for K/V elements of kv_elem bytes: kRing slots of a K and a V
+// fragment (16 bytes per bf16 fragment, 32 per fp32 one) for each of the CTA's lanes.
+__host__ __device__ constexpr size_t attend_ring_bytes(size_t kv_elem) {
+    return static_cast<size_t>(kRing) * 2 * kv_elem * 8 * kAThreads;
+}
+
+inline AttendSmem attend_smem(int nsp, size_t kv_elem) {
     constexpr size_t kList = static_cast<size_t>(kAttendBlocks) * kKeysPerBlock * 4;
     constexpr size_t kRow = static_cast<size_t>(kD) * 4;
     size_t work = static_cast<size_t>(nsp) * kRow;
@@ -212,7 +219,8 @@ inline AttendSmem attend_smem(int nsp) {
     AttendSmem m;
     m.work = work;
     m.merge_cap = static_cast<int>(work / kRow);
-    m.total = work + static_cast<size_t>(kAWarps) * kCombinePitch * 4 + 32;
+    m.total = work + static_cast<size_t>(kAWarps) * kCombinePitch * 4 + 64 +
+              attend_ring_bytes(kv_elem);
     return m;
 }
 
@@ -510,6 +518,7 @@ struct RowFrag<__nv_bfloat16> {
         k = __ldg(reinterpret_cast<const uint4*>(kp));
         v = __ldg(reinterpret_cast<const uint4*>(vp));
     }
+    __device__ __forceinline__ void from_pieces(const uint4 (&p)[2]) { k = p[0]; v = p[1]; }
     __device__ __forceinline__ void unpack(float (&kf)[8], float (&vf)[8]) const {
         const uint32_t kw[4] = {k.x, k.y, k.z, k.w}, vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -531,6 +540,12 @@ struct RowFrag<float> {
         k1 = __ldg(reinterpret_cast<const float4*>(kp) + 1);
         v0 = __ldg(reinterpret_cast<const float4*>(vp));
         v1 = __ldg(reinterpret_cast<const float4*>(vp) + 1);
+    }
+    __device__ __forceinline__ void from_pieces(const uint4 (&p)[4]) {
+        k0 = *reinterpret_cast<const float4*>(&p[0]);
+        k1 = *reinterpret_cast<const float4*>(&p[1]);
+        v0 = *reinterpret_cast<const float4*>(&p[2]);
+        v1 = *reinterpret_cast<const float4*>(&p[3]);
     }
     __device__ __forceinline__ void unpack(float (&kf)[8], float (&vf)[8]) const {
         kf[0] = k0.x; kf[1] = k0.y; kf[2] = k0.z; kf[3] = k0.w;
@@ -554,8 +569,9 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned* p, unsigned
 // the exact set T = [0, n_sink) u [n - n_local, n) with log u = 0, so that the 68 sink/local rows
 // do not pile onto the CTA of the last blocks. Each CTA folds its rows into one partial softmax;
 // the last CTA of each query row merges the row's nsb + 1 partials by log-sum-exp.
-// Each half-warp reads its rows straight from global memory (16 lanes x 16 bytes of a bf16 row),
-// with the rows two and one ahead in flight while the current row is reduced.
+// Each half-warp takes every eighth row; each lane streams its own pieces of the rows (16 bytes
+// of a bf16 K row and of its V row) through a private ring of kRing slots in shared memory with
+// cp.async, so kRing rows per lane are in flight while the current one is reduced.
 template <typename KV>
 __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -633,32 +649,52 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     }
     auto key_of = [&](int r) { return exact ? (r < t_a ? r : t_b + (r - t_a)) : lidx[r]; };
 
-    // ---- rows: half-warp hw takes entries hw, hw + 8, ... (the warp stays converged)
+    // ---- rows: half-warp hw takes entries hw, hw + 8, ...; each lane streams its own 16-byte
+    //      pieces of the rows through a private cp.async ring of kRing slots in shared memory
     float m = -INFINITY, l = 0.0f, o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = 0.0f;
-    const KV* Kb = reinterpret_cast<const KV*>(a.keys) + static_cast<size_t>(bg) * a.ncap * kD + 8 * hl;
-    const KV* Vb = reinterpret_cast<const KV*>(a.values) + static_cast<size_t>(bg) * a.ncap * kD + 8 * hl;
-    constexpr int kStride = 2 * kAWarps;
+    constexpr int kPieces = static_cast<int>(sizeof(KV)) / 2;     // 16-byte pieces per fragment
+    const uint8_t* Kb = reinterpret_cast<const uint8_t*>(a.keys) +
+                        (static_cast<size_t>(bg) * a.ncap * kD + 8 * hl) * sizeof(KV);
+    const uint8_t* Vb = reinterpret_cast<const uint8_t*>(a.values) +
+                        (static_cast<size_t>(bg) * a.ncap * kD + 8 * hl) * sizeof(KV);
+    uint4* ring = reinterpret_cast<uint4*>(smem + a.work_bytes + kAWarps * kCombinePitch * 4 + 64);
     const bool weighted = !exact && a.K > 0;
-    RowFrag<KV> f0, f1, f2;
-    int r = 2 * warp + half;
-    if (r < nsel) {
-        const size_t key = static_cast<size_t>(key_of(r)) * kD;
-        f0.load(Kb + key, Vb + key);
-    }
-    if (r + kStride < nsel) {
-        const size_t key = static_cast<size_t>(key_of(r + kStride)) * kD;
-        f1.load(Kb + key, Vb + key);
-    }
-    for (int r0 = 2 * warp; r0 < nsel; r0 += kStride) {
-        const bool live = r < nsel;
-        if (r + 2 * kStride < nsel) {
-            const size_t key = static_cast<size_t>(key_of(r + 2 * kStride)) * kD;
-            f2.load(Kb + key, Vb + key);
+    const int hw = 2 * warp + half;
+    auto issue = [&](int k) {                    // entry hw + 8 k into slot k % kRing
+        const int r = hw + 2 * kAWarps * k;
+        if (r < nsel) {
+            const size_t off = static_cast<size_t>(key_of(r)) * kD * sizeof(KV);
+            const int slot = k % kRing;
+#pragma unroll
+            for (int c = 0; c < kPieces; ++c) {
+                cp_async16(ring + ((slot * 2 + 0) * kPieces + c) * kAThreads + tid, Kb + off + 16 * c);
+                cp_async16(ring + ((slot * 2 + 1) * kPieces + c) * kAThreads + tid, Vb + off + 16 * c);
+            }
+        }
+        cp_async_commit();
+    };
+    const int nk = (nsel - 2 * warp + 2 * kAWarps - 1) / (2 * kAWarps);   // the warp's iterations
+#pragma unroll
+    for (int k = 0; k < kRing; ++k) issue(k);
+    for (int k = 0; k < nk; ++k) {
+        cp_async_wait_pending<kRing - 1>();
+        const bool live = hw + 2 * kAWarps * k < nsel;
+        const int slot = k % kRing;
+        RowFrag<KV> f;
+        {
+            uint4 kv[2 * kPieces];
+#pragma unroll
+            for (int c = 0; c < kPieces; ++c) {
+                kv[c] = ring[((slot * 2 + 0) * kPieces + c) * kAThreads + tid];
+                kv[kPieces + c] = ring[((slot * 2 + 1) * kPieces + c) * kAThreads + tid];
+            }
+            f.from_pieces(kv);
         }
         float kf[8], vf[8];
-        f0.unpack(kf, vf);
+        f.unpack(kf, vf);
+        issue(k + kRing);                        // the slot's pieces are in registers now
         float kb2 = 0.0f, dot = 0.0f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -678,7 +714,6 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
                 float cs = den > 0.0f ? __fdividef(dot - qmu, den) : 0.0f;
                 cs = fminf(1.0f, fmaxf(-1.0f, cs));
                 if (a.table_only || (cs > -0.9f && cs < 0.999f)) {
-                    // linear interpolation in the per-call table of log u over the cosine
                     const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
                     const int i = min(static_cast<int>(tt), kLuIntervals - 1);
                     const float g0 = __ldg(a.logu_tab + i), g1 = __ldg(a.logu_tab + i + 1);
@@ -696,10 +731,8 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
             for (int i = 0; i < 8; ++i) o[i] = fmaf(o[i], corr, pw * vf[i]);
             m = mn;
         }
-        f0 = f1;
-        f1 = f2;
-        r += kStride;
     }
+    cp_async_wait_pending<0>();
 
     // ---- merge the two half-warps, then the warps (fixed order)
     {
@@ -834,7 +867,9 @@ size_t collide_smem_for(int G, int cpad, int K) {
     }
 }
 
-size_t attend_smem_for(int nblk) { return attend_smem(attend_partials(nblk)).total; }
+size_t attend_smem_for(int nblk, bool kv_bf16) {
+    return attend_smem(attend_partials(nblk), kv_bf16 ? 2 : 4).total;
+}
 
 constexpr size_t kMaxSmem = 232448;   // 227 KB opt-in per CTA
 
@@ -844,8 +879,8 @@ constexpr size_t kMaxSmem = 232448;   // 227 KB opt-in per CTA
 bool decode_supported(const DecodeShape& s, bool kv_bf16) {
     const int G = s.Hq / s.Hkv;
     if (!pick_collide(G)) return false;
-    (void)kv_bf16;
-    return collide_smem_for(G, s.cpad, s.K) <= kMaxSmem && attend_smem_for(s.nblk) <= kMaxSmem;
+    return collide_smem_for(G, s.cpad, s.K) <= kMaxSmem &&
+           attend_smem_for(s.nblk, kv_bf16) <= kMaxSmem;
 }
 
 cudaError_t prepare_decode() {
@@ -930,7 +965,7 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     ca.scale = s.scale;
     KernelFn scan = pick_collide(G);
     const size_t smem_scan = collide_smem_for(G, s.cpad, s.K);
-    if (!scan || smem_scan > kMaxSmem || attend_smem_for(s.nblk) > kMaxSmem)
+    if (!scan || smem_scan > kMaxSmem || attend_smem_for(s.nblk, kv_bf16) > kMaxSmem)
         return cudaErrorNotSupported;
     if (blk0 < 0 || blk0 > s.nblk) return cudaErrorInvalidValue;
     if (blk0 < s.nblk) {
@@ -946,7 +981,7 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
                           const DecodeScratch& ws, cudaStream_t st) {
     const int G = s.Hq / s.Hkv;
     AttendFn attend = pick_attend(kv_bf16);
-    const size_t smem_att = attend_smem_for(s.nblk);
+    const size_t smem_att = attend_smem_for(s.nblk, kv_bf16);
     if (smem_att > kMaxSmem) return cudaErrorNotSupported;
     AArgs aa;
     aa.selmask = ws.selmask;
@@ -978,7 +1013,7 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
     aa.scale = s.scale;
     aa.log_c2 = s.L >= 2 ? logf(0.5f * static_cast<float>(s.L) * static_cast<float>(s.L - 1)) : 0.0f;
     {
-        const AttendSmem m = attend_smem(attend_partials(s.nblk));
+        const AttendSmem m = attend_smem(attend_partials(s.nblk), kv_bf16 ? 2 : 4);
         aa.merge_cap = m.merge_cap;
         aa.work_bytes = static_cast<int>(m.work);
     }
