@@ -367,17 +367,20 @@ size_t cp_codes_bytes(int B, int Hkv, int n, int L) {
     return static_cast<size_t>(B) * Hkv * nblk * L * kKeysPerBlock;
 }
 
-cudaError_t launch_cp_logu_table(int K, int L, float* table, cudaStream_t st) {
-    static double x[2][kGlMax], w[2][kGlMax];
-    static bool ready = false;
-    if (!ready) {                                 // computed once; identical on every call
+struct GaussLegendreSets {
+    double x[2][kGlMax], w[2][kGlMax];
+    GaussLegendreSets() {
         gauss_legendre(96, x[0], w[0]);
         gauss_legendre(192, x[1], w[1]);
-        ready = true;
     }
-    cudaError_t e = cudaMemcpyToSymbolAsync(g_gl_x, x, sizeof(x), 0, cudaMemcpyHostToDevice, st);
+};
+
+cudaError_t launch_cp_logu_table(int K, int L, float* table, cudaStream_t st) {
+    static const GaussLegendreSets gl;            // built once, thread-safe (a function static)
+    cudaError_t e = cudaMemcpyToSymbolAsync(g_gl_x, gl.x, sizeof(gl.x), 0, cudaMemcpyHostToDevice,
+                                            st);
     if (e != cudaSuccess) return e;
-    e = cudaMemcpyToSymbolAsync(g_gl_w, w, sizeof(w), 0, cudaMemcpyHostToDevice, st);
+    e = cudaMemcpyToSymbolAsync(g_gl_w, gl.w, sizeof(gl.w), 0, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return e;
     cp_logu_table_kernel<<<kLogUTableIntervals + 1, kCpTableThreads, 0, st>>>(K, L, table);
     return cudaGetLastError();
