@@ -397,10 +397,10 @@ mp_status mp_decode_attention(const void* q, mp_dtype q_dtype, const uint32_t* c
     if (!ensure_prepared()) return MP_ERR_CUDA;
     const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
     cudaError_t e = query_encode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
-                                   stream);
+                                 stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
     return to_status(scan_and_attend(q, q_dtype == MP_BF16, codes, centre, keys, values,
-                                    kv_dtype == MP_BF16, s, out, ws, stream));
+                                     kv_dtype == MP_BF16, s, out, ws, stream));
 }
 
 mp_status mp_encode_query(const void* q, mp_dtype q_dtype, const float* centre, const void* W,
@@ -419,7 +419,7 @@ mp_status mp_encode_query(const void* q, mp_dtype q_dtype, const float* centre, 
     if (!ensure_prepared()) return MP_ERR_CUDA;
     const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
     return to_status(query_encode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
-                                    stream));
+                                  stream));
 }
 
 mp_status mp_sampled_attention(const void* q, mp_dtype q_dtype, const uint32_t* codes,
@@ -436,7 +436,7 @@ mp_status mp_sampled_attention(const void* q, mp_dtype q_dtype, const uint32_t* 
     if (!ensure_prepared()) return MP_ERR_CUDA;
     const DecodeScratch ws = carve_decode_scratch(workspace, s, false);
     return to_status(scan_and_attend(q, q_dtype == MP_BF16, codes, centre, keys, values,
-                                    kv_dtype == MP_BF16, s, out, ws, stream));
+                                     kv_dtype == MP_BF16, s, out, ws, stream));
 }
 
 size_t mp_buckets_bytes(int B, int Hkv, int n, int K, int L) {
@@ -483,8 +483,8 @@ mp_status mp_sampled_attention_buckets(const void* q, mp_dtype q_dtype, const ui
     if (e != cudaSuccess) return MP_ERR_CUDA;
     if (tail)
         return to_status(scan_and_attend(q, q_dtype == MP_BF16, codes, centre, keys, values,
-                                        kv_dtype == MP_BF16, s, out, ws, stream,
-                                        s.n_indexed / kKeysPerBlock));
+                                         kv_dtype == MP_BF16, s, out, ws, stream,
+                                         s.n_indexed / kKeysPerBlock));
     return to_status(launch_attend(q, q_dtype == MP_BF16, centre, keys, values,
                                    kv_dtype == MP_BF16, s, out, ws, stream));
 }
@@ -506,10 +506,10 @@ mp_status mp_debug_select(const void* q, mp_dtype q_dtype, const uint32_t* codes
     DecodeScratch ws = carve_decode_scratch(workspace, s, true);
     if (s.qwords > 0) ws.qbits = q_bits;
     cudaError_t e = query_encode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
-                                   stream);
+                                 stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
     e = scan_and_attend(q, q_dtype == MP_BF16, codes, centre, keys, values, kv_dtype == MP_BF16, s,
-                       out, ws, stream);
+                        out, ws, stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
     e = launch_compact_selection(ws.selmask, s.B * s.Hq, s.n, s.nblk, sel_idx, sel_count, stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
