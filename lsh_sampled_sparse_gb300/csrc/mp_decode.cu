@@ -1,7 +1,7 @@
-// Decode step: query encoding, then one fused kernel that streams the packed codes of a block
-// of 1024 keys, selects the keys colliding with the query in >= 2 tables, gathers only those
-// K/V rows, and folds them with importance weights into a partial softmax; the last block of
-// each KV head merges the partials by log-sum-exp.
+// Decode step: query encoding; a scan kernel that streams the packed codes of a block of 1024
+// keys and selects the keys colliding with the query in >= 2 tables; an attend kernel that
+// gathers only those K/V rows and folds them with importance weights into partial softmaxes,
+// the last CTA of each query row merging the partials by log-sum-exp.
 //
 // The method is Algorithm 1 of "MagicPIG: LSH Sampling for Efficient LLM Generation" (method
 // details, algorithm execution), with the inclusion probability of the hash-function-choice
@@ -170,26 +170,16 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// Fused collide -> select -> gather -> attend, one CTA per (1024-key block, sequence x KV head)
+// Collide -> select, one CTA per (1024-key block, sequence x KV head); the gather + attend +
+// merge kernel follows as a programmatic dependent
 // ------------------------------------------------------------------------------------------------
 struct CArgs {
     const uint32_t* codes;
     const uint32_t* qmask;
-    const float4* qstat;
-    const void* q;
-    const float* centre;
-    const void* keys;
-    const void* values;
-    float* pm;
-    float* pl;
-    float* po;
-    unsigned* counters;
-    float* out;
     uint32_t* selmask;
-    int q_bf16, n, nblk, Hq, Hkv, K, L, C, cpad, n_sink, n_local;
+    int n, nblk, Hq, Hkv, K, L, C, cpad, n_sink, n_local;
     int cblk;                                    // code blocks per head in memory
     int blk0;                                    // first block scanned (grid x + blk0)
-    float scale;
 };
 
 template <typename KV>
@@ -237,6 +227,18 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
                      static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
                  "l"(src)
                  : "memory");
+}
+// The same copy with an L2 eviction-priority policy (from l2_evict_first) for data read once
+__device__ __forceinline__ void cp_async16_hint(void* dst, const void* src, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    return policy;
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
@@ -317,11 +319,13 @@ __device__ __forceinline__ void scan_tables_async(const uint32_t* cb, uint32_t* 
                                                   uint32_t (&ge1)[G], uint32_t (&ge2)[G]) {
     constexpr int kSlot = K * kWordsPerBlock;      // words per table
     constexpr int kPieces = K * 8;                 // 16-byte pieces per table
+    const uint64_t policy = l2_evict_first();      // the codes are read once per decode step
     auto issue = [&](int t, int slot) {
         const uint32_t* src = cb + static_cast<size_t>(t) * kSlot;
         uint32_t* dst = ring + slot * kSlot;
 #pragma unroll
-        for (int pc = lane; pc < kPieces; pc += 32) cp_async16(dst + 4 * pc, src + 4 * pc);
+        for (int pc = lane; pc < kPieces; pc += 32)
+            cp_async16_hint(dst + 4 * pc, src + 4 * pc, policy);
     };
 #pragma unroll
     for (int d = 0; d < kRingDepth - 1; ++d) {
@@ -938,18 +942,7 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     CArgs ca;
     ca.codes = codes;
     ca.qmask = ws.qmask;
-    ca.qstat = ws.qstat;
-    ca.q = q;
-    ca.centre = centre;
-    ca.keys = keys;
-    ca.values = values;
-    ca.pm = ws.pm;
-    ca.pl = ws.pl;
-    ca.po = ws.po;
-    ca.counters = ws.counters;
-    ca.out = out;
     ca.selmask = ws.selmask;
-    ca.q_bf16 = q_bf16;
     ca.n = s.n;
     ca.nblk = s.nblk;
     ca.Hq = s.Hq;
@@ -962,7 +955,6 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     ca.n_local = s.n_local;
     ca.cblk = s.cblk;
     ca.blk0 = blk0;
-    ca.scale = s.scale;
     KernelFn scan = pick_collide(G);
     const size_t smem_scan = collide_smem_for(G, s.cpad, s.K);
     if (!scan || smem_scan > kMaxSmem || attend_smem_for(s.nblk, kv_bf16) > kMaxSmem)
