@@ -154,10 +154,21 @@ __global__ void __launch_bounds__(kBuildThreads)
 // warp_transpose32 of U independent words, interleaved so that their shuffles overlap
 template <int U>
 __device__ __forceinline__ void warp_transpose32_x(uint32_t (&x)[U], int lane) {
-    const uint32_t low[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
 #pragma unroll
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < 2; ++i) {                // s = 16, 8: whole bytes, one byte permute
         const int s = 16 >> i;
+        const bool up = (lane & s) != 0;
+        const uint32_t sel = i == 0 ? (up ? 0x3276u : 0x5410u) : (up ? 0x3715u : 0x6240u);
+        uint32_t y[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) y[u] = __shfl_xor_sync(0xffffffffu, x[u], s);
+#pragma unroll
+        for (int u = 0; u < U; ++u) x[u] = __byte_perm(x[u], y[u], sel);
+    }
+    const uint32_t low[3] = {0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const int s = 4 >> i;
         const bool up = (lane & s) != 0;
         const uint32_t keep = up ? ~low[i] : low[i];
         uint32_t y[U];

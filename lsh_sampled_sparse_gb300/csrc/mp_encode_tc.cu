@@ -18,8 +18,8 @@
 //   warp 0   TMA producer: 128-key x 128-dim bf16 tiles, 128-byte swizzle, 3-stage ring
 //   warp 1   TMEM allocator and single-thread MMA issuer: M=128, N<=256, K=16 x (1 + 8) per
 //            tile, double-buffered fp32 accumulators (2 x 256 TMEM columns)
-//   warps 2-17 epilogue: tcgen05.ld the accumulator; per key (lane) shift its sign bits into
-//            a 32-bit word for 32 hyperplanes (funnel shift, no predicates), transpose the
+//   warps 2-17 epilogue: tcgen05.ld the accumulator; per key (lane) gather its sign bits into
+//            a 32-bit word for 32 hyperplanes (funnel shifts and FP32 sums), transpose the
 //            32x32 bit block across the warp with 5 shuffle stages so that each lane holds one
 //            hyperplane's 32-key word, stage a block's words in shared memory, then write each
 //            plane row (128 bytes) of the block with coalesced stores. When the head changes
@@ -195,16 +195,42 @@ __device__ __forceinline__ void tmem_ld_wait() {
 __device__ __forceinline__ void epi_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
 }
-// Bit c of the result = the sign bit of accumulator column c (c_c - w_c . k, so the bit is
-// [w_c . k > c_c]) for c in 0..31, shifted in by funnel shifts in four independent chains.
+// 1.0 if the fp32 accumulator (as bits) is negative, else 0.0: -2^126 x, saturated to [0, 1]
+// (denormals flush to zero), on the FP32 pipe
+__device__ __forceinline__ float neg_as_one(uint32_t v) {
+    float r;
+    asm("mul.rn.ftz.sat.f32 %0, %1, 0fFE800000;" : "=f"(r) : "f"(__uint_as_float(v)));
+    return r;
+}
+// Bit c of the result = [accumulator column c < 0] (c_c - w_c . k, so the bit is
+// [w_c . k > c_c]) for c in 0..31, one byte per chain of 8 columns. Funnel shifts move the sign
+// bits in; they run on the integer pipe at half rate. kFpBytes of the bytes (from byte 0) are
+// summed on the FP32 pipe instead, as 2^23 + sum_c 2^c [acc_c < 0], whose low mantissa bits are
+// the byte (exact: small integers). For the SimHash epilogue, which has no other
+// FP32 work, one FP byte of four balanced the two pipes best (0, 1, 2 and 3 measured); the MIPS
+// epilogue already spends the FP32 pipe on its per-element FMA and takes none. The two forms
+// differ only for an accumulator of -0 or a negative denormal, i.e. an exact or sub-2^-126 tie,
+// where either bit lies within the near-tie band.
+template <int kFpBytes>
 __device__ __forceinline__ uint32_t pack_signs(const uint32_t (&v)[32]) {
-    uint32_t x[4] = {0u, 0u, 0u, 0u};
+    uint32_t x[4];
 #pragma unroll
-    for (int c = 7; c >= 0; --c) {
+    for (int k = 0; k < 4; ++k) {
+        if (k < kFpBytes) {
+            // pairs, quads, then the byte (a tree: four dependent steps instead of eight)
+            float p[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) x[k] = __funnelshift_l(v[8 * k + c], x[k], 1);
+            for (int c = 0; c < 4; ++c)
+                p[c] = fmaf(neg_as_one(v[8 * k + 2 * c + 1]), 2.0f, neg_as_one(v[8 * k + 2 * c]));
+            const float q0 = fmaf(p[1], 4.0f, p[0]), q1 = fmaf(p[3], 4.0f, p[2]);
+            x[k] = __float_as_uint(fmaf(q1, 16.0f, q0) + 8388608.0f);   // + 2^23
+        } else {
+            x[k] = 0u;
+#pragma unroll
+            for (int c = 7; c >= 0; --c) x[k] = __funnelshift_l(v[8 * k + c], x[k], 1);
+        }
     }
-    return x[0] | (x[1] << 8) | (x[2] << 16) | (x[3] << 24);
+    return __byte_perm(__byte_perm(x[0], x[1], 0x0040), __byte_perm(x[2], x[3], 0x0040), 0x5410);
 }
 // kMode: kSign, the SimHash codes; kMips, the MIPS -> cosine variant, whose keys carry an extra
 // coordinate a_i = sqrt(max(0, r^2 - |k_i - mu|^2)) on a (d + 1)-th row of W: the epilogue
@@ -530,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     code64 = cd;
                                 }
                             } else {
-                                x[g] = pack_signs(v);
+                                x[g] = pack_signs<kMode == kSign ? 1 : 0>(v);
                             }
                         }
                     }

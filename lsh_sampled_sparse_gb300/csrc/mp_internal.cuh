@@ -182,13 +182,22 @@ __device__ __forceinline__ float load_elem(const void* p, bool bf16, size_t i) {
 // bit r of lane b is that element. Each stage swaps the off-diagonal s x s blocks.
 // Lanes without bit s of their index keep the positions b with (b & s) == 0 and take the
 // partner's such bits moved up by s; lanes with bit s keep the others and take the partner's
-// moved down by s. A rotation does both moves (the bits it wraps around are masked off), so a
-// stage is one shuffle, one funnel shift and one three-input logic op.
+// moved down by s. For s = 16 and 8 the blocks are whole bytes and one byte permute of the lane's
+// and the partner's word does both; for s = 4, 2, 1 a rotation does both moves (the bits it
+// wraps around are masked off) and a three-input logic op merges. Every stage has one shuffle.
 __device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
-    const uint32_t low[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+    {
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 16);
+        x = __byte_perm(x, y, (lane & 16) ? 0x3276 : 0x5410);   // [y2 y3 x2 x3] / [x0 x1 y0 y1]
+    }
+    {
+        const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 8);
+        x = __byte_perm(x, y, (lane & 8) ? 0x3715 : 0x6240);    // [y1 x1 y3 x3] / [x0 y0 x2 y2]
+    }
+    const uint32_t low[3] = {0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
 #pragma unroll
-    for (int i = 0; i < 5; ++i) {
-        const int s = 16 >> i;
+    for (int i = 0; i < 3; ++i) {
+        const int s = 4 >> i;
         const bool up = (lane & s) != 0;
         const uint32_t keep = up ? ~low[i] : low[i];
         const uint32_t y = __shfl_xor_sync(0xffffffffu, x, s);
