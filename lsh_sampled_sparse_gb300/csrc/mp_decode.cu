@@ -794,8 +794,8 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     if (!misc[4]) return;
 
     // ---- merge: the partial outputs are staged in shared memory (the row list's space) with
-    //      cp.async, issued before the maximum is known; m of every partial is loaded meanwhile
-    //      and sc[j] = exp(m_j - M) kept in cbuf. Rounds of kMergeCap partials.
+    //      cp.async, issued before the maximum is known; m and l of the partials are loaded
+    //      meanwhile and sc[j] = exp(m_j - M) kept in cbuf. Rounds of kMergeCap partials.
     const int kMergeCap = a.merge_cap;
     float* stage = reinterpret_cast<float*>(smem);
     float* red = cbuf;                            // [0, 8): reductions
@@ -808,8 +808,14 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
         cp_async_commit();
     };
     stage_round(0);
-    float mx = -INFINITY;
-    for (int j = tid; j < nsp; j += kAThreads) mx = fmaxf(mx, __ldcg(a.pm + rb + j));
+    // thread j < nsp keeps (m_j, l_j) of the first round from this one round trip
+    float pm0 = -INFINITY, pl0 = 0.0f;
+    if (tid < nsp) {
+        pm0 = __ldcg(a.pm + rb + tid);
+        pl0 = __ldcg(a.pl + rb + tid);
+    }
+    float mx = pm0;
+    for (int j = tid + kAThreads; j < nsp; j += kAThreads) mx = fmaxf(mx, __ldcg(a.pm + rb + j));
 #pragma unroll
     for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) red[warp] = mx;
@@ -821,9 +827,11 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     for (int j0 = 0; j0 < nsp; j0 += kMergeCap) {
         const int cnt = min(kMergeCap, nsp - j0);
         if (tid < cnt) {
-            const float sj = M == -INFINITY ? 0.0f : expf(__ldcg(a.pm + rb + j0 + tid) - M);
+            const float pmj = j0 == 0 ? pm0 : __ldcg(a.pm + rb + j0 + tid);
+            const float plj = j0 == 0 ? pl0 : __ldcg(a.pl + rb + j0 + tid);
+            const float sj = M == -INFINITY ? 0.0f : expf(pmj - M);
             sc[tid] = sj;
-            ls = fmaf(sj, __ldcg(a.pl + rb + j0 + tid), ls);
+            ls = fmaf(sj, plj, ls);
         }
         cp_async_wait_pending<0>();
         __syncthreads();                         // staged rows and scales visible to all
