@@ -10,7 +10,8 @@
 //
 // Build, one kernel: a cluster of R CTAs per (table, sequence x KV head), each CTA one key range
 // (R = 1, 2, 4 or 8, so that a range holds about 12 blocks: short contexts take fewer, longer
-// ranges and pay the per-range histogram work fewer times). A CTA stages its range's plane rows, counts its codes in a shared-memory
+// ranges and pay the per-range histogram work fewer times). A CTA stages its range's plane rows,
+// decodes the codes of floor(32 / K) 32-key words per warp bit transpose, counts them in a shared-memory
 // histogram (the count's old value is the key's rank among the range's keys of that code), reads
 // the other ranges' histograms through distributed shared memory to get the table's offsets and
 // its own write base per code, sorts its keys by code in shared memory and writes them out in
@@ -36,7 +37,7 @@ constexpr size_t kClusterBuildSmem = 200 * 1024;   // dynamic shared memory of a
 constexpr int kClusterThreads = 512;  // threads of a cluster-build CTA
 constexpr int kMaxClusterRanges = 8;  // CTAs (key ranges) of a cluster-build table, at most
 constexpr int kClusterRangeBlocks = 12;   // blocks a cluster-build range aims at
-constexpr int kWordsAtOnce = 4;       // 32-key words a cluster-build warp decodes together
+constexpr int kWordsAtOnce = 2;       // bit transposes a cluster-build warp runs together
 constexpr int kStageRow = kWordsPerBlock + 1;   // staged plane row stride (words): lanes reading
                                                 // word w of planes 0..K-1 hit distinct banks
 
@@ -182,16 +183,20 @@ __device__ __forceinline__ void warp_transpose32_x(uint32_t (&x)[U], int lane) {
     }
 }
 
-// Codes of the staged 32-key words w0 .. w0 + U - 1 (lane j gets key j's code of each word;
-// words at or past nw give 0). Plane rows are kStageRow words apart, blocks srow words apart.
+// Codes of staged 32-key words, P = floor(32 / K) words per transposed 32x32 bit block: lane
+// l < P K loads plane l % K of word w + l / K, so after the transpose bits [q K, q K + K) of
+// lane j are the code of key j of word w + q. Transposes u = 0 .. U-1 take words
+// w0 + u P .. w0 + u P + P - 1 (words at or past nw give 0). Plane rows are kStageRow words
+// apart, blocks srow words apart.
 template <int U>
-__device__ __forceinline__ void staged_codes(const uint32_t* stage, int w0, int nw, int K,
+__device__ __forceinline__ void staged_codes(const uint32_t* stage, int w0, int nw, int K, int P,
                                              int srow, int lane, uint32_t (&x)[U]) {
+    const int dw = lane / K, pl = lane - dw * K;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const int wi = w0 + u;
-        x[u] = (lane < K && wi < nw)
-                   ? stage[(wi / kWordsPerBlock) * srow + lane * kStageRow + wi % kWordsPerBlock]
+        const int wi = w0 + u * P + dw;
+        x[u] = (dw < P && wi < nw)
+                   ? stage[(wi / kWordsPerBlock) * srow + pl * kStageRow + wi % kWordsPerBlock]
                    : 0u;
     }
     warp_transpose32_x<U>(x, lane);
@@ -235,8 +240,8 @@ __host__ __device__ __forceinline__ size_t cluster_build_smem(int rb, int K) {
 }
 
 // One CTA per key range, a cluster of R CTAs per table (grid x = R; the cluster size is set at
-// launch). Each warp takes kWordsAtOnce 32-key words at a time so that their shuffles and shared
-// atomics overlap.
+// launch). Each warp runs kWordsAtOnce bit transposes at a time (each decoding floor(32 / K)
+// words) so that their shuffles and shared atomics overlap.
 template <int R>
 __global__ void __launch_bounds__(kClusterThreads)
     bucket_build_cluster_kernel(const uint32_t* codes, int n, int K, int L, int nblk, int cblk,
@@ -275,17 +280,24 @@ __global__ void __launch_bounds__(kClusterThreads)
         }
     }
     __syncthreads();
-    // pass 1: count; the count before the key's own is its rank within (range, code)
-    for (int w0 = warp * U; w0 < nw; w0 += (T / 32) * U) {
-        uint32_t c[U], rk[U];
-        staged_codes<U>(stage, w0, nw, K, srow, lane, c);
+    // pass 1: count; the count before the key's own is its rank within (range, code). One
+    // transpose decodes P = floor(32 / K) words (three at K = 10).
+    if (K == 0) {
+        for (int i = tid; i < m; i += T) crank[i] = atomicAdd(&hist[0], 1u);
+    } else {
+        const int P = 32 / K;
+        const uint32_t cmask = (1u << K) - 1u;
+        for (int w0 = warp * U * P; w0 < nw; w0 += (T / 32) * U * P) {
+            uint32_t x[U];
+            staged_codes<U>(stage, w0, nw, K, P, srow, lane, x);
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            rk[u] = (w0 + u) * 32 + lane < m ? atomicAdd(&hist[c[u]], 1u) : 0u;
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = (w0 + u) * 32 + lane;
-            if (i < m) crank[i] = (c[u] << 16) | rk[u];
+            for (int u = 0; u < U; ++u) {
+                for (int q = 0; q < P; ++q) {
+                    const int i = (w0 + u * P + q) * 32 + lane;
+                    const uint32_t c = (x[u] >> (q * K)) & cmask;
+                    if (i < m) crank[i] = (c << 16) | atomicAdd(&hist[c], 1u);
+                }
+            }
         }
     }
     cluster.sync();                        // every range's histogram is complete
