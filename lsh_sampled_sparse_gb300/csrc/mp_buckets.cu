@@ -11,7 +11,7 @@
 // Build, one kernel: a cluster of R CTAs per (table, sequence x KV head), each CTA one key range
 // (R = 1, 2, 4 or 8, so that a range holds about 12 blocks: short contexts take fewer, longer
 // ranges and pay the per-range histogram work fewer times). A CTA stages its range's plane rows,
-// decodes the codes of floor(32 / K) 32-key words per warp bit transpose, counts them in a shared-memory
+// decodes the codes of min(4, floor(32 / K)) 32-key words per warp bit transpose, counts them in a shared-memory
 // histogram (the count's old value is the key's rank among the range's keys of that code), reads
 // the other ranges' histograms through distributed shared memory to get the table's offsets and
 // its own write base per code, sorts its keys by code in shared memory and writes them out in
@@ -183,13 +183,13 @@ __device__ __forceinline__ void warp_transpose32_x(uint32_t (&x)[U], int lane) {
     }
 }
 
-// Codes of staged 32-key words, P = floor(32 / K) words per transposed 32x32 bit block: lane
+// Codes of staged 32-key words, P words per transposed 32x32 bit block (P K <= 32): lane
 // l < P K loads plane l % K of word w + l / K, so after the transpose bits [q K, q K + K) of
 // lane j are the code of key j of word w + q. Transposes u = 0 .. U-1 take words
 // w0 + u P .. w0 + u P + P - 1 (words at or past nw give 0). Plane rows are kStageRow words
 // apart, blocks srow words apart.
-template <int U>
-__device__ __forceinline__ void staged_codes(const uint32_t* stage, int w0, int nw, int K, int P,
+template <int U, int P>
+__device__ __forceinline__ void staged_codes(const uint32_t* stage, int w0, int nw, int K,
                                              int srow, int lane, uint32_t (&x)[U]) {
     const int dw = lane / K, pl = lane - dw * K;
 #pragma unroll
@@ -200,6 +200,37 @@ __device__ __forceinline__ void staged_codes(const uint32_t* stage, int w0, int 
                    : 0u;
     }
     warp_transpose32_x<U>(x, lane);
+}
+
+// Pass 1 of the cluster build for P words per transpose: every key's code, and its rank among
+// the range's keys of that code (the histogram count before its own), as (code << 16) | rank.
+// The U P atomics of a round are issued back to back.
+template <int U, int P, int T>
+__device__ __forceinline__ void count_codes(const uint32_t* stage, int nw, int m, int K, int srow,
+                                            uint32_t* hist, uint32_t* crank) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t cmask = (1u << K) - 1u;
+    for (int w0 = warp * U * P; w0 < nw; w0 += (T / 32) * U * P) {
+        uint32_t x[U];
+        staged_codes<U, P>(stage, w0, nw, K, srow, lane, x);
+        uint32_t c[U][P], rk[U][P];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                c[u][q] = (x[u] >> (q * K)) & cmask;
+                rk[u][q] = (w0 + u * P + q) * 32 + lane < m ? atomicAdd(&hist[c[u][q]], 1u) : 0u;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+            for (int q = 0; q < P; ++q) {
+                const int i = (w0 + u * P + q) * 32 + lane;
+                if (i < m) crank[i] = (c[u][q] << 16) | rk[u][q];
+            }
+        }
+    }
 }
 
 // In-place exclusive prefix sum of v[0, nb) by the whole CTA of T threads; wsum holds T / 32
@@ -240,8 +271,8 @@ __host__ __device__ __forceinline__ size_t cluster_build_smem(int rb, int K) {
 }
 
 // One CTA per key range, a cluster of R CTAs per table (grid x = R; the cluster size is set at
-// launch). Each warp runs kWordsAtOnce bit transposes at a time (each decoding floor(32 / K)
-// words) so that their shuffles and shared atomics overlap.
+// launch). Each warp runs kWordsAtOnce bit transposes at a time (each decoding
+// min(4, floor(32 / K)) words) so that their shuffles and shared atomics overlap.
 template <int R>
 __global__ void __launch_bounds__(kClusterThreads)
     bucket_build_cluster_kernel(const uint32_t* codes, int n, int K, int L, int nblk, int cblk,
@@ -281,24 +312,17 @@ __global__ void __launch_bounds__(kClusterThreads)
     }
     __syncthreads();
     // pass 1: count; the count before the key's own is its rank within (range, code). One
-    // transpose decodes P = floor(32 / K) words (three at K = 10).
+    // transpose decodes min(4, floor(32 / K)) words (three at K = 10).
     if (K == 0) {
         for (int i = tid; i < m; i += T) crank[i] = atomicAdd(&hist[0], 1u);
+    } else if (K <= 8) {
+        count_codes<U, 4, T>(stage, nw, m, K, srow, hist, crank);
+    } else if (K <= 10) {
+        count_codes<U, 3, T>(stage, nw, m, K, srow, hist, crank);
+    } else if (K <= 16) {
+        count_codes<U, 2, T>(stage, nw, m, K, srow, hist, crank);
     } else {
-        const int P = 32 / K;
-        const uint32_t cmask = (1u << K) - 1u;
-        for (int w0 = warp * U * P; w0 < nw; w0 += (T / 32) * U * P) {
-            uint32_t x[U];
-            staged_codes<U>(stage, w0, nw, K, P, srow, lane, x);
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                for (int q = 0; q < P; ++q) {
-                    const int i = (w0 + u * P + q) * 32 + lane;
-                    const uint32_t c = (x[u] >> (q * K)) & cmask;
-                    if (i < m) crank[i] = (c << 16) | atomicAdd(&hist[c], 1u);
-                }
-            }
-        }
+        count_codes<U, 1, T>(stage, nw, m, K, srow, hist, crank);
     }
     cluster.sync();                        // every range's histogram is complete
     for (int c = tid; c < nb; c += T) {
