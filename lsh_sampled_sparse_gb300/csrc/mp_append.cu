@@ -18,8 +18,8 @@ constexpr int kAppendPlanes = 32;                              // hyperplanes pe
 constexpr int kAppendKeysAtOnce = 4;                           // independent sums a lane carries
 
 // One CTA per (chunk of 32 hyperplanes, head). The chunk of W and the range's centred keys are
-// staged in shared memory, kStageBatch loads in flight per thread; warp w then takes the range's w-th
-// 32-key word, lane j hyperplane j0 + j, and rewrites that word's bits of the range only (each
+// staged in shared memory, kStageBatch loads in flight per thread; warp w then takes the range's
+// w-th 32-key word, lane j hyperplane j0 + j, and rewrites that word's bits of the range only (each
 // (plane, word) has one owner, so a plain read-modify-write). Each sum runs over e in order,
 // fmaf(W[e][j], k[e] - mu[e], acc): the arithmetic of the CUDA-core block encoder.
 __global__ void __launch_bounds__(kAppendThreads)

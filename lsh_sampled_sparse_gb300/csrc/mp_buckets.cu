@@ -11,14 +11,15 @@
 // Build, one kernel: a cluster of R CTAs per (table, sequence x KV head), each CTA one key range
 // (R = 1, 2, 4 or 8, so that a range holds about 12 blocks: short contexts take fewer, longer
 // ranges and pay the per-range histogram work fewer times). A CTA stages its range's plane rows,
-// decodes the codes of min(4, floor(32 / K)) 32-key words per warp bit transpose, counts them in a shared-memory
-// histogram (the count's old value is the key's rank among the range's keys of that code), reads
-// the other ranges' histograms through distributed shared memory to get the table's offsets and
-// its own write base per code, sorts its keys by code in shared memory and writes them out in
-// runs, so a bucket's part from one range is one contiguous store. Ranges too large for shared
-// memory (very long contexts) take three kernels instead: per-range counts to the scratch words,
-// one CTA per table scanning them into offsets and write bases, and a scatter with one shared
-// atomic per key; the scratch [kBucketRanges][2^K] per table after the members serves them.
+// decodes the codes of min(4, floor(32 / K)) 32-key words per warp bit transpose, counts them in
+// a shared-memory histogram (the count's old value is the key's rank among the range's keys of
+// that code), reads the other ranges' histograms through distributed shared memory to get the
+// table's offsets and its own write base per code, sorts its keys by code in shared memory and
+// writes them out in runs, so a bucket's part from one range is one contiguous store. Ranges too
+// large for shared memory (very long contexts) take three kernels instead: per-range counts to
+// the scratch words, one CTA per table scanning them into offsets and write bases, and a scatter
+// with one shared atomic per key; the scratch [kBucketRanges][2^K] per table after the members
+// serves them.
 // Lookup: one warp per (query row, table) reads the query's bucket and sets each key's bit in
 // two saturating bitmaps, ge1 (>= 1 table) and ge2 (>= 2 tables), stored in
 // the selection-word layout of the dense scan ([row][block][32 words]).
@@ -48,9 +49,9 @@ __host__ __device__ __forceinline__ size_t bucket_words(int n, int K, int L) {
 }
 
 // Walk the keys of key range `range` of table t: stage kStageBlocks blocks' plane rows at a
-// time (row stride kStageRow); then each warp takes 32-key words: lane p < K holds plane p's word, and one 32x32 bit
-// transpose leaves in lane j the K-bit code of the word's key j. f(key, code) is called by the
-// lane of every key (keys past n are skipped).
+// time (row stride kStageRow); then each warp takes 32-key words: lane p < K holds plane p's
+// word, and one 32x32 bit transpose leaves in lane j the K-bit code of the word's key j.
+// f(key, code) is called by the lane of every key (keys past n are skipped).
 template <typename F>
 __device__ __forceinline__ void for_range_keys(const uint32_t* codes, int bh, int t, int range,
                                               int n, int K, int L, int nblk, int cblk,
