@@ -312,30 +312,41 @@ __device__ __forceinline__ void cp_async_wait_pending() {
 // Phase 1 for a compile-time K with the plane rows streamed through a per-warp shared-memory
 // ring: table t + kRingDepth - 1 is copied (cp.async, 16 B per lane) while table t is reduced,
 // so each warp keeps kRingDepth tables (kRingDepth * K * 128 bytes) in flight without holding
-// them in registers. cb points at the block's first plane row (no lane offset).
+// them in registers. cb points at the block's first plane row (no lane offset). The codes are
+// read once per decode step: their copies carry the L2 evict-first policy.
+template <int K>
+__device__ __forceinline__ void ring_issue(const uint32_t* cb, uint32_t* ring, int t, int slot,
+                                           int lane, uint64_t policy) {
+    constexpr int kSlot = K * kWordsPerBlock;      // words per table
+    constexpr int kPieces = K * 8;                 // 16-byte pieces per table
+    const uint32_t* src = cb + static_cast<size_t>(t) * kSlot;
+    uint32_t* dst = ring + slot * kSlot;
+#pragma unroll
+    for (int pc = lane; pc < kPieces; pc += 32) cp_async16_hint(dst + 4 * pc, src + 4 * pc, policy);
+}
+// The ring's first kRingDepth - 1 tables, one commit group each. The codes are an input of the
+// call, not something the query encoding writes, so the scan issues these before it waits.
+template <int K>
+__device__ __forceinline__ void ring_fill(const uint32_t* cb, uint32_t* ring, int t0, int t1,
+                                          int lane) {
+    const uint64_t policy = l2_evict_first();
+#pragma unroll
+    for (int d = 0; d < kRingDepth - 1; ++d) {
+        if (t0 + d < t1) ring_issue<K>(cb, ring, t0 + d, d, lane, policy);
+        cp_async_commit();
+    }
+}
+// The ring after ring_fill (its groups may have been followed by other, completed ones).
 template <int G, int K>
 __device__ __forceinline__ void scan_tables_async(const uint32_t* cb, uint32_t* ring,
                                                   const uint32_t* qneg, int t0, int t1, int lane,
                                                   uint32_t (&ge1)[G], uint32_t (&ge2)[G]) {
-    constexpr int kSlot = K * kWordsPerBlock;      // words per table
-    constexpr int kPieces = K * 8;                 // 16-byte pieces per table
-    const uint64_t policy = l2_evict_first();      // the codes are read once per decode step
-    auto issue = [&](int t, int slot) {
-        const uint32_t* src = cb + static_cast<size_t>(t) * kSlot;
-        uint32_t* dst = ring + slot * kSlot;
-#pragma unroll
-        for (int pc = lane; pc < kPieces; pc += 32)
-            cp_async16_hint(dst + 4 * pc, src + 4 * pc, policy);
-    };
-#pragma unroll
-    for (int d = 0; d < kRingDepth - 1; ++d) {
-        if (t0 + d < t1) issue(t0 + d, d);
-        cp_async_commit();
-    }
+    constexpr int kSlot = K * kWordsPerBlock;
+    const uint64_t policy = l2_evict_first();
     int slot = 0;
     for (int t = t0; t < t1; ++t) {
         const int nt = t + kRingDepth - 1;
-        if (nt < t1) issue(nt, (slot + kRingDepth - 1) % kRingDepth);
+        if (nt < t1) ring_issue<K>(cb, ring, nt, (slot + kRingDepth - 1) % kRingDepth, lane, policy);
         cp_async_commit();
         cp_async_wait_pending<kRingDepth - 1>();   // this lane's pieces of table t have landed
         __syncwarp();                              // ... and every other lane's
@@ -435,16 +446,22 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
                      static_cast<size_t>(warp) * kRingDepth * a.K * kWordsPerBlock;
 
     // ---- before the query masks exist: let the attend kernel be scheduled (it waits for this
-    //      kernel's completion itself), and pull this warp's first tables of codes (an input of
-    //      the call) into L2
+    //      kernel's completion itself), and start this warp's first tables of codes (an input
+    //      of the call): into the ring for the ring's K, else into L2
     allow_dependents();
-    {
-        const int t0 = (a.L * warp) / kWarps;
-        const uint32_t* first = a.codes + (static_cast<size_t>(bg) * a.cblk + blk) * a.C * kWordsPerBlock +
-                                static_cast<size_t>(t0) * a.K * kWordsPerBlock;
-        const int rows = min(kRingDepth * a.K, ((a.L * (warp + 1)) / kWarps - t0) * a.K);
-        for (int r = lane; r < rows; r += 32)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(first + static_cast<size_t>(r) * kWordsPerBlock));
+    const int t0 = (a.L * warp) / kWarps, t1 = (a.L * (warp + 1)) / kWarps;
+    const uint32_t* cb0 = a.codes + (static_cast<size_t>(bg) * a.cblk + blk) * a.C * kWordsPerBlock;
+    switch (a.K) {
+        case 8: ring_fill<8>(cb0, ring, t0, t1, lane); break;
+        case 9: ring_fill<9>(cb0, ring, t0, t1, lane); break;
+        case 10: ring_fill<10>(cb0, ring, t0, t1, lane); break;
+        case 11: ring_fill<11>(cb0, ring, t0, t1, lane); break;
+        default: {
+            const uint32_t* first = cb0 + static_cast<size_t>(t0) * a.K * kWordsPerBlock;
+            const int rows = min(kRingDepth * a.K, (t1 - t0) * a.K);
+            for (int r = lane; r < rows; r += 32)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(first + static_cast<size_t>(r) * kWordsPerBlock));
+        }
     }
     wait_for_predecessor();
 
@@ -467,9 +484,6 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
         ge2[h] = 0u;
     }
     {
-        const int t0 = (a.L * warp) / kWarps, t1 = (a.L * (warp + 1)) / kWarps;
-        const uint32_t* cb0 = a.codes +
-                              (static_cast<size_t>(bg) * a.cblk + blk) * a.C * kWordsPerBlock;
         const uint32_t* cb = cb0 + lane;
         switch (a.K) {
             case 0:

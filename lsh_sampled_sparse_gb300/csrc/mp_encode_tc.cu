@@ -483,8 +483,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t* dst = a.codes + (static_cast<size_t>(bg) * a.cblk + a.blk0 + blk) *
                                                   static_cast<size_t>(a.C) * kWordsPerBlock +
                                     static_cast<size_t>(j0) * kWordsPerBlock;
-                    for (int r = ew; r < Nc; r += kEpiWarps)
-                        dst[r * kWordsPerBlock + lane] = stg[lane * kStgPitch + r];
+                    // four rows per warp instruction: lane l takes words 4 (l % 8) .. + 3 of
+                    // row r0 + l / 8 (bank (w + r) mod 32: distinct across the warp)
+                    const int rl = lane >> 3, c4 = (lane & 7) * 4;
+                    for (int r0 = 4 * ew; r0 < Nc; r0 += 4 * kEpiWarps) {
+                        const int r = r0 + rl;
+                        if (r < Nc) {
+                            uint4 v;
+                            v.x = stg[(c4 + 0) * kStgPitch + r];
+                            v.y = stg[(c4 + 1) * kStgPitch + r];
+                            v.z = stg[(c4 + 2) * kStgPitch + r];
+                            v.w = stg[(c4 + 3) * kStgPitch + r];
+                            *reinterpret_cast<uint4*>(dst + r * kWordsPerBlock + c4) = v;
+                        }
+                    }
                 }
             }
             epi_sync();
