@@ -3,7 +3,8 @@
 
 One step = the whole path over one batch of synthetic input: for every layer, centre the keys
 (mp_key_mean), build the packed SimHash codes (mp_build_tables, tcgen05), encode the queries
-(mp_encode_query) and run the fused collide/select/gather/attend kernel (mp_sampled_attention).
+(mp_encode_query) and run the collide/select and gather/attend/merge kernels
+(mp_sampled_attention).
 Default workload: Llama-3.1-8B-shaped decode at 96K context (B=1, 32 query / 8 KV heads, d=128,
 n=98,304, 32 layers, (K, L) = (10, 150), 4 sink + 64 local tokens exact), bf16 K/V.
 
