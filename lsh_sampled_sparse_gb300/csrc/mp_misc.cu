@@ -57,16 +57,41 @@ __global__ void __launch_bounds__(kMeanThreads)
     }
     __syncthreads();
     if (!last) return;
-    // the head's partials, in range order: two halves of the ranges, one column per thread
-    const int col = tid % kD, half = tid / kD;
-    const float* ph0 = partial + static_cast<size_t>(bh) * nsplit * kD + col;
-    float s = 0.0f;
-#pragma unroll 8
-    for (int k = half; k < nsplit; k += 2) s += __ldcg(ph0 + static_cast<size_t>(k) * kD);
-    red[half][col] = s;
+    // the head's partials: thread t sums columns 4 (t % 32) .. + 3 of the ranges k = t / 32,
+    // t / 32 + 8, ... in order (16-byte loads, all of a thread's in flight at once), then the
+    // 8 slices add up in order: a fixed order, and one memory round trip for the partials
+    static_assert(kMeanThreads == 256 && kPhases >= 8, "8 slices of 32 four-column groups");
+    const int c4 = tid & 31, slice = tid >> 5;
+    const float4* ph4 = reinterpret_cast<const float4*>(partial + static_cast<size_t>(bh) * nsplit * kD) + c4;
+    float4 acc4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    constexpr int kBatch = 16;
+    for (int k0 = slice; k0 < nsplit; k0 += 8 * kBatch) {
+        float4 v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int k = k0 + 8 * j;
+            v[j] = k < nsplit ? __ldcg(ph4 + static_cast<size_t>(k) * (kD / 4))
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            acc4.x += v[j].x;
+            acc4.y += v[j].y;
+            acc4.z += v[j].z;
+            acc4.w += v[j].w;
+        }
+    }
+    red[slice][4 * c4 + 0] = acc4.x;
+    red[slice][4 * c4 + 1] = acc4.y;
+    red[slice][4 * c4 + 2] = acc4.z;
+    red[slice][4 * c4 + 3] = acc4.w;
     __syncthreads();
-    if (tid < kD) centre[static_cast<size_t>(bh) * kD + tid] = (red[0][tid] + red[1][tid]) /
-                                                               static_cast<float>(n);
+    if (tid < kD) {
+        float t = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) t += red[q][tid];
+        centre[static_cast<size_t>(bh) * kD + tid] = t / static_cast<float>(n);
+    }
     if (tid == 0) counters[bh] = 0u;
 }
 
