@@ -214,6 +214,13 @@ __global__ void __launch_bounds__(kCpThreads) collide_cp_kernel(const CpCArgs a)
     const int b = bg / a.Hkv, g = bg % a.Hkv;
     const int row0 = b * a.Hq + g * G;
     allow_dependents();
+    const uint8_t* base = a.codes + (static_cast<size_t>(bg) * a.cblk + blk) * a.L * kKeysPerBlock +
+                          lane * 32;
+    const int t0 = (a.L * warp) / kCpWarps, t1 = (a.L * (warp + 1)) / kCpWarps;
+    // the codes are an input of the call: pull this warp's tables into L2 before the wait
+    if ((lane & 3) == 0)
+        for (int t = t0; t < t1; ++t)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(base + static_cast<size_t>(t) * kKeysPerBlock));
     wait_for_predecessor();                      // the query codes of this call
     for (int i = tid; i < G * a.L; i += kCpThreads)
         qc[i] = a.qcodes[static_cast<size_t>(row0 + i / a.L) * a.qbytes + i % a.L];
@@ -224,9 +231,6 @@ __global__ void __launch_bounds__(kCpThreads) collide_cp_kernel(const CpCArgs a)
         ge1[h] = 0u;
         ge2[h] = 0u;
     }
-    const uint8_t* base = a.codes + (static_cast<size_t>(bg) * a.cblk + blk) * a.L * kKeysPerBlock +
-                          lane * 32;
-    const int t0 = (a.L * warp) / kCpWarps, t1 = (a.L * (warp + 1)) / kCpWarps;
     for (int t = t0; t < t1; ++t) {
         const uint4* p = reinterpret_cast<const uint4*>(base + static_cast<size_t>(t) * kKeysPerBlock);
         const uint4 c0 = __ldcs(p), c1 = __ldcs(p + 1);
