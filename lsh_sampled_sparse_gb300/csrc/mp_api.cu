@@ -222,7 +222,7 @@ size_t mp_codes_bytes(int B, int Hkv, int n, int K, int L) {
 size_t mp_key_mean_workspace_bytes(int B, int Hkv, int n, int d) {
     if (B < 1 || Hkv < 1 || n < 1 || d != kD) return 0;
     // partial column sums per row range, then one counter per head
-    return align256(static_cast<size_t>(B) * Hkv * key_mean_splits(n) * kD * 4 +
+    return align256(static_cast<size_t>(B) * Hkv * key_mean_splits(B * Hkv, n) * kD * 4 +
                     static_cast<size_t>(B) * Hkv * 4);
 }
 
@@ -242,7 +242,8 @@ mp_status mp_key_mean_cap(const void* keys, mp_dtype key_dtype, int B, int Hkv, 
     if (ws_bytes < mp_key_mean_workspace_bytes(B, Hkv, n, d)) return MP_ERR_WORKSPACE;
     if (!ensure_prepared()) return MP_ERR_CUDA;
     return to_status(launch_key_mean(keys, key_dtype == MP_BF16, B * Hkv, n_capacity, n, centre,
-                                     static_cast<float*>(workspace), key_mean_splits(n), stream));
+                                     static_cast<float*>(workspace), key_mean_splits(B * Hkv, n),
+                                     stream));
 }
 
 mp_status mp_build_tables(const void* keys, mp_dtype key_dtype, const float* centre,

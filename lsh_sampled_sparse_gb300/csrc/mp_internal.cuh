@@ -58,7 +58,7 @@ DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug);
 // ---- launchers (each returns the launch error, cudaSuccess otherwise) -------------------------
 cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int ncap, int n, float* centre,
                             float* partial, int nsplit, cudaStream_t st);
-int key_mean_splits(int n);
+int key_mean_splits(int BH, int n);
 
 // Encode whole 1024-key blocks [blk0, blk1) of every head of a cache laid out for ncap keys
 // per head (keys >= ncap read as zero).

@@ -1,5 +1,7 @@
 // Key centre, the fp32 CUDA-core encoder, and the inspection kernels (selection lists,
 // collision counts, unpacked codes).
+#include <algorithm>
+
 #include "mp_internal.cuh"
 
 namespace mp {
@@ -9,14 +11,16 @@ namespace {
 // Centre: mu = (1/n) sum_i k_i per head ("LSH Sampling...", method details, data preprocessing
 // and centering). Fixed partition into row ranges, fixed reduction order: run-to-run identical.
 // ------------------------------------------------------------------------------------------------
-constexpr int kMeanRows = 1024;    // rows per partial sum
+constexpr int kMeanMaxRows = 1024;   // rows per partial sum for long contexts
+constexpr int kMeanMinRows = 64;     // ... and at least this many for short ones
+constexpr int kMeanCtas = 608;       // row ranges wanted in all (four per SM of a GB300)
 constexpr int kMeanThreads = 256;
 
 // One CTA per (row range, head): the range's column sums into `partial`; the last CTA of a head
 // to finish (release-acquire counter) adds the head's partials in range order and writes mu.
 template <typename T>
 __global__ void __launch_bounds__(kMeanThreads)
-    key_mean_kernel(const T* keys, int ncap, int n, int nsplit, float* partial,
+    key_mean_kernel(const T* keys, int ncap, int n, int rows, int nsplit, float* partial,
                     unsigned* counters, float* centre) {
     // thread -> (column group of 16 bytes, row phase); rows stride by the number of row phases
     constexpr int kPer = 16 / sizeof(T);                 // elements per 16-byte load
@@ -26,7 +30,7 @@ __global__ void __launch_bounds__(kMeanThreads)
     __shared__ int last;
     const int bh = blockIdx.y, split = blockIdx.x, tid = threadIdx.x;
     const int cg = tid % kGroups, ph = tid / kGroups;
-    const int r0 = split * kMeanRows, r1 = min(n, r0 + kMeanRows);
+    const int r0 = split * rows, r1 = min(n, r0 + rows);
     const T* base = keys + static_cast<size_t>(bh) * ncap * kD + cg * kPer;
     float acc[kPer];
 #pragma unroll
@@ -99,7 +103,8 @@ __global__ void __launch_bounds__(kMeanThreads)
 // fp32 CUDA-core encoder for dtype pairs the tensor-core path does not take (fp32 keys or W):
 // bit_{i,j} = [sum_e W[e][j] (k_i[e] - mu[e]) > 0] in fp32, one key per thread, a warp's 32 keys
 // form one word per hyperplane through a ballot. Whole 1024-key blocks from blk0 on (keys at or
-// past ncap read as zero).
+// past ncap read as zero). Grid z splits the hyperplanes when there are few keys, so that short
+// contexts still fill the GPU; every sum is the same sequence of fmaf over e either way.
 // ------------------------------------------------------------------------------------------------
 constexpr int kSimtKeys = 64;      // keys per CTA (2 words)
 constexpr int kSimtPlanes = 16;    // hyperplanes per pass
@@ -124,7 +129,11 @@ __global__ void __launch_bounds__(kSimtKeys)
     const int word = (i0 % kKeysPerBlock) / 32 + warp;
     uint32_t* dst = codes + (static_cast<size_t>(bh) * cblk + blk) * static_cast<size_t>(C) *
                                 kWordsPerBlock + word;
-    for (int j0 = 0; j0 < C; j0 += kSimtPlanes) {
+    const int passes = (C + kSimtPlanes - 1) / kSimtPlanes;
+    const int per = (passes + gridDim.z - 1) / gridDim.z;          // passes of this CTA
+    const int j_lo = blockIdx.z * per * kSimtPlanes;
+    const int j_hi = min(C, j_lo + per * kSimtPlanes);
+    for (int j0 = j_lo; j0 < j_hi; j0 += kSimtPlanes) {
         __syncthreads();
         for (int idx = tid; idx < kD * kSimtPlanes; idx += kSimtKeys) {
             const int e = idx / kSimtPlanes, c = idx % kSimtPlanes, j = j0 + c;
@@ -229,7 +238,20 @@ __global__ void codes_unpack_kernel(const uint32_t* codes, int n, int nblk, int 
 
 }  // namespace
 
-int key_mean_splits(int n) { return (n + kMeanRows - 1) / kMeanRows; }
+// Rows per range: 1024, halved (down to 64) while the BH heads would give fewer than kMeanCtas
+// ranges, so that short contexts spread over the GPU too. A function of (BH, n) only: the
+// workspace size and the launch agree.
+int key_mean_rows(int BH, int n) {
+    int rows = kMeanMaxRows;
+    while (rows > kMeanMinRows &&
+           static_cast<long long>(BH) * ((n + rows - 1) / rows) < kMeanCtas)
+        rows /= 2;
+    return rows;
+}
+int key_mean_splits(int BH, int n) {
+    const int rows = key_mean_rows(BH, n);
+    return (n + rows - 1) / rows;
+}
 
 cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int ncap, int n, float* centre,
                             float* partial, int nsplit, cudaStream_t st) {
@@ -238,13 +260,16 @@ cudaError_t launch_key_mean(const void* keys, bool bf16, int BH, int ncap, int n
     cudaError_t e = cudaMemsetAsync(counters, 0, static_cast<size_t>(BH) * sizeof(unsigned), st);
     if (e != cudaSuccess) return e;
     const dim3 grid(nsplit, BH);
+    const int rows = key_mean_rows(BH, n);
+    if (nsplit != key_mean_splits(BH, n)) return cudaErrorInvalidValue;
     if (bf16)
         key_mean_kernel<__nv_bfloat16><<<grid, kMeanThreads, 0, st>>>(
-            reinterpret_cast<const __nv_bfloat16*>(keys), ncap, n, nsplit, partial, counters,
-            centre);
+            reinterpret_cast<const __nv_bfloat16*>(keys), ncap, n, rows, nsplit, partial,
+            counters, centre);
     else
         key_mean_kernel<float><<<grid, kMeanThreads, 0, st>>>(
-            reinterpret_cast<const float*>(keys), ncap, n, nsplit, partial, counters, centre);
+            reinterpret_cast<const float*>(keys), ncap, n, rows, nsplit, partial, counters,
+            centre);
     return cudaGetLastError();
 }
 
@@ -254,7 +279,12 @@ cudaError_t launch_encode_simt(const void* keys, bool keys_bf16, const float* ce
     const int C = K * L;
     if (C == 0 || blk1 <= blk0) return cudaSuccess;
     const int cblk = (ncap + kKeysPerBlock - 1) / kKeysPerBlock;
-    const dim3 grid((blk1 - blk0) * (kKeysPerBlock / kSimtKeys), B * Hkv);
+    const int tiles = (blk1 - blk0) * (kKeysPerBlock / kSimtKeys) * B * Hkv;
+    // hyperplane parts: enough CTAs for about four per SM, at most one part per pass
+    const int passes = (C + kSimtPlanes - 1) / kSimtPlanes;
+    const int want = (4 * device_sm_count() + tiles - 1) / tiles;
+    const int parts = std::max(1, std::min(passes, want));
+    const dim3 grid((blk1 - blk0) * (kKeysPerBlock / kSimtKeys), B * Hkv, parts);
     encode_simt_kernel<<<grid, kSimtKeys, 0, st>>>(keys, keys_bf16, centre, W, w_bf16, ncap, C,
                                                     cblk, blk0, codes);
     return cudaGetLastError();

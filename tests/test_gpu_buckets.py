@@ -85,6 +85,8 @@ def _decode_both(mp, wl, x, W, centre, codes, buckets):
     dict(B=1, Hq=4, Hkv=4, n=3000, K=8, L=75, kv_dtype=F32),      # fp32, no GQA
     dict(B=1, Hq=8, Hkv=1, n=2048, K=12, L=20, kv_dtype=BF),      # the largest K, GQA 8
     dict(B=1, Hq=2, Hkv=1, n=1500, K=3, L=7, kv_dtype=BF),        # tiny tables: full buckets
+    dict(B=1, Hq=4, Hkv=2, n=4100, K=9, L=40, kv_dtype=BF),       # 3 code words per transpose
+    dict(B=1, Hq=4, Hkv=1, n=3333, K=11, L=30, kv_dtype=BF),      # 2 code words per transpose
 ])
 def test_buckets_build_and_decode_match_the_scan(mp, shape):
     wl = small_workload(**shape)
