@@ -60,7 +60,7 @@ extern "C" {
 typedef enum {
     MP_OK = 0,
     MP_ERR_INVALID_ARG = 1,   /* bad shape, null pointer, misalignment, inconsistent sizes */
-    MP_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement (e.g. d != 128) */
+    MP_ERR_UNSUPPORTED = 2,   /* a valid request the library does not implement (e.g. d != 128) */
     MP_ERR_CUDA = 3,          /* a CUDA runtime call failed; cudaGetLastError() has the cause */
     MP_ERR_TIMEOUT = 4,       /* a device-side bounded wait gave up (see mp_device_status) */
     MP_ERR_WORKSPACE = 5      /* the workspace passed is smaller than *_workspace_bytes */
