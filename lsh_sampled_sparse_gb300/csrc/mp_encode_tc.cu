@@ -195,6 +195,10 @@ __device__ __forceinline__ void tmem_ld_wait() {
 __device__ __forceinline__ void epi_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
 }
+// the four epilogue warps of one 64-column group (named barriers 2 .. 5)
+__device__ __forceinline__ void group_sync(int cg) {
+    asm volatile("bar.sync %0, 128;" ::"r"(2 + cg) : "memory");
+}
 // 1.0 if the fp32 accumulator (as bits) is negative, else 0.0: -2^126 x, saturated to [0, 1]
 // (denormals flush to zero), on the FP32 pipe
 __device__ __forceinline__ float neg_as_one(uint32_t v) {
@@ -469,9 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the argmax codes, its Nc / d table rows of 1024 code bytes
         uint8_t* stg_bytes = reinterpret_cast<uint8_t*>(stg);
         auto store_unit = [&](int bg, int blk) {
-            epi_sync();
-            if (!aborted) {
-                if constexpr (kMode == kArgmax) {
+            if constexpr (kMode == kArgmax) {
+                epi_sync();
+                if (!aborted) {
                     const int ntab = Nc / kD, L = a.C / kD;
                     uint8_t* dst = reinterpret_cast<uint8_t*>(a.codes) +
                                    ((static_cast<size_t>(bg) * a.cblk + a.blk0 + blk) * L + j0 / kD) *
@@ -479,16 +483,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (et < ntab * (kKeysPerBlock / 4))
                         reinterpret_cast<uint32_t*>(dst)[et] =
                             reinterpret_cast<const uint32_t*>(stg_bytes)[et];
-                } else {
+                }
+                epi_sync();
+            } else {
+                // the staged words of planes colA .. colA + 63 come from the four warps of this
+                // column group alone, so those four store them, between barriers of their own
+                group_sync(ew >> 2);
+                if (!aborted) {
                     uint32_t* dst = a.codes + (static_cast<size_t>(bg) * a.cblk + a.blk0 + blk) *
                                                   static_cast<size_t>(a.C) * kWordsPerBlock +
                                     static_cast<size_t>(j0) * kWordsPerBlock;
                     // four rows per warp instruction: lane l takes words 4 (l % 8) .. + 3 of
                     // row r0 + l / 8 (bank (w + r) mod 32: distinct across the warp)
                     const int rl = lane >> 3, c4 = (lane & 7) * 4;
-                    for (int r0 = 4 * ew; r0 < Nc; r0 += 4 * kEpiWarps) {
+                    const int rend = min(Nc, colA + 64);
+                    for (int r0 = colA + 4 * (ew & 3); r0 < rend; r0 += 16) {
                         const int r = r0 + rl;
-                        if (r < Nc) {
+                        if (r < rend) {
                             uint4 v;
                             v.x = stg[(c4 + 0) * kStgPitch + r];
                             v.y = stg[(c4 + 1) * kStgPitch + r];
@@ -498,8 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                group_sync(ew >> 2);
             }
-            epi_sync();
         };
         for (int ab = 0; ab < 2; ++ab) {
             fill_next();
