@@ -182,11 +182,6 @@ struct CArgs {
     int blk0;                                    // first block scanned (grid x + blk0)
 };
 
-template <typename KV>
-__host__ __device__ constexpr int stage_rows() {
-    return sizeof(KV) == 2 ? 64 : 32;   // 32 KB of K+V rows either way
-}
-
 // Attend CTA shared memory: [work][cbuf][misc]. The work region holds the CTA's row list, and in
 // the merging CTA up to `merge_cap` staged partial outputs (all of them unless that exceeds
 // 48 KB; the merge then runs in rounds).
@@ -262,42 +257,6 @@ __device__ __forceinline__ void load_qneg(const uint32_t* p, uint32_t (&v)[G]) {
     } else {
 #pragma unroll
         for (int h = 0; h < G; ++h) v[h] = p[h];
-    }
-}
-
-// Phase 1 for a compile-time K: tables [t0, t1) of one 32-key word (this lane). The K plane
-// words of table t+1 are loaded while table t is reduced, so two tables' loads are in flight.
-template <int G, int K>
-__device__ __forceinline__ void scan_tables_k(const uint32_t* cb, const uint32_t* qneg, int t0,
-                                              int t1, uint32_t (&ge1)[G], uint32_t (&ge2)[G]) {
-    uint32_t cur[K], nxt[K];
-    if (t0 < t1) {
-#pragma unroll
-        for (int b = 0; b < K; ++b) cur[b] = __ldcs(cb + static_cast<size_t>(t0 * K + b) * kWordsPerBlock);
-    }
-    for (int t = t0; t < t1; ++t) {
-        if (t + 1 < t1) {
-#pragma unroll
-            for (int b = 0; b < K; ++b)
-                nxt[b] = __ldcs(cb + static_cast<size_t>((t + 1) * K + b) * kWordsPerBlock);
-        }
-        uint32_t acc[G];
-#pragma unroll
-        for (int h = 0; h < G; ++h) acc[h] = 0xffffffffu;
-#pragma unroll
-        for (int b = 0; b < K; ++b) {
-            uint32_t qn[G];
-            load_qneg<G>(qneg + (t * K + b) * G, qn);
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] &= cur[b] ^ qn[h];
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            ge2[h] |= ge1[h] & acc[h];
-            ge1[h] |= acc[h];
-        }
-#pragma unroll
-        for (int b = 0; b < K; ++b) cur[b] = nxt[b];
     }
 }
 
@@ -532,10 +491,6 @@ struct RowFrag;
 template <>
 struct RowFrag<__nv_bfloat16> {
     uint4 k, v;
-    __device__ __forceinline__ void load(const __nv_bfloat16* kp, const __nv_bfloat16* vp) {
-        k = __ldg(reinterpret_cast<const uint4*>(kp));
-        v = __ldg(reinterpret_cast<const uint4*>(vp));
-    }
     __device__ __forceinline__ void from_pieces(const uint4 (&p)[2]) { k = p[0]; v = p[1]; }
     __device__ __forceinline__ void unpack(float (&kf)[8], float (&vf)[8]) const {
         const uint32_t kw[4] = {k.x, k.y, k.z, k.w}, vw[4] = {v.x, v.y, v.z, v.w};
@@ -553,12 +508,6 @@ struct RowFrag<__nv_bfloat16> {
 template <>
 struct RowFrag<float> {
     float4 k0, k1, v0, v1;
-    __device__ __forceinline__ void load(const float* kp, const float* vp) {
-        k0 = __ldg(reinterpret_cast<const float4*>(kp));
-        k1 = __ldg(reinterpret_cast<const float4*>(kp) + 1);
-        v0 = __ldg(reinterpret_cast<const float4*>(vp));
-        v1 = __ldg(reinterpret_cast<const float4*>(vp) + 1);
-    }
     __device__ __forceinline__ void from_pieces(const uint4 (&p)[4]) {
         k0 = *reinterpret_cast<const float4*>(&p[0]);
         k1 = *reinterpret_cast<const float4*>(&p[1]);
