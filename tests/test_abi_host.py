@@ -71,6 +71,22 @@ def test_workspace_sizes(L):
     assert mp.key_mean_workspace_bytes(1, 8, 98304, 64) == 0
 
 
+@pytest.mark.parametrize("B,Hkv,n,rows", [
+    (1, 8, 98304, 1024),     # 96 ranges per head x 8 heads = 768: long ranges
+    (4, 8, 16384, 512),      # 16 x 32 = 512 < 608 ranges: halved once
+    (1, 1, 4096, 64),        # a single short head: the 64-key floor
+    (32, 8, 32768, 1024),    # many heads: long ranges
+    (1, 1, 100, 64),         # one short range
+])
+def test_key_mean_ranges_fill_the_gpu(B, Hkv, n, rows):
+    # the workspace holds one 128-float range sum per (head, range) plus a counter per head;
+    # ranges are 1024 keys, halved down to 64 while the heads would have fewer than 608 of them
+    import lsh_sampled_sparse_gb300 as mp
+    ranges = (n + rows - 1) // rows
+    want = B * Hkv * ranges * 128 * 4 + B * Hkv * 4
+    assert mp.key_mean_workspace_bytes(B, Hkv, n, 128) == (want + 255) // 256 * 256
+
+
 def _decode(L, ws_bytes=1 << 20, d=128, Hq=4, Hkv=1, n=1000, K=10, Lt=150, flags=0,
             null_q=False, ptr=0x10000):
     import lsh_sampled_sparse_gb300 as mp
