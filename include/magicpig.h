@@ -134,9 +134,10 @@ MP_API size_t mp_key_mean_workspace_bytes(int B, int Hkv, int n, int d);
  * accumulation in a fixed order (run-to-run identical).
  * ("LSH Sampling...", method details, data preprocessing and centering: keys are centred before
  * the tables are built; "don't pick the tallest", section 5.)
- * One kernel: each CTA sums a range of 1024 rows, the last CTA of a head adds the ranges in
- * order. Errors: MP_ERR_INVALID_ARG for n < 1, null pointers; MP_ERR_WORKSPACE if ws_bytes is
- * short. */
+ * One kernel: each CTA sums a range of rows (1024, halved down to 64 while the B*Hkv heads
+ * would have fewer than 608 ranges, a function of B*Hkv and n only), the last CTA of a head adds
+ * the ranges in order. Errors: MP_ERR_INVALID_ARG for n < 1, null pointers; MP_ERR_WORKSPACE if
+ * ws_bytes is short. */
 MP_API mp_status mp_key_mean(const void* keys, mp_dtype key_dtype, int B, int Hkv, int n, int d,
                              float* centre, void* workspace, size_t ws_bytes,
                              cudaStream_t stream);
