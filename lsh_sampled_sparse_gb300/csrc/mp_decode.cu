@@ -409,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     //      of the call): into the ring for the ring's K, else into L2
     allow_dependents();
     const int t0 = (a.L * warp) / kWarps, t1 = (a.L * (warp + 1)) / kWarps;
-    const uint32_t* cb0 = a.codes + (static_cast<size_t>(bg) * a.cblk + blk) * a.C * kWordsPerBlock;
+    const uint32_t* cb0 =
+        a.codes + (static_cast<size_t>(bg) * a.cblk + blk) * a.C * kWordsPerBlock;
     switch (a.K) {
         case 8: ring_fill<8>(cb0, ring, t0, t1, lane); break;
         case 9: ring_fill<9>(cb0, ring, t0, t1, lane); break;
@@ -419,12 +420,13 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
             const uint32_t* first = cb0 + static_cast<size_t>(t0) * a.K * kWordsPerBlock;
             const int rows = min(kRingDepth * a.K, (t1 - t0) * a.K);
             for (int r = lane; r < rows; r += 32)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(first + static_cast<size_t>(r) * kWordsPerBlock));
+                asm volatile("prefetch.global.L2 [%0];"
+                             ::"l"(first + static_cast<size_t>(r) * kWordsPerBlock));
         }
     }
     wait_for_predecessor();
 
-    // ---- prologue: the group's query masks (one contiguous piece), q and mu as floats
+    // ---- prologue: the group's query masks (one contiguous piece)
     {
         const uint4* src = reinterpret_cast<const uint4*>(a.qmask +
                                                           static_cast<size_t>(bg) * a.cpad * G);
