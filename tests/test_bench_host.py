@@ -45,3 +45,24 @@ def test_defaults_are_the_96k_workload():
     a = bench.parse_args([])
     assert a.workload == "llama8b_n96k_32layers" and a.gpus == 1 and a.warmup >= 3
     assert bench.job_throughput(1, 1024, 5, 1000.0) == pytest.approx(5120.0)
+
+
+def test_reference_arm_prints_the_contract_line():
+    # the oracle arm on the smallest workload: one JSON line with the keys the driver reads
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    res = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--workload", "tiny_f32_n4096", "--steps", "1", "--warmup", "1",
+                          "--cpu-seconds", "1"], capture_output=True, text=True, timeout=300,
+                         cwd=root)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "queries/s"
+    for key in ("metric", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "dtype", "data", "config"):
+        assert key in line, key
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["e2e"]["value"] == line["value"]
