@@ -630,7 +630,8 @@ def cpu_oracle_sample(wl, state, W, budget_s: float):
                       f" A1 encode on {wl.C} hyperplanes, A2-A5 for its {wl.G} query heads, run"
                       f" on the first {n_s} of the {wl.n} keys ({t_total:.1f} s) and scaled"
                       f" x{wl.n / n_s:g} to the full context (every oracle step is linear in n);"
-                      f" fp64 numpy"}
+                      f" fp64 numpy, whose BLAS spreads the projections over up to {cores} host"
+                      f" cores while the per-key steps run on one"}
 
 
 def run_e2e(mp, wl, W, state, ws_mean, ws_dec, steps: int):
@@ -926,7 +927,8 @@ def run_reference(args):
     sample = (f"per step one (sequence, KV head) unit of layer 0 of {wl.name}: A0 centre, A1 "
               f"encode on {wl.C} hyperplanes, A2-A5 for {wl.G} query heads, run on the first "
               f"{n_s} of the {wl.n} keys and scaled x{wl.n / n_s:g} to the full context (every "
-              f"oracle step is linear in n); fp64 numpy oracle")
+              f"oracle step is linear in n); fp64 numpy oracle, whose BLAS spreads the "
+              f"projections over up to {cores} host cores while the per-key steps run on one")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
