@@ -5,30 +5,35 @@ call or execute this module; the product package never does, and it shares no co
 helper with the CUDA path. Inputs reach it only from the seeded generators in ``workloads``.
 
 What it is: a plain, slow CPU restatement in float64 (numpy) of one decode step of the method,
-taken step by step in the order of Algorithm 1 ("MagicPIG: LSH Sampling for Efficient LLM
-Generation", method details, "algorithm execution") and of the five-line estimator sketch
-("MagicPIG: don't pick the tallest", section 5, "A hash that knows its odds"):
+written from the definitions the pages give ("MagicPIG: LSH Sampling for Efficient LLM
+Generation", background and method details; "MagicPIG: don't pick the tallest", section 5):
 
-  1. centre the keys:            kbar_i = k_i - mu, mu the mean key        (data preprocessing)
-  2. SimHash-encode the keys:     bit_{i,j} = [w_j . kbar_i > 0]           (LSH basics; hash choice)
-     and the query (not centred): qbit_j = [w_j . q > 0]
-     L tables of K bits: code_t = sum_b bit_{t*K+b} << b
-  3. collision count:             cnt_i = #{t : code_t(k_i) = code_t(q)}
-  4. sample set:                  S = {i not in T : cnt_i >= 2}            (hash choice; sketch)
-  5. p_i = 1 - arccos(cos(q, kbar_i))/pi,
-     u_i = 1 - (1-p_i^K)^L - L p_i^K (1-p_i^K)^(L-1)                       (u_i formula)
-  6. o = softmax([s_S - log u_S, s_T]) . [V_S, V_T],  s = q.k/sqrt(d)     (Algorithm 1, last step)
+  centring        kbar_i = k_i - mu, mu the mean of the n cached keys    (data preprocessing)
+  SimHash bits    bit_{i,j} = [w_j . kbar_i > 0], query bits [w_j . q > 0] (q not centred);
+                  L tables of K bits, code_t = sum_b bit_{t*K+b} << b     (LSH basics; hash choice)
+  collisions      cnt_i = #{t : code_t(k_i) = code_t(q)}
+  sample set      S = {i not in T : cnt_i >= 2}                           (hash choice; section 5)
+  bit agreement   p_i = 1 - theta_i/pi, theta_i the angle of q and kbar_i (SimHash's probability)
+  inclusion       u_i = P[Binomial(L, p_i^K) >= 2]
+                      = 1 - (1-p_i^K)^L - L p_i^K (1-p_i^K)^(L-1)         (the u_i formula)
+  estimate        o = (sum_S e^{s_i}/u_i v_i + sum_T e^{s_i} v_i)
+                      / (sum_S e^{s_i}/u_i + sum_T e^{s_i}),   s_i = q.k_i/sqrt(d)
+                  the self-normalised importance-sampling estimator over S (method details,
+                  estimator) joined with exact attention over the static set T (Algorithm 1's
+                  last step); the two sums are kept as log-domain partials and merged by
+                  log-sum-exp, the "recursive attention" merge of the system co-design section.
 
 Readings of points the pages leave open (each is also listed in the design notes):
-  * p uses the centred key (the sketch's ``cos(q, K_S - mu)``); Algorithm 1 prints the uncentred
-    ||K_S||, but SimHash's 1 - theta/pi holds for the vectors actually hashed, which are centred.
+  * p uses the centred key ("don't pick the tallest" section 5 takes the cosine of q and
+    K_S - mu); Algorithm 1 prints the uncentred ||K_S||, but SimHash's 1 - theta/pi holds for
+    the vectors actually hashed, which are centred.
   * scores use the raw keys for both S and T; the softmax is shift-invariant, so centred scores
     give the same output (section 5: every score shifts by the same amount).
   * the query is not centred.
   * bit = 1 iff the projection is strictly positive.
   * bit b of table t is hyperplane column t*K + b, least significant bit first.
-  * a zero-length q or kbar has cosine 0, so p = 1/2 (the sketch's note on zero-length vectors).
-  * log u is evaluated stably in the log domain (the sketch's note on stable probability
+  * a zero-length q or kbar has cosine 0, so p = 1/2 (section 5 asks for zero-length handling).
+  * log u is evaluated stably in the log domain (section 5 asks for stable probability
     arithmetic): directly when L p^K >= 1/2, else as the binomial tail series from its j = 2 term.
     If p = 0 (such a key cannot collide in exact arithmetic) log u is clamped to log(DBL_MIN).
   * if S and T are both empty the output is the zero vector.
@@ -429,22 +434,50 @@ def inclusion_probability(p, K: int, L: int) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------------------------
-# Step 6: the self-normalised importance-sampling estimate over S, joined with exact attention
-#         over T ("LSH Sampling..." method details: estimator approximation; Algorithm 1, last
-#         step; "don't pick the tallest" section 5 sketch, with the exact scores s_exact)
+# Step 6: the estimate. "LSH Sampling..." method details (estimator) gives the self-normalised
+# importance-sampling ratio over the sampled set S, each selected key weighted by e^{s_i}/u_i;
+# Algorithm 1's last step and "don't pick the tallest" section 5 add the static set T (sink and
+# recent tokens) with its ordinary weights e^{s_i}. So
+#     o = (sum_S e^{s_i - log u_i} v_i + sum_T e^{s_i} v_i) / (sum_S e^{s_i - log u_i} + sum_T e^{s_i}).
+# Each of the two sums is kept as a log-domain partial (M, Z, N): M the largest log-weight a_i,
+# Z = sum e^{a_i - M}, N = sum e^{a_i - M} v_i; two partials join by log-sum-exp, the "recursive
+# attention" merge of the system co-design section.
 # ----------------------------------------------------------------------------------------------
+def _log_weight_partial(log_w, V, d: int):
+    """(M, Z, N) of the log-weights log_w [m] and values V [m, d]; M = -inf for no terms."""
+    a = np.asarray(log_w, dtype=np.float64).reshape(-1)
+    if a.size == 0:
+        return -math.inf, 0.0, np.zeros(d)
+    M = float(a.max())
+    e = np.exp(a - M)
+    return M, float(e.sum()), e @ as64(V).reshape(-1, d)
+
+
+def _merge_partials(parts, d: int) -> np.ndarray:
+    """sum_j e^{M_j - M} N_j / sum_j e^{M_j - M} Z_j with M = max_j M_j; zeros if all are empty."""
+    M = max(p[0] for p in parts)
+    if M == -math.inf:
+        return np.zeros(d)
+    num = np.zeros(d)
+    den = 0.0
+    for Mj, Zj, Nj in parts:
+        if Mj != -math.inf:
+            f = math.exp(Mj - M)
+            num += f * Nj
+            den += f * Zj
+    return num / den
+
+
 def snis_attention(q, K_S, V_S, logu_S, K_T, V_T, scale: float) -> np.ndarray:
-    """softmax([s_S - log u_S, s_T]) . [V_S, V_T] with s = scale * q.k; zeros if S, T empty."""
+    """The estimate o above for scores s = scale * q.k: the sampled partial with log-weights
+    s_i - log u_i, the exact partial with log-weights s_i, merged; zeros if S and T are empty."""
     qv = as64(q)
     d = qv.shape[0]
     KS = as64(K_S).reshape(-1, d)
     KT = as64(K_T).reshape(-1, d)
-    logits = np.concatenate([(KS @ qv) * scale - as64(logu_S).reshape(-1), (KT @ qv) * scale])
-    if logits.size == 0:
-        return np.zeros(d)
-    w = np.exp(logits - logits.max())
-    w /= w.sum()
-    return w @ np.concatenate([as64(V_S).reshape(-1, d), as64(V_T).reshape(-1, d)])
+    sampled = _log_weight_partial((KS @ qv) * scale - as64(logu_S).reshape(-1), V_S, d)
+    exact = _log_weight_partial((KT @ qv) * scale, V_T, d)
+    return _merge_partials([sampled, exact], d)
 
 
 def full_attention(q, keys, values, scale: float) -> np.ndarray:
@@ -460,8 +493,10 @@ def full_attention(q, keys, values, scale: float) -> np.ndarray:
 def decode_head(q, keys, values, centre, key_codes, q_code, K: int, L: int, n_sink: int,
                 n_local: int, scale: float | None = None, centred_scores: bool = False,
                 radius: float | None = None, cross_polytope: bool = False) -> dict:
-    """Steps 3-6 for one query head against its KV head's codes. With `radius` (the MIPS variant)
-    p uses q.kbar_i / (|q| r) in place of the cosine; with cross_polytope, p is the
+    """One query head against its KV head's codes: counts, S, then for every i in S the
+    collision probability p_i = 1 - theta_i/pi of SimHash (theta_i the angle of q and k_i - mu),
+    log u_i of the binomial tail, and the estimate o of snis_attention. With `radius` (the MIPS
+    variant) p uses q.kbar_i / (|q| r) in place of the cosine; with cross_polytope, p is the
     cross-polytope collision probability of that cosine (codes are then cross-polytope codes)."""
     qv = as64(q)
     k = as64(keys)

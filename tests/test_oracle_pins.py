@@ -145,6 +145,102 @@ def _brute_codes(keys, centre, W, K, L):
     return out
 
 
+def test_key_centre_is_the_mean_over_all_n_keys_by_scalar_loops():
+    # "LSH Sampling..." data preprocessing: mu = (1/n) sum_{i=1..n} k_i; integer-valued keys
+    # make every partial sum exact, so a divide by n - 1 or a dropped row cannot pass
+    rng = np.random.default_rng(31)
+    for n, d in ((1, 3), (7, 5), (64, 4)):
+        keys = rng.integers(-40, 41, size=(n, d)).astype(np.float64)
+        want = [Fraction(sum(int(keys[i][e]) for i in range(n)), n) for e in range(d)]
+        got = O.key_centre(keys)
+        assert [Fraction(float(x)).limit_denominator(10 ** 6) for x in got] == want
+
+
+def _band_offset(c: float, rest_norm2: float) -> float:
+    """delta with delta = c * 1e-5 * sqrt(delta^2 + rest_norm2): a vector (delta, rest) whose
+    projection delta * |w| on w = |w| e_0 sits at c times the band 1e-5 |w| |x|."""
+    t = c * 1e-5
+    return t * math.sqrt(rest_norm2) / math.sqrt(1.0 - t * t)
+
+
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_key_near_tie_band_edges(sign):
+    # the band is |w_j . (k_i - mu)| < 1e-5 |w_j| |k_i| with the RAW key norm: the key
+    # (delta, 0, 8, 4) has centred part (delta, 0, 3, 4) for mu = (0, 0, 5, 0); w_0 = 7 e_0
+    mu = np.array([0.0, 0.0, 5.0, 0.0])
+    W = np.zeros((4, 2))
+    W[0, 0] = 7.0
+    W[:, 1] = [0.0, 3.0, 0.0, 4.0]
+    for c, inside in ((0.999, True), (1.001, False), (0.5, True), (2.0, False)):
+        delta = sign * _band_offset(c, 8.0 ** 2 + 4.0 ** 2)
+        key = np.array([[delta, 0.0, 8.0, 4.0]])
+        _, bits, near = O.encode_keys(key, mu, W, 1, 2)
+        assert bool(near[0, 0]) is inside, (c, sign)
+        assert bool(bits[0, 0]) is (sign > 0)
+        assert not near[0, 1]                      # projection 16, far from the band
+
+
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_query_near_tie_band_edges(sign):
+    # the query is not centred: |w_j . q| < 1e-5 |w_j| |q|, here q = (delta, 0, 3, 4), w_0 = 7 e_0
+    W = np.zeros((4, 1))
+    W[0, 0] = 7.0
+    for c, inside in ((0.999, True), (1.001, False)):
+        q = np.array([sign * _band_offset(c, 25.0), 0.0, 3.0, 4.0])
+        _, bits, near = O.encode_query(q, W, 1, 1)
+        assert bool(near[0, 0]) is inside, (c, sign)
+        assert bool(bits[0, 0]) is (sign > 0)
+
+
+def test_replay_takes_every_flip_inside_the_band_and_rejects_any_outside():
+    rng = np.random.default_rng(32)
+    ob = rng.random((6, 40)) < 0.5
+    near = rng.random((6, 40)) < 0.3
+    other = ob.copy()
+    flips = near & (rng.random((6, 40)) < 0.5)
+    other[flips] = ~other[flips]
+    got, count = O.replay_bits(ob, near, other)
+    assert count == int(flips.sum()) > 0
+    assert np.array_equal(got, other)              # every flip in the band is taken
+    assert np.array_equal(O.replay_bits(ob, near, ob)[0], ob) and O.replay_bits(ob, near, ob)[1] == 0
+    i, j = np.argwhere(~near)[0]
+    bad = other.copy()
+    bad[i, j] = ~bad[i, j]                          # one flip outside the band
+    with pytest.raises(AssertionError):
+        O.replay_bits(ob, near, bad)
+
+
+def test_estimate_is_the_weighted_ratio_by_scalar_loops():
+    # o = (sum_S e^{s_i}/u_i v_i + sum_T e^{s_i} v_i) / (sum_S e^{s_i}/u_i + sum_T e^{s_i}),
+    # evaluated with 60-digit arithmetic; the sampled scores sit 700 above the exact ones in the
+    # second case (plain exponentials of either would overflow a double)
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 60
+    rng = np.random.default_rng(33)
+    d = 6
+    for shift in (0.0, 700.0):
+        KS = rng.standard_normal((4, d))
+        VS = rng.standard_normal((4, d))
+        KT = rng.standard_normal((3, d))
+        VT = rng.standard_normal((3, d))
+        q = rng.standard_normal(d)
+        u = rng.uniform(0.01, 1.0, size=4)
+        scale = 0.9
+        sS = [mpmath.mpf(scale * float(KS[i] @ q)) + shift for i in range(4)]
+        sT = [mpmath.mpf(scale * float(KT[i] @ q)) for i in range(3)]
+        wS = [mpmath.exp(sS[i]) / mpmath.mpf(u[i]) for i in range(4)]
+        wT = [mpmath.exp(x) for x in sT]
+        den = sum(wS) + sum(wT)
+        want = [float((sum(wS[i] * VS[i][e] for i in range(4)) +
+                       sum(wT[i] * VT[i][e] for i in range(3))) / den) for e in range(d)]
+        KS_shift = KS + (shift / scale) * q / float(q @ q)   # raises each sampled score by shift
+        got = O.snis_attention(q, KS_shift, VS, np.log(u), KT, VT, scale)
+        assert np.allclose(got, want, rtol=0, atol=1e-9)
+    # only one of the two parts present
+    assert np.allclose(O.snis_attention(q, KS[:0], VS[:0], np.zeros(0), KT, VT, scale),
+                       _brute_attention(q.tolist(), KT.tolist(), VT.tolist(), scale), atol=1e-13)
+
+
 def test_codes_counts_and_set_by_brute_force():
     rng = np.random.default_rng(3)
     d, n, K, L = 3, 9, 2, 3
