@@ -54,7 +54,7 @@ extern "C" {
 #define MP_API
 #endif
 
-#define MP_ABI_VERSION 4
+#define MP_ABI_VERSION 5
 #define MP_KEYS_PER_BLOCK 1024
 
 typedef enum {
@@ -192,12 +192,17 @@ MP_API size_t mp_decode_workspace_bytes(int B, int Hq, int Hkv, int n, int d,
  *   cnt_i  = #{t : code_t(k_i) == code_t(q)}           from the packed codes
  *   S      = {i not in T : cnt_i >= 2}
  *   p_i    = 1 - arccos(q.(k_i - mu) / (|q| |k_i - mu|)) / pi
- *   u_i    = 1 - (1 - p_i^K)^L - L p_i^K (1 - p_i^K)^(L-1)      (evaluated stably in log space)
+ *   u_i    = 1 - (1 - p_i^K)^L - L p_i^K (1 - p_i^K)^(L-1)
  *   out    = softmax([s_S - log u_S, s_T]) . [V_S, V_T],   s = scale * q.k_i  (raw keys)
- * The softmax over S and T is computed in pieces of 1024 keys and merged by log-sum-exp (the
- * "recursive attention" merge of the system co-design section). If S and T are both empty the
- * output row is zero. Zero-length q or k - mu gives cosine 0 (p = 1/2).
- * Errors: MP_ERR_INVALID_ARG (shapes, null, Hq % Hkv, n_sink/n_local < 0, flags != 0),
+ * log u_i is evaluated for every selected key in closed form, in fp32, in the log domain: directly
+ * when L p^K >= 1/2, else as the binomial tail series from its second term (mp_debug_log_inclusion
+ * returns the same function). The softmax over S and T is computed in pieces of 1024 keys and
+ * merged by log-sum-exp (the "recursive attention" merge of the system co-design section). If S
+ * and T are both empty the output row is zero. Zero-length q or k - mu gives cosine 0 (p = 1/2).
+ * A query row with a NaN or infinite element gets a NaN output row; the other rows are unaffected
+ * and the status word is not raised.
+ * Errors: MP_ERR_INVALID_ARG (shapes, null, Hq % Hkv, n_sink/n_local < 0, flags other than
+ *         MP_FLAG_MIPS or MP_FLAG_CROSS_POLYTOPE, or a flag without its radius / log u table),
  *         MP_ERR_UNSUPPORTED (d != 128, Hq/Hkv not in {1, 2, 4, 8}, or K*L*(Hq/Hkv) so
  *         large that a CTA's query masks no longer fit in shared memory),
  *         MP_ERR_WORKSPACE (ws_bytes < mp_decode_workspace_bytes). */
@@ -334,6 +339,35 @@ MP_API mp_status mp_debug_select(const void* q, mp_dtype q_dtype, const uint32_t
                                  uint32_t* q_bits, int32_t* sel_idx, int32_t* sel_count,
                                  uint8_t* cnt, void* workspace, size_t ws_bytes,
                                  cudaStream_t stream);
+
+/* mp_sampled_attention_buckets plus what it decided, for checking the bucketed retrieval against
+ * a reference: the query encoding of mp_encode_query (its sign bits into q_bits), the bucket lookup
+ * (and the scan of keys appended since the tables were built), the same attend kernel, and the
+ * sampled sets S (T excluded, ascending) into sel_idx / sel_count, laid out as in mp_debug_select.
+ * The workspace is mp_debug_workspace_bytes. Errors as mp_sampled_attention_buckets. */
+MP_API mp_status mp_debug_select_buckets(const void* q, mp_dtype q_dtype, const uint32_t* buckets,
+                                         const uint32_t* codes, const float* centre,
+                                         const void* W, mp_dtype w_dtype, const void* keys,
+                                         const void* values, mp_dtype kv_dtype, int B, int Hq,
+                                         int Hkv, int n, int d, const mp_params* prm, float* out,
+                                         uint32_t* q_bits, int32_t* sel_idx, int32_t* sel_count,
+                                         void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* log u at each of `count` cosines c (float32 device arrays cosines -> out), evaluated by the
+ * device function the decode kernels apply to every selected key of the SimHash codes: p = 1 -
+ * arccos(c) / pi, u = P[Binomial(L, p^K) >= 2] ("LSH Sampling...", method details, the u_i formula),
+ * in fp32 in the log domain; p = 0 gives log(FLT_MIN), L = 1 gives -inf. For checking that
+ * evaluation against a reference. Errors: MP_ERR_INVALID_ARG (count < 0, K outside [0, 32],
+ * L < 1, null or misaligned arrays). */
+MP_API mp_status mp_debug_log_inclusion(const float* cosines, int count, int K, int L, float* out,
+                                        cudaStream_t stream);
+
+/* Test hook of the failure path: one thread waits, with the bounded wait the tensor-core encoder
+ * uses on its pipeline barriers, on an mbarrier that nothing completes (no arrival, copy or MMA is
+ * issued), gives up after limit_us microseconds (1 to 100000) and records MP_ERR_TIMEOUT in the
+ * device status word, as a stalled encoder would; mp_device_status then returns it once.
+ * The paper has no counterpart. Errors: MP_ERR_INVALID_ARG (limit out of range). */
+MP_API mp_status mp_debug_wait_expiry(int limit_us, cudaStream_t stream);
 
 /* Unpack codes into one integer per (key, table): table_codes[b][g][i][t] = code_t(k_i) =
  * sum_b bit_{i, t*K+b} << b. Requires K <= 32. */

@@ -20,7 +20,10 @@ from .binding import (  # noqa: F401
     codes_unpack,
     cp_codes_bytes,
     cp_logu_table,
+    debug_log_inclusion,
     debug_select,
+    debug_select_buckets,
+    debug_wait_expiry,
     debug_workspace_bytes,
     decode_attention,
     decode_workspace_bytes,

@@ -104,6 +104,11 @@ def _declare(L):
         "mp_build_buckets_cap": (_c_int, [_vp] + [_c_int] * 6 + [_vp, _vp]),
         "mp_sampled_attention_buckets": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int]
                                          + [_c_int] * 5 + [P, _vp, _vp, _c_size, _vp]),
+        "mp_debug_select_buckets": (_c_int, [_vp, _c_int, _vp, _vp, _vp, _vp, _c_int, _vp, _vp,
+                                             _c_int] + [_c_int] * 5
+                                    + [P, _vp, _vp, _vp, _vp, _vp, _c_size, _vp]),
+        "mp_debug_log_inclusion": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp]),
+        "mp_debug_wait_expiry": (_c_int, [_c_int, _vp]),
         "mp_device_status": (_c_int, [ctypes.POINTER(_c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -472,6 +477,52 @@ def debug_select(q, codes, centre, W, keys, values, K: int, L: int, n_sink: int,
         _nbytes(ws), _stream(stream)), "mp_debug_select")
     return {"out": out, "q_bits": q_bits[..., :qwords], "sel_idx": sel_idx,
             "sel_count": sel_count, "cnt": cnt}
+
+
+def debug_select_buckets(q, buckets, codes, centre, W, keys, values, K: int, L: int,
+                         n_sink: int, n_local: int, scale: float = 0.0, stream=None, n=None,
+                         n_indexed: int = 0, radius=None) -> dict:
+    """The bucketed decode plus its decisions: out, q_bits, per-row ascending sample sets."""
+    _cuda(q, "q", 3)
+    _cuda(keys, "keys", 4)
+    _cuda(buckets, "buckets")
+    B, Hq, d = q.shape
+    Hkv = keys.shape[1]
+    n, cap = _lengths(keys.shape, n)
+    dev = q.device
+    qwords = (K * L + 31) // 32
+    out = torch.empty(B, Hq, d, dtype=torch.float32, device=dev)
+    q_bits = torch.zeros(B, Hq, max(qwords, 1), dtype=torch.int32, device=dev)
+    sel_idx = torch.full((B, Hq, n), -1, dtype=torch.int32, device=dev)
+    sel_count = torch.zeros(B, Hq, dtype=torch.int32, device=dev)
+    p = _params(K, L, n_sink, n_local, scale, cap, n_indexed, radius=radius)
+    need = int(lib().mp_debug_workspace_bytes(B, Hq, Hkv, n, d, ctypes.byref(p)))
+    if need == 0:
+        raise MagicPIGError("mp_debug_workspace_bytes rejected the shapes/parameters")
+    ws = _workspace(None, need, dev)
+    _check(lib().mp_debug_select_buckets(
+        _ptr(q), _dtype(q, "q"), _ptr(buckets), _ptr(codes), _ptr(centre), _ptr(W),
+        _dtype(W, "W"), _ptr(keys), _ptr(values), _dtype(keys, "keys"), B, Hq, Hkv, n, d,
+        ctypes.byref(p), _ptr(out), _ptr(q_bits) if qwords else None, _ptr(sel_idx),
+        _ptr(sel_count), _ptr(ws), _nbytes(ws), _stream(stream)), "mp_debug_select_buckets")
+    return {"out": out, "q_bits": q_bits[..., :qwords], "sel_idx": sel_idx,
+            "sel_count": sel_count}
+
+
+def debug_log_inclusion(cosines, K: int, L: int, out=None, stream=None):
+    """log u at each cosine (float32 CUDA tensor), as the decode kernels evaluate it."""
+    _cuda(cosines, "cosines")
+    if cosines.dtype != torch.float32:
+        raise TypeError("cosines must be float32")
+    out = torch.empty_like(cosines) if out is None else out
+    _check(lib().mp_debug_log_inclusion(_ptr(cosines), cosines.numel(), K, L, _ptr(out),
+                                        _stream(stream)), "mp_debug_log_inclusion")
+    return out
+
+
+def debug_wait_expiry(limit_us: int, stream=None) -> None:
+    """Run the failure path's test hook: a bounded wait that gives up after limit_us."""
+    _check(lib().mp_debug_wait_expiry(int(limit_us), _stream(stream)), "mp_debug_wait_expiry")
 
 
 def codes_unpack(codes, B: int, Hkv: int, n: int, K: int, L: int, stream=None):

@@ -109,47 +109,58 @@ int device_sm_count() {
     return dev < 0 || g_sm_count[dev] <= 0 ? 148 : g_sm_count[dev];
 }
 
-size_t decode_scratch_bytes(const DecodeShape& s, bool debug) {
+// Decode workspace, in order (each piece 256-byte aligned): query bits, query masks, query
+// norms, the attend kernel's partials, merge counters, selection words, the bucketed lookup's
+// >= 1 bitmap.
+namespace {
+struct ScratchSizes {
+    size_t qbits, qmask, qstat, pml, po, counters, sel;
+    int n_counters;
+};
+ScratchSizes scratch_sizes(const DecodeShape& s) {
     const size_t rows = static_cast<size_t>(s.B) * s.Hq;
-    size_t b = 0;
-    b += align256(rows * s.qwords * 4);                  // qbits
-    b += align256(rows * s.cpad * 4);                    // qmask
-    b += align256(rows * 16);                            // qstat
     const size_t nsp = attend_partials(s.nblk);
-    b += align256(rows * nsp * 4) * 2;                   // pm, pl
-    b += align256(rows * nsp * kD * 4);                  // po
-    b += align256(rows * 4);                             // counters
-    b += align256(rows * s.nblk * 32 * 4);               // selection words
-    b += align256(rows * s.nblk * 32 * 4);               // >= 1 bitmap of the bucketed lookup
-    b += align256((kLogUTableIntervals + 1) * 4);        // log u table
+    ScratchSizes z;
+    z.qbits = align256(rows * s.qwords * 4);
+    z.qmask = align256(rows * s.cpad * 4);
+    z.qstat = align256(rows * 16);
+    z.pml = align256(rows * nsp * 4);
+    z.po = align256(rows * nsp * kD * 4);
+    z.n_counters = static_cast<int>(rows);
+    z.counters = align256(static_cast<size_t>(z.n_counters) * 4);
+    z.sel = align256(rows * s.nblk * 32 * 4);
+    return z;
+}
+}  // namespace
+
+size_t decode_scratch_bytes(const DecodeShape& s, bool debug) {
+    const ScratchSizes z = scratch_sizes(s);
     (void)debug;                                         // the debug path needs nothing more
-    return b;
+    return z.qbits + z.qmask + z.qstat + 2 * z.pml + z.po + z.counters + 2 * z.sel;
 }
 
 DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug) {
-    const size_t rows = static_cast<size_t>(s.B) * s.Hq;
+    const ScratchSizes z = scratch_sizes(s);
     uint8_t* p = static_cast<uint8_t*>(ws);
     DecodeScratch d;
     d.qbits = reinterpret_cast<uint32_t*>(p);
-    p += align256(rows * s.qwords * 4);
+    p += z.qbits;
     d.qmask = reinterpret_cast<uint32_t*>(p);
-    p += align256(rows * s.cpad * 4);
+    p += z.qmask;
     d.qstat = reinterpret_cast<float4*>(p);
-    p += align256(rows * 16);
-    const size_t nsp = attend_partials(s.nblk);
+    p += z.qstat;
     d.pm = reinterpret_cast<float*>(p);
-    p += align256(rows * nsp * 4);
+    p += z.pml;
     d.pl = reinterpret_cast<float*>(p);
-    p += align256(rows * nsp * 4);
+    p += z.pml;
     d.po = reinterpret_cast<float*>(p);
-    p += align256(rows * nsp * kD * 4);
+    p += z.po;
     d.counters = reinterpret_cast<unsigned*>(p);
-    p += align256(rows * 4);
+    d.n_counters = z.n_counters;
+    p += z.counters;
     d.selmask = reinterpret_cast<uint32_t*>(p);
-    p += align256(rows * s.nblk * 32 * 4);
+    p += z.sel;
     d.sel_ge1 = reinterpret_cast<uint32_t*>(p);
-    p += align256(rows * s.nblk * 32 * 4);
-    d.logu_tab = reinterpret_cast<float*>(p);
     (void)debug;
     return d;
 }
@@ -177,22 +188,35 @@ cudaError_t scan_and_attend(const void* q, bool q_bf16, const uint32_t* codes,
 
 using namespace mp;
 
+namespace mp {
+mp_status validate_decode(const void* q, mp_dtype q_dtype, const uint32_t* codes,
+                          const float* centre, const void* W, mp_dtype w_dtype, const void* keys,
+                          const void* values, mp_dtype kv_dtype, int B, int Hq, int Hkv, int n,
+                          int d, const mp_params* prm, const float* out, DecodeShape* s) {
+    if (!fill_shape(B, Hq, Hkv, n, d, prm, s)) return MP_ERR_INVALID_ARG;
+    if (!valid_dtype(q_dtype) || !valid_dtype(w_dtype) || !valid_dtype(kv_dtype))
+        return MP_ERR_INVALID_ARG;
+    if (!q || !centre || !keys || !values || !out) return MP_ERR_INVALID_ARG;
+    if (s->C > 0 && (!codes || !W)) return MP_ERR_INVALID_ARG;
+    if (!aligned(keys, 16) || !aligned(values, 16) || !aligned(out, 4) ||
+        !aligned(centre, 16) || !aligned(q, q_dtype == MP_BF16 ? 2 : 4) ||
+        (codes && !aligned(codes, 16)))
+        return MP_ERR_INVALID_ARG;
+    if (d != kD) return MP_ERR_UNSUPPORTED;
+    if (!decode_supported(*s, kv_dtype == MP_BF16)) return MP_ERR_UNSUPPORTED;
+    return MP_OK;
+}
+}  // namespace mp
+
 static mp_status check_decode(const void* q, mp_dtype q_dtype, const uint32_t* codes,
                               const float* centre, const void* W, mp_dtype w_dtype,
                               const void* keys, const void* values, mp_dtype kv_dtype, int B,
                               int Hq, int Hkv, int n, int d, const mp_params* prm, float* out,
                               void* workspace, size_t ws_bytes, bool debug, DecodeShape* s) {
-    if (!fill_shape(B, Hq, Hkv, n, d, prm, s)) return MP_ERR_INVALID_ARG;
-    if (!valid_dtype(q_dtype) || !valid_dtype(w_dtype) || !valid_dtype(kv_dtype))
-        return MP_ERR_INVALID_ARG;
-    if (!q || !centre || !keys || !values || !out || !workspace) return MP_ERR_INVALID_ARG;
-    if (s->C > 0 && (!codes || !W)) return MP_ERR_INVALID_ARG;
-    if (!aligned(keys, 16) || !aligned(values, 16) || !aligned(out, 4) ||
-        !aligned(centre, 16) || !aligned(q, q_dtype == MP_BF16 ? 2 : 4) ||
-        !aligned(workspace, 256) || (codes && !aligned(codes, 16)))
-        return MP_ERR_INVALID_ARG;
-    if (d != kD) return MP_ERR_UNSUPPORTED;
-    if (!decode_supported(*s, kv_dtype == MP_BF16)) return MP_ERR_UNSUPPORTED;
+    const mp_status st = validate_decode(q, q_dtype, codes, centre, W, w_dtype, keys, values,
+                                         kv_dtype, B, Hq, Hkv, n, d, prm, out, s);
+    if (st != MP_OK) return st;
+    if (!workspace || !aligned(workspace, 256)) return MP_ERR_INVALID_ARG;
     if (ws_bytes < decode_scratch_bytes(*s, debug)) return MP_ERR_WORKSPACE;
     return MP_OK;
 }
@@ -512,7 +536,8 @@ mp_status mp_debug_select(const void* q, mp_dtype q_dtype, const uint32_t* codes
     e = scan_and_attend(q, q_dtype == MP_BF16, codes, centre, keys, values, kv_dtype == MP_BF16, s,
                         out, ws, stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
-    e = launch_compact_selection(ws.selmask, s.B * s.Hq, s.n, s.nblk, sel_idx, sel_count, stream);
+    e = launch_compact_selection(ws.selmask, s.B * s.Hq, s.n, s.nblk, s.n_sink, s.n_local,
+                                 sel_idx, sel_count, stream);
     if (e != cudaSuccess) return MP_ERR_CUDA;
     if (cnt) {
         if (s.C == 0) {
@@ -525,6 +550,61 @@ mp_status mp_debug_select(const void* q, mp_dtype q_dtype, const uint32_t* codes
         if (e != cudaSuccess) return MP_ERR_CUDA;
     }
     return MP_OK;
+}
+
+mp_status mp_debug_select_buckets(const void* q, mp_dtype q_dtype, const uint32_t* buckets,
+                                  const uint32_t* codes, const float* centre, const void* W,
+                                  mp_dtype w_dtype, const void* keys, const void* values,
+                                  mp_dtype kv_dtype, int B, int Hq, int Hkv, int n, int d,
+                                  const mp_params* prm, float* out, uint32_t* q_bits,
+                                  int32_t* sel_idx, int32_t* sel_count, void* workspace,
+                                  size_t ws_bytes, cudaStream_t stream) {
+    if (!buckets) return MP_ERR_INVALID_ARG;
+    DecodeShape s;
+    // the buckets stand in for the codes in the shared checks (the codes are checked below)
+    const mp_status st = check_decode(q, q_dtype, buckets, centre, W, w_dtype, keys, values,
+                                      kv_dtype, B, Hq, Hkv, n, d, prm, out, workspace, ws_bytes,
+                                      true, &s);
+    if (st != MP_OK) return st;
+    if (s.K > kMaxBucketBits || s.cp) return MP_ERR_UNSUPPORTED;
+    if (!sel_idx || !sel_count || (s.qwords > 0 && !q_bits)) return MP_ERR_INVALID_ARG;
+    const bool tail = s.n_indexed < s.n && s.C > 0;
+    if (tail && (!codes || !aligned(codes, 16))) return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    DecodeScratch ws = carve_decode_scratch(workspace, s, true);
+    if (s.qwords > 0) ws.qbits = q_bits;
+    cudaError_t e = query_encode(q, q_dtype == MP_BF16, centre, W, w_dtype == MP_BF16, s, ws,
+                                 stream);
+    if (e != cudaSuccess) return MP_ERR_CUDA;
+    e = launch_bucket_lookup(buckets, ws.qbits, s, ws.sel_ge1, ws.selmask, stream);
+    if (e != cudaSuccess) return MP_ERR_CUDA;
+    // the same kernels as mp_sampled_attention_buckets
+    if (tail)
+        e = scan_and_attend(q, q_dtype == MP_BF16, codes, centre, keys, values,
+                            kv_dtype == MP_BF16, s, out, ws, stream, s.n_indexed / kKeysPerBlock);
+    else
+        e = launch_attend(q, q_dtype == MP_BF16, centre, keys, values, kv_dtype == MP_BF16, s,
+                          out, ws, stream);
+    if (e != cudaSuccess) return MP_ERR_CUDA;
+    return to_status(launch_compact_selection(ws.selmask, s.B * s.Hq, s.n, s.nblk, s.n_sink,
+                                              s.n_local, sel_idx, sel_count, stream));
+}
+
+mp_status mp_debug_log_inclusion(const float* cosines, int count, int K, int L, float* out,
+                                 cudaStream_t stream) {
+    if (count < 0 || K < 0 || K > 32 || L < 1) return MP_ERR_INVALID_ARG;
+    if (count > 0 && (!cosines || !out || !aligned(cosines, 4) || !aligned(out, 4)))
+        return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    return to_status(launch_log_inclusion(cosines, count, K, L, out, stream));
+}
+
+mp_status mp_debug_wait_expiry(int limit_us, cudaStream_t stream) {
+    if (limit_us < 1 || limit_us > 100000) return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    int* status = device_status_ptr();
+    if (!status) return MP_ERR_CUDA;
+    return to_status(launch_wait_expiry(1000ull * static_cast<unsigned>(limit_us), status, stream));
 }
 
 mp_status mp_codes_unpack(const uint32_t* codes, int B, int Hkv, int n, int K, int L,

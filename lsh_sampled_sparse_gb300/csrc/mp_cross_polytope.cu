@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kCpTableThreads) cp_logu_table_kernel(int K, i
     } else {
         p = cp_quadrature(c, 0, 96, red);
     }
-    if (threadIdx.x == 0) table[i] = log_inclusion_ref(static_cast<float>(p), K, L);
+    if (threadIdx.x == 0) table[i] = log_inclusion_p(static_cast<float>(p), K, L);
 }
 
 // Gauss-Legendre nodes and weights on [-1, 1] by Newton's method on P_n (host, double).

@@ -7,6 +7,8 @@
 // details, algorithm execution), with the inclusion probability of the hash-function-choice
 // section and the exact sink/local set ("static cache") of the system co-design section, whose
 // "recursive attention" merge of partial outputs is the log-sum-exp merge done here.
+#include <algorithm>
+
 #include "mp_internal.cuh"
 
 namespace mp {
@@ -14,60 +16,15 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr float kLogFltMin = -87.336544750553102f;   // log(FLT_MIN)
-constexpr float kPi = 3.14159265358979323846f;
 constexpr int kCombinePitch = 132;                  // floats per (warp, head) partial: o, m, l
 constexpr int kAttendBlocks = kAttendBlockGroup;
 constexpr int kAWarps = 4;                          // attend CTA: 4 warps, 8 half-warps on rows
 static_assert(kAttendBlocks <= kAWarps, "one warp lists each block of an attend CTA");
 constexpr int kAThreads = 32 * kAWarps;
-constexpr int kRing = 4;                            // rows in flight per lane (cp.async ring)
 static_assert(kAThreads == kD, "the attend merge gives one thread to each of the 128 output dims");
 constexpr int kRingDepth = 4;                       // tables in flight per warp in the async scan
 constexpr int kRingMinK = 8, kRingMaxK = 11;        // K range the async scan handles
-constexpr int kLuIntervals = kLogUTableIntervals;   // log u table: cosine grid on [-1, 1]
-
-// 1 / (j + 1) for the binomial-tail series below
-__constant__ float c_inv_next[66] = {
-    1.0f / 1, 1.0f / 2, 1.0f / 3, 1.0f / 4, 1.0f / 5, 1.0f / 6, 1.0f / 7, 1.0f / 8, 1.0f / 9,
-    1.0f / 10, 1.0f / 11, 1.0f / 12, 1.0f / 13, 1.0f / 14, 1.0f / 15, 1.0f / 16, 1.0f / 17,
-    1.0f / 18, 1.0f / 19, 1.0f / 20, 1.0f / 21, 1.0f / 22, 1.0f / 23, 1.0f / 24, 1.0f / 25,
-    1.0f / 26, 1.0f / 27, 1.0f / 28, 1.0f / 29, 1.0f / 30, 1.0f / 31, 1.0f / 32, 1.0f / 33,
-    1.0f / 34, 1.0f / 35, 1.0f / 36, 1.0f / 37, 1.0f / 38, 1.0f / 39, 1.0f / 40, 1.0f / 41,
-    1.0f / 42, 1.0f / 43, 1.0f / 44, 1.0f / 45, 1.0f / 46, 1.0f / 47, 1.0f / 48, 1.0f / 49,
-    1.0f / 50, 1.0f / 51, 1.0f / 52, 1.0f / 53, 1.0f / 54, 1.0f / 55, 1.0f / 56, 1.0f / 57,
-    1.0f / 58, 1.0f / 59, 1.0f / 60, 1.0f / 61, 1.0f / 62, 1.0f / 63, 1.0f / 64, 1.0f / 65,
-    1.0f / 66};
-
-// log u(p) = log P[Binomial(L, p^K) >= 2] in fp32, two branches: directly when L p^K >= 1/2,
-// else as log t_2 + log(1 + sum_{j>=3} t_j / t_2) with t_j the binomial terms; p <= 0 clamps to
-// log(FLT_MIN). log C(L, 2) comes in as log_c2, the series ratios (L - j) / (j + 1) use a
-// reciprocal table (at most 64 terms: below L p^K = 1/2 they shrink at least threefold per step),
-// log p and exp use the fast hardware approximations (errors far below the 1e-3 output
-// tolerance); log1p(-x) stays exact because (L - 2) multiplies it.
-__device__ __forceinline__ float log_inclusion_fast(float p, int K, int L, float log_c2) {
-    if (L < 2) return -INFINITY;
-    if (K == 0) return 0.0f;                       // p^0 = 1 and L >= 2: u = 1
-    if (!(p > 0.0f)) return kLogFltMin;
-    const float lx = static_cast<float>(K) * __logf(p);
-    const float x = __expf(lx);
-    const float Lf = static_cast<float>(L);
-    if (x >= 1.0f) return 0.0f;
-    const float l1 = log1pf(-x);
-    if (Lf * x >= 0.5f) {
-        const float u = 1.0f - __expf(Lf * l1) - Lf * x * __expf((Lf - 1.0f) * l1);
-        return __logf(fmaxf(u, 1.17549435e-38f));
-    }
-    const float r = __fdividef(x, 1.0f - x);
-    float term = 1.0f, tot = 1.0f;
-    const int jmax = min(L, 65);
-    for (int j = 2; j < jmax; ++j) {
-        term *= (Lf - static_cast<float>(j)) * c_inv_next[j] * r;
-        tot += term;
-        if (term < 1e-9f * tot) break;
-    }
-    return log_c2 + 2.0f * lx + (Lf - 2.0f) * l1 + __logf(tot);
-}
+constexpr int kLuIntervals = kLogUTableIntervals;   // cross-polytope log u table: cosine grid
 
 // ------------------------------------------------------------------------------------------------
 // Query encoding: qbit_j = [w_j . q > 0] (the query is not centred), |q| and q.mu for the cosine.
@@ -86,8 +43,7 @@ struct QArgs {
     uint32_t* qmask;
     float4* qstat;
     unsigned* counters;
-    float* logu_tab;
-    int q_bf16, w_bf16, BHq, Hq, G, C, cpad, qwords, n_counters, K, L, qrow_ctas;
+    int q_bf16, w_bf16, BHq, Hq, G, C, cpad, qwords, n_counters;
 };
 
 __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
@@ -95,14 +51,6 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
     __shared__ float Ws[kD][32];                 // this word's 32 hyperplane columns
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     allow_dependents();                          // the scan may start streaming codes meanwhile
-    if (blockIdx.y == a.qrow_ctas) {
-        // the extra row of CTAs fills the log u table on the cosine grid c_i = -1 + 2 i / N
-        for (int i = blockIdx.x * kThreads + tid; i <= kLuIntervals; i += gridDim.x * kThreads) {
-            const float c = fminf(1.0f, -1.0f + 2.0f * static_cast<float>(i) / kLuIntervals);
-            a.logu_tab[i] = log_inclusion_ref(1.0f - acosf(c) / kPi, a.K, a.L);
-        }
-        return;
-    }
     const int wd = blockIdx.x, r0 = blockIdx.y * kQRows;
     const int nq = min(kQRows, a.BHq - r0);
     {
@@ -136,9 +84,14 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
     const int Hkv = a.Hq / a.G;
     if (warp < nq && a.C > 0) {
         const int j = wd * 32 + lane;
-        float s = 0.0f;
-#pragma unroll 16
-        for (int e = 0; e < kD; ++e) s = fmaf(Ws[e][lane], Qs[warp][e], s);
+        // four interleaved partial sums over the 128 dimensions (a short dependency chain)
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 8
+        for (int e = 0; e < kD; e += 4) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s4[i] = fmaf(Ws[e + i][lane], Qs[warp][e + i], s4[i]);
+        }
+        const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         const bool bit = j < a.C && s > 0.0f;
         const uint32_t word = __ballot_sync(0xffffffffu, bit);
         if (lane == 0) a.qbits[static_cast<size_t>(row) * a.qwords + wd] = word;
@@ -182,30 +135,23 @@ struct CArgs {
     int blk0;                                    // first block scanned (grid x + blk0)
 };
 
-// Attend CTA shared memory: [work][cbuf][misc]. The work region holds the CTA's row list, and in
-// the merging CTA up to `merge_cap` staged partial outputs (all of them unless that exceeds
-// 48 KB; the merge then runs in rounds).
+// Attend CTA shared memory: [work][selection words][prefix counts][row keys][cbuf][misc]. The
+// work region holds a round of rcap staged K/V rows, and in the merging CTA up to `merge_cap`
+// staged partial outputs (the merge runs in rounds when a row has more partials).
+constexpr int kAttendRows = 64;                      // rows staged per round of an attend CTA
 struct AttendSmem {
     size_t work, total;
-    int merge_cap;
+    int merge_cap, rcap;
 };
-// Bytes of the per-lane row ring for K/V elements of kv_elem bytes: kRing slots of a K and a V
-// fragment (16 bytes per bf16 fragment, 32 per fp32 one) for each of the CTA's lanes.
-__host__ __device__ constexpr size_t attend_ring_bytes(size_t kv_elem) {
-    return static_cast<size_t>(kRing) * 2 * kv_elem * 8 * kAThreads;
-}
-
 inline AttendSmem attend_smem(int nsp, size_t kv_elem) {
-    constexpr size_t kList = static_cast<size_t>(kAttendBlocks) * kKeysPerBlock * 4;
-    constexpr size_t kRow = static_cast<size_t>(kD) * 4;
-    size_t work = static_cast<size_t>(nsp) * kRow;
-    if (work > 48 * 1024) work = 48 * 1024;
-    if (work < kList) work = kList;
+    (void)nsp;
     AttendSmem m;
-    m.work = work;
-    m.merge_cap = static_cast<int>(work / kRow);
-    m.total = work + static_cast<size_t>(kAWarps) * kCombinePitch * 4 + 64 +
-              attend_ring_bytes(kv_elem);
+    m.rcap = kAttendRows;
+    m.work = static_cast<size_t>(kAttendRows) * 2 * kD * kv_elem;
+    m.merge_cap = static_cast<int>(m.work / (static_cast<size_t>(kD) * 4));
+    m.total = m.work + static_cast<size_t>(kAThreads) * 4 + (kAThreads + 4) * 4 +
+              static_cast<size_t>(kAttendRows) * 4 + static_cast<size_t>(kAWarps) * kCombinePitch * 4 +
+              32;
     return m;
 }
 
@@ -380,33 +326,31 @@ struct AArgs {
     float* po;
     unsigned* counters;
     float* out;
-    const float* logu_tab;
+    const float* logu_tab;                       // cross-polytope log u table; null for SimHash
     int q_bf16, n, nblk, nsb, Hq, Hkv, G, K, L, n_sink, n_local;
     int ncap;                                    // K/V rows per head in memory
     const float* radius;                         // MIPS variant: longest centred key per head
-    int table_only;                              // log u from the table at every cosine
-    float scale, log_c2;
+    float scale;
     int merge_cap;                               // partials staged per merge round
-    int work_bytes;                              // bytes of the list / merge stage region
+    int work_bytes;                              // bytes of the row / merge stage region
+    int rcap;                                    // rows staged per round
 };
 
-// Collide + select: per (1024-key block, sequence x KV head) the selection words
-// S_h = [>= 2 of L tables match] & valid & not T, for every query head h of the group.
+// The scan of one (1024-key block, sequence x KV head) for its GQA group of G query heads,
+// run by all kThreads threads of a CTA: before the query masks exist, let the next kernel be
+// scheduled and start this warp's first tables of codes (an input of the call) into the ring for
+// the ring's K, else into L2; wait for the query encoding; copy the group's query masks into
+// shared memory; per 32-key word (lane) and table, match = AND_b (plane ^ qmask), kept as
+// bit-sliced saturating counters ge1 = (>= 1 match), ge2 = (>= 2 matches); the warps split the L
+// tables and their counters combine in a fixed order. Threads tid < G * 32 return the selection
+// word w = tid % 32 of head tid / 32, S = ge2 & valid & not T, in *sel and the block's T word in
+// *tmask. Shared memory: qneg [cpad][G], gebuf [kWarps][2][G][32], ring (per warp
+// [kRingDepth][K][32]); the CTA is past a barrier on return.
 template <int G>
-__global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
+__device__ __forceinline__ void scan_block(const CArgs& a, int blk, int bg, uint32_t* qneg,
+                                           uint32_t* gebuf, uint32_t* ring, uint32_t* sel,
+                                           uint32_t* tmask) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int blk = blockIdx.x + a.blk0, bg = blockIdx.y;
-    const int b = bg / a.Hkv, g = bg % a.Hkv;
-    const int row0 = b * a.Hq + g * G;          // first query row of this KV head's group
-    uint32_t* qneg = reinterpret_cast<uint32_t*>(smem);                    // [cpad][G]
-    uint32_t* gebuf = qneg + static_cast<size_t>(a.cpad) * G;              // [8][2][G][32]
-    uint32_t* ring = gebuf + kWarps * 2 * G * 32 +                         // [8][depth][K][32]
-                     static_cast<size_t>(warp) * kRingDepth * a.K * kWordsPerBlock;
-
-    // ---- before the query masks exist: let the attend kernel be scheduled (it waits for this
-    //      kernel's completion itself), and start this warp's first tables of codes (an input
-    //      of the call): into the ring for the ring's K, else into L2
     allow_dependents();
     const int t0 = (a.L * warp) / kWarps, t1 = (a.L * (warp + 1)) / kWarps;
     const uint32_t* cb0 =
@@ -426,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     }
     wait_for_predecessor();
 
-    // ---- prologue: the group's query masks (one contiguous piece)
+    // ---- the group's query masks (one contiguous piece)
     {
         const uint4* src = reinterpret_cast<const uint4*>(a.qmask +
                                                           static_cast<size_t>(bg) * a.cpad * G);
@@ -436,30 +380,25 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     cp_async_wait_all();
     __syncthreads();
 
-    // ---- phase 1: per 32-key word (lane), per table, match = AND_b (plane ^ qmask); keep
-    //      bit-sliced saturating counters ge1 = (>= 1 match), ge2 = (>= 2 matches)
     uint32_t ge1[G], ge2[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         ge1[h] = 0u;
         ge2[h] = 0u;
     }
-    {
-        const uint32_t* cb = cb0 + lane;
-        switch (a.K) {
-            case 0:
+    switch (a.K) {
+        case 0:
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    ge1[h] = (t1 - t0 >= 1) ? 0xffffffffu : 0u;
-                    ge2[h] = (t1 - t0 >= 2) ? 0xffffffffu : 0u;
-                }
-                break;
-            case 8: scan_tables_async<G, 8>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
-            case 9: scan_tables_async<G, 9>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
-            case 10: scan_tables_async<G, 10>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
-            case 11: scan_tables_async<G, 11>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
-            default: scan_tables_any<G>(cb, qneg, a.K, t0, t1, ge1, ge2); break;
-        }
+            for (int h = 0; h < G; ++h) {
+                ge1[h] = (t1 - t0 >= 1) ? 0xffffffffu : 0u;
+                ge2[h] = (t1 - t0 >= 2) ? 0xffffffffu : 0u;
+            }
+            break;
+        case 8: scan_tables_async<G, 8>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
+        case 9: scan_tables_async<G, 9>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
+        case 10: scan_tables_async<G, 10>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
+        case 11: scan_tables_async<G, 11>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
+        default: scan_tables_any<G>(cb0 + lane, qneg, a.K, t0, t1, ge1, ge2); break;
     }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
@@ -481,48 +420,49 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
         const uint32_t valid = bits_below(a.n - key0);
         const uint32_t tm =
             (bits_below(a.n_sink - key0) | ~bits_below(a.n - a.n_local - key0)) & valid;
-        const uint32_t s = g2 & valid & ~tm;
-        a.selmask[(static_cast<size_t>(row0 + h) * a.nblk + blk) * 32 + w] = s;
+        *sel = g2 & valid & ~tm;
+        *tmask = tm;
     }
-    __syncthreads();
 }
 
-// A K or V row fragment: the 8 elements [8 hl, 8 hl + 8) a lane of a half-warp holds
-template <typename KV>
-struct RowFrag;
-template <>
-struct RowFrag<__nv_bfloat16> {
-    uint4 k, v;
-    __device__ __forceinline__ void from_pieces(const uint4 (&p)[2]) { k = p[0]; v = p[1]; }
-    __device__ __forceinline__ void unpack(float (&kf)[8], float (&vf)[8]) const {
-        const uint32_t kw[4] = {k.x, k.y, k.z, k.w}, vw[4] = {v.x, v.y, v.z, v.w};
+// Collide + select: per (1024-key block, sequence x KV head) the selection words
+// S_h = [>= 2 of L tables match] & valid & not T, for every query head h of the group.
+template <int G>
+__global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int blk = blockIdx.x + a.blk0, bg = blockIdx.y;
+    const int b = bg / a.Hkv, g = bg % a.Hkv;
+    const int row0 = b * a.Hq + g * G;          // first query row of this KV head's group
+    uint32_t* qneg = reinterpret_cast<uint32_t*>(smem);                    // [cpad][G]
+    uint32_t* gebuf = qneg + static_cast<size_t>(a.cpad) * G;              // [8][2][G][32]
+    uint32_t* ring = gebuf + kWarps * 2 * G * 32 +                         // [8][depth][K][32]
+                     static_cast<size_t>(warp) * kRingDepth * a.K * kWordsPerBlock;
+    uint32_t s = 0u, tm = 0u;
+    scan_block<G>(a, blk, bg, qneg, gebuf, ring, &s, &tm);
+    if (threadIdx.x < G * 32) {
+        const int h = threadIdx.x >> 5, w = threadIdx.x & 31;
+        a.selmask[(static_cast<size_t>(row0 + h) * a.nblk + blk) * 32 + w] = s;
+    }
+}
+
+// The 8 consecutive elements [8 hl, 8 hl + 8) of a staged K or V row as floats.
+__device__ __forceinline__ void load8(const uint8_t* p, const __nv_bfloat16*, float (&f)[8]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw[i]));
-            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[i]));
-            kf[2 * i] = a.x;
-            kf[2 * i + 1] = a.y;
-            vf[2 * i] = b.x;
-            vf[2 * i + 1] = b.y;
-        }
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
     }
-};
-template <>
-struct RowFrag<float> {
-    float4 k0, k1, v0, v1;
-    __device__ __forceinline__ void from_pieces(const uint4 (&p)[4]) {
-        k0 = *reinterpret_cast<const float4*>(&p[0]);
-        k1 = *reinterpret_cast<const float4*>(&p[1]);
-        v0 = *reinterpret_cast<const float4*>(&p[2]);
-        v1 = *reinterpret_cast<const float4*>(&p[3]);
-    }
-    __device__ __forceinline__ void unpack(float (&kf)[8], float (&vf)[8]) const {
-        kf[0] = k0.x; kf[1] = k0.y; kf[2] = k0.z; kf[3] = k0.w;
-        kf[4] = k1.x; kf[5] = k1.y; kf[6] = k1.z; kf[7] = k1.w;
-        vf[0] = v0.x; vf[1] = v0.y; vf[2] = v0.z; vf[3] = v0.w;
-        vf[4] = v1.x; vf[5] = v1.y; vf[6] = v1.z; vf[7] = v1.w;
-    }
-};
+}
+__device__ __forceinline__ void load8(const uint8_t* p, const float*, float (&f)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 16);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
 
 __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned* p, unsigned v) {
     unsigned old;
@@ -538,9 +478,8 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned* p, unsigned
 // the exact set T = [0, n_sink) u [n - n_local, n) with log u = 0, so that the 68 sink/local rows
 // do not pile onto the CTA of the last blocks. Each CTA folds its rows into one partial softmax;
 // the last CTA of each query row merges the row's nsb + 1 partials by log-sum-exp.
-// Each half-warp takes every eighth row; each lane streams its own pieces of the rows (16 bytes
-// of a bf16 K row and of its V row) through a private ring of kRing slots in shared memory with
-// cp.async, so kRing rows per lane are in flight while the current one is reduced.
+// Rows come in rounds of up to rcap: their K and V rows are staged in shared memory with cp.async
+// (one round trip for the whole round), then the 8 half-warps fold them 8 at a time.
 template <typename KV>
 __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -551,157 +490,193 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     const bool exact = sb == a.nsb;              // this CTA takes T
     const int nsp = a.nsb + 1;                   // partials per query row
 
-    int* lidx = reinterpret_cast<int*>(smem);
-    float* cbuf = reinterpret_cast<float*>(smem + a.work_bytes);
-    int* misc = reinterpret_cast<int*>(cbuf + kAWarps * kCombinePitch);  // [0..3] counts, [4]
+    constexpr int kRowBytes = 2 * kD * static_cast<int>(sizeof(KV));     // K then V
+    constexpr int kPieces = kRowBytes / 16;
+    constexpr int kWords = kAttendBlocks * 32;                            // selection words
+    static_assert(kWords == kAThreads, "one selection word per thread");
+    uint8_t* stage = smem;                                    // [rcap] rows; later the merge
+    uint32_t* wsel = reinterpret_cast<uint32_t*>(smem + a.work_bytes);      // [kWords]
+    int* wpre = reinterpret_cast<int*>(wsel + kWords);                      // [kWords + 4]
+    int* rowkey = wpre + kWords + 4;                                        // [rcap]
+    float* cbuf = reinterpret_cast<float*>(rowkey + a.rcap);                // [4][kCombinePitch]
+    int* misc = reinterpret_cast<int*>(cbuf + kAWarps * kCombinePitch);     // [8]
 
     const int half = lane >> 4, hl = lane & 15;
+    const unsigned hmask = 0xffffu << (lane & 16);
     float q8[8], mu8[8];                         // inputs of the call: readable right away
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         q8[i] = load_elem(a.q, a.q_bf16, static_cast<size_t>(row) * kD + 8 * hl + i);
         mu8[i] = a.centre[static_cast<size_t>(bg) * kD + 8 * hl + i];
     }
-    wait_for_predecessor();                      // selection words, query norms, log u table
+    wait_for_predecessor();                      // selection words, query norms
     const float4 st = a.qstat[row];
     const float qn = st.x, qmu = st.y;
     const float rad = a.radius ? a.radius[bg] : 0.0f;   // MIPS: cos = q.(k - mu) / (|q| r)
 
-    // ---- the rows of this CTA: T by arithmetic, or the selected keys of its blocks by a list
+    // ---- the rows of this CTA: T by arithmetic, or the selected keys of its blocks, found
+    //      through the selection words and their prefix counts (no list is materialised)
     const int t_a = min(a.n_sink, a.n), t_b = max(a.n - a.n_local, t_a);
+    const int blk0 = sb * kAttendBlocks;
     int nsel;
     if (exact) {
         nsel = t_a + (a.n - t_b);
     } else {
-        const int blk0 = sb * kAttendBlocks;
         const int nb = min(kAttendBlocks, a.nblk - blk0);
         uint32_t U = 0u;
-        int key0 = 0, excl = 0;
         if (warp < nb) {
+            // the scan already masked its words; selection words from elsewhere (the bucketed
+            // lookup's >= 2 bitmap) need valid & not T here
             const int blk = blk0 + warp;
-            key0 = blk * kKeysPerBlock + lane * 32;
-            {
-                // the scan already masked its words; selection words from elsewhere (the
-                // bucketed lookup's >= 2 bitmap) need valid & not T here
-                const uint32_t valid = bits_below(a.n - key0);
-                const uint32_t tmask =
-                    (bits_below(a.n_sink - key0) | ~bits_below(a.n - a.n_local - key0)) & valid;
-                U = a.selmask[(static_cast<size_t>(row) * a.nblk + blk) * 32 + lane] & valid & ~tmask;
-            }
-            const int c = __popc(U);
-            int incl = c;
+            const int key0 = blk * kKeysPerBlock + lane * 32;
+            const uint32_t valid = bits_below(a.n - key0);
+            const uint32_t tmask =
+                (bits_below(a.n_sink - key0) | ~bits_below(a.n - a.n_local - key0)) & valid;
+            U = a.selmask[(static_cast<size_t>(row) * a.nblk + blk) * 32 + lane] & valid & ~tmask;
+        }
+        wsel[tid] = U;
+        const int c = __popc(U);
+        int incl = c;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            excl = incl - c;
-            if (lane == 31) misc[warp] = incl;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
         }
+        if (lane == 31) misc[warp] = incl;
         __syncthreads();
-        int base = 0;
-        nsel = 0;
-        for (int w = 0; w < nb; ++w) {
-            if (w < warp) base += misc[w];
-            nsel += misc[w];
-        }
-        if (warp < nb) {
-            int pos = base + excl;
-            uint32_t bits = U;
-            while (bits) {
-                const int bit = __ffs(bits) - 1;
-                bits &= bits - 1;
-                lidx[pos++] = key0 + bit;
-            }
-        }
+        int before = 0;
+        for (int w = 0; w < warp; ++w) before += misc[w];
+        wpre[tid] = before + incl - c;
+        if (tid == kAThreads - 1) wpre[kWords] = before + incl;
         __syncthreads();
+        nsel = wpre[kWords];
     }
-    auto key_of = [&](int r) { return exact ? (r < t_a ? r : t_b + (r - t_a)) : lidx[r]; };
+    // key of entry i: T by arithmetic; else the word holding it (the last with wpre <= i) and its
+    // (i - wpre)-th set bit
+    auto key_of = [&](int i) -> int {
+        if (exact) return i < t_a ? i : t_b + (i - t_a);
+        int lo = 0, hi = kWords - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (wpre[mid] <= i) lo = mid;
+            else hi = mid - 1;
+        }
+        const int bit = static_cast<int>(__fns(wsel[lo], 0, i - wpre[lo] + 1));
+        return (blk0 + (lo >> 5)) * kKeysPerBlock + (lo & 31) * 32 + bit;
+    };
 
-    // ---- rows: half-warp hw takes entries hw, hw + 8, ...; each lane streams its own 16-byte
-    //      pieces of the rows through a private cp.async ring of kRing slots in shared memory
+    // ---- rounds of rcap rows: stage them (cp.async, one round trip), then each half-warp folds
+    //      entries hw, hw + 8, ... in batches of 8: partial q.k and |k - mu|^2 over the lane's 8
+    //      dimensions, one reduce-scatter so that lanes 2j, 2j + 1 hold pair j's sums, the
+    //      log-weight s - log u lane-parallel (u in closed form, the cross-polytope table, or 1
+    //      for T), one online-softmax step
     float m = -INFINITY, l = 0.0f, o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = 0.0f;
-    constexpr int kPieces = static_cast<int>(sizeof(KV)) / 2;     // 16-byte pieces per fragment
-    const uint8_t* Kb = reinterpret_cast<const uint8_t*>(a.keys) +
-                        (static_cast<size_t>(bg) * a.ncap * kD + 8 * hl) * sizeof(KV);
-    const uint8_t* Vb = reinterpret_cast<const uint8_t*>(a.values) +
-                        (static_cast<size_t>(bg) * a.ncap * kD + 8 * hl) * sizeof(KV);
-    uint4* ring = reinterpret_cast<uint4*>(smem + a.work_bytes + kAWarps * kCombinePitch * 4 + 64);
+    const uint8_t* Kg = reinterpret_cast<const uint8_t*>(a.keys) +
+                        static_cast<size_t>(bg) * a.ncap * kD * sizeof(KV);
+    const uint8_t* Vg = reinterpret_cast<const uint8_t*>(a.values) +
+                        static_cast<size_t>(bg) * a.ncap * kD * sizeof(KV);
     const bool weighted = !exact && a.K > 0;
     const int hw = 2 * warp + half;
-    auto issue = [&](int k) {                    // entry hw + 8 k into slot k % kRing
-        const int r = hw + 2 * kAWarps * k;
-        if (r < nsel) {
-            const size_t off = static_cast<size_t>(key_of(r)) * kD * sizeof(KV);
-            const int slot = k % kRing;
+    constexpr int kHalves = 2 * kAWarps;
+    for (int base = 0; base < nsel; base += a.rcap) {
+        const int nr = min(a.rcap, nsel - base);
+        if (tid < nr) rowkey[tid] = key_of(base + tid);
+        for (int r = tid + kAThreads; r < nr; r += kAThreads) rowkey[r] = key_of(base + r);
+        __syncthreads();
+        for (int i = tid; i < nr * kPieces; i += kAThreads) {
+            const int r = i / kPieces, pc = i - r * kPieces;
+            const size_t key = static_cast<size_t>(rowkey[r]);
+            const uint8_t* src = (pc < kPieces / 2 ? Kg : Vg) + key * kD * sizeof(KV) +
+                                 16 * (pc % (kPieces / 2));
+            cp_async16(stage + r * kRowBytes + 16 * pc, src);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+        for (int ent = hw; ent < nr; ent += 8 * kHalves) {
+            const int cnt = min(8, (nr - ent + kHalves - 1) / kHalves);
+            float pd[8], pk[8];
 #pragma unroll
-            for (int c = 0; c < kPieces; ++c) {
-                cp_async16(ring + ((slot * 2 + 0) * kPieces + c) * kAThreads + tid, Kb + off + 16 * c);
-                cp_async16(ring + ((slot * 2 + 1) * kPieces + c) * kAThreads + tid, Vb + off + 16 * c);
+            for (int j = 0; j < 8; ++j) {
+                const int r = j < cnt ? ent + j * kHalves : ent;
+                float kf[8];
+                load8(stage + r * kRowBytes + 8 * hl * sizeof(KV), static_cast<const KV*>(nullptr),
+                      kf);
+                float d = 0.0f, k2 = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float x = kf[i] - mu8[i];
+                    k2 = fmaf(x, x, k2);
+                    d = fmaf(q8[i], kf[i], d);
+                }
+                pd[j] = d;
+                pk[j] = k2;
             }
-        }
-        cp_async_commit();
-    };
-    const int nk = (nsel - 2 * warp + 2 * kAWarps - 1) / (2 * kAWarps);   // the warp's iterations
+            // each level keeps half the pairs and adds the partner's copy of them
 #pragma unroll
-    for (int k = 0; k < kRing; ++k) issue(k);
-    for (int k = 0; k < nk; ++k) {
-        cp_async_wait_pending<kRing - 1>();
-        const bool live = hw + 2 * kAWarps * k < nsel;
-        const int slot = k % kRing;
-        RowFrag<KV> f;
-        {
-            uint4 kv[2 * kPieces];
+            for (int lv = 0; lv < 3; ++lv) {
+                const int off = 8 >> lv, nk = 4 >> lv;
+                const bool up = (hl & off) != 0;
 #pragma unroll
-            for (int c = 0; c < kPieces; ++c) {
-                kv[c] = ring[((slot * 2 + 0) * kPieces + c) * kAThreads + tid];
-                kv[kPieces + c] = ring[((slot * 2 + 1) * kPieces + c) * kAThreads + tid];
-            }
-            f.from_pieces(kv);
-        }
-        float kf[8], vf[8];
-        f.unpack(kf, vf);
-        issue(k + kRing);                        // the slot's pieces are in registers now
-        float kb2 = 0.0f, dot = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float dk = kf[i] - mu8[i];
-            kb2 = fmaf(dk, dk, kb2);
-            dot = fmaf(q8[i], kf[i], dot);
-        }
-#pragma unroll
-        for (int sh = 8; sh; sh >>= 1) {
-            kb2 += __shfl_xor_sync(0xffffffffu, kb2, sh);
-            dot += __shfl_xor_sync(0xffffffffu, dot, sh);
-        }
-        if (live) {
-            float lw = 0.0f;
-            if (weighted) {
-                const float den = qn * (a.radius ? rad : sqrtf(kb2));
-                float cs = den > 0.0f ? __fdividef(dot - qmu, den) : 0.0f;
-                cs = fminf(1.0f, fmaxf(-1.0f, cs));
-                if (a.table_only || (cs > -0.9f && cs < 0.999f)) {
-                    const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
-                    const int i = min(static_cast<int>(tt), kLuIntervals - 1);
-                    const float g0 = __ldg(a.logu_tab + i), g1 = __ldg(a.logu_tab + i + 1);
-                    lw = fmaf(tt - static_cast<float>(i), g1 - g0, g0);
-                } else {
-                    lw = log_inclusion_fast(1.0f - acosf(cs) * (1.0f / kPi), a.K, a.L, a.log_c2);
+                for (int i = 0; i < nk; ++i) {
+                    const float sd = up ? pd[i] : pd[i + nk];
+                    const float sk = up ? pk[i] : pk[i + nk];
+                    const float rd = __shfl_xor_sync(hmask, sd, off);
+                    const float rk = __shfl_xor_sync(hmask, sk, off);
+                    pd[i] = (up ? pd[i + nk] : pd[i]) + rd;
+                    pk[i] = (up ? pk[i + nk] : pk[i]) + rk;
                 }
             }
-            const float logit = dot * a.scale - lw;
-            const float mn = fmaxf(m, logit);
-            const float corr = __expf(m - mn);
-            const float pw = __expf(logit - mn);
-            l = l * corr + pw;
+            const float dot = pd[0] + __shfl_xor_sync(hmask, pd[0], 1);
+            const float kb2 = pk[0] + __shfl_xor_sync(hmask, pk[0], 1);
+            const int jl = hl >> 1;
+            float logit = -INFINITY;
+            if (jl < cnt) {
+                float lw = 0.0f;
+                if (weighted) {
+                    const float den = qn * (a.radius ? rad : sqrtf(kb2));
+                    float cs = den > 0.0f ? (dot - qmu) / den : 0.0f;
+                    cs = fminf(1.0f, fmaxf(-1.0f, cs));
+                    if (a.logu_tab) {                    // cross-polytope: p has no closed form
+                        const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
+                        const int ti = min(static_cast<int>(tt), kLuIntervals - 1);
+                        const float g0 = __ldg(a.logu_tab + ti), g1 = __ldg(a.logu_tab + ti + 1);
+                        lw = fmaf(tt - static_cast<float>(ti), g1 - g0, g0);
+                    } else {
+                        lw = log_inclusion_cos(cs, a.K, a.L);   // closed form, per row
+                    }
+                }
+                logit = dot * a.scale - lw;
+            }
+            float bm = logit;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] = fmaf(o[i], corr, pw * vf[i]);
+            for (int sh = 8; sh; sh >>= 1) bm = fmaxf(bm, __shfl_xor_sync(hmask, bm, sh));
+            const float mn = fmaxf(m, bm);
+            const float corr = __expf(m - mn);
+            const float wgt = jl < cnt ? __expf(logit - mn) : 0.0f;
+            float ws = (hl & 1) ? 0.0f : wgt;                    // each pair counted once
+#pragma unroll
+            for (int sh = 8; sh; sh >>= 1) ws += __shfl_xor_sync(hmask, ws, sh);
+            l = fmaf(l, corr, ws);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] *= corr;
+            const int src0 = lane & 16;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float wj = __shfl_sync(hmask, wgt, src0 + 2 * j);
+                if (j < cnt) {
+                    float vf[8];
+                    load8(stage + (ent + j * kHalves) * kRowBytes + (kD + 8 * hl) * sizeof(KV),
+                          static_cast<const KV*>(nullptr), vf);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) o[i] = fmaf(wj, vf[i], o[i]);
+                }
+            }
             m = mn;
         }
+        __syncthreads();                                         // the stage is refilled next
     }
-    cp_async_wait_pending<0>();
 
     // ---- merge the two half-warps, then the warps (fixed order)
     {
@@ -762,14 +737,14 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     //      cp.async, issued before the maximum is known; m and l of the partials are loaded
     //      meanwhile and sc[j] = exp(m_j - M) kept in cbuf. Rounds of kMergeCap partials.
     const int kMergeCap = a.merge_cap;
-    float* stage = reinterpret_cast<float*>(smem);
+    float* mst = reinterpret_cast<float*>(smem);
     float* red = cbuf;                            // [0, 8): reductions
     float* sc = cbuf + 8;                         // scales, kMergeCap at a time
     const size_t rb = static_cast<size_t>(row) * nsp;
     auto stage_round = [&](int j0) {
         const int cnt = min(kMergeCap, nsp - j0);
         const float* src = a.po + (rb + j0) * kD;
-        for (int i = tid; i < cnt * (kD / 4); i += kAThreads) cp_async16(stage + 4 * i, src + 4 * i);
+        for (int i = tid; i < cnt * (kD / 4); i += kAThreads) cp_async16(mst + 4 * i, src + 4 * i);
         cp_async_commit();
     };
     stage_round(0);
@@ -801,7 +776,7 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
         cp_async_wait_pending<0>();
         __syncthreads();                         // staged rows and scales visible to all
 #pragma unroll 8
-        for (int j = 0; j < cnt; ++j) Os = fmaf(sc[j], stage[j * kD + tid], Os);
+        for (int j = 0; j < cnt; ++j) Os = fmaf(sc[j], mst[j * kD + tid], Os);
         __syncthreads();                         // stage and scales are refilled next round
         if (j0 + kMergeCap < nsp) stage_round(j0 + kMergeCap);
     }
@@ -812,8 +787,16 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     float Ls = 0.0f;
 #pragma unroll
     for (int w = 0; w < kAWarps; ++w) Ls += red[4 + w];
-    a.out[static_cast<size_t>(row) * kD + tid] = Ls > 0.0f ? Os / Ls : 0.0f;
+    // a query with a NaN or infinite element has no defined output: NaN, not a silent zero
+    a.out[static_cast<size_t>(row) * kD + tid] =
+        isfinite(qn) ? (Ls > 0.0f ? Os / Ls : 0.0f) : __int_as_float(0x7fc00000);
     if (tid == 0) a.counters[row] = 0u;
+}
+
+// Inspection: log u at given cosines, the function both attend paths evaluate per row.
+__global__ void log_inclusion_kernel(const float* cosines, int count, int K, int L, float* out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < count) out[i] = log_inclusion_cos(cosines[i], K, L);
 }
 
 typedef void (*KernelFn)(const CArgs);
@@ -850,7 +833,6 @@ size_t attend_smem_for(int nblk, bool kv_bf16) {
 
 constexpr size_t kMaxSmem = 232448;   // 227 KB opt-in per CTA
 
-// launch `kern` so that it may be scheduled while the previous kernel in the stream finishes
 }  // namespace
 
 bool decode_supported(const DecodeShape& s, bool kv_bf16) {
@@ -875,7 +857,16 @@ cudaError_t prepare_decode() {
         if (e != cudaSuccess) return e;
     }
     cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, log_inclusion_kernel);
+    if (e != cudaSuccess) return e;
     return cudaFuncGetAttributes(&fa, qencode_kernel);
+}
+
+cudaError_t launch_log_inclusion(const float* cosines, int count, int K, int L, float* out,
+                                 cudaStream_t st) {
+    if (count <= 0) return cudaSuccess;
+    log_inclusion_kernel<<<(count + 255) / 256, 256, 0, st>>>(cosines, count, K, L, out);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, const void* W,
@@ -897,21 +888,14 @@ cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, cons
     qa.C = s.C;
     qa.cpad = s.cpad;
     qa.qwords = s.qwords;
-    qa.n_counters = s.B * s.Hq;
-    qa.logu_tab = ws.logu_tab;
-    qa.K = s.K;
-    qa.L = s.L;
-    qa.qrow_ctas = (qa.BHq + kQRows - 1) / kQRows;
-    const dim3 qgrid(s.qwords > 0 ? s.qwords : 1, qa.qrow_ctas + 1);
+    qa.n_counters = ws.n_counters;
+    const dim3 qgrid(s.qwords > 0 ? s.qwords : 1, (qa.BHq + kQRows - 1) / kQRows);
     qencode_kernel<<<qgrid, kThreads, 0, st>>>(qa);
     return cudaGetLastError();
 }
 
-cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
-                           const float* centre, const void* keys, const void* values,
-                           bool kv_bf16, const DecodeShape& s, float* out,
-                           const DecodeScratch& ws, cudaStream_t st, int blk0) {
-    const int G = s.Hq / s.Hkv;
+namespace {
+CArgs scan_args(const uint32_t* codes, const DecodeShape& s, const DecodeScratch& ws, int blk0) {
     CArgs ca;
     ca.codes = codes;
     ca.qmask = ws.qmask;
@@ -928,6 +912,17 @@ cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
     ca.n_local = s.n_local;
     ca.cblk = s.cblk;
     ca.blk0 = blk0;
+    return ca;
+}
+
+}  // namespace
+
+cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
+                           const float* centre, const void* keys, const void* values,
+                           bool kv_bf16, const DecodeShape& s, float* out,
+                           const DecodeScratch& ws, cudaStream_t st, int blk0) {
+    const int G = s.Hq / s.Hkv;
+    const CArgs ca = scan_args(codes, s, ws, blk0);
     KernelFn scan = pick_collide(G);
     const size_t smem_scan = collide_smem_for(G, s.cpad, s.K);
     if (!scan || smem_scan > kMaxSmem || attend_smem_for(s.nblk, kv_bf16) > kMaxSmem)
@@ -960,8 +955,7 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
     aa.po = ws.po;
     aa.counters = ws.counters;
     aa.out = out;
-    aa.logu_tab = s.logu_ext ? s.logu_ext : ws.logu_tab;
-    aa.table_only = s.logu_ext != nullptr;     // no closed form for p: the table everywhere
+    aa.logu_tab = s.logu_ext;                  // cross-polytope only: p has no closed form
     aa.q_bf16 = q_bf16;
     aa.n = s.n;
     aa.nblk = s.nblk;
@@ -976,11 +970,11 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
     aa.ncap = s.ncap;
     aa.radius = s.radius;
     aa.scale = s.scale;
-    aa.log_c2 = s.L >= 2 ? logf(0.5f * static_cast<float>(s.L) * static_cast<float>(s.L - 1)) : 0.0f;
     {
         const AttendSmem m = attend_smem(attend_partials(s.nblk), kv_bf16 ? 2 : 4);
         aa.merge_cap = m.merge_cap;
         aa.work_bytes = static_cast<int>(m.work);
+        aa.rcap = m.rcap;
     }
     return launch_dependent(attend, dim3(aa.nsb + 1, s.B * s.Hq), dim3(kAThreads), smem_att, st,
                             aa);

@@ -65,7 +65,6 @@ static_assert(kStgPitch == 257, "staging pitch");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffC % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
 
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s: far beyond any real wait
 constexpr int kSign = 0, kMips = 1, kArgmax = 2;         // epilogue modes of the encoder
 constexpr uint32_t kXchOff = 2 * kKeysPerBlock;          // argmax: exchange area after the codes
 static_assert(kXchOff + 2 * 2 * 2 * kTileM * 8 <= kWordsPerBlock * kStgPitch * 4,
@@ -85,52 +84,6 @@ struct EncodeArgs {
 };
 
 // ---- PTX wrappers -----------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Bounded wait: false on timeout (status raised, abort flag set) or when another role aborted.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0u) {
-            if (*abort_flag) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
-                *abort_flag = 1;
-                atomicExch(status, (int)MP_ERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2) {
     asm volatile(
@@ -658,9 +611,30 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
+// The failure path's test hook: one thread waits, with the encoder's bounded wait, on an
+// mbarrier whose phase nothing completes (no arrival, no copy, no MMA), so the wait gives up
+// after limit_ns and raises MP_ERR_TIMEOUT in the status word, as a stalled encoder would.
+__global__ void wait_expiry_kernel(unsigned long long limit_ns, int* status) {
+    __shared__ __align__(8) uint64_t bar_storage;
+    __shared__ int abort_flag;
+    const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(&bar_storage));
+    abort_flag = 0;
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_wait(bar, 0, &abort_flag, status, limit_ns);
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 }  // namespace
 
+cudaError_t launch_wait_expiry(unsigned long long limit_ns, int* status, cudaStream_t st) {
+    wait_expiry_kernel<<<1, 1, 0, st>>>(limit_ns, status);
+    return cudaGetLastError();
+}
+
 cudaError_t prepare_encode_tc() {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, wait_expiry_kernel) != cudaSuccess) return cudaErrorNotSupported;
     for (auto fn : {encode_tc_kernel<kSign>, encode_tc_kernel<kMips>, encode_tc_kernel<kArgmax>}) {
         const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    kSmemBytes);

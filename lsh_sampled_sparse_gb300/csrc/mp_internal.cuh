@@ -13,7 +13,7 @@ constexpr int kKeysPerBlock = MP_KEYS_PER_BLOCK;   // keys per bit-sliced code b
 constexpr int kWordsPerBlock = kKeysPerBlock / 32;  // uint32 words per plane row
 constexpr int kD = 128;                             // the only head dimension supported
 constexpr int kAttendBlockGroup = 4;                // 1024-key blocks per attend CTA
-constexpr int kLogUTableIntervals = 4096;           // log u table over the cosine in [-1, 1]
+constexpr int kLogUTableIntervals = 4096;           // cross-polytope log u table over the cosine
 constexpr int kMaxBucketBits = 12;                  // bucketed tables: at most 2^12 buckets a table
 constexpr int kBucketRanges = 8;                    // key ranges a table's bucket build is split into
 constexpr int kAppendMaxKeys = 64;                  // mp_encode_keys ranges up to this run on CUDA cores
@@ -35,9 +35,9 @@ struct DecodeScratch {
     float* pl;           // [B*Hq][nsp] its sum of weights
     float* po;           // [B*Hq][nsp][128] its weighted value sum
     unsigned* counters;  // [B*Hq] attend CTAs finished, for the last one's merge
+    int n_counters;      // counters the query encoding resets
     uint32_t* selmask;   // [B*Hq][nblk][32] selection words, written by the scan kernel
     uint32_t* sel_ge1;   // [B*Hq][nblk][32] keys hit by >= 1 table (bucketed lookup only)
-    float* logu_tab;     // [kLogUTableIntervals + 1] log u at cosines -1 + 2 i / intervals
 };
 
 struct DecodeShape {
@@ -53,6 +53,12 @@ struct DecodeShape {
 };
 
 size_t decode_scratch_bytes(const DecodeShape& s, bool debug);
+// Shapes, parameters, dtypes, pointers and alignment of a decode call, everything but the
+// workspace (the checks of mp_decode_attention); fills *s on success.
+mp_status validate_decode(const void* q, mp_dtype q_dtype, const uint32_t* codes,
+                          const float* centre, const void* W, mp_dtype w_dtype, const void* keys,
+                          const void* values, mp_dtype kv_dtype, int B, int Hq, int Hkv, int n,
+                          int d, const mp_params* prm, const float* out, DecodeShape* s);
 DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug);
 
 // ---- launchers (each returns the launch error, cudaSuccess otherwise) -------------------------
@@ -82,8 +88,9 @@ cudaError_t launch_encode_append(const void* keys, bool keys_bf16, const float* 
 cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, const void* W,
                            bool w_bf16, const DecodeShape& s, const DecodeScratch& ws,
                            cudaStream_t st);
-// the code scan over blocks [blk0, nblk) (selection words of those blocks), then the attend
-// kernel over every block; cudaErrorNotSupported if it cannot fit a CTA
+// blk0 == 0: the fused scan + gather + attend kernel over every block; blk0 > 0: the code scan
+// over blocks [blk0, nblk) (selection words of those blocks), then the attend kernel over every
+// block. cudaErrorNotSupported if it cannot fit a CTA
 cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
                            const float* centre, const void* keys, const void* values,
                            bool kv_bf16, const DecodeShape& s, float* out,
@@ -106,8 +113,15 @@ cudaError_t launch_bucket_lookup(const uint32_t* buckets, const uint32_t* qbits,
                                  cudaStream_t st);
 cudaError_t prepare_buckets();
 
+// ascending indices of the selection words' keys, masked with the valid keys and not T
 cudaError_t launch_compact_selection(const uint32_t* selmask, int rows, int n, int nblk,
-                                     int32_t* sel_idx, int32_t* sel_count, cudaStream_t st);
+                                     int n_sink, int n_local, int32_t* sel_idx,
+                                     int32_t* sel_count, cudaStream_t st);
+// log u at count cosines, as the decode kernels evaluate it (log_inclusion_cos)
+cudaError_t launch_log_inclusion(const float* cosines, int count, int K, int L, float* out,
+                                 cudaStream_t st);
+// one bounded wait on an mbarrier that nothing completes (the failure path's test hook)
+cudaError_t launch_wait_expiry(unsigned long long limit_ns, int* status, cudaStream_t st);
 cudaError_t launch_collision_counts(const uint32_t* codes, const uint32_t* qbits,
                                     const DecodeShape& s, uint8_t* cnt, cudaStream_t st);
 cudaError_t launch_codes_unpack(const uint32_t* codes, int BH, int n, int K, int L,
@@ -217,9 +231,16 @@ __device__ __forceinline__ void wait_for_predecessor() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// log u(p) = log P[Binomial(L, p^K) >= 2] in fp32 with the accurate library functions, used to
-// fill the per-call table of log u over the cosine; same two-branch definition as below.
-__device__ inline float log_inclusion_ref(float p, int K, int L) {
+// log u(p) = log P[Binomial(L, p^K) >= 2] in fp32: the inclusion probability u = 1 - (1-p^K)^L -
+// L p^K (1-p^K)^(L-1) of the hash-function-choice section of "LSH Sampling...", in the log domain
+// ("don't pick the tallest", section 5, asks for stable probability arithmetic). With x = p^K and
+// lambda = L x: for lambda >= 0.05 directly, u = -expm1(L log1p(-x)) - lambda e^{(L-1) log1p(-x)}
+// (the two terms cancel to lambda^2 / 2 at worst, a factor 40 at lambda = 0.05, so u keeps about
+// 20 correct bits); below, log t_2 + log1p(sum_{j>=3} t_j / t_2) with t_j the binomial terms, whose
+// ratios t_{j+1} / t_j = (L - j) / (j + 1) * x / (1 - x) are then below 0.02: seven terms leave a
+// remainder under 1e-13. p <= 0 (a key that cannot collide) clamps to log(FLT_MIN); L < 2 gives
+// -inf (no key can collide in two tables); K = 0 gives 0 (every key collides in every table).
+__device__ inline float log_inclusion_p(float p, int K, int L) {
     if (L < 2) return -INFINITY;
     if (K == 0) return 0.0f;
     if (!(p > 0.0f)) return -87.336544750553102f;   // log(FLT_MIN)
@@ -228,20 +249,80 @@ __device__ inline float log_inclusion_ref(float p, int K, int L) {
     const float Lf = static_cast<float>(L);
     if (x >= 1.0f) return 0.0f;
     const float l1 = log1pf(-x);
-    if (Lf * x >= 0.5f) {
-        const float u = 1.0f - expf(Lf * l1) - Lf * x * expf((Lf - 1.0f) * l1);
+    const float lam = Lf * x;
+    if (lam >= 0.05f) {
+        const float u = -expm1f(Lf * l1) - lam * expf((Lf - 1.0f) * l1);
         return logf(fmaxf(u, 1.17549435e-38f));
     }
     const float r = x / (1.0f - x);
-    float term = 1.0f, tot = 1.0f;
-    for (int j = 2; j < L; ++j) {
-        term *= static_cast<float>(L - j) / static_cast<float>(j + 1) * r;
-        tot += term;
-        if (term < 1e-9f * tot) break;
+    float term = 1.0f, sum = 0.0f;
+#pragma unroll
+    for (int j = 2; j < 9; ++j) {
+        if (j >= L) break;
+        term *= (Lf - static_cast<float>(j)) * (1.0f / static_cast<float>(j + 1)) * r;
+        sum += term;
     }
-    return logf(0.5f * Lf * (Lf - 1.0f)) + 2.0f * lx + (Lf - 2.0f) * l1 + logf(tot);
+    return logf(0.5f * Lf * (Lf - 1.0f)) + 2.0f * lx + (Lf - 2.0f) * l1 + log1pf(sum);
 }
 
+// log u at the cosine c of q and k - mu. SimHash's bit agreement is p = 1 - arccos(c) / pi
+// ("LSH Sampling...", background, LSH basics), evaluated as arccos(-c) / pi: the same number,
+// without the cancellation of 1 - (1 - small) as c approaches -1.
+__device__ inline float log_inclusion_cos(float c, int K, int L) {
+    return log_inclusion_p(acosf(-c) * 0.318309886183790672f, K, L);
+}
+
+// ---- mbarriers and the bounded wait every spin in this library goes through -----------------
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;   // 4 s: far beyond any real wait
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait: false on timeout (status raised, abort flag set) or when another role aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0u) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicExch(status, (int)MP_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
 // bits of a 32-key word whose offset within the word is below x (x may be out of [0, 32])
 __device__ __forceinline__ uint32_t bits_below(int x) {
     return x <= 0 ? 0u : (x >= 32 ? 0xffffffffu : ((1u << x) - 1u));

@@ -163,14 +163,18 @@ __global__ void __launch_bounds__(kSimtKeys)
 // Inspection kernels
 // ------------------------------------------------------------------------------------------------
 // Per query row: ascending indices of the selected keys from the per-block selection words.
-__global__ void compact_selection_kernel(const uint32_t* selmask, int n, int nblk, int32_t* sel_idx,
-                                         int32_t* sel_count) {
+__global__ void compact_selection_kernel(const uint32_t* selmask, int n, int nblk, int n_sink,
+                                         int n_local, int32_t* sel_idx, int32_t* sel_count) {
     const int row = blockIdx.x, lane = threadIdx.x;
     const uint32_t* m = selmask + static_cast<size_t>(row) * nblk * 32;
     int32_t* out = sel_idx + static_cast<size_t>(row) * n;
     int pos = 0;
     for (int blk = 0; blk < nblk; ++blk) {
-        const uint32_t w = m[blk * 32 + lane];
+        // the scan's words exclude T already; the bucketed lookup's do not
+        const int key0 = blk * kKeysPerBlock + lane * 32;
+        const uint32_t valid = bits_below(n - key0);
+        const uint32_t tm = (bits_below(n_sink - key0) | ~bits_below(n - n_local - key0)) & valid;
+        const uint32_t w = m[blk * 32 + lane] & valid & ~tm;
         const int c = __popc(w);
         int incl = c;
 #pragma unroll
@@ -291,8 +295,10 @@ cudaError_t launch_encode_simt(const void* keys, bool keys_bf16, const float* ce
 }
 
 cudaError_t launch_compact_selection(const uint32_t* selmask, int rows, int n, int nblk,
-                                     int32_t* sel_idx, int32_t* sel_count, cudaStream_t st) {
-    compact_selection_kernel<<<rows, 32, 0, st>>>(selmask, n, nblk, sel_idx, sel_count);
+                                     int n_sink, int n_local, int32_t* sel_idx,
+                                     int32_t* sel_count, cudaStream_t st) {
+    compact_selection_kernel<<<rows, 32, 0, st>>>(selmask, n, nblk, n_sink, n_local, sel_idx,
+                                                  sel_count);
     return cudaGetLastError();
 }
 

@@ -48,8 +48,6 @@ void* scratch_address() {
     return g_scratch_addr[dev];
 }
 
-bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 }  // namespace
 }  // namespace mp
 
@@ -58,42 +56,13 @@ extern "C" mp_status mp_decode_attention_noalloc(
     mp_dtype w_dtype, const void* keys, const void* values, mp_dtype kv_dtype, int B, int Hq,
     int Hkv, int n, int d, const mp_params* prm, float* out, cudaStream_t stream) {
     using namespace mp;
-    // shapes and parameters: the same rules as mp_decode_attention (0 means rejected)
-    const size_t need = mp_decode_workspace_bytes(B, Hq, Hkv, n, d, prm);
-    if (need == 0) return MP_ERR_INVALID_ARG;
-    const bool dt_ok = (q_dtype == MP_F32 || q_dtype == MP_BF16) &&
-                       (w_dtype == MP_F32 || w_dtype == MP_BF16) &&
-                       (kv_dtype == MP_F32 || kv_dtype == MP_BF16);
-    if (!dt_ok) return MP_ERR_INVALID_ARG;
-    if (prm->flags & MP_FLAG_CROSS_POLYTOPE) return MP_ERR_UNSUPPORTED;
+    // the same checks as mp_decode_attention, on the same shape description
     DecodeShape s;
-    s.B = B;
-    s.Hq = Hq;
-    s.Hkv = Hkv;
-    s.n = n;
-    s.d = d;
-    s.K = prm->K;
-    s.L = prm->L;
-    s.C = prm->K * prm->L;
-    s.qwords = (s.C + 31) / 32;
-    s.cpad = (s.C + 3) & ~3;
-    s.nblk = (n + kKeysPerBlock - 1) / kKeysPerBlock;
-    s.ncap = prm->n_capacity > 0 ? prm->n_capacity : n;
-    s.cblk = (s.ncap + kKeysPerBlock - 1) / kKeysPerBlock;
-    s.n_indexed = prm->n_indexed > 0 ? prm->n_indexed : n;
-    s.radius = prm->radius;
-    s.cp = false;
-    s.logu_ext = nullptr;
-    s.n_sink = prm->n_sink;
-    s.n_local = prm->n_local;
-    s.scale = prm->scale > 0.0f ? prm->scale : 1.0f / sqrtf(static_cast<float>(d));
-    if (!q || !centre || !keys || !values || !out) return MP_ERR_INVALID_ARG;
-    if (s.C > 0 && (!codes || !W)) return MP_ERR_INVALID_ARG;
-    if (!is_aligned(keys, 16) || !is_aligned(values, 16) || !is_aligned(out, 4) ||
-        !is_aligned(centre, 16) || !is_aligned(q, q_dtype == MP_BF16 ? 2 : 4) ||
-        (codes && !is_aligned(codes, 16)))
-        return MP_ERR_INVALID_ARG;
-    if (d != kD || !decode_supported(s, kv_dtype == MP_BF16)) return MP_ERR_UNSUPPORTED;
+    const mp_status st = validate_decode(q, q_dtype, codes, centre, W, w_dtype, keys, values,
+                                         kv_dtype, B, Hq, Hkv, n, d, prm, out, &s);
+    if (st != MP_OK) return st;
+    if (s.cp) return MP_ERR_UNSUPPORTED;   // its query encoding and scan are not wired here
+    const size_t need = decode_scratch_bytes(s, false);
     if (need > kScratchBytes) return MP_ERR_WORKSPACE;   // larger than the built-in scratch
     void* base = scratch_address();
     if (!base) return MP_ERR_CUDA;

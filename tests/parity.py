@@ -6,6 +6,8 @@ What is compared, for one (sequence, KV head) unit and each query head of its GQ
   * query sign bits: same rule with |w_j.q| < 1e-5 |w_j| |q|
   * collision counts (saturating at 255) and the sample set S: exact, after replay
   * the output row: max_e |o_gpu - o_ref| / max_e |o_ref| <= 1e-3 (fp32 accumulation on the GPU)
+The bucketed decode is compared the same way, with the oracle's counts taken through its own
+bucket tables (check_unit_buckets).
 """
 from __future__ import annotations
 
@@ -105,6 +107,71 @@ def check_unit(b: int, g: int, *, q, keys, values, centre, W, K, L, n_sink, n_lo
         rep.rows += 1
         rep.max_rel_err = max(rep.max_rel_err, err)
         rep.set_sizes.append(int(r["S"].size))
+    return rep
+
+
+def _replayed_key_codes(b, g, keys, centre, W, K, L, unpacked, radius, rep):
+    kb = O.as64(keys[b, g])
+    mu = O.as64(centre[b, g])
+    if radius is None:
+        _, obits, onear = O.encode_keys(kb, mu, W, K, L)
+    else:
+        _, obits, onear = O.encode_keys_mips(kb, mu, W, float(radius), K, L)
+    if K * L:
+        gbits = unpacked_to_bits(unpacked[b, g], K)
+        kbits, rep.key_flips = O.replay_bits(obits, onear, gbits, what=f"key bits ({b},{g})")
+    else:
+        kbits = obits
+    return O.table_codes(kbits, K, L)
+
+
+def check_unit_buckets(b: int, g: int, *, q, keys, values, centre, W, K, L, n_sink, n_local,
+                       gpu: dict, unpacked, n_indexed=None, radius=None) -> UnitReport:
+    """Compare one (b, g) unit of the bucketed decode (debug_select_buckets' outputs moved to the
+    CPU) with the oracle's bucket route: the oracle builds its own tables (bucket_tables) of the
+    codes of keys [0, n_indexed) after near-tie replay and counts each query's hits from them
+    (bucket_collision_counts); keys of the blocks from n_indexed / 1024 on, which the decode scans,
+    are counted directly. Sample sets exactly, outputs within 1e-3."""
+    rep = UnitReport()
+    kb = O.as64(keys[b, g])
+    vb = O.as64(values[b, g])
+    mu = O.as64(centre[b, g])
+    n, d = kb.shape
+    Hq, Hkv = q.shape[1], keys.shape[1]
+    G = Hq // Hkv
+    C = K * L
+    ni = n if not n_indexed else int(n_indexed)
+    tail0 = (ni // 1024) * 1024 if ni < n else n
+    kcodes = _replayed_key_codes(b, g, keys, centre, W, K, L, unpacked, radius, rep)
+    offsets, members = O.bucket_tables(kcodes[:ni], K, L)
+    T = O.exact_set_mask(n, n_sink, n_local)
+    Wd = O.as64(W)[:d]
+    for h in range(g * G, (g + 1) * G):
+        qv = O.as64(q[b, h])
+        _, qb, qnear = O.encode_query(qv, Wd, K, L)
+        gq = words_to_bits(gpu["q_bits"][b, h], C)
+        qbits, f = O.replay_bits(qb[0], qnear[0], gq, what=f"query bits ({b},{h})")
+        rep.q_flips += f
+        qcode = O.table_codes(qbits[None, :], K, L)[0]
+        cnt_direct = O.collision_counts(kcodes, qcode)
+        cnt_tables = O.bucket_collision_counts(offsets, members, qcode, ni)
+        assert np.array_equal(cnt_tables, cnt_direct[:ni]), "bucket and direct counts differ"
+        cnt = np.concatenate([cnt_tables[:tail0], cnt_direct[tail0:]])
+        S = O.sampled_set(cnt, T)
+        r = O.decode_head(qv, kb, vb, mu, kcodes, qcode, K, L, n_sink, n_local,
+                          radius=None if radius is None else float(radius))
+        assert np.array_equal(r["S"], S)
+        cnt_gpu = int(gpu["sel_count"][b, h])
+        got_S = np.asarray(gpu["sel_idx"][b, h][:cnt_gpu], dtype=np.int64)
+        assert np.array_equal(got_S, S), (
+            f"bucketed sample set differs at ({b},{h}): gpu {cnt_gpu} keys, oracle {S.size}; "
+            f"only gpu {np.setdiff1d(got_S, S)[:8].tolist()}, "
+            f"only oracle {np.setdiff1d(S, got_S)[:8].tolist()}")
+        err = row_rel_err(gpu["out"][b, h], r["o"])
+        assert err <= OUT_REL_TOL, f"bucketed output ({b},{h}) max relative error {err:.3e}"
+        rep.rows += 1
+        rep.max_rel_err = max(rep.max_rel_err, err)
+        rep.set_sizes.append(int(S.size))
     return rep
 
 

@@ -13,7 +13,7 @@ blocks, and that decode must select exactly what the scan selects.
 import pytest
 import torch
 
-from tests.parity import check_unit
+from tests.parity import check_unit, check_unit_buckets
 from workloads import make_hyperplanes, make_layer, small_workload
 
 pytestmark = pytest.mark.gpu
@@ -80,11 +80,18 @@ def test_spare_capacity_decodes_like_the_contiguous_cache(mp, dt):
     torch.cuda.synchronize()
     assert torch.equal(out, want)
     if dt == BF:
+        # the bucketed decode on the capacity layout equals the one on the contiguous cache
         buckets = mp.build_buckets(codes_c, wl.B, wl.Hkv, wl.n, wl.K, wl.L, n_capacity=cap)
         mp.encode_query(x["q"], centre_c, W, kc.shape, *args, ws, n=wl.n)
         mp.sampled_attention_buckets(x["q"], buckets, centre_c, kc, vc, *args, out, ws, n=wl.n)
+        b_contig = mp.build_buckets(codes, wl.B, wl.Hkv, wl.n, wl.K, wl.L)
+        want_b = torch.empty_like(want)
+        ws2 = _decode_ws(mp, wl, wl.n)
+        mp.encode_query(x["q"], centre, W, x["keys"].shape, *args, ws2)
+        mp.sampled_attention_buckets(x["q"], b_contig, centre, x["keys"], x["values"], *args,
+                                     want_b, ws2)
         torch.cuda.synchronize()
-        assert torch.equal(out, want)
+        assert torch.equal(out, want_b)
     assert mp.device_status() == 0
 
 
@@ -139,10 +146,11 @@ def test_fp32_appends_equal_a_full_build(mp):
     assert torch.equal(got, want)
 
 
-@pytest.mark.parametrize("n0", [2500, 2048, 3100])
-def test_bucket_tables_plus_appended_tail_select_like_the_scan(mp, n0):
-    # tables built for the prompt (a ragged block, a block boundary, or all keys), keys appended
-    # since found by the scan of their blocks: the selection, hence the output, equals the scan's
+@pytest.mark.parametrize("n0", [2500, 2048, 3100, 700])
+def test_bucket_tables_plus_appended_tail_against_the_oracle(mp, n0):
+    # tables built for the prompt (a ragged block, a block boundary, all keys, or less than one
+    # block), keys appended since found by the scan of their blocks: the oracle's bucket route
+    # over the first n0 keys plus direct counts for the scanned blocks gives the same sets
     wl = small_workload(B=2, Hq=8, Hkv=2, n=3100)
     cap = 4000
     steps = [(n0, wl.n)] if n0 < wl.n else []
@@ -151,13 +159,22 @@ def test_bucket_tables_plus_appended_tail_select_like_the_scan(mp, n0):
     q = x["q"].cuda()
     args = (wl.K, wl.L, wl.n_sink, wl.n_local)
     ws = _decode_ws(mp, wl, wl.n)
-    out_scan = torch.empty(wl.B, wl.Hq, wl.d, dtype=torch.float32, device="cuda")
-    out_buck = torch.empty_like(out_scan)
-    mp.encode_query(q, centre, W, kc.shape, *args, ws, n=wl.n)
-    mp.sampled_attention(q, codes, centre, kc, vc, *args, out_scan, ws, n=wl.n)
+    out_buck = torch.empty(wl.B, wl.Hq, wl.d, dtype=torch.float32, device="cuda")
     mp.encode_query(q, centre, W, kc.shape, *args, ws, n=wl.n)
     mp.sampled_attention_buckets(q, buckets, centre, kc, vc, *args, out_buck, ws, codes=codes,
                                  n=wl.n, n_indexed=n0)
+    dbg = mp.debug_select_buckets(q, buckets, codes, centre, W, kc, vc, *args, n=wl.n,
+                                  n_indexed=n0)
+    scan = mp.debug_select(q, codes, centre, W, kc, vc, *args, n=wl.n, counts=False)
+    unpacked = mp.codes_unpack(codes, wl.B, wl.Hkv, cap, wl.K, wl.L)[:, :, :wl.n]
     torch.cuda.synchronize()
     assert mp.device_status() == 0
-    assert torch.equal(out_scan, out_buck)
+    assert torch.equal(out_buck, dbg["out"])
+    assert torch.equal(dbg["sel_idx"], scan["sel_idx"])
+    gpu = {k: v.cpu().numpy() for k, v in dbg.items()}
+    for b in range(wl.B):
+        for g in range(wl.Hkv):
+            check_unit_buckets(b, g, q=x["q"], keys=x["keys"], values=x["values"],
+                               centre=centre.cpu(), W=W.cpu(), K=wl.K, L=wl.L, n_sink=wl.n_sink,
+                               n_local=wl.n_local, gpu=gpu, unpacked=unpacked.cpu().numpy(),
+                               n_indexed=n0)

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle as O
-from tests.parity import check_unit
+from tests.parity import check_unit, row_rel_err
 from workloads import make_hyperplanes, make_layer, small_workload
 
 pytestmark = pytest.mark.gpu
@@ -73,7 +73,7 @@ def test_mips_decode_matches_the_oracle(mp, shape, tensor_cores):
     assert flips <= 1e-5 * wl.B * wl.Hkv * wl.n * wl.C
 
 
-def test_mips_ranges_equal_a_full_encode_and_buckets_equal_the_scan(mp):
+def test_mips_ranges_equal_a_full_encode_and_buckets_select_like_the_scan(mp):
     wl = small_workload(B=2, Hq=8, Hkv=2, n=2600)
     xc = {k: v.cuda() for k, v in make_layer(wl).items()}
     W = _w_aug(wl).cuda()
@@ -101,9 +101,19 @@ def test_mips_ranges_equal_a_full_encode_and_buckets_equal_the_scan(mp):
     mp.encode_query(xc["q"], centre, W, xc["keys"].shape, *args, ws, radius=radius)
     mp.sampled_attention_buckets(xc["q"], buckets, centre, xc["keys"], xc["values"], *args,
                                  out_buck, ws, radius=radius)
+    # the two retrievals select the same sets; the gathers of those sets agree to rounding
+    sel_s = mp.debug_select(xc["q"], full, centre, W, xc["keys"], xc["values"], *args,
+                            counts=False, radius=radius)
+    sel_b = mp.debug_select_buckets(xc["q"], buckets, full, centre, W, xc["keys"], xc["values"],
+                                    *args, radius=radius)
     torch.cuda.synchronize()
     assert mp.device_status() == 0
-    assert torch.equal(out_scan, out_buck)
+    assert torch.equal(sel_s["sel_idx"], sel_b["sel_idx"])
+    assert torch.equal(out_buck, sel_b["out"]) and torch.equal(out_scan, sel_s["out"])
+    gs, gb = out_scan.cpu().numpy(), out_buck.cpu().numpy()
+    for b in range(wl.B):
+        for h in range(wl.Hq):
+            assert row_rel_err(gb[b, h], gs[b, h].astype(np.float64)) <= 1e-4
     # the variant samples differently from the plain cosine on the same keys
     plain = mp.decode_attention(xc["q"], mp.build_tables(xc["keys"], centre, W[:wl.d].contiguous(),
                                                          wl.K, wl.L),

@@ -202,6 +202,73 @@ def test_graph_capture_replays_the_same_step(mp):
 
 
 # ------------------------------------------------------------------------------------------------
+# log u as the kernels evaluate it, against the oracle's fp64 binomial tail
+# ------------------------------------------------------------------------------------------------
+LOGU_ABS, LOGU_REL = 1e-4, 1e-6      # |log u_gpu - log u| <= 1e-4 + 1e-6 |log u|, c in (-1, 1]
+
+
+@pytest.mark.parametrize("K,L", [(8, 75), (9, 120), (10, 150), (11, 300), (2, 3)])
+def test_log_inclusion_matches_the_oracle_over_the_cosine(mp, K, L):
+    # the function every selected key's weight goes through ("LSH Sampling...", method details,
+    # the u_i formula), at 10^4 grid cosines, 4,000 random ones and the ends of the range
+    rng = np.random.default_rng(400 + K)
+    c = np.concatenate([-1.0 + 2.0 * np.arange(1, 10001) / 10000.0, rng.uniform(-1, 1, 4000),
+                        1.0 - np.logspace(-7, -1, 200), -1.0 + np.logspace(-6, -1, 200)])
+    c32 = torch.tensor(c, dtype=torch.float32)
+    got = mp.debug_log_inclusion(c32.cuda(), K, L).cpu().double().numpy()
+    cc = c32.double().numpy()                       # both sides at the same fp32 cosines
+    p = 1.0 - np.arccos(cc) / np.pi
+    want = O.log_inclusion_probability(p, K, L)
+    err = np.abs(got - want)
+    bound = LOGU_ABS + LOGU_REL * np.abs(want)
+    worst = int(np.argmax(err / bound))
+    assert np.all(err <= bound), (f"c = {cc[worst]!r}: gpu {got[worst]!r}, oracle "
+                                  f"{want[worst]!r}")
+    # c = -1: p = 0, no collision is possible; the GPU clamps to log(FLT_MIN)
+    at_m1 = mp.debug_log_inclusion(torch.tensor([-1.0], device="cuda"), K, L).item()
+    assert at_m1 == pytest.approx(np.log(np.finfo(np.float32).tiny), rel=1e-6)
+
+
+def test_log_inclusion_degenerate_parameters(mp):
+    c = torch.linspace(-0.99, 1.0, 50, device="cuda")
+    assert torch.all(mp.debug_log_inclusion(c, 0, 4) == 0.0)          # K = 0: u = 1
+    assert torch.all(torch.isneginf(mp.debug_log_inclusion(c, 10, 1)))  # L = 1: u = 0
+
+
+def test_nan_in_a_query_gives_a_nan_row_and_leaves_the_others(mp):
+    wl = small_workload(B=2, Hq=8, Hkv=2, n=5000, index=306)
+    x = {k: v.cuda() for k, v in make_layer(wl).items()}
+    W = make_hyperplanes(wl).cuda()
+    c = mp.key_mean(x["keys"])
+    codes = mp.build_tables(x["keys"], c, W, wl.K, wl.L)
+    args = (wl.K, wl.L, wl.n_sink, wl.n_local)
+    clean = mp.decode_attention(x["q"], codes, c, W, x["keys"], x["values"], *args)
+    buckets = mp.build_buckets(codes, wl.B, wl.Hkv, wl.n, wl.K, wl.L)
+    q = x["q"].clone()
+    q[1, 5, 17] = float("nan")
+    ws = torch.empty(mp.decode_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.n, wl.d, *args),
+                     dtype=torch.uint8, device="cuda")
+    scan = mp.decode_attention(q, codes, c, W, x["keys"], x["values"], *args)
+    buck = torch.empty_like(scan)
+    mp.encode_query(q, c, W, x["keys"].shape, *args, ws)
+    mp.sampled_attention_buckets(q, buckets, c, x["keys"], x["values"], *args, buck, ws)
+    torch.cuda.synchronize()
+    assert mp.device_status() == 0                     # not a device-side failure
+    keep = torch.ones(wl.B, wl.Hq, dtype=torch.bool)
+    keep[1, 5] = False
+    for out in (scan, buck):
+        assert torch.all(torch.isnan(out[1, 5]))
+        assert torch.all(torch.isfinite(out[keep.cuda()]))
+    # the other rows keep their values; the NaN row's own selection changes the group's union
+    # of rows, hence the order of some sums, so only up to rounding
+    got, want = scan.cpu().numpy(), clean.cpu().numpy()
+    for b in range(wl.B):
+        for hh in range(wl.Hq):
+            if keep[b, hh]:
+                assert row_rel_err(got[b, hh], want[b, hh].astype(np.float64)) <= 1e-5
+
+
+# ------------------------------------------------------------------------------------------------
 # Full-size workloads: the whole layer runs on the GPU in the benchmark's launch configuration,
 # the oracle checks sampled (sequence, KV head) units.
 # ------------------------------------------------------------------------------------------------
