@@ -194,9 +194,12 @@ MP_API size_t mp_decode_workspace_bytes(int B, int Hq, int Hkv, int n, int d,
  *   p_i    = 1 - arccos(q.(k_i - mu) / (|q| |k_i - mu|)) / pi
  *   u_i    = 1 - (1 - p_i^K)^L - L p_i^K (1 - p_i^K)^(L-1)
  *   out    = softmax([s_S - log u_S, s_T]) . [V_S, V_T],   s = scale * q.k_i  (raw keys)
- * log u_i is evaluated for every selected key in closed form, in fp32, in the log domain: directly
- * when L p^K >= 1/2, else as the binomial tail series from its second term (mp_debug_log_inclusion
- * returns the same function). The softmax over S and T is computed in pieces of 1024 keys and
+ * log u is a closed form, evaluated in fp32 in the log domain: directly when L p^K >= 0.05, else
+ * as the binomial tail series from its second term. The query encoding tabulates it per call at
+ * the 4097 cosines -1 + 2 i / 4096; a selected key takes the linear interpolation of that table
+ * wherever the chord of its interval lies within 2e-5 of the closed form at the interval's
+ * midpoint, and the closed form itself elsewhere (mp_debug_log_inclusion returns exactly this
+ * evaluation). The softmax over S and T is computed in pieces of 1024 keys and
  * merged by log-sum-exp (the "recursive attention" merge of the system co-design section). If S
  * and T are both empty the output row is zero. Zero-length q or k - mu gives cosine 0 (p = 1/2).
  * A query row with a NaN or infinite element gets a NaN output row; the other rows are unaffected
@@ -353,8 +356,9 @@ MP_API mp_status mp_debug_select_buckets(const void* q, mp_dtype q_dtype, const 
                                          uint32_t* q_bits, int32_t* sel_idx, int32_t* sel_count,
                                          void* workspace, size_t ws_bytes, cudaStream_t stream);
 
-/* log u at each of `count` cosines c (float32 device arrays cosines -> out), evaluated by the
- * device function the decode kernels apply to every selected key of the SimHash codes: p = 1 -
+/* log u at each of `count` cosines c (float32 device arrays cosines -> out), evaluated as the
+ * decode kernels evaluate it for every selected key of the SimHash codes (the per-call table and
+ * the closed form where the table is not used, as mp_decode_attention describes): p = 1 -
  * arccos(c) / pi, u = P[Binomial(L, p^K) >= 2] ("LSH Sampling...", method details, the u_i formula),
  * in fp32 in the log domain; p = 0 gives log(FLT_MIN), L = 1 gives -inf. For checking that
  * evaluation against a reference. Errors: MP_ERR_INVALID_ARG (count < 0, K outside [0, 32],

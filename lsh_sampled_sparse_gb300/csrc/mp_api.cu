@@ -111,10 +111,10 @@ int device_sm_count() {
 
 // Decode workspace, in order (each piece 256-byte aligned): query bits, query masks, query
 // norms, the attend kernel's partials, merge counters, selection words, the bucketed lookup's
-// >= 1 bitmap.
+// >= 1 bitmap, the table of log u over the cosine.
 namespace {
 struct ScratchSizes {
-    size_t qbits, qmask, qstat, pml, po, counters, sel;
+    size_t qbits, qmask, qstat, pml, po, counters, sel, tab;
     int n_counters;
 };
 ScratchSizes scratch_sizes(const DecodeShape& s) {
@@ -129,6 +129,7 @@ ScratchSizes scratch_sizes(const DecodeShape& s) {
     z.n_counters = static_cast<int>(rows);
     z.counters = align256(static_cast<size_t>(z.n_counters) * 4);
     z.sel = align256(rows * s.nblk * 32 * 4);
+    z.tab = align256((kLogUTableIntervals + 1) * 4);
     return z;
 }
 }  // namespace
@@ -136,7 +137,7 @@ ScratchSizes scratch_sizes(const DecodeShape& s) {
 size_t decode_scratch_bytes(const DecodeShape& s, bool debug) {
     const ScratchSizes z = scratch_sizes(s);
     (void)debug;                                         // the debug path needs nothing more
-    return z.qbits + z.qmask + z.qstat + 2 * z.pml + z.po + z.counters + 2 * z.sel;
+    return z.qbits + z.qmask + z.qstat + 2 * z.pml + z.po + z.counters + 2 * z.sel + z.tab;
 }
 
 DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug) {
@@ -161,6 +162,8 @@ DecodeScratch carve_decode_scratch(void* ws, const DecodeShape& s, bool debug) {
     d.selmask = reinterpret_cast<uint32_t*>(p);
     p += z.sel;
     d.sel_ge1 = reinterpret_cast<uint32_t*>(p);
+    p += z.sel;
+    d.logu_tab = reinterpret_cast<float*>(p);
     (void)debug;
     return d;
 }

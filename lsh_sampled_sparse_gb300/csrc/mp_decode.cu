@@ -24,7 +24,7 @@ constexpr int kAThreads = 32 * kAWarps;
 static_assert(kAThreads == kD, "the attend merge gives one thread to each of the 128 output dims");
 constexpr int kRingDepth = 4;                       // tables in flight per warp in the async scan
 constexpr int kRingMinK = 8, kRingMaxK = 11;        // K range the async scan handles
-constexpr int kLuIntervals = kLogUTableIntervals;   // cross-polytope log u table: cosine grid
+constexpr int kLuIntervals = kLogUTableIntervals;   // log u tables: cosine grid intervals
 
 // ------------------------------------------------------------------------------------------------
 // Query encoding: qbit_j = [w_j . q > 0] (the query is not centred), |q| and q.mu for the cosine.
@@ -43,7 +43,8 @@ struct QArgs {
     uint32_t* qmask;
     float4* qstat;
     unsigned* counters;
-    int q_bf16, w_bf16, BHq, Hq, G, C, cpad, qwords, n_counters;
+    float* logu_tab;                             // filled by the extra row of CTAs
+    int q_bf16, w_bf16, BHq, Hq, G, C, cpad, qwords, n_counters, K, L, qrow_ctas;
 };
 
 __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
@@ -51,6 +52,12 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
     __shared__ float Ws[kD][32];                 // this word's 32 hyperplane columns
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     allow_dependents();                          // the scan may start streaming codes meanwhile
+    if (blockIdx.y == a.qrow_ctas) {
+        // the extra row of CTAs: the attend kernel's table of log u over the cosine
+        for (int i = blockIdx.x * kThreads + tid; i <= kLuIntervals; i += gridDim.x * kThreads)
+            a.logu_tab[i] = log_inclusion_entry(i, a.K, a.L);
+        return;
+    }
     const int wd = blockIdx.x, r0 = blockIdx.y * kQRows;
     const int nq = min(kQRows, a.BHq - r0);
     {
@@ -326,7 +333,8 @@ struct AArgs {
     float* po;
     unsigned* counters;
     float* out;
-    const float* logu_tab;                       // cross-polytope log u table; null for SimHash
+    const float* logu_tab;                       // log u over the cosine (SimHash: per call)
+    int table_only;                              // cross-polytope: the table at every cosine
     int q_bf16, n, nblk, nsb, Hq, Hkv, G, K, L, n_sink, n_local;
     int ncap;                                    // K/V rows per head in memory
     const float* radius;                         // MIPS variant: longest centred key per head
@@ -568,8 +576,8 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     // ---- rounds of rcap rows: stage them (cp.async, one round trip), then each half-warp folds
     //      entries hw, hw + 8, ... in batches of 8: partial q.k and |k - mu|^2 over the lane's 8
     //      dimensions, one reduce-scatter so that lanes 2j, 2j + 1 hold pair j's sums, the
-    //      log-weight s - log u lane-parallel (u in closed form, the cross-polytope table, or 1
-    //      for T), one online-softmax step
+    //      log-weight s - log u lane-parallel (log u from the per-call table or its closed
+    //      form, the cross-polytope table, or 0 for T), one online-softmax step
     float m = -INFINITY, l = 0.0f, o[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i] = 0.0f;
@@ -638,13 +646,13 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
                     const float den = qn * (a.radius ? rad : sqrtf(kb2));
                     float cs = den > 0.0f ? (dot - qmu) / den : 0.0f;
                     cs = fminf(1.0f, fmaxf(-1.0f, cs));
-                    if (a.logu_tab) {                    // cross-polytope: p has no closed form
+                    if (a.table_only) {                  // cross-polytope: p has no closed form
                         const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
                         const int ti = min(static_cast<int>(tt), kLuIntervals - 1);
                         const float g0 = __ldg(a.logu_tab + ti), g1 = __ldg(a.logu_tab + ti + 1);
                         lw = fmaf(tt - static_cast<float>(ti), g1 - g0, g0);
                     } else {
-                        lw = log_inclusion_cos(cs, a.K, a.L);   // closed form, per row
+                        lw = log_inclusion_at(cs, a.logu_tab, a.K, a.L);
                     }
                 }
                 logit = dot * a.scale - lw;
@@ -793,10 +801,14 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     if (tid == 0) a.counters[row] = 0u;
 }
 
-// Inspection: log u at given cosines, the function both attend paths evaluate per row.
+// Inspection: log u at given cosines exactly as the attend kernel evaluates it for SimHash codes
+// (the per-call table, here rebuilt in shared memory, and the closed form where it is not used).
 __global__ void log_inclusion_kernel(const float* cosines, int count, int K, int L, float* out) {
+    __shared__ float tab[kLuIntervals + 1];      // the table the query encoding fills per call
+    for (int i = threadIdx.x; i <= kLuIntervals; i += blockDim.x) tab[i] = log_inclusion_entry(i, K, L);
+    __syncthreads();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < count) out[i] = log_inclusion_cos(cosines[i], K, L);
+    if (i < count) out[i] = log_inclusion_at(cosines[i], tab, K, L);
 }
 
 typedef void (*KernelFn)(const CArgs);
@@ -889,7 +901,11 @@ cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, cons
     qa.cpad = s.cpad;
     qa.qwords = s.qwords;
     qa.n_counters = ws.n_counters;
-    const dim3 qgrid(s.qwords > 0 ? s.qwords : 1, (qa.BHq + kQRows - 1) / kQRows);
+    qa.logu_tab = ws.logu_tab;
+    qa.K = s.K;
+    qa.L = s.L;
+    qa.qrow_ctas = (qa.BHq + kQRows - 1) / kQRows;
+    const dim3 qgrid(s.qwords > 0 ? s.qwords : 1, qa.qrow_ctas + 1);
     qencode_kernel<<<qgrid, kThreads, 0, st>>>(qa);
     return cudaGetLastError();
 }
@@ -955,7 +971,8 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
     aa.po = ws.po;
     aa.counters = ws.counters;
     aa.out = out;
-    aa.logu_tab = s.logu_ext;                  // cross-polytope only: p has no closed form
+    aa.logu_tab = s.logu_ext ? s.logu_ext : ws.logu_tab;
+    aa.table_only = s.logu_ext != nullptr;     // cross-polytope: p has no closed form
     aa.q_bf16 = q_bf16;
     aa.n = s.n;
     aa.nblk = s.nblk;

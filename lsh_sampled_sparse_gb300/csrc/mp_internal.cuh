@@ -13,7 +13,7 @@ constexpr int kKeysPerBlock = MP_KEYS_PER_BLOCK;   // keys per bit-sliced code b
 constexpr int kWordsPerBlock = kKeysPerBlock / 32;  // uint32 words per plane row
 constexpr int kD = 128;                             // the only head dimension supported
 constexpr int kAttendBlockGroup = 4;                // 1024-key blocks per attend CTA
-constexpr int kLogUTableIntervals = 4096;           // cross-polytope log u table over the cosine
+constexpr int kLogUTableIntervals = 4096;           // log u tables over the cosine: intervals
 constexpr int kMaxBucketBits = 12;                  // bucketed tables: at most 2^12 buckets a table
 constexpr int kBucketRanges = 8;                    // key ranges a table's bucket build is split into
 constexpr int kAppendMaxKeys = 64;                  // mp_encode_keys ranges up to this run on CUDA cores
@@ -38,6 +38,7 @@ struct DecodeScratch {
     int n_counters;      // counters the query encoding resets
     uint32_t* selmask;   // [B*Hq][nblk][32] selection words, written by the scan kernel
     uint32_t* sel_ge1;   // [B*Hq][nblk][32] keys hit by >= 1 table (bucketed lookup only)
+    float* logu_tab;     // [kLogUTableIntervals + 1] log_inclusion_entry(i), filled per call
 };
 
 struct DecodeShape {
@@ -88,9 +89,9 @@ cudaError_t launch_encode_append(const void* keys, bool keys_bf16, const float* 
 cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, const void* W,
                            bool w_bf16, const DecodeShape& s, const DecodeScratch& ws,
                            cudaStream_t st);
-// blk0 == 0: the fused scan + gather + attend kernel over every block; blk0 > 0: the code scan
-// over blocks [blk0, nblk) (selection words of those blocks), then the attend kernel over every
-// block. cudaErrorNotSupported if it cannot fit a CTA
+// The code scan over blocks [blk0, nblk) (selection words of those blocks; every block when
+// blk0 == 0), then the attend kernel over every block. cudaErrorNotSupported if it cannot fit a
+// CTA
 cudaError_t launch_collide(const void* q, bool q_bf16, const uint32_t* codes,
                            const float* centre, const void* keys, const void* values,
                            bool kv_bf16, const DecodeShape& s, float* out,
@@ -270,6 +271,44 @@ __device__ inline float log_inclusion_p(float p, int K, int L) {
 // without the cancellation of 1 - (1 - small) as c approaches -1.
 __device__ inline float log_inclusion_cos(float c, int K, int L) {
     return log_inclusion_p(acosf(-c) * 0.318309886183790672f, K, L);
+}
+
+// The attend kernel's log u for SimHash keys: linear interpolation in a per-call table of the
+// closed form at the cosines -1 + 2 i / N (N = kLogUTableIntervals), on every interval where the
+// chord stays within kLogUTableTol of the closed form; the closed form itself elsewhere.
+// Linear interpolation errs most near an interval's midpoint, by about h^2 |f''| / 8, so the gap
+// there measures it. Where log u bends sharply (the cosine near +-1, or many bits and few
+// tables) the gap is larger and those intervals keep the closed form.
+constexpr float kLogUTableTol = 2e-5f;
+
+__device__ __forceinline__ float log_inclusion_grid(float i, int K, int L) {
+    return log_inclusion_cos(fminf(1.0f, -1.0f + 2.0f * i / kLogUTableIntervals), K, L);
+}
+
+// Entry i of the table: log u at the cosine -1 + 2 i / N, or NaN when an interval it bounds is
+// not interpolated (every cosine of such an interval then takes the closed form).
+__device__ inline float log_inclusion_entry(int i, int K, int L) {
+    const float fi = log_inclusion_grid(static_cast<float>(i), K, L);
+    for (int j = i - 1; j <= i; ++j) {
+        if (j < 0 || j >= kLogUTableIntervals) continue;
+        const float fa = j == i ? fi : log_inclusion_grid(static_cast<float>(j), K, L);
+        const float fb = j == i ? log_inclusion_grid(static_cast<float>(j + 1), K, L) : fi;
+        const float fm = log_inclusion_grid(static_cast<float>(j) + 0.5f, K, L);
+        if (!(fabsf(fm - 0.5f * (fa + fb)) <= kLogUTableTol)) return __int_as_float(0x7fc00000);
+    }
+    return fi;
+}
+
+// tab: the table above, in global or shared memory (plain loads).
+__device__ __forceinline__ float log_inclusion_at(float c, const float* tab, int K, int L) {
+    if (c > -1.0f && c < 1.0f) {
+        const float tt = (c + 1.0f) * (0.5f * kLogUTableIntervals);
+        const int i = min(static_cast<int>(tt), kLogUTableIntervals - 1);
+        const float g0 = tab[i], g1 = tab[i + 1];
+        const float lw = fmaf(tt - static_cast<float>(i), g1 - g0, g0);
+        if (lw == lw) return lw;                 // NaN: an interval kept for the closed form
+    }
+    return log_inclusion_cos(c, K, L);
 }
 
 // ---- mbarriers and the bounded wait every spin in this library goes through -----------------

@@ -207,10 +207,13 @@ def test_graph_capture_replays_the_same_step(mp):
 LOGU_ABS, LOGU_REL = 1e-4, 1e-6      # |log u_gpu - log u| <= 1e-4 + 1e-6 |log u|, c in (-1, 1]
 
 
-@pytest.mark.parametrize("K,L", [(8, 75), (9, 120), (10, 150), (11, 300), (2, 3)])
+@pytest.mark.parametrize("K,L", [(8, 75), (9, 120), (10, 150), (11, 300), (2, 3), (12, 2),
+                                 (24, 2), (32, 5), (16, 10), (20, 1000)])
 def test_log_inclusion_matches_the_oracle_over_the_cosine(mp, K, L):
     # the function every selected key's weight goes through ("LSH Sampling...", method details,
-    # the u_i formula), at 10^4 grid cosines, 4,000 random ones and the ends of the range
+    # the u_i formula), as the attend kernel evaluates it (its per-call table, and the closed form
+    # on the intervals where the table's chord is not close enough: few tables and many bits bend
+    # log u sharply near cos = 1), at 10^4 grid cosines, 4,000 random ones and the range's ends
     rng = np.random.default_rng(400 + K)
     c = np.concatenate([-1.0 + 2.0 * np.arange(1, 10001) / 10000.0, rng.uniform(-1, 1, 4000),
                         1.0 - np.logspace(-7, -1, 200), -1.0 + np.logspace(-6, -1, 200)])
