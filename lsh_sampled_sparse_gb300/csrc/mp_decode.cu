@@ -54,12 +54,22 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
     allow_dependents();                          // the scan may start streaming codes meanwhile
     if (blockIdx.y == a.qrow_ctas) {
         // the extra row of CTAs: the attend kernel's table of log u over the cosine
-        for (int i = blockIdx.x * kThreads + tid; i <= kLuIntervals; i += gridDim.x * kThreads)
-            a.logu_tab[i] = log_inclusion_entry(i, a.K, a.L);
+        for (int seg = blockIdx.x; seg < kLogUSegments; seg += gridDim.x)
+            log_inclusion_segment(seg, a.K, a.L, &Ws[0][0], a.logu_tab);
         return;
     }
     const int wd = blockIdx.x, r0 = blockIdx.y * kQRows;
     const int nq = min(kQRows, a.BHq - r0);
+    const int row = r0 + warp;
+    const int Hkv = a.Hq / a.G;
+    // the CTAs of word 0 also compute |q| and q.mu: the centre is loaded with the other inputs
+    float mu4[kD / 32] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (blockIdx.x == 0 && warp < nq) {
+        const int b = row / a.Hq, g = (row % a.Hq) / a.G;
+        const float* mu = a.centre + (static_cast<size_t>(b) * Hkv + g) * kD;
+#pragma unroll
+        for (int k = 0; k < kD / 32; ++k) mu4[k] = mu[lane + 32 * k];
+    }
     {
         // all loads first, then the stores: the loop bodies must not wait for each other
         constexpr int kQPer = kQRows * kD / kThreads, kWPer = kD * 32 / kThreads;
@@ -87,8 +97,6 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
         }
     }
     __syncthreads();
-    const int row = r0 + warp;
-    const int Hkv = a.Hq / a.G;
     if (warp < nq && a.C > 0) {
         const int j = wd * 32 + lane;
         // four interleaved partial sums over the 128 dimensions (a short dependency chain)
@@ -109,13 +117,12 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
     }
     if (blockIdx.x == 0) {
         if (warp < nq) {
-            const int b = row / a.Hq, h = row % a.Hq, g = h / a.G;
-            const float* mu = a.centre + (static_cast<size_t>(b) * Hkv + g) * kD;
             float nn = 0.0f, qm = 0.0f;
-            for (int e = lane; e < kD; e += 32) {
-                const float x = Qs[warp][e];
+#pragma unroll
+            for (int k = 0; k < kD / 32; ++k) {
+                const float x = Qs[warp][lane + 32 * k];
                 nn = fmaf(x, x, nn);
-                qm = fmaf(x, mu[e], qm);
+                qm = fmaf(x, mu4[k], qm);
             }
 #pragma unroll
             for (int o = 16; o; o >>= 1) {
@@ -573,10 +580,11 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
         return (blk0 + (lo >> 5)) * kKeysPerBlock + (lo & 31) * 32 + bit;
     };
 
-    // ---- rounds of rcap rows: stage them (cp.async, one round trip), then each half-warp folds
-    //      entries hw, hw + 8, ... in batches of 8: partial q.k and |k - mu|^2 over the lane's 8
-    //      dimensions, one reduce-scatter so that lanes 2j, 2j + 1 hold pair j's sums, the
-    //      log-weight s - log u lane-parallel (log u from the per-call table or its closed
+    // ---- rounds of rcap rows: each warp stages the rows it folds (cp.async, one round trip;
+    //      a warp whose rows land early computes while others still wait), then each half-warp
+    //      folds entries hw, hw + 8, ... in batches of 8: partial q.k and |k - mu|^2 over the
+    //      lane's 8 dimensions, one reduce-scatter so that lanes 2j, 2j + 1 hold pair j's sums,
+    //      the log-weight s - log u lane-parallel (log u from the per-call table or its closed
     //      form, the cross-polytope table, or 0 for T), one online-softmax step
     float m = -INFINITY, l = 0.0f, o[8];
 #pragma unroll
@@ -593,15 +601,20 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
         if (tid < nr) rowkey[tid] = key_of(base + tid);
         for (int r = tid + kAThreads; r < nr; r += kAThreads) rowkey[r] = key_of(base + r);
         __syncthreads();
-        for (int i = tid; i < nr * kPieces; i += kAThreads) {
-            const int r = i / kPieces, pc = i - r * kPieces;
+        // the rows of this warp's two half-warps (r % 8 in {2 warp, 2 warp + 1}), one row (K then
+        // V) per instruction
+        for (int j2 = 0;; ++j2) {
+            const int r = 2 * warp + (j2 & 1) + 8 * (j2 >> 1);
+            if (r >= nr) break;
             const size_t key = static_cast<size_t>(rowkey[r]);
-            const uint8_t* src = (pc < kPieces / 2 ? Kg : Vg) + key * kD * sizeof(KV) +
-                                 16 * (pc % (kPieces / 2));
-            cp_async16(stage + r * kRowBytes + 16 * pc, src);
+            for (int pc = lane; pc < kPieces; pc += 32) {
+                const uint8_t* src = (pc < kPieces / 2 ? Kg : Vg) + key * kD * sizeof(KV) +
+                                     16 * (pc % (kPieces / 2));
+                cp_async16(stage + r * kRowBytes + 16 * pc, src);
+            }
         }
         cp_async_wait_all();
-        __syncthreads();
+        __syncwarp();
         for (int ent = hw; ent < nr; ent += 8 * kHalves) {
             const int cnt = min(8, (nr - ent + kHalves - 1) / kHalves);
             float pd[8], pk[8];
@@ -805,8 +818,8 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
 // (the per-call table, here rebuilt in shared memory, and the closed form where it is not used).
 __global__ void log_inclusion_kernel(const float* cosines, int count, int K, int L, float* out) {
     __shared__ float tab[kLuIntervals + 1];      // the table the query encoding fills per call
-    for (int i = threadIdx.x; i <= kLuIntervals; i += blockDim.x) tab[i] = log_inclusion_entry(i, K, L);
-    __syncthreads();
+    __shared__ float buf[2 * kLogUSegment + 3];
+    for (int seg = 0; seg < kLogUSegments; ++seg) log_inclusion_segment(seg, K, L, buf, tab);
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < count) out[i] = log_inclusion_at(cosines[i], tab, K, L);
 }

@@ -38,7 +38,7 @@ struct DecodeScratch {
     int n_counters;      // counters the query encoding resets
     uint32_t* selmask;   // [B*Hq][nblk][32] selection words, written by the scan kernel
     uint32_t* sel_ge1;   // [B*Hq][nblk][32] keys hit by >= 1 table (bucketed lookup only)
-    float* logu_tab;     // [kLogUTableIntervals + 1] log_inclusion_entry(i), filled per call
+    float* logu_tab;     // [kLogUTableIntervals + 1] log_inclusion_segment's table, filled per call
 };
 
 struct DecodeShape {
@@ -285,19 +285,44 @@ __device__ __forceinline__ float log_inclusion_grid(float i, int K, int L) {
     return log_inclusion_cos(fminf(1.0f, -1.0f + 2.0f * i / kLogUTableIntervals), K, L);
 }
 
-// Entry i of the table: log u at the cosine -1 + 2 i / N, or NaN when an interval it bounds is
-// not interpolated (every cosine of such an interval then takes the closed form).
-__device__ inline float log_inclusion_entry(int i, int K, int L) {
-    const float fi = log_inclusion_grid(static_cast<float>(i), K, L);
-    for (int j = i - 1; j <= i; ++j) {
-        if (j < 0 || j >= kLogUTableIntervals) continue;
-        const float fa = j == i ? fi : log_inclusion_grid(static_cast<float>(j), K, L);
-        const float fb = j == i ? log_inclusion_grid(static_cast<float>(j + 1), K, L) : fi;
-        const float fm = log_inclusion_grid(static_cast<float>(j) + 0.5f, K, L);
-        if (!(fabsf(fm - 0.5f * (fa + fb)) <= kLogUTableTol)) return __int_as_float(0x7fc00000);
-    }
-    return fi;
+__device__ __forceinline__ bool log_inclusion_chord_ok(float fa, float fb, float fm) {
+    return fabsf(fm - 0.5f * (fa + fb)) <= kLogUTableTol;   // false for NaN or inf - inf
 }
+
+// Entries [seg * kLogUSegment, (seg + 1) * kLogUSegment) (those <= N) of the table: entry i is
+// log u at the cosine -1 + 2 i / N, or NaN when an interval it bounds is not interpolated (every
+// cosine of such an interval then takes the closed form). The closed form is evaluated once per
+// grid point and interval midpoint of the segment (and its two neighbours) into buf, shared
+// memory of at least 2 * kLogUSegment + 3 floats. Called by every thread of the block.
+constexpr int kLogUSegment = 128;
+__device__ inline void log_inclusion_segment(int seg, int K, int L, float* buf, float* tab) {
+    const int i0 = seg * kLogUSegment;
+    float* fg = buf;                             // grid points i0 - 1 .. i0 + kLogUSegment
+    float* fm = buf + kLogUSegment + 2;          // midpoints of intervals i0 - 1 .. i0 + kLogUSegment - 1
+    for (int k = threadIdx.x; k < 2 * kLogUSegment + 3; k += blockDim.x) {
+        if (k < kLogUSegment + 2) {
+            const int i = i0 - 1 + k;
+            fg[k] = i >= 0 && i <= kLogUTableIntervals
+                        ? log_inclusion_grid(static_cast<float>(i), K, L) : 0.0f;
+        } else {
+            const int j = i0 - 1 + (k - (kLogUSegment + 2));
+            fm[k - (kLogUSegment + 2)] = j >= 0 && j < kLogUTableIntervals
+                        ? log_inclusion_grid(static_cast<float>(j) + 0.5f, K, L) : 0.0f;
+        }
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < kLogUSegment; t += blockDim.x) {
+        const int i = i0 + t;
+        if (i > kLogUTableIntervals) break;
+        float e = fg[t + 1];
+        if (i >= 1 && !log_inclusion_chord_ok(fg[t], fg[t + 1], fm[t])) e = __int_as_float(0x7fc00000);
+        if (i < kLogUTableIntervals && !log_inclusion_chord_ok(fg[t + 1], fg[t + 2], fm[t + 1]))
+            e = __int_as_float(0x7fc00000);
+        tab[i] = e;
+    }
+    __syncthreads();                             // buf is refilled by the next segment
+}
+constexpr int kLogUSegments = kLogUTableIntervals / kLogUSegment + 1;
 
 // tab: the table above, in global or shared memory (plain loads).
 __device__ __forceinline__ float log_inclusion_at(float c, const float* tab, int K, int L) {
