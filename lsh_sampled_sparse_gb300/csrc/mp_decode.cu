@@ -8,6 +8,7 @@
 // section and the exact sink/local set ("static cache") of the system co-design section, whose
 // "recursive attention" merge of partial outputs is the log-sum-exp merge done here.
 #include <algorithm>
+#include <type_traits>
 
 #include "mp_internal.cuh"
 
@@ -596,106 +597,126 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     const bool weighted = !exact && a.K > 0;
     const int hw = 2 * warp + half;
     constexpr int kHalves = 2 * kAWarps;
+    // One online-softmax step of this half-warp over its rows ent + kHalves j, j < cnt <= NB: the
+    // partial sums of NB rows are reduce-scattered so that lanes j LPR .. j LPR + LPR - 1 hold row
+    // j's (LPR = 16 / NB), the log-weight is computed lane-parallel, V is folded in.
+    auto fold = [&](int ent, int cnt, auto nb_tag) {
+        constexpr int NB = decltype(nb_tag)::value;
+        constexpr int LPR = 16 / NB;
+        if (cnt <= 0) return;
+        float pd[NB], pk[NB];
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            const int r = j < cnt ? ent + j * kHalves : ent;
+            float kf[8];
+            load8(stage + r * kRowBytes + 8 * hl * sizeof(KV), static_cast<const KV*>(nullptr), kf);
+            float d = 0.0f, k2 = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float x = kf[i] - mu8[i];
+                k2 = fmaf(x, x, k2);
+                d = fmaf(q8[i], kf[i], d);
+            }
+            pd[j] = d;
+            pk[j] = k2;
+        }
+        // each level keeps half the rows and adds the partner's copy of them
+#pragma unroll
+        for (int lv = 0; (8 >> lv) >= LPR; ++lv) {
+            const int off = 8 >> lv, nk = (NB / 2) >> lv;
+            const bool up = (hl & off) != 0;
+#pragma unroll
+            for (int i = 0; i < nk; ++i) {
+                const float sd = up ? pd[i] : pd[i + nk];
+                const float sk = up ? pk[i] : pk[i + nk];
+                const float rd = __shfl_xor_sync(hmask, sd, off);
+                const float rk = __shfl_xor_sync(hmask, sk, off);
+                pd[i] = (up ? pd[i + nk] : pd[i]) + rd;
+                pk[i] = (up ? pk[i + nk] : pk[i]) + rk;
+            }
+        }
+        float dot = pd[0], kb2 = pk[0];
+#pragma unroll
+        for (int sh = LPR / 2; sh; sh >>= 1) {
+            dot += __shfl_xor_sync(hmask, dot, sh);
+            kb2 += __shfl_xor_sync(hmask, kb2, sh);
+        }
+        const int jl = hl / LPR;
+        float logit = -INFINITY;
+        if (jl < cnt) {
+            float lw = 0.0f;
+            if (weighted) {
+                const float den = qn * (a.radius ? rad : sqrtf(kb2));
+                float cs = den > 0.0f ? (dot - qmu) / den : 0.0f;
+                cs = fminf(1.0f, fmaxf(-1.0f, cs));
+                if (a.table_only) {                      // cross-polytope: p has no closed form
+                    const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
+                    const int ti = min(static_cast<int>(tt), kLuIntervals - 1);
+                    const float g0 = __ldg(a.logu_tab + ti), g1 = __ldg(a.logu_tab + ti + 1);
+                    lw = fmaf(tt - static_cast<float>(ti), g1 - g0, g0);
+                } else {
+                    lw = log_inclusion_at(cs, a.logu_tab, a.K, a.L);
+                }
+            }
+            logit = dot * a.scale - lw;
+        }
+        float bm = logit;
+#pragma unroll
+        for (int sh = 8; sh; sh >>= 1) bm = fmaxf(bm, __shfl_xor_sync(hmask, bm, sh));
+        const float mn = fmaxf(m, bm);
+        const float corr = __expf(m - mn);
+        const float wgt = jl < cnt ? __expf(logit - mn) : 0.0f;
+        float ws = (hl % LPR) ? 0.0f : wgt;                    // each row counted once
+#pragma unroll
+        for (int sh = 8; sh; sh >>= 1) ws += __shfl_xor_sync(hmask, ws, sh);
+        l = fmaf(l, corr, ws);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] *= corr;
+        const int src0 = lane & 16;
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            const float wj = __shfl_sync(hmask, wgt, src0 + LPR * j);
+            if (j < cnt) {
+                float vf[8];
+                load8(stage + (ent + j * kHalves) * kRowBytes + (kD + 8 * hl) * sizeof(KV),
+                      static_cast<const KV*>(nullptr), vf);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = fmaf(wj, vf[i], o[i]);
+            }
+        }
+        m = mn;
+    };
+    static_assert(kAttendRows == 8 * kHalves, "a round gives each half-warp 8 rows");
+    // rows of this half-warp among the first nr of a round from entry ent, at most 4
+    auto rows4 = [&](int nr, int ent) { return min(4, max(0, (nr - ent + kHalves - 1) / kHalves)); };
     for (int base = 0; base < nsel; base += a.rcap) {
         const int nr = min(a.rcap, nsel - base);
         if (tid < nr) rowkey[tid] = key_of(base + tid);
         for (int r = tid + kAThreads; r < nr; r += kAThreads) rowkey[r] = key_of(base + r);
         __syncthreads();
-        // the rows of this warp's two half-warps (r % 8 in {2 warp, 2 warp + 1}), one row (K then
-        // V) per instruction
-        for (int j2 = 0;; ++j2) {
-            const int r = 2 * warp + (j2 & 1) + 8 * (j2 >> 1);
-            if (r >= nr) break;
-            const size_t key = static_cast<size_t>(rowkey[r]);
-            for (int pc = lane; pc < kPieces; pc += 32) {
-                const uint8_t* src = (pc < kPieces / 2 ? Kg : Vg) + key * kD * sizeof(KV) +
-                                     16 * (pc % (kPieces / 2));
-                cp_async16(stage + r * kRowBytes + 16 * pc, src);
+        // the rows of this warp's two half-warps (r = hw + 8 j), one row (K then V) per
+        // instruction, in two commit groups: each half-warp's j = 0..3, then j = 4..7
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+            for (int jj = 0; jj < 8; ++jj) {
+                const int r = 2 * warp + (jj & 1) + kHalves * (4 * g + (jj >> 1));
+                if (r >= nr) continue;
+                const size_t key = static_cast<size_t>(rowkey[r]);
+                for (int pc = lane; pc < kPieces; pc += 32) {
+                    const uint8_t* src = (pc < kPieces / 2 ? Kg : Vg) + key * kD * sizeof(KV) +
+                                         16 * (pc % (kPieces / 2));
+                    cp_async16(stage + r * kRowBytes + 16 * pc, src);
+                }
             }
+            cp_async_commit();
         }
-        cp_async_wait_all();
+        // the first four rows of each half-warp are folded while the other four are in flight
+        cp_async_wait_pending<1>();
         __syncwarp();
-        for (int ent = hw; ent < nr; ent += 8 * kHalves) {
-            const int cnt = min(8, (nr - ent + kHalves - 1) / kHalves);
-            float pd[8], pk[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int r = j < cnt ? ent + j * kHalves : ent;
-                float kf[8];
-                load8(stage + r * kRowBytes + 8 * hl * sizeof(KV), static_cast<const KV*>(nullptr),
-                      kf);
-                float d = 0.0f, k2 = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float x = kf[i] - mu8[i];
-                    k2 = fmaf(x, x, k2);
-                    d = fmaf(q8[i], kf[i], d);
-                }
-                pd[j] = d;
-                pk[j] = k2;
-            }
-            // each level keeps half the pairs and adds the partner's copy of them
-#pragma unroll
-            for (int lv = 0; lv < 3; ++lv) {
-                const int off = 8 >> lv, nk = 4 >> lv;
-                const bool up = (hl & off) != 0;
-#pragma unroll
-                for (int i = 0; i < nk; ++i) {
-                    const float sd = up ? pd[i] : pd[i + nk];
-                    const float sk = up ? pk[i] : pk[i + nk];
-                    const float rd = __shfl_xor_sync(hmask, sd, off);
-                    const float rk = __shfl_xor_sync(hmask, sk, off);
-                    pd[i] = (up ? pd[i + nk] : pd[i]) + rd;
-                    pk[i] = (up ? pk[i + nk] : pk[i]) + rk;
-                }
-            }
-            const float dot = pd[0] + __shfl_xor_sync(hmask, pd[0], 1);
-            const float kb2 = pk[0] + __shfl_xor_sync(hmask, pk[0], 1);
-            const int jl = hl >> 1;
-            float logit = -INFINITY;
-            if (jl < cnt) {
-                float lw = 0.0f;
-                if (weighted) {
-                    const float den = qn * (a.radius ? rad : sqrtf(kb2));
-                    float cs = den > 0.0f ? (dot - qmu) / den : 0.0f;
-                    cs = fminf(1.0f, fmaxf(-1.0f, cs));
-                    if (a.table_only) {                  // cross-polytope: p has no closed form
-                        const float tt = (cs + 1.0f) * (0.5f * kLuIntervals);
-                        const int ti = min(static_cast<int>(tt), kLuIntervals - 1);
-                        const float g0 = __ldg(a.logu_tab + ti), g1 = __ldg(a.logu_tab + ti + 1);
-                        lw = fmaf(tt - static_cast<float>(ti), g1 - g0, g0);
-                    } else {
-                        lw = log_inclusion_at(cs, a.logu_tab, a.K, a.L);
-                    }
-                }
-                logit = dot * a.scale - lw;
-            }
-            float bm = logit;
-#pragma unroll
-            for (int sh = 8; sh; sh >>= 1) bm = fmaxf(bm, __shfl_xor_sync(hmask, bm, sh));
-            const float mn = fmaxf(m, bm);
-            const float corr = __expf(m - mn);
-            const float wgt = jl < cnt ? __expf(logit - mn) : 0.0f;
-            float ws = (hl & 1) ? 0.0f : wgt;                    // each pair counted once
-#pragma unroll
-            for (int sh = 8; sh; sh >>= 1) ws += __shfl_xor_sync(hmask, ws, sh);
-            l = fmaf(l, corr, ws);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) o[i] *= corr;
-            const int src0 = lane & 16;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float wj = __shfl_sync(hmask, wgt, src0 + 2 * j);
-                if (j < cnt) {
-                    float vf[8];
-                    load8(stage + (ent + j * kHalves) * kRowBytes + (kD + 8 * hl) * sizeof(KV),
-                          static_cast<const KV*>(nullptr), vf);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) o[i] = fmaf(wj, vf[i], o[i]);
-                }
-            }
-            m = mn;
-        }
+        fold(hw, rows4(nr, hw), std::integral_constant<int, 4>());
+        cp_async_wait_pending<0>();
+        __syncwarp();
+        fold(hw + 4 * kHalves, rows4(nr, hw + 4 * kHalves), std::integral_constant<int, 4>());
         __syncthreads();                                         // the stage is refilled next
     }
 
@@ -879,6 +900,21 @@ cudaError_t prepare_decode() {
         cudaError_t e = cudaFuncSetAttribute(pick_attend(bf != 0),
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kMaxSmem));
+        if (e != cudaSuccess) return e;
+    }
+    // one shared-memory carve-out (the largest) for every kernel of a decode step: an SM still
+    // running CTAs of one kernel can then take CTAs of the next without first draining to
+    // reconfigure its L1 / shared-memory split
+    const void* fns[] = {reinterpret_cast<const void*>(qencode_kernel),
+                         reinterpret_cast<const void*>(pick_collide(1)),
+                         reinterpret_cast<const void*>(pick_collide(2)),
+                         reinterpret_cast<const void*>(pick_collide(4)),
+                         reinterpret_cast<const void*>(pick_collide(8)),
+                         reinterpret_cast<const void*>(pick_attend(false)),
+                         reinterpret_cast<const void*>(pick_attend(true))};
+    for (const void* f : fns) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
     }
     cudaFuncAttributes fa;
