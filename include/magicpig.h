@@ -54,7 +54,7 @@ extern "C" {
 #define MP_API
 #endif
 
-#define MP_ABI_VERSION 5
+#define MP_ABI_VERSION 6
 #define MP_KEYS_PER_BLOCK 1024
 
 typedef enum {
@@ -63,7 +63,9 @@ typedef enum {
     MP_ERR_UNSUPPORTED = 2,   /* a valid request the library does not implement (e.g. d != 128) */
     MP_ERR_CUDA = 3,          /* a CUDA runtime call failed; cudaGetLastError() has the cause */
     MP_ERR_TIMEOUT = 4,       /* a device-side bounded wait gave up (see mp_device_status) */
-    MP_ERR_WORKSPACE = 5      /* the workspace passed is smaller than *_workspace_bytes */
+    MP_ERR_WORKSPACE = 5,     /* the workspace passed is smaller than *_workspace_bytes */
+    MP_ERR_BOUNDS = 6         /* an index check of the MP_CHECKS build failed (see
+                                 mp_debug_check_report); never raised by the product build */
 } mp_status;
 
 typedef enum { MP_F32 = 0, MP_BF16 = 1 } mp_dtype;
@@ -403,9 +405,23 @@ MP_API mp_status mp_decode_attention_noalloc(const void* q, mp_dtype q_dtype,
                                              int Hkv, int n, int d, const mp_params* prm,
                                              float* out, cudaStream_t stream);
 
-/* Synchronise the current device, return its status word (MP_OK or MP_ERR_TIMEOUT) through
- * *status and reset it to MP_OK. Returns MP_ERR_CUDA if the device cannot be reached. */
+/* Synchronise the current device, return its status word (MP_OK, MP_ERR_TIMEOUT, or in the
+ * MP_CHECKS build MP_ERR_BOUNDS) through *status and reset it, with the check site beside it, to
+ * MP_OK. Returns MP_ERR_CUDA if the device cannot be reached. */
 MP_API mp_status mp_device_status(int* status);
+
+/* The MP_CHECKS build (the library compiled with -DMP_CHECKS=1, libmagicpig_checks.so): every
+ * kernel of the decode path, the bucketed lookup and the tensor-core encoder check the indices of
+ * their global accesses (code blocks, selection words, K/V rows, partial states, bucket ranges
+ * and members, code words written) and skip an access that is out of range instead of making
+ * it, raising MP_ERR_BOUNDS in the status word. A stand-in for a memory checker: the paper has
+ * no counterpart. Synchronises the device and returns through *enabled 1 in that build, 0 in the
+ * product build, and through *site the site of the first failed check since the status word was
+ * last reset (0 if none): 1 query encoding stores, 2 scanned code block, 3 selection words
+ * written, 4 K/V row copied, 5 partial state or output written, 6 selection words read,
+ * 7 bucket range beyond the table's keys, 8 bucket member beyond n_indexed, 9 code words written
+ * by the encoder. Neither word is reset. Errors: MP_ERR_INVALID_ARG (null), MP_ERR_CUDA. */
+MP_API mp_status mp_debug_check_report(int* enabled, int* site);
 
 #ifdef __cplusplus
 }

@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     build_buckets,
     build_tables,
     buckets_bytes,
+    check_report,
     codes_bytes,
     codes_unpack,
     cp_codes_bytes,

@@ -65,7 +65,11 @@ _LIB = None
 
 
 def library_path() -> str:
-    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmagicpig.so")
+    """libmagicpig.so, or with MAGICPIG_CHECKS=1 in the environment the MP_CHECKS build
+    libmagicpig_checks.so (python -m lsh_sampled_sparse_gb300.build --checks)."""
+    name = "libmagicpig_checks.so" if os.environ.get("MAGICPIG_CHECKS") == "1" \
+        else "libmagicpig.so"
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), name)
 
 
 def _declare(L):
@@ -110,6 +114,7 @@ def _declare(L):
         "mp_debug_log_inclusion": (_c_int, [_vp, _c_int, _c_int, _c_int, _vp, _vp]),
         "mp_debug_wait_expiry": (_c_int, [_c_int, _vp]),
         "mp_device_status": (_c_int, [ctypes.POINTER(_c_int)]),
+        "mp_debug_check_report": (_c_int, [ctypes.POINTER(_c_int), ctypes.POINTER(_c_int)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -534,7 +539,17 @@ def codes_unpack(codes, B: int, Hkv: int, n: int, K: int, L: int, stream=None):
 
 
 def device_status() -> int:
-    """Synchronise the device; return and clear its status word (0 = MP_OK, 4 = timeout)."""
+    """Synchronise the device; return and clear its status word (0 = MP_OK, 4 = timeout,
+    6 = a failed index check of the MP_CHECKS build)."""
     v = _c_int(0)
     _check(lib().mp_device_status(ctypes.byref(v)), "mp_device_status")
     return int(v.value)
+
+
+def check_report() -> tuple[bool, int]:
+    """(whether the loaded library is the MP_CHECKS build, the site of the first failed index
+    check since the status word was last cleared, 0 if none); clears nothing."""
+    en, site = _c_int(0), _c_int(0)
+    _check(lib().mp_debug_check_report(ctypes.byref(en), ctypes.byref(site)),
+           "mp_debug_check_report")
+    return bool(en.value), int(site.value)

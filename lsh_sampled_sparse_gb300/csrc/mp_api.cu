@@ -10,8 +10,9 @@
 
 namespace mp {
 
-// One status word per device; kernels with bounded waits raise MP_ERR_TIMEOUT here.
-__device__ int g_device_status;
+// One status word per device; kernels with bounded waits raise MP_ERR_TIMEOUT here, the index
+// checks of the MP_CHECKS build MP_ERR_BOUNDS (with the first failed site in the second word).
+__device__ int g_device_status[2];
 
 namespace {
 constexpr int kMaxDevices = 64;
@@ -234,6 +235,7 @@ const char* mp_status_string(mp_status s) {
         case MP_ERR_CUDA: return "MP_ERR_CUDA";
         case MP_ERR_TIMEOUT: return "MP_ERR_TIMEOUT";
         case MP_ERR_WORKSPACE: return "MP_ERR_WORKSPACE";
+        case MP_ERR_BOUNDS: return "MP_ERR_BOUNDS";
         default: return "MP_UNKNOWN_STATUS";
     }
 }
@@ -626,11 +628,22 @@ mp_status mp_device_status(int* status) {
     if (!status) return MP_ERR_INVALID_ARG;
     if (!ensure_prepared()) return MP_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return MP_ERR_CUDA;
-    int v = 0;
-    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return MP_ERR_CUDA;
-    const int zero = 0;
-    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return MP_ERR_CUDA;
-    *status = v;
+    int v[2] = {0, 0};
+    if (cudaMemcpyFromSymbol(v, g_device_status, sizeof(v)) != cudaSuccess) return MP_ERR_CUDA;
+    const int zero[2] = {0, 0};
+    if (cudaMemcpyToSymbol(g_device_status, zero, sizeof(zero)) != cudaSuccess) return MP_ERR_CUDA;
+    *status = v[0];
+    return MP_OK;
+}
+
+mp_status mp_debug_check_report(int* enabled, int* site) {
+    if (!enabled || !site) return MP_ERR_INVALID_ARG;
+    if (!ensure_prepared()) return MP_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MP_ERR_CUDA;
+    int v[2] = {0, 0};
+    if (cudaMemcpyFromSymbol(v, g_device_status, sizeof(v)) != cudaSuccess) return MP_ERR_CUDA;
+    *enabled = MP_CHECKS;
+    *site = v[0] == MP_ERR_BOUNDS ? v[1] : 0;
     return MP_OK;
 }
 

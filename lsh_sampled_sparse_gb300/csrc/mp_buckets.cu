@@ -390,7 +390,8 @@ __device__ __forceinline__ uint32_t query_code(const uint32_t* qb, int K, int t)
 // loaded before their atomics are issued, so that a warp waits about three memory round trips.
 __global__ void __launch_bounds__(kLookupWarps * 32)
     bucket_lookup_kernel(const uint32_t* buckets, const uint32_t* qbits, int qwords, int Hq,
-                         int Hkv, int n, int K, int L, int nblk, uint32_t* ge1, uint32_t* ge2) {
+                         int Hkv, int n, int K, int L, int nblk, uint32_t* ge1, uint32_t* ge2,
+                         int* status) {
     allow_dependents();
     constexpr int U = kLookupUnroll;
     const int row = blockIdx.y, lane = threadIdx.x & 31;
@@ -402,14 +403,27 @@ __global__ void __launch_bounds__(kLookupWarps * 32)
     const uint32_t* base = buckets + static_cast<size_t>(bh) * bucket_words(n, K, L);
     const uint32_t c = query_code(qbits + static_cast<size_t>(row) * qwords, K, t);
     const uint32_t* off = base + static_cast<size_t>(t) * (nb + 1);
-    const uint32_t lo = __ldg(off + c), hi = __ldg(off + c + 1);
+    // a table built by mp_build_buckets has lo <= hi <= n and members below n; the range and
+    // the members are clamped to that all the same (the buckets are the caller's memory), and
+    // the MP_CHECKS build reports a table that needed it
+    uint32_t lo = __ldg(off + c), hi = __ldg(off + c + 1);
+    if (lane == 0) {
+        mp_check(status, hi, static_cast<long long>(n) + 1, kSiteBucketRange);
+        mp_check(status, lo, static_cast<long long>(hi) + 1, kSiteBucketRange);
+    }
+    hi = min(hi, static_cast<uint32_t>(n));
+    lo = min(lo, hi);
     const uint32_t* mem = base + static_cast<size_t>(L) * (nb + 1) + static_cast<size_t>(t) * n;
     uint32_t* g1 = ge1 + static_cast<size_t>(row) * nblk * kWordsPerBlock;
     uint32_t* g2 = ge2 + static_cast<size_t>(row) * nblk * kWordsPerBlock;
     for (uint32_t i0 = lo + lane; i0 < hi; i0 += 32u * U) {
         uint32_t key[U], old[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) key[u] = i0 + 32u * u < hi ? __ldg(mem + i0 + 32u * u) : ~0u;
+        for (int u = 0; u < U; ++u) {
+            key[u] = i0 + 32u * u < hi ? __ldg(mem + i0 + 32u * u) : ~0u;
+            if (key[u] != ~0u && !mp_check(status, key[u], n, kSiteBucketKey)) key[u] = ~0u;
+            if (key[u] >= static_cast<uint32_t>(n)) key[u] = ~0u;
+        }
 #pragma unroll
         for (int u = 0; u < U; ++u)
             old[u] = key[u] != ~0u ? atomicOr(g1 + (key[u] >> 5), 1u << (key[u] & 31u)) : 0u;
@@ -500,7 +514,7 @@ cudaError_t launch_bucket_lookup(const uint32_t* buckets, const uint32_t* qbits,
     const dim3 grid((s.L + kLookupWarps - 1) / kLookupWarps, s.B * s.Hq);
     bucket_lookup_kernel<<<grid, kLookupWarps * 32, 0, st>>>(buckets, qbits, s.qwords, s.Hq,
                                                              s.Hkv, s.n_indexed, s.K, s.L, s.nblk,
-                                                             ge1, ge2);
+                                                             ge1, ge2, device_status_ptr());
     return cudaGetLastError();
 }
 

@@ -45,6 +45,7 @@ struct QArgs {
     float4* qstat;
     unsigned* counters;
     float* logu_tab;                             // filled by the extra row of CTAs
+    int* status;                                 // index checks of the MP_CHECKS build
     int q_bf16, w_bf16, BHq, Hq, G, C, cpad, qwords, n_counters, K, L, qrow_ctas;
 };
 
@@ -110,11 +111,16 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
         const float s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         const bool bit = j < a.C && s > 0.0f;
         const uint32_t word = __ballot_sync(0xffffffffu, bit);
-        if (lane == 0) a.qbits[static_cast<size_t>(row) * a.qwords + wd] = word;
+        const long long qbi = static_cast<long long>(row) * a.qwords + wd;
+        if (lane == 0 && mp_check(a.status, qbi, static_cast<long long>(a.BHq) * a.qwords,
+                                  kSiteQencodeStore))
+            a.qbits[qbi] = word;
         const int b = row / a.Hq, h = row % a.Hq;
         const size_t bg = static_cast<size_t>(b) * Hkv + h / a.G;
-        if (j < a.cpad)
-            a.qmask[(bg * a.cpad + j) * a.G + (h % a.G)] = bit ? 0u : 0xffffffffu;
+        const long long qmi = (static_cast<long long>(bg) * a.cpad + j) * a.G + (h % a.G);
+        if (j < a.cpad &&
+            mp_check(a.status, qmi, static_cast<long long>(a.BHq) * a.cpad, kSiteQencodeStore))
+            a.qmask[qmi] = bit ? 0u : 0xffffffffu;
     }
     if (blockIdx.x == 0) {
         if (warp < nq) {
@@ -130,7 +136,8 @@ __global__ void __launch_bounds__(kThreads) qencode_kernel(const QArgs a) {
                 nn += __shfl_xor_sync(0xffffffffu, nn, o);
                 qm += __shfl_xor_sync(0xffffffffu, qm, o);
             }
-            if (lane == 0) a.qstat[row] = make_float4(sqrtf(nn), qm, 0.0f, 0.0f);
+            if (lane == 0 && mp_check(a.status, row, a.BHq, kSiteQencodeStore))
+                a.qstat[row] = make_float4(sqrtf(nn), qm, 0.0f, 0.0f);
         }
         if (blockIdx.y == 0)
             for (int i = tid; i < a.n_counters; i += kThreads) a.counters[i] = 0u;
@@ -148,6 +155,7 @@ struct CArgs {
     int n, nblk, Hq, Hkv, K, L, C, cpad, n_sink, n_local;
     int cblk;                                    // code blocks per head in memory
     int blk0;                                    // first block scanned (grid x + blk0)
+    int* status;                                 // index checks of the MP_CHECKS build
 };
 
 // Attend CTA shared memory: [work][selection words][prefix counts][row keys][cbuf][misc]. The
@@ -345,6 +353,7 @@ struct AArgs {
     int table_only;                              // cross-polytope: the table at every cosine
     int q_bf16, n, nblk, nsb, Hq, Hkv, G, K, L, n_sink, n_local;
     int ncap;                                    // K/V rows per head in memory
+    int* status;                                 // index checks of the MP_CHECKS build
     const float* radius;                         // MIPS variant: longest centred key per head
     float scale;
     int merge_cap;                               // partials staged per merge round
@@ -448,6 +457,10 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int blk = blockIdx.x + a.blk0, bg = blockIdx.y;
+    if (!mp_check(a.status, static_cast<long long>(bg) * a.cblk + blk,
+                  static_cast<long long>(gridDim.y) * a.cblk, kSiteScanCodes) ||
+        !mp_check(a.status, blk, a.nblk, kSiteScanCodes))
+        return;                                  // the whole CTA: the condition is uniform
     const int b = bg / a.Hkv, g = bg % a.Hkv;
     const int row0 = b * a.Hq + g * G;          // first query row of this KV head's group
     uint32_t* qneg = reinterpret_cast<uint32_t*>(smem);                    // [cpad][G]
@@ -458,7 +471,10 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     scan_block<G>(a, blk, bg, qneg, gebuf, ring, &s, &tm);
     if (threadIdx.x < G * 32) {
         const int h = threadIdx.x >> 5, w = threadIdx.x & 31;
-        a.selmask[(static_cast<size_t>(row0 + h) * a.nblk + blk) * 32 + w] = s;
+        const long long si = (static_cast<long long>(row0 + h) * a.nblk + blk) * 32 + w;
+        if (mp_check(a.status, si, static_cast<long long>(gridDim.y) * G * a.nblk * 32,
+                     kSiteScanSelect))
+            a.selmask[si] = s;
     }
 }
 
@@ -548,7 +564,10 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
             const uint32_t valid = bits_below(a.n - key0);
             const uint32_t tmask =
                 (bits_below(a.n_sink - key0) | ~bits_below(a.n - a.n_local - key0)) & valid;
-            U = a.selmask[(static_cast<size_t>(row) * a.nblk + blk) * 32 + lane] & valid & ~tmask;
+            const long long wi = (static_cast<long long>(row) * a.nblk + blk) * 32 + lane;
+            if (mp_check(a.status, wi, static_cast<long long>(gridDim.y) * a.nblk * 32,
+                         kSiteAttendSelect))
+                U = a.selmask[wi] & valid & ~tmask;
         }
         wsel[tid] = U;
         const int c = __popc(U);
@@ -702,6 +721,9 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
                 const int r = 2 * warp + (jj & 1) + kHalves * (4 * g + (jj >> 1));
                 if (r >= nr) continue;
                 const size_t key = static_cast<size_t>(rowkey[r]);
+                if (!mp_check(a.status, static_cast<long long>(key), min(a.n, a.ncap),
+                              kSiteAttendRow))
+                    continue;
                 for (int pc = lane; pc < kPieces; pc += 32) {
                     const uint8_t* src = (pc < kPieces / 2 ? Kg : Vg) + key * kD * sizeof(KV) +
                                          16 * (pc % (kPieces / 2));
@@ -746,7 +768,8 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     }
     __syncthreads();
     const size_t prow = static_cast<size_t>(row) * nsp + sb;
-    if (tid < kD) {
+    if (tid < kD && mp_check(a.status, static_cast<long long>(prow),
+                             static_cast<long long>(gridDim.y) * nsp, kSiteAttendPartial)) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kAWarps; ++w) M = fmaxf(M, cbuf[w * kCombinePitch + 128]);
@@ -830,8 +853,9 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
 #pragma unroll
     for (int w = 0; w < kAWarps; ++w) Ls += red[4 + w];
     // a query with a NaN or infinite element has no defined output: NaN, not a silent zero
-    a.out[static_cast<size_t>(row) * kD + tid] =
-        isfinite(qn) ? (Ls > 0.0f ? Os / Ls : 0.0f) : __int_as_float(0x7fc00000);
+    if (mp_check(a.status, row, gridDim.y, kSiteAttendPartial))
+        a.out[static_cast<size_t>(row) * kD + tid] =
+            isfinite(qn) ? (Ls > 0.0f ? Os / Ls : 0.0f) : __int_as_float(0x7fc00000);
     if (tid == 0) a.counters[row] = 0u;
 }
 
@@ -951,6 +975,7 @@ cudaError_t launch_qencode(const void* q, bool q_bf16, const float* centre, cons
     qa.qwords = s.qwords;
     qa.n_counters = ws.n_counters;
     qa.logu_tab = ws.logu_tab;
+    qa.status = device_status_ptr();
     qa.K = s.K;
     qa.L = s.L;
     qa.qrow_ctas = (qa.BHq + kQRows - 1) / kQRows;
@@ -977,6 +1002,7 @@ CArgs scan_args(const uint32_t* codes, const DecodeShape& s, const DecodeScratch
     ca.n_local = s.n_local;
     ca.cblk = s.cblk;
     ca.blk0 = blk0;
+    ca.status = device_status_ptr();
     return ca;
 }
 
@@ -1034,6 +1060,7 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
     aa.n_sink = s.n_sink;
     aa.n_local = s.n_local;
     aa.ncap = s.ncap;
+    aa.status = device_status_ptr();
     aa.radius = s.radius;
     aa.scale = s.scale;
     {

@@ -426,9 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the argmax codes, its Nc / d table rows of 1024 code bytes
         uint8_t* stg_bytes = reinterpret_cast<uint8_t*>(stg);
         auto store_unit = [&](int bg, int blk) {
+            const bool in_range =
+                mp_check(a.status, static_cast<long long>(bg) * a.cblk + a.blk0 + blk,
+                         static_cast<long long>(a.units / a.nblk) * a.cblk, kSiteEncodeCodes);
             if constexpr (kMode == kArgmax) {
                 epi_sync();
-                if (!aborted) {
+                if (!aborted && in_range) {
                     const int ntab = Nc / kD, L = a.C / kD;
                     uint8_t* dst = reinterpret_cast<uint8_t*>(a.codes) +
                                    ((static_cast<size_t>(bg) * a.cblk + a.blk0 + blk) * L + j0 / kD) *
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the staged words of planes colA .. colA + 63 come from the four warps of this
                 // column group alone, so those four store them, between barriers of their own
                 group_sync(ew >> 2);
-                if (!aborted) {
+                if (!aborted && in_range) {
                     uint32_t* dst = a.codes + (static_cast<size_t>(bg) * a.cblk + a.blk0 + blk) *
                                                   static_cast<size_t>(a.C) * kWordsPerBlock +
                                     static_cast<size_t>(j0) * kWordsPerBlock;

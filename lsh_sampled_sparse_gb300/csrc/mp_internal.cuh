@@ -22,8 +22,45 @@ constexpr int kAppendMaxKeys = 64;                  // mp_encode_keys ranges up 
 // keys) plus one for the exact sink/local set.
 inline int attend_partials(int nblk) { return (nblk + kAttendBlockGroup - 1) / kAttendBlockGroup + 1; }
 
-// Device status word values (mp_status codes); kernels only ever raise MP_ERR_TIMEOUT.
+// Device status word values (mp_status codes): kernels raise MP_ERR_TIMEOUT (a bounded wait gave
+// up) and, in the MP_CHECKS build, MP_ERR_BOUNDS. The word after it keeps the site of the first
+// failed index check.
 int* device_status_ptr();          // address of this device's status word (nullptr on error)
+
+#ifndef MP_CHECKS
+#define MP_CHECKS 0
+#endif
+// Sites of the index checks (the number mp_debug_check_report returns).
+enum CheckSite : int {
+    kSiteQencodeStore = 1,       // query bits / masks / norms written by the query encoding
+    kSiteScanCodes = 2,          // the code block a scan CTA streams
+    kSiteScanSelect = 3,         // the selection words a scan CTA writes
+    kSiteAttendRow = 4,          // a K/V row the attend kernel copies (key < n)
+    kSiteAttendPartial = 5,      // a partial softmax state or an output row it writes
+    kSiteAttendSelect = 6,       // the selection words it reads
+    kSiteBucketRange = 7,        // a bucket's [offset, next offset) outside the table's n keys
+    kSiteBucketKey = 8,          // a bucket member outside [0, n)
+    kSiteEncodeCodes = 9,        // the code words an encoder CTA writes
+};
+
+// Index check of the MP_CHECKS build (the memory checker's stand-in): there an index outside
+// [0, limit) raises MP_ERR_BOUNDS in the status word, keeps `site` beside it if it is the first,
+// and returns false so that the caller skips the access; nothing traps. In the product build it
+// is true and compiles away.
+__device__ __forceinline__ bool mp_check(int* status, long long idx, long long limit, int site) {
+#if MP_CHECKS
+    if (idx >= 0 && idx < limit) return true;
+    if (status && atomicCAS(status, 0, static_cast<int>(MP_ERR_BOUNDS)) == 0)
+        atomicExch(status + 1, site);
+    return false;
+#else
+    (void)status;
+    (void)idx;
+    (void)limit;
+    (void)site;
+    return true;
+#endif
+}
 int device_sm_count();
 
 // Scratch carved out of the decode workspace (all pointers 256-byte aligned).

@@ -42,9 +42,9 @@ def test_status_strings_and_version(L):
     header_version = int(re.search(r"#define MP_ABI_VERSION (\d+)", open(HEADER).read()).group(1))
     assert mp.abi_version() == header_version
     assert ctypes.sizeof(mp.Params) == 48          # mp_params: 8 four-byte fields, 2 pointers
-    names = [L.mp_status_string(i).decode() for i in range(6)]
+    names = [L.mp_status_string(i).decode() for i in range(7)]
     assert names == ["MP_OK", "MP_ERR_INVALID_ARG", "MP_ERR_UNSUPPORTED", "MP_ERR_CUDA",
-                     "MP_ERR_TIMEOUT", "MP_ERR_WORKSPACE"]
+                     "MP_ERR_TIMEOUT", "MP_ERR_WORKSPACE", "MP_ERR_BOUNDS"]
 
 
 def test_codes_bytes(L):
@@ -243,3 +243,15 @@ def test_package_has_no_cpu_fallback_and_never_imports_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
+
+
+def test_checks_build_compiles_and_exports_the_same_symbols():
+    # the MP_CHECKS build (index checks that raise MP_ERR_BOUNDS) is the same boundary
+    from lsh_sampled_sparse_gb300.build import build
+    path = build(checks=True)
+    assert path.endswith("libmagicpig_checks.so")
+    C = ctypes.CDLL(path)
+    missing = [n for n in declared_functions() if not hasattr(C, n)]
+    assert not missing, missing
+    C.mp_status_string.restype = ctypes.c_char_p
+    assert C.mp_status_string(6) == b"MP_ERR_BOUNDS"
