@@ -475,7 +475,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(bar_tempty + 8 * ab);
         }
         int it = 0;
-        int prev_bg = -1, prev_blk = 0;          // the unit whose words are still staged
         int bg = u_begin / a.nblk, blk = u_begin % a.nblk;
         for (int u = u_begin; u < u_end; ++u) {
             const int ntile = tiles_in_block(blk);
@@ -546,9 +545,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0 && !aborted) mbar_arrive(bar_tempty + 8 * ab);
-                // the previous unit's rows go out only now, after this unit's first buffer
-                // was released, so that the MMA keeps running meanwhile
-                if (t == 0 && prev_bg >= 0) store_unit(prev_bg, prev_blk);
                 if constexpr (kMode == kArgmax) {
                     // the two halves of a table meet: (|y|, code) per (table, half, key row) in
                     // the exchange area (two parities, so a tile's reads never race the next
@@ -576,14 +572,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            prev_bg = bg;
-            prev_blk = blk;
+            // the block's rows go out once its last tile is staged (its accumulator already
+            // released, so the MMA keeps running meanwhile); kept out of the tile loop, whose
+            // body then stays free of the store's registers and barriers
+            store_unit(bg, blk);
             if (++blk == a.nblk) {
                 blk = 0;
                 ++bg;
             }
         }
-        if (prev_bg >= 0) store_unit(prev_bg, prev_blk);
     }
     tc_fence_before();
     __syncthreads();
