@@ -23,7 +23,7 @@ constexpr int kAWarps = 4;                          // attend CTA: 4 warps, 8 ha
 static_assert(kAttendBlocks <= kAWarps, "one warp lists each block of an attend CTA");
 constexpr int kAThreads = 32 * kAWarps;
 static_assert(kAThreads == kD, "the attend merge gives one thread to each of the 128 output dims");
-constexpr int kRingDepth = 4;                       // tables in flight per warp in the async scan
+constexpr int kRingDepth = 5;                       // tables in flight per warp in the async scan
 constexpr int kRingMinK = 8, kRingMaxK = 11;        // K range the async scan handles
 constexpr int kLuIntervals = kLogUTableIntervals;   // log u tables: cosine grid intervals
 
@@ -180,10 +180,12 @@ inline AttendSmem attend_smem(int nsp, size_t kv_elem) {
 
 template <int G>
 size_t collide_smem_bytes(int cpad, int K) {
-    const size_t ring = (K >= kRingMinK && K <= kRingMaxK)
+    // with the ring, each warp's counters go into its own ring once it has drained
+    static_assert(kRingDepth * kRingMinK >= 2 * 8, "a drained ring holds its warp's counters");
+    const size_t area = (K >= kRingMinK && K <= kRingMaxK)
                             ? static_cast<size_t>(kWarps) * kRingDepth * K * kWordsPerBlock * 4
-                            : 0;
-    return static_cast<size_t>(cpad) * G * 4 + static_cast<size_t>(kWarps) * 2 * G * 32 * 4 + ring;
+                            : static_cast<size_t>(kWarps) * 2 * G * 32 * 4;
+    return static_cast<size_t>(cpad) * G * 4 + area;
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -369,11 +371,14 @@ struct AArgs {
 // bit-sliced saturating counters ge1 = (>= 1 match), ge2 = (>= 2 matches); the warps split the L
 // tables and their counters combine in a fixed order. Threads tid < G * 32 return the selection
 // word w = tid % 32 of head tid / 32, S = ge2 & valid & not T, in *sel and the block's T word in
-// *tmask. Shared memory: qneg [cpad][G], gebuf [kWarps][2][G][32], ring (per warp
-// [kRingDepth][K][32]); the CTA is past a barrier on return.
+// *tmask. Shared memory: qneg [cpad][G], then per warp either its ring [kRingDepth][K][32]
+// (K in the ring's range; the warp's counters [2][G][32] go into its own ring once drained) or
+// its counters alone; warp w's counters start at gebuf + w * gstride. The CTA is past a barrier
+// on return.
 template <int G>
 __device__ __forceinline__ void scan_block(const CArgs& a, int blk, int bg, uint32_t* qneg,
-                                           uint32_t* gebuf, uint32_t* ring, uint32_t* sel,
+                                           uint32_t* gebuf, int gstride, uint32_t* ring,
+                                           uint32_t* sel,
                                            uint32_t* tmask) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     allow_dependents();
@@ -425,10 +430,11 @@ __device__ __forceinline__ void scan_block(const CArgs& a, int blk, int bg, uint
         case 11: scan_tables_async<G, 11>(cb0, ring, qneg, t0, t1, lane, ge1, ge2); break;
         default: scan_tables_any<G>(cb0 + lane, qneg, a.K, t0, t1, ge1, ge2); break;
     }
+    uint32_t* mine = gebuf + warp * gstride;     // this warp's ring, drained (or its own slot)
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        gebuf[((warp * 2 + 0) * G + h) * 32 + lane] = ge1[h];
-        gebuf[((warp * 2 + 1) * G + h) * 32 + lane] = ge2[h];
+        mine[(0 * G + h) * 32 + lane] = ge1[h];
+        mine[(1 * G + h) * 32 + lane] = ge2[h];
     }
     __syncthreads();
     if (tid < G * 32) {
@@ -436,8 +442,8 @@ __device__ __forceinline__ void scan_block(const CArgs& a, int blk, int bg, uint
         uint32_t g1 = 0u, g2 = 0u;
 #pragma unroll
         for (int ww = 0; ww < kWarps; ++ww) {
-            const uint32_t a1 = gebuf[((ww * 2 + 0) * G + h) * 32 + w];
-            const uint32_t a2 = gebuf[((ww * 2 + 1) * G + h) * 32 + w];
+            const uint32_t a1 = gebuf[ww * gstride + (0 * G + h) * 32 + w];
+            const uint32_t a2 = gebuf[ww * gstride + (1 * G + h) * 32 + w];
             g2 |= a2 | (g1 & a1);
             g1 |= a1;
         }
@@ -464,11 +470,12 @@ __global__ void __launch_bounds__(kThreads, 3) collide_kernel(const CArgs a) {
     const int b = bg / a.Hkv, g = bg % a.Hkv;
     const int row0 = b * a.Hq + g * G;          // first query row of this KV head's group
     uint32_t* qneg = reinterpret_cast<uint32_t*>(smem);                    // [cpad][G]
-    uint32_t* gebuf = qneg + static_cast<size_t>(a.cpad) * G;              // [8][2][G][32]
-    uint32_t* ring = gebuf + kWarps * 2 * G * 32 +                         // [8][depth][K][32]
-                     static_cast<size_t>(warp) * kRingDepth * a.K * kWordsPerBlock;
+    uint32_t* area = qneg + static_cast<size_t>(a.cpad) * G;
+    const bool ringed = a.K >= kRingMinK && a.K <= kRingMaxK;
+    const int rstride = kRingDepth * a.K * kWordsPerBlock;                 // ring words per warp
+    uint32_t* ring = area + static_cast<size_t>(warp) * rstride;          // [8][depth][K][32]
     uint32_t s = 0u, tm = 0u;
-    scan_block<G>(a, blk, bg, qneg, gebuf, ring, &s, &tm);
+    scan_block<G>(a, blk, bg, qneg, area, ringed ? rstride : 2 * G * 32, ring, &s, &tm);
     if (threadIdx.x < G * 32) {
         const int h = threadIdx.x >> 5, w = threadIdx.x & 31;
         const long long si = (static_cast<long long>(row0 + h) * a.nblk + blk) * 32 + w;
