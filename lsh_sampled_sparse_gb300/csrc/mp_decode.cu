@@ -161,7 +161,8 @@ struct CArgs {
 // Attend CTA shared memory: [work][selection words][prefix counts][row keys][cbuf][misc]. The
 // work region holds a round of rcap staged K/V rows, and in the merging CTA up to `merge_cap`
 // staged partial outputs (the merge runs in rounds when a row has more partials).
-constexpr int kAttendRows = 64;                      // rows staged per round of an attend CTA
+constexpr int kAttendRows = 64;                      // row slots in an attend CTA's stage
+constexpr int kRowKeys = 256;                        // selected keys listed once per attend CTA
 struct AttendSmem {
     size_t work, total;
     int merge_cap, rcap;
@@ -173,7 +174,7 @@ inline AttendSmem attend_smem(int nsp, size_t kv_elem) {
     m.work = static_cast<size_t>(kAttendRows) * 2 * kD * kv_elem;
     m.merge_cap = static_cast<int>(m.work / (static_cast<size_t>(kD) * 4));
     m.total = m.work + static_cast<size_t>(kAThreads) * 4 + (kAThreads + 4) * 4 +
-              static_cast<size_t>(kAttendRows) * 4 + static_cast<size_t>(kAWarps) * kCombinePitch * 4 +
+              static_cast<size_t>(kRowKeys) * 4 + static_cast<size_t>(kAWarps) * kCombinePitch * 4 +
               32;
     return m;
 }
@@ -517,8 +518,9 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel_gpu(unsigned* p, unsigned
 // the exact set T = [0, n_sink) u [n - n_local, n) with log u = 0, so that the 68 sink/local rows
 // do not pile onto the CTA of the last blocks. Each CTA folds its rows into one partial softmax;
 // the last CTA of each query row merges the row's nsb + 1 partials by log-sum-exp.
-// Rows come in rounds of up to rcap: their K and V rows are staged in shared memory with cp.async
-// (one round trip for the whole round), then the 8 half-warps fold them 8 at a time.
+// Each warp copies and folds its own rows (row e goes to half-warp e mod 8) in a pipeline of
+// groups of four rows per half-warp through two sets of row slots in shared memory: the group
+// after next is copied (cp.async) into a group's slots as soon as that group is folded.
 template <typename KV>
 __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     extern __shared__ __align__(16) uint8_t smem[];
@@ -536,8 +538,8 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     uint8_t* stage = smem;                                    // [rcap] rows; later the merge
     uint32_t* wsel = reinterpret_cast<uint32_t*>(smem + a.work_bytes);      // [kWords]
     int* wpre = reinterpret_cast<int*>(wsel + kWords);                      // [kWords + 4]
-    int* rowkey = wpre + kWords + 4;                                        // [rcap]
-    float* cbuf = reinterpret_cast<float*>(rowkey + a.rcap);                // [4][kCombinePitch]
+    int* rowkey = wpre + kWords + 4;                                        // [kRowKeys]
+    float* cbuf = reinterpret_cast<float*>(rowkey + kRowKeys);              // [4][kCombinePitch]
     int* misc = reinterpret_cast<int*>(cbuf + kAWarps * kCombinePitch);     // [8]
 
     const int half = lane >> 4, hl = lane & 15;
@@ -607,10 +609,10 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
         return (blk0 + (lo >> 5)) * kKeysPerBlock + (lo & 31) * 32 + bit;
     };
 
-    // ---- rounds of rcap rows: each warp stages the rows it folds (cp.async, one round trip;
-    //      a warp whose rows land early computes while others still wait), then each half-warp
-    //      folds entries hw, hw + 8, ... in batches of 8: partial q.k and |k - mu|^2 over the
-    //      lane's 8 dimensions, one reduce-scatter so that lanes 2j, 2j + 1 hold pair j's sums,
+    // ---- the rows: each warp copies the rows it folds (cp.async) in groups and folds each
+    //      group as it lands (a warp whose rows land early computes while others still wait);
+    //      a half-warp folds its rows of a group together: partial q.k and |k - mu|^2 over the
+    //      lane's 8 dimensions, one reduce-scatter so that a few lanes hold each row's sums,
     //      the log-weight s - log u lane-parallel (log u from the per-call table or its closed
     //      form, the cross-polytope table, or 0 for T), one online-softmax step
     float m = -INFINITY, l = 0.0f, o[8];
@@ -712,22 +714,22 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
         }
         m = mn;
     };
-    static_assert(kAttendRows == 8 * kHalves, "a round gives each half-warp 8 rows");
-    // rows of this half-warp among the first nr of a round from entry ent, at most 4
-    auto rows4 = [&](int nr, int ent) { return min(4, max(0, (nr - ent + kHalves - 1) / kHalves)); };
-    for (int base = 0; base < nsel; base += a.rcap) {
-        const int nr = min(a.rcap, nsel - base);
-        if (tid < nr) rowkey[tid] = key_of(base + tid);
-        for (int r = tid + kAThreads; r < nr; r += kAThreads) rowkey[r] = key_of(base + r);
-        __syncthreads();
-        // the rows of this warp's two half-warps (r = hw + 8 j), one row (K then V) per
-        // instruction, in two commit groups: each half-warp's j = 0..3, then j = 4..7
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
+    static_assert(kAttendRows == 8 * kHalves, "the stage gives each half-warp 8 row slots");
+    // the keys of the first kRowKeys entries, listed once (later ones are found on demand)
+    for (int i = tid; i < min(nsel, kRowKeys); i += kAThreads) rowkey[i] = key_of(i);
+    __syncthreads();
+    // Group k of a warp: entries hw + 8 (4 k + j), j < 4, of its two half-warps, in the slots
+    // hw + 8 (4 (k & 1) + j); group k + 2 reuses group k's slots once group k is folded.
+    const int lo_hw = 2 * warp;                  // the warp's first half-warp has its most rows
+    const int ngroups = nsel > lo_hw ? ((nsel - lo_hw + kHalves - 1) / kHalves + 3) / 4 : 0;
+    const int my_rows = nsel > hw ? (nsel - hw + kHalves - 1) / kHalves : 0;
+    auto issue = [&](int k) {                    // one row (K then V) per instruction
+        if (k < ngroups) {
             for (int jj = 0; jj < 8; ++jj) {
-                const int r = 2 * warp + (jj & 1) + kHalves * (4 * g + (jj >> 1));
-                if (r >= nr) continue;
-                const size_t key = static_cast<size_t>(rowkey[r]);
+                const int e = lo_hw + (jj & 1) + kHalves * (4 * k + (jj >> 1));
+                if (e >= nsel) continue;
+                const int r = lo_hw + (jj & 1) + kHalves * (4 * (k & 1) + (jj >> 1));
+                const size_t key = static_cast<size_t>(e < kRowKeys ? rowkey[e] : key_of(e));
                 if (!mp_check(a.status, static_cast<long long>(key), min(a.n, a.ncap),
                               kSiteAttendRow))
                     continue;
@@ -737,17 +739,20 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
                     cp_async16(stage + r * kRowBytes + 16 * pc, src);
                 }
             }
-            cp_async_commit();
         }
-        // the first four rows of each half-warp are folded while the other four are in flight
-        cp_async_wait_pending<1>();
+        cp_async_commit();                       // one group per call, empty or not
+    };
+    issue(0);
+    issue(1);
+    for (int k = 0; k < ngroups; ++k) {
+        cp_async_wait_pending<1>();              // group k has landed (group k + 1 may not have)
         __syncwarp();
-        fold(hw, rows4(nr, hw), std::integral_constant<int, 4>());
-        cp_async_wait_pending<0>();
-        __syncwarp();
-        fold(hw + 4 * kHalves, rows4(nr, hw + 4 * kHalves), std::integral_constant<int, 4>());
-        __syncthreads();                                         // the stage is refilled next
+        fold(hw + kHalves * 4 * (k & 1), min(4, max(0, my_rows - 4 * k)),
+             std::integral_constant<int, 4>());
+        __syncwarp();                            // every lane is done with group k's slots
+        issue(k + 2);
     }
+    cp_async_wait_pending<0>();
 
     // ---- merge the two half-warps, then the warps (fixed order)
     {
