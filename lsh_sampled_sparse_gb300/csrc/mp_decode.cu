@@ -159,18 +159,17 @@ struct CArgs {
 };
 
 // Attend CTA shared memory: [work][selection words][prefix counts][row keys][cbuf][misc]. The
-// work region holds a round of rcap staged K/V rows, and in the merging CTA up to `merge_cap`
-// staged partial outputs (the merge runs in rounds when a row has more partials).
+// work region holds kAttendRows row slots of staged K/V rows, and in the merging CTA up to
+// `merge_cap` staged partial outputs (the merge runs in rounds when a row has more partials).
 constexpr int kAttendRows = 64;                      // row slots in an attend CTA's stage
 constexpr int kRowKeys = 256;                        // selected keys listed once per attend CTA
 struct AttendSmem {
     size_t work, total;
-    int merge_cap, rcap;
+    int merge_cap;
 };
 inline AttendSmem attend_smem(int nsp, size_t kv_elem) {
     (void)nsp;
     AttendSmem m;
-    m.rcap = kAttendRows;
     m.work = static_cast<size_t>(kAttendRows) * 2 * kD * kv_elem;
     m.merge_cap = static_cast<int>(m.work / (static_cast<size_t>(kD) * 4));
     m.total = m.work + static_cast<size_t>(kAThreads) * 4 + (kAThreads + 4) * 4 +
@@ -361,7 +360,6 @@ struct AArgs {
     float scale;
     int merge_cap;                               // partials staged per merge round
     int work_bytes;                              // bytes of the row / merge stage region
-    int rcap;                                    // rows staged per round
 };
 
 // The scan of one (1024-key block, sequence x KV head) for its GQA group of G query heads,
@@ -535,7 +533,7 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     constexpr int kPieces = kRowBytes / 16;
     constexpr int kWords = kAttendBlocks * 32;                            // selection words
     static_assert(kWords == kAThreads, "one selection word per thread");
-    uint8_t* stage = smem;                                    // [rcap] rows; later the merge
+    uint8_t* stage = smem;                                    // [kAttendRows] rows; later the merge
     uint32_t* wsel = reinterpret_cast<uint32_t*>(smem + a.work_bytes);      // [kWords]
     int* wpre = reinterpret_cast<int*>(wsel + kWords);                      // [kWords + 4]
     int* rowkey = wpre + kWords + 4;                                        // [kRowKeys]
@@ -1079,7 +1077,6 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
         const AttendSmem m = attend_smem(attend_partials(s.nblk), kv_bf16 ? 2 : 4);
         aa.merge_cap = m.merge_cap;
         aa.work_bytes = static_cast<int>(m.work);
-        aa.rcap = m.rcap;
     }
     return launch_dependent(attend, dim3(aa.nsb + 1, s.B * s.Hq), dim3(kAThreads), smem_att, st,
                             aa);
