@@ -863,6 +863,9 @@ def run_ours(args):
         else "of fallback"
 
     decode_ms = run_decode_only(mp, wl, W, state, ws_dec, args.steps, graph is not None)
+    # algorithmic bytes of A2-A5 per layer over the event-free decode time per layer
+    dec_gbs = (alg["sampled_attention"]["bytes"] + alg["encode_query"]["bytes"]) * layers \
+        / (decode_ms / 1e3) / 1e9
     append_us = run_append(mp, wl, W, state, args.steps, graph is not None)
     line = {
         "metric": METRIC,
@@ -892,13 +895,23 @@ def run_ours(args):
         },
         "roofline": roof,
         "roofline_decode": {
-            "bound": "hbm", "kernel": "sampled_attention (collide_kernel + attend_kernel)",
-            "achieved": rooflines["sampled_attention"]["achieved"], "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": rooflines["sampled_attention"]["frac"],
-            "traffic": rooflines["sampled_attention"]["traffic"],
+            "bound": "hbm",
+            "kernel": "decode step A2-A5 per layer (qencode_kernel + collide_kernel + "
+                      "attend_kernel), timed over the event-free graph of K decode steps",
+            "achieved": dec_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": dec_gbs / peaks["hbm_gbs"],
+            "us_per_layer": decode_ms * 1e3 / layers,
+            "traffic": (None if rooflines["sampled_attention"]["traffic"] is None
+                        or rooflines["encode_query"]["traffic"] is None
+                        else rooflines["sampled_attention"]["traffic"]
+                        + rooflines["encode_query"]["traffic"]),
             "peak_source": roof["peak_source"],
-            "frac_of_nominal": rooflines["sampled_attention"]["achieved"] / NOMINAL_HBM_GBS,
+            "frac_of_nominal": dec_gbs / NOMINAL_HBM_GBS,
             "nominal_peak": NOMINAL_HBM_GBS,
+            "stage_events_frac": rooflines["sampled_attention"]["frac"],
+            "stage_events_note": "collide + attend alone between CUDA events (rooflines."
+                                 "sampled_attention): the events cut the query encoding's "
+                                 "overlap with the scan",
             "target": ">= 0.60 of HBM peak; the workload's description quotes the peak as the "
                       "chip's ~8 TB/s (frac_of_nominal), frac is against the measured copy "
                       "bandwidth"},
@@ -908,13 +921,9 @@ def run_ours(args):
                     "decode steps)",
             "queries_per_s": world * queries_per_step / (decode_ms / 1e3),
             "attention_ms_per_token": decode_ms,
-            "hbm_gbs": (alg["sampled_attention"]["bytes"] + alg["encode_query"]["bytes"]) * layers
-                       / (decode_ms / 1e3) / 1e9,
-            "hbm_frac": (alg["sampled_attention"]["bytes"] + alg["encode_query"]["bytes"]) * layers
-                        / (decode_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-            "hbm_frac_of_nominal": (alg["sampled_attention"]["bytes"] +
-                                    alg["encode_query"]["bytes"]) * layers
-                                   / (decode_ms / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+            "hbm_gbs": dec_gbs,
+            "hbm_frac": dec_gbs / peaks["hbm_gbs"],
+            "hbm_frac_of_nominal": dec_gbs / NOMINAL_HBM_GBS,
             "sampled_attention_gbs": rooflines["sampled_attention"]["achieved"],
             "append_us_per_layer": append_us,
             "append_note": "mp_encode_keys of one new key per layer (all heads), the incremental "
