@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(kClusterThreads)
     __shared__ uint32_t wsum[T / 32];
     const int nb = 1 << K, r = static_cast<int>(cluster.block_rank()), t = blockIdx.y,
               bh = blockIdx.z;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int rb = (nblk + R - 1) / R;
     const int b0 = (nblk * r) / R, b1 = (nblk * (r + 1)) / R;
     const int nbk = b1 - b0, nw = nbk * kWordsPerBlock, k0 = b0 * kKeysPerBlock;
