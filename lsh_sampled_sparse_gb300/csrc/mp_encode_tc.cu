@@ -476,6 +476,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int it = 0;
         int bg = u_begin / a.nblk, blk = u_begin % a.nblk;
+        // MIPS: this lane's key norm and its head's radius, loaded a tile ahead of their use
+        float nk_next = 0.0f, r_next = 0.0f;
+        auto load_norm = [&](int bg_, int blk_, int t_) {
+            const int key = (a.blk0 + blk_) * kKeysPerBlock + t_ * kTileM + quad * 32 + lane;
+            r_next = __ldg(a.radius + bg_);
+            nk_next = key < a.n ? __ldg(a.norms + static_cast<size_t>(bg_) * a.n + key) : r_next;
+        };
+        if constexpr (kMode == kMips) {
+            if (u_begin < u_end) load_norm(bg, blk, 0);
+        }
         for (int u = u_begin; u < u_end; ++u) {
             const int ntile = tiles_in_block(blk);
             for (int t = 0; t < ntile; ++t, ++it) {
@@ -492,10 +502,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int code64 = 0;
                 float aext = 0.0f;           // MIPS: this lane's key's extra coordinate
                 if constexpr (kMode == kMips) {
-                    const int key = (a.blk0 + blk) * kKeysPerBlock + t * kTileM + quad * 32 + lane;
-                    const float r = __ldg(a.radius + bg);
-                    const float nk = key < a.n ? __ldg(a.norms + static_cast<size_t>(bg) * a.n + key)
-                                               : r;
+                    const float nk = nk_next, r = r_next;
+                    if (t + 1 < ntile) {
+                        load_norm(bg, blk, t + 1);
+                    } else if (u + 1 < u_end) {   // the next unit's first tile
+                        const int nblk = blk + 1 == a.nblk ? 0 : blk + 1;
+                        load_norm(blk + 1 == a.nblk ? bg + 1 : bg, nblk, 0);
+                    }
                     aext = sqrtf(fmaxf(0.0f, fmaf(r, r, -nk * nk)));
                 }
                 if (!aborted) {
