@@ -363,9 +363,9 @@ struct AArgs {
 };
 
 // The scan of one (1024-key block, sequence x KV head) for its GQA group of G query heads,
-// run by all kThreads threads of a CTA: before the query masks exist, let the next kernel be
-// scheduled and start this warp's first tables of codes (an input of the call) into the ring for
-// the ring's K, else into L2; wait for the query encoding; copy the group's query masks into
+// run by all kThreads threads of a CTA: before the query masks exist, start this warp's first
+// tables of codes (an input of the call) into the ring for the ring's K, else into L2; wait for
+// the query encoding, then let the next kernel be scheduled; copy the group's query masks into
 // shared memory; per 32-key word (lane) and table, match = AND_b (plane ^ qmask), kept as
 // bit-sliced saturating counters ge1 = (>= 1 match), ge2 = (>= 2 matches); the warps split the L
 // tables and their counters combine in a fixed order. Threads tid < G * 32 return the selection
