@@ -22,7 +22,9 @@ constexpr int kAttendBlocks = kAttendBlockGroup;
 constexpr int kAWarps = 4;                          // attend CTA: 4 warps, 8 half-warps on rows
 static_assert(kAttendBlocks <= kAWarps, "one warp lists each block of an attend CTA");
 constexpr int kAThreads = 32 * kAWarps;
-static_assert(kAThreads == kD, "the attend merge gives one thread to each of the 128 output dims");
+constexpr int kMergeRegs = 8;                       // partials a merging warp holds in registers
+static_assert(kAThreads == kD && 4 * 32 == kD,
+              "the attend merge: a thread per output dim; a merging lane holds 4 dims");
 constexpr int kRingDepth = 5;                       // tables in flight per warp in the async scan
 constexpr int kRingMinK = 8, kRingMaxK = 11;        // K range the async scan handles
 constexpr int kLuIntervals = kLogUTableIntervals;   // log u tables: cosine grid intervals
@@ -159,19 +161,16 @@ struct CArgs {
 };
 
 // Attend CTA shared memory: [work][selection words][prefix counts][row keys][cbuf][misc]. The
-// work region holds kAttendRows row slots of staged K/V rows, and in the merging CTA up to
-// `merge_cap` staged partial outputs (the merge runs in rounds when a row has more partials).
+// work region holds kAttendRows row slots of staged K/V rows; cbuf joins the warps' partials.
 constexpr int kAttendRows = 64;                      // row slots in an attend CTA's stage
 constexpr int kRowKeys = 256;                        // selected keys listed once per attend CTA
 struct AttendSmem {
     size_t work, total;
-    int merge_cap;
 };
 inline AttendSmem attend_smem(int nsp, size_t kv_elem) {
     (void)nsp;
     AttendSmem m;
     m.work = static_cast<size_t>(kAttendRows) * 2 * kD * kv_elem;
-    m.merge_cap = static_cast<int>(m.work / (static_cast<size_t>(kD) * 4));
     m.total = m.work + static_cast<size_t>(kAThreads) * 4 + (kAThreads + 4) * 4 +
               static_cast<size_t>(kRowKeys) * 4 + static_cast<size_t>(kAWarps) * kCombinePitch * 4 +
               32;
@@ -358,7 +357,6 @@ struct AArgs {
     int* status;                                 // index checks of the MP_CHECKS build
     const float* radius;                         // MIPS variant: longest centred key per head
     float scale;
-    int merge_cap;                               // partials staged per merge round
     int work_bytes;                              // bytes of the row / merge stage region
 };
 
@@ -808,60 +806,67 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     __syncthreads();
     if (!misc[4]) return;
 
-    // ---- merge: the partial outputs are staged in shared memory (the row list's space) with
-    //      cp.async, issued before the maximum is known; m and l of the partials are loaded
-    //      meanwhile and sc[j] = exp(m_j - M) kept in cbuf. Rounds of kMergeCap partials.
-    const int kMergeCap = a.merge_cap;
-    float* mst = reinterpret_cast<float*>(smem);
-    float* red = cbuf;                            // [0, 8): reductions
-    float* sc = cbuf + 8;                         // scales, kMergeCap at a time
+    // ---- merge: warp w folds the row's partials j = w, w + 4, w + 8, ... in ascending order,
+    //      lane l dims 4l..4l+3; a pass loads kMergeRegs partials per warp into registers at once
+    //      (one round trip covers 4 * kMergeRegs partials) and rescales a running maximum. The
+    //      four warps' (m, l, o) are then joined through shared memory in warp order.
     const size_t rb = static_cast<size_t>(row) * nsp;
-    auto stage_round = [&](int j0) {
-        const int cnt = min(kMergeCap, nsp - j0);
-        const float* src = a.po + (rb + j0) * kD;
-        for (int i = tid; i < cnt * (kD / 4); i += kAThreads) cp_async16(mst + 4 * i, src + 4 * i);
-        cp_async_commit();
-    };
-    stage_round(0);
-    // thread j < nsp keeps (m_j, l_j) of the first round from this one round trip
-    float pm0 = -INFINITY, pl0 = 0.0f;
-    if (tid < nsp) {
-        pm0 = __ldcg(a.pm + rb + tid);
-        pl0 = __ldcg(a.pl + rb + tid);
-    }
-    float mx = pm0;
-    for (int j = tid + kAThreads; j < nsp; j += kAThreads) mx = fmaxf(mx, __ldcg(a.pm + rb + j));
+    float mw = -INFINITY, lw = 0.0f;
+    float4 ow = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int j0 = warp; j0 < nsp; j0 += kAWarps * kMergeRegs) {
+        float pmj[kMergeRegs], plj[kMergeRegs];
+        float4 poj[kMergeRegs];
 #pragma unroll
-    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[warp] = mx;
+        for (int c = 0; c < kMergeRegs; ++c) {
+            const int j = j0 + kAWarps * c;
+            pmj[c] = -INFINITY;
+            plj[c] = 0.0f;
+            poj[c] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (j < nsp) {
+                pmj[c] = __ldcg(a.pm + rb + j);
+                plj[c] = __ldcg(a.pl + rb + j);
+                poj[c] = __ldcg(reinterpret_cast<const float4*>(a.po + (rb + j) * kD) + lane);
+            }
+        }
+        float mn = mw;
+#pragma unroll
+        for (int c = 0; c < kMergeRegs; ++c) mn = fmaxf(mn, pmj[c]);
+        if (mn != -INFINITY) {
+            const float sa = expf(mw - mn);      // 0 while nothing is folded (mw = -inf)
+            lw *= sa;
+            ow = make_float4(ow.x * sa, ow.y * sa, ow.z * sa, ow.w * sa);
+#pragma unroll
+            for (int c = 0; c < kMergeRegs; ++c) {
+                const float sj = expf(pmj[c] - mn);   // 0 for an empty partial (m = -inf)
+                lw = fmaf(sj, plj[c], lw);
+                ow = make_float4(fmaf(sj, poj[c].x, ow.x), fmaf(sj, poj[c].y, ow.y),
+                                 fmaf(sj, poj[c].z, ow.z), fmaf(sj, poj[c].w, ow.w));
+            }
+            mw = mn;
+        }
+    }
+    {
+        float* dst = cbuf + warp * kCombinePitch;
+        reinterpret_cast<float4*>(dst)[lane] = ow;
+        if (lane == 0) {
+            dst[128] = mw;
+            dst[129] = lw;
+        }
+    }
     __syncthreads();
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kAWarps; ++w) M = fmaxf(M, red[w]);
-    float ls = 0.0f, Os = 0.0f;
-    for (int j0 = 0; j0 < nsp; j0 += kMergeCap) {
-        const int cnt = min(kMergeCap, nsp - j0);
-        if (tid < cnt) {
-            const float pmj = j0 == 0 ? pm0 : __ldcg(a.pm + rb + j0 + tid);
-            const float plj = j0 == 0 ? pl0 : __ldcg(a.pl + rb + j0 + tid);
-            const float sj = M == -INFINITY ? 0.0f : expf(pmj - M);
-            sc[tid] = sj;
-            ls = fmaf(sj, plj, ls);
+    for (int w = 0; w < kAWarps; ++w) M = fmaxf(M, cbuf[w * kCombinePitch + 128]);
+    float Ls = 0.0f, Os = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < kAWarps; ++w) {
+            const float* rr = cbuf + w * kCombinePitch;
+            const float sw = expf(rr[128] - M);
+            Ls = fmaf(sw, rr[129], Ls);
+            Os = fmaf(sw, rr[tid], Os);
         }
-        cp_async_wait_pending<0>();
-        __syncthreads();                         // staged rows and scales visible to all
-#pragma unroll 8
-        for (int j = 0; j < cnt; ++j) Os = fmaf(sc[j], mst[j * kD + tid], Os);
-        __syncthreads();                         // stage and scales are refilled next round
-        if (j0 + kMergeCap < nsp) stage_round(j0 + kMergeCap);
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-    if (lane == 0) red[4 + warp] = ls;
-    __syncthreads();
-    float Ls = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kAWarps; ++w) Ls += red[4 + w];
     // a query with a NaN or infinite element has no defined output: NaN, not a silent zero
     if (mp_check(a.status, row, gridDim.y, kSiteAttendPartial))
         a.out[static_cast<size_t>(row) * kD + tid] =
@@ -1075,7 +1080,6 @@ cudaError_t launch_attend(const void* q, bool q_bf16, const float* centre, const
     aa.scale = s.scale;
     {
         const AttendSmem m = attend_smem(attend_partials(s.nblk), kv_bf16 ? 2 : 4);
-        aa.merge_cap = m.merge_cap;
         aa.work_bytes = static_cast<int>(m.work);
     }
     return launch_dependent(attend, dim3(aa.nsb + 1, s.B * s.Hq), dim3(kAThreads), smem_att, st,
