@@ -307,5 +307,14 @@ def test_full_size_llama70b_layer(mp):
     assert _summary(reps)[3] == wl.G
 
 
+def test_long_ragged_context_merges_75_partials(mp):
+    """n = 300,000 (293 blocks, the last ragged): 74 sampled partials and the exact one per query
+    head, so the last-arrival merge folds them in three passes of up to 32 (the 96K and 128K
+    layers above take one and two)."""
+    wl = small_workload(name="ctx300k", index=731, B=1, Hq=8, Hkv=2, n=300_000)
+    reps = _full_size(mp, wl, [(0, 0), (0, 1)])
+    assert _summary(reps)[3] == 2 * wl.G
+
+
 def test_device_status_is_clean(mp):
     assert mp.device_status() == 0
