@@ -267,8 +267,8 @@ MP_API mp_status mp_key_radius(const void* keys, mp_dtype key_dtype, const float
  * taken, gets 0 in the extra coordinate).
  * norms_scratch: NULL, or caller-owned device memory of B*Hkv*n_capacity floats. With it, bf16
  * keys and W and more than 64 keys, whole 1024-key blocks are re-encoded on the tensor cores
- * (the centred part by MMA, the extra coordinate added in fp32 before the sign; the norms of
- * the blocks' keys are written to the scratch first). Otherwise fp32 CUDA cores encode the range
+ * (the centred part and the extra coordinate, split exactly into three bf16 terms, both by MMA;
+ * the norms of the blocks' keys are written to the scratch first). Otherwise fp32 CUDA cores encode the range
  * itself, keeping the other keys' bits of the words it touches.
  * Errors as mp_encode_keys; MP_ERR_INVALID_ARG also for a NULL radius. */
 MP_API mp_status mp_encode_keys_mips(const void* keys, mp_dtype key_dtype, const float* centre,

@@ -357,7 +357,7 @@ struct AArgs {
     int* status;                                 // index checks of the MP_CHECKS build
     const float* radius;                         // MIPS variant: longest centred key per head
     float scale;
-    int work_bytes;                              // bytes of the row / merge stage region
+    int work_bytes;                              // bytes of the row stage region
 };
 
 // The scan of one (1024-key block, sequence x KV head) for its GQA group of G query heads,
@@ -531,7 +531,7 @@ __global__ void __launch_bounds__(kAThreads, 6) attend_kernel(const AArgs a) {
     constexpr int kPieces = kRowBytes / 16;
     constexpr int kWords = kAttendBlocks * 32;                            // selection words
     static_assert(kWords == kAThreads, "one selection word per thread");
-    uint8_t* stage = smem;                                    // [kAttendRows] rows; later the merge
+    uint8_t* stage = smem;                                    // [kAttendRows] K/V row slots
     uint32_t* wsel = reinterpret_cast<uint32_t*>(smem + a.work_bytes);      // [kWords]
     int* wpre = reinterpret_cast<int*>(wsel + kWords);                      // [kWords + 4]
     int* rowkey = wpre + kWords + 4;                                        // [kRowKeys]

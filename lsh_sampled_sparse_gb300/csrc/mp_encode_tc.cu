@@ -15,7 +15,8 @@
 //
 // Structure (one CTA per SM, persistent over a contiguous range of 1024-key blocks, and one
 // 256-hyperplane chunk of W held in shared memory for the CTA's whole life):
-//   warp 0   TMA producer: 128-key x 128-dim bf16 tiles, 128-byte swizzle, 3-stage ring
+//   warp 0   TMA producer: 128-key x 128-dim bf16 tiles, 128-byte swizzle, 3-stage ring (2 for
+//            the MIPS variant, whose producer warp also writes each tile's key slice)
 //   warp 1   TMEM allocator and single-thread MMA issuer: M=128, N<=256, K=16 x (1 + 8) per
 //            tile, double-buffered fp32 accumulators (2 x 256 TMEM columns)
 //   warps 2-17 epilogue: tcgen05.ld the accumulator; per key (lane) gather its sign bits into
@@ -36,7 +37,6 @@ namespace {
 
 constexpr int kTileM = 128;            // keys per MMA tile (TMEM lanes)
 constexpr int kChunkN = 256;           // hyperplanes per CTA (MMA N, TMEM columns per buffer)
-constexpr int kStages = 3;             // A-tile ring depth
 // 16 epilogue warps + 2 = 18 warps: some SM sub-partition holds 5 of them, and its 16K
 // registers cap the kernel at 96 registers per thread (ptxas picks that from the launch bound).
 constexpr int kEpiWarps = 16;
@@ -47,25 +47,39 @@ constexpr uint32_t kBBytes = kChunkN * kD * 2;         // 64 KB
 constexpr uint32_t kBHalfBytes = kChunkN * 128;        // 32 KB
 constexpr int kStgPitch = kWordsPerBlock * 8 + 1;      // 257: staging row pitch (words)
 
-constexpr uint32_t kOffA = 0;
-constexpr uint32_t kOffB = kOffA + kStages * kStageBytes;
 // Centre region: 256 rows x 128 bytes, 128-byte swizzle, four K=16 slices per row: slices 0-2
 // hold the c_j terms of three heads (B operand, rows = hyperplanes), slice 3 of rows 0-127 the
 // constant [1, 1, 1, 0, ...] (A operand, rows = keys).
-constexpr uint32_t kOffC = kOffB + kBBytes;
 constexpr uint32_t kCBytes = kChunkN * 128;            // 32 KB
 constexpr int kCSlots = 3;
 constexpr int kOnesSlice = 3;
-constexpr uint32_t kOffStg = kOffC + kCBytes;
-constexpr uint32_t kOffBars = kOffStg + kWordsPerBlock * kStgPitch * 4;
-constexpr uint32_t kOffMisc = kOffBars + 128;
-constexpr uint32_t kOffWd = kOffMisc + 16;             // MIPS: W[d][j0 + r] as floats
-constexpr uint32_t kSmemBytes = kOffWd + kChunkN * 4 + 1024;  // + alignment slack
 static_assert(kStgPitch == 257, "staging pitch");
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffC % 1024 == 0, "swizzled operands start on 1024-byte boundaries");
 
 constexpr int kSign = 0, kMips = 1, kArgmax = 2;         // epilogue modes of the encoder
+
+// Shared memory of an encoder CTA: the A-tile ring, the -W chunk (B), the centre region, for
+// the MIPS variant its key slices, the word staging, barriers and the MIPS row of W. The MIPS
+// variant's key slices ([1, 1, 1, a_hi, a_mid, a_lo, 0, ...] per key: the extra coordinate a_i
+// enters the contraction beside the centre) take one K=16 slice per ring stage of a 128-row,
+// 128-byte-swizzled region; they fit beside a 2-stage ring.
+template <int kMode>
+struct EncLayout {
+    static constexpr int kStages = kMode == kMips ? 2 : 3;            // A-tile ring depth
+    static constexpr uint32_t kOffA = 0;
+    static constexpr uint32_t kOffB = kOffA + kStages * kStageBytes;
+    static constexpr uint32_t kOffC = kOffB + kBBytes;
+    static constexpr uint32_t kOffKs = kOffC + kCBytes;               // MIPS key slices
+    static constexpr uint32_t kKsBytes = kMode == kMips ? kTileM * 128 : 0;
+    static constexpr uint32_t kOffStg = kOffKs + kKsBytes;
+    static constexpr uint32_t kOffBars = kOffStg + kWordsPerBlock * kStgPitch * 4;
+    static constexpr uint32_t kOffMisc = kOffBars + 128;
+    static constexpr uint32_t kOffWd = kOffMisc + 16;               // MIPS: W[d][j0 + r]
+    static constexpr uint32_t kSmemBytes = kOffWd + kChunkN * 4 + 1024;   // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kOffC % 1024 == 0 && kOffKs % 1024 == 0,
+                  "swizzled operands start on 1024-byte boundaries");
+    static_assert(kMode != kMips || kStages <= 4, "a key slice per ring stage");
+};
 constexpr uint32_t kXchOff = 2 * kKeysPerBlock;          // argmax: exchange area after the codes
 static_assert(kXchOff + 2 * 2 * 2 * kTileM * 8 <= kWordsPerBlock * kStgPitch * 4,
               "the argmax staging fits the word staging area");
@@ -165,7 +179,7 @@ __device__ __forceinline__ float neg_as_one(uint32_t v) {
 // summed on the FP32 pipe instead, as 2^23 + sum_c 2^c [acc_c < 0], whose low mantissa bits are
 // the byte (exact: small integers). For the SimHash epilogue, which has no other
 // FP32 work, one FP byte of four balanced the two pipes best (0, 1, 2 and 3 measured); the MIPS
-// epilogue already spends the FP32 pipe on its per-element FMA and takes none. The two forms
+// variant's extra coordinate enters the contraction, so its epilogue is the same. The two forms
 // differ only for an accumulator of -0 or a negative denormal, i.e. an exact or sub-2^-126 tie,
 // where either bit lies within the near-tie band.
 template <int kFpBytes>
@@ -187,12 +201,14 @@ __device__ __forceinline__ uint32_t pack_signs(const uint32_t (&v)[32]) {
             for (int c = 7; c >= 0; --c) x[k] = __funnelshift_l(v[8 * k + c], x[k], 1);
         }
     }
-    if (kFpBytes == 0) return x[0] | (x[1] << 8) | (x[2] << 16) | (x[3] << 24);   // MIPS: 1% faster
     return __byte_perm(__byte_perm(x[0], x[1], 0x0040), __byte_perm(x[2], x[3], 0x0040), 0x5410);
 }
 // kMode: kSign, the SimHash codes; kMips, the MIPS -> cosine variant, whose keys carry an extra
-// coordinate a_i = sqrt(max(0, r^2 - |k_i - mu|^2)) on a (d + 1)-th row of W: the epilogue
-// subtracts W[d][j] a_i from each accumulator before taking its sign (one fp32 FMA per element);
+// coordinate a_i = sqrt(max(0, r^2 - |k_i - mu|^2)) on a (d + 1)-th row of W: the producer warp
+// writes each tile's key slice [1, 1, 1, a_hi, a_mid, a_lo, 0, ...] (a_i split exactly into three
+// bf16 terms, from the norms it loads two tiles ahead) and the centre's B slice carries
+// [c_hi, c_mid, c_lo, -W[d][j] x 3], so the first K=16 step puts c_j - W[d][j] a_i into the
+// accumulator and the epilogue is the SimHash one;
 // kArgmax, the cross-polytope codes: W is G [L][d][d] (hyperplane j = row j % d of G_{j / d}), a
 // chunk holds two tables, and the epilogue keeps, per key and table, the first index of the
 // largest |accumulator| (two warps cover a table's 128 columns and meet in shared memory), then
@@ -203,13 +219,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sA = smem + kOffA;
-    uint8_t* sB = smem + kOffB;
-    uint32_t* stg = reinterpret_cast<uint32_t*>(smem + kOffStg);
-    uint8_t* sC = smem + kOffC;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    using Lay = EncLayout<kMode>;
+    constexpr int kStages = Lay::kStages;
+    uint8_t* sA = smem + Lay::kOffA;
+    uint8_t* sB = smem + Lay::kOffB;
+    uint32_t* stg = reinterpret_cast<uint32_t*>(smem + Lay::kOffStg);
+    uint8_t* sC = smem + Lay::kOffC;
+    uint8_t* sK = smem + Lay::kOffKs;            // MIPS: the key slices
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kOffBars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Lay::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Lay::kOffMisc + 4);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = blockIdx.x % a.nchunk;
@@ -227,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
+            // MIPS: the stage is full once its TMA bytes and its key slice are in place
+            mbar_init(bar_full + 8 * s, kMode == kMips ? 2 : 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -266,6 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 0-127 (the rest of the slice stays 0)
     for (int i = tid; i < static_cast<int>(kCBytes / 16); i += kThreads)
         reinterpret_cast<uint4*>(sC)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (kMode == kMips) {
+        for (int i = tid; i < static_cast<int>(Lay::kKsBytes / 16); i += kThreads)
+            reinterpret_cast<uint4*>(sK)[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     __syncthreads();
     if (tid < kTileM) {
         const uint32_t one2 = 0x3F803F80u;   // two bf16 1.0
@@ -287,9 +311,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
-        if (lane == 0) {
+        // (MIPS: the whole warp; besides the loads it writes each tile's key slice, from the
+        // keys' norms and the head's radius, which it loads two tiles ahead)
+        if (kMode == kMips || lane == 0) {
             int it = 0;
             bool ok = true;
+            // MIPS prefetch: norms of this lane's keys (rows lane + 32 i) and the radius, for the
+            // next tile (nk1, r1) and the one after (nk2, r2); `ahead` is the tile after those
+            float nk1[4] = {0.0f, 0.0f, 0.0f, 0.0f}, nk2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float r1 = 0.0f, r2 = 0.0f;
+            int ahead_u = u_begin, ahead_t = 0;
+            auto load_ahead = [&](float (&nk)[4], float& r) {
+                if (ahead_u >= u_end) return;
+                const int bg_ = ahead_u / a.nblk, blk_ = ahead_u % a.nblk;
+                const int key0 = (a.blk0 + blk_) * kKeysPerBlock + ahead_t * kTileM;
+                r = __ldg(a.radius + bg_);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int key = key0 + lane + 32 * i;
+                    nk[i] = key < a.n ? __ldg(a.norms + static_cast<size_t>(bg_) * a.n + key) : r;
+                }
+                const int rows_ = min(kKeysPerBlock, a.n - (a.blk0 + blk_) * kKeysPerBlock);
+                if (++ahead_t == (rows_ + kTileM - 1) / kTileM) {
+                    ahead_t = 0;
+                    ++ahead_u;
+                }
+            };
+            if constexpr (kMode == kMips) {
+                load_ahead(nk1, r1);
+                load_ahead(nk2, r2);
+            }
             for (int u = u_begin; u < u_end && ok; ++u) {
                 const int bg = u / a.nblk, blk = u % a.nblk;
                 const int rows = min(kKeysPerBlock, a.n - (a.blk0 + blk) * kKeysPerBlock);
@@ -297,18 +348,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t < ntile; ++t, ++it) {
                     const int s = it % kStages;
                     const uint32_t ph = (it / kStages) & 1;
-                    if (!mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, a.status)) {
+                    bool got = mbar_wait(bar_empty + 8 * s, ph ^ 1, abort_flag, a.status);
+                    if constexpr (kMode == kMips) got = __all_sync(0xffffffffu, got);
+                    if (!got) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
-                    const uint32_t dst = smem_u32(sA + s * kStageBytes);
-                    const int row0 = (a.blk0 + blk) * kKeysPerBlock + t * kTileM;
-                    tma_load_3d(dst, &kmap, bar_full + 8 * s, 0, row0, bg);
-                    tma_load_3d(dst + kHalfBytes, &kmap, bar_full + 8 * s, 64, row0, bg);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+                        const uint32_t dst = smem_u32(sA + s * kStageBytes);
+                        const int row0 = (a.blk0 + blk) * kKeysPerBlock + t * kTileM;
+                        tma_load_3d(dst, &kmap, bar_full + 8 * s, 0, row0, bg);
+                        tma_load_3d(dst + kHalfBytes, &kmap, bar_full + 8 * s, 64, row0, bg);
+                    }
+                    if constexpr (kMode == kMips) {
+                        // key row r of slice s: [1, 1, 1, a_hi, a_mid, a_lo, 0, 0] in its first
+                        // 16 bytes, a = sqrt(max(0, r^2 - |k - mu|^2)) split exactly into three
+                        // bf16 terms (the rest of the slice stays 0)
+                        float nk[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            nk[i] = nk1[i];
+                            nk1[i] = nk2[i];
+                        }
+                        const float r = r1;
+                        r1 = r2;
+                        load_ahead(nk2, r2);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int row = lane + 32 * i;
+                            const float ae = sqrtf(fmaxf(0.0f, fmaf(r, r, -nk[i] * nk[i])));
+                            const __nv_bfloat16 hi = __float2bfloat16_rn(ae);
+                            const float r1 = ae - __bfloat162float(hi);
+                            const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+                            const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+                            *reinterpret_cast<uint4*>(sK + row * 128 + (((2 * s) ^ (row & 7)) << 4)) =
+                                make_uint4(0x3F803F80u,
+                                           0x3F80u | (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16),
+                                           static_cast<uint32_t>(__bfloat16_as_ushort(mid)) |
+                                               (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16),
+                                           0u);
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar_full + 8 * s);
+                    }
                 }
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 // drain: let loads already issued land before the CTA can exit (bounded)
                 for (int k = 1; k <= kStages && it - k >= 0; ++k) {
                     const int i2 = it - k;
@@ -339,9 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + ab * kChunkN;
-                    // D = 1 . c (three bf16 terms), then D += k . (-w) over the 128 dimensions
-                    tc_mma(d_tmem, sw128_desc(c_base + kOnesSlice * 32), sw128_desc(c_base + c_slice),
-                           idesc, 0u);
+                    // D = 1 . c (three bf16 terms) (MIPS: - w_d . a too, from the stage's key
+                    // slice), then D += k . (-w) over the 128 dimensions
+                    const uint32_t a_first = kMode == kMips
+                                                 ? smem_u32(sK) + static_cast<uint32_t>(s) * 32
+                                                 : c_base + kOnesSlice * 32;
+                    tc_mma(d_tmem, sw128_desc(a_first), sw128_desc(c_base + c_slice), idesc, 0u);
 #pragma unroll
                     for (int k = 0; k < kD / 16; ++k) {
                         const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
@@ -362,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int et = tid - 64;                 // 0..511
         const uint32_t tquad = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
         bool aborted = false;
-        float* sWd = reinterpret_cast<float*>(smem + kOffWd);
+        float* sWd = reinterpret_cast<float*>(smem + Lay::kOffWd);
         if constexpr (kMode == kMips) {
             if (et < kChunkN)
                 sWd[et] = et < Nc ? __bfloat162float(a.W[static_cast<size_t>(kD) * a.C + j0 + et])
@@ -394,10 +484,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
                 const uint32_t w01 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) |
                                      (static_cast<uint32_t>(__bfloat16_as_ushort(mid)) << 16);
-                const uint32_t w2 = __bfloat16_as_ushort(lo);
+                uint32_t w2 = __bfloat16_as_ushort(lo), w3 = 0u;
+                if constexpr (kMode == kMips) {
+                    // -W[d][j] against the key slice's three terms of a (a bf16 value: exact)
+                    const uint32_t nw = __bfloat16_as_ushort(__float2bfloat16_rn(-sWd[et]));
+                    w2 |= nw << 16;
+                    w3 = nw | (nw << 16);
+                }
                 const int slot = h % kCSlots;
                 *reinterpret_cast<uint4*>(sC + et * 128 + (((2 * slot) ^ (et & 7)) << 4)) =
-                    make_uint4(w01, w2, 0u, 0u);
+                    make_uint4(w01, w2, w3, 0u);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
         };
@@ -476,16 +572,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int it = 0;
         int bg = u_begin / a.nblk, blk = u_begin % a.nblk;
-        // MIPS: this lane's key norm and its head's radius, loaded a tile ahead of their use
-        float nk_next = 0.0f, r_next = 0.0f;
-        auto load_norm = [&](int bg_, int blk_, int t_) {
-            const int key = (a.blk0 + blk_) * kKeysPerBlock + t_ * kTileM + quad * 32 + lane;
-            r_next = __ldg(a.radius + bg_);
-            nk_next = key < a.n ? __ldg(a.norms + static_cast<size_t>(bg_) * a.n + key) : r_next;
-        };
-        if constexpr (kMode == kMips) {
-            if (u_begin < u_end) load_norm(bg, blk, 0);
-        }
         for (int u = u_begin; u < u_end; ++u) {
             const int ntile = tiles_in_block(blk);
             for (int t = 0; t < ntile; ++t, ++it) {
@@ -500,17 +586,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t x[2] = {0u, 0u};
                 float best64 = -1.0f;        // argmax: this lane's key over this warp's 64 columns
                 int code64 = 0;
-                float aext = 0.0f;           // MIPS: this lane's key's extra coordinate
-                if constexpr (kMode == kMips) {
-                    const float nk = nk_next, r = r_next;
-                    if (t + 1 < ntile) {
-                        load_norm(bg, blk, t + 1);
-                    } else if (u + 1 < u_end) {   // the next unit's first tile
-                        const int nblk = blk + 1 == a.nblk ? 0 : blk + 1;
-                        load_norm(blk + 1 == a.nblk ? bg + 1 : bg, nblk, 0);
-                    }
-                    aext = sqrtf(fmaxf(0.0f, fmaf(r, r, -nk * nk)));
-                }
                 if (!aborted) {
                     tc_fence_after();
                     const uint32_t trow = tquad + ab * kChunkN;
@@ -520,17 +595,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint32_t v[32];
                             tmem_ld32(trow + colA + 32 * g, v);
                             tmem_ld_wait();
-                            if constexpr (kMode == kMips) {
-                                const float4* wd4 = reinterpret_cast<const float4*>(sWd + colA + 32 * g);
-#pragma unroll
-                                for (int c4 = 0; c4 < 8; ++c4) {
-                                    const float4 w = wd4[c4];
-                                    v[4 * c4 + 0] = __float_as_uint(fmaf(-w.x, aext, __uint_as_float(v[4 * c4 + 0])));
-                                    v[4 * c4 + 1] = __float_as_uint(fmaf(-w.y, aext, __uint_as_float(v[4 * c4 + 1])));
-                                    v[4 * c4 + 2] = __float_as_uint(fmaf(-w.z, aext, __uint_as_float(v[4 * c4 + 2])));
-                                    v[4 * c4 + 3] = __float_as_uint(fmaf(-w.w, aext, __uint_as_float(v[4 * c4 + 3])));
-                                }
-                            }
                             if constexpr (kMode == kArgmax) {
                                 // y = -accumulator; first index of the largest |y| of the group
                                 float bst = -1.0f;
@@ -548,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     code64 = cd;
                                 }
                             } else {
-                                x[g] = pack_signs<kMode == kSign ? 1 : 0>(v);
+                                x[g] = pack_signs<1>(v);
                             }
                         }
                     }
@@ -648,9 +712,15 @@ cudaError_t launch_wait_expiry(unsigned long long limit_ns, int* status, cudaStr
 cudaError_t prepare_encode_tc() {
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, wait_expiry_kernel) != cudaSuccess) return cudaErrorNotSupported;
-    for (auto fn : {encode_tc_kernel<kSign>, encode_tc_kernel<kMips>, encode_tc_kernel<kArgmax>}) {
-        const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   kSmemBytes);
+    const struct {
+        void (*fn)(const CUtensorMap, const EncodeArgs);
+        uint32_t smem;
+    } kernels[] = {{encode_tc_kernel<kSign>, EncLayout<kSign>::kSmemBytes},
+                   {encode_tc_kernel<kMips>, EncLayout<kMips>::kSmemBytes},
+                   {encode_tc_kernel<kArgmax>, EncLayout<kArgmax>::kSmemBytes}};
+    for (const auto& k : kernels) {
+        const cudaError_t e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(k.smem));
         if (e != cudaSuccess) return e;
     }
     return encode_tiled_fn() ? cudaSuccess : cudaErrorNotSupported;
@@ -694,11 +764,14 @@ cudaError_t launch_encode_tc(const void* keys, const float* centre, const void* 
     if (parts > a.units) parts = a.units;
     a.parts = parts;
     if (argmax)
-        encode_tc_kernel<kArgmax><<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
+        encode_tc_kernel<kArgmax><<<a.nchunk * parts, kThreads, EncLayout<kArgmax>::kSmemBytes,
+                                    st>>>(map, a);
     else if (norms)
-        encode_tc_kernel<kMips><<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
+        encode_tc_kernel<kMips><<<a.nchunk * parts, kThreads, EncLayout<kMips>::kSmemBytes,
+                                  st>>>(map, a);
     else
-        encode_tc_kernel<kSign><<<a.nchunk * parts, kThreads, kSmemBytes, st>>>(map, a);
+        encode_tc_kernel<kSign><<<a.nchunk * parts, kThreads, EncLayout<kSign>::kSmemBytes,
+                                  st>>>(map, a);
     return cudaGetLastError();
 }
 
