@@ -16,45 +16,73 @@ constexpr int kRadiusThreads = 256;
 constexpr int kMipsKeys = 64;          // keys per encoding CTA (two 32-key words)
 constexpr int kMipsPlanes = 16;        // hyperplanes per pass
 
-constexpr int kRadiusRowsAtOnce = 4;   // key rows a warp has in flight
+constexpr int kRadiusRowsAtOnce = 4;   // key rows a half-warp has in flight
 
-// |k_i - mu| of keys [k0, k1): a warp per key row (kRadiusRowsAtOnce rows in flight), lane 4
-// consecutive elements. With radius: its maximum into radius[bh] (the maximum of non-negative
-// floats through their ordered bit patterns); with norms: each row's into norms[bh][i].
+// the 8 elements [8 hl, 8 hl + 8) of key row `row` minus the centre, squared and summed
+__device__ __forceinline__ float row_part_sq(const void* keys, int keys_bf16, size_t row, int hl,
+                                             const float (&mu)[8]) {
+    float f[8];
+    if (keys_bf16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __nv_bfloat16*>(keys) + row * kD + 8 * hl);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(keys) +
+                                                          row * kD + 8 * hl);
+        const float4 a = p[0], b = p[1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float x = f[i] - mu[i];
+        s = fmaf(x, x, s);
+    }
+    return s;
+}
+
+// |k_i - mu| of keys [k0, k1): a half-warp per key row (16 lanes x 16-byte loads of a bf16 row,
+// two for fp32; kRadiusRowsAtOnce rows in flight), lane hl elements 8 hl .. 8 hl + 7. With
+// radius: its maximum into radius[bh] (the maximum of non-negative floats through their ordered
+// bit patterns); with norms: each row's into norms[bh][i].
 __global__ void __launch_bounds__(kRadiusThreads)
     key_radius_kernel(const void* keys, int keys_bf16, const float* centre, int ncap, int k0,
                       int k1, float* radius, float* norms) {
     constexpr int U = kRadiusRowsAtOnce;
-    const int bh = blockIdx.y, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kHalves = kRadiusThreads / 16;
+    const int bh = blockIdx.y, lane = threadIdx.x & 31, hw = threadIdx.x >> 4, hl = lane & 15;
+    const unsigned hmask = 0xffffu << (lane & 16);
     const int r0 = k0 + blockIdx.x * kRadiusRows, r1 = min(k1, r0 + kRadiusRows);
-    float mu[4];
+    float mu[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) mu[i] = centre[static_cast<size_t>(bh) * kD + 4 * lane + i];
+    for (int i = 0; i < 8; ++i) mu[i] = centre[static_cast<size_t>(bh) * kD + 8 * hl + i];
     float best = 0.0f;
-    for (int rb = r0 + warp * U; rb < r1; rb += (kRadiusThreads / 32) * U) {
+    for (int rb = r0 + hw * U; rb < r1; rb += kHalves * U) {
         float s[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int r = min(rb + u, r1 - 1);            // past r1: a repeat of the last row
-            const size_t base = (static_cast<size_t>(bh) * ncap + r) * kD + 4 * lane;
-            s[u] = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float x = load_elem(keys, keys_bf16, base + i) - mu[i];
-                s[u] = fmaf(x, x, s[u]);
-            }
+            s[u] = row_part_sq(keys, keys_bf16, static_cast<size_t>(bh) * ncap + r, hl, mu);
         }
 #pragma unroll
-        for (int o = 16; o; o >>= 1)
+        for (int o = 8; o; o >>= 1)
 #pragma unroll
-            for (int u = 0; u < U; ++u) s[u] += __shfl_xor_sync(0xffffffffu, s[u], o);
+            for (int u = 0; u < U; ++u) s[u] += __shfl_xor_sync(hmask, s[u], o);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const float nr = sqrtf(s[u]);
             best = fmaxf(best, nr);
-            if (norms && lane == u && rb + u < r1) norms[static_cast<size_t>(bh) * ncap + rb + u] = nr;
+            if (norms && hl == u && rb + u < r1) norms[static_cast<size_t>(bh) * ncap + rb + u] = nr;
         }
     }
+    best = fmaxf(best, __shfl_xor_sync(0xffffffffu, best, 16));
     if (radius && lane == 0)
         atomicMax(reinterpret_cast<unsigned*>(radius + bh), __float_as_uint(best));
 }
