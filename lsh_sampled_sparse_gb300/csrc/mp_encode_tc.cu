@@ -596,17 +596,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tmem_ld32(trow + colA + 32 * g, v);
                             tmem_ld_wait();
                             if constexpr (kMode == kArgmax) {
-                                // y = -accumulator; first index of the largest |y| of the group
-                                float bst = -1.0f;
-                                int cd = 0;
+                                // y = -accumulator; first index of the largest |y| of the group:
+                                // the leading accumulator and its column, compared by magnitude
+                                // (one compare and two selects per element), the code
+                                // 2 i + [accumulator > 0] formed once from the winner
+                                float bv = 0.0f;
+                                int bi = 0;
 #pragma unroll
                                 for (int c = 0; c < 32; ++c) {
                                     const float ac = __uint_as_float(v[c]);
-                                    if (fabsf(ac) > bst) {
-                                        bst = fabsf(ac);
-                                        cd = 2 * ((colA & (kD - 1)) + 32 * g + c) + (ac > 0.0f ? 1 : 0);
+                                    if (fabsf(ac) > fabsf(bv)) {
+                                        bv = ac;
+                                        bi = c;
                                     }
                                 }
+                                const float bst = fabsf(bv);
+                                const int cd = 2 * ((colA & (kD - 1)) + 32 * g + bi) + (bv > 0.0f ? 1 : 0);
                                 if (g == 0 || bst > best64) {
                                     best64 = bst;
                                     code64 = cd;
