@@ -691,6 +691,42 @@ def test_cp_code_replay_accepts_only_runner_up_near_ties():
         O.replay_codes(oc, alt, near, np.array([[4, 2]]))     # not a near tie
 
 
+def _cp_gap_offset(c, rest_norm2):
+    """delta with 7 delta = c * 1e-5 * 7 * sqrt((1 + delta)^2 + rest_norm2): the two largest
+    |(G x)_i| = 7 (1 + delta) and 7 sit c times the band 1e-5 |g|max |x| apart (G rows 7 e_0,
+    7 e_1, e_2, e_3, so |g|max = 7 and x = (1 + delta, 1, ...))."""
+    delta = 0.0
+    for _ in range(60):
+        delta = c * 1e-5 * math.sqrt((1.0 + delta) ** 2 + rest_norm2)
+    return delta
+
+
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_cp_near_tie_band_edges(sign):
+    # cross-polytope: near iff the two largest |G x| differ by less than 1e-5 |g|max |x|; the
+    # code is 2 i + [(G x)_i < 0] of the largest, the runner-up code that of the second
+    G = np.diag([7.0, 7.0, 1.0, 1.0])
+    for c, inside in ((0.999, True), (1.001, False), (0.5, True), (2.0, False)):
+        delta = _cp_gap_offset(c, 1.0 + 0.02)
+        x = np.array([[sign * (1.0 + delta), 1.0, 0.1, 0.1]])
+        code, alt, near = O.cp_hash(x, G)
+        assert bool(near[0]) is inside, (c, sign)
+        assert code[0] == (0 if sign > 0 else 1) and alt[0] == 2
+
+
+def test_cp_key_band_uses_the_raw_key_norm():
+    # keys are hashed centred, but the band scales with the raw key's norm (as for SimHash):
+    # key (1 + delta, 1, 0.1, 5.1) with centre (0, 0, 0, 5) hashes x = (1 + delta, 1, 0.1, 0.1)
+    G = np.diag([7.0, 7.0, 1.0, 1.0])[None]
+    mu = np.array([0.0, 0.0, 0.0, 5.0])
+    for c, inside in ((0.999, True), (1.001, False)):
+        delta = _cp_gap_offset(c, 1.0 + 0.01 + 5.1 ** 2)
+        key = np.array([[1.0 + delta, 1.0, 0.1, 5.1]])
+        code, alt, near = O.encode_keys_cp(key, mu, G)
+        assert bool(near[0, 0]) is inside, c
+        assert code[0, 0] == 0 and alt[0, 0] == 2
+
+
 def test_cp_importance_weights_are_unbiased_over_rotation_draws():
     # Horvitz-Thompson with the cross-polytope inclusion probability (one hash per table)
     rng = np.random.default_rng(33)
