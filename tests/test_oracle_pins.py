@@ -606,6 +606,27 @@ def test_mips_codes_by_brute_force():
             assert codes[i, t] == c
 
 
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_mips_near_tie_band_edges(sign):
+    # MIPS keys: near iff |P| < 1e-5 |w_j| (|k_i| + r), the raw key's norm plus the radius. Key
+    # (delta, 3, 9), centre (0, 0, 5), r = 6: the centred part (delta, 3, 4), the extra coordinate
+    # sqrt(11 - delta^2); column 0 of W_aug is 7 e_0, so P = 7 delta
+    mu = np.array([0.0, 0.0, 5.0])
+    W = np.zeros((4, 2))
+    W[0, 0] = 7.0
+    W[:, 1] = [0.0, 1.0, 1.0, 1.0]
+    r = 6.0
+    for c, inside in ((0.999, True), (1.001, False), (0.5, True), (2.0, False)):
+        delta = 0.0
+        for _ in range(60):
+            delta = c * 1e-5 * (math.sqrt(delta * delta + 90.0) + r)
+        key = np.array([[sign * delta, 3.0, 9.0]])
+        _, bits, near = O.encode_keys_mips(key, mu, W, r, 1, 2)
+        assert bool(near[0, 0]) is inside, (c, sign)
+        assert bool(bits[0, 0]) is (sign > 0)
+        assert not near[0, 1]
+
+
 def test_mips_importance_weights_are_unbiased_over_hyperplane_draws():
     # Horvitz-Thompson with the variant's inclusion probability: fails if p ignored the radius
     # or the query took the extra row
