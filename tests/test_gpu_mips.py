@@ -37,9 +37,13 @@ def _w_aug(wl):
     (dict(B=1, Hq=4, Hkv=2, n=3000, K=10, L=150, kv_dtype=BF), True),
     (dict(B=1, Hq=4, Hkv=2, n=3000, K=10, L=150, kv_dtype=BF), False),
     (dict(B=2, Hq=2, Hkv=1, n=1500, K=8, L=75, kv_dtype=F32, q_dtype=F32, w_dtype=F32), True),
+    # 20 blocks per head, the last of 544 keys: each encoder CTA takes several units, so the key
+    # slices' norms are fetched ahead across blocks, ragged blocks and heads
+    (dict(B=2, Hq=8, Hkv=4, n=20000, K=10, L=150, kv_dtype=BF), True),
 ])
 def test_mips_decode_matches_the_oracle(mp, shape, tensor_cores):
-    # bf16 with tensor_cores: the tcgen05 encoder adds the extra coordinate in its epilogue
+    # bf16 with tensor_cores: the tcgen05 encoder takes the extra coordinate into its first MMA
+    # step (per-tile key slices beside the centre)
     wl = small_workload(**shape)
     x = make_layer(wl)
     xc = {k: v.cuda() for k, v in x.items()}
