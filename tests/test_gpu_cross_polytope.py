@@ -15,7 +15,7 @@ import torch
 
 import oracle as O
 from tests.parity import OUT_REL_TOL, row_rel_err
-from workloads import make_layer, small_workload
+from workloads import WORKLOADS, make_layer, small_workload
 
 pytestmark = pytest.mark.gpu
 
@@ -182,3 +182,44 @@ def test_cp_odd_tables_and_group_sizes(mp, shape):
                 cnt = int(dbg["sel_count"][b, h])
                 assert np.array_equal(dbg["sel_idx"][b, h, :cnt].cpu().numpy(), r["S"])
                 assert row_rel_err(dbg["out"][b, h].cpu().numpy(), r["o"]) <= OUT_REL_TOL
+
+
+def test_cp_full_96k_layer_against_the_oracle(mp):
+    # the 96K workload's layer shape (B=1, 32 query heads over 8 KV heads, n = 98,304) with
+    # L = 16 cross-polytope tables, encoded on the tensor cores; two KV heads checked
+    wl = WORKLOADS["llama8b_n96k_32layers"].replace(K=1, L=L_CP)
+    x = make_layer(wl, 0)
+    xc = {k: v.cuda() for k, v in x.items()}
+    G = _rotations(L_CP, wl.d, 78, BF)
+    Gc = G.cuda()
+    table = mp.cp_logu_table(1, L_CP)
+    centre = mp.key_mean(xc["keys"])
+    codes = mp.encode_keys_cp(xc["keys"], centre, Gc, L_CP, 0, wl.n)
+    args = (1, L_CP, wl.n_sink, wl.n_local)
+    dbg = mp.debug_select(xc["q"], codes, centre, Gc, xc["keys"], xc["values"], *args,
+                          counts=False, logu_table=table)
+    torch.cuda.synchronize()
+    assert mp.device_status() == 0
+    gk = _unpack(codes, wl.B, wl.Hkv, wl.n, L_CP)
+    qbytes = dbg["q_bits"].cpu().numpy().view(np.uint8).reshape(wl.B, wl.Hq, -1)[:, :, :L_CP]
+    cen = centre.cpu().double().numpy()
+    Gd = G.double().numpy()
+    flips = rows = 0
+    for g in (0, 3):
+        keys = O.as64(x["keys"][0, g])
+        oc, alt, near = O.encode_keys_cp(keys, cen[0, g], Gd)
+        kc, f = O.replay_codes(oc, alt, near, gk[0, g], what=f"key codes {g}")
+        flips += f
+        for h in range(g * wl.G, (g + 1) * wl.G):
+            qv = O.as64(x["q"][0, h])
+            qo, qa, qn = O.encode_query_cp(qv, Gd)
+            qc, f = O.replay_codes(qo, qa, qn, qbytes[0, h][None, :].astype(np.int64),
+                                   what=f"query codes {h}")
+            flips += f
+            r = O.decode_head(qv, keys, O.as64(x["values"][0, g]), cen[0, g], kc, qc[0], 1,
+                              L_CP, wl.n_sink, wl.n_local, cross_polytope=True)
+            cnt = int(dbg["sel_count"][0, h])
+            assert np.array_equal(dbg["sel_idx"][0, h, :cnt].cpu().numpy(), r["S"]), (h, cnt)
+            assert row_rel_err(dbg["out"][0, h].cpu().numpy(), r["o"]) <= OUT_REL_TOL, h
+            rows += 1
+    assert rows == 2 * wl.G and flips <= 1e-4 * 2 * wl.n * L_CP

@@ -12,7 +12,7 @@ import torch
 
 import oracle as O
 from tests.parity import check_unit, row_rel_err
-from workloads import make_hyperplanes, make_layer, small_workload
+from workloads import WORKLOADS, make_hyperplanes, make_layer, small_workload
 
 pytestmark = pytest.mark.gpu
 
@@ -124,3 +124,34 @@ def test_mips_ranges_equal_a_full_encode_and_buckets_select_like_the_scan(mp):
                                 centre, W[:wl.d].contiguous(), xc["keys"], xc["values"], *args)
     assert not torch.equal(plain, out_scan)
     assert np.isfinite(out_scan.cpu().numpy()).all()
+
+
+def test_mips_full_96k_layer_against_the_oracle(mp):
+    # one layer of the 96K workload (B=1, 32 query heads over 8 KV heads, n = 98,304) encoded on
+    # the tensor cores as the bench does; two (sequence, KV head) units checked against the oracle
+    wl = WORKLOADS["llama8b_n96k_32layers"]
+    x = make_layer(wl, 0)
+    xc = {k: v.cuda() for k, v in x.items()}
+    W = _w_aug(wl)
+    Wc = W.cuda()
+    centre = mp.key_mean(xc["keys"])
+    radius = mp.key_radius(xc["keys"], centre)
+    codes = mp.encode_keys_mips(xc["keys"], centre, Wc, radius, wl.K, wl.L, 0, wl.n)
+    dbg = mp.debug_select(xc["q"], codes, centre, Wc, xc["keys"], xc["values"], wl.K, wl.L,
+                          wl.n_sink, wl.n_local, counts=False, radius=radius)
+    unpacked = mp.codes_unpack(codes, wl.B, wl.Hkv, wl.n, wl.K, wl.L).cpu().numpy()
+    torch.cuda.synchronize()
+    assert mp.device_status() == 0
+    gpu = {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for k, v in dbg.items()}
+    rad = radius.cpu().double().numpy()
+    cen = centre.cpu()
+    flips = 0
+    for b, g in [(0, 0), (0, 5)]:
+        want = O.mips_radius(x["keys"][b, g], cen[b, g])
+        assert abs(rad[b, g] - want) <= 1e-5 * want
+        rep = check_unit(b, g, q=x["q"], keys=x["keys"], values=x["values"], centre=cen, W=W,
+                         K=wl.K, L=wl.L, n_sink=wl.n_sink, n_local=wl.n_local, gpu=gpu,
+                         unpacked=unpacked, radius=rad[b, g], check_counts=False)
+        flips += rep.key_flips
+        assert rep.rows == wl.G and all(sz > 0 for sz in rep.set_sizes)
+    assert flips <= 1e-5 * 2 * wl.n * wl.C
