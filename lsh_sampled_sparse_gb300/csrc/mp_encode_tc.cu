@@ -362,9 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(dst + kHalfBytes, &kmap, bar_full + 8 * s, 64, row0, bg);
                     }
                     if constexpr (kMode == kMips) {
-                        // key row r of slice s: [1, 1, 1, a_hi, a_mid, a_lo, 0, 0] in its first
-                        // 16 bytes, a = sqrt(max(0, r^2 - |k - mu|^2)) split exactly into three
-                        // bf16 terms (the rest of the slice stays 0)
+                        // key row `row` of slice s: [1, 1, 1, a_hi, a_mid, a_lo, 0, 0] in its
+                        // first 16 bytes, a = sqrt(max(0, r^2 - |k - mu|^2)) split exactly into
+                        // three bf16 terms (the rest of the slice stays 0)
                         float nk[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -379,15 +379,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int row = lane + 32 * i;
                             const float ae = sqrtf(fmaxf(0.0f, fmaf(r, r, -nk[i] * nk[i])));
                             const __nv_bfloat16 hi = __float2bfloat16_rn(ae);
-                            const float r1 = ae - __bfloat162float(hi);
-                            const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-                            const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-                            *reinterpret_cast<uint4*>(sK + row * 128 + (((2 * s) ^ (row & 7)) << 4)) =
-                                make_uint4(0x3F803F80u,
-                                           0x3F80u | (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16),
-                                           static_cast<uint32_t>(__bfloat16_as_ushort(mid)) |
-                                               (static_cast<uint32_t>(__bfloat16_as_ushort(lo)) << 16),
-                                           0u);
+                            const float rem = ae - __bfloat162float(hi);
+                            const __nv_bfloat16 mid = __float2bfloat16_rn(rem);
+                            const __nv_bfloat16 lo =
+                                __float2bfloat16_rn(rem - __bfloat162float(mid));
+                            const uint32_t bhi = __bfloat16_as_ushort(hi);
+                            const uint32_t bmid = __bfloat16_as_ushort(mid);
+                            const uint32_t blo = __bfloat16_as_ushort(lo);
+                            uint8_t* dst = sK + row * 128 + (((2 * s) ^ (row & 7)) << 4);
+                            *reinterpret_cast<uint4*>(dst) =
+                                make_uint4(0x3F803F80u, 0x3F80u | (bhi << 16), bmid | (blo << 16), 0u);
                         }
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         __syncwarp();
