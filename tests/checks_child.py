@@ -11,6 +11,8 @@ exits 0 when every assertion holds.
    with a bucket site. No access leaves the table: the offsets read are those of the query's
    code (< 2^K) and the members read lie below the clamped range end (<= n).
 3. The status word resets and the next clean call stays clean.
+4. The MIPS and cross-polytope variants (their encoder instantiations on the tensor cores, their
+   decodes) on clean inputs: no check fails.
 """
 import os
 import sys
@@ -88,6 +90,22 @@ def main() -> None:
     assert mp.check_report() == (True, 0)
     mp.encode_query(x["q"], centre, Wd, x["keys"].shape, *args, ws)
     mp.sampled_attention_buckets(x["q"], buckets, centre, x["keys"], x["values"], *args, out, ws)
+    torch.cuda.synchronize()
+    assert mp.check_report() == (True, 0)
+    assert mp.device_status() == 0
+
+    # 4. the variants' encoders and decodes on clean inputs
+    W_aug = torch.cat([Wd, torch.randn(1, Wd.shape[1], device="cuda").to(Wd.dtype)], 0).contiguous()
+    radius = mp.key_radius(x["keys"], centre)
+    mcodes = mp.encode_keys_mips(x["keys"], centre, W_aug, radius, wl.K, wl.L, 0, wl.n)
+    mp.decode_attention(x["q"], mcodes, centre, W_aug, x["keys"], x["values"], *args,
+                        radius=radius)
+    L_cp = 16
+    G = torch.randn(L_cp, wl.d, wl.d, device="cuda").to(torch.bfloat16).contiguous()
+    table = mp.cp_logu_table(1, L_cp)
+    ccodes = mp.encode_keys_cp(x["keys"], centre, G, L_cp, 0, wl.n)
+    mp.decode_attention(x["q"], ccodes, centre, G, x["keys"], x["values"], 1, L_cp, wl.n_sink,
+                        wl.n_local, logu_table=table)
     torch.cuda.synchronize()
     assert mp.check_report() == (True, 0)
     assert mp.device_status() == 0
